@@ -1,0 +1,18 @@
+"""ReLU activation-sparse feedforward layer for GB300 (sm_103a).
+
+The computation runs in ``libtwell.so`` (CUDA kernels behind the C ABI of
+``include/twell.h``); this package only marshals torch tensors into it.
+"""
+from ._lib import TwellError, lib_path, load  # noqa: F401
+from .ops import (  # noqa: F401
+    HybridFFN,
+    TwELL,
+    Hybrid,
+    TwellFFN,
+    dense_gemm,
+    new_status,
+    raise_if_device_error,
+    twell_ffn_fwd,
+    twell_gate_pack,
+    twell_pack,
+)

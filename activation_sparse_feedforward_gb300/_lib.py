@@ -1,0 +1,94 @@
+"""ctypes declarations of the C ABI in ``include/twell.h``.
+
+Loading fails loudly when ``libtwell.so`` has not been built: there is no fallback
+implementation of any operation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB_PATH
+
+c_void_p = ctypes.c_void_p
+c_int = ctypes.c_int
+c_size_t = ctypes.c_size_t
+c_float = ctypes.c_float
+
+TW_OK, TW_EINVAL, TW_EALIGN, TW_EUNSUPPORTED, TW_ECAPACITY, TW_ETIMEOUT, TW_ECUDA, TW_EWORKSPACE = range(8)
+
+
+class TwTwell(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("I", ctypes.c_int32), ("W", ctypes.c_int32), ("C", ctypes.c_int32),
+                ("cnt", c_void_p), ("val", c_void_p), ("idx", c_void_p), ("row_nnz", c_void_p),
+                ("ovf", c_void_p), ("ovf_rows", c_void_p), ("n_ovf", c_void_p)]
+
+
+class TwHybrid(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("I", ctypes.c_int32), ("R", ctypes.c_int32),
+                ("backup_cap", ctypes.c_int32),
+                ("row_nnz", c_void_p), ("ell_nnz", c_void_p), ("ell_idx", c_void_p), ("ell_a", c_void_p),
+                ("ell_u", c_void_p), ("backup_slot", c_void_p), ("backup_tok", c_void_p),
+                ("backup_a", c_void_p), ("backup_u", c_void_p), ("n_backup", c_void_p)]
+
+
+# name -> (restype, argtypes); every symbol declared in include/twell.h
+SIGNATURES = {
+    "tw_status_str": (ctypes.c_char_p, [c_int]),
+    "tw_abi_version": (c_int, []),
+    "twell_pack": (c_int, [c_void_p, c_int, c_int, c_int, c_int, ctypes.POINTER(TwTwell), c_void_p, c_void_p]),
+    "twell_gate_pack": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, ctypes.POINTER(TwTwell),
+                                c_void_p, c_void_p, c_void_p]),
+    "twell_ffn_fwd_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int, c_int]),
+    "twell_ffn_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int,
+                              ctypes.POINTER(TwTwell), c_void_p, c_size_t, c_void_p, c_void_p, c_void_p]),
+    "hybrid_ffn_fwd_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int, c_int, c_int]),
+    "hybrid_ffn_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
+                               ctypes.POINTER(TwHybrid), c_void_p, c_size_t, c_void_p, c_void_p, c_void_p]),
+    "hybrid_ffn_bwd_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+    "hybrid_ffn_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
+                               ctypes.POINTER(TwHybrid), c_float, c_void_p, c_void_p, c_void_p, c_void_p,
+                               c_void_p, c_size_t, c_void_p, c_void_p]),
+    "tw_dense_gemm": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p,
+                              c_void_p]),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib_path() -> str:
+    return LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load ``libtwell.so`` (once) and declare every entry point's signature."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libtwell.so not found at {LIB_PATH}: build it first with "
+                "`python -m activation_sparse_feedforward_gb300.build` (or __graft_entry__.build()). "
+                "There is no non-CUDA fallback.")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+class TwellError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = load().tw_status_str(code).decode()
+        super().__init__(f"{where}: {msg}")
+
+
+def check(code: int, where: str) -> None:
+    if code != TW_OK:
+        raise TwellError(code, where)

@@ -1,0 +1,395 @@
+// extern "C" entry points declared in include/twell.h: host-side validation,
+// workspace layout and the launch sequence of each operation. Everything is
+// enqueued on the caller's stream; nothing is allocated, freed or synchronised.
+#include <stdint.h>
+#include <string.h>
+
+#include <initializer_list>
+
+#include "tw_internal.h"
+
+namespace {
+
+constexpr int kAbiVersion = 1;
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+int round_up(int v, int m) { return (v + m - 1) / m * m; }
+
+// Bump allocator over the caller's workspace (or a dry run with base == nullptr
+// that only measures). Every block starts on a 256-byte boundary.
+struct Carve {
+  uint8_t* base;
+  size_t off = 0;
+  explicit Carve(void* b) : base(static_cast<uint8_t*>(b)) {}
+  template <class T>
+  T* take(size_t n) {
+    off = (off + 255) & ~static_cast<size_t>(255);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += n * sizeof(T);
+    return p;
+  }
+};
+
+tw_status from_cuda(cudaError_t e) { return e == cudaSuccess ? TW_OK : TW_ECUDA; }
+
+#define TW_TRY(expr)                           \
+  do {                                         \
+    cudaError_t e_ = (expr);                   \
+    if (e_ != cudaSuccess) return TW_ECUDA;    \
+  } while (0)
+
+tw_status check_tile_geometry(int T, int I, int W, int C) {
+  if (T < 0) return TW_EINVAL;
+  if (W != 64 && W != 128) return TW_EUNSUPPORTED;
+  if (I < 64 || I > 65536 || I % W != 0) return TW_EUNSUPPORTED;
+  if (C < 1 || C > W) return TW_EINVAL;
+  return TW_OK;
+}
+
+tw_status check_model_width(int d) {
+  if (d < 256 || d > 2048 || d % 256 != 0) return TW_EUNSUPPORTED;
+  return TW_OK;
+}
+
+tw_status check_twell(const tw_twell* o, int T, int I, int W, int C) {
+  if (o == nullptr) return TW_EINVAL;
+  if (o->T != T || o->I != I || o->W != W || o->C != C) return TW_EINVAL;
+  if (T == 0) return TW_OK;
+  const void* ptrs[] = {o->cnt, o->val, o->idx, o->row_nnz, o->ovf, o->ovf_rows, o->n_ovf};
+  for (const void* p : ptrs) {
+    if (p == nullptr) return TW_EINVAL;
+    if (!aligned16(p)) return TW_EALIGN;
+  }
+  return TW_OK;
+}
+
+tw_status check_ptrs(std::initializer_list<const void*> ptrs) {
+  for (const void* p : ptrs) {
+    if (p == nullptr) return TW_EINVAL;
+    if (!aligned16(p)) return TW_EALIGN;
+  }
+  return TW_OK;
+}
+
+tw_status check_hybrid(const tw_hybrid* h, int T, int I, bool gated) {
+  if (h == nullptr) return TW_EINVAL;
+  if (h->T != T || h->I != I || h->R < 1 || h->R > I || h->backup_cap < 0 || h->backup_cap > T) return TW_EINVAL;
+  tw_status st = check_ptrs({h->row_nnz, h->ell_nnz, h->ell_idx, h->ell_a, h->backup_slot, h->n_backup});
+  if (st != TW_OK) return st;
+  if (gated) {
+    st = check_ptrs({h->ell_u});
+    if (st != TW_OK) return st;
+  }
+  if (h->backup_cap > 0) {
+    st = check_ptrs({h->backup_tok, h->backup_a});
+    if (st != TW_OK) return st;
+    if (gated) {
+      st = check_ptrs({h->backup_u});
+      if (st != TW_OK) return st;
+    }
+  }
+  return TW_OK;
+}
+
+// ------------------------------------------------------------------ workspace layouts
+struct FwdWs {
+  uint16_t* X;
+  uint16_t* H;
+};
+FwdWs carve_twell_fwd(Carve& c, int d, int I, int ovf_cap) {
+  const int ra = round_up(ovf_cap, 128);
+  FwdWs w{};
+  w.X = c.take<uint16_t>(static_cast<size_t>(ra) * d);
+  w.H = c.take<uint16_t>(static_cast<size_t>(ra) * I);
+  return w;
+}
+
+struct HybFwdWs {
+  uint16_t* cnt;
+  uint16_t* val;
+  uint8_t* idx;
+  uint8_t* ovf;
+  int32_t* ovf_rows;
+  int32_t* n_ovf;
+  uint16_t* X;
+  uint16_t* H;
+};
+HybFwdWs carve_hybrid_fwd(Carve& c, int T, int d, int I, int W, int C, int backup_cap) {
+  const size_t nT = static_cast<size_t>(I / W);
+  const int ra = round_up(backup_cap, 128);
+  HybFwdWs w{};
+  w.cnt = c.take<uint16_t>(static_cast<size_t>(T) * nT);
+  w.val = c.take<uint16_t>(static_cast<size_t>(T) * nT * C);
+  w.idx = c.take<uint8_t>(static_cast<size_t>(T) * nT * C);
+  w.ovf = c.take<uint8_t>(static_cast<size_t>(T));
+  w.ovf_rows = c.take<int32_t>(static_cast<size_t>(T));
+  w.n_ovf = c.take<int32_t>(1);
+  w.X = c.take<uint16_t>(static_cast<size_t>(ra) * d);
+  w.H = c.take<uint16_t>(static_cast<size_t>(ra) * I);
+  return w;
+}
+
+struct HybBwdWs {
+  float* dg;
+  float* du;
+  int32_t* col_cnt;
+  int32_t* col_ptr;
+  int32_t* col_cur;
+  int32_t* csc;
+  uint16_t* dY;
+  uint16_t* X;
+  uint16_t* dG;
+  uint16_t* dU;
+  uint16_t* H;
+};
+HybBwdWs carve_hybrid_bwd(Carve& c, int T, int d, int I, int R, int backup_cap) {
+  const size_t TR = static_cast<size_t>(T) * R;
+  const int ra = round_up(backup_cap, 128);
+  HybBwdWs w{};
+  w.dg = c.take<float>(TR);
+  w.du = c.take<float>(TR);
+  w.col_cnt = c.take<int32_t>(static_cast<size_t>(I) + 1);
+  w.col_ptr = c.take<int32_t>(static_cast<size_t>(I) + 1);
+  w.col_cur = c.take<int32_t>(static_cast<size_t>(I));
+  w.csc = c.take<int32_t>(TR);
+  w.dY = c.take<uint16_t>(static_cast<size_t>(ra) * d);
+  w.X = c.take<uint16_t>(static_cast<size_t>(ra) * d);
+  w.dG = c.take<uint16_t>(static_cast<size_t>(ra) * I);
+  w.dU = c.take<uint16_t>(static_cast<size_t>(ra) * I);
+  w.H = c.take<uint16_t>(static_cast<size_t>(ra) * I);
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tw_status_str(int status) {
+  switch (status) {
+    case TW_OK: return "TW_OK";
+    case TW_EINVAL: return "TW_EINVAL: invalid argument";
+    case TW_EALIGN: return "TW_EALIGN: pointer not 16-byte aligned";
+    case TW_EUNSUPPORTED: return "TW_EUNSUPPORTED: shape outside the implemented range";
+    case TW_ECAPACITY: return "TW_ECAPACITY: more overflow/backup rows than the buffers hold";
+    case TW_ETIMEOUT: return "TW_ETIMEOUT: a bounded pipeline wait gave up";
+    case TW_ECUDA: return "TW_ECUDA: CUDA runtime error";
+    case TW_EWORKSPACE: return "TW_EWORKSPACE: workspace too small";
+    default: return "unknown tw_status";
+  }
+}
+
+int tw_abi_version(void) { return kAbiVersion; }
+
+tw_status twell_pack(const uint16_t* A, int T, int I, int W, int C, const tw_twell* out, int32_t* dev_status,
+                     void* stream) {
+  tw_status st = check_tile_geometry(T, I, W, C);
+  if (st != TW_OK) return st;
+  st = check_twell(out, T, I, W, C);
+  if (st != TW_OK) return st;
+  if (T == 0) return TW_OK;
+  st = check_ptrs({A, dev_status});
+  if (st != TW_OK) return st;
+  cudaStream_t s = as_stream(stream);
+  TW_TRY(tw::launch_pack_dense(A, T, I, W, C, *out, s));
+  TW_TRY(tw::launch_compact_rows(out->ovf, nullptr, 0, T, out->ovf_rows, T, out->n_ovf, nullptr, nullptr, T,
+                                 dev_status, s));
+  return TW_OK;
+}
+
+static tw_status gate_pack_impl(const uint16_t* x, const uint16_t* Wg, int T, int d, int I, int W, int C,
+                                const tw_twell& o, uint16_t* a_dense, int cap_check, int32_t* dev_status,
+                                cudaStream_t s) {
+  TW_TRY(cudaMemsetAsync(o.row_nnz, 0, sizeof(int32_t) * T, s));
+  TW_TRY(cudaMemsetAsync(o.ovf, 0, static_cast<size_t>(T), s));
+  TW_TRY(tw::gemm_gate_pack(x, Wg, T, d, I, W, C, o, a_dense, dev_status, s));
+  TW_TRY(tw::launch_compact_rows(o.ovf, nullptr, 0, T, o.ovf_rows, T, o.n_ovf, nullptr, nullptr, cap_check,
+                                 dev_status, s));
+  return TW_OK;
+}
+
+tw_status twell_gate_pack(const uint16_t* x, const uint16_t* Wg, int T, int d, int I, int W, int C,
+                          const tw_twell* out, uint16_t* a_dense, int32_t* dev_status, void* stream) {
+  tw_status st = check_tile_geometry(T, I, W, C);
+  if (st != TW_OK) return st;
+  st = check_model_width(d);
+  if (st != TW_OK) return st;
+  st = check_twell(out, T, I, W, C);
+  if (st != TW_OK) return st;
+  if (T == 0) return TW_OK;
+  st = check_ptrs({x, Wg, dev_status});
+  if (st != TW_OK) return st;
+  if (a_dense != nullptr && !aligned16(a_dense)) return TW_EALIGN;
+  return gate_pack_impl(x, Wg, T, d, I, W, C, *out, a_dense, T, dev_status, as_stream(stream));
+}
+
+size_t twell_ffn_fwd_workspace_size(int T, int d, int I, int W, int C, int ovf_cap) {
+  (void)T;
+  (void)W;
+  (void)C;
+  Carve c(nullptr);
+  carve_twell_fwd(c, d, I, ovf_cap < 0 ? 0 : ovf_cap);
+  return c.off + 256;
+}
+
+tw_status twell_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, int T, int d,
+                        int I, int W, int C, int ovf_cap, const tw_twell* tw_out, void* ws, size_t ws_bytes,
+                        uint16_t* y, int32_t* dev_status, void* stream) {
+  tw_status st = check_tile_geometry(T, I, W, C);
+  if (st != TW_OK) return st;
+  st = check_model_width(d);
+  if (st != TW_OK) return st;
+  if (ovf_cap < 0 || ovf_cap > T) return TW_EINVAL;
+  st = check_twell(tw_out, T, I, W, C);
+  if (st != TW_OK) return st;
+  if (T == 0) return TW_OK;
+  st = check_ptrs({x, Wg, Wd, y, dev_status});
+  if (st != TW_OK) return st;
+  if (Wu != nullptr && !aligned16(Wu)) return TW_EALIGN;
+  if (ws_bytes < twell_ffn_fwd_workspace_size(T, d, I, W, C, ovf_cap)) return TW_EWORKSPACE;
+  if (ovf_cap > 0 && ws == nullptr) return TW_EINVAL;
+  cudaStream_t s = as_stream(stream);
+  const tw_twell& o = *tw_out;
+  Carve c(reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(ws) + 255) & ~static_cast<uintptr_t>(255)));
+  const FwdWs w = carve_twell_fwd(c, d, I, ovf_cap);
+  const int ra = round_up(ovf_cap, 128);
+
+  st = gate_pack_impl(x, Wg, T, d, I, W, C, o, nullptr, ovf_cap, dev_status, s);
+  if (st != TW_OK) return st;
+  tw::SparseFwdArgs a{};
+  a.x = x; a.Wu = Wu; a.Wd = Wd;
+  a.T = T; a.d = d; a.I = I; a.W = W; a.C = C; a.nT = I / W;
+  a.cnt = o.cnt; a.val = o.val; a.idx = o.idx; a.ovf = o.ovf;
+  a.backup_slot = nullptr;
+  a.y = y;
+  TW_TRY(tw::launch_sparse_fwd(a, s));
+  if (ovf_cap > 0) {
+    TW_TRY(tw::launch_gather_rows(x, d, o.ovf_rows, o.n_ovf, ovf_cap, ra, w.X, s));
+    TW_TRY(tw::gemm_backup_hidden(w.X, Wg, Wu, ra, o.n_ovf, ovf_cap, d, I, w.H, nullptr, nullptr, dev_status, s));
+    TW_TRY(tw::gemm_rows_times_nmajor(w.H, Wd, nullptr, nullptr, 1, ra, o.n_ovf, ovf_cap, I, d, y, d, o.ovf_rows,
+                                      dev_status, s));
+  }
+  return TW_OK;
+}
+
+size_t hybrid_ffn_fwd_workspace_size(int T, int d, int I, int W, int C, int R, int backup_cap) {
+  (void)R;
+  if (T < 0 || W <= 0 || C <= 0) return 0;
+  Carve c(nullptr);
+  carve_hybrid_fwd(c, T, d, I, W, C, backup_cap < 0 ? 0 : backup_cap);
+  return c.off + 256;
+}
+
+tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, int T, int d,
+                         int I, int W, int C, const tw_hybrid* saved, void* ws, size_t ws_bytes, uint16_t* y,
+                         int32_t* dev_status, void* stream) {
+  tw_status st = check_tile_geometry(T, I, W, C);
+  if (st != TW_OK) return st;
+  st = check_model_width(d);
+  if (st != TW_OK) return st;
+  const bool gated = Wu != nullptr;
+  st = check_hybrid(saved, T, I, gated);
+  if (st != TW_OK) return st;
+  if (T == 0) return TW_OK;
+  st = check_ptrs({x, Wg, Wd, y, dev_status, ws});
+  if (st != TW_OK) return st;
+  if (gated && !aligned16(Wu)) return TW_EALIGN;
+  const int R = saved->R, cap = saved->backup_cap;
+  if (ws_bytes < hybrid_ffn_fwd_workspace_size(T, d, I, W, C, R, cap)) return TW_EWORKSPACE;
+  cudaStream_t s = as_stream(stream);
+  Carve c(reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(ws) + 255) & ~static_cast<uintptr_t>(255)));
+  const HybFwdWs w = carve_hybrid_fwd(c, T, d, I, W, C, cap);
+  const int ra = round_up(cap, 128);
+  tw_twell o{T, I, W, C, w.cnt, w.val, w.idx, saved->row_nnz, w.ovf, w.ovf_rows, w.n_ovf};
+
+  st = gate_pack_impl(x, Wg, T, d, I, W, C, o, nullptr, T, dev_status, s);
+  if (st != TW_OK) return st;
+  TW_TRY(tw::launch_compact_rows(o.ovf, saved->row_nnz, R, T, saved->backup_tok, cap, saved->n_backup,
+                                 saved->backup_slot, saved->ell_nnz, cap, dev_status, s));
+  tw::SparseFwdArgs a{};
+  a.x = x; a.Wu = Wu; a.Wd = Wd;
+  a.T = T; a.d = d; a.I = I; a.W = W; a.C = C; a.nT = I / W;
+  a.cnt = o.cnt; a.val = o.val; a.idx = o.idx; a.ovf = o.ovf;
+  a.backup_slot = saved->backup_slot;
+  a.ell_idx = saved->ell_idx; a.ell_a = saved->ell_a; a.ell_u = saved->ell_u; a.R = R;
+  a.y = y;
+  TW_TRY(tw::launch_sparse_fwd(a, s));
+  if (cap > 0) {
+    TW_TRY(tw::launch_gather_rows(x, d, saved->backup_tok, saved->n_backup, cap, ra, w.X, s));
+    TW_TRY(tw::gemm_backup_hidden(w.X, Wg, Wu, ra, saved->n_backup, cap, d, I, w.H, saved->backup_a,
+                                  gated ? saved->backup_u : nullptr, dev_status, s));
+    TW_TRY(tw::gemm_rows_times_nmajor(w.H, Wd, nullptr, nullptr, 1, ra, saved->n_backup, cap, I, d, y, d,
+                                      saved->backup_tok, dev_status, s));
+  }
+  return TW_OK;
+}
+
+size_t hybrid_ffn_bwd_workspace_size(int T, int d, int I, int R, int backup_cap) {
+  if (T < 0 || R < 1) return 0;
+  Carve c(nullptr);
+  carve_hybrid_bwd(c, T, d, I, R, backup_cap < 0 ? 0 : backup_cap);
+  return c.off + 256;
+}
+
+tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* Wg, const uint16_t* Wu,
+                         const uint16_t* Wd, int T, int d, int I, const tw_hybrid* saved, float l1, uint16_t* dx,
+                         float* dWg, float* dWu, float* dWd, void* ws, size_t ws_bytes, int32_t* dev_status,
+                         void* stream) {
+  if (T < 0 || I < 64 || I > 65536 || I % 64 != 0) return TW_EUNSUPPORTED;
+  tw_status st = check_model_width(d);
+  if (st != TW_OK) return st;
+  const bool gated = Wu != nullptr;
+  st = check_hybrid(saved, T, I, gated);
+  if (st != TW_OK) return st;
+  st = check_ptrs({Wg, Wd, dWg, dWd, dev_status, ws});
+  if (st != TW_OK) return st;
+  if (gated) {
+    st = check_ptrs({Wu, dWu});
+    if (st != TW_OK) return st;
+  }
+  if (T > 0) {
+    st = check_ptrs({dy, x, dx});
+    if (st != TW_OK) return st;
+  }
+  const int R = saved->R, cap = saved->backup_cap;
+  if (ws_bytes < hybrid_ffn_bwd_workspace_size(T, d, I, R, cap)) return TW_EWORKSPACE;
+  cudaStream_t s = as_stream(stream);
+  Carve c(reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(ws) + 255) & ~static_cast<uintptr_t>(255)));
+  const HybBwdWs w = carve_hybrid_bwd(c, T, d, I, R, cap);
+  const int ra = round_up(cap, 128);
+
+  tw::SparseBwdArgs a{};
+  a.dy = dy; a.x = x; a.Wg = Wg; a.Wu = Wu; a.Wd = Wd;
+  a.T = T; a.d = d; a.I = I; a.R = R; a.l1 = l1;
+  a.ell_nnz = saved->ell_nnz; a.backup_slot = saved->backup_slot;
+  a.ell_idx = saved->ell_idx; a.ell_a = saved->ell_a; a.ell_u = saved->ell_u;
+  a.dg = w.dg; a.du = w.du; a.dx = dx;
+  a.col_cnt = w.col_cnt; a.col_ptr = w.col_ptr; a.col_cur = w.col_cur; a.csc = w.csc;
+  a.dWg = dWg; a.dWu = dWu; a.dWd = dWd;
+  TW_TRY(tw::launch_sparse_bwd(a, s));
+  if (cap > 0 && T > 0) {
+    TW_TRY(tw::launch_gather_rows(dy, d, saved->backup_tok, saved->n_backup, cap, ra, w.dY, s));
+    TW_TRY(tw::launch_gather_rows(x, d, saved->backup_tok, saved->n_backup, cap, ra, w.X, s));
+    TW_TRY(tw::gemm_backup_grad(w.dY, Wd, ra, saved->n_backup, cap, d, I, saved->backup_a,
+                                gated ? saved->backup_u : nullptr, l1, w.dG, w.dU, w.H, dev_status, s));
+    TW_TRY(tw::gemm_rows_times_nmajor(w.dG, Wg, w.dU, Wu, gated ? 2 : 1, ra, saved->n_backup, cap, I, d, dx, d,
+                                      saved->backup_tok, dev_status, s));
+    TW_TRY(tw::gemm_weight_grad_add(w.dG, w.X, ra, saved->n_backup, cap, I, d, dWg, dev_status, s));
+    if (gated) TW_TRY(tw::gemm_weight_grad_add(w.dU, w.X, ra, saved->n_backup, cap, I, d, dWu, dev_status, s));
+    TW_TRY(tw::gemm_weight_grad_add(w.H, w.dY, ra, saved->n_backup, cap, I, d, dWd, dev_status, s));
+  }
+  return TW_OK;
+}
+
+tw_status tw_dense_gemm(const uint16_t* A, const uint16_t* B, int M, int N, int K, int a_mn, int b_mn, float* D,
+                        int32_t* dev_status, void* stream) {
+  if (M < 1 || N < 1 || K < 1 || N % 64 != 0 || K % 64 != 0) return TW_EINVAL;
+  if (a_mn && M % 64 != 0) return TW_EINVAL;
+  tw_status st = check_ptrs({A, B, D, dev_status});
+  if (st != TW_OK) return st;
+  return from_cuda(tw::gemm_dense_test(A, B, M, N, K, a_mn, b_mn, D, dev_status, as_stream(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,547 @@
+// Persistent tcgen05 GEMM for sm_103a:  D[M, N] = sum over segments of A_s B_s
+// (bf16 operands, fp32 accumulation in TMEM), with a pluggable epilogue that reads
+// the accumulator straight out of TMEM.
+//
+//  * Warp 0 (one lane) streams A and B tiles into a STAGES-deep shared-memory ring
+//    with TMA (cp.async.bulk.tensor, 128-byte swizzle), signalling mbarriers.
+//  * Warp 1 allocates TMEM; one lane issues tcgen05.mma (M = 128, N = BN, K = 16)
+//    into one of two accumulator buffers and commits each ring slot back to the
+//    producer when its MMAs retire.
+//  * Warps 2-5 (128 threads, one accumulator row each) run the epilogue of tile i
+//    while the MMAs of tile i + 1 fill the other TMEM buffer.
+//
+// A is [M, K] with K contiguous ("K-major") or stored [K, M] ("MN-major"); the same
+// for B with N in place of M. DUAL issues a second MMA with a second B operand into
+// its own accumulator (gate and up projections of the same rows in one pass).
+// `segments == 2` continues the K loop over a second (A, B) pair into the same
+// accumulator. M and K may be read from device memory (counts produced by earlier
+// kernels in the stream), so the launch does not need them on the host.
+#pragma once
+
+#include "tw_common.cuh"
+
+namespace tw {
+
+constexpr int GEMM_BM = 128;
+constexpr int GEMM_BK = 64;
+constexpr int GEMM_THREADS = 192;
+
+struct GemmShape {
+  int M;             // rows of D when m_dev == nullptr
+  const int* m_dev;  // optional device row count, clamped to [0, m_cap]
+  int m_cap;
+  int N;             // multiple of BN
+  int K;             // reduction length when k_dev == nullptr
+  const int* k_dev;  // optional device K, clamped to [0, k_cap]; memory past K must read as zero
+  int k_cap;
+  int segments;      // 1 or 2
+  int32_t* status;
+};
+
+template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES>
+struct GemmTraits {
+  static constexpr int NB = DUAL ? 2 : 1;
+  static constexpr int A_BYTES = GEMM_BM * GEMM_BK * 2;
+  static constexpr int B_BYTES = BN * GEMM_BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
+  static constexpr int ACC_COLS = BN * NB;
+  static constexpr int TMEM_COLS = 2 * ACC_COLS;
+  static constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, BN, A_MN, B_MN);
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64, 128, 192 or 256");
+  static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
+  static_assert((2 * STAGES + 4) * 8 + 8 <= BAR_BYTES, "barrier area");
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+};
+
+// Bounded wait used only while draining after an abort: ignores the abort flag.
+TW_DEV bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  const uint32_t addr = smem_addr(bar);
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(addr, parity)) {
+    if (global_timer_ns() - t0 > TW_WAIT_LIMIT_NS) return false;
+  }
+  return true;
+}
+
+template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES, class Epi>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
+                   const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
+                   const GemmShape shape, const __grid_constant__ typename Epi::Params ep) {
+  using Tr = GemmTraits<BN, A_MN, B_MN, DUAL, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
+  uint8_t* tiles = smem_raw + pad;
+  uint64_t* full = reinterpret_cast<uint64_t*>(tiles + STAGES * Tr::STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;   // [2] accumulator ready for the epilogue
+  uint64_t* tempty = tfull + 2;       // [2] accumulator drained by the epilogue
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull + b, 1);
+      mbar_init(tempty + b, 4);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA0);
+    tma_prefetch_desc(&tmB0);
+    if (DUAL || shape.segments > 1) {
+      tma_prefetch_desc(&tmB1);
+      if (shape.segments > 1) tma_prefetch_desc(&tmA1);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Tr::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  int M = shape.M;
+  if (shape.m_dev != nullptr) M = min(max(*shape.m_dev, 0), shape.m_cap);
+  int K = shape.K;
+  if (shape.k_dev != nullptr) K = min(max(*shape.k_dev, 0), shape.k_cap);
+  const int m_tiles = (M + GEMM_BM - 1) / GEMM_BM;
+  const int n_tiles = shape.N / BN;
+  const int num_tiles = (K > 0) ? m_tiles * n_tiles : 0;
+  const int kb_per_seg = (K + GEMM_BK - 1) / GEMM_BK;
+  const int kb_total = kb_per_seg * shape.segments;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const int m0 = (tile / n_tiles) * GEMM_BM;
+        const int n0 = (tile % n_tiles) * BN;
+        for (int kb = 0; kb < kb_total; ++kb) {
+          if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, shape.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sA = tiles + stage * Tr::STAGE_BYTES;
+          uint8_t* sB = sA + Tr::A_BYTES;
+          const int seg = kb / kb_per_seg;
+          const int k0 = (kb - seg * kb_per_seg) * GEMM_BK;
+          const CUtensorMap* ta = seg ? &tmA1 : &tmA0;
+          const CUtensorMap* tb = seg ? &tmB1 : &tmB0;
+          mbar_arrive_expect_tx(full + stage, Tr::STAGE_BYTES);
+          if (!A_MN) {
+            tma_load_2d(sA, ta, full + stage, k0, m0);
+          } else {
+            tma_load_2d(sA, ta, full + stage, m0, k0);
+            tma_load_2d(sA + 8192, ta, full + stage, m0 + 64, k0);
+          }
+#pragma unroll
+          for (int nb = 0; nb < Tr::NB; ++nb) {
+            const CUtensorMap* tbb = (nb == 0) ? tb : &tmB1;
+            uint8_t* dst = sB + nb * Tr::B_BYTES;
+            if (!B_MN) {
+              tma_load_2d(dst, tbb, full + stage, k0, n0);
+            } else {
+#pragma unroll
+              for (int c = 0; c < BN / 64; ++c) tma_load_2d(dst + c * 8192, tbb, full + stage, n0 + c * 64, k0);
+            }
+          }
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // let the loads already issued land before the CTA can exit
+        for (long i = 0; i < STAGES && i < issued; ++i) {
+          const long q = issued - 1 - i;
+          mbar_wait_drain(full + (q % STAGES), static_cast<uint32_t>((q / STAGES) & 1));
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      bool issued_any = false;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
+        const int buf = local & 1;
+        const uint32_t use = static_cast<uint32_t>(local >> 1);
+        if (!mbar_wait(tempty + buf, (use & 1u) ^ 1u, abort_flag, shape.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d0 = tmem_base + static_cast<uint32_t>(buf * Tr::ACC_COLS);
+        for (int kb = 0; kb < kb_total; ++kb) {
+          if (!mbar_wait(full + stage, phase, abort_flag, shape.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a_base = smem_addr(tiles + stage * Tr::STAGE_BYTES);
+          const uint32_t b_base = a_base + Tr::A_BYTES;
+#pragma unroll
+          for (int k16 = 0; k16 < GEMM_BK / 16; ++k16) {
+            const uint64_t ad = A_MN ? smem_desc_sw128(a_base + k16 * 2048, 8192, 1024)
+                                     : smem_desc_sw128(a_base + k16 * 32, 16, 1024);
+            const uint32_t acc = (kb > 0 || k16 > 0) ? 1u : 0u;
+#pragma unroll
+            for (int nb = 0; nb < Tr::NB; ++nb) {
+              const uint32_t bb = b_base + nb * Tr::B_BYTES;
+              const uint64_t bd = B_MN ? smem_desc_sw128(bb + k16 * 2048, 8192, 1024)
+                                       : smem_desc_sw128(bb + k16 * 32, 16, 1024);
+              tc_mma_bf16(d0 + nb * BN, ad, bd, Tr::IDESC, acc);
+            }
+          }
+          issued_any = true;
+          tc_commit(empty + stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(tfull + buf);
+      }
+      if (!ok && issued_any) {
+        // wait for MMAs in flight before TMEM is released: the commit completes the
+        // current phase of this ring slot's "empty" barrier (parity == phase)
+        uint64_t* drain = empty + stage;
+        tc_commit(drain);
+        mbar_wait_drain(drain, phase);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue warps
+    const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
+    const int row = quarter * 32 + lane;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+      const int buf = local & 1;
+      const uint32_t use = static_cast<uint32_t>(local >> 1);
+      int ok = 0;
+      if (lane == 0) ok = mbar_wait(tfull + buf, use & 1u, abort_flag, shape.status) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const int m = (tile / n_tiles) * GEMM_BM + row;
+      const int n0 = (tile % n_tiles) * BN;
+      Epi e(ep, m, M, n0);
+      const uint32_t tbase =
+          tmem_base + static_cast<uint32_t>(buf * Tr::ACC_COLS) + (static_cast<uint32_t>(quarter * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v0[32];
+        uint32_t v1[32];
+        tmem_ld32(tbase + c * 32, v0);
+        if (DUAL) tmem_ld32(tbase + BN + c * 32, v1);
+        tmem_wait_ld();
+        e.chunk(c, v0, v1);
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty + buf);
+      e.finish();
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, Tr::TMEM_COLS);
+  }
+}
+
+// ======================================================================= epilogues
+// Each epilogue object lives in one thread for one tile: it owns accumulator row m
+// (valid when m < M) and columns [n0, n0 + BN), delivered 32 columns at a time.
+
+// D[m][n] = acc (fp32), row stride ldd.
+struct EpiStoreF32 {
+  struct Params {
+    float* D;
+    int ldd;
+  };
+  const Params& p;
+  int m, M, n0;
+  TW_DEV EpiStoreF32(const Params& p_, int m_, int M_, int n0_) : p(p_), m(m_), M(M_), n0(n0_) {}
+  TW_DEV void chunk(int c, const uint32_t (&v)[32], const uint32_t (&)[32]) {
+    if (m >= M) return;
+    float4* dst = reinterpret_cast<float4*>(p.D + static_cast<size_t>(m) * p.ldd + n0 + c * 32);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
+                           __uint_as_float(v[4 * i + 3]));
+  }
+  TW_DEV void finish() {}
+};
+
+// D[m][n] += acc (fp32 read-modify-write), row stride ldd.
+struct EpiAddF32 {
+  struct Params {
+    float* D;
+    int ldd;
+  };
+  const Params& p;
+  int m, M, n0;
+  TW_DEV EpiAddF32(const Params& p_, int m_, int M_, int n0_) : p(p_), m(m_), M(M_), n0(n0_) {}
+  TW_DEV void chunk(int c, const uint32_t (&v)[32], const uint32_t (&)[32]) {
+    if (m >= M) return;
+    float4* dst = reinterpret_cast<float4*>(p.D + static_cast<size_t>(m) * p.ldd + n0 + c * 32);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float4 o = dst[i];
+      o.x += __uint_as_float(v[4 * i]);
+      o.y += __uint_as_float(v[4 * i + 1]);
+      o.z += __uint_as_float(v[4 * i + 2]);
+      o.w += __uint_as_float(v[4 * i + 3]);
+      dst[i] = o;
+    }
+  }
+  TW_DEV void finish() {}
+};
+
+// out[row_map[m]][n] = bf16(acc) (row_map == nullptr: row m), row stride ldo.
+struct EpiScatterBf16 {
+  struct Params {
+    uint16_t* out;
+    int ldo;
+    const int32_t* row_map;
+  };
+  const Params& p;
+  int m, M, n0;
+  TW_DEV EpiScatterBf16(const Params& p_, int m_, int M_, int n0_) : p(p_), m(m_), M(M_), n0(n0_) {}
+  TW_DEV void chunk(int c, const uint32_t (&v)[32], const uint32_t (&)[32]) {
+    if (m >= M) return;
+    const int r = p.row_map ? p.row_map[m] : m;
+    uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(r) * p.ldo + n0 + c * 32);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint4 q;
+      q.x = pack_bf16x2(__uint_as_float(v[8 * i + 0]), __uint_as_float(v[8 * i + 1]));
+      q.y = pack_bf16x2(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3]));
+      q.z = pack_bf16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5]));
+      q.w = pack_bf16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7]));
+      dst[i] = q;
+    }
+  }
+  TW_DEV void finish() {}
+};
+
+// Gate projection epilogue: a = bf16(ReLU(acc)) packed into TwELL. The thread owns
+// one token row; it walks its columns in ascending order, so every (row, tile)
+// ELL is filled in ascending column order without atomics. Only nonzeros are
+// stored (padding slots stay untouched); cnt is always written; row_nnz and ovf
+// are combined across column tiles with one atomic per (row, CTA tile).
+struct EpiTwellPack {
+  struct Params {
+    int T, W, C, nT;
+    uint16_t* cnt;
+    uint16_t* val;
+    uint8_t* idx;
+    int32_t* row_nnz;
+    uint8_t* ovf;
+    uint16_t* a_dense;  // optional [T, I] bf16 copy of a (verification only)
+    int lda;
+  };
+  const Params& p;
+  int m, n0;
+  bool valid;
+  int c_tile;   // nonzeros seen so far in the current TwELL tile
+  int total;    // nonzeros of this row in this CTA tile
+  bool any_ovf;
+  TW_DEV EpiTwellPack(const Params& p_, int m_, int M_, int n0_)
+      : p(p_), m(m_), n0(n0_), valid(m_ < M_), c_tile(0), total(0), any_ovf(false) {}
+  TW_DEV void chunk(int c, const uint32_t (&v)[32], const uint32_t (&)[32]) {
+    if (!valid) return;
+    const int col0 = n0 + c * 32;
+    const int k = col0 / p.W;
+    const int local0 = col0 - k * p.W;
+    const size_t slot_base = (static_cast<size_t>(m) * p.nT + k) * p.C;
+    uint32_t packed[16];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float g = __uint_as_float(v[i]);
+      const uint16_t a = f32_to_bf16(g > 0.0f ? g : 0.0f);
+      if (i & 1)
+        packed[i >> 1] |= static_cast<uint32_t>(a) << 16;
+      else
+        packed[i >> 1] = a;
+      if (a & 0x7FFFu) {
+        if (c_tile < p.C) {
+          p.val[slot_base + c_tile] = a;
+          p.idx[slot_base + c_tile] = static_cast<uint8_t>(local0 + i);
+        }
+        ++c_tile;
+      }
+    }
+    if (p.a_dense != nullptr) {
+      uint4* dst = reinterpret_cast<uint4*>(p.a_dense + static_cast<size_t>(m) * p.lda + col0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+    }
+    if (local0 + 32 == p.W) {  // last chunk of this TwELL tile
+      p.cnt[static_cast<size_t>(m) * p.nT + k] = static_cast<uint16_t>(c_tile);
+      total += c_tile;
+      any_ovf |= (c_tile > p.C);
+      c_tile = 0;
+    }
+  }
+  TW_DEV void finish() {
+    if (!valid) return;
+    if (total) atomicAdd(p.row_nnz + m, total);
+    if (any_ovf) p.ovf[m] = 1;
+  }
+};
+
+// Dense-backup forward epilogue on a (gate, up) accumulator pair:
+//   a = bf16(ReLU(g)), h = bf16(a * u) (gated) or h = a (non-gated).
+// Writes h (the next GEMM's A operand) and optionally a and bf16(u) (saved for the
+// backward). Rows in [M, end of tile) are written as zeros so that later GEMMs whose
+// K runs over these rows read zeros.
+template <bool GATED>
+struct EpiBackupHidden {
+  struct Params {
+    uint16_t* H;
+    uint16_t* save_a;  // optional
+    uint16_t* save_u;  // optional
+    int ld;            // row stride of H / save_a / save_u (= I)
+    int rows_alloc;    // rows the buffers hold
+  };
+  const Params& p;
+  int m, M, n0;
+  TW_DEV EpiBackupHidden(const Params& p_, int m_, int M_, int n0_) : p(p_), m(m_), M(M_), n0(n0_) {}
+  TW_DEV void chunk(int c, const uint32_t (&g)[32], const uint32_t (&u)[32]) {
+    if (m >= p.rows_alloc) return;
+    const bool live = m < M;
+    const size_t off = static_cast<size_t>(m) * p.ld + n0 + c * 32;
+    uint32_t hh[16], aa[16], uu[16];
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      float a0 = 0.f, a1 = 0.f, h0 = 0.f, h1 = 0.f, u0 = 0.f, u1 = 0.f;
+      if (live) {
+        const float g0 = __uint_as_float(g[i]), g1 = __uint_as_float(g[i + 1]);
+        a0 = bf16_to_f32(f32_to_bf16(g0 > 0.f ? g0 : 0.f));
+        a1 = bf16_to_f32(f32_to_bf16(g1 > 0.f ? g1 : 0.f));
+        if (GATED) {
+          u0 = __uint_as_float(u[i]);
+          u1 = __uint_as_float(u[i + 1]);
+          h0 = a0 * u0;
+          h1 = a1 * u1;
+        } else {
+          h0 = a0;
+          h1 = a1;
+        }
+      }
+      hh[i >> 1] = pack_bf16x2(h0, h1);
+      aa[i >> 1] = pack_bf16x2(a0, a1);
+      uu[i >> 1] = pack_bf16x2(u0, u1);
+    }
+    uint4* dh = reinterpret_cast<uint4*>(p.H + off);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dh[i] = make_uint4(hh[4 * i], hh[4 * i + 1], hh[4 * i + 2], hh[4 * i + 3]);
+    if (p.save_a != nullptr && live) {
+      uint4* da = reinterpret_cast<uint4*>(p.save_a + off);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) da[i] = make_uint4(aa[4 * i], aa[4 * i + 1], aa[4 * i + 2], aa[4 * i + 3]);
+    }
+    if (GATED && p.save_u != nullptr && live) {
+      uint4* du = reinterpret_cast<uint4*>(p.save_u + off);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) du[i] = make_uint4(uu[4 * i], uu[4 * i + 1], uu[4 * i + 2], uu[4 * i + 3]);
+    }
+  }
+  TW_DEV void finish() {}
+};
+
+// Dense-backup backward epilogue on dh = dY Wd^T with the saved a and u rows:
+//   du = dh * a,  dg = (dh * u + l1) on a != 0 (non-gated: dh + l1), else 0,
+//   h = a * u (non-gated: a).
+// Writes dG, dU and H as bf16 GEMM operands; rows in [M, end of tile) become zeros.
+template <bool GATED>
+struct EpiBackupGrad {
+  struct Params {
+    const uint16_t* a;
+    const uint16_t* u;
+    uint16_t* dG;
+    uint16_t* dU;
+    uint16_t* H;
+    float l1;
+    int ld;
+    int rows_alloc;
+  };
+  const Params& p;
+  int m, M, n0;
+  TW_DEV EpiBackupGrad(const Params& p_, int m_, int M_, int n0_) : p(p_), m(m_), M(M_), n0(n0_) {}
+  TW_DEV void chunk(int c, const uint32_t (&dh)[32], const uint32_t (&)[32]) {
+    if (m >= p.rows_alloc) return;
+    const bool live = m < M;
+    const size_t off = static_cast<size_t>(m) * p.ld + n0 + c * 32;
+    uint32_t gg[16], uo[16], hh[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 av = make_uint4(0, 0, 0, 0), uv = make_uint4(0, 0, 0, 0);
+      if (live) {
+        av = reinterpret_cast<const uint4*>(p.a + off)[q];
+        if (GATED) uv = reinterpret_cast<const uint4*>(p.u + off)[q];
+      }
+      const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
+      const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        float dg2[2], du2[2], h2[2];
+#pragma unroll
+        for (int hlf = 0; hlf < 2; ++hlf) {
+          const int i = q * 8 + w * 2 + hlf;
+          const float a = hlf ? bf16_hi(aw[w]) : bf16_lo(aw[w]);
+          const float u = GATED ? (hlf ? bf16_hi(uw[w]) : bf16_lo(uw[w])) : 1.0f;
+          const float d = __uint_as_float(dh[i]);
+          const bool act = live && (a != 0.0f);
+          dg2[hlf] = act ? (GATED ? d * u : d) + p.l1 : 0.0f;
+          du2[hlf] = act ? d * a : 0.0f;
+          h2[hlf] = live ? (GATED ? a * u : a) : 0.0f;
+        }
+        gg[q * 4 + w] = pack_bf16x2(dg2[0], dg2[1]);
+        uo[q * 4 + w] = pack_bf16x2(du2[0], du2[1]);
+        hh[q * 4 + w] = pack_bf16x2(h2[0], h2[1]);
+      }
+    }
+    uint4* pg = reinterpret_cast<uint4*>(p.dG + off);
+    uint4* ph = reinterpret_cast<uint4*>(p.H + off);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      pg[i] = make_uint4(gg[4 * i], gg[4 * i + 1], gg[4 * i + 2], gg[4 * i + 3]);
+      ph[i] = make_uint4(hh[4 * i], hh[4 * i + 1], hh[4 * i + 2], hh[4 * i + 3]);
+    }
+    if (GATED) {
+      uint4* pu = reinterpret_cast<uint4*>(p.dU + off);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) pu[i] = make_uint4(uo[4 * i], uo[4 * i + 1], uo[4 * i + 2], uo[4 * i + 3]);
+    }
+  }
+  TW_DEV void finish() {}
+};
+
+}  // namespace tw

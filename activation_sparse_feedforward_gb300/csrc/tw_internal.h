@@ -1,0 +1,106 @@
+// Host-side interfaces between the C-ABI layer (tw_api.cu) and the kernel
+// launchers (tw_kernels.cu, tw_gemm.cu). Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/twell.h"
+
+namespace tw {
+
+int device_sm_count();
+
+// ---------------------------------------------------------------- tw_kernels.cu
+// Dense bf16 [T, I] -> TwELL counts/slots/row_nnz/ovf (not the overflow list).
+cudaError_t launch_pack_dense(const uint16_t* A, int T, int I, int W, int C, const tw_twell& o, cudaStream_t s);
+
+// Ascending list of rows whose flag holds. flag(t) = ovf[t] != 0, or, when
+// row_nnz != nullptr, ovf[t] != 0 || row_nnz[t] > R. Writes list[0..min(n, list_cap)),
+// *count = n, slot_of[t] (rank, -1 when unflagged, -2 when past list_cap) and
+// ell_nnz[t] (row_nnz when unflagged, else 0) when those pointers are non-null.
+// Raises TW_ECAPACITY when n > cap_check.
+cudaError_t launch_compact_rows(const uint8_t* ovf, const int32_t* row_nnz, int R, int T, int32_t* list,
+                                int list_cap, int32_t* count, int32_t* slot_of, int32_t* ell_nnz, int cap_check,
+                                int32_t* status, cudaStream_t s);
+
+// out[i] = src[rows[i]] for i < min(*n, cap); rows [n, round_up(n, 128)) (below
+// rows_alloc) are zero-filled. Row length d bf16.
+cudaError_t launch_gather_rows(const uint16_t* src, int d, const int32_t* rows, const int32_t* n, int cap,
+                               int rows_alloc, uint16_t* out, cudaStream_t s);
+
+struct SparseFwdArgs {
+  const uint16_t *x, *Wu, *Wd;
+  int T, d, I, W, C, nT;
+  const uint16_t* cnt;
+  const uint16_t* val;
+  const uint8_t* idx;
+  const uint8_t* ovf;             // TwELL mode: skip rows with ovf
+  const int32_t* backup_slot;     // Hybrid mode: skip rows with slot != -1
+  uint16_t* ell_idx;              // Hybrid mode outputs (R slots per row)
+  uint16_t* ell_a;
+  uint16_t* ell_u;
+  int R;
+  uint16_t* y;
+};
+cudaError_t launch_sparse_fwd(const SparseFwdArgs& a, cudaStream_t s);
+
+struct SparseBwdArgs {
+  const uint16_t *dy, *x, *Wg, *Wu, *Wd;
+  int T, d, I, R;
+  float l1;
+  const int32_t* ell_nnz;
+  const int32_t* backup_slot;
+  const uint16_t* ell_idx;
+  const uint16_t* ell_a;
+  const uint16_t* ell_u;
+  float* dg;        // [T, R] per-entry dg (workspace)
+  float* du;        // [T, R] per-entry du (workspace, gated)
+  uint16_t* dx;
+  // transposed Hybrid (workspace)
+  int32_t* col_cnt;   // [I + 1]
+  int32_t* col_ptr;   // [I + 1]
+  int32_t* col_cur;   // [I]
+  int32_t* csc;       // [T * R]
+  float *dWg, *dWu, *dWd;
+};
+// Per-token ELL backward (dh, du, dg, dx) + transposed Hybrid + ELL weight gradients
+// (dW overwritten; the dense backup part is added afterwards).
+cudaError_t launch_sparse_bwd(const SparseBwdArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------- tw_gemm.cu
+bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                    uint32_t box_inner, uint32_t box_outer);
+
+// gate projection + ReLU + TwELL pack
+cudaError_t gemm_gate_pack(const uint16_t* x, const uint16_t* Wg, int T, int d, int I, int W, int C,
+                           const tw_twell& o, uint16_t* a_dense, int32_t* status, cudaStream_t s);
+
+// dense backup forward: H = h(X Wg^T, X Wu^T) over n (device) rows of X [rows_alloc, d];
+// optional saved a / u.
+cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint16_t* Wu, int rows_alloc,
+                               const int32_t* n_dev, int cap, int d, int I, uint16_t* H, uint16_t* save_a,
+                               uint16_t* save_u, int32_t* status, cudaStream_t s);
+
+// out[row_map[m]] = bf16(sum_s A_s B_s) with A_s [rows_alloc, K] K-major and B_s
+// stored [K, N] (N-major); M = n (device) rows, up to cap.
+cudaError_t gemm_rows_times_nmajor(const uint16_t* A0, const uint16_t* B0, const uint16_t* A1, const uint16_t* B1,
+                                   int segments, int rows_alloc, const int32_t* n_dev, int cap, int K, int N,
+                                   uint16_t* out, int ldo, const int32_t* row_map, int32_t* status, cudaStream_t s);
+
+// dense backup backward part 1: dh = dY Wd^T and the epilogue producing dG, dU, H.
+cudaError_t gemm_backup_grad(const uint16_t* dY, const uint16_t* Wd, int rows_alloc, const int32_t* n_dev, int cap,
+                             int d, int I, const uint16_t* a, const uint16_t* u, float l1, uint16_t* dG,
+                             uint16_t* dU, uint16_t* H, int32_t* status, cudaStream_t s);
+
+// D[I, d] += P^T Q with P [rows_alloc, I] and Q [rows_alloc, d] (both stored with
+// the reduction over rows), K = n (device) rows, up to cap.
+cudaError_t gemm_weight_grad_add(const uint16_t* P, const uint16_t* Q, int rows_alloc, const int32_t* n_dev,
+                                 int cap, int I, int d, float* D, int32_t* status, cudaStream_t s);
+
+cudaError_t gemm_dense_test(const uint16_t* A, const uint16_t* B, int M, int N, int K, int a_mn, int b_mn, float* D,
+                            int32_t* status, cudaStream_t s);
+
+}  // namespace tw

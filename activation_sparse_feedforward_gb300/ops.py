@@ -1,0 +1,240 @@
+"""Torch-facing binding of the C ABI: allocates outputs and workspaces with torch,
+passes raw device pointers and the current CUDA stream, and raises on host-side
+error codes. Every step of the computation runs in the library's CUDA kernels.
+
+Device-side conditions (capacity exceeded, a bounded wait timing out) land in an
+int32 status tensor; ``raise_if_device_error(status)`` synchronises and checks it.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+
+BF16 = torch.bfloat16
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _check_bf16(name: str, t: torch.Tensor, shape: tuple[int, ...] | None = None) -> None:
+    if t.dtype != BF16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor")
+    if shape is not None and tuple(t.shape) != shape:
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shape}")
+
+
+def new_status(device=None) -> torch.Tensor:
+    """A zeroed device status word."""
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def raise_if_device_error(status: torch.Tensor, where: str = "device") -> None:
+    code = int(status.item())
+    if code != _lib.TW_OK:
+        raise _lib.TwellError(code, where)
+
+
+@dataclass
+class TwELL:
+    """TwELL buffers (see ``tw_twell`` in include/twell.h)."""
+
+    T: int
+    I: int
+    W: int
+    C: int
+    cnt: torch.Tensor       # [T, nT] uint16 stored as int16 bits
+    val: torch.Tensor       # [T, nT, C] bf16
+    idx: torch.Tensor       # [T, nT, C] uint8
+    row_nnz: torch.Tensor   # [T] int32
+    ovf: torch.Tensor       # [T] uint8
+    ovf_rows: torch.Tensor  # [T] int32
+    n_ovf: torch.Tensor     # [1] int32
+
+    @staticmethod
+    def empty(T: int, I: int, W: int, C: int, device="cuda") -> "TwELL":
+        nT = I // W
+        return TwELL(T, I, W, C,
+                     cnt=torch.empty((T, nT), dtype=torch.int16, device=device),
+                     val=torch.empty((T, nT, C), dtype=BF16, device=device),
+                     idx=torch.empty((T, nT, C), dtype=torch.uint8, device=device),
+                     row_nnz=torch.empty(T, dtype=torch.int32, device=device),
+                     ovf=torch.empty(T, dtype=torch.uint8, device=device),
+                     ovf_rows=torch.empty(max(T, 1), dtype=torch.int32, device=device),
+                     n_ovf=torch.zeros(1, dtype=torch.int32, device=device))
+
+    def struct(self) -> _lib.TwTwell:
+        return _lib.TwTwell(self.T, self.I, self.W, self.C, _ptr(self.cnt), _ptr(self.val), _ptr(self.idx),
+                            _ptr(self.row_nnz), _ptr(self.ovf), _ptr(self.ovf_rows), _ptr(self.n_ovf))
+
+
+@dataclass
+class Hybrid:
+    """Hybrid buffers saved by the training forward (see ``tw_hybrid``)."""
+
+    T: int
+    I: int
+    R: int
+    backup_cap: int
+    row_nnz: torch.Tensor      # [T] int32
+    ell_nnz: torch.Tensor      # [T] int32
+    ell_idx: torch.Tensor      # [T, R] int16 bits of uint16
+    ell_a: torch.Tensor        # [T, R] bf16
+    ell_u: torch.Tensor | None  # [T, R] bf16
+    backup_slot: torch.Tensor  # [T] int32
+    backup_tok: torch.Tensor   # [max(cap,1)] int32
+    backup_a: torch.Tensor     # [max(cap,1), I] bf16
+    backup_u: torch.Tensor | None
+    n_backup: torch.Tensor     # [1] int32
+
+    @staticmethod
+    def empty(T: int, I: int, R: int, backup_cap: int, gated: bool, device="cuda") -> "Hybrid":
+        cap1 = max(backup_cap, 1)
+        return Hybrid(T, I, R, backup_cap,
+                      row_nnz=torch.empty(max(T, 1), dtype=torch.int32, device=device),
+                      ell_nnz=torch.empty(max(T, 1), dtype=torch.int32, device=device),
+                      ell_idx=torch.empty((max(T, 1), R), dtype=torch.int16, device=device),
+                      ell_a=torch.empty((max(T, 1), R), dtype=BF16, device=device),
+                      ell_u=torch.empty((max(T, 1), R), dtype=BF16, device=device) if gated else None,
+                      backup_slot=torch.empty(max(T, 1), dtype=torch.int32, device=device),
+                      backup_tok=torch.empty(cap1, dtype=torch.int32, device=device),
+                      backup_a=torch.empty((cap1, I), dtype=BF16, device=device),
+                      backup_u=torch.empty((cap1, I), dtype=BF16, device=device) if gated else None,
+                      n_backup=torch.zeros(1, dtype=torch.int32, device=device))
+
+    def struct(self) -> _lib.TwHybrid:
+        return _lib.TwHybrid(self.T, self.I, self.R, self.backup_cap, _ptr(self.row_nnz), _ptr(self.ell_nnz),
+                             _ptr(self.ell_idx), _ptr(self.ell_a), _ptr(self.ell_u), _ptr(self.backup_slot),
+                             _ptr(self.backup_tok), _ptr(self.backup_a), _ptr(self.backup_u),
+                             _ptr(self.n_backup))
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+# ---------------------------------------------------------------------------- ops
+
+def twell_pack(A: torch.Tensor, W: int, C: int, status: torch.Tensor | None = None) -> TwELL:
+    """TwELL of a dense bf16 [T, I] matrix."""
+    _check_bf16("A", A)
+    T, I = A.shape
+    out = TwELL.empty(T, I, W, C, A.device)
+    st = status if status is not None else new_status(A.device)
+    s = out.struct()
+    _lib.check(_lib.load().twell_pack(_ptr(A), T, I, W, C, s, _ptr(st), _stream()), "twell_pack")
+    return out
+
+
+def twell_gate_pack(x: torch.Tensor, Wg: torch.Tensor, W: int, C: int, want_dense: bool = False,
+                    status: torch.Tensor | None = None, out: TwELL | None = None):
+    """a = bf16(ReLU(x Wg^T)) packed into TwELL by the fused tensor-core kernel.
+    Returns (TwELL, dense a or None)."""
+    _check_bf16("x", x)
+    T, d = x.shape
+    I = Wg.shape[0]
+    _check_bf16("Wg", Wg, (I, d))
+    out = out or TwELL.empty(T, I, W, C, x.device)
+    dense = torch.empty((T, I), dtype=BF16, device=x.device) if want_dense else None
+    st = status if status is not None else new_status(x.device)
+    s = out.struct()
+    _lib.check(_lib.load().twell_gate_pack(_ptr(x), _ptr(Wg), T, d, I, W, C, s, _ptr(dense), _ptr(st), _stream()),
+               "twell_gate_pack")
+    return out, dense
+
+
+class TwellFFN:
+    """Preallocated inference forward: y = FFN(x) through TwELL."""
+
+    def __init__(self, T: int, d: int, I: int, W: int, C: int, ovf_cap: int | None = None, device="cuda"):
+        self.T, self.d, self.I, self.W, self.C = T, d, I, W, C
+        self.ovf_cap = T if ovf_cap is None else ovf_cap
+        self.tw = TwELL.empty(T, I, W, C, device)
+        self.ws_bytes = int(_lib.load().twell_ffn_fwd_workspace_size(T, d, I, W, C, self.ovf_cap))
+        self.ws = _workspace(self.ws_bytes, device)
+        self.y = torch.empty((T, d), dtype=BF16, device=device)
+        self.status = new_status(device)
+        self._tws = self.tw.struct()
+
+    def __call__(self, x, Wg, Wu, Wd) -> torch.Tensor:
+        _check_bf16("x", x, (self.T, self.d))
+        for n, w in (("Wg", Wg), ("Wu", Wu), ("Wd", Wd)):
+            if w is not None:
+                _check_bf16(n, w, (self.I, self.d))
+        code = _lib.load().twell_ffn_fwd(_ptr(x), _ptr(Wg), _ptr(Wu), _ptr(Wd), self.T, self.d, self.I, self.W,
+                                         self.C, self.ovf_cap, self._tws, _ptr(self.ws), self.ws_bytes,
+                                         _ptr(self.y), _ptr(self.status), _stream())
+        _lib.check(code, "twell_ffn_fwd")
+        return self.y
+
+
+def twell_ffn_fwd(x, Wg, Wu, Wd, W: int, C: int, ovf_cap: int | None = None):
+    """One-shot inference forward. Returns (y, TwELL, status)."""
+    T, d = x.shape
+    f = TwellFFN(T, d, Wg.shape[0], W, C, ovf_cap, x.device)
+    y = f(x, Wg, Wu, Wd)
+    return y, f.tw, f.status
+
+
+class HybridFFN:
+    """Preallocated training forward + backward through the Hybrid format."""
+
+    def __init__(self, T: int, d: int, I: int, W: int, C: int, R: int, backup_cap: int, gated: bool = True,
+                 device="cuda"):
+        self.T, self.d, self.I, self.W, self.C, self.R = T, d, I, W, C, R
+        self.backup_cap = backup_cap
+        self.gated = gated
+        L = _lib.load()
+        self.saved = Hybrid.empty(T, I, R, backup_cap, gated, device)
+        self._hs = self.saved.struct()
+        self.fwd_ws_bytes = int(L.hybrid_ffn_fwd_workspace_size(T, d, I, W, C, R, backup_cap))
+        self.bwd_ws_bytes = int(L.hybrid_ffn_bwd_workspace_size(T, d, I, R, backup_cap))
+        self.fwd_ws = _workspace(self.fwd_ws_bytes, device)
+        self.bwd_ws = _workspace(self.bwd_ws_bytes, device)
+        self.y = torch.empty((T, d), dtype=BF16, device=device)
+        self.dx = torch.empty((T, d), dtype=BF16, device=device)
+        self.dWg = torch.empty((I, d), dtype=torch.float32, device=device)
+        self.dWu = torch.empty((I, d), dtype=torch.float32, device=device) if gated else None
+        self.dWd = torch.empty((I, d), dtype=torch.float32, device=device)
+        self.status = new_status(device)
+
+    def forward(self, x, Wg, Wu, Wd) -> torch.Tensor:
+        _check_bf16("x", x, (self.T, self.d))
+        if (Wu is not None) != self.gated:
+            raise ValueError("Wu must be given exactly for the gated form")
+        code = _lib.load().hybrid_ffn_fwd(_ptr(x), _ptr(Wg), _ptr(Wu), _ptr(Wd), self.T, self.d, self.I, self.W,
+                                          self.C, self._hs, _ptr(self.fwd_ws), self.fwd_ws_bytes, _ptr(self.y),
+                                          _ptr(self.status), _stream())
+        _lib.check(code, "hybrid_ffn_fwd")
+        return self.y
+
+    def backward(self, dy, x, Wg, Wu, Wd, l1: float):
+        _check_bf16("dy", dy, (self.T, self.d))
+        code = _lib.load().hybrid_ffn_bwd(_ptr(dy), _ptr(x), _ptr(Wg), _ptr(Wu), _ptr(Wd), self.T, self.d, self.I,
+                                          self._hs, float(l1), _ptr(self.dx), _ptr(self.dWg), _ptr(self.dWu),
+                                          _ptr(self.dWd), _ptr(self.bwd_ws), self.bwd_ws_bytes,
+                                          _ptr(self.status), _stream())
+        _lib.check(code, "hybrid_ffn_bwd")
+        return self.dx, self.dWg, self.dWu, self.dWd
+
+
+def dense_gemm(A: torch.Tensor, B: torch.Tensor, M: int, N: int, K: int, a_mn: bool, b_mn: bool,
+               status: torch.Tensor | None = None) -> torch.Tensor:
+    """D = A B (fp32) on the tcgen05 GEMM engine. A is [M, K] (a_mn False) or stored
+    [K, M]; B is stored [N, K] (b_mn False) or [K, N]."""
+    _check_bf16("A", A)
+    _check_bf16("B", B)
+    D = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    st = status if status is not None else new_status(A.device)
+    _lib.check(_lib.load().tw_dense_gemm(_ptr(A), _ptr(B), M, N, K, int(a_mn), int(b_mn), _ptr(D), _ptr(st),
+                                         _stream()), "tw_dense_gemm")
+    return D

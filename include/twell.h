@@ -1,0 +1,189 @@
+/*
+ * twell.h -- C ABI of the activation-sparse ReLU feedforward library (sm_103a).
+ *
+ * The operation (gist.science explainer "Sparser, Faster, Lighter Transformer
+ * Language Models", section 2.B "Kernel Design"; Table 2 of the thelatestinai
+ * listing for the two forms):
+ *
+ *   gated:      a = ReLU(x Wg^T),  u = x Wu^T,  h = a * u,  y = h Wd
+ *   non-gated:  a = ReLU(x W1^T),                h = a,      y = h W2
+ *
+ * computed through the TwELL format (inference) and the Hybrid format (training),
+ * with an L1 penalty l1 * sum(a) on the hidden activations in training
+ * (explainer 2.C "Training Recipe").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor pointers are DEVICE pointers, row-major, densely packed. bf16 values
+ *   are passed as their 16-bit patterns (uint16_t). x, y, dy, dx are [T, d].
+ *   Every weight is [I, d]: row j of Wg (W1) and Wu is neuron j's input weight
+ *   vector; row j of Wd (W2) is the vector neuron j adds to y. Wu == NULL selects
+ *   the non-gated form.
+ * - Shapes: T >= 0 tokens; d % 64 == 0 and 64 <= d <= 16384; W in {64, 128};
+ *   I % W == 0, 64 <= I <= 65536; 1 <= C <= W; 1 <= R <= I.
+ *   T == 0 is a valid no-op.
+ * - Alignment: every pointer must be 16-byte aligned (TMA and 128-bit accesses).
+ * - Ownership: the caller allocates and frees every buffer, including the
+ *   workspace whose size the *_workspace_size() functions return. The library
+ *   never allocates, frees or synchronises; it only enqueues kernels (and small
+ *   cudaMemsetAsync calls) on `stream`, a cudaStream_t passed as void* (NULL =
+ *   the legacy default stream).
+ * - Errors found on the host (bad shape, NULL or misaligned pointer, workspace too
+ *   small) are returned synchronously before anything is enqueued. Launch errors
+ *   return TW_ECUDA. Conditions only the GPU can see (a capacity exceeded, a
+ *   bounded wait that timed out) are written to *dev_status, a device int32 the
+ *   caller zeroes beforehand and reads after synchronising: kernels only raise it
+ *   (atomicMax of the tw_status code), never clear it.
+ * - Calls on one stream are ordered; calls on different streams must not share a
+ *   workspace or output.
+ */
+#ifndef TWELL_H
+#define TWELL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TW_OK = 0,
+  TW_EINVAL = 1,        /* bad shape / NULL pointer / bad parameter */
+  TW_EALIGN = 2,        /* pointer not 16-byte aligned */
+  TW_EUNSUPPORTED = 3,  /* shape outside what the kernels implement */
+  TW_ECAPACITY = 4,     /* device: more overflow/backup rows than the buffers hold */
+  TW_ETIMEOUT = 5,      /* device: a bounded pipeline wait gave up */
+  TW_ECUDA = 6,         /* a CUDA runtime call or launch failed */
+  TW_EWORKSPACE = 7     /* workspace smaller than *_workspace_size() */
+} tw_status;
+
+/* TwELL (tile-wise ELLPACK) of a [T, I] activation matrix with tile width W and
+ * capacity C (explainer 2.A "New Sparse Data Format: TwELL"; wispaper blog,
+ * "1. TwELL: Tile-wise ELLPACK"). nT = I / W tiles per row.
+ *   cnt[t*nT + k]           true (uncapped) number of nonzeros of row t in tile k
+ *   val[(t*nT + k)*C + s]   bf16 value of the s-th nonzero (ascending column), s < min(cnt, C)
+ *   idx[(t*nT + k)*C + s]   its column inside the tile, 0 <= idx < W
+ *   row_nnz[t]              sum over k of cnt
+ *   ovf[t]                  1 if some cnt > C (the row is served by the dense path)
+ *   ovf_rows[0 .. *n_ovf)   the rows with ovf == 1, ascending (array holds T entries)
+ * Slots s >= min(cnt, C) are left unspecified. A value is nonzero when its bf16
+ * magnitude bits are nonzero (-0.0 is zero). All arrays are caller-allocated. */
+typedef struct {
+  int32_t T, I, W, C;
+  uint16_t* cnt;
+  uint16_t* val;
+  uint8_t* idx;
+  int32_t* row_nnz;
+  uint8_t* ovf;
+  int32_t* ovf_rows;
+  int32_t* n_ovf;
+} tw_twell;
+
+/* Hybrid format saved by the training forward (explainer 2.A "Hybrid Format for
+ * Training"; wispaper blog, "2. The Hybrid Training Algorithm"). Row t goes to the
+ * dense backup when its TwELL overflowed or row_nnz[t] > R, else to the ELL.
+ *   row_nnz[t]                      active neurons of row t
+ *   ell_nnz[t]                      entries stored in the ELL (0 for backup rows)
+ *   ell_idx[t*R + s]                global neuron index, ascending in s
+ *   ell_a[t*R + s], ell_u[t*R + s]  bf16 a and u at that neuron (ell_u unused when non-gated)
+ *   backup_slot[t]                  slot of row t in the backup, or -1
+ *   backup_tok[b]                   token of backup slot b, ascending in b
+ *   backup_a[b*I + j], backup_u[b*I + j]   full bf16 rows of a and u
+ *   n_backup[0]                     number of backup rows (may exceed backup_cap:
+ *                                   then only backup_cap rows are written and
+ *                                   TW_ECAPACITY is raised in *dev_status)
+ * ell_* slots s >= ell_nnz[t] are unspecified. */
+typedef struct {
+  int32_t T, I, R, backup_cap;
+  int32_t* row_nnz;
+  int32_t* ell_nnz;
+  uint16_t* ell_idx;
+  uint16_t* ell_a;
+  uint16_t* ell_u;
+  int32_t* backup_slot;
+  int32_t* backup_tok;
+  uint16_t* backup_a;
+  uint16_t* backup_u;
+  int32_t* n_backup;
+} tw_hybrid;
+
+/* Human-readable name of a tw_status code. */
+const char* tw_status_str(int status);
+
+/* ABI version of this header (bumped on any incompatible change). */
+int tw_abi_version(void);
+
+/* Pack a dense bf16 [T, I] matrix A into TwELL (all fields of *out, including
+ * row_nnz, ovf, ovf_rows and n_ovf). Bit-exact: the result depends only on A.
+ * Defines the format of explainer 2.A; used standalone and as a test hook. */
+tw_status twell_pack(const uint16_t* A, int T, int I, int W, int C,
+                     const tw_twell* out, int32_t* dev_status, void* stream);
+
+/* Gate projection with the TwELL pack fused into its epilogue (explainer 2.B
+ * "Inference Kernels", "Gate Projection"): a = bf16(ReLU(x Wg^T)) with fp32
+ * accumulation on the tensor cores, written straight into *out; the dense [T, I]
+ * activation is never stored unless a_dense != NULL (a [T, I] bf16 buffer that
+ * receives it, for verification only). Fills every field of *out. */
+tw_status twell_gate_pack(const uint16_t* x, const uint16_t* Wg, int T, int d, int I,
+                          int W, int C, const tw_twell* out, uint16_t* a_dense,
+                          int32_t* dev_status, void* stream);
+
+/* Workspace bytes twell_ffn_fwd needs for up to ovf_cap overflow rows. */
+size_t twell_ffn_fwd_workspace_size(int T, int d, int I, int W, int C, int ovf_cap);
+
+/* Inference forward through TwELL (explainer 2.B "Inference Kernels"): the fused
+ * gate+pack kernel, then one kernel that, for every stored entry (t, j) of a
+ * non-overflow row, takes the dot product u = x_t . Wu[j] and adds (a*u) * Wd[j]
+ * to y_t (never materialising the dense hidden state), and the dense tensor-core
+ * path for overflow rows (at most ovf_cap of them; more raise TW_ECAPACITY and
+ * leave the extra rows of y unwritten). y is [T, d] bf16 (fp32 accumulation, one
+ * rounding). *tw receives the TwELL of a as a by-product. */
+tw_status twell_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* Wu,
+                        const uint16_t* Wd, int T, int d, int I, int W, int C,
+                        int ovf_cap, const tw_twell* tw, void* ws, size_t ws_bytes,
+                        uint16_t* y, int32_t* dev_status, void* stream);
+
+/* Workspace bytes hybrid_ffn_fwd needs. */
+size_t hybrid_ffn_fwd_workspace_size(int T, int d, int I, int W, int C, int R, int backup_cap);
+
+/* Training forward (explainer 2.B "Training Kernels"): gate+pack into TwELL,
+ * conversion of TwELL into the Hybrid *saved (sizes taken from saved->R and
+ * saved->backup_cap), u on the support of ELL rows, y from the ELL rows on the CUDA
+ * cores and from the backup rows on the tensor cores. *saved holds what the
+ * backward needs. */
+tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* Wu,
+                         const uint16_t* Wd, int T, int d, int I, int W, int C,
+                         const tw_hybrid* saved, void* ws, size_t ws_bytes,
+                         uint16_t* y, int32_t* dev_status, void* stream);
+
+/* Workspace bytes hybrid_ffn_bwd needs. */
+size_t hybrid_ffn_bwd_workspace_size(int T, int d, int I, int R, int backup_cap);
+
+/* Training backward over the saved Hybrid (explainer 2.B "Backpropagation"):
+ * gradient of L = sum(dy * y) + l1 * sum(a):
+ *   dh = dy Wd^T on the support;  du = dh * a;  dg = (dh * u + l1) on the support
+ *   (non-gated: dg = dh + l1);  dx = dg Wg + du Wu  (bf16 [T, d]);
+ *   dWg = dg^T x, dWu = du^T x, dWd = h^T dy  (fp32 [I, d], overwritten).
+ * The ELL part runs on the CUDA cores with the weight gradients accumulated over
+ * the transposed Hybrid; backup rows use tensor-core GEMMs. dWu is ignored when
+ * Wu == NULL. */
+tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* Wg,
+                         const uint16_t* Wu, const uint16_t* Wd, int T, int d, int I,
+                         const tw_hybrid* saved, float l1, uint16_t* dx, float* dWg,
+                         float* dWu, float* dWd, void* ws, size_t ws_bytes,
+                         int32_t* dev_status, void* stream);
+
+/* Dense bf16 GEMM on the tensor cores, D[M, N] (fp32) = A B, the engine of the
+ * dense backup path, exposed to check its operand layouts. a_mn == 0: A is [M, K]
+ * (K contiguous); a_mn == 1: A is stored [K, M]. b_mn == 0: B is stored [N, K];
+ * b_mn == 1: B is stored [K, N]. Requires M, N, K >= 1, N % 64 == 0, K % 64 == 0,
+ * and M % 64 == 0 when a_mn == 1. */
+tw_status tw_dense_gemm(const uint16_t* A, const uint16_t* B, int M, int N, int K,
+                        int a_mn, int b_mn, float* D, int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TWELL_H */

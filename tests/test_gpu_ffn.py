@@ -1,0 +1,162 @@
+"""GPU parity of the whole path against the fp64 oracle: TwELL inference forward,
+Hybrid training forward (including the saved Hybrid) and backward."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import activation_sparse_feedforward_gb300 as tw  # noqa: E402
+from gpu_util import assert_close, bits_of, f64_of, to_dev  # noqa: E402
+from oracle import ffn, formats  # noqa: E402
+from synthetic import FFNSpec, WORKLOADS, make_inputs  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    tw.load()
+
+
+def _dev_inputs(inp):
+    return {k: to_dev(v) for k, v in inp.items() if k in ("x", "Wg", "Wu", "Wd", "dy")}
+
+
+MEDIUM = [
+    WORKLOADS["tiny_fwd"],
+    FFNSpec("med_gated", T=777, d=512, I=1280, mean_active=20, outlier_frac=0.03, W=128, C=8, R=48, seed=5),
+    FFNSpec("med_nongated", T=600, d=768, I=1024, gated=False, mean_active=25, outlier_frac=0.02, W=64, C=8,
+            R=64, seed=6),
+    FFNSpec("med_w64_d2048", T=300, d=2048, I=704, mean_active=10, outlier_frac=0.02, W=64, C=6, R=24, seed=7),
+]
+
+
+@pytest.mark.parametrize("spec", MEDIUM, ids=lambda s: s.name)
+def test_twell_forward_matches_oracle(spec):
+    inp = make_inputs(spec)
+    dv = _dev_inputs(inp)
+    y, twl, status = tw.twell_ffn_fwd(dv["x"], dv["Wg"], dv["Wu"], dv["Wd"], spec.W, spec.C)
+    tw.raise_if_device_error(status)
+    ref = ffn.forward(inp["x"], inp["Wg"], inp["Wu"], inp["Wd"])
+    assert_close(f64_of(y), ref["y"], "y")
+    # overflow rows were served by the dense path: check them on their own too
+    n = int(twl.n_ovf.item())
+    rows = twl.ovf_rows[:n].cpu().numpy()
+    assert n > 0 and set(inp["outliers"].tolist()) <= set(rows.tolist())
+    assert_close(f64_of(y)[rows], ref["y"][rows], "y (overflow rows)")
+
+
+def test_twell_forward_full_size_sampled():
+    spec = WORKLOADS["gated_fwd_d2048_i5632"]
+    inp = make_inputs(spec)
+    dv = _dev_inputs(inp)
+    y, twl, status = tw.twell_ffn_fwd(dv["x"], dv["Wg"], dv["Wu"], dv["Wd"], spec.W, spec.C)
+    tw.raise_if_device_error(status)
+    rows = np.unique(np.concatenate([np.arange(3, spec.T, 509), inp["outliers"][:12], [0, spec.T - 1]]))
+    ref = ffn.forward(inp["x"][rows], inp["Wg"], inp["Wu"], inp["Wd"])
+    assert_close(f64_of(y)[rows], ref["y"], "y (sampled rows)")
+
+
+def test_twell_forward_nongated_full_size_sampled():
+    spec = WORKLOADS["nongated_fwd_d2048_i8192"]
+    inp = make_inputs(spec)
+    dv = _dev_inputs(inp)
+    y, twl, status = tw.twell_ffn_fwd(dv["x"], dv["Wg"], None, dv["Wd"], spec.W, spec.C)
+    tw.raise_if_device_error(status)
+    rows = np.unique(np.concatenate([np.arange(1, spec.T, 1021), inp["outliers"][:8]]))
+    ref = ffn.forward(inp["x"][rows], inp["Wg"], None, inp["Wd"])
+    assert_close(f64_of(y)[rows], ref["y"], "y (sampled rows)")
+
+
+def test_twell_forward_capacity_exceeded_is_reported():
+    spec = WORKLOADS["tiny_fwd"]
+    inp = make_inputs(spec)
+    dv = _dev_inputs(inp)
+    f = tw.TwellFFN(spec.T, spec.d, spec.I, spec.W, spec.C, ovf_cap=2)   # 5 outliers overflow
+    f(dv["x"], dv["Wg"], dv["Wu"], dv["Wd"])
+    with pytest.raises(tw.TwellError, match="TW_ECAPACITY"):
+        tw.raise_if_device_error(f.status)
+
+
+def _run_hybrid(spec, inp, backup_cap, l1=None, dy_zero=False):
+    dv = _dev_inputs(inp)
+    h = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, backup_cap, gated=spec.gated)
+    y = h.forward(dv["x"], dv["Wg"], dv["Wu"], dv["Wd"])
+    dy = torch.zeros_like(dv["dy"]) if dy_zero else dv["dy"]
+    grads = h.backward(dy, dv["x"], dv["Wg"], dv["Wu"], dv["Wd"], spec.l1 if l1 is None else l1)
+    torch.cuda.synchronize()
+    tw.raise_if_device_error(h.status)
+    return h, y, grads
+
+
+@pytest.mark.parametrize("spec", MEDIUM, ids=lambda s: s.name)
+@pytest.mark.parametrize("l1", [2e-5, 0.05])
+def test_hybrid_forward_backward_match_oracle(spec, l1):
+    inp = make_inputs(spec, with_dy=True)
+    h, y, (dx, dWg, dWu, dWd) = _run_hybrid(spec, inp, backup_cap=spec.T // 4, l1=l1)
+    f = ffn.forward(inp["x"], inp["Wg"], inp["Wu"], inp["Wd"])
+    b = ffn.backward(inp["x"], inp["Wg"], inp["Wu"], inp["Wd"], inp["dy"], l1, fwd=f)
+    assert_close(f64_of(y), f["y"], "y")
+    assert_close(f64_of(dx), b["dx"], "dx")
+    assert_close(dWg.cpu().numpy(), b["dWg"], "dWg")
+    assert_close(dWd.cpu().numpy(), b["dWd"], "dWd")
+    if spec.gated:
+        assert_close(dWu.cpu().numpy(), b["dWu"], "dWu")
+    nb = int(h.saved.n_backup.item())
+    assert 0 < nb <= spec.T // 4
+
+
+def test_hybrid_l1_only_gradient_closed_form():
+    """dy = 0, l1 = 1: dWg[j] = sum of x_t over tokens where neuron j fires,
+    dx_t = sum of Wg[j] over the neurons token t fires, dWu = dWd = 0."""
+    spec = MEDIUM[1]
+    inp = make_inputs(spec, with_dy=True)
+    h, y, (dx, dWg, dWu, dWd) = _run_hybrid(spec, inp, backup_cap=spec.T // 4, l1=1.0, dy_zero=True)
+    x = ffn.bf16_to_f64(inp["x"])
+    Wg = ffn.bf16_to_f64(inp["Wg"])
+    act = (x @ Wg.T) > 0
+    assert_close(dWg.cpu().numpy(), act.T.astype(np.float64) @ x, "dWg (L1 only)")
+    assert_close(f64_of(dx), act.astype(np.float64) @ Wg, "dx (L1 only)")
+    assert float(dWu.abs().max()) == 0.0 and float(dWd.abs().max()) == 0.0
+
+
+def test_hybrid_saved_format_matches_oracle_packing():
+    spec = MEDIUM[1]
+    inp = make_inputs(spec, with_dy=True)
+    h, y, _ = _run_hybrid(spec, inp, backup_cap=spec.T // 4)
+    # reference Hybrid built by the oracle from the gate kernel's own activations
+    _, dense = tw.twell_gate_pack(to_dev(inp["x"]), to_dev(inp["Wg"]), spec.W, spec.C, want_dense=True)
+    A = bits_of(dense)
+    U = ffn.forward(inp["x"], inp["Wg"], inp["Wu"], inp["Wd"])["u"]
+    ref = formats.hybrid_pack(A, U, spec.W, spec.C, spec.R)
+    s = h.saved
+    np.testing.assert_array_equal(s.row_nnz.cpu().numpy(), ref["row_nnz"])
+    np.testing.assert_array_equal(s.backup_slot.cpu().numpy(), ref["backup_slot"])
+    np.testing.assert_array_equal(s.ell_nnz.cpu().numpy(), ref["ell_nnz"])
+    nb = int(s.n_backup.item())
+    np.testing.assert_array_equal(s.backup_tok[:nb].cpu().numpy(), ref["backup_tok"])
+    v = ref["ell_valid"]
+    np.testing.assert_array_equal(s.ell_idx.cpu().numpy().view(np.uint16).astype(np.int64)[v], ref["ell_idx"][v])
+    np.testing.assert_array_equal(bits_of(s.ell_a)[v], ref["ell_a"][v])
+    assert_close(ffn.bf16_to_f64(bits_of(s.ell_u))[v], ref["ell_u"][v], "ell u")
+    np.testing.assert_array_equal(bits_of(s.backup_a)[:nb], ref["backup_a"])
+    assert_close(ffn.bf16_to_f64(bits_of(s.backup_u)[:nb]), ref["backup_u"], "backup u")
+
+
+def test_hybrid_full_size_sampled():
+    spec = WORKLOADS["train_d2048_i5632_m29_o1"]
+    inp = make_inputs(spec, with_dy=True)
+    h, y, (dx, dWg, dWu, dWd) = _run_hybrid(spec, inp, backup_cap=256)
+    rows = np.unique(np.concatenate([np.arange(5, spec.T, 1013), inp["outliers"][:10], [spec.T - 1]]))
+    f = ffn.forward(inp["x"][rows], inp["Wg"], inp["Wu"], inp["Wd"])
+    b = ffn.backward(inp["x"][rows], inp["Wg"], inp["Wu"], inp["Wd"], inp["dy"][rows], spec.l1, fwd=f)
+    assert_close(f64_of(y)[rows], f["y"], "y (sampled rows)")
+    assert_close(f64_of(dx)[rows], b["dx"], "dx (sampled rows)")
+    J = np.array([0, 1, 17, 1000, 2047, 4096, 5631])
+    r = ffn.backward_weight_rows(inp["x"], inp["Wg"], inp["Wu"], inp["Wd"], inp["dy"], spec.l1, J)
+    assert_close(dWg[J].cpu().numpy(), r["dWg"], "dWg (sampled neurons)")
+    assert_close(dWu[J].cpu().numpy(), r["dWu"], "dWu (sampled neurons)")
+    assert_close(dWd[J].cpu().numpy(), r["dWd"], "dWd (sampled neurons)")
+    assert int(h.saved.n_backup.item()) >= len(inp["outliers"])
