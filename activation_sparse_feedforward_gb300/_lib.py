@@ -9,7 +9,7 @@ import ctypes
 import os
 import threading
 
-from .build import LIB_PATH
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtwell.so")
 
 c_void_p = ctypes.c_void_p
 c_int = ctypes.c_int

@@ -98,12 +98,14 @@ tw_status check_hybrid(const tw_hybrid* h, int T, int I, bool gated) {
 struct FwdWs {
   uint16_t* X;
   uint16_t* H;
+  uint16_t* H_lo;
 };
 FwdWs carve_twell_fwd(Carve& c, int d, int I, int ovf_cap) {
   const int ra = round_up(ovf_cap, 128);
   FwdWs w{};
   w.X = c.take<uint16_t>(static_cast<size_t>(ra) * d);
   w.H = c.take<uint16_t>(static_cast<size_t>(ra) * I);
+  w.H_lo = c.take<uint16_t>(static_cast<size_t>(ra) * I);
   return w;
 }
 
@@ -116,6 +118,7 @@ struct HybFwdWs {
   int32_t* n_ovf;
   uint16_t* X;
   uint16_t* H;
+  uint16_t* H_lo;
 };
 HybFwdWs carve_hybrid_fwd(Carve& c, int T, int d, int I, int W, int C, int backup_cap) {
   const size_t nT = static_cast<size_t>(I / W);
@@ -129,6 +132,7 @@ HybFwdWs carve_hybrid_fwd(Carve& c, int T, int d, int I, int W, int C, int backu
   w.n_ovf = c.take<int32_t>(1);
   w.X = c.take<uint16_t>(static_cast<size_t>(ra) * d);
   w.H = c.take<uint16_t>(static_cast<size_t>(ra) * I);
+  w.H_lo = c.take<uint16_t>(static_cast<size_t>(ra) * I);
   return w;
 }
 
@@ -141,13 +145,12 @@ struct HybBwdWs {
   int32_t* csc;
   uint16_t* dY;
   uint16_t* X;
-  uint16_t* dG;
-  uint16_t* dU;
-  uint16_t* H;
+  tw::BackupGradOut g;  // dG, dU, H as (hi, lo) bf16 pairs
 };
 HybBwdWs carve_hybrid_bwd(Carve& c, int T, int d, int I, int R, int backup_cap) {
   const size_t TR = static_cast<size_t>(T) * R;
   const int ra = round_up(backup_cap, 128);
+  const size_t rI = static_cast<size_t>(ra) * I;
   HybBwdWs w{};
   w.dg = c.take<float>(TR);
   w.du = c.take<float>(TR);
@@ -157,9 +160,12 @@ HybBwdWs carve_hybrid_bwd(Carve& c, int T, int d, int I, int R, int backup_cap) 
   w.csc = c.take<int32_t>(TR);
   w.dY = c.take<uint16_t>(static_cast<size_t>(ra) * d);
   w.X = c.take<uint16_t>(static_cast<size_t>(ra) * d);
-  w.dG = c.take<uint16_t>(static_cast<size_t>(ra) * I);
-  w.dU = c.take<uint16_t>(static_cast<size_t>(ra) * I);
-  w.H = c.take<uint16_t>(static_cast<size_t>(ra) * I);
+  w.g.dG = c.take<uint16_t>(rI);
+  w.g.dG_lo = c.take<uint16_t>(rI);
+  w.g.dU = c.take<uint16_t>(rI);
+  w.g.dU_lo = c.take<uint16_t>(rI);
+  w.g.H = c.take<uint16_t>(rI);
+  w.g.H_lo = c.take<uint16_t>(rI);
   return w;
 }
 
@@ -267,9 +273,11 @@ tw_status twell_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* W
   TW_TRY(tw::launch_sparse_fwd(a, s));
   if (ovf_cap > 0) {
     TW_TRY(tw::launch_gather_rows(x, d, o.ovf_rows, o.n_ovf, ovf_cap, ra, w.X, s));
-    TW_TRY(tw::gemm_backup_hidden(w.X, Wg, Wu, ra, o.n_ovf, ovf_cap, d, I, w.H, nullptr, nullptr, dev_status, s));
-    TW_TRY(tw::gemm_rows_times_nmajor(w.H, Wd, nullptr, nullptr, 1, ra, o.n_ovf, ovf_cap, I, d, y, d, o.ovf_rows,
-                                      dev_status, s));
+    TW_TRY(tw::gemm_backup_hidden(w.X, Wg, Wu, ra, o.n_ovf, ovf_cap, d, I, w.H, w.H_lo, nullptr, nullptr,
+                                  dev_status, s));
+    const uint16_t* A[2] = {w.H, w.H_lo};
+    const uint16_t* B[2] = {Wd, Wd};
+    TW_TRY(tw::gemm_rows_times_nmajor(A, B, 2, ra, o.n_ovf, ovf_cap, I, d, y, d, o.ovf_rows, dev_status, s));
   }
   return TW_OK;
 }
@@ -318,10 +326,12 @@ tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* 
   TW_TRY(tw::launch_sparse_fwd(a, s));
   if (cap > 0) {
     TW_TRY(tw::launch_gather_rows(x, d, saved->backup_tok, saved->n_backup, cap, ra, w.X, s));
-    TW_TRY(tw::gemm_backup_hidden(w.X, Wg, Wu, ra, saved->n_backup, cap, d, I, w.H, saved->backup_a,
+    TW_TRY(tw::gemm_backup_hidden(w.X, Wg, Wu, ra, saved->n_backup, cap, d, I, w.H, w.H_lo, saved->backup_a,
                                   gated ? saved->backup_u : nullptr, dev_status, s));
-    TW_TRY(tw::gemm_rows_times_nmajor(w.H, Wd, nullptr, nullptr, 1, ra, saved->n_backup, cap, I, d, y, d,
-                                      saved->backup_tok, dev_status, s));
+    const uint16_t* A[2] = {w.H, w.H_lo};
+    const uint16_t* B[2] = {Wd, Wd};
+    TW_TRY(tw::gemm_rows_times_nmajor(A, B, 2, ra, saved->n_backup, cap, I, d, y, d, saved->backup_tok, dev_status,
+                                      s));
   }
   return TW_OK;
 }
@@ -372,13 +382,18 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
   if (cap > 0 && T > 0) {
     TW_TRY(tw::launch_gather_rows(dy, d, saved->backup_tok, saved->n_backup, cap, ra, w.dY, s));
     TW_TRY(tw::launch_gather_rows(x, d, saved->backup_tok, saved->n_backup, cap, ra, w.X, s));
-    TW_TRY(tw::gemm_backup_grad(w.dY, Wd, ra, saved->n_backup, cap, d, I, saved->backup_a,
-                                gated ? saved->backup_u : nullptr, l1, w.dG, w.dU, w.H, dev_status, s));
-    TW_TRY(tw::gemm_rows_times_nmajor(w.dG, Wg, w.dU, Wu, gated ? 2 : 1, ra, saved->n_backup, cap, I, d, dx, d,
-                                      saved->backup_tok, dev_status, s));
-    TW_TRY(tw::gemm_weight_grad_add(w.dG, w.X, ra, saved->n_backup, cap, I, d, dWg, dev_status, s));
-    if (gated) TW_TRY(tw::gemm_weight_grad_add(w.dU, w.X, ra, saved->n_backup, cap, I, d, dWu, dev_status, s));
-    TW_TRY(tw::gemm_weight_grad_add(w.H, w.dY, ra, saved->n_backup, cap, I, d, dWd, dev_status, s));
+    const int32_t* nb = saved->n_backup;
+    const tw::BackupGradOut& g = w.g;
+    TW_TRY(tw::gemm_backup_grad(w.dY, Wd, ra, nb, cap, d, I, saved->backup_a, gated ? saved->backup_u : nullptr,
+                                l1, g, dev_status, s));
+    // dx = (dG + dG_lo) Wg + (dU + dU_lo) Wu, scattered back to the backup tokens
+    const uint16_t* A[4] = {g.dG, g.dG_lo, g.dU, g.dU_lo};
+    const uint16_t* B[4] = {Wg, Wg, Wu, Wu};
+    TW_TRY(tw::gemm_rows_times_nmajor(A, B, gated ? 4 : 2, ra, nb, cap, I, d, dx, d, saved->backup_tok, dev_status,
+                                      s));
+    TW_TRY(tw::gemm_weight_grad_add(g.dG, g.dG_lo, w.X, ra, nb, cap, I, d, dWg, dev_status, s));
+    if (gated) TW_TRY(tw::gemm_weight_grad_add(g.dU, g.dU_lo, w.X, ra, nb, cap, I, d, dWu, dev_status, s));
+    TW_TRY(tw::gemm_weight_grad_add(g.H, g.H_lo, w.dY, ra, nb, cap, I, d, dWd, dev_status, s));
   }
   return TW_OK;
 }

@@ -50,9 +50,8 @@ static bool tmap_mnmajor(CUtensorMap* m, const uint16_t* p, int K, int cols) {
 }
 
 template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES, class Epi>
-static cudaError_t run_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1,
-                            const CUtensorMap& b1, const GemmShape& sh, const typename Epi::Params& ep,
-                            int max_rows, cudaStream_t s) {
+static cudaError_t run_gemm(const GemmMaps& maps, const GemmShape& sh, const typename Epi::Params& ep, int max_rows,
+                            cudaStream_t s) {
   using Tr = GemmTraits<BN, A_MN, B_MN, DUAL, STAGES>;
   auto kern = gemm_tc_kernel<BN, A_MN, B_MN, DUAL, STAGES, Epi>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::SMEM_BYTES);
@@ -60,7 +59,7 @@ static cudaError_t run_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const 
   const long tiles = static_cast<long>((max_rows + GEMM_BM - 1) / GEMM_BM) * (sh.N / BN);
   if (tiles <= 0) return cudaSuccess;
   const int grid = static_cast<int>(std::min<long>(tiles, device_sm_count()));
-  kern<<<grid, GEMM_THREADS, Tr::SMEM_BYTES, s>>>(a0, b0, a1, b1, sh, ep);
+  kern<<<grid, GEMM_THREADS, Tr::SMEM_BYTES, s>>>(maps, sh, ep);
   return cudaGetLastError();
 }
 
@@ -78,93 +77,104 @@ static GemmShape shape_static(int M, int N, int K, int32_t* status) {
   return g;
 }
 
+// unused map slots repeat the first ones so that every slot holds a valid map
+static void fill_unused(GemmMaps& m, int used_a, int used_b) {
+  for (int i = used_a; i < GEMM_MAX_SEGMENTS; ++i) m.a[i] = m.a[0];
+  for (int i = used_b; i < GEMM_MAX_SEGMENTS; ++i) m.b[i] = m.b[0];
+}
+
 // ------------------------------------------------------------------ gate + pack
 cudaError_t gemm_gate_pack(const uint16_t* x, const uint16_t* Wg, int T, int d, int I, int W, int C,
                            const tw_twell& o, uint16_t* a_dense, int32_t* status, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   EpiTwellPack::Params ep{T, W, C, I / W, o.cnt, o.val, o.idx, o.row_nnz, o.ovf, a_dense, I};
   const GemmShape sh = shape_static(T, I, d, status);
-  CUtensorMap ta, tb;
-  if (I % 256 == 0) {
-    if (!tmap_kmajor(&ta, x, T, d, 128) || !tmap_kmajor(&tb, Wg, I, d, 256)) return cudaErrorInvalidValue;
-    return run_gemm<256, false, false, false, 4, EpiTwellPack>(ta, tb, ta, tb, sh, ep, T, s);
-  }
-  if (I % 128 == 0) {
-    if (!tmap_kmajor(&ta, x, T, d, 128) || !tmap_kmajor(&tb, Wg, I, d, 128)) return cudaErrorInvalidValue;
-    return run_gemm<128, false, false, false, 6, EpiTwellPack>(ta, tb, ta, tb, sh, ep, T, s);
-  }
-  if (!tmap_kmajor(&ta, x, T, d, 128) || !tmap_kmajor(&tb, Wg, I, d, 64)) return cudaErrorInvalidValue;
-  return run_gemm<64, false, false, false, 8, EpiTwellPack>(ta, tb, ta, tb, sh, ep, T, s);
+  GemmMaps maps;
+  const int bn = (I % 256 == 0) ? 256 : (I % 128 == 0) ? 128 : 64;
+  if (!tmap_kmajor(&maps.a[0], x, T, d, 128) || !tmap_kmajor(&maps.b[0], Wg, I, d, bn)) return cudaErrorInvalidValue;
+  fill_unused(maps, 1, 1);
+  if (bn == 256) return run_gemm<256, false, false, false, 4, EpiTwellPack>(maps, sh, ep, T, s);
+  if (bn == 128) return run_gemm<128, false, false, false, 6, EpiTwellPack>(maps, sh, ep, T, s);
+  return run_gemm<64, false, false, false, 8, EpiTwellPack>(maps, sh, ep, T, s);
 }
 
 // ------------------------------------------------------------------ dense backup, forward
 cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint16_t* Wu, int rows_alloc,
-                               const int32_t* n_dev, int cap, int d, int I, uint16_t* H, uint16_t* save_a,
-                               uint16_t* save_u, int32_t* status, cudaStream_t s) {
+                               const int32_t* n_dev, int cap, int d, int I, uint16_t* H, uint16_t* H_lo,
+                               float* save_a, float* save_u, int32_t* status, cudaStream_t s) {
   if (cap <= 0) return cudaSuccess;
   GemmShape sh = shape_static(0, I, d, status);
   sh.m_dev = n_dev;
   sh.m_cap = cap;
-  CUtensorMap ta, tg, tu;
-  if (!tmap_kmajor(&ta, X, rows_alloc, d, 128) || !tmap_kmajor(&tg, Wg, I, d, 64)) return cudaErrorInvalidValue;
+  GemmMaps maps;
+  if (!tmap_kmajor(&maps.a[0], X, rows_alloc, d, 128) || !tmap_kmajor(&maps.b[0], Wg, I, d, 64))
+    return cudaErrorInvalidValue;
   if (Wu != nullptr) {
-    if (!tmap_kmajor(&tu, Wu, I, d, 64)) return cudaErrorInvalidValue;
-    typename EpiBackupHidden<true>::Params ep{H, save_a, save_u, I, rows_alloc};
-    return run_gemm<64, false, false, true, 6, EpiBackupHidden<true>>(ta, tg, ta, tu, sh, ep, cap, s);
+    if (!tmap_kmajor(&maps.b[1], Wu, I, d, 64)) return cudaErrorInvalidValue;
+    fill_unused(maps, 1, 2);
+    typename EpiBackupHidden<true>::Params ep{H, H_lo, save_a, save_u, I, rows_alloc};
+    return run_gemm<64, false, false, true, 6, EpiBackupHidden<true>>(maps, sh, ep, cap, s);
   }
-  typename EpiBackupHidden<false>::Params ep{H, save_a, nullptr, I, rows_alloc};
-  return run_gemm<64, false, false, false, 8, EpiBackupHidden<false>>(ta, tg, ta, tg, sh, ep, cap, s);
+  fill_unused(maps, 1, 1);
+  typename EpiBackupHidden<false>::Params ep{H, H_lo, save_a, nullptr, I, rows_alloc};
+  return run_gemm<64, false, false, false, 8, EpiBackupHidden<false>>(maps, sh, ep, cap, s);
 }
 
-cudaError_t gemm_rows_times_nmajor(const uint16_t* A0, const uint16_t* B0, const uint16_t* A1, const uint16_t* B1,
-                                   int segments, int rows_alloc, const int32_t* n_dev, int cap, int K, int N,
-                                   uint16_t* out, int ldo, const int32_t* row_map, int32_t* status, cudaStream_t s) {
+cudaError_t gemm_rows_times_nmajor(const uint16_t* const* A, const uint16_t* const* B, int segments, int rows_alloc,
+                                   const int32_t* n_dev, int cap, int K, int N, uint16_t* out, int ldo,
+                                   const int32_t* row_map, int32_t* status, cudaStream_t s) {
   if (cap <= 0) return cudaSuccess;
+  if (segments < 1 || segments > GEMM_MAX_SEGMENTS) return cudaErrorInvalidValue;
   GemmShape sh = shape_static(0, N, K, status);
   sh.m_dev = n_dev;
   sh.m_cap = cap;
   sh.segments = segments;
-  CUtensorMap ta0, tb0, ta1, tb1;
-  if (!tmap_kmajor(&ta0, A0, rows_alloc, K, 128) || !tmap_mnmajor(&tb0, B0, K, N)) return cudaErrorInvalidValue;
-  if (segments > 1) {
-    if (!tmap_kmajor(&ta1, A1, rows_alloc, K, 128) || !tmap_mnmajor(&tb1, B1, K, N)) return cudaErrorInvalidValue;
-  } else {
-    ta1 = ta0;
-    tb1 = tb0;
-  }
+  GemmMaps maps;
+  for (int i = 0; i < segments; ++i)
+    if (!tmap_kmajor(&maps.a[i], A[i], rows_alloc, K, 128) || !tmap_mnmajor(&maps.b[i], B[i], K, N))
+      return cudaErrorInvalidValue;
+  fill_unused(maps, segments, segments);
   EpiScatterBf16::Params ep{out, ldo, row_map};
-  return run_gemm<64, false, true, false, 8, EpiScatterBf16>(ta0, tb0, ta1, tb1, sh, ep, cap, s);
+  return run_gemm<64, false, true, false, 8, EpiScatterBf16>(maps, sh, ep, cap, s);
 }
 
 // ------------------------------------------------------------------ dense backup, backward
 cudaError_t gemm_backup_grad(const uint16_t* dY, const uint16_t* Wd, int rows_alloc, const int32_t* n_dev, int cap,
-                             int d, int I, const uint16_t* a, const uint16_t* u, float l1, uint16_t* dG,
-                             uint16_t* dU, uint16_t* H, int32_t* status, cudaStream_t s) {
+                             int d, int I, const float* a, const float* u, float l1, const BackupGradOut& o,
+                             int32_t* status, cudaStream_t s) {
   if (cap <= 0) return cudaSuccess;
   GemmShape sh = shape_static(0, I, d, status);
   sh.m_dev = n_dev;
   sh.m_cap = cap;
-  CUtensorMap ta, tb;
-  if (!tmap_kmajor(&ta, dY, rows_alloc, d, 128) || !tmap_kmajor(&tb, Wd, I, d, 64)) return cudaErrorInvalidValue;
+  GemmMaps maps;
+  if (!tmap_kmajor(&maps.a[0], dY, rows_alloc, d, 128) || !tmap_kmajor(&maps.b[0], Wd, I, d, 64))
+    return cudaErrorInvalidValue;
+  fill_unused(maps, 1, 1);
   if (u != nullptr) {
-    typename EpiBackupGrad<true>::Params ep{a, u, dG, dU, H, l1, I, rows_alloc};
-    return run_gemm<64, false, false, false, 8, EpiBackupGrad<true>>(ta, tb, ta, tb, sh, ep, cap, s);
+    typename EpiBackupGrad<true>::Params ep{a, u, o.dG, o.dG_lo, o.dU, o.dU_lo, o.H, o.H_lo, l1, I, rows_alloc};
+    return run_gemm<64, false, false, false, 8, EpiBackupGrad<true>>(maps, sh, ep, cap, s);
   }
-  typename EpiBackupGrad<false>::Params ep{a, nullptr, dG, nullptr, H, l1, I, rows_alloc};
-  return run_gemm<64, false, false, false, 8, EpiBackupGrad<false>>(ta, tb, ta, tb, sh, ep, cap, s);
+  typename EpiBackupGrad<false>::Params ep{a, nullptr, o.dG, o.dG_lo, nullptr, nullptr, o.H, o.H_lo, l1, I, rows_alloc};
+  return run_gemm<64, false, false, false, 8, EpiBackupGrad<false>>(maps, sh, ep, cap, s);
 }
 
-cudaError_t gemm_weight_grad_add(const uint16_t* P, const uint16_t* Q, int rows_alloc, const int32_t* n_dev,
-                                 int cap, int I, int d, float* D, int32_t* status, cudaStream_t s) {
+cudaError_t gemm_weight_grad_add(const uint16_t* P_hi, const uint16_t* P_lo, const uint16_t* Q, int rows_alloc,
+                                 const int32_t* n_dev, int cap, int I, int d, float* D, int32_t* status,
+                                 cudaStream_t s) {
   if (cap <= 0) return cudaSuccess;
   GemmShape sh = shape_static(I, d, 0, status);
   sh.k_dev = n_dev;
   sh.k_cap = cap;
-  CUtensorMap ta, tb;
-  if (!tmap_mnmajor(&ta, P, rows_alloc, I) || !tmap_mnmajor(&tb, Q, rows_alloc, d)) return cudaErrorInvalidValue;
+  sh.segments = 2;
+  GemmMaps maps;
+  if (!tmap_mnmajor(&maps.a[0], P_hi, rows_alloc, I) || !tmap_mnmajor(&maps.a[1], P_lo, rows_alloc, I) ||
+      !tmap_mnmajor(&maps.b[0], Q, rows_alloc, d))
+    return cudaErrorInvalidValue;
+  maps.b[1] = maps.b[0];
+  fill_unused(maps, 2, 2);
   EpiAddF32::Params ep{D, d};
-  if (d % 256 == 0) return run_gemm<256, true, true, false, 4, EpiAddF32>(ta, tb, ta, tb, sh, ep, I, s);
-  return run_gemm<64, true, true, false, 8, EpiAddF32>(ta, tb, ta, tb, sh, ep, I, s);
+  if (d % 256 == 0) return run_gemm<256, true, true, false, 4, EpiAddF32>(maps, sh, ep, I, s);
+  return run_gemm<64, true, true, false, 8, EpiAddF32>(maps, sh, ep, I, s);
 }
 
 // ------------------------------------------------------------------ layout test GEMM
@@ -172,14 +182,15 @@ cudaError_t gemm_dense_test(const uint16_t* A, const uint16_t* B, int M, int N, 
                             int32_t* status, cudaStream_t s) {
   const GemmShape sh = shape_static(M, N, K, status);
   EpiStoreF32::Params ep{D, N};
-  CUtensorMap ta, tb;
-  const bool oka = a_mn ? tmap_mnmajor(&ta, A, K, M) : tmap_kmajor(&ta, A, M, K, 128);
-  const bool okb = b_mn ? tmap_mnmajor(&tb, B, K, N) : tmap_kmajor(&tb, B, N, K, 64);
+  GemmMaps maps;
+  const bool oka = a_mn ? tmap_mnmajor(&maps.a[0], A, K, M) : tmap_kmajor(&maps.a[0], A, M, K, 128);
+  const bool okb = b_mn ? tmap_mnmajor(&maps.b[0], B, K, N) : tmap_kmajor(&maps.b[0], B, N, K, 64);
   if (!oka || !okb) return cudaErrorInvalidValue;
-  if (!a_mn && !b_mn) return run_gemm<64, false, false, false, 8, EpiStoreF32>(ta, tb, ta, tb, sh, ep, M, s);
-  if (!a_mn && b_mn) return run_gemm<64, false, true, false, 8, EpiStoreF32>(ta, tb, ta, tb, sh, ep, M, s);
-  if (a_mn && !b_mn) return run_gemm<64, true, false, false, 8, EpiStoreF32>(ta, tb, ta, tb, sh, ep, M, s);
-  return run_gemm<64, true, true, false, 8, EpiStoreF32>(ta, tb, ta, tb, sh, ep, M, s);
+  fill_unused(maps, 1, 1);
+  if (!a_mn && !b_mn) return run_gemm<64, false, false, false, 8, EpiStoreF32>(maps, sh, ep, M, s);
+  if (!a_mn && b_mn) return run_gemm<64, false, true, false, 8, EpiStoreF32>(maps, sh, ep, M, s);
+  if (a_mn && !b_mn) return run_gemm<64, true, false, false, 8, EpiStoreF32>(maps, sh, ep, M, s);
+  return run_gemm<64, true, true, false, 8, EpiStoreF32>(maps, sh, ep, M, s);
 }
 
 }  // namespace tw

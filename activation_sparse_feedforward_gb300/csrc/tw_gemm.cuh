@@ -13,9 +13,11 @@
 // A is [M, K] with K contiguous ("K-major") or stored [K, M] ("MN-major"); the same
 // for B with N in place of M. DUAL issues a second MMA with a second B operand into
 // its own accumulator (gate and up projections of the same rows in one pass).
-// `segments == 2` continues the K loop over a second (A, B) pair into the same
-// accumulator. M and K may be read from device memory (counts produced by earlier
-// kernels in the stream), so the launch does not need them on the host.
+// `segments == S` (up to 4) continues the K loop over S (A, B) pairs into the same
+// accumulator: a second product (dx = dG Wg + dU Wu) or the low half of an operand
+// split into two bf16 parts (x = hi + lo) to keep fp32-level precision. M and K may
+// be read from device memory (counts produced by earlier kernels in the stream), so
+// the launch does not need them on the host.
 #pragma once
 
 #include "tw_common.cuh"
@@ -34,8 +36,17 @@ struct GemmShape {
   int K;             // reduction length when k_dev == nullptr
   const int* k_dev;  // optional device K, clamped to [0, k_cap]; memory past K must read as zero
   int k_cap;
-  int segments;      // 1 or 2
+  int segments;      // 1 to 4 (A, B) pairs
   int32_t* status;
+};
+
+constexpr int GEMM_MAX_SEGMENTS = 4;
+
+// Tensor maps of every operand: segment s reads a[s] and b[s]; the DUAL form reads
+// b[0] and b[1] against a[0].
+struct GemmMaps {
+  CUtensorMap a[GEMM_MAX_SEGMENTS];
+  CUtensorMap b[GEMM_MAX_SEGMENTS];
 };
 
 template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES>
@@ -67,9 +78,8 @@ TW_DEV bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
 
 template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES, class Epi>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
-                   const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
-                   const GemmShape shape, const __grid_constant__ typename Epi::Params ep) {
+    gemm_tc_kernel(const __grid_constant__ GemmMaps maps, const GemmShape shape,
+                   const __grid_constant__ typename Epi::Params ep) {
   using Tr = GemmTraits<BN, A_MN, B_MN, DUAL, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
@@ -97,12 +107,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA0);
-    tma_prefetch_desc(&tmB0);
-    if (DUAL || shape.segments > 1) {
-      tma_prefetch_desc(&tmB1);
-      if (shape.segments > 1) tma_prefetch_desc(&tmA1);
+    for (int sgi = 0; sgi < shape.segments; ++sgi) {
+      tma_prefetch_desc(&maps.a[sgi]);
+      tma_prefetch_desc(&maps.b[sgi]);
     }
+    if (DUAL) tma_prefetch_desc(&maps.b[1]);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, Tr::TMEM_COLS);
@@ -142,8 +151,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           uint8_t* sB = sA + Tr::A_BYTES;
           const int seg = kb / kb_per_seg;
           const int k0 = (kb - seg * kb_per_seg) * GEMM_BK;
-          const CUtensorMap* ta = seg ? &tmA1 : &tmA0;
-          const CUtensorMap* tb = seg ? &tmB1 : &tmB0;
+          const CUtensorMap* ta = &maps.a[seg];
+          const CUtensorMap* tb = &maps.b[seg];
           mbar_arrive_expect_tx(full + stage, Tr::STAGE_BYTES);
           if (!A_MN) {
             tma_load_2d(sA, ta, full + stage, k0, m0);
@@ -153,7 +162,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
 #pragma unroll
           for (int nb = 0; nb < Tr::NB; ++nb) {
-            const CUtensorMap* tbb = (nb == 0) ? tb : &tmB1;
+            const CUtensorMap* tbb = (nb == 0) ? tb : &maps.b[1];
             uint8_t* dst = sB + nb * Tr::B_BYTES;
             if (!B_MN) {
               tma_load_2d(dst, tbb, full + stage, k0, n0);
@@ -416,19 +425,38 @@ struct EpiTwellPack {
   }
 };
 
+// Eight fp32 values as an exact-to-2^-16 pair of bf16 vectors: hi = bf16(v),
+// lo = bf16(v - hi). A GEMM run over both halves (two K segments against the same
+// other operand) keeps the precision of an fp32 operand.
+TW_DEV void split8(const float (&v)[8], uint4& hi, uint4& lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    h[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    l[i] = pack_bf16x2(v[2 * i] - bf16_lo(h[i]), v[2 * i + 1] - bf16_hi(h[i]));
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
 // Dense-backup forward epilogue on a (gate, up) accumulator pair:
-//   a = bf16(ReLU(g)), h = bf16(a * u) (gated) or h = a (non-gated).
-// Writes h (the next GEMM's A operand) and optionally a and bf16(u) (saved for the
-// backward). Rows in [M, end of tile) are written as zeros so that later GEMMs whose
-// K runs over these rows read zeros.
+//   a = ReLU(g), h = a * u (gated) or a (non-gated), all fp32.
+// h is written as the bf16 pair (H, H_lo) that the down-projection GEMM runs over,
+// so backup rows lose no more precision than the CUDA-core path, whose h never
+// leaves fp32. Backup rows are the high-activity rows (hundreds of large terms per
+// output), where a single bf16 rounding of h would dominate the error of y.
+// Optionally saves a and u in fp32 (the Hybrid's dense backup) for the backward.
+// Rows in [M, end of tile) are written as zeros so that later GEMMs whose K runs
+// over these rows read zeros.
 template <bool GATED>
 struct EpiBackupHidden {
   struct Params {
     uint16_t* H;
-    uint16_t* save_a;  // optional
-    uint16_t* save_u;  // optional
-    int ld;            // row stride of H / save_a / save_u (= I)
-    int rows_alloc;    // rows the buffers hold
+    uint16_t* H_lo;
+    float* save_a;  // optional
+    float* save_u;  // optional
+    int ld;         // row stride of every buffer (= I)
+    int rows_alloc; // rows H / H_lo hold
   };
   const Params& p;
   int m, M, n0;
@@ -437,57 +465,46 @@ struct EpiBackupHidden {
     if (m >= p.rows_alloc) return;
     const bool live = m < M;
     const size_t off = static_cast<size_t>(m) * p.ld + n0 + c * 32;
-    uint32_t hh[16], aa[16], uu[16];
 #pragma unroll
-    for (int i = 0; i < 32; i += 2) {
-      float a0 = 0.f, a1 = 0.f, h0 = 0.f, h1 = 0.f, u0 = 0.f, u1 = 0.f;
-      if (live) {
-        const float g0 = __uint_as_float(g[i]), g1 = __uint_as_float(g[i + 1]);
-        a0 = bf16_to_f32(f32_to_bf16(g0 > 0.f ? g0 : 0.f));
-        a1 = bf16_to_f32(f32_to_bf16(g1 > 0.f ? g1 : 0.f));
-        if (GATED) {
-          u0 = __uint_as_float(u[i]);
-          u1 = __uint_as_float(u[i + 1]);
-          h0 = a0 * u0;
-          h1 = a1 * u1;
-        } else {
-          h0 = a0;
-          h1 = a1;
-        }
+    for (int q = 0; q < 4; ++q) {
+      float a[8], uv[8], h[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float gv = __uint_as_float(g[8 * q + i]);
+        a[i] = (live && gv > 0.f) ? gv : 0.f;
+        uv[i] = (GATED && live) ? __uint_as_float(u[8 * q + i]) : 0.f;
+        h[i] = GATED ? a[i] * uv[i] : a[i];
       }
-      hh[i >> 1] = pack_bf16x2(h0, h1);
-      aa[i >> 1] = pack_bf16x2(a0, a1);
-      uu[i >> 1] = pack_bf16x2(u0, u1);
-    }
-    uint4* dh = reinterpret_cast<uint4*>(p.H + off);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) dh[i] = make_uint4(hh[4 * i], hh[4 * i + 1], hh[4 * i + 2], hh[4 * i + 3]);
-    if (p.save_a != nullptr && live) {
-      uint4* da = reinterpret_cast<uint4*>(p.save_a + off);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) da[i] = make_uint4(aa[4 * i], aa[4 * i + 1], aa[4 * i + 2], aa[4 * i + 3]);
-    }
-    if (GATED && p.save_u != nullptr && live) {
-      uint4* du = reinterpret_cast<uint4*>(p.save_u + off);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) du[i] = make_uint4(uu[4 * i], uu[4 * i + 1], uu[4 * i + 2], uu[4 * i + 3]);
+      uint4 hi, lo;
+      split8(h, hi, lo);
+      reinterpret_cast<uint4*>(p.H + off)[q] = hi;
+      reinterpret_cast<uint4*>(p.H_lo + off)[q] = lo;
+      if (p.save_a != nullptr && live) {
+        float4* da = reinterpret_cast<float4*>(p.save_a + off) + 2 * q;
+        da[0] = make_float4(a[0], a[1], a[2], a[3]);
+        da[1] = make_float4(a[4], a[5], a[6], a[7]);
+      }
+      if (GATED && p.save_u != nullptr && live) {
+        float4* du = reinterpret_cast<float4*>(p.save_u + off) + 2 * q;
+        du[0] = make_float4(uv[0], uv[1], uv[2], uv[3]);
+        du[1] = make_float4(uv[4], uv[5], uv[6], uv[7]);
+      }
     }
   }
   TW_DEV void finish() {}
 };
 
-// Dense-backup backward epilogue on dh = dY Wd^T with the saved a and u rows:
-//   du = dh * a,  dg = (dh * u + l1) on a != 0 (non-gated: dh + l1), else 0,
-//   h = a * u (non-gated: a).
-// Writes dG, dU and H as bf16 GEMM operands; rows in [M, end of tile) become zeros.
+// Dense-backup backward epilogue on dh = dY Wd^T with the saved fp32 a and u rows:
+//   du = dh * a,  dg = (dh * u + l1) where a > 0 (non-gated: dh + l1), else 0,
+//   h = a * u (non-gated: a),
+// each written as a (hi, lo) bf16 pair for the dx and weight-gradient GEMMs. Rows in
+// [M, end of tile) become zeros.
 template <bool GATED>
 struct EpiBackupGrad {
   struct Params {
-    const uint16_t* a;
-    const uint16_t* u;
-    uint16_t* dG;
-    uint16_t* dU;
-    uint16_t* H;
+    const float* a;
+    const float* u;
+    uint16_t *dG, *dG_lo, *dU, *dU_lo, *H, *H_lo;
     float l1;
     int ld;
     int rows_alloc;
@@ -499,46 +516,44 @@ struct EpiBackupGrad {
     if (m >= p.rows_alloc) return;
     const bool live = m < M;
     const size_t off = static_cast<size_t>(m) * p.ld + n0 + c * 32;
-    uint32_t gg[16], uo[16], hh[16];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      uint4 av = make_uint4(0, 0, 0, 0), uv = make_uint4(0, 0, 0, 0);
+      float av[8], uv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) av[i] = uv[i] = 0.f;
       if (live) {
-        av = reinterpret_cast<const uint4*>(p.a + off)[q];
-        if (GATED) uv = reinterpret_cast<const uint4*>(p.u + off)[q];
-      }
-      const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
-      const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        float dg2[2], du2[2], h2[2];
-#pragma unroll
-        for (int hlf = 0; hlf < 2; ++hlf) {
-          const int i = q * 8 + w * 2 + hlf;
-          const float a = hlf ? bf16_hi(aw[w]) : bf16_lo(aw[w]);
-          const float u = GATED ? (hlf ? bf16_hi(uw[w]) : bf16_lo(uw[w])) : 1.0f;
-          const float d = __uint_as_float(dh[i]);
-          const bool act = live && (a != 0.0f);
-          dg2[hlf] = act ? (GATED ? d * u : d) + p.l1 : 0.0f;
-          du2[hlf] = act ? d * a : 0.0f;
-          h2[hlf] = live ? (GATED ? a * u : a) : 0.0f;
+        const float4* pa = reinterpret_cast<const float4*>(p.a + off) + 2 * q;
+        const float4 a0 = pa[0], a1 = pa[1];
+        av[0] = a0.x; av[1] = a0.y; av[2] = a0.z; av[3] = a0.w;
+        av[4] = a1.x; av[5] = a1.y; av[6] = a1.z; av[7] = a1.w;
+        if (GATED) {
+          const float4* pu = reinterpret_cast<const float4*>(p.u + off) + 2 * q;
+          const float4 u0 = pu[0], u1 = pu[1];
+          uv[0] = u0.x; uv[1] = u0.y; uv[2] = u0.z; uv[3] = u0.w;
+          uv[4] = u1.x; uv[5] = u1.y; uv[6] = u1.z; uv[7] = u1.w;
         }
-        gg[q * 4 + w] = pack_bf16x2(dg2[0], dg2[1]);
-        uo[q * 4 + w] = pack_bf16x2(du2[0], du2[1]);
-        hh[q * 4 + w] = pack_bf16x2(h2[0], h2[1]);
       }
-    }
-    uint4* pg = reinterpret_cast<uint4*>(p.dG + off);
-    uint4* ph = reinterpret_cast<uint4*>(p.H + off);
+      float dg[8], du[8], h[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      pg[i] = make_uint4(gg[4 * i], gg[4 * i + 1], gg[4 * i + 2], gg[4 * i + 3]);
-      ph[i] = make_uint4(hh[4 * i], hh[4 * i + 1], hh[4 * i + 2], hh[4 * i + 3]);
-    }
-    if (GATED) {
-      uint4* pu = reinterpret_cast<uint4*>(p.dU + off);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) pu[i] = make_uint4(uo[4 * i], uo[4 * i + 1], uo[4 * i + 2], uo[4 * i + 3]);
+      for (int i = 0; i < 8; ++i) {
+        const float d = __uint_as_float(dh[8 * q + i]);
+        const bool act = av[i] > 0.f;
+        dg[i] = act ? (GATED ? d * uv[i] : d) + p.l1 : 0.f;
+        du[i] = act ? d * av[i] : 0.f;
+        h[i] = GATED ? av[i] * uv[i] : av[i];
+      }
+      uint4 hi, lo;
+      split8(dg, hi, lo);
+      reinterpret_cast<uint4*>(p.dG + off)[q] = hi;
+      reinterpret_cast<uint4*>(p.dG_lo + off)[q] = lo;
+      split8(h, hi, lo);
+      reinterpret_cast<uint4*>(p.H + off)[q] = hi;
+      reinterpret_cast<uint4*>(p.H_lo + off)[q] = lo;
+      if (GATED) {
+        split8(du, hi, lo);
+        reinterpret_cast<uint4*>(p.dU + off)[q] = hi;
+        reinterpret_cast<uint4*>(p.dU_lo + off)[q] = lo;
+      }
     }
   }
   TW_DEV void finish() {}

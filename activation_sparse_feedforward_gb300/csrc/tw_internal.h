@@ -78,27 +78,32 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t o
 cudaError_t gemm_gate_pack(const uint16_t* x, const uint16_t* Wg, int T, int d, int I, int W, int C,
                            const tw_twell& o, uint16_t* a_dense, int32_t* status, cudaStream_t s);
 
-// dense backup forward: H = h(X Wg^T, X Wu^T) over n (device) rows of X [rows_alloc, d];
-// optional saved a / u.
+// dense backup forward: h(X Wg^T, X Wu^T) over n (device) rows of X [rows_alloc, d],
+// written as the bf16 pair H + H_lo; optional saved fp32 a / u.
 cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint16_t* Wu, int rows_alloc,
-                               const int32_t* n_dev, int cap, int d, int I, uint16_t* H, uint16_t* save_a,
-                               uint16_t* save_u, int32_t* status, cudaStream_t s);
+                               const int32_t* n_dev, int cap, int d, int I, uint16_t* H, uint16_t* H_lo,
+                               float* save_a, float* save_u, int32_t* status, cudaStream_t s);
 
-// out[row_map[m]] = bf16(sum_s A_s B_s) with A_s [rows_alloc, K] K-major and B_s
-// stored [K, N] (N-major); M = n (device) rows, up to cap.
-cudaError_t gemm_rows_times_nmajor(const uint16_t* A0, const uint16_t* B0, const uint16_t* A1, const uint16_t* B1,
-                                   int segments, int rows_alloc, const int32_t* n_dev, int cap, int K, int N,
-                                   uint16_t* out, int ldo, const int32_t* row_map, int32_t* status, cudaStream_t s);
+// out[row_map[m]] = bf16(sum_s A[s] B[s]) over `segments` pairs, A[s] [rows_alloc, K]
+// K-major and B[s] stored [K, N] (N-major); M = n (device) rows, up to cap.
+cudaError_t gemm_rows_times_nmajor(const uint16_t* const* A, const uint16_t* const* B, int segments, int rows_alloc,
+                                   const int32_t* n_dev, int cap, int K, int N, uint16_t* out, int ldo,
+                                   const int32_t* row_map, int32_t* status, cudaStream_t s);
 
-// dense backup backward part 1: dh = dY Wd^T and the epilogue producing dG, dU, H.
+// dense backup backward part 1: dh = dY Wd^T and the epilogue producing dG, dU and H,
+// each as a (hi, lo) bf16 pair [rows_alloc, I].
+struct BackupGradOut {
+  uint16_t *dG, *dG_lo, *dU, *dU_lo, *H, *H_lo;
+};
 cudaError_t gemm_backup_grad(const uint16_t* dY, const uint16_t* Wd, int rows_alloc, const int32_t* n_dev, int cap,
-                             int d, int I, const uint16_t* a, const uint16_t* u, float l1, uint16_t* dG,
-                             uint16_t* dU, uint16_t* H, int32_t* status, cudaStream_t s);
+                             int d, int I, const float* a, const float* u, float l1, const BackupGradOut& o,
+                             int32_t* status, cudaStream_t s);
 
-// D[I, d] += P^T Q with P [rows_alloc, I] and Q [rows_alloc, d] (both stored with
-// the reduction over rows), K = n (device) rows, up to cap.
-cudaError_t gemm_weight_grad_add(const uint16_t* P, const uint16_t* Q, int rows_alloc, const int32_t* n_dev,
-                                 int cap, int I, int d, float* D, int32_t* status, cudaStream_t s);
+// D[I, d] += (P_hi + P_lo)^T Q with P [rows_alloc, I] and Q [rows_alloc, d] (both
+// stored with the reduction over rows), K = n (device) rows, up to cap.
+cudaError_t gemm_weight_grad_add(const uint16_t* P_hi, const uint16_t* P_lo, const uint16_t* Q, int rows_alloc,
+                                 const int32_t* n_dev, int cap, int I, int d, float* D, int32_t* status,
+                                 cudaStream_t s);
 
 cudaError_t gemm_dense_test(const uint16_t* A, const uint16_t* B, int M, int N, int K, int a_mn, int b_mn, float* D,
                             int32_t* status, cudaStream_t s);

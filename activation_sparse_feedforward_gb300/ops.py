@@ -92,8 +92,8 @@ class Hybrid:
     ell_u: torch.Tensor | None  # [T, R] bf16
     backup_slot: torch.Tensor  # [T] int32
     backup_tok: torch.Tensor   # [max(cap,1)] int32
-    backup_a: torch.Tensor     # [max(cap,1), I] bf16
-    backup_u: torch.Tensor | None
+    backup_a: torch.Tensor     # [max(cap,1), I] fp32
+    backup_u: torch.Tensor | None  # [max(cap,1), I] fp32
     n_backup: torch.Tensor     # [1] int32
 
     @staticmethod
@@ -107,8 +107,8 @@ class Hybrid:
                       ell_u=torch.empty((max(T, 1), R), dtype=BF16, device=device) if gated else None,
                       backup_slot=torch.empty(max(T, 1), dtype=torch.int32, device=device),
                       backup_tok=torch.empty(cap1, dtype=torch.int32, device=device),
-                      backup_a=torch.empty((cap1, I), dtype=BF16, device=device),
-                      backup_u=torch.empty((cap1, I), dtype=BF16, device=device) if gated else None,
+                      backup_a=torch.empty((cap1, I), dtype=torch.float32, device=device),
+                      backup_u=torch.empty((cap1, I), dtype=torch.float32, device=device) if gated else None,
                       n_backup=torch.zeros(1, dtype=torch.int32, device=device))
 
     def struct(self) -> _lib.TwHybrid:

@@ -19,9 +19,10 @@
  *   Every weight is [I, d]: row j of Wg (W1) and Wu is neuron j's input weight
  *   vector; row j of Wd (W2) is the vector neuron j adds to y. Wu == NULL selects
  *   the non-gated form.
- * - Shapes: T >= 0 tokens; d % 64 == 0 and 64 <= d <= 16384; W in {64, 128};
- *   I % W == 0, 64 <= I <= 65536; 1 <= C <= W; 1 <= R <= I.
- *   T == 0 is a valid no-op.
+ * - Shapes: T >= 0 tokens; d % 256 == 0 and 256 <= d <= 2048 (the sparse kernels
+ *   keep a whole d-vector per warp in registers); W in {64, 128}; I % W == 0,
+ *   64 <= I <= 65536; 1 <= C <= W; 1 <= R <= I; 0 <= backup_cap <= T.
+ *   T == 0 is a valid no-op. Other shapes return TW_EUNSUPPORTED.
  * - Alignment: every pointer must be 16-byte aligned (TMA and 128-bit accesses).
  * - Ownership: the caller allocates and frees every buffer, including the
  *   workspace whose size the *_workspace_size() functions return. The library
@@ -89,7 +90,9 @@ typedef struct {
  *   ell_a[t*R + s], ell_u[t*R + s]  bf16 a and u at that neuron (ell_u unused when non-gated)
  *   backup_slot[t]                  slot of row t in the backup, or -1
  *   backup_tok[b]                   token of backup slot b, ascending in b
- *   backup_a[b*I + j], backup_u[b*I + j]   full bf16 rows of a and u
+ *   backup_a[b*I + j], backup_u[b*I + j]   full fp32 rows of a = ReLU(g) and u (the
+ *                                   backup rows carry the largest activations, so
+ *                                   they are kept at full precision)
  *   n_backup[0]                     number of backup rows (may exceed backup_cap:
  *                                   then only backup_cap rows are written and
  *                                   TW_ECAPACITY is raised in *dev_status)
@@ -103,8 +106,8 @@ typedef struct {
   uint16_t* ell_u;
   int32_t* backup_slot;
   int32_t* backup_tok;
-  uint16_t* backup_a;
-  uint16_t* backup_u;
+  float* backup_a;
+  float* backup_u;
   int32_t* n_backup;
 } tw_hybrid;
 
