@@ -52,6 +52,9 @@ SIGNATURES = {
                                c_void_p, c_size_t, c_void_p, c_void_p]),
     "tw_dense_gemm": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p,
                               c_void_p]),
+    "tw_trace_begin": (c_int, [ctypes.POINTER(c_void_p), c_int]),
+    "tw_trace_end": (c_int, []),
+    "tw_trace_label": (ctypes.c_char_p, [c_int]),
 }
 
 _lib = None

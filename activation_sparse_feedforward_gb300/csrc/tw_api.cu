@@ -189,6 +189,16 @@ const char* tw_status_str(int status) {
 
 int tw_abi_version(void) { return kAbiVersion; }
 
+tw_status tw_trace_begin(void* const* events, int capacity) {
+  if (events == nullptr || capacity < 1) return TW_EINVAL;
+  tw::trace_begin(events, capacity);
+  return TW_OK;
+}
+
+int tw_trace_end(void) { return tw::trace_end(); }
+
+const char* tw_trace_label(int i) { return tw::trace_label(i); }
+
 tw_status twell_pack(const uint16_t* A, int T, int I, int W, int C, const tw_twell* out, int32_t* dev_status,
                      void* stream) {
   tw_status st = check_tile_geometry(T, I, W, C);
@@ -208,8 +218,8 @@ tw_status twell_pack(const uint16_t* A, int T, int I, int W, int C, const tw_twe
 static tw_status gate_pack_impl(const uint16_t* x, const uint16_t* Wg, int T, int d, int I, int W, int C,
                                 const tw_twell& o, uint16_t* a_dense, int cap_check, int32_t* dev_status,
                                 cudaStream_t s) {
-  TW_TRY(cudaMemsetAsync(o.row_nnz, 0, sizeof(int32_t) * T, s));
-  TW_TRY(cudaMemsetAsync(o.ovf, 0, static_cast<size_t>(T), s));
+  TW_TRY(tw::memset_async(o.row_nnz, 0, sizeof(int32_t) * T, s));
+  TW_TRY(tw::memset_async(o.ovf, 0, static_cast<size_t>(T), s));
   TW_TRY(tw::gemm_gate_pack(x, Wg, T, d, I, W, C, o, a_dense, dev_status, s));
   TW_TRY(tw::launch_compact_rows(o.ovf, nullptr, 0, T, o.ovf_rows, T, o.n_ovf, nullptr, nullptr, cap_check,
                                  dev_status, s));

@@ -51,7 +51,7 @@ static bool tmap_mnmajor(CUtensorMap* m, const uint16_t* p, int K, int cols) {
 
 template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES, class Epi>
 static cudaError_t run_gemm(const GemmMaps& maps, const GemmShape& sh, const typename Epi::Params& ep, int max_rows,
-                            cudaStream_t s) {
+                            cudaStream_t s, const char* label) {
   using Tr = GemmTraits<BN, A_MN, B_MN, DUAL, STAGES>;
   auto kern = gemm_tc_kernel<BN, A_MN, B_MN, DUAL, STAGES, Epi>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::SMEM_BYTES);
@@ -60,6 +60,7 @@ static cudaError_t run_gemm(const GemmMaps& maps, const GemmShape& sh, const typ
   if (tiles <= 0) return cudaSuccess;
   const int grid = static_cast<int>(std::min<long>(tiles, device_sm_count()));
   kern<<<grid, GEMM_THREADS, Tr::SMEM_BYTES, s>>>(maps, sh, ep);
+  trace_mark(s, label);
   return cudaGetLastError();
 }
 
@@ -93,9 +94,9 @@ cudaError_t gemm_gate_pack(const uint16_t* x, const uint16_t* Wg, int T, int d, 
   const int bn = (I % 256 == 0) ? 256 : (I % 128 == 0) ? 128 : 64;
   if (!tmap_kmajor(&maps.a[0], x, T, d, 128) || !tmap_kmajor(&maps.b[0], Wg, I, d, bn)) return cudaErrorInvalidValue;
   fill_unused(maps, 1, 1);
-  if (bn == 256) return run_gemm<256, false, false, false, 4, EpiTwellPack>(maps, sh, ep, T, s);
-  if (bn == 128) return run_gemm<128, false, false, false, 6, EpiTwellPack>(maps, sh, ep, T, s);
-  return run_gemm<64, false, false, false, 8, EpiTwellPack>(maps, sh, ep, T, s);
+  if (bn == 256) return run_gemm<256, false, false, false, 4, EpiTwellPack>(maps, sh, ep, T, s, "gate_pack");
+  if (bn == 128) return run_gemm<128, false, false, false, 6, EpiTwellPack>(maps, sh, ep, T, s, "gate_pack");
+  return run_gemm<64, false, false, false, 8, EpiTwellPack>(maps, sh, ep, T, s, "gate_pack");
 }
 
 // ------------------------------------------------------------------ dense backup, forward
@@ -113,11 +114,11 @@ cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint
     if (!tmap_kmajor(&maps.b[1], Wu, I, d, 64)) return cudaErrorInvalidValue;
     fill_unused(maps, 1, 2);
     typename EpiBackupHidden<true>::Params ep{H, H_lo, save_a, save_u, I, rows_alloc};
-    return run_gemm<64, false, false, true, 6, EpiBackupHidden<true>>(maps, sh, ep, cap, s);
+    return run_gemm<64, false, false, true, 6, EpiBackupHidden<true>>(maps, sh, ep, cap, s, "backup_hidden");
   }
   fill_unused(maps, 1, 1);
   typename EpiBackupHidden<false>::Params ep{H, H_lo, save_a, nullptr, I, rows_alloc};
-  return run_gemm<64, false, false, false, 8, EpiBackupHidden<false>>(maps, sh, ep, cap, s);
+  return run_gemm<64, false, false, false, 8, EpiBackupHidden<false>>(maps, sh, ep, cap, s, "backup_hidden");
 }
 
 cudaError_t gemm_rows_times_nmajor(const uint16_t* const* A, const uint16_t* const* B, int segments, int rows_alloc,
@@ -135,7 +136,7 @@ cudaError_t gemm_rows_times_nmajor(const uint16_t* const* A, const uint16_t* con
       return cudaErrorInvalidValue;
   fill_unused(maps, segments, segments);
   EpiScatterBf16::Params ep{out, ldo, row_map};
-  return run_gemm<64, false, true, false, 8, EpiScatterBf16>(maps, sh, ep, cap, s);
+  return run_gemm<64, false, true, false, 8, EpiScatterBf16>(maps, sh, ep, cap, s, "backup_rows_gemm");
 }
 
 // ------------------------------------------------------------------ dense backup, backward
@@ -152,10 +153,10 @@ cudaError_t gemm_backup_grad(const uint16_t* dY, const uint16_t* Wd, int rows_al
   fill_unused(maps, 1, 1);
   if (u != nullptr) {
     typename EpiBackupGrad<true>::Params ep{a, u, o.dG, o.dG_lo, o.dU, o.dU_lo, o.H, o.H_lo, l1, I, rows_alloc};
-    return run_gemm<64, false, false, false, 8, EpiBackupGrad<true>>(maps, sh, ep, cap, s);
+    return run_gemm<64, false, false, false, 8, EpiBackupGrad<true>>(maps, sh, ep, cap, s, "backup_grad");
   }
   typename EpiBackupGrad<false>::Params ep{a, nullptr, o.dG, o.dG_lo, nullptr, nullptr, o.H, o.H_lo, l1, I, rows_alloc};
-  return run_gemm<64, false, false, false, 8, EpiBackupGrad<false>>(maps, sh, ep, cap, s);
+  return run_gemm<64, false, false, false, 8, EpiBackupGrad<false>>(maps, sh, ep, cap, s, "backup_grad");
 }
 
 cudaError_t gemm_weight_grad_add(const uint16_t* P_hi, const uint16_t* P_lo, const uint16_t* Q, int rows_alloc,
@@ -173,8 +174,8 @@ cudaError_t gemm_weight_grad_add(const uint16_t* P_hi, const uint16_t* P_lo, con
   maps.b[1] = maps.b[0];
   fill_unused(maps, 2, 2);
   EpiAddF32::Params ep{D, d};
-  if (d % 256 == 0) return run_gemm<256, true, true, false, 4, EpiAddF32>(maps, sh, ep, I, s);
-  return run_gemm<64, true, true, false, 8, EpiAddF32>(maps, sh, ep, I, s);
+  if (d % 256 == 0) return run_gemm<256, true, true, false, 4, EpiAddF32>(maps, sh, ep, I, s, "backup_weight_grad");
+  return run_gemm<64, true, true, false, 8, EpiAddF32>(maps, sh, ep, I, s, "backup_weight_grad");
 }
 
 // ------------------------------------------------------------------ layout test GEMM
@@ -187,10 +188,10 @@ cudaError_t gemm_dense_test(const uint16_t* A, const uint16_t* B, int M, int N, 
   const bool okb = b_mn ? tmap_mnmajor(&maps.b[0], B, K, N) : tmap_kmajor(&maps.b[0], B, N, K, 64);
   if (!oka || !okb) return cudaErrorInvalidValue;
   fill_unused(maps, 1, 1);
-  if (!a_mn && !b_mn) return run_gemm<64, false, false, false, 8, EpiStoreF32>(maps, sh, ep, M, s);
-  if (!a_mn && b_mn) return run_gemm<64, false, true, false, 8, EpiStoreF32>(maps, sh, ep, M, s);
-  if (a_mn && !b_mn) return run_gemm<64, true, false, false, 8, EpiStoreF32>(maps, sh, ep, M, s);
-  return run_gemm<64, true, true, false, 8, EpiStoreF32>(maps, sh, ep, M, s);
+  if (!a_mn && !b_mn) return run_gemm<64, false, false, false, 8, EpiStoreF32>(maps, sh, ep, M, s, "dense_gemm");
+  if (!a_mn && b_mn) return run_gemm<64, false, true, false, 8, EpiStoreF32>(maps, sh, ep, M, s, "dense_gemm");
+  if (a_mn && !b_mn) return run_gemm<64, true, false, false, 8, EpiStoreF32>(maps, sh, ep, M, s, "dense_gemm");
+  return run_gemm<64, true, true, false, 8, EpiStoreF32>(maps, sh, ep, M, s, "dense_gemm");
 }
 
 }  // namespace tw

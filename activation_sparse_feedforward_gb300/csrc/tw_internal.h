@@ -13,6 +13,15 @@ namespace tw {
 
 int device_sm_count();
 
+// Timing trace (tw_trace_begin): records the next caller event on `s` after a launch.
+void trace_begin(void* const* events, int capacity);
+int trace_end();
+const char* trace_label(int i);
+void trace_mark(cudaStream_t s, const char* label);
+
+// cudaMemsetAsync followed by a trace mark
+cudaError_t memset_async(void* p, int v, size_t bytes, cudaStream_t s);
+
 // ---------------------------------------------------------------- tw_kernels.cu
 // Dense bf16 [T, I] -> TwELL counts/slots/row_nnz/ovf (not the overflow list).
 cudaError_t launch_pack_dense(const uint16_t* A, int T, int I, int W, int C, const tw_twell& o, cudaStream_t s);

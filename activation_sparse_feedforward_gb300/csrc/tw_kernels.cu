@@ -29,6 +29,45 @@ int device_sm_count() {
   return cached[dev];
 }
 
+// ---------------------------------------------------------------- timing trace
+namespace {
+constexpr int kTraceLabels = 16384;
+struct TraceState {
+  void* const* events = nullptr;
+  int cap = 0;
+  int n = 0;
+  bool on = false;
+  const char* labels[kTraceLabels];
+};
+TraceState g_trace;
+}  // namespace
+
+void trace_begin(void* const* events, int capacity) {
+  g_trace.events = events;
+  g_trace.cap = capacity;
+  g_trace.n = 0;
+  g_trace.on = events != nullptr && capacity > 0;
+}
+int trace_end() {
+  g_trace.on = false;
+  return g_trace.n;
+}
+const char* trace_label(int i) {
+  if (i < 0 || i >= g_trace.n || i >= kTraceLabels) return nullptr;
+  return g_trace.labels[i];
+}
+void trace_mark(cudaStream_t s, const char* label) {
+  if (!g_trace.on || g_trace.n >= g_trace.cap) return;
+  cudaEventRecord(static_cast<cudaEvent_t>(g_trace.events[g_trace.n]), s);
+  if (g_trace.n < kTraceLabels) g_trace.labels[g_trace.n] = label;
+  ++g_trace.n;
+}
+cudaError_t memset_async(void* p, int v, size_t bytes, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(p, v, bytes, s);
+  trace_mark(s, "memset");
+  return e;
+}
+
 static int warp_grid(long rows, int warps_per_block) {
   const long blocks = (rows + warps_per_block - 1) / warps_per_block;
   const long cap = static_cast<long>(device_sm_count()) * 32;
@@ -97,6 +136,7 @@ cudaError_t launch_pack_dense(const uint16_t* A, int T, int I, int W, int C, con
     pack_dense_kernel<4><<<grid, 256, 0, s>>>(A, T, I, C, nT, o.cnt, o.val, o.idx, o.row_nnz, o.ovf);
   else
     pack_dense_kernel<2><<<grid, 256, 0, s>>>(A, T, I, C, nT, o.cnt, o.val, o.idx, o.row_nnz, o.ovf);
+  trace_mark(s, "pack_dense");
   return cudaGetLastError();
 }
 
@@ -157,6 +197,7 @@ cudaError_t launch_compact_rows(const uint8_t* ovf, const int32_t* row_nnz, int 
                                 int32_t* status, cudaStream_t s) {
   compact_rows_kernel<<<1, 1024, 0, s>>>(ovf, row_nnz, R, T, list, list_cap, count, slot_of, ell_nnz, cap_check,
                                          status);
+  trace_mark(s, "compact_rows");
   return cudaGetLastError();
 }
 
@@ -186,6 +227,7 @@ cudaError_t launch_gather_rows(const uint16_t* src, int d, const int32_t* rows, 
   if (rows_alloc <= 0) return cudaSuccess;
   const int grid = warp_grid(rows_alloc, 8);
   gather_rows_kernel<<<std::min(grid, device_sm_count() * 4), 256, 0, s>>>(src, d, rows, n, cap, rows_alloc, out);
+  trace_mark(s, "gather_rows");
   return cudaGetLastError();
 }
 
@@ -313,6 +355,7 @@ static cudaError_t sparse_fwd_dispatch(const SparseFwdArgs& a, cudaStream_t s) {
 #undef TW_CASE
     default: return cudaErrorInvalidValue;
   }
+  trace_mark(s, "sparse_fwd");
   return cudaGetLastError();
 }
 
@@ -540,15 +583,20 @@ static cudaError_t sparse_bwd_dispatch(const SparseBwdArgs& a, cudaStream_t s) {
 #undef TW_CASE
     default: return cudaErrorInvalidValue;
   }
+  trace_mark(s, "sparse_bwd_token");
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(a.col_cnt, 0, sizeof(int32_t) * (a.I + 1), s);
+  e = memset_async(a.col_cnt, 0, sizeof(int32_t) * (a.I + 1), s);
   if (e != cudaSuccess) return e;
   csc_count_kernel<<<grid, 256, 0, s>>>(a.ell_nnz, a.ell_idx, a.T, a.R, a.col_cnt);
+  trace_mark(s, "csc_count");
   csc_scan_kernel<<<1, 1024, 0, s>>>(a.col_cnt, a.I, a.col_ptr, a.col_cur);
+  trace_mark(s, "csc_scan");
   csc_fill_kernel<<<grid, 256, 0, s>>>(a.ell_nnz, a.ell_idx, a.T, a.R, a.col_cur, a.csc);
+  trace_mark(s, "csc_fill");
   const int gw = std::min(a.I, device_sm_count() * 8);
   ell_weight_grad_kernel<GATED><<<gw, a.d / 8, 0, s>>>(a);
+  trace_mark(s, "ell_weight_grad");
   return cudaGetLastError();
 }
 

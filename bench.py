@@ -1,0 +1,460 @@
+"""Benchmark of the activation-sparse FFN hot path on one GB300 (or N replicas).
+
+A step is one Hybrid training step of one gated ReLU FFN layer through the
+library's C ABI: hybrid_ffn_fwd (gate GEMM + fused TwELL pack, Hybrid conversion,
+sparse up/down on the CUDA cores, dense backup on the tensor cores) followed by
+hybrid_ffn_bwd (sparse backward with L1 injection, transposed-Hybrid weight
+gradients, dense backup GEMMs). Inputs are seeded synthetic bf16 tensors of the
+pages' 1.5B-model FFN shape (see synthetic/workloads.py for the recipe).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline] [--sweep]
+
+Prints ONE JSON line (rank 0). Timing: W untimed warm-up steps, then K steps each
+bracketed by CUDA events on the launching stream with a 256 MiB L2 flush between
+steps (outside the events); barrier + synchronize around the timed region and the
+max over ranks. Per-kernel durations come from events the library records after
+each of its launches during the timed steps (tw_trace_begin).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sparse gated-FFN fwd+bwd input tokens/ms (d2048,I5632) and % of roofline"
+UNIT = "tokens/ms"
+DEFAULT_WORKLOAD = "train_d2048_i5632_m29_o1"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ distributed plumbing
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend: str):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, v: float, device) -> float:
+        if self.pg is None:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines: list[str] = []
+        self.target = self._nvsmi_index(device_index)
+
+    @staticmethod
+    def _nvsmi_index(device_index: int) -> str | None:
+        try:
+            import torch
+            p = torch.cuda.get_device_properties(device_index)
+            bus = getattr(p, "pci_bus_id", None)
+            dom = getattr(p, "pci_domain_id", 0)
+            dev = getattr(p, "pci_device_id", 0)
+            if bus is not None:
+                return f"{dom:08X}:{bus:02X}:{dev:02X}.0"
+        except Exception:
+            pass
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            return vis.split(",")[device_index]
+        return str(device_index)
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.target is not None:
+            cmd += ["-i", self.target]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ algorithmic work per kernel
+def kernel_work(label: str, spec, stats: dict) -> tuple[str, float] | None:
+    """(bound, algorithmic bytes or FLOPs) of one launch of a kernel, from the step's
+    measured active counts. Bytes count each tensor the kernel must read or write
+    once; weights are read once per launch."""
+    T, d, I, R = spec.T, spec.d, spec.I, spec.R
+    nT = I // spec.W
+    nnz_ell = stats["nnz_ell"]          # entries in ELL rows
+    nb = stats["n_backup"]
+    g = 2 if spec.gated else 1          # weight matrices gathered per entry in the forward
+    if label == "gate_pack":
+        return "tensor", 2.0 * T * d * I
+    if label == "sparse_fwd":
+        # x (gated) + y + TwELL counts + TwELL entries (val, idx) + ELL written (idx, a, u) + weights
+        b = (T * d * 2 if spec.gated else 0) + T * d * 2 + T * nT * 2 + nnz_ell * 3 + nnz_ell * 6 + g * I * d * 2
+        return "hbm", float(b)
+    if label == "sparse_bwd_token":
+        # dy + dx + ELL read (idx, a, u) + dg/du written + three weight matrices
+        return "hbm", float(2 * T * d * 2 + nnz_ell * 6 + nnz_ell * 8 + 3 * I * d * 2)
+    if label == "ell_weight_grad":
+        # x and dy read + dW written (fp32, 3 matrices) + csc, dg/du, a/u per entry
+        return "hbm", float(2 * T * d * 2 + 3 * I * d * 4 + nnz_ell * (4 + 8 + 4))
+    if label == "backup_hidden":
+        return "tensor", 2.0 * 2 * nb * d * I
+    if label == "backup_grad":
+        return "tensor", 2.0 * nb * d * I
+    if label == "backup_rows_gemm":
+        return "tensor", 2.0 * 2 * nb * I * d      # two K segments (hi, lo); the dx GEMM has four
+    if label == "backup_weight_grad":
+        return "tensor", 2.0 * 2 * nb * I * d
+    return None
+
+
+# ------------------------------------------------------------------ oracle timing (CPU)
+def oracle_sample_time(spec, inp, n_tokens: int) -> tuple[float, int, str]:
+    """Time the fp64 oracle (as it stands) over the whole hot path for a sample of
+    n_tokens tokens: dense forward, TwELL and Hybrid packing, dense backward."""
+    import numpy as np
+
+    from oracle import ffn, formats
+
+    rows = np.arange(n_tokens)
+    x, dy = inp["x"][rows], inp["dy"][rows]
+    t0 = time.perf_counter()
+    f = ffn.forward(x, inp["Wg"], inp["Wu"], inp["Wd"])
+    formats.twell_pack(f["a"], spec.W, spec.C)
+    formats.hybrid_pack(f["a"], f["u"], spec.W, spec.C, spec.R)
+    ffn.backward(x, inp["Wg"], inp["Wu"], inp["Wd"], dy, spec.l1, fwd=f)
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return dt, cores, f"first {n_tokens} tokens of {spec.name}, full weights, fp64 numpy (BLAS threads: all cores)"
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, dist: Dist) -> dict | None:
+    import numpy as np
+    import torch
+
+    import activation_sparse_feedforward_gb300 as tw
+    from synthetic import WORKLOADS, make_inputs
+
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    peaks = _peaks()
+    spec = WORKLOADS[args.workload].with_(seed=dist.rank)
+    inp = make_inputs(spec, with_dy=True)
+
+    def to_dev(b):
+        return None if b is None else torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    x, Wg, Wu, Wd, dy = (to_dev(inp[k]) for k in ("x", "Wg", "Wu", "Wd", "dy"))
+    backup_cap = min(spec.T, max(128, int(math.ceil(spec.outlier_frac * spec.T * 1.5 / 128.0)) * 128 + 128))
+    h = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, backup_cap, gated=spec.gated, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        h.forward(x, Wg, Wu, Wd)
+        h.backward(dy, x, Wg, Wu, Wd, spec.l1)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    tw.raise_if_device_error(h.status, "warm-up")
+    stats = {"n_backup": int(h.saved.n_backup.item()), "nnz_ell": int(h.saved.ell_nnz.sum().item()),
+             "nnz": int(h.saved.row_nnz[:spec.T].sum().item())}
+
+    # kernel trace events (materialised once so their handles exist)
+    per_step_cap = 64
+    tev = [torch.cuda.Event(enable_timing=True) for _ in range(per_step_cap * args.steps)]
+    for e in tev:
+        e.record(stream)
+    torch.cuda.synchronize(dev)
+    import ctypes
+    arr = (ctypes.c_void_p * len(tev))(*[e.cuda_event for e in tev])
+    L = tw.load()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(dist.local_rank)
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    _lib_check = L.tw_trace_begin(arr, len(tev))
+    assert _lib_check == 0
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    n_ev = L.tw_trace_end()
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    clk = clocks.stop()
+    tw.raise_if_device_error(h.status, "timed steps")
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = dist.max(sum(step_ms), dev)
+    ms_per_step = total_ms / args.steps
+    value = spec.T * dist.world * args.steps / total_ms
+
+    # per-kernel durations: event i ends launch i; the step's start event precedes launch 0
+    labels = [L.tw_trace_label(i).decode() for i in range(n_ev)]
+    if n_ev % args.steps != 0 or n_ev == len(tev):
+        raise RuntimeError(f"kernel trace incomplete: {n_ev} events for {args.steps} steps")
+    per_step = n_ev // args.steps
+    per_kernel: dict[str, list[float]] = {}
+    launches = 0
+    for i in range(args.steps):
+        prev = starts[i]
+        for k in range(i * per_step, (i + 1) * per_step):
+            per_kernel.setdefault(labels[k], []).append(prev.elapsed_time(tev[k]))
+            launches += labels[k] != "memset"
+            prev = tev[k]
+    kernels = {lab: {"launches": len(v), "total_ms": sum(v), "avg_us": 1e3 * sum(v) / len(v)}
+               for lab, v in per_kernel.items()}
+    total_k = sum(v["total_ms"] for v in kernels.values()) or 1.0
+    for v in kernels.values():
+        v["share"] = v["total_ms"] / total_k
+    dom = max((lab for lab in kernels if lab != "memset"), key=lambda lab: kernels[lab]["total_ms"])
+    bound, work = kernel_work(dom, spec, stats) or ("hbm", 0.0)
+    avg_s = kernels[dom]["avg_us"] * 1e-6
+    if bound == "tensor":
+        achieved = work / avg_s / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        unit = "TFLOP/s"
+    else:
+        achieved = work / avg_s / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": None,
+                "peak_source": f"{peaks['source']} ({'bf16 sustained' if bound == 'tensor' else 'HBM copy'})"}
+    for lab, v in kernels.items():
+        kw = kernel_work(lab, spec, stats)
+        if kw:
+            b, w = kw
+            v["bound"] = b
+            v["achieved"] = (w / (v["avg_us"] * 1e-6)) / (1e12 if b == "tensor" else 1e9)
+
+    # step roofline: slower of (gate + backup + sparse FLOPs at tensor peak) and
+    # (algorithmic bytes at HBM peak)
+    F = 2.0 * spec.T * spec.d * spec.I + 14.0 * spec.d * spec.I * stats["n_backup"] + 16.0 * spec.d * stats["nnz_ell"]
+    B = (3 * spec.T * spec.d * 2 + 2 * spec.T * spec.d * 2 + 2 * 3 * spec.I * spec.d * 2 + 3 * spec.I * spec.d * 4
+         + stats["nnz_ell"] * (6 + 6 + 8 + 4))
+    t_roof = max(F / (peaks["bf16_tflops_sustained"] * 1e12), B / (peaks["hbm_gbs"] * 1e9))
+    step_roof = {"tokens_per_ms": spec.T / (t_roof * 1e3), "frac": (spec.T / ms_per_step) / (spec.T / (t_roof * 1e3)),
+                 "flops": F, "bytes": B}
+
+    # end to end through the public API with host buffers (pinned), per step:
+    # H2D of x and dy, the step, D2H of y and dx
+    hx = x.cpu().pin_memory()
+    hdy = dy.cpu().pin_memory()
+    hy = torch.empty_like(hx).pin_memory()
+    hdx = torch.empty_like(hx).pin_memory()
+    xd = torch.empty_like(x)
+    dyd = torch.empty_like(dy)
+
+    def e2e_step():
+        xd.copy_(hx, non_blocking=True)
+        dyd.copy_(hdy, non_blocking=True)
+        h.forward(xd, Wg, Wu, Wd)
+        h.backward(dyd, xd, Wg, Wu, Wd, spec.l1)
+        hy.copy_(h.y, non_blocking=True)
+        hdx.copy_(h.dx, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    e_s.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e_e.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = dist.max(e_s.elapsed_time(e_e), dev)
+    e2e = {"value": spec.T * dist.world * args.steps / e2e_ms, "unit": UNIT,
+           "h2d_bytes_per_step": int(hx.numel() * 2 + hdy.numel() * 2),
+           "d2h_bytes_per_step": int(hy.numel() * 2 + hdx.numel() * 2)}
+
+    # dense bf16 FFN (torch/cuBLAS) forward + backward with the same L1 term, same run
+    dense = None
+    if not args.no_dense:
+        Wg_, Wu_, Wd_ = (w.detach().clone().requires_grad_(True) for w in (Wg, Wu, Wd))
+        x_ = x.detach().clone().requires_grad_(True)
+
+        def dense_step():
+            g = x_ @ Wg_.T
+            a = torch.relu(g)
+            yy = (a * (x_ @ Wu_.T)) @ Wd_
+            loss_like = yy
+            torch.autograd.backward([loss_like, a], [dy, torch.full_like(a, spec.l1)])
+            x_.grad = Wg_.grad = Wu_.grad = Wd_.grad = None
+
+        for _ in range(2):
+            dense_step()
+        torch.cuda.synchronize(dev)
+        ds, de = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ds.record(stream)
+        for _ in range(max(3, args.steps // 2)):
+            dense_step()
+        de.record(stream)
+        torch.cuda.synchronize(dev)
+        dense = {"value": spec.T * max(3, args.steps // 2) / ds.elapsed_time(de), "unit": UNIT,
+                 "impl": "torch bf16 matmul + autograd (cuBLAS)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": spec.name, "tokens": spec.T, "d": spec.d, "I": spec.I, "gated": spec.gated,
+                   "mean_active": spec.mean_active, "outlier_frac": spec.outlier_frac, "W": spec.W, "C": spec.C,
+                   "R": spec.R, "backup_cap": backup_cap, "l1": spec.l1,
+                   "step": "hybrid_ffn_fwd + hybrid_ffn_bwd", "l2": "256 MiB flush between steps (untimed)",
+                   "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "single GPU"},
+        "measured": {"nnz_per_token": stats["nnz"] / spec.T, "nnz_ell": stats["nnz_ell"],
+                     "n_backup": stats["n_backup"]},
+        "roofline": roofline,
+        "step_roofline": step_roof,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "kernels": {k_: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
+                    for k_, v in sorted(kernels.items(), key=lambda kv: -kv[1]["total_ms"])},
+        "clocks": clk,
+        "dense_bf16": dense,
+    }
+    if dist.rank == 0 and not args.no_cpu_baseline:
+        n_s = args.cpu_sample_tokens
+        dt, cores, sample = oracle_sample_time(spec, inp, n_s)
+        line["cpu_baseline"] = {"value": n_s / (dt * 1e3), "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": sample, "seconds": dt}
+    return line
+
+
+# ------------------------------------------------------------------ reference arm (the oracle)
+def run_reference(args, dist: Dist) -> dict | None:
+    if dist.rank != 0:
+        return None
+    from synthetic import WORKLOADS, make_inputs
+
+    spec = WORKLOADS[args.workload]
+    inp = make_inputs(spec, with_dy=True)
+    n_s = args.reference_sample_tokens
+    for _ in range(args.warmup):
+        oracle_sample_time(spec, inp, min(n_s, 64))
+    times = []
+    for _ in range(args.steps):
+        dt, cores, sample = oracle_sample_time(spec, inp, n_s)
+        times.append(dt)
+    total = sum(times)
+    value = n_s * args.steps / (total * 1e3)
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": spec.name, "tokens_per_step": n_s},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=2048)
+    ap.add_argument("--reference-sample-tokens", type=int, default=256)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    dist = Dist()
+    if args.impl == "reference":
+        line = run_reference(args, dist)
+    else:
+        import torch
+        dist.init("nccl" if torch.cuda.is_available() else "gloo")
+        line = run_ours(args, dist)
+        dist.close()
+    if line is not None and dist.rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -185,6 +185,19 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
 tw_status tw_dense_gemm(const uint16_t* A, const uint16_t* B, int M, int N, int K,
                         int a_mn, int b_mn, float* D, int32_t* dev_status, void* stream);
 
+/* Kernel-level timing hook for measurement tools (no counterpart on the pages).
+ * While a trace is active, every kernel or memset the library enqueues is followed
+ * by cudaEventRecord(events[i], stream) with the next caller-created event, and its
+ * label is kept; the time between consecutive events (the first measured from an
+ * event the caller records just before the call) is that launch's device duration.
+ * Recording stops silently when `capacity` events are used. Process-wide state, not
+ * thread-safe: trace one host thread at a time. tw_trace_end() stops tracing and
+ * returns the number of events recorded; tw_trace_label(i) names event i (a static
+ * string; "memset" for cudaMemsetAsync calls), or NULL when i is out of range. */
+tw_status tw_trace_begin(void* const* events, int capacity);
+int tw_trace_end(void);
+const char* tw_trace_label(int i);
+
 #ifdef __cplusplus
 }
 #endif
