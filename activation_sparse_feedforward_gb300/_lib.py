@@ -43,6 +43,8 @@ SIGNATURES = {
     "twell_ffn_fwd_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int, c_int]),
     "twell_ffn_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int,
                               ctypes.POINTER(TwTwell), c_void_p, c_size_t, c_void_p, c_void_p, c_void_p]),
+    "twell_ffn_fwd_fixed_scratch": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
+                                            c_int, c_int, ctypes.POINTER(TwTwell), c_void_p, c_void_p, c_void_p]),
     "hybrid_ffn_fwd_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int, c_int, c_int]),
     "hybrid_ffn_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
                                ctypes.POINTER(TwHybrid), c_void_p, c_size_t, c_void_p, c_void_p, c_void_p]),

@@ -147,6 +147,29 @@ tw_status twell_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* W
                         int ovf_cap, const tw_twell* tw, void* ws, size_t ws_bytes,
                         uint16_t* y, int32_t* dev_status, void* stream);
 
+/* twell_ffn_fwd for callers that cannot allocate device memory (the pages have no
+ * counterpart of this call). Some callers own only their inputs and outputs: a
+ * plugin that a host framework hands I/O pointers but no workspace, or a serving
+ * loop where cudaMalloc is off limits because it can synchronise the device and
+ * stall for milliseconds. This call computes exactly what twell_ffn_fwd computes,
+ * with the same arguments minus the workspace: the overflow path's scratch comes
+ * from one fixed 16 MiB array in device memory that the library defines.
+ *  - Limit: returns TW_EWORKSPACE (before enqueuing anything) when
+ *    twell_ffn_fwd_workspace_size(T, d, I, W, C, ovf_cap) exceeds 16 MiB; at
+ *    d = 2048, I = 5632 that allows ovf_cap up to 512 overflow rows.
+ *  - The array occupies 16 MiB on every GPU where the library's code is loaded,
+ *    until the process exits.
+ *  - The first call on each device looks up the array's device address (with that
+ *    device current); make that first call before any stream capture.
+ *  - All calls share the one array and it keeps the previous call's contents;
+ *    nothing in it needs to start at zero. Calls whose GPU work overlaps (on
+ *    unordered streams) race on it: order them on one stream.
+ *  - Allocates and frees nothing. */
+tw_status twell_ffn_fwd_fixed_scratch(const uint16_t* x, const uint16_t* Wg, const uint16_t* Wu,
+                                      const uint16_t* Wd, int T, int d, int I, int W, int C,
+                                      int ovf_cap, const tw_twell* tw, uint16_t* y,
+                                      int32_t* dev_status, void* stream);
+
 /* Workspace bytes hybrid_ffn_fwd needs. */
 size_t hybrid_ffn_fwd_workspace_size(int T, int d, int I, int W, int C, int R, int backup_cap);
 
