@@ -46,6 +46,7 @@ tw_status check_tile_geometry(int T, int I, int W, int C) {
   if (W != 64 && W != 128) return TW_EUNSUPPORTED;
   if (I < 64 || I > 65536 || I % W != 0) return TW_EUNSUPPORTED;
   if (C < 1 || C > W) return TW_EINVAL;
+  if ((I / W) * C > 12288) return TW_EUNSUPPORTED;  // per-warp entry list of the sparse forward
   return TW_OK;
 }
 
@@ -119,6 +120,7 @@ struct HybFwdWs {
   uint16_t* X;
   uint16_t* H;
   uint16_t* H_lo;
+  float* acc;  // split-K accumulator of the down projection [ra, d]
 };
 HybFwdWs carve_hybrid_fwd(Carve& c, int T, int d, int I, int W, int C, int backup_cap) {
   const size_t nT = static_cast<size_t>(I / W);
@@ -133,6 +135,7 @@ HybFwdWs carve_hybrid_fwd(Carve& c, int T, int d, int I, int W, int C, int backu
   w.X = c.take<uint16_t>(static_cast<size_t>(ra) * d);
   w.H = c.take<uint16_t>(static_cast<size_t>(ra) * I);
   w.H_lo = c.take<uint16_t>(static_cast<size_t>(ra) * I);
+  w.acc = c.take<float>(static_cast<size_t>(ra) * d);
   return w;
 }
 
@@ -146,6 +149,7 @@ struct HybBwdWs {
   uint16_t* dY;
   uint16_t* X;
   tw::BackupGradOut g;  // dG, dU, H as (hi, lo) bf16 pairs
+  float* acc;           // split-K accumulator of dx for the backup rows [ra, d]
 };
 HybBwdWs carve_hybrid_bwd(Carve& c, int T, int d, int I, int R, int backup_cap) {
   const size_t TR = static_cast<size_t>(T) * R;
@@ -166,6 +170,7 @@ HybBwdWs carve_hybrid_bwd(Carve& c, int T, int d, int I, int R, int backup_cap) 
   w.g.dU_lo = c.take<uint16_t>(rI);
   w.g.H = c.take<uint16_t>(rI);
   w.g.H_lo = c.take<uint16_t>(rI);
+  w.acc = c.take<float>(static_cast<size_t>(ra) * d);
   return w;
 }
 
@@ -276,11 +281,11 @@ tw_status twell_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* W
   if (st != TW_OK) return st;
   tw::SparseFwdArgs a{};
   a.x = x; a.Wu = Wu; a.Wd = Wd;
-  a.T = T; a.d = d; a.I = I; a.W = W; a.C = C; a.nT = I / W;
+  a.T = T; a.d = d; a.I = I; a.W = W; a.C = C; a.nT = I / W; a.L = (I / W) * C;
   a.cnt = o.cnt; a.val = o.val; a.idx = o.idx; a.ovf = o.ovf;
   a.backup_slot = nullptr;
   a.y = y;
-  TW_TRY(tw::launch_sparse_fwd(a, s));
+  TW_TRY(tw::launch_sparse_fwd(a, dev_status, s));
   if (ovf_cap > 0) {
     TW_TRY(tw::launch_gather_rows(x, d, o.ovf_rows, o.n_ovf, ovf_cap, ra, w.X, s));
     TW_TRY(tw::gemm_backup_hidden(w.X, Wg, Wu, ra, o.n_ovf, ovf_cap, d, I, w.H, w.H_lo, nullptr, nullptr,
@@ -328,20 +333,20 @@ tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* 
                                  saved->backup_slot, saved->ell_nnz, cap, dev_status, s));
   tw::SparseFwdArgs a{};
   a.x = x; a.Wu = Wu; a.Wd = Wd;
-  a.T = T; a.d = d; a.I = I; a.W = W; a.C = C; a.nT = I / W;
+  a.T = T; a.d = d; a.I = I; a.W = W; a.C = C; a.nT = I / W; a.L = (I / W) * C;
   a.cnt = o.cnt; a.val = o.val; a.idx = o.idx; a.ovf = o.ovf;
   a.backup_slot = saved->backup_slot;
   a.ell_idx = saved->ell_idx; a.ell_a = saved->ell_a; a.ell_u = saved->ell_u; a.R = R;
   a.y = y;
-  TW_TRY(tw::launch_sparse_fwd(a, s));
+  TW_TRY(tw::launch_sparse_fwd(a, dev_status, s));
   if (cap > 0) {
     TW_TRY(tw::launch_gather_rows(x, d, saved->backup_tok, saved->n_backup, cap, ra, w.X, s));
     TW_TRY(tw::gemm_backup_hidden(w.X, Wg, Wu, ra, saved->n_backup, cap, d, I, w.H, w.H_lo, saved->backup_a,
                                   gated ? saved->backup_u : nullptr, dev_status, s));
     const uint16_t* A[2] = {w.H, w.H_lo};
     const uint16_t* B[2] = {Wd, Wd};
-    TW_TRY(tw::gemm_rows_times_nmajor(A, B, 2, ra, saved->n_backup, cap, I, d, y, d, saved->backup_tok, dev_status,
-                                      s));
+    TW_TRY(tw::gemm_rows_times_nmajor_splitk(A, B, 2, ra, saved->n_backup, cap, I, d, w.acc, dev_status, s));
+    TW_TRY(tw::launch_scatter_rows_bf16(w.acc, d, saved->n_backup, cap, saved->backup_tok, y, d, s));
   }
   return TW_OK;
 }
@@ -388,7 +393,7 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
   a.dg = w.dg; a.du = w.du; a.dx = dx;
   a.col_cnt = w.col_cnt; a.col_ptr = w.col_ptr; a.col_cur = w.col_cur; a.csc = w.csc;
   a.dWg = dWg; a.dWu = dWu; a.dWd = dWd;
-  TW_TRY(tw::launch_sparse_bwd(a, s));
+  TW_TRY(tw::launch_sparse_bwd(a, dev_status, s));
   if (cap > 0 && T > 0) {
     TW_TRY(tw::launch_gather_rows(dy, d, saved->backup_tok, saved->n_backup, cap, ra, w.dY, s));
     TW_TRY(tw::launch_gather_rows(x, d, saved->backup_tok, saved->n_backup, cap, ra, w.X, s));
@@ -399,8 +404,8 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
     // dx = (dG + dG_lo) Wg + (dU + dU_lo) Wu, scattered back to the backup tokens
     const uint16_t* A[4] = {g.dG, g.dG_lo, g.dU, g.dU_lo};
     const uint16_t* B[4] = {Wg, Wg, Wu, Wu};
-    TW_TRY(tw::gemm_rows_times_nmajor(A, B, gated ? 4 : 2, ra, nb, cap, I, d, dx, d, saved->backup_tok, dev_status,
-                                      s));
+    TW_TRY(tw::gemm_rows_times_nmajor_splitk(A, B, gated ? 4 : 2, ra, nb, cap, I, d, w.acc, dev_status, s));
+    TW_TRY(tw::launch_scatter_rows_bf16(w.acc, d, nb, cap, saved->backup_tok, dx, d, s));
     TW_TRY(tw::gemm_weight_grad_add(g.dG, g.dG_lo, w.X, ra, nb, cap, I, d, dWg, dev_status, s));
     if (gated) TW_TRY(tw::gemm_weight_grad_add(g.dU, g.dU_lo, w.X, ra, nb, cap, I, d, dWu, dev_status, s));
     TW_TRY(tw::gemm_weight_grad_add(g.H, g.H_lo, w.dY, ra, nb, cap, I, d, dWd, dev_status, s));

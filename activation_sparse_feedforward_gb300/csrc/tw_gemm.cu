@@ -139,6 +139,36 @@ cudaError_t gemm_rows_times_nmajor(const uint16_t* const* A, const uint16_t* con
   return run_gemm<64, false, true, false, 8, EpiScatterBf16>(maps, sh, ep, cap, s, "backup_rows_gemm");
 }
 
+// Same product for few rows, spread over every SM: 256-wide column tiles, each tile's
+// K loop (all segments) cut into slices whose partial sums are added into the fp32
+// accumulator acc [cap, N] (zeroed here); launch_scatter_rows_bf16 then writes the
+// bf16 rows out.
+cudaError_t gemm_rows_times_nmajor_splitk(const uint16_t* const* A, const uint16_t* const* B, int segments,
+                                          int rows_alloc, const int32_t* n_dev, int cap, int K, int N, float* acc,
+                                          int32_t* status, cudaStream_t s) {
+  if (cap <= 0) return cudaSuccess;
+  if (segments < 1 || segments > GEMM_MAX_SEGMENTS || N % 256 != 0) return cudaErrorInvalidValue;
+  cudaError_t e = memset_async(acc, 0, sizeof(float) * static_cast<size_t>(cap) * N, s);
+  if (e != cudaSuccess) return e;
+  GemmShape sh = shape_static(0, N, K, status);
+  sh.m_dev = n_dev;
+  sh.m_cap = cap;
+  sh.segments = segments;
+  const int tiles = ((cap + GEMM_BM - 1) / GEMM_BM) * (N / 256);
+  const int kb_total = ((K + GEMM_BK - 1) / GEMM_BK) * segments;
+  sh.ksplit = std::max(1, std::min(kb_total, (2 * device_sm_count() + tiles - 1) / tiles));
+  GemmMaps maps;
+  for (int i = 0; i < segments; ++i)
+    if (!tmap_kmajor(&maps.a[i], A[i], rows_alloc, K, 128) || !tmap_mnmajor(&maps.b[i], B[i], K, N))
+      return cudaErrorInvalidValue;
+  fill_unused(maps, segments, segments);
+  EpiRedF32::Params ep{acc, N};
+  const int units = tiles * sh.ksplit;
+  // rows of work units instead of rows of D: run_gemm sizes the grid from max_rows
+  return run_gemm<256, false, true, false, 4, EpiRedF32>(maps, sh, ep, units * GEMM_BM / (N / 256), s,
+                                                          "backup_rows_gemm");
+}
+
 // ------------------------------------------------------------------ dense backup, backward
 cudaError_t gemm_backup_grad(const uint16_t* dY, const uint16_t* Wd, int rows_alloc, const int32_t* n_dev, int cap,
                              int d, int I, const float* a, const float* u, float l1, const BackupGradOut& o,

@@ -37,6 +37,8 @@ struct GemmShape {
   const int* k_dev;  // optional device K, clamped to [0, k_cap]; memory past K must read as zero
   int k_cap;
   int segments;      // 1 to 4 (A, B) pairs
+  int ksplit;        // >= 1: each output tile's K loop is cut into ksplit work units
+                     // (only for epilogues that accumulate, e.g. EpiRedF32)
   int32_t* status;
 };
 
@@ -65,16 +67,6 @@ struct GemmTraits {
   static_assert((2 * STAGES + 4) * 8 + 8 <= BAR_BYTES, "barrier area");
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
-
-// Bounded wait used only while draining after an abort: ignores the abort flag.
-TW_DEV bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
-  const uint32_t addr = smem_addr(bar);
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(addr, parity)) {
-    if (global_timer_ns() - t0 > TW_WAIT_LIMIT_NS) return false;
-  }
-  return true;
-}
 
 template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES, class Epi>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
@@ -131,6 +123,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const int num_tiles = (K > 0) ? m_tiles * n_tiles : 0;
   const int kb_per_seg = (K + GEMM_BK - 1) / GEMM_BK;
   const int kb_total = kb_per_seg * shape.segments;
+  // work unit = (output tile, slice of its K loop); empty slices are skipped by
+  // every role alike
+  const int ksplit = max(1, shape.ksplit);
+  const int kb_chunk = (kb_total + ksplit - 1) / ksplit;
+  const int num_units = num_tiles * ksplit;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -139,10 +136,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       uint32_t phase = 0;
       long issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      for (int unit = blockIdx.x; ok && unit < num_units; unit += gridDim.x) {
+        const int tile = unit / ksplit;
+        const int kb_lo = (unit - tile * ksplit) * kb_chunk;
+        const int kb_hi = min(kb_total, kb_lo + kb_chunk);
+        if (kb_lo >= kb_hi) continue;
         const int m0 = (tile / n_tiles) * GEMM_BM;
         const int n0 = (tile % n_tiles) * BN;
-        for (int kb = 0; kb < kb_total; ++kb) {
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, shape.status)) {
             ok = false;
             break;
@@ -194,16 +195,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       int local = 0;
       bool ok = true;
       bool issued_any = false;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
+      for (int unit = blockIdx.x; ok && unit < num_units; unit += gridDim.x) {
+        const int tile = unit / ksplit;
+        const int kb_lo = (unit - tile * ksplit) * kb_chunk;
+        const int kb_hi = min(kb_total, kb_lo + kb_chunk);
+        if (kb_lo >= kb_hi) continue;
         const int buf = local & 1;
         const uint32_t use = static_cast<uint32_t>(local >> 1);
+        ++local;
         if (!mbar_wait(tempty + buf, (use & 1u) ^ 1u, abort_flag, shape.status)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(buf * Tr::ACC_COLS);
-        for (int kb = 0; kb < kb_total; ++kb) {
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait(full + stage, phase, abort_flag, shape.status)) {
             ok = false;
             break;
@@ -215,7 +221,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           for (int k16 = 0; k16 < GEMM_BK / 16; ++k16) {
             const uint64_t ad = A_MN ? smem_desc_sw128(a_base + k16 * 2048, 8192, 1024)
                                      : smem_desc_sw128(a_base + k16 * 32, 16, 1024);
-            const uint32_t acc = (kb > 0 || k16 > 0) ? 1u : 0u;
+            const uint32_t acc = (kb > kb_lo || k16 > 0) ? 1u : 0u;
 #pragma unroll
             for (int nb = 0; nb < Tr::NB; ++nb) {
               const uint32_t bb = b_base + nb * Tr::B_BYTES;
@@ -247,9 +253,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
     const int row = quarter * 32 + lane;
     int local = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+    for (int unit = blockIdx.x; unit < num_units; unit += gridDim.x) {
+      const int tile = unit / ksplit;
+      const int kb_lo = (unit - tile * ksplit) * kb_chunk;
+      if (kb_lo >= min(kb_total, kb_lo + kb_chunk)) continue;
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
+      ++local;
       int ok = 0;
       if (lane == 0) ok = mbar_wait(tfull + buf, use & 1u, abort_flag, shape.status) ? 1 : 0;
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -328,6 +338,27 @@ struct EpiAddF32 {
       o.w += __uint_as_float(v[4 * i + 3]);
       dst[i] = o;
     }
+  }
+  TW_DEV void finish() {}
+};
+
+// acc[m][n] += D with fp32 vector atomics: one K slice of a split-K product (acc is
+// zeroed beforehand, and every slice of the tile adds its part).
+struct EpiRedF32 {
+  struct Params {
+    float* acc;
+    int ld;
+  };
+  const Params& p;
+  int m, M, n0;
+  TW_DEV EpiRedF32(const Params& p_, int m_, int M_, int n0_) : p(p_), m(m_), M(M_), n0(n0_) {}
+  TW_DEV void chunk(int c, const uint32_t (&v)[32], const uint32_t (&)[32]) {
+    if (m >= M) return;
+    float4* dst = reinterpret_cast<float4*>(p.acc + static_cast<size_t>(m) * p.ld + n0 + c * 32);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      atomicAdd(dst + i, make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                     __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
   }
   TW_DEV void finish() {}
 };

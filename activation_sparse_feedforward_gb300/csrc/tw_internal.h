@@ -52,9 +52,10 @@ struct SparseFwdArgs {
   uint16_t* ell_a;
   uint16_t* ell_u;
   int R;
+  int L;                          // per-warp entry list capacity: nT * C (<= 12288)
   uint16_t* y;
 };
-cudaError_t launch_sparse_fwd(const SparseFwdArgs& a, cudaStream_t s);
+cudaError_t launch_sparse_fwd(const SparseFwdArgs& a, int32_t* status, cudaStream_t s);
 
 struct SparseBwdArgs {
   const uint16_t *dy, *x, *Wg, *Wu, *Wd;
@@ -75,9 +76,10 @@ struct SparseBwdArgs {
   int32_t* csc;       // [T * R]
   float *dWg, *dWu, *dWd;
 };
-// Per-token ELL backward (dh, du, dg, dx) + transposed Hybrid + ELL weight gradients
-// (dW overwritten; the dense backup part is added afterwards).
-cudaError_t launch_sparse_bwd(const SparseBwdArgs& a, cudaStream_t s);
+// ELL backward: dh pass (dg, du per entry, column counts), transposed Hybrid, dx
+// pass, weight-gradient pass (dW overwritten; the dense backup part is added
+// afterwards). col_cnt is zeroed here.
+cudaError_t launch_sparse_bwd(const SparseBwdArgs& a, int32_t* status, cudaStream_t s);
 
 // ---------------------------------------------------------------- tw_gemm.cu
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
@@ -98,6 +100,15 @@ cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint
 cudaError_t gemm_rows_times_nmajor(const uint16_t* const* A, const uint16_t* const* B, int segments, int rows_alloc,
                                    const int32_t* n_dev, int cap, int K, int N, uint16_t* out, int ldo,
                                    const int32_t* row_map, int32_t* status, cudaStream_t s);
+
+// The same product spread over every SM with split K: partial sums are added into
+// the fp32 accumulator acc [cap, N] (zeroed first); launch_scatter_rows_bf16 writes
+// the finished rows.
+cudaError_t gemm_rows_times_nmajor_splitk(const uint16_t* const* A, const uint16_t* const* B, int segments,
+                                          int rows_alloc, const int32_t* n_dev, int cap, int K, int N, float* acc,
+                                          int32_t* status, cudaStream_t s);
+cudaError_t launch_scatter_rows_bf16(const float* acc, int N, const int32_t* n_dev, int cap, const int32_t* row_map,
+                                     uint16_t* out, int ldo, cudaStream_t s);
 
 // dense backup backward part 1: dh = dY Wd^T and the epilogue producing dG, dU and H,
 // each as a (hi, lo) bf16 pair [rows_alloc, I].

@@ -1,0 +1,613 @@
+// CUDA-core kernels of the sparse part of the FFN (gist.science explainer, 2.B:
+// "Fused Up/Down Projection" for inference, "Sparse MatMul" and "Backpropagation"
+// for training), organised for GB300's memory system.
+//
+// Every stored entry (t, j) costs whole d-vector gathers of weight rows (Wu[j],
+// Wd[j], Wg[j]) or token rows (x_t, dy_t). They are served from the 129 MB L2, which
+// delivers ~20 TB/s of random-row gathers only when every SM keeps ~30 rows (4 KB
+// each) in flight all the time. Register-resident accumulators (x_t, y_t, dx_t) leave
+// no room for that many rows in registers, so the row passes stream weight rows
+// through a small per-warp shared-memory ring filled by bulk copies (cp.async.bulk)
+// that lane 0 issues a few rows ahead:
+//
+//  forward   warp per token: enumerate the token's TwELL entries into a shared-memory
+//            list (j, a); stream Wu[j] rows: u = x_t . Wu[j], h = a u (gated); then
+//            stream Wd[j] rows: y_t = sum h Wd[j]                 (x_t, then y_t, in registers)
+//  dh        warp per ELL token: stream Wd[j]: dh = dy_t . Wd[j];
+//            dg = dh u + l1 (non-gated: dh + l1), du = dh a; counts the columns of
+//            the transposed Hybrid                                 (dy_t in registers)
+//  dx        warp per ELL token: stream Wg[j], Wu[j]: dx_t = sum dg Wg[j] + du Wu[j]
+//  dW        warp per (256-wide slice of d, neuron j) over the transposed Hybrid:
+//            dWg[j] = sum dg x_t, dWu[j] = sum du x_t, dWd[j] = sum a u dy_t;
+//            slices outermost so the x / dy slices in use stay in L2, and the fp32
+//            gradient rows are written with streaming stores that do not evict them.
+//
+// Lane l of a warp owns elements [256 q + 8 l, 256 q + 8 l + 8) of each 256-wide
+// chunk q of a d-vector, so every shared-memory row read is conflict-free and every
+// direct global read is a coalesced 512-byte transaction.
+#include <algorithm>
+
+#include "tw_common.cuh"
+#include "tw_internal.h"
+
+namespace tw {
+
+namespace {
+
+constexpr int kFwdRing = 2;   // row slots per warp
+constexpr int kDhRing = 3;
+constexpr int kDxRing = 3;
+constexpr int kWgradUnroll = 8;
+
+TW_DEV void axpy8(float (&y)[8], float h, const uint4& w) {
+  y[0] = fmaf(h, bf16_lo(w.x), y[0]);
+  y[1] = fmaf(h, bf16_hi(w.x), y[1]);
+  y[2] = fmaf(h, bf16_lo(w.y), y[2]);
+  y[3] = fmaf(h, bf16_hi(w.y), y[3]);
+  y[4] = fmaf(h, bf16_lo(w.z), y[4]);
+  y[5] = fmaf(h, bf16_hi(w.z), y[5]);
+  y[6] = fmaf(h, bf16_lo(w.w), y[6]);
+  y[7] = fmaf(h, bf16_hi(w.w), y[7]);
+}
+TW_DEV uint4 pack8(const float (&y)[8]) {
+  return make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                    pack_bf16x2(y[6], y[7]));
+}
+TW_DEV uint4 ldg16(const uint4* p) { return __ldg(p); }
+// dot product of a lane's NCH chunks with a row in shared memory, four independent
+// partial sums (a single chain would serialise 8 * NCH dependent FMAs)
+template <int NCH>
+TW_DEV float dot_row(const uint4 (&xv)[NCH], const uint4* row, int lane) {
+  float p[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int q = 0; q < NCH; ++q) {
+    const uint4 w = row[q * 32 + lane];
+    const uint4& x = xv[q];
+    p[0] = fmaf(bf16_lo(x.x), bf16_lo(w.x), p[0]);
+    p[1] = fmaf(bf16_hi(x.x), bf16_hi(w.x), p[1]);
+    p[2] = fmaf(bf16_lo(x.y), bf16_lo(w.y), p[2]);
+    p[3] = fmaf(bf16_hi(x.y), bf16_hi(w.y), p[3]);
+    p[0] = fmaf(bf16_lo(x.z), bf16_lo(w.z), p[0]);
+    p[1] = fmaf(bf16_hi(x.z), bf16_hi(w.z), p[1]);
+    p[2] = fmaf(bf16_lo(x.w), bf16_lo(w.w), p[2]);
+    p[3] = fmaf(bf16_hi(x.w), bf16_hi(w.w), p[3]);
+  }
+  return (p[0] + p[1]) + (p[2] + p[3]);
+}
+TW_DEV void stcs_f32x8(float* p, const float (&v)[8]) {
+  __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
+  __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(v[4], v[5], v[6], v[7]));
+}
+
+int grid_for(long items, int per_block, int blocks_per_sm) {
+  const long blocks = (items + per_block - 1) / per_block;
+  return static_cast<int>(
+      std::max<long>(1, std::min<long>(blocks, static_cast<long>(device_sm_count()) * blocks_per_sm)));
+}
+
+__host__ __device__ constexpr uint32_t round_up_u(uint32_t v, uint32_t m) { return (v + m - 1) / m * m; }
+
+// shared memory of one forward warp: ring | neuron list (u16) | h list (f32)
+__host__ __device__ inline uint32_t fwd_warp_smem(int nch, int L) {
+  return round_up_u(kFwdRing * nch * 512u + round_up_u(2u * L, 16u) + 4u * L, 128u);
+}
+
+}  // namespace
+
+// ====================================================================== forward
+// Rows served by the dense path (TwELL overflow, Hybrid backup) are skipped. The
+// token's entries come from the TwELL counts tile by tile (ballot over tiles with a
+// nonzero count; the first cnt lanes take the tile's slots), i.e. in ascending
+// neuron order, into the warp's list; in training they also go to the Hybrid ELL.
+// The warp's row stream is then Wu[j_0..j_n-1] (gated only) followed by
+// Wd[j_0..j_n-1]. The list holds up to a.L = (I / W) * C entries, the most a
+// non-overflow row has.
+template <int NCH, bool GATED, bool HYBRID>
+__global__ void __launch_bounds__(256) sparse_fwd_kernel(const SparseFwdArgs a, int32_t* status) {
+  constexpr int S = kFwdRing;
+  constexpr uint32_t ROWB = NCH * 512;
+  constexpr int d = NCH * 256;
+  extern __shared__ __align__(128) uint8_t fwd_smem[];
+  __shared__ uint64_t bars[8 * S];
+  __shared__ int abort_flag;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int wpb = blockDim.x >> 5;
+  uint8_t* wbase = fwd_smem + static_cast<size_t>(warp) * fwd_warp_smem(NCH, a.L);
+  WarpRing<S> ring{wbase, bars + warp * S, ROWB};
+  uint16_t* lj = reinterpret_cast<uint16_t*>(wbase + S * ROWB);
+  float* lh = reinterpret_cast<float*>(wbase + S * ROWB + round_up_u(2u * a.L, 16u));
+  if (threadIdx.x == 0) abort_flag = 0;
+  __syncthreads();
+  ring.init(lane);
+
+  uint32_t g = 0;  // rows of this warp's stream consumed so far
+  for (int t = blockIdx.x * wpb + warp; t < a.T; t += gridDim.x * wpb) {
+    const bool skip = HYBRID ? (a.backup_slot[t] != -1) : (a.ovf[t] != 0);
+    if (skip) continue;
+    // ------------------------------------------------------------ entry list
+    const size_t rb = static_cast<size_t>(t) * a.R;
+    const uint16_t* cnt_row = a.cnt + static_cast<size_t>(t) * a.nT;
+    int n = 0;
+    for (int kb = 0; kb < a.nT; kb += 32) {
+      const int k = kb + lane;
+      const int c = (k < a.nT) ? min(static_cast<int>(cnt_row[k]), a.C) : 0;
+      unsigned mask = __ballot_sync(0xFFFFFFFFu, c > 0);
+      while (mask) {
+        const int src = __ffs(mask) - 1;
+        mask &= mask - 1;
+        const int kk = kb + src;
+        const int cc = __shfl_sync(0xFFFFFFFFu, c, src);
+        if (lane < cc) {
+          const size_t sb = (static_cast<size_t>(t) * a.nT + kk) * a.C + lane;
+          const int j = kk * a.W + a.idx[sb];
+          const uint16_t ab = a.val[sb];
+          lj[n + lane] = static_cast<uint16_t>(j);
+          lh[n + lane] = bf16_to_f32(ab);
+          if (HYBRID) {
+            a.ell_idx[rb + n + lane] = static_cast<uint16_t>(j);
+            a.ell_a[rb + n + lane] = ab;
+          }
+        }
+        n += cc;
+      }
+    }
+    __syncwarp();
+    const int total = GATED ? 2 * n : n;
+    auto row_src = [&](int k) -> const uint16_t* {
+      if (GATED && k < n) return a.Wu + static_cast<size_t>(lj[k]) * d;
+      return a.Wd + static_cast<size_t>(lj[GATED ? k - n : k]) * d;
+    };
+    if (lane == 0)
+      for (int k = 0; k < S && k < total; ++k) ring.issue(g + k, row_src(k));
+    int k = 0;
+    bool ok = true;
+    // ------------------------------------------------------------ up: h = a (x_t . Wu[j])
+    if (GATED) {
+      uint4 xv[NCH];
+      const uint4* xr = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * d);
+#pragma unroll
+      for (int q = 0; q < NCH; ++q) xv[q] = ldg16(xr + q * 32 + lane);
+      for (; k < n; ++k) {
+        if (!ring.wait(g + k, &abort_flag, status)) {
+          ok = false;
+          break;
+        }
+        const float u = warp_sum(dot_row<NCH>(xv, reinterpret_cast<const uint4*>(ring.slot(g + k)), lane));
+        if (lane == 0) {
+          lh[k] *= u;
+          if (HYBRID) a.ell_u[rb + k] = f32_to_bf16(u);
+        }
+        __syncwarp();
+        if (lane == 0 && k + S < total) {
+          fence_proxy_async_smem();
+          ring.issue(g + k + S, row_src(k + S));
+        }
+      }
+    }
+    // ------------------------------------------------------------ down: y_t = sum h Wd[j]
+    if (ok) {
+      float y[NCH][8];
+#pragma unroll
+      for (int q = 0; q < NCH; ++q)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y[q][i] = 0.f;
+      for (; k < total; ++k) {
+        if (!ring.wait(g + k, &abort_flag, status)) {
+          ok = false;
+          break;
+        }
+        const float h = lh[GATED ? k - n : k];
+        const uint4* row = reinterpret_cast<const uint4*>(ring.slot(g + k));
+#pragma unroll
+        for (int q = 0; q < NCH; ++q) axpy8(y[q], h, row[q * 32 + lane]);
+        __syncwarp();
+        if (lane == 0 && k + S < total) {
+          fence_proxy_async_smem();
+          ring.issue(g + k + S, row_src(k + S));
+        }
+      }
+      if (ok) {
+        uint4* yr = reinterpret_cast<uint4*>(a.y + static_cast<size_t>(t) * d);
+#pragma unroll
+        for (int q = 0; q < NCH; ++q) yr[q * 32 + lane] = pack8(y[q]);
+      }
+    }
+    if (!ok) {
+      if (lane == 0) ring.drain(g + k, g + min(total, k + S));
+      break;
+    }
+    g += total;
+    __syncwarp();  // the list is rewritten by the next token
+  }
+}
+
+// ====================================================================== backward: dh
+// One warp per ELL token, dy_t in registers, the row stream is Wd[j_0..j_n-1].
+// Lane l holds entry 32 b + l of the current batch b (neuron, a, u) and the neurons
+// of batch b + 1, which is all the producer needs to issue rows up to 32 ahead.
+//   dh = dy_t . Wd[j];  dg = dh u + l1 (non-gated: dh + l1);  du = dh a.
+// Also counts the entries of every neuron column for the transposed Hybrid.
+template <int NCH, bool GATED>
+__global__ void __launch_bounds__(256) sparse_dh_kernel(const SparseBwdArgs a, int32_t* status) {
+  constexpr int S = kDhRing;
+  constexpr uint32_t ROWB = NCH * 512;
+  constexpr int d = NCH * 256;
+  extern __shared__ __align__(128) uint8_t dh_smem[];
+  __shared__ uint64_t bars[8 * S];
+  __shared__ int abort_flag;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int wpb = blockDim.x >> 5;
+  WarpRing<S> ring{dh_smem + static_cast<size_t>(warp) * S * ROWB, bars + warp * S, ROWB};
+  if (threadIdx.x == 0) abort_flag = 0;
+  __syncthreads();
+  ring.init(lane);
+  uint32_t g = 0;
+  for (int t = blockIdx.x * wpb + warp; t < a.T; t += gridDim.x * wpb) {
+    const int n = a.ell_nnz[t];
+    if (n == 0) continue;
+    const size_t rb = static_cast<size_t>(t) * a.R;
+    auto load_j = [&](int e) { return e < n ? static_cast<int>(a.ell_idx[rb + e]) : 0; };
+    int jcur = load_j(lane), jnxt = load_j(32 + lane);
+    if (lane < n) atomicAdd(a.col_cnt + jcur, 1);
+    if (32 + lane < n) atomicAdd(a.col_cnt + jnxt, 1);
+    for (int k = 0; k < S && k < n; ++k) {
+      const int j = __shfl_sync(0xFFFFFFFFu, k < 32 ? jcur : jnxt, k & 31);
+      if (lane == 0) ring.issue(g + k, a.Wd + static_cast<size_t>(j) * d);
+    }
+    uint4 dyv[NCH];
+    const uint4* dyr = reinterpret_cast<const uint4*>(a.dy + static_cast<size_t>(t) * d);
+#pragma unroll
+    for (int q = 0; q < NCH; ++q) dyv[q] = ldg16(dyr + q * 32 + lane);
+    float acur = 0.f, ucur = 1.f, dg_keep = 0.f, du_keep = 0.f;
+    bool ok = true;
+    int k = 0;
+    for (; k < n; ++k) {
+      if ((k & 31) == 0) {  // new batch: coefficients of its entries, neurons of the one after
+        if (k > 0) {
+          jcur = jnxt;
+          jnxt = load_j(k + 32 + lane);
+          if (k + 32 + lane < n) atomicAdd(a.col_cnt + jnxt, 1);
+        }
+        acur = (k + lane < n) ? bf16_to_f32(a.ell_a[rb + k + lane]) : 0.f;
+        ucur = (GATED && k + lane < n) ? bf16_to_f32(a.ell_u[rb + k + lane]) : 1.f;
+      }
+      if (!ring.wait(g + k, &abort_flag, status)) {
+        ok = false;
+        break;
+      }
+      const float dh = warp_sum(dot_row<NCH>(dyv, reinterpret_cast<const uint4*>(ring.slot(g + k)), lane));
+      if (lane == (k & 31)) {
+        dg_keep = (GATED ? dh * ucur : dh) + a.l1;
+        du_keep = dh * acur;
+      }
+      __syncwarp();
+      const int kn = k + S;
+      if (kn < n) {
+        const int j = __shfl_sync(0xFFFFFFFFu, (kn >> 5) == (k >> 5) ? jcur : jnxt, kn & 31);
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          ring.issue(g + kn, a.Wd + static_cast<size_t>(j) * d);
+        }
+      }
+      if ((k & 31) == 31 || k == n - 1) {  // batch done: its lanes store their coefficients
+        const int e = (k & ~31) + lane;
+        if (e < n) {
+          a.dg[rb + e] = dg_keep;
+          if (GATED) a.du[rb + e] = du_keep;
+        }
+      }
+    }
+    if (!ok) {
+      if (lane == 0) ring.drain(g + k, g + min(n, k + S));
+      break;
+    }
+    g += n;
+  }
+}
+
+// ====================================================================== backward: dx
+// One warp per ELL token, dx_t accumulated in registers (fp32), the row stream is
+// Wg[j_0], Wu[j_0], Wg[j_1], Wu[j_1], ... (non-gated: Wg only):
+//   dx_t = sum over entries of dg Wg[j] + du Wu[j].
+// Tokens without ELL entries get dx = 0 (backup rows are overwritten by the dense
+// path afterwards).
+template <int NCH, bool GATED>
+__global__ void __launch_bounds__(256) sparse_dx_kernel(const SparseBwdArgs a, int32_t* status) {
+  constexpr int S = kDxRing;
+  constexpr int RPE = GATED ? 2 : 1;  // rows per entry
+  constexpr uint32_t ROWB = NCH * 512;
+  constexpr int d = NCH * 256;
+  extern __shared__ __align__(128) uint8_t dx_smem[];
+  __shared__ uint64_t bars[8 * S];
+  __shared__ int abort_flag;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int wpb = blockDim.x >> 5;
+  WarpRing<S> ring{dx_smem + static_cast<size_t>(warp) * S * ROWB, bars + warp * S, ROWB};
+  if (threadIdx.x == 0) abort_flag = 0;
+  __syncthreads();
+  ring.init(lane);
+  uint32_t g = 0;
+  for (int t = blockIdx.x * wpb + warp; t < a.T; t += gridDim.x * wpb) {
+    const int n = a.ell_nnz[t];
+    float acc[NCH][8];
+#pragma unroll
+    for (int q = 0; q < NCH; ++q)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[q][i] = 0.f;
+    const size_t rb = static_cast<size_t>(t) * a.R;
+    const int total = RPE * n;
+    bool ok = true;
+    int k = 0;
+    if (n > 0) {
+      auto load_j = [&](int e) { return e < n ? static_cast<int>(a.ell_idx[rb + e]) : 0; };
+      int jcur = load_j(lane), jnxt = load_j(32 + lane);
+      auto src_of = [&](int kk, int j) -> const uint16_t* {
+        return ((GATED && (kk & 1)) ? a.Wu : a.Wg) + static_cast<size_t>(j) * d;
+      };
+      for (int kk = 0; kk < S && kk < total; ++kk) {
+        const int e = kk / RPE;
+        const int j = __shfl_sync(0xFFFFFFFFu, e < 32 ? jcur : jnxt, e & 31);
+        if (lane == 0) ring.issue(g + kk, src_of(kk, j));
+      }
+      float gcur = 0.f, ucur = 0.f;
+      for (; k < total; ++k) {
+        const int e = k / RPE;
+        if ((k % (32 * RPE)) == 0) {
+          if (k > 0) {
+            jcur = jnxt;
+            jnxt = load_j(e + 32 + lane);
+          }
+          gcur = (e + lane < n) ? a.dg[rb + e + lane] : 0.f;
+          ucur = (GATED && e + lane < n) ? a.du[rb + e + lane] : 0.f;
+        }
+        if (!ring.wait(g + k, &abort_flag, status)) {
+          ok = false;
+          break;
+        }
+        const float c = __shfl_sync(0xFFFFFFFFu, (GATED && (k & 1)) ? ucur : gcur, e & 31);
+        const uint4* row = reinterpret_cast<const uint4*>(ring.slot(g + k));
+#pragma unroll
+        for (int q = 0; q < NCH; ++q) axpy8(acc[q], c, row[q * 32 + lane]);
+        __syncwarp();
+        const int kn = k + S;
+        if (kn < total) {
+          const int en = kn / RPE;
+          const int j = __shfl_sync(0xFFFFFFFFu, (en >> 5) == (e >> 5) ? jcur : jnxt, en & 31);
+          if (lane == 0) {
+            fence_proxy_async_smem();
+            ring.issue(g + kn, src_of(kn, j));
+          }
+        }
+      }
+    }
+    if (!ok) {
+      if (lane == 0) ring.drain(g + k, g + min(total, k + S));
+      break;
+    }
+    uint4* dr = reinterpret_cast<uint4*>(a.dx + static_cast<size_t>(t) * d);
+#pragma unroll
+    for (int q = 0; q < NCH; ++q) dr[q * 32 + lane] = pack8(acc[q]);
+    g += total;
+  }
+}
+
+// ====================================================================== transposed Hybrid
+// Exclusive scan of the per-neuron counts (one CTA, each thread a run of consecutive
+// neurons): col_ptr[0..I], col_cur = col_ptr.
+__global__ void __launch_bounds__(1024) csc_scan_kernel(const int32_t* __restrict__ col_cnt, int I,
+                                                        int32_t* __restrict__ col_ptr, int32_t* __restrict__ col_cur) {
+  __shared__ int warp_tot[32];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int per = (I + blockDim.x - 1) / blockDim.x;
+  const int lo = min(I, tid * per), hi = min(I, lo + per);
+  int sum = 0;
+  for (int j = lo; j < hi; ++j) sum += col_cnt[j];
+  const int incl = warp_inclusive_scan(sum);
+  if (lane == 31) warp_tot[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int v = lane < (blockDim.x >> 5) ? warp_tot[lane] : 0;
+    warp_tot[lane] = warp_inclusive_scan(v);
+  }
+  __syncthreads();
+  int run = (wid ? warp_tot[wid - 1] : 0) + incl - sum;
+  for (int j = lo; j < hi; ++j) {
+    col_ptr[j] = run;
+    col_cur[j] = run;
+    run += col_cnt[j];
+  }
+  if (tid == blockDim.x - 1) col_ptr[I] = warp_tot[(blockDim.x >> 5) - 1];
+}
+
+__global__ void __launch_bounds__(256) csc_fill_kernel(const int32_t* __restrict__ ell_nnz,
+                                                       const uint16_t* __restrict__ ell_idx, int T, int R,
+                                                       int32_t* __restrict__ col_cur, int32_t* __restrict__ csc) {
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
+    const int n = ell_nnz[t];
+    for (int s = lane; s < n; s += 32) {
+      const size_t e = static_cast<size_t>(t) * R + s;
+      csc[atomicAdd(col_cur + ell_idx[e], 1)] = static_cast<int32_t>(e);
+    }
+  }
+}
+
+// ====================================================================== backward: dW
+// One warp per (256-wide slice c of d, neuron j), slices outermost, so that while
+// slice c is processed only x[:, slice c] and dy[:, slice c] (16 MB at T = 16384) are
+// gathered: they stay in L2. Lane l owns 8 columns of the slice. The column's
+// entries are taken 32 at a time: lane r loads entry r's token and coefficients
+// (one round trip for all 32), then the warp walks them with kWgradUnroll entries'
+// row slices in flight:
+//   dWg[j] += dg x_t,  dWu[j] += du x_t,  dWd[j] += (a u) dy_t   (fp32, overwritten,
+// streaming stores).
+template <bool GATED>
+__global__ void __launch_bounds__(256, 2) ell_weight_grad_kernel(const SparseBwdArgs a) {
+  constexpr int U = kWgradUnroll;
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  const long items = static_cast<long>(a.d / 256) * a.I;
+  for (long it = static_cast<long>(blockIdx.x) * wpb + (threadIdx.x >> 5); it < items;
+       it += static_cast<long>(gridDim.x) * wpb) {
+    const int c = static_cast<int>(it / a.I);
+    const int j = static_cast<int>(it - static_cast<long>(c) * a.I);
+    const int col = c * 256 + lane * 8;
+    const int lo = a.col_ptr[j], hi = a.col_ptr[j + 1];
+    float g[8], u[8], h[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) g[i] = u[i] = h[i] = 0.f;
+    for (int e0 = lo; e0 < hi; e0 += 32) {
+      const int m = min(32, hi - e0);
+      int tl = 0;
+      float gl = 0.f, ul = 0.f, hl = 0.f;
+      if (lane < m) {
+        const int ent = a.csc[e0 + lane];
+        tl = ent / a.R;
+        gl = a.dg[ent];
+        const float av = bf16_to_f32(a.ell_a[ent]);
+        ul = GATED ? a.du[ent] : 0.f;
+        hl = GATED ? av * bf16_to_f32(a.ell_u[ent]) : av;
+      }
+      for (int r = 0; r < m; r += U) {
+        uint4 xv[U], dv[U];
+        float cg[U], cu[U], ch[U];
+#pragma unroll
+        for (int q = 0; q < U; ++q) {
+          const int src = min(r + q, 31);
+          const int t = __shfl_sync(0xFFFFFFFFu, tl, src);
+          const float gq = __shfl_sync(0xFFFFFFFFu, gl, src);
+          const float uq = __shfl_sync(0xFFFFFFFFu, ul, src);
+          const float hq = __shfl_sync(0xFFFFFFFFu, hl, src);
+          const bool live = r + q < m;
+          const size_t row = static_cast<size_t>(t) * a.d + col;
+          xv[q] = live ? ldg16(reinterpret_cast<const uint4*>(a.x + row)) : make_uint4(0, 0, 0, 0);
+          dv[q] = live ? ldg16(reinterpret_cast<const uint4*>(a.dy + row)) : make_uint4(0, 0, 0, 0);
+          cg[q] = live ? gq : 0.f;
+          cu[q] = live ? uq : 0.f;
+          ch[q] = live ? hq : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < U; ++q) {
+          axpy8(g, cg[q], xv[q]);
+          if (GATED) axpy8(u, cu[q], xv[q]);
+          axpy8(h, ch[q], dv[q]);
+        }
+      }
+    }
+    const size_t o = static_cast<size_t>(j) * a.d + col;
+    stcs_f32x8(a.dWg + o, g);
+    if (GATED) stcs_f32x8(a.dWu + o, u);
+    stcs_f32x8(a.dWd + o, h);
+  }
+}
+
+// ====================================================================== launchers
+#define TW_NCH_SWITCH(nch, CALL)           \
+  switch (nch) {                           \
+    case 1: CALL(1); break;                \
+    case 2: CALL(2); break;                \
+    case 3: CALL(3); break;                \
+    case 4: CALL(4); break;                \
+    case 5: CALL(5); break;                \
+    case 6: CALL(6); break;                \
+    case 7: CALL(7); break;                \
+    case 8: CALL(8); break;                \
+    default: return cudaErrorInvalidValue; \
+  }
+
+// largest per-warp entry list the forward supports
+constexpr int kFwdListMax = 12288;
+
+template <class K>
+static cudaError_t set_smem(K kern, size_t bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+}
+
+// warps per CTA for a kernel whose warps need `per_warp` bytes of shared memory:
+// at most 8, and a CTA of at most 110 KB so that two fit on an SM
+static int warps_for(size_t per_warp) {
+  return static_cast<int>(std::max<size_t>(1, std::min<size_t>(8, (110u << 10) / per_warp)));
+}
+
+template <bool GATED, bool HYBRID>
+static cudaError_t launch_fwd(const SparseFwdArgs& a, int32_t* status, cudaStream_t s) {
+  const int nch = a.d / 256;
+  const size_t per_warp = fwd_warp_smem(nch, a.L);
+  const int wpb = warps_for(per_warp);
+  const size_t smem = per_warp * wpb;
+  const int grid = grid_for(a.T, wpb, 8);
+#define TW_FWD(n)                                                                    \
+  {                                                                                  \
+    cudaError_t e = set_smem(sparse_fwd_kernel<n, GATED, HYBRID>, smem);             \
+    if (e != cudaSuccess) return e;                                                  \
+    sparse_fwd_kernel<n, GATED, HYBRID><<<grid, wpb * 32, smem, s>>>(a, status);     \
+  }
+  TW_NCH_SWITCH(nch, TW_FWD)
+#undef TW_FWD
+  trace_mark(s, "sparse_fwd");
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sparse_fwd(const SparseFwdArgs& a, int32_t* status, cudaStream_t s) {
+  if (a.T == 0) return cudaSuccess;
+  if (a.L < 1 || a.L > kFwdListMax) return cudaErrorInvalidValue;
+  const bool gated = a.Wu != nullptr;
+  const bool hybrid = a.backup_slot != nullptr;
+  if (gated) return hybrid ? launch_fwd<true, true>(a, status, s) : launch_fwd<true, false>(a, status, s);
+  return hybrid ? launch_fwd<false, true>(a, status, s) : launch_fwd<false, false>(a, status, s);
+}
+
+template <bool GATED>
+static cudaError_t launch_bwd(const SparseBwdArgs& a, int32_t* status, cudaStream_t s) {
+  cudaError_t e = memset_async(a.col_cnt, 0, sizeof(int32_t) * (a.I + 1), s);
+  if (e != cudaSuccess) return e;
+  const int nch = a.d / 256;
+  const size_t rowb = static_cast<size_t>(nch) * 512;
+  if (a.T > 0) {
+    const int wpb = warps_for(kDhRing * rowb);
+    const size_t smem = kDhRing * rowb * wpb;
+    const int grid = grid_for(a.T, wpb, 8);
+#define TW_DH(n)                                                         \
+  {                                                                      \
+    e = set_smem(sparse_dh_kernel<n, GATED>, smem);                      \
+    if (e != cudaSuccess) return e;                                      \
+    sparse_dh_kernel<n, GATED><<<grid, wpb * 32, smem, s>>>(a, status);  \
+  }
+    TW_NCH_SWITCH(nch, TW_DH)
+#undef TW_DH
+    trace_mark(s, "sparse_dh");
+  }
+  csc_scan_kernel<<<1, 1024, 0, s>>>(a.col_cnt, a.I, a.col_ptr, a.col_cur);
+  trace_mark(s, "csc_scan");
+  if (a.T > 0) {
+    csc_fill_kernel<<<grid_for(a.T, 8, 8), 256, 0, s>>>(a.ell_nnz, a.ell_idx, a.T, a.R, a.col_cur, a.csc);
+    trace_mark(s, "csc_fill");
+    const int wpb = warps_for(kDxRing * rowb);
+    const size_t smem = kDxRing * rowb * wpb;
+    const int grid = grid_for(a.T, wpb, 8);
+#define TW_DX(n)                                                         \
+  {                                                                      \
+    e = set_smem(sparse_dx_kernel<n, GATED>, smem);                      \
+    if (e != cudaSuccess) return e;                                      \
+    sparse_dx_kernel<n, GATED><<<grid, wpb * 32, smem, s>>>(a, status);  \
+  }
+    TW_NCH_SWITCH(nch, TW_DX)
+#undef TW_DX
+    trace_mark(s, "sparse_dx");
+  }
+  const long items = static_cast<long>(nch) * a.I;
+  ell_weight_grad_kernel<GATED><<<grid_for(items, 8, 16), 256, 0, s>>>(a);
+  trace_mark(s, "ell_weight_grad");
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sparse_bwd(const SparseBwdArgs& a, int32_t* status, cudaStream_t s) {
+  if (a.Wu != nullptr) return launch_bwd<true>(a, status, s);
+  return launch_bwd<false>(a, status, s);
+}
+
+}  // namespace tw
