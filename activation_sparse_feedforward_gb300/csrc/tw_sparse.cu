@@ -37,46 +37,96 @@ namespace {
 constexpr int kFwdRing = 2;   // row slots per warp
 constexpr int kDhRing = 3;
 constexpr int kDxRing = 3;
-constexpr int kWgradUnroll = 8;
+constexpr int kWgradUnroll = 6;
 
-TW_DEV void axpy8(float (&y)[8], float h, const uint4& w) {
-  y[0] = fmaf(h, bf16_lo(w.x), y[0]);
-  y[1] = fmaf(h, bf16_hi(w.x), y[1]);
-  y[2] = fmaf(h, bf16_lo(w.y), y[2]);
-  y[3] = fmaf(h, bf16_hi(w.y), y[3]);
-  y[4] = fmaf(h, bf16_lo(w.z), y[4]);
-  y[5] = fmaf(h, bf16_hi(w.z), y[5]);
-  y[6] = fmaf(h, bf16_lo(w.w), y[6]);
-  y[7] = fmaf(h, bf16_hi(w.w), y[7]);
+// ---------------------------------------------------------------- row arithmetic
+// These loops are bound by instruction issue, so they use Blackwell's
+// mixed-precision FMA (bf16 x bf16 + fp32: the product of two bf16 values is exact
+// in fp32, one rounding per FMA, like converting first) for dot products, and its
+// packed fp32x2 FMA for axpys. Eight fp32 accumulators live as four packed pairs.
+typedef unsigned long long f32x2;
+struct F8 {
+  f32x2 v[4];
+};
+TW_DEV void f8_zero(F8& a) { a.v[0] = a.v[1] = a.v[2] = a.v[3] = 0ull; }
+TW_DEV f32x2 f2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
 }
-TW_DEV uint4 pack8(const float (&y)[8]) {
-  return make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-                    pack_bf16x2(y[6], y[7]));
+TW_DEV float2 f2_split(f32x2 v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return make_float2(lo, hi);
+}
+TW_DEV f32x2 bf16x2_to_f32x2(uint32_t w) { return f2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)); }
+TW_DEV void fma2(f32x2& acc, f32x2 a, f32x2 b) { asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b)); }
+// y += h * w over 8 bf16 elements (h2 = {h, h})
+TW_DEV void axpy8(F8& y, f32x2 h2, const uint4& w) {
+  fma2(y.v[0], h2, bf16x2_to_f32x2(w.x));
+  fma2(y.v[1], h2, bf16x2_to_f32x2(w.y));
+  fma2(y.v[2], h2, bf16x2_to_f32x2(w.z));
+  fma2(y.v[3], h2, bf16x2_to_f32x2(w.w));
+}
+// g += cg * x and u += cu * x sharing one conversion of x
+TW_DEV void axpy8_two(F8& g, f32x2 cg2, F8& u, f32x2 cu2, const uint4& x) {
+  const f32x2 x0 = bf16x2_to_f32x2(x.x), x1 = bf16x2_to_f32x2(x.y), x2 = bf16x2_to_f32x2(x.z),
+              x3 = bf16x2_to_f32x2(x.w);
+  fma2(g.v[0], cg2, x0);
+  fma2(g.v[1], cg2, x1);
+  fma2(g.v[2], cg2, x2);
+  fma2(g.v[3], cg2, x3);
+  fma2(u.v[0], cu2, x0);
+  fma2(u.v[1], cu2, x1);
+  fma2(u.v[2], cu2, x2);
+  fma2(u.v[3], cu2, x3);
+}
+TW_DEV uint4 pack8(const F8& y) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 p = f2_split(y.v[i]);
+    w[i] = pack_bf16x2(p.x, p.y);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+TW_DEV void stcs_f32x8(float* p, const F8& y) {
+  const float2 a = f2_split(y.v[0]), b = f2_split(y.v[1]), c = f2_split(y.v[2]), d = f2_split(y.v[3]);
+  __stcs(reinterpret_cast<float4*>(p), make_float4(a.x, a.y, b.x, b.y));
+  __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(c.x, c.y, d.x, d.y));
+}
+// p[0..3] += x . w over 8 bf16 pairs (mixed-precision FMA, four partial sums)
+TW_DEV void dot8(const uint4& x, const uint4& w, float (&p)[4]) {
+  asm("{\n\t"
+      ".reg .b16 x0, x1, x2, x3, x4, x5, x6, x7, w0, w1, w2, w3, w4, w5, w6, w7;\n\t"
+      "mov.b32 {x0, x1}, %4;\n\t"
+      "mov.b32 {x2, x3}, %5;\n\t"
+      "mov.b32 {x4, x5}, %6;\n\t"
+      "mov.b32 {x6, x7}, %7;\n\t"
+      "mov.b32 {w0, w1}, %8;\n\t"
+      "mov.b32 {w2, w3}, %9;\n\t"
+      "mov.b32 {w4, w5}, %10;\n\t"
+      "mov.b32 {w6, w7}, %11;\n\t"
+      "fma.rn.f32.bf16 %0, x0, w0, %0;\n\t"
+      "fma.rn.f32.bf16 %1, x1, w1, %1;\n\t"
+      "fma.rn.f32.bf16 %2, x2, w2, %2;\n\t"
+      "fma.rn.f32.bf16 %3, x3, w3, %3;\n\t"
+      "fma.rn.f32.bf16 %0, x4, w4, %0;\n\t"
+      "fma.rn.f32.bf16 %1, x5, w5, %1;\n\t"
+      "fma.rn.f32.bf16 %2, x6, w6, %2;\n\t"
+      "fma.rn.f32.bf16 %3, x7, w7, %3;\n\t"
+      "}"
+      : "+f"(p[0]), "+f"(p[1]), "+f"(p[2]), "+f"(p[3])
+      : "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w), "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w));
 }
 TW_DEV uint4 ldg16(const uint4* p) { return __ldg(p); }
-// dot product of a lane's NCH chunks with a row in shared memory, four independent
-// partial sums (a single chain would serialise 8 * NCH dependent FMAs)
+// dot product of a lane's NCH chunks with a row in shared memory
 template <int NCH>
 TW_DEV float dot_row(const uint4 (&xv)[NCH], const uint4* row, int lane) {
   float p[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int q = 0; q < NCH; ++q) {
-    const uint4 w = row[q * 32 + lane];
-    const uint4& x = xv[q];
-    p[0] = fmaf(bf16_lo(x.x), bf16_lo(w.x), p[0]);
-    p[1] = fmaf(bf16_hi(x.x), bf16_hi(w.x), p[1]);
-    p[2] = fmaf(bf16_lo(x.y), bf16_lo(w.y), p[2]);
-    p[3] = fmaf(bf16_hi(x.y), bf16_hi(w.y), p[3]);
-    p[0] = fmaf(bf16_lo(x.z), bf16_lo(w.z), p[0]);
-    p[1] = fmaf(bf16_hi(x.z), bf16_hi(w.z), p[1]);
-    p[2] = fmaf(bf16_lo(x.w), bf16_lo(w.w), p[2]);
-    p[3] = fmaf(bf16_hi(x.w), bf16_hi(w.w), p[3]);
-  }
+  for (int q = 0; q < NCH; ++q) dot8(xv[q], row[q * 32 + lane], p);
   return (p[0] + p[1]) + (p[2] + p[3]);
-}
-TW_DEV void stcs_f32x8(float* p, const float (&v)[8]) {
-  __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
-  __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(v[4], v[5], v[6], v[7]));
 }
 
 int grid_for(long items, int per_block, int blocks_per_sm) {
@@ -187,20 +237,19 @@ __global__ void __launch_bounds__(256) sparse_fwd_kernel(const SparseFwdArgs a, 
     }
     // ------------------------------------------------------------ down: y_t = sum h Wd[j]
     if (ok) {
-      float y[NCH][8];
+      F8 y[NCH];
 #pragma unroll
-      for (int q = 0; q < NCH; ++q)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) y[q][i] = 0.f;
+      for (int q = 0; q < NCH; ++q) f8_zero(y[q]);
       for (; k < total; ++k) {
         if (!ring.wait(g + k, &abort_flag, status)) {
           ok = false;
           break;
         }
         const float h = lh[GATED ? k - n : k];
+        const f32x2 h2 = f2(h, h);
         const uint4* row = reinterpret_cast<const uint4*>(ring.slot(g + k));
 #pragma unroll
-        for (int q = 0; q < NCH; ++q) axpy8(y[q], h, row[q * 32 + lane]);
+        for (int q = 0; q < NCH; ++q) axpy8(y[q], h2, row[q * 32 + lane]);
         __syncwarp();
         if (lane == 0 && k + S < total) {
           fence_proxy_async_smem();
@@ -332,11 +381,9 @@ __global__ void __launch_bounds__(256) sparse_dx_kernel(const SparseBwdArgs a, i
   uint32_t g = 0;
   for (int t = blockIdx.x * wpb + warp; t < a.T; t += gridDim.x * wpb) {
     const int n = a.ell_nnz[t];
-    float acc[NCH][8];
+    F8 acc[NCH];
 #pragma unroll
-    for (int q = 0; q < NCH; ++q)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[q][i] = 0.f;
+    for (int q = 0; q < NCH; ++q) f8_zero(acc[q]);
     const size_t rb = static_cast<size_t>(t) * a.R;
     const int total = RPE * n;
     bool ok = true;
@@ -368,9 +415,10 @@ __global__ void __launch_bounds__(256) sparse_dx_kernel(const SparseBwdArgs a, i
           break;
         }
         const float c = __shfl_sync(0xFFFFFFFFu, (GATED && (k & 1)) ? ucur : gcur, e & 31);
+        const f32x2 c2 = f2(c, c);
         const uint4* row = reinterpret_cast<const uint4*>(ring.slot(g + k));
 #pragma unroll
-        for (int q = 0; q < NCH; ++q) axpy8(acc[q], c, row[q * 32 + lane]);
+        for (int q = 0; q < NCH; ++q) axpy8(acc[q], c2, row[q * 32 + lane]);
         __syncwarp();
         const int kn = k + S;
         if (kn < total) {
@@ -457,9 +505,10 @@ __global__ void __launch_bounds__(256, 2) ell_weight_grad_kernel(const SparseBwd
     const int j = static_cast<int>(it - static_cast<long>(c) * a.I);
     const int col = c * 256 + lane * 8;
     const int lo = a.col_ptr[j], hi = a.col_ptr[j + 1];
-    float g[8], u[8], h[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) g[i] = u[i] = h[i] = 0.f;
+    F8 g, u, h;
+    f8_zero(g);
+    f8_zero(u);
+    f8_zero(h);
     for (int e0 = lo; e0 < hi; e0 += 32) {
       const int m = min(32, hi - e0);
       int tl = 0;
@@ -492,9 +541,11 @@ __global__ void __launch_bounds__(256, 2) ell_weight_grad_kernel(const SparseBwd
         }
 #pragma unroll
         for (int q = 0; q < U; ++q) {
-          axpy8(g, cg[q], xv[q]);
-          if (GATED) axpy8(u, cu[q], xv[q]);
-          axpy8(h, ch[q], dv[q]);
+          if (GATED)
+            axpy8_two(g, f2(cg[q], cg[q]), u, f2(cu[q], cu[q]), xv[q]);
+          else
+            axpy8(g, f2(cg[q], cg[q]), xv[q]);
+          axpy8(h, f2(ch[q], ch[q]), dv[q]);
         }
       }
     }
