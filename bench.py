@@ -8,7 +8,8 @@ gradients, dense backup GEMMs). Inputs are seeded synthetic bf16 tensors of the
 pages' 1.5B-model FFN shape (see synthetic/workloads.py for the recipe).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-cpu-baseline] [--sweep]
+                    [--workload NAME] [--tokens T] [--no-cpu-baseline]
+                    [--no-dense] [--no-inference] [--sweep]
 
 Prints ONE JSON line (rank 0). Timing: W untimed warm-up steps, then K steps each
 bracketed by CUDA events on the launching stream with a 256 MiB L2 flush between
@@ -202,6 +203,89 @@ def oracle_sample_time(spec, inp, n_tokens: int) -> tuple[float, int, str]:
     return dt, cores, f"first {n_tokens} tokens of {spec.name}, full weights, fp64 numpy (BLAS threads: all cores)"
 
 
+# ------------------------------------------------------------------ secondary measurements
+def _time_steps(fn, steps: int, warmup: int, flush, stream) -> float:
+    """Average device ms of fn over `steps` calls, L2 flushed (untimed) before each."""
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    total = 0.0
+    for _ in range(steps):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        e.synchronize()
+        total += s.elapsed_time(e)
+    return total / steps
+
+
+def measure_inference(dev, flush, stream, steps: int) -> dict:
+    """TwELL inference forward at the gated and non-gated 1.5B FFN shapes, next to the
+    dense bf16 forward (cuBLAS through torch) on the same inputs."""
+    import numpy as np
+    import torch
+
+    import activation_sparse_feedforward_gb300 as tw
+    from synthetic import WORKLOADS, make_inputs
+
+    out = {}
+    for name in ("gated_fwd_d2048_i5632", "nongated_fwd_d2048_i8192"):
+        spec = WORKLOADS[name]
+        inp = make_inputs(spec)
+        x, Wg, Wu, Wd = (None if inp[k] is None else
+                         torch.from_numpy(inp[k].view(np.int16)).view(torch.bfloat16).to(dev)
+                         for k in ("x", "Wg", "Wu", "Wd"))
+        f = tw.TwellFFN(spec.T, spec.d, spec.I, spec.W, spec.C, ovf_cap=512, device=dev)
+        ms = _time_steps(lambda: f(x, Wg, Wu, Wd), steps, 3, flush, stream)
+        tw.raise_if_device_error(f.status, name)
+
+        def dense():
+            a = torch.relu(x @ Wg.T)
+            h = a * (x @ Wu.T) if Wu is not None else a
+            return h @ Wd
+
+        ms_d = _time_steps(dense, steps, 3, flush, stream)
+        out[name] = {"tokens_per_ms": spec.T / ms, "ms": ms, "dense_bf16_tokens_per_ms": spec.T / ms_d,
+                     "n_overflow_rows": int(f.tw.n_ovf.item()),
+                     "nnz_per_token": float(f.tw.row_nnz.float().mean().item())}
+    return out
+
+
+def measure_sweep(dev, flush, stream, steps: int) -> list:
+    """The training step over the sparsity sweep (mean actives x outlier fraction)."""
+    import numpy as np
+    import torch
+
+    import activation_sparse_feedforward_gb300 as tw
+    from synthetic import WORKLOADS, make_inputs
+
+    rows = []
+    for m in (29, 108, 911):
+        for o in (0, 1, 5):
+            spec = WORKLOADS[f"train_d2048_i5632_m{m}_o{o}"]
+            inp = make_inputs(spec, with_dy=True)
+            x, Wg, Wu, Wd, dy = (torch.from_numpy(inp[k].view(np.int16)).view(torch.bfloat16).to(dev)
+                                 for k in ("x", "Wg", "Wu", "Wd", "dy"))
+            h = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, spec.T, gated=True, device=dev)
+
+            def step():
+                h.forward(x, Wg, Wu, Wd)
+                h.backward(dy, x, Wg, Wu, Wd, spec.l1)
+
+            ms = _time_steps(step, steps, 3, flush, stream)
+            tw.raise_if_device_error(h.status, spec.name)
+            rows.append({"workload": spec.name, "tokens_per_ms": spec.T / ms, "ms": ms,
+                         "n_backup": int(h.saved.n_backup.item()),
+                         "nnz_per_token": float(h.saved.row_nnz.float().mean().item())})
+            del h
+            torch.cuda.empty_cache()
+    return rows
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args, dist: Dist) -> dict | None:
     import numpy as np
@@ -214,6 +298,8 @@ def run_ours(args, dist: Dist) -> dict | None:
     torch.cuda.set_device(dev)
     peaks = _peaks()
     spec = WORKLOADS[args.workload].with_(seed=dist.rank)
+    if args.tokens:
+        spec = spec.with_(T=args.tokens)
     inp = make_inputs(spec, with_dy=True)
 
     def to_dev(b):
@@ -395,6 +481,10 @@ def run_ours(args, dist: Dist) -> dict | None:
         "clocks": clk,
         "dense_bf16": dense,
     }
+    if not args.no_inference:
+        line["inference"] = measure_inference(dev, flush, stream, max(3, args.steps // 2))
+    if args.sweep:
+        line["sweep"] = measure_sweep(dev, flush, stream, max(3, args.steps // 4))
     if dist.rank == 0 and not args.no_cpu_baseline:
         n_s = args.cpu_sample_tokens
         dt, cores, sample = oracle_sample_time(spec, inp, n_s)
@@ -439,6 +529,10 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--no-inference", action="store_true", help="skip the TwELL inference forward figures")
+    ap.add_argument("--sweep", action="store_true", help="also time the training sparsity sweep")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the workload's token count (small cases for profiler captures)")
     ap.add_argument("--cpu-sample-tokens", type=int, default=2048)
     ap.add_argument("--reference-sample-tokens", type=int, default=256)
     args = ap.parse_args()

@@ -81,6 +81,12 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.tw_dense_gemm(16, 16, 64, 60, 64, 0, 0, 16, 16, None) == _lib.TW_EINVAL
 
 
+def test_trace_hook_host_side(lib):
+    assert lib.tw_trace_begin(None, 4) == _lib.TW_EINVAL
+    assert lib.tw_trace_end() == 0
+    assert lib.tw_trace_label(0) is None
+
+
 def test_workspace_sizes_grow_with_capacity(lib):
     a = lib.twell_ffn_fwd_workspace_size(16384, 2048, 5632, 128, 16, 0)
     b = lib.twell_ffn_fwd_workspace_size(16384, 2048, 5632, 128, 16, 200)

@@ -30,6 +30,8 @@ MEDIUM = [
     FFNSpec("med_nongated", T=600, d=768, I=1024, gated=False, mean_active=25, outlier_frac=0.02, W=64, C=8,
             R=64, seed=6),
     FFNSpec("med_w64_d2048", T=300, d=2048, I=704, mean_active=10, outlier_frac=0.02, W=64, C=6, R=24, seed=7),
+    # dense-ish regime: long ELL rows (R = 320) and wide TwELL tiles (C = 32)
+    FFNSpec("med_long_rows", T=513, d=512, I=1280, mean_active=200, outlier_frac=0.02, W=128, C=32, R=320, seed=8),
 ]
 
 
@@ -147,10 +149,13 @@ def test_hybrid_saved_format_matches_oracle_packing():
     assert_close(s.backup_u[:nb].cpu().numpy(), ref["backup_u"], "backup u")
 
 
-def test_hybrid_full_size_sampled():
-    spec = WORKLOADS["train_d2048_i5632_m29_o1"]
+@pytest.mark.parametrize("name,backup_cap", [("train_d2048_i5632_m29_o1", 256),
+                                             ("train_d2048_i5632_m108_o5", 1280),
+                                             ("train_d2048_i5632_m911_o0", 16384)])
+def test_hybrid_full_size_sampled(name, backup_cap):
+    spec = WORKLOADS[name]
     inp = make_inputs(spec, with_dy=True)
-    h, y, (dx, dWg, dWu, dWd) = _run_hybrid(spec, inp, backup_cap=256)
+    h, y, (dx, dWg, dWu, dWd) = _run_hybrid(spec, inp, backup_cap=backup_cap)
     rows = np.unique(np.concatenate([np.arange(5, spec.T, 1013), inp["outliers"][:10], [spec.T - 1]]))
     f = ffn.forward(inp["x"][rows], inp["Wg"], inp["Wu"], inp["Wd"])
     b = ffn.backward(inp["x"][rows], inp["Wg"], inp["Wu"], inp["Wd"], inp["dy"][rows], spec.l1, fwd=f)
