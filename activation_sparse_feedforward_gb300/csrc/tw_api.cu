@@ -145,7 +145,7 @@ struct HybBwdWs {
   int32_t* col_cnt;
   int32_t* col_ptr;
   int32_t* col_cur;
-  int32_t* csc;
+  uint4* csc;
   uint16_t* dY;
   uint16_t* X;
   tw::BackupGradOut g;  // dG, dU, H as (hi, lo) bf16 pairs
@@ -161,7 +161,7 @@ HybBwdWs carve_hybrid_bwd(Carve& c, int T, int d, int I, int R, int backup_cap) 
   w.col_cnt = c.take<int32_t>(static_cast<size_t>(I) + 1);
   w.col_ptr = c.take<int32_t>(static_cast<size_t>(I) + 1);
   w.col_cur = c.take<int32_t>(static_cast<size_t>(I));
-  w.csc = c.take<int32_t>(TR);
+  w.csc = c.take<uint4>(TR);
   w.dY = c.take<uint16_t>(static_cast<size_t>(ra) * d);
   w.X = c.take<uint16_t>(static_cast<size_t>(ra) * d);
   w.g.dG = c.take<uint16_t>(rI);
@@ -222,12 +222,13 @@ tw_status twell_pack(const uint16_t* A, int T, int I, int W, int C, const tw_twe
 
 static tw_status gate_pack_impl(const uint16_t* x, const uint16_t* Wg, int T, int d, int I, int W, int C,
                                 const tw_twell& o, uint16_t* a_dense, int cap_check, int32_t* dev_status,
-                                cudaStream_t s) {
+                                cudaStream_t s, bool list_overflow = true) {
   TW_TRY(tw::memset_async(o.row_nnz, 0, sizeof(int32_t) * T, s));
   TW_TRY(tw::memset_async(o.ovf, 0, static_cast<size_t>(T), s));
   TW_TRY(tw::gemm_gate_pack(x, Wg, T, d, I, W, C, o, a_dense, dev_status, s));
-  TW_TRY(tw::launch_compact_rows(o.ovf, nullptr, 0, T, o.ovf_rows, T, o.n_ovf, nullptr, nullptr, cap_check,
-                                 dev_status, s));
+  if (list_overflow)
+    TW_TRY(tw::launch_compact_rows(o.ovf, nullptr, 0, T, o.ovf_rows, T, o.n_ovf, nullptr, nullptr, cap_check,
+                                   dev_status, s));
   return TW_OK;
 }
 
@@ -327,7 +328,8 @@ tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* 
   const int ra = round_up(cap, 128);
   tw_twell o{T, I, W, C, w.cnt, w.val, w.idx, saved->row_nnz, w.ovf, w.ovf_rows, w.n_ovf};
 
-  st = gate_pack_impl(x, Wg, T, d, I, W, C, o, nullptr, T, dev_status, s);
+  // the backup list below covers the overflow rows, so the TwELL's own list is not built
+  st = gate_pack_impl(x, Wg, T, d, I, W, C, o, nullptr, T, dev_status, s, false);
   if (st != TW_OK) return st;
   TW_TRY(tw::launch_compact_rows(o.ovf, saved->row_nnz, R, T, saved->backup_tok, cap, saved->n_backup,
                                  saved->backup_slot, saved->ell_nnz, cap, dev_status, s));
@@ -365,6 +367,8 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
   if (T < 0 || I < 64 || I > 65536 || I % 64 != 0) return TW_EUNSUPPORTED;
   tw_status st = check_model_width(d);
   if (st != TW_OK) return st;
+  // token rows are addressed by 32-bit offsets in 16-byte units in the transposed Hybrid
+  if (static_cast<uint64_t>(T) * static_cast<uint64_t>(d / 8) > 0xFFFFFFFFull) return TW_EUNSUPPORTED;
   const bool gated = Wu != nullptr;
   st = check_hybrid(saved, T, I, gated);
   if (st != TW_OK) return st;

@@ -73,7 +73,7 @@ struct SparseBwdArgs {
   int32_t* col_cnt;   // [I + 1]
   int32_t* col_ptr;   // [I + 1]
   int32_t* col_cur;   // [I]
-  int32_t* csc;       // [T * R]
+  uint4* csc;         // [T * R] column-ordered entry records
   float *dWg, *dWu, *dWd;
 };
 // ELL backward: dh pass (dg, du per entry, column counts), transposed Hybrid, dx

@@ -137,7 +137,32 @@ cudaError_t launch_pack_dense(const uint16_t* A, int T, int I, int W, int C, con
 // One CTA of 1024 threads; thread i owns a run of consecutive rows. It counts the
 // flagged rows of its run, a block-wide exclusive scan of the counts gives the run's
 // first rank, and a second walk over the run writes the ranks, so the list comes out
-// in ascending row order.
+// in ascending row order. Runs are a multiple of 16 rows where T allows it, so both
+// walks move 16 rows at a time with vector loads and stores.
+namespace {
+// flags of rows t0 .. t0 + 15 as a bit mask; z receives their row_nnz (0 without it)
+TW_DEV uint32_t flags16(const uint8_t* __restrict__ ovf, const int32_t* __restrict__ row_nnz, int R, int t0,
+                        int (&z)[16]) {
+  const uint4 f = *reinterpret_cast<const uint4*>(ovf + t0);
+  const uint32_t fw[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int4 v = row_nnz != nullptr ? reinterpret_cast<const int4*>(row_nnz + t0)[q] : make_int4(0, 0, 0, 0);
+    z[4 * q] = v.x;
+    z[4 * q + 1] = v.y;
+    z[4 * q + 2] = v.z;
+    z[4 * q + 3] = v.w;
+  }
+  uint32_t m = 0;
+#pragma unroll
+  for (int b = 0; b < 16; ++b) {
+    const bool o = ((fw[b >> 2] >> (8 * (b & 3))) & 0xFFu) != 0;
+    m |= ((o || (row_nnz != nullptr && z[b] > R)) ? 1u : 0u) << b;
+  }
+  return m;
+}
+}  // namespace
+
 __global__ void __launch_bounds__(1024) compact_rows_kernel(const uint8_t* __restrict__ ovf,
                                                             const int32_t* __restrict__ row_nnz, int R, int T,
                                                             int32_t* __restrict__ list, int list_cap,
@@ -147,8 +172,6 @@ __global__ void __launch_bounds__(1024) compact_rows_kernel(const uint8_t* __res
   __shared__ int warp_tot[32];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int nwarps = blockDim.x >> 5;
-  // runs of 16 rows (a multiple of 16 so that the flags of a run load as one 16-byte
-  // vector and the counts as four) when the run length allows it
   int per = (T + blockDim.x - 1) / blockDim.x;
   per = (per + 15) / 16 * 16;
   const int lo = min(T, tid * per), hi = min(T, lo + per);
@@ -160,21 +183,8 @@ __global__ void __launch_bounds__(1024) compact_rows_kernel(const uint8_t* __res
   };
   int n = 0;
   if (vec) {
-    for (int t0 = lo; t0 < hi; t0 += 16) {
-      const uint4 f = *reinterpret_cast<const uint4*>(ovf + t0);
-      const uint32_t fw[4] = {f.x, f.y, f.z, f.w};
-      int4 z[4] = {make_int4(0, 0, 0, 0), make_int4(0, 0, 0, 0), make_int4(0, 0, 0, 0), make_int4(0, 0, 0, 0)};
-      if (row_nnz != nullptr)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) z[q] = reinterpret_cast<const int4*>(row_nnz + t0)[q];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int zz[4] = {z[q].x, z[q].y, z[q].z, z[q].w};
-#pragma unroll
-        for (int b = 0; b < 4; ++b)
-          n += (((fw[q] >> (8 * b)) & 0xFFu) != 0 || (row_nnz != nullptr && zz[b] > R)) ? 1 : 0;
-      }
-    }
+    int z[16];
+    for (int t0 = lo; t0 < hi; t0 += 16) n += __popc(flags16(ovf, row_nnz, R, t0, z));
   } else {
     for (int t = lo; t < hi; ++t) n += flagged(t) ? 1 : 0;
   }
@@ -187,16 +197,38 @@ __global__ void __launch_bounds__(1024) compact_rows_kernel(const uint8_t* __res
   }
   __syncthreads();
   int pos = (wid ? warp_tot[wid - 1] : 0) + incl - n;
-  for (int t = lo; t < hi; ++t) {
-    const bool f = flagged(t);
-    if (f) {
-      if (pos < list_cap) list[pos] = t;
-      if (slot_of) slot_of[t] = pos < list_cap ? pos : -2;
-      ++pos;
-    } else if (slot_of) {
-      slot_of[t] = -1;
+  if (vec) {
+    for (int t0 = lo; t0 < hi; t0 += 16) {
+      int z[16], sl[16], en[16];
+      const uint32_t m = flags16(ovf, row_nnz, R, t0, z);
+#pragma unroll
+      for (int b = 0; b < 16; ++b) {
+        const bool f = (m >> b) & 1u;
+        if (f && pos < list_cap) list[pos] = t0 + b;
+        sl[b] = f ? (pos < list_cap ? pos : -2) : -1;
+        en[b] = f ? 0 : z[b];
+        pos += f ? 1 : 0;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (slot_of)
+          reinterpret_cast<int4*>(slot_of + t0)[q] = make_int4(sl[4 * q], sl[4 * q + 1], sl[4 * q + 2], sl[4 * q + 3]);
+        if (ell_nnz)
+          reinterpret_cast<int4*>(ell_nnz + t0)[q] = make_int4(en[4 * q], en[4 * q + 1], en[4 * q + 2], en[4 * q + 3]);
+      }
     }
-    if (ell_nnz) ell_nnz[t] = f ? 0 : row_nnz[t];
+  } else {
+    for (int t = lo; t < hi; ++t) {
+      const bool f = flagged(t);
+      if (f) {
+        if (pos < list_cap) list[pos] = t;
+        if (slot_of) slot_of[t] = pos < list_cap ? pos : -2;
+        ++pos;
+      } else if (slot_of) {
+        slot_of[t] = -1;
+      }
+      if (ell_nnz) ell_nnz[t] = f ? 0 : row_nnz[t];
+    }
   }
   if (tid == blockDim.x - 1) {
     const int total = warp_tot[nwarps - 1];

@@ -37,7 +37,7 @@ namespace {
 constexpr int kFwdRing = 2;   // row slots per warp
 constexpr int kDhRing = 3;
 constexpr int kDxRing = 3;
-constexpr int kWgradUnroll = 6;
+constexpr int kWgradUnroll = 8;
 
 // ---------------------------------------------------------------- row arithmetic
 // These loops are bound by instruction issue, so they use Blackwell's
@@ -470,89 +470,107 @@ __global__ void __launch_bounds__(1024) csc_scan_kernel(const int32_t* __restric
   if (tid == blockDim.x - 1) col_ptr[I] = warp_tot[(blockDim.x >> 5) - 1];
 }
 
-__global__ void __launch_bounds__(256) csc_fill_kernel(const int32_t* __restrict__ ell_nnz,
-                                                       const uint16_t* __restrict__ ell_idx, int T, int R,
-                                                       int32_t* __restrict__ col_cur, int32_t* __restrict__ csc) {
+// Scatters every ELL entry into its column of the transposed Hybrid as one
+// 16-byte record {token row offset in 16-byte units, dg, du, h = a u (non-gated: a)},
+// so the weight-gradient pass reads one coalesced record per entry and nothing else
+// but the gathered rows.
+template <bool GATED>
+__global__ void __launch_bounds__(256) csc_fill_kernel(const SparseBwdArgs a) {
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
-  for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += gridDim.x * wpb) {
-    const int n = ell_nnz[t];
+  const uint32_t row16 = static_cast<uint32_t>(a.d / 8);
+  for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < a.T; t += gridDim.x * wpb) {
+    const int n = a.ell_nnz[t];
     for (int s = lane; s < n; s += 32) {
-      const size_t e = static_cast<size_t>(t) * R + s;
-      csc[atomicAdd(col_cur + ell_idx[e], 1)] = static_cast<int32_t>(e);
+      const size_t e = static_cast<size_t>(t) * a.R + s;
+      const float av = bf16_to_f32(a.ell_a[e]);
+      const float h = GATED ? av * bf16_to_f32(a.ell_u[e]) : av;
+      const uint4 rec = make_uint4(static_cast<uint32_t>(t) * row16, __float_as_uint(a.dg[e]),
+                                   GATED ? __float_as_uint(a.du[e]) : 0u, __float_as_uint(h));
+      a.csc[atomicAdd(a.col_cur + a.ell_idx[e], 1)] = rec;
     }
   }
 }
 
 // ====================================================================== backward: dW
-// One warp per (256-wide slice c of d, neuron j), slices outermost, so that while
-// slice c is processed only x[:, slice c] and dy[:, slice c] (16 MB at T = 16384) are
-// gathered: they stay in L2. Lane l owns 8 columns of the slice. The column's
-// entries are taken 32 at a time: lane r loads entry r's token and coefficients
-// (one round trip for all 32), then the warp walks them with kWgradUnroll entries'
-// row slices in flight:
-//   dWg[j] += dg x_t,  dWu[j] += du x_t,  dWd[j] += (a u) dy_t   (fp32, overwritten,
-// streaming stores).
+// One warp per (256-wide slice c of d, neuron j, side), slices outermost, so that
+// while slice c is processed only x[:, slice c] and dy[:, slice c] (16 MB at
+// T = 16384) are gathered: they stay in L2. The x side accumulates
+//   dWg[j] += dg x_t,  dWu[j] += du x_t   (gated)
+// and the dy side
+//   dWd[j] += h dy_t,  h = a u (non-gated: a)
+// (fp32, overwritten, streaming stores); splitting the sides halves the registers a
+// warp needs, so more warps and more row slices are in flight per SM. Lane l owns 8
+// columns of the slice. The column's records are staged 32 at a time in the warp's
+// shared memory with the coefficients already paired for the packed FMA
+// ({dg, dg, du, du}, {h, h, row}); a chunk whose length is not a multiple of the
+// unroll is padded with zero coefficients on the chunk's last row (an L1 hit), so
+// the inner loop has no predication and keeps kWgradUnroll row slices in flight.
 template <bool GATED>
-__global__ void __launch_bounds__(256, 2) ell_weight_grad_kernel(const SparseBwdArgs a) {
+__global__ void __launch_bounds__(256, 3) ell_weight_grad_kernel(const SparseBwdArgs a) {
   constexpr int U = kWgradUnroll;
+  static_assert(32 % U == 0, "the unroll must divide the staging chunk");
+  __shared__ float4 stage[8][2][32];
   const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   const int wpb = blockDim.x >> 5;
-  const long items = static_cast<long>(a.d / 256) * a.I;
-  for (long it = static_cast<long>(blockIdx.x) * wpb + (threadIdx.x >> 5); it < items;
-       it += static_cast<long>(gridDim.x) * wpb) {
-    const int c = static_cast<int>(it / a.I);
-    const int j = static_cast<int>(it - static_cast<long>(c) * a.I);
-    const int col = c * 256 + lane * 8;
+  float4(&cgu)[32] = stage[warp][0];
+  float4(&chr)[32] = stage[warp][1];
+  const int items = (a.d / 256) * a.I * 2;
+  for (int it = blockIdx.x * wpb + warp; it < items; it += gridDim.x * wpb) {
+    const bool xside = (it & 1) == 0;
+    const int cj = it >> 1;
+    const int c = cj / a.I;
+    const int j = cj - c * a.I;
+    const uint4* src = reinterpret_cast<const uint4*>(xside ? a.x : a.dy) + c * 32 + lane;
     const int lo = a.col_ptr[j], hi = a.col_ptr[j + 1];
-    F8 g, u, h;
-    f8_zero(g);
-    f8_zero(u);
-    f8_zero(h);
+    F8 p, q2;
+    f8_zero(p);
+    f8_zero(q2);
     for (int e0 = lo; e0 < hi; e0 += 32) {
       const int m = min(32, hi - e0);
-      int tl = 0;
-      float gl = 0.f, ul = 0.f, hl = 0.f;
-      if (lane < m) {
-        const int ent = a.csc[e0 + lane];
-        tl = ent / a.R;
-        gl = a.dg[ent];
-        const float av = bf16_to_f32(a.ell_a[ent]);
-        ul = GATED ? a.du[ent] : 0.f;
-        hl = GATED ? av * bf16_to_f32(a.ell_u[ent]) : av;
-      }
-      for (int r = 0; r < m; r += U) {
-        uint4 xv[U], dv[U];
-        float cg[U], cu[U], ch[U];
+      uint4 r = lane < m ? a.csc[e0 + lane] : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t last = __shfl_sync(0xFFFFFFFFu, r.x, m - 1);
+      if (lane >= m) r.x = last;
+      __syncwarp();  // the previous chunk's reads of the stage are done
+      const float cg = __uint_as_float(r.y), cu = __uint_as_float(r.z), ch = __uint_as_float(r.w);
+      cgu[lane] = make_float4(cg, cg, cu, cu);
+      chr[lane] = make_float4(ch, ch, __uint_as_float(r.x), 0.f);
+      __syncwarp();
+      if (xside) {
+        for (int k = 0; k < m; k += U) {
+          uint4 v[U];
 #pragma unroll
-        for (int q = 0; q < U; ++q) {
-          const int src = min(r + q, 31);
-          const int t = __shfl_sync(0xFFFFFFFFu, tl, src);
-          const float gq = __shfl_sync(0xFFFFFFFFu, gl, src);
-          const float uq = __shfl_sync(0xFFFFFFFFu, ul, src);
-          const float hq = __shfl_sync(0xFFFFFFFFu, hl, src);
-          const bool live = r + q < m;
-          const size_t row = static_cast<size_t>(t) * a.d + col;
-          xv[q] = live ? ldg16(reinterpret_cast<const uint4*>(a.x + row)) : make_uint4(0, 0, 0, 0);
-          dv[q] = live ? ldg16(reinterpret_cast<const uint4*>(a.dy + row)) : make_uint4(0, 0, 0, 0);
-          cg[q] = live ? gq : 0.f;
-          cu[q] = live ? uq : 0.f;
-          ch[q] = live ? hq : 0.f;
+          for (int q = 0; q < U; ++q) v[q] = ldg16(src + __float_as_uint(chr[k + q].z));
+#pragma unroll
+          for (int q = 0; q < U; ++q) {
+            const float4 e = cgu[k + q];
+            if (GATED)
+              axpy8_two(p, f2(e.x, e.y), q2, f2(e.z, e.w), v[q]);
+            else
+              axpy8(p, f2(e.x, e.y), v[q]);
+          }
         }
+      } else {
+        for (int k = 0; k < m; k += U) {
+          uint4 v[U];
 #pragma unroll
-        for (int q = 0; q < U; ++q) {
-          if (GATED)
-            axpy8_two(g, f2(cg[q], cg[q]), u, f2(cu[q], cu[q]), xv[q]);
-          else
-            axpy8(g, f2(cg[q], cg[q]), xv[q]);
-          axpy8(h, f2(ch[q], ch[q]), dv[q]);
+          for (int q = 0; q < U; ++q) v[q] = ldg16(src + __float_as_uint(chr[k + q].z));
+#pragma unroll
+          for (int q = 0; q < U; ++q) {
+            const float2 hh = *reinterpret_cast<const float2*>(&chr[k + q]);
+            axpy8(p, f2(hh.x, hh.y), v[q]);
+          }
         }
       }
     }
-    const size_t o = static_cast<size_t>(j) * a.d + col;
-    stcs_f32x8(a.dWg + o, g);
-    if (GATED) stcs_f32x8(a.dWu + o, u);
-    stcs_f32x8(a.dWd + o, h);
+    const size_t o = static_cast<size_t>(j) * a.d + c * 256 + lane * 8;
+    if (xside) {
+      stcs_f32x8(a.dWg + o, p);
+      if (GATED) stcs_f32x8(a.dWu + o, q2);
+    } else {
+      stcs_f32x8(a.dWd + o, p);
+    }
   }
 }
 
@@ -635,7 +653,7 @@ static cudaError_t launch_bwd(const SparseBwdArgs& a, int32_t* status, cudaStrea
   csc_scan_kernel<<<1, 1024, 0, s>>>(a.col_cnt, a.I, a.col_ptr, a.col_cur);
   trace_mark(s, "csc_scan");
   if (a.T > 0) {
-    csc_fill_kernel<<<grid_for(a.T, 8, 8), 256, 0, s>>>(a.ell_nnz, a.ell_idx, a.T, a.R, a.col_cur, a.csc);
+    csc_fill_kernel<GATED><<<grid_for(a.T, 8, 8), 256, 0, s>>>(a);
     trace_mark(s, "csc_fill");
     const int wpb = warps_for(kDxRing * rowb);
     const size_t smem = kDxRing * rowb * wpb;
@@ -650,8 +668,8 @@ static cudaError_t launch_bwd(const SparseBwdArgs& a, int32_t* status, cudaStrea
 #undef TW_DX
     trace_mark(s, "sparse_dx");
   }
-  const long items = static_cast<long>(nch) * a.I;
-  ell_weight_grad_kernel<GATED><<<grid_for(items, 8, 16), 256, 0, s>>>(a);
+  const long items = static_cast<long>(nch) * a.I * 2;
+  ell_weight_grad_kernel<GATED><<<grid_for(items, 8, 3), 256, 0, s>>>(a);
   trace_mark(s, "ell_weight_grad");
   return cudaGetLastError();
 }

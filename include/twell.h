@@ -193,7 +193,8 @@ size_t hybrid_ffn_bwd_workspace_size(int T, int d, int I, int R, int backup_cap)
  *   dWg = dg^T x, dWu = du^T x, dWd = h^T dy  (fp32 [I, d], overwritten).
  * The ELL part runs on the CUDA cores with the weight gradients accumulated over
  * the transposed Hybrid; backup rows use tensor-core GEMMs. dWu is ignored when
- * Wu == NULL. */
+ * Wu == NULL. TW_EUNSUPPORTED when T * d / 8 exceeds 2^32 - 1 (token rows are
+ * addressed by 32-bit offsets). */
 tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* Wg,
                          const uint16_t* Wu, const uint16_t* Wd, int T, int d, int I,
                          const tw_hybrid* saved, float l1, uint16_t* dx, float* dWg,
