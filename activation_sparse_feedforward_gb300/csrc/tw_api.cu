@@ -46,7 +46,7 @@ tw_status check_tile_geometry(int T, int I, int W, int C) {
   if (W != 64 && W != 128) return TW_EUNSUPPORTED;
   if (I < 64 || I > 65536 || I % W != 0) return TW_EUNSUPPORTED;
   if (C < 1 || C > W) return TW_EINVAL;
-  if ((I / W) * C > 12288) return TW_EUNSUPPORTED;  // per-warp entry list of the sparse forward
+  if ((I / W) * C > tw::kMaxList) return TW_EUNSUPPORTED;  // per-token entry list of the sparse forward
   return TW_OK;
 }
 
@@ -286,7 +286,7 @@ tw_status twell_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* W
   a.cnt = o.cnt; a.val = o.val; a.idx = o.idx; a.ovf = o.ovf;
   a.backup_slot = nullptr;
   a.y = y;
-  TW_TRY(tw::launch_sparse_fwd(a, dev_status, s));
+  TW_TRY(tw::launch_token_fwd(a, s));
   if (ovf_cap > 0) {
     TW_TRY(tw::launch_gather_rows(x, d, o.ovf_rows, o.n_ovf, ovf_cap, ra, w.X, s));
     TW_TRY(tw::gemm_backup_hidden(w.X, Wg, Wu, ra, o.n_ovf, ovf_cap, d, I, w.H, w.H_lo, nullptr, nullptr,
@@ -340,7 +340,7 @@ tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* 
   a.backup_slot = saved->backup_slot;
   a.ell_idx = saved->ell_idx; a.ell_a = saved->ell_a; a.ell_u = saved->ell_u; a.R = R;
   a.y = y;
-  TW_TRY(tw::launch_sparse_fwd(a, dev_status, s));
+  TW_TRY(tw::launch_token_fwd(a, s));
   if (cap > 0) {
     TW_TRY(tw::launch_gather_rows(x, d, saved->backup_tok, saved->n_backup, cap, ra, w.X, s));
     TW_TRY(tw::gemm_backup_hidden(w.X, Wg, Wu, ra, saved->n_backup, cap, d, I, w.H, w.H_lo, saved->backup_a,
@@ -397,7 +397,7 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
   a.dg = w.dg; a.du = w.du; a.dx = dx;
   a.col_cnt = w.col_cnt; a.col_ptr = w.col_ptr; a.col_cur = w.col_cur; a.csc = w.csc;
   a.dWg = dWg; a.dWu = dWu; a.dWd = dWd;
-  TW_TRY(tw::launch_sparse_bwd(a, dev_status, s));
+  TW_TRY(tw::launch_sparse_bwd(a, s));
   if (cap > 0 && T > 0) {
     TW_TRY(tw::launch_gather_rows(dy, d, saved->backup_tok, saved->n_backup, cap, ra, w.dY, s));
     TW_TRY(tw::launch_gather_rows(x, d, saved->backup_tok, saved->n_backup, cap, ra, w.X, s));

@@ -40,6 +40,10 @@ cudaError_t launch_compact_rows(const uint8_t* ovf, const int32_t* row_nnz, int 
 cudaError_t launch_gather_rows(const uint16_t* src, int d, const int32_t* rows, const int32_t* n, int cap,
                                int rows_alloc, uint16_t* out, cudaStream_t s);
 
+// Largest per-token entry list of the sparse forward, (I / W) * C: two lists of
+// 10 bytes an entry live in one CTA's shared memory.
+constexpr int kMaxList = 10240;
+
 struct SparseFwdArgs {
   const uint16_t *x, *Wu, *Wd;
   int T, d, I, W, C, nT;
@@ -52,10 +56,11 @@ struct SparseFwdArgs {
   uint16_t* ell_a;
   uint16_t* ell_u;
   int R;
-  int L;                          // per-warp entry list capacity: nT * C (<= 12288)
+  int L;                          // per-token entry list capacity: nT * C (<= kMaxList)
   uint16_t* y;
 };
-cudaError_t launch_sparse_fwd(const SparseFwdArgs& a, int32_t* status, cudaStream_t s);
+// TwELL / Hybrid forward of the non-dense rows (tw_token.cu)
+cudaError_t launch_token_fwd(const SparseFwdArgs& a, cudaStream_t s);
 
 struct SparseBwdArgs {
   const uint16_t *dy, *x, *Wg, *Wu, *Wd;
@@ -76,10 +81,12 @@ struct SparseBwdArgs {
   uint4* csc;         // [T * R] column-ordered entry records
   float *dWg, *dWu, *dWd;
 };
-// ELL backward: dh pass (dg, du per entry, column counts), transposed Hybrid, dx
-// pass, weight-gradient pass (dW overwritten; the dense backup part is added
-// afterwards). col_cnt is zeroed here.
-cudaError_t launch_sparse_bwd(const SparseBwdArgs& a, int32_t* status, cudaStream_t s);
+// Token side of the ELL backward (tw_token.cu): dh, dg and du per entry, column
+// counts of the transposed Hybrid (col_cnt must be zero), dx.
+cudaError_t launch_token_bwd(const SparseBwdArgs& a, cudaStream_t s);
+// ELL backward (tw_sparse.cu): zeroes col_cnt, token side, transposed Hybrid,
+// weight gradients (dW overwritten; the dense backup part is added afterwards).
+cudaError_t launch_sparse_bwd(const SparseBwdArgs& a, cudaStream_t s);
 
 // ---------------------------------------------------------------- tw_gemm.cu
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,

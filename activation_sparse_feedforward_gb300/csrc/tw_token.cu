@@ -1,0 +1,434 @@
+// Token-major CUDA-core kernels of the sparse FFN (gist.science explainer, 2.B:
+// "Fused Up/Down Projection" for inference and the training forward, and the
+// hidden-gradient / input-gradient half of "Backpropagation").
+//
+// One CTA per token (a persistent loop over tokens), one warp per 256-wide slice of
+// d: lane l of warp c owns elements [256 c + 8 l, 256 c + 8 l + 8) of every d-vector.
+// Weight-row slices (512 bytes per warp) are gathered straight into registers, eight
+// entries at a time, so no row passes through shared memory. Each token runs two
+// passes over its entries, in windows of kWin entries:
+//
+//   pass A (dot)   every warp forms its slice's partial dot products of eight rows
+//                  with the token's vector slice; a shuffle reduce-scatter leaves
+//                  entry e's warp sum on lanes 4e..4e+3; the CTA adds the slices'
+//                  partials in shared memory;
+//   pass B (axpy)  every warp accumulates its slice of sum_k c_k W[j_k] in fp32.
+//
+//  forward   list = the token's TwELL entries (j, a) in ascending neuron order,
+//            pass A: u = x_t . Wu[j], h = a u (gated; non-gated h = a),
+//            pass B: y_t = sum h Wd[j]; in training the list is also the Hybrid
+//            ELL row (idx, a, u).
+//  backward  list = the token's ELL row (j, a, u),
+//            pass A: dh = dy_t . Wd[j]; dg = dh u + l1 (non-gated: dh + l1), du = dh a,
+//            pass B: dx_t = sum dg Wg[j] + du Wu[j]; also counts every neuron
+//            column for the transposed Hybrid.
+#include <algorithm>
+
+#include "tw_common.cuh"
+#include "tw_internal.h"
+
+namespace tw {
+
+namespace {
+
+constexpr int kGroup = 8;   // entries gathered together by a warp
+constexpr int kWin = 256;   // entries per window (shared-memory partial sums)
+// Resident CTAs per SM: 48 warps at d = 2048 (six CTAs of eight warps, 40 registers
+// a thread). The passes stall on L2 latency between short bursts of arithmetic, so
+// warps, not per-warp loads in flight, are what keeps the gathers streaming.
+__host__ __device__ constexpr int ctas_per_sm(int nch) { return 48 / nch < 32 ? 48 / nch : 32; }
+
+__host__ __device__ constexpr uint32_t rup(uint32_t v, uint32_t m) { return (v + m - 1) / m * m; }
+
+typedef unsigned long long f32x2;
+TW_DEV f32x2 pair(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+TW_DEV float2 unpair(f32x2 v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return make_float2(lo, hi);
+}
+TW_DEV void fma2(f32x2& acc, f32x2 a, f32x2 b) { asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b)); }
+TW_DEV f32x2 widen(uint32_t w) { return pair(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)); }
+
+// eight fp32 accumulators as four packed pairs
+struct Acc8 {
+  f32x2 v[4];
+  TW_DEV void zero() { v[0] = v[1] = v[2] = v[3] = 0ull; }
+  // this += c2 * w over 8 bf16 elements (c2 = {c, c})
+  TW_DEV void axpy(f32x2 c2, const uint4& w) {
+    fma2(v[0], c2, widen(w.x));
+    fma2(v[1], c2, widen(w.y));
+    fma2(v[2], c2, widen(w.z));
+    fma2(v[3], c2, widen(w.w));
+  }
+  TW_DEV uint4 to_bf16() const {
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 p = unpair(v[i]);
+      o[i] = pack_bf16x2(p.x, p.y);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+  }
+};
+
+// x . w over 8 bf16 pairs: Blackwell's mixed-precision FMA (bf16 x bf16 + fp32; the
+// product is exact in fp32, one rounding per step), two chains
+TW_DEV float dot8(const uint4& x, const uint4& w) {
+  float s0 = 0.f, s1 = 0.f;
+  asm("{\n\t"
+      ".reg .b16 x0, x1, x2, x3, x4, x5, x6, x7, w0, w1, w2, w3, w4, w5, w6, w7;\n\t"
+      "mov.b32 {x0, x1}, %2;\n\t"
+      "mov.b32 {x2, x3}, %3;\n\t"
+      "mov.b32 {x4, x5}, %4;\n\t"
+      "mov.b32 {x6, x7}, %5;\n\t"
+      "mov.b32 {w0, w1}, %6;\n\t"
+      "mov.b32 {w2, w3}, %7;\n\t"
+      "mov.b32 {w4, w5}, %8;\n\t"
+      "mov.b32 {w6, w7}, %9;\n\t"
+      "fma.rn.f32.bf16 %0, x0, w0, %0;\n\t"
+      "fma.rn.f32.bf16 %1, x1, w1, %1;\n\t"
+      "fma.rn.f32.bf16 %0, x2, w2, %0;\n\t"
+      "fma.rn.f32.bf16 %1, x3, w3, %1;\n\t"
+      "fma.rn.f32.bf16 %0, x4, w4, %0;\n\t"
+      "fma.rn.f32.bf16 %1, x5, w5, %1;\n\t"
+      "fma.rn.f32.bf16 %0, x6, w6, %0;\n\t"
+      "fma.rn.f32.bf16 %1, x7, w7, %1;\n\t"
+      "}"
+      : "+f"(s0), "+f"(s1)
+      : "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w), "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w));
+  return s0 + s1;
+}
+
+// Warp reduce-scatter of eight per-lane values: on return every lane of the quad
+// 4e..4e+3 holds the warp-wide sum of p[e].
+TW_DEV float reduce8(float (&p)[8], int lane) {
+  const bool b16 = lane & 16, b8 = lane & 8, b4 = lane & 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = b16 ? p[i] : p[i + 4];
+    const float keep = b16 ? p[i + 4] : p[i];
+    p[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = b8 ? p[i] : p[i + 2];
+    const float keep = b8 ? p[i + 2] : p[i];
+    p[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+  }
+  const float send = b4 ? p[0] : p[1];
+  float s = (b4 ? p[1] : p[0]) + __shfl_xor_sync(0xFFFFFFFFu, send, 4);
+  s += __shfl_xor_sync(0xFFFFFFFFu, s, 2);
+  s += __shfl_xor_sync(0xFFFFFFFFu, s, 1);
+  return s;
+}
+
+TW_DEV uint4 ldg16(const uint4* p) { return __ldg(p); }
+
+// Block-wide exclusive scan of one int per thread; *total gets the sum. One
+// __syncthreads, plus a trailing one when `reuse` (scratch is rewritten before the
+// caller's next barrier); scratch holds one int per warp.
+TW_DEV int block_exclusive_scan(int v, int* scratch, int* total, bool reuse) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int incl = warp_inclusive_scan(v);
+  if (lane == 31) scratch[wid] = incl;
+  __syncthreads();
+  int before = 0, all = 0;
+  for (int w = 0; w < nw; ++w) {
+    const int s = scratch[w];
+    before += w < wid ? s : 0;
+    all += s;
+  }
+  if (reuse) __syncthreads();
+  *total = all;
+  return before + incl - v;
+}
+
+// Pass A over the list window [w0, w0 + m): part[k - w0] = this warp's slice of
+// vec . W[j_k] for every k of the window rounded up to kGroup (entries past the list
+// end repeat its last neuron; their sums are never read).
+TW_DEV void pass_dot(const uint4* Wslice, uint32_t row16, const uint16_t* lj, int w0, int m, const uint4& vec,
+                     float* part, int lane) {
+  for (int k0 = 0; k0 < m; k0 += kGroup) {
+    uint4 v[kGroup];
+#pragma unroll
+    for (int q = 0; q < kGroup; ++q) v[q] = ldg16(Wslice + static_cast<uint32_t>(lj[w0 + k0 + q]) * row16);
+    float p[kGroup];
+#pragma unroll
+    for (int q = 0; q < kGroup; ++q) p[q] = dot8(vec, v[q]);
+    const float s = reduce8(p, lane);
+    if ((lane & 3) == 0) part[k0 + (lane >> 2)] = s;
+  }
+}
+
+// shared memory of one token CTA: two buffers of (neuron list | coefficient pairs),
+// partial sums, scan scratch. Lists hold cap entries plus a group of padding.
+__host__ __device__ inline uint32_t token_smem_bytes(int nch, int cap, int ncoef) {
+  const uint32_t lp = rup(static_cast<uint32_t>(cap) + kGroup, kGroup);
+  return 2u * (rup(2u * lp, 16u) + ncoef * 8u * lp) + 4u * nch * kWin + 4u * 33u;
+}
+
+}  // namespace
+
+// ====================================================================== forward
+// Rows served by the dense path (TwELL overflow, Hybrid backup) are skipped. The
+// entry list is built by the CTA: thread k takes TwELL tile k, an exclusive scan of
+// the tiles' counts places their slots, so the list is in ascending neuron order.
+// Lists are double-buffered over tokens, so a token needs no closing barrier: a
+// warp still in the down pass of token t reads the other buffer than token t + 1
+// writes, and token t + 2 writes it only after barriers every warp passes.
+template <int NCH, bool GATED, bool HYBRID>
+__global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_fwd_kernel(const SparseFwdArgs a) {
+  constexpr uint32_t row16 = NCH * 32;  // uint4 per d-row
+  extern __shared__ __align__(16) uint8_t tsm[];
+  const int lane = threadIdx.x & 31, c = threadIdx.x >> 5;
+  const uint32_t lp = rup(static_cast<uint32_t>(a.L) + kGroup, kGroup);
+  const uint32_t list_bytes = rup(2u * lp, 16u) + 8u * lp;
+  float* part = reinterpret_cast<float*>(tsm + 2 * list_bytes);
+  int* scratch = reinterpret_cast<int*>(part + NCH * kWin);
+  const uint4* Wu4 = reinterpret_cast<const uint4*>(a.Wu) + c * 32 + lane;
+  const uint4* Wd4 = reinterpret_cast<const uint4*>(a.Wd) + c * 32 + lane;
+  const bool vec_slots = a.C % 16 == 0;  // a tile's slots load as 16-byte vectors
+  int buf = 0;
+
+  for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
+    const bool skip = HYBRID ? (a.backup_slot[t] != -1) : (a.ovf[t] != 0);
+    if (skip) continue;
+    uint16_t* lj = reinterpret_cast<uint16_t*>(tsm + buf * list_bytes);
+    f32x2* lh = reinterpret_cast<f32x2*>(tsm + buf * list_bytes + rup(2u * lp, 16u));
+    buf ^= 1;
+    const size_t rb = static_cast<size_t>(t) * a.R;
+    // ------------------------------------------------------------ entry list
+    int n = 0, last_pos = -1, last_j = 0;
+    for (int kb = 0; kb < a.nT; kb += blockDim.x) {
+      const int k = kb + threadIdx.x;
+      const int cnt = k < a.nT ? min(static_cast<int>(a.cnt[static_cast<size_t>(t) * a.nT + k]), a.C) : 0;
+      const size_t sb = (static_cast<size_t>(t) * a.nT + k) * a.C;
+      // the tile's first 16 slots, loaded before the scan so the load overlaps it
+      uint4 iv = make_uint4(0u, 0u, 0u, 0u), v0 = iv, v1 = iv;
+      if (vec_slots && cnt > 0) {
+        iv = *reinterpret_cast<const uint4*>(a.idx + sb);
+        v0 = *reinterpret_cast<const uint4*>(a.val + sb);
+        v1 = *reinterpret_cast<const uint4*>(a.val + sb + 8);
+      }
+      int tot;
+      const int off = n + block_exclusive_scan(cnt, scratch, &tot, kb + static_cast<int>(blockDim.x) < a.nT);
+      auto put = [&](int i, int jj, uint16_t ab) {
+        const int j = k * a.W + jj;
+        const float av = bf16_to_f32(ab);
+        lj[off + i] = static_cast<uint16_t>(j);
+        lh[off + i] = pair(av, av);
+        if (HYBRID) {
+          a.ell_idx[rb + off + i] = static_cast<uint16_t>(j);
+          a.ell_a[rb + off + i] = ab;
+        }
+        last_pos = off + i;
+        last_j = j;
+      };
+      if (vec_slots) {
+        const uint32_t iw[4] = {iv.x, iv.y, iv.z, iv.w};
+        const uint32_t vw[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (i < cnt)
+            put(i, static_cast<int>((iw[i >> 2] >> (8 * (i & 3))) & 0xFFu), static_cast<uint16_t>(vw[i >> 1] >> (16 * (i & 1))));
+      }
+      for (int i = vec_slots ? 16 : 0; i < cnt; ++i) put(i, a.idx[sb + i], a.val[sb + i]);
+      n += tot;
+    }
+    if (n > 0 && last_pos == n - 1) {  // the list's last writer pads it to a whole group (zero coefficients)
+#pragma unroll
+      for (int i = 0; i < kGroup; ++i) {
+        lj[n + i] = static_cast<uint16_t>(last_j);
+        lh[n + i] = 0ull;
+      }
+    }
+    const uint4 xs = GATED ? ldg16(reinterpret_cast<const uint4*>(a.x) + static_cast<size_t>(t) * row16 + c * 32 + lane)
+                           : make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    Acc8 y;
+    y.zero();
+    for (int w0 = 0; w0 < n; w0 += kWin) {
+      const int m = min(kWin, n - w0);
+      if (GATED) {
+        // -------------------------------------------------------- up: h = a (x_t . Wu[j])
+        pass_dot(Wu4, row16, lj, w0, m, xs, part + c * kWin, lane);
+        __syncthreads();
+        for (int k = threadIdx.x; k < m; k += blockDim.x) {
+          float u = 0.f;
+#pragma unroll
+          for (int w = 0; w < NCH; ++w) u += part[w * kWin + k];
+          const float h = unpair(lh[w0 + k]).x * u;
+          lh[w0 + k] = pair(h, h);
+          if (HYBRID) a.ell_u[rb + w0 + k] = f32_to_bf16(u);
+        }
+        __syncthreads();
+      }
+      // ---------------------------------------------------------- down: y_t += sum h Wd[j]
+      for (int k0 = 0; k0 < m; k0 += kGroup) {
+        uint4 v[kGroup];
+#pragma unroll
+        for (int q = 0; q < kGroup; ++q) v[q] = ldg16(Wd4 + static_cast<uint32_t>(lj[w0 + k0 + q]) * row16);
+#pragma unroll
+        for (int q = 0; q < kGroup; ++q) y.axpy(lh[w0 + k0 + q], v[q]);
+      }
+    }
+    reinterpret_cast<uint4*>(a.y)[static_cast<size_t>(t) * row16 + c * 32 + lane] = y.to_bf16();
+  }
+}
+
+// ====================================================================== backward
+// Tokens without ELL entries get dx = 0 (backup rows are overwritten by the dense
+// path afterwards). The window lists are double-buffered like the forward's.
+template <int NCH, bool GATED>
+__global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_bwd_kernel(const SparseBwdArgs a) {
+  constexpr uint32_t row16 = NCH * 32;
+  constexpr uint32_t lp = rup(kWin + kGroup, kGroup);
+  constexpr uint32_t list_bytes = rup(2u * lp, 16u) + 2u * 8u * lp;
+  extern __shared__ __align__(16) uint8_t tsm[];
+  const int lane = threadIdx.x & 31, c = threadIdx.x >> 5;
+  float* part = reinterpret_cast<float*>(tsm + 2 * list_bytes);
+  const uint4* Wg4 = reinterpret_cast<const uint4*>(a.Wg) + c * 32 + lane;
+  const uint4* Wu4 = reinterpret_cast<const uint4*>(a.Wu) + c * 32 + lane;
+  const uint4* Wd4 = reinterpret_cast<const uint4*>(a.Wd) + c * 32 + lane;
+  int buf = 0;
+
+  for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
+    const int n = a.ell_nnz[t];
+    const size_t rb = static_cast<size_t>(t) * a.R;
+    const uint4 dys = n > 0 ? ldg16(reinterpret_cast<const uint4*>(a.dy) + static_cast<size_t>(t) * row16 + c * 32 + lane)
+                            : make_uint4(0u, 0u, 0u, 0u);
+    Acc8 dx;
+    dx.zero();
+    for (int w0 = 0; w0 < n; w0 += kWin) {
+      const int m = min(kWin, n - w0);
+      uint16_t* lj = reinterpret_cast<uint16_t*>(tsm + buf * list_bytes);
+      f32x2* lg = reinterpret_cast<f32x2*>(tsm + buf * list_bytes + rup(2u * lp, 16u));  // a, then dg
+      f32x2* lu = lg + lp;                                                                // u, then du
+      buf ^= 1;
+      for (int k = threadIdx.x; k < rup(m, kGroup); k += blockDim.x) {
+        const int e = min(k, m - 1);
+        const int j = a.ell_idx[rb + w0 + e];
+        lj[k] = static_cast<uint16_t>(j);
+        if (k < m) {
+          atomicAdd(a.col_cnt + j, 1);
+          lg[k] = pair(bf16_to_f32(a.ell_a[rb + w0 + k]), 0.f);
+          lu[k] = pair(GATED ? bf16_to_f32(a.ell_u[rb + w0 + k]) : 1.f, 0.f);
+        } else {
+          lg[k] = 0ull;
+          lu[k] = 0ull;
+        }
+      }
+      __syncthreads();
+      // ---------------------------------------------------------- dh = dy_t . Wd[j]
+      pass_dot(Wd4, row16, lj, 0, m, dys, part + c * kWin, lane);
+      __syncthreads();
+      for (int k = threadIdx.x; k < m; k += blockDim.x) {
+        float dh = 0.f;
+#pragma unroll
+        for (int w = 0; w < NCH; ++w) dh += part[w * kWin + k];
+        const float av = unpair(lg[k]).x, uv = unpair(lu[k]).x;
+        const float dg = (GATED ? dh * uv : dh) + a.l1;
+        const float du = dh * av;
+        a.dg[rb + w0 + k] = dg;
+        if (GATED) a.du[rb + w0 + k] = du;
+        lg[k] = pair(dg, dg);
+        lu[k] = pair(du, du);
+      }
+      __syncthreads();
+      // ---------------------------------------------------------- dx_t += dg Wg[j] + du Wu[j]
+      for (int k0 = 0; k0 < m; k0 += kGroup / 2) {
+        uint4 v[kGroup];
+#pragma unroll
+        for (int q = 0; q < kGroup / 2; ++q) {
+          const uint32_t r = static_cast<uint32_t>(lj[k0 + q]) * row16;
+          v[2 * q] = ldg16(Wg4 + r);
+          if (GATED) v[2 * q + 1] = ldg16(Wu4 + r);
+        }
+#pragma unroll
+        for (int q = 0; q < kGroup / 2; ++q) {
+          dx.axpy(lg[k0 + q], v[2 * q]);
+          if (GATED) dx.axpy(lu[k0 + q], v[2 * q + 1]);
+        }
+      }
+    }
+    reinterpret_cast<uint4*>(a.dx)[static_cast<size_t>(t) * row16 + c * 32 + lane] = dx.to_bf16();
+  }
+}
+
+// ====================================================================== launchers
+namespace {
+template <class K>
+cudaError_t set_smem(K kern, size_t bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+}
+int token_grid(int T, int nch) {
+  const int per_sm = ctas_per_sm(nch);
+  return std::max(1, std::min(T, device_sm_count() * per_sm));
+}
+}  // namespace
+
+#define TW_NCH_CASES(CALL) \
+  case 1: CALL(1); break;  \
+  case 2: CALL(2); break;  \
+  case 3: CALL(3); break;  \
+  case 4: CALL(4); break;  \
+  case 5: CALL(5); break;  \
+  case 6: CALL(6); break;  \
+  case 7: CALL(7); break;  \
+  case 8: CALL(8); break;  \
+  default: return cudaErrorInvalidValue;
+
+template <bool GATED, bool HYBRID>
+static cudaError_t token_fwd(const SparseFwdArgs& a, cudaStream_t s) {
+  const int nch = a.d / 256;
+  const size_t smem = token_smem_bytes(nch, a.L, 1);
+  const int grid = token_grid(a.T, nch);
+#define TW_TF(n)                                                            \
+  {                                                                         \
+    cudaError_t e = set_smem(token_fwd_kernel<n, GATED, HYBRID>, smem);     \
+    if (e != cudaSuccess) return e;                                         \
+    token_fwd_kernel<n, GATED, HYBRID><<<grid, n * 32, smem, s>>>(a);       \
+  }
+  switch (nch) { TW_NCH_CASES(TW_TF) }
+#undef TW_TF
+  trace_mark(s, "sparse_fwd");
+  return cudaGetLastError();
+}
+
+cudaError_t launch_token_fwd(const SparseFwdArgs& a, cudaStream_t s) {
+  if (a.T == 0) return cudaSuccess;
+  if (a.L < 1 || a.L > kMaxList) return cudaErrorInvalidValue;
+  const bool gated = a.Wu != nullptr;
+  const bool hybrid = a.backup_slot != nullptr;
+  if (gated) return hybrid ? token_fwd<true, true>(a, s) : token_fwd<true, false>(a, s);
+  return hybrid ? token_fwd<false, true>(a, s) : token_fwd<false, false>(a, s);
+}
+
+template <bool GATED>
+static cudaError_t token_bwd(const SparseBwdArgs& a, cudaStream_t s) {
+  const int nch = a.d / 256;
+  const size_t smem = token_smem_bytes(nch, kWin, 2);
+  const int grid = token_grid(a.T, nch);
+#define TW_TB(n)                                                   \
+  {                                                                \
+    cudaError_t e = set_smem(token_bwd_kernel<n, GATED>, smem);    \
+    if (e != cudaSuccess) return e;                                \
+    token_bwd_kernel<n, GATED><<<grid, n * 32, smem, s>>>(a);      \
+  }
+  switch (nch) { TW_NCH_CASES(TW_TB) }
+#undef TW_TB
+  trace_mark(s, "sparse_bwd_token");
+  return cudaGetLastError();
+}
+
+cudaError_t launch_token_bwd(const SparseBwdArgs& a, cudaStream_t s) {
+  if (a.T == 0) return cudaSuccess;
+  return a.Wu != nullptr ? token_bwd<true>(a, s) : token_bwd<false>(a, s);
+}
+
+}  // namespace tw

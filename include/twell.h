@@ -20,8 +20,9 @@
  *   vector; row j of Wd (W2) is the vector neuron j adds to y. Wu == NULL selects
  *   the non-gated form.
  * - Shapes: T >= 0 tokens; d % 256 == 0 and 256 <= d <= 2048 (the sparse kernels
- *   keep a whole d-vector per warp in registers); W in {64, 128}; I % W == 0,
- *   64 <= I <= 65536; 1 <= C <= W; 1 <= R <= I; 0 <= backup_cap <= T.
+ *   give each warp of a token's CTA one 256-wide slice of d); W in {64, 128};
+ *   I % W == 0, 64 <= I <= 65536; 1 <= C <= W; (I / W) * C <= 10240 (a token's
+ *   entry list lives in shared memory); 1 <= R <= I; 0 <= backup_cap <= T.
  *   T == 0 is a valid no-op. Other shapes return TW_EUNSUPPORTED.
  * - Alignment: every pointer must be 16-byte aligned (TMA and 128-bit accesses).
  * - Ownership: the caller allocates and frees every buffer, including the
