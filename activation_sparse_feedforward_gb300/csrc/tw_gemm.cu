@@ -203,9 +203,9 @@ cudaError_t gemm_weight_grad_add(const uint16_t* P_hi, const uint16_t* P_lo, con
     return cudaErrorInvalidValue;
   maps.b[1] = maps.b[0];
   fill_unused(maps, 2, 2);
-  EpiAddF32::Params ep{D, d};
-  if (d % 256 == 0) return run_gemm<256, true, true, false, 4, EpiAddF32>(maps, sh, ep, I, s, "backup_weight_grad");
-  return run_gemm<64, true, true, false, 8, EpiAddF32>(maps, sh, ep, I, s, "backup_weight_grad");
+  EpiRedF32::Params ep{D, d};
+  if (d % 256 == 0) return run_gemm<256, true, true, false, 4, EpiRedF32>(maps, sh, ep, I, s, "backup_weight_grad");
+  return run_gemm<64, true, true, false, 8, EpiRedF32>(maps, sh, ep, I, s, "backup_weight_grad");
 }
 
 // ------------------------------------------------------------------ layout test GEMM
