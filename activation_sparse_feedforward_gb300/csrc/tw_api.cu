@@ -397,8 +397,9 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
   a.dg = w.dg; a.du = w.du; a.dx = dx;
   a.col_cnt = w.col_cnt; a.col_ptr = w.col_ptr; a.col_cur = w.col_cur; a.csc = w.csc;
   a.dWg = dWg; a.dWu = dWu; a.dWd = dWd;
-  TW_TRY(tw::launch_sparse_bwd(a, s));
-  if (cap > 0 && T > 0) {
+  TW_TRY(tw::launch_sparse_bwd_tokens(a, s));
+  const bool backup = cap > 0 && T > 0;
+  if (backup) {
     TW_TRY(tw::launch_gather_rows(dy, d, saved->backup_tok, saved->n_backup, cap, ra, w.dY, s));
     TW_TRY(tw::launch_gather_rows(x, d, saved->backup_tok, saved->n_backup, cap, ra, w.X, s));
     const int32_t* nb = saved->n_backup;
@@ -410,10 +411,14 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
     const uint16_t* B[4] = {Wg, Wg, Wu, Wu};
     TW_TRY(tw::gemm_rows_times_nmajor_splitk(A, B, gated ? 4 : 2, ra, nb, cap, I, d, w.acc, dev_status, s));
     TW_TRY(tw::launch_scatter_rows_bf16(w.acc, d, nb, cap, saved->backup_tok, dx, d, s));
-    TW_TRY(tw::gemm_weight_grad_add(g.dG, g.dG_lo, w.X, ra, nb, cap, I, d, dWg, dev_status, s));
-    if (gated) TW_TRY(tw::gemm_weight_grad_add(g.dU, g.dU_lo, w.X, ra, nb, cap, I, d, dWu, dev_status, s));
-    TW_TRY(tw::gemm_weight_grad_add(g.H, g.H_lo, w.dY, ra, nb, cap, I, d, dWd, dev_status, s));
+    // the backup rows' weight gradients are written first (when there are any);
+    // the ELL part is then added to them
+    TW_TRY(tw::gemm_weight_grad(g.dG, g.dG_lo, w.X, ra, nb, cap, I, d, dWg, dev_status, s));
+    if (gated) TW_TRY(tw::gemm_weight_grad(g.dU, g.dU_lo, w.X, ra, nb, cap, I, d, dWu, dev_status, s));
+    TW_TRY(tw::gemm_weight_grad(g.H, g.H_lo, w.dY, ra, nb, cap, I, d, dWd, dev_status, s));
   }
+  a.dW_base_rows = backup ? saved->n_backup : nullptr;
+  TW_TRY(tw::launch_sparse_bwd_weights(a, s));
   return TW_OK;
 }
 

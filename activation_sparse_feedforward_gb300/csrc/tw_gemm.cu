@@ -189,9 +189,8 @@ cudaError_t gemm_backup_grad(const uint16_t* dY, const uint16_t* Wd, int rows_al
   return run_gemm<64, false, false, false, 8, EpiBackupGrad<false>>(maps, sh, ep, cap, s, "backup_grad");
 }
 
-cudaError_t gemm_weight_grad_add(const uint16_t* P_hi, const uint16_t* P_lo, const uint16_t* Q, int rows_alloc,
-                                 const int32_t* n_dev, int cap, int I, int d, float* D, int32_t* status,
-                                 cudaStream_t s) {
+cudaError_t gemm_weight_grad(const uint16_t* P_hi, const uint16_t* P_lo, const uint16_t* Q, int rows_alloc,
+                             const int32_t* n_dev, int cap, int I, int d, float* D, int32_t* status, cudaStream_t s) {
   if (cap <= 0) return cudaSuccess;
   GemmShape sh = shape_static(I, d, 0, status);
   sh.k_dev = n_dev;
@@ -203,9 +202,9 @@ cudaError_t gemm_weight_grad_add(const uint16_t* P_hi, const uint16_t* P_lo, con
     return cudaErrorInvalidValue;
   maps.b[1] = maps.b[0];
   fill_unused(maps, 2, 2);
-  EpiRedF32::Params ep{D, d};
-  if (d % 256 == 0) return run_gemm<256, true, true, false, 4, EpiRedF32>(maps, sh, ep, I, s, "backup_weight_grad");
-  return run_gemm<64, true, true, false, 8, EpiRedF32>(maps, sh, ep, I, s, "backup_weight_grad");
+  EpiStoreF32::Params ep{D, d};
+  if (d % 256 == 0) return run_gemm<256, true, true, false, 4, EpiStoreF32>(maps, sh, ep, I, s, "backup_weight_grad");
+  return run_gemm<64, true, true, false, 8, EpiStoreF32>(maps, sh, ep, I, s, "backup_weight_grad");
 }
 
 // ------------------------------------------------------------------ layout test GEMM

@@ -80,13 +80,19 @@ struct SparseBwdArgs {
   int32_t* col_cur;   // [I]
   uint4* csc;         // [T * R] column-ordered entry records
   float *dWg, *dWu, *dWd;
+  // when non-null and *dW_base_rows > 0, dW already holds the dense backup rows'
+  // part and the ELL part is added to it; otherwise dW is overwritten
+  const int32_t* dW_base_rows;
 };
 // Token side of the ELL backward (tw_token.cu): dh, dg and du per entry, column
 // counts of the transposed Hybrid (col_cnt must be zero), dx.
 cudaError_t launch_token_bwd(const SparseBwdArgs& a, cudaStream_t s);
-// ELL backward (tw_sparse.cu): zeroes col_cnt, token side, transposed Hybrid,
-// weight gradients (dW overwritten; the dense backup part is added afterwards).
-cudaError_t launch_sparse_bwd(const SparseBwdArgs& a, cudaStream_t s);
+// ELL backward (tw_sparse.cu), token side: zeroes col_cnt, launch_token_bwd,
+// transposed Hybrid (column pointers and records).
+cudaError_t launch_sparse_bwd_tokens(const SparseBwdArgs& a, cudaStream_t s);
+// ELL backward, column side: weight gradients over the transposed Hybrid (see
+// SparseBwdArgs::dW_base_rows for overwrite / accumulate).
+cudaError_t launch_sparse_bwd_weights(const SparseBwdArgs& a, cudaStream_t s);
 
 // ---------------------------------------------------------------- tw_gemm.cu
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
@@ -126,11 +132,11 @@ cudaError_t gemm_backup_grad(const uint16_t* dY, const uint16_t* Wd, int rows_al
                              int d, int I, const float* a, const float* u, float l1, const BackupGradOut& o,
                              int32_t* status, cudaStream_t s);
 
-// D[I, d] += (P_hi + P_lo)^T Q with P [rows_alloc, I] and Q [rows_alloc, d] (both
-// stored with the reduction over rows), K = n (device) rows, up to cap.
-cudaError_t gemm_weight_grad_add(const uint16_t* P_hi, const uint16_t* P_lo, const uint16_t* Q, int rows_alloc,
-                                 const int32_t* n_dev, int cap, int I, int d, float* D, int32_t* status,
-                                 cudaStream_t s);
+// D[I, d] = (P_hi + P_lo)^T Q with P [rows_alloc, I] and Q [rows_alloc, d] (both
+// stored with the reduction over rows), K = n (device) rows, up to cap. Writes
+// nothing when n == 0.
+cudaError_t gemm_weight_grad(const uint16_t* P_hi, const uint16_t* P_lo, const uint16_t* Q, int rows_alloc,
+                             const int32_t* n_dev, int cap, int I, int d, float* D, int32_t* status, cudaStream_t s);
 
 cudaError_t gemm_dense_test(const uint16_t* A, const uint16_t* B, int M, int N, int K, int a_mn, int b_mn, float* D,
                             int32_t* status, cudaStream_t s);

@@ -62,6 +62,18 @@ TW_DEV void stcs_f32x8(float* p, const F8& y) {
   __stcs(reinterpret_cast<float4*>(p), make_float4(a.x, a.y, b.x, b.y));
   __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(c.x, c.y, d.x, d.y));
 }
+// y added into p with fp32 vector reductions (the L2 does the adds; no round trip)
+TW_DEV void red_f32x8(float* p, const F8& y) {
+  const float2 a = f2_split(y.v[0]), b = f2_split(y.v[1]), c = f2_split(y.v[2]), d = f2_split(y.v[3]);
+  atomicAdd(reinterpret_cast<float4*>(p), make_float4(a.x, a.y, b.x, b.y));
+  atomicAdd(reinterpret_cast<float4*>(p) + 1, make_float4(c.x, c.y, d.x, d.y));
+}
+TW_DEV void out_f32x8(float* p, const F8& y, bool add) {
+  if (add)
+    red_f32x8(p, y);
+  else
+    stcs_f32x8(p, y);
+}
 TW_DEV uint4 ldg16(const uint4* p) { return __ldg(p); }
 int grid_for(long items, int per_block, int blocks_per_sm) {
   const long blocks = (items + per_block - 1) / per_block;
@@ -129,7 +141,8 @@ __global__ void __launch_bounds__(256) csc_fill_kernel(const SparseBwdArgs a) {
 //   dWg[j] += dg x_t,  dWu[j] += du x_t   (gated)
 // and the dy side
 //   dWd[j] += h dy_t,  h = a u (non-gated: a)
-// (fp32, overwritten, streaming stores); splitting the sides halves the registers a
+// (fp32; streaming stores, or reductions into dW when it already holds the dense
+// backup rows' part); splitting the sides halves the registers a
 // warp needs, so more warps and more row slices are in flight per SM. Lane l owns 8
 // columns of the slice. The column's records are staged 32 at a time in the warp's
 // shared memory with the coefficients already paired for the packed FMA
@@ -146,6 +159,8 @@ __global__ void __launch_bounds__(256, 3) ell_weight_grad_kernel(const SparseBwd
   const int wpb = blockDim.x >> 5;
   float4(&cgu)[32] = stage[warp][0];
   float4(&chr)[32] = stage[warp][1];
+  // dW already holds the dense backup rows' part when there are backup rows
+  const bool add = a.dW_base_rows != nullptr && *a.dW_base_rows > 0;
   const int items = (a.d / 256) * a.I * 2;
   for (int it = blockIdx.x * wpb + warp; it < items; it += gridDim.x * wpb) {
     const bool xside = (it & 1) == 0;
@@ -196,20 +211,19 @@ __global__ void __launch_bounds__(256, 3) ell_weight_grad_kernel(const SparseBwd
     }
     const size_t o = static_cast<size_t>(j) * a.d + c * 256 + lane * 8;
     if (xside) {
-      stcs_f32x8(a.dWg + o, p);
-      if (GATED) stcs_f32x8(a.dWu + o, q2);
+      out_f32x8(a.dWg + o, p, add);
+      if (GATED) out_f32x8(a.dWu + o, q2, add);
     } else {
-      stcs_f32x8(a.dWd + o, p);
+      out_f32x8(a.dWd + o, p, add);
     }
   }
 }
 
 // ====================================================================== launchers
 template <bool GATED>
-static cudaError_t launch_bwd(const SparseBwdArgs& a, cudaStream_t s) {
+static cudaError_t token_side(const SparseBwdArgs& a, cudaStream_t s) {
   cudaError_t e = memset_async(a.col_cnt, 0, sizeof(int32_t) * (a.I + 1), s);
   if (e != cudaSuccess) return e;
-  const int nch = a.d / 256;
   e = launch_token_bwd(a, s);  // dh, dg, du, column counts, dx
   if (e != cudaSuccess) return e;
   csc_scan_kernel<<<1, 1024, 0, s>>>(a.col_cnt, a.I, a.col_ptr, a.col_cur);
@@ -218,15 +232,21 @@ static cudaError_t launch_bwd(const SparseBwdArgs& a, cudaStream_t s) {
     csc_fill_kernel<GATED><<<grid_for(a.T, 8, 8), 256, 0, s>>>(a);
     trace_mark(s, "csc_fill");
   }
-  const long items = static_cast<long>(nch) * a.I * 2;
-  ell_weight_grad_kernel<GATED><<<grid_for(items, 8, 3), 256, 0, s>>>(a);
-  trace_mark(s, "ell_weight_grad");
   return cudaGetLastError();
 }
 
-cudaError_t launch_sparse_bwd(const SparseBwdArgs& a, cudaStream_t s) {
-  if (a.Wu != nullptr) return launch_bwd<true>(a, s);
-  return launch_bwd<false>(a, s);
+cudaError_t launch_sparse_bwd_tokens(const SparseBwdArgs& a, cudaStream_t s) {
+  return a.Wu != nullptr ? token_side<true>(a, s) : token_side<false>(a, s);
+}
+
+cudaError_t launch_sparse_bwd_weights(const SparseBwdArgs& a, cudaStream_t s) {
+  const long items = static_cast<long>(a.d / 256) * a.I * 2;
+  if (a.Wu != nullptr)
+    ell_weight_grad_kernel<true><<<grid_for(items, 8, 3), 256, 0, s>>>(a);
+  else
+    ell_weight_grad_kernel<false><<<grid_for(items, 8, 3), 256, 0, s>>>(a);
+  trace_mark(s, "ell_weight_grad");
+  return cudaGetLastError();
 }
 
 }  // namespace tw

@@ -110,6 +110,23 @@ def test_hybrid_forward_backward_match_oracle(spec, l1):
     assert 0 < nb <= spec.T // 4
 
 
+@pytest.mark.parametrize("backup_cap", [0, 64])
+def test_hybrid_without_backup_rows(backup_cap):
+    """No row needs the dense backup: the weight gradients come from the ELL pass
+    alone, whether or not backup capacity exists."""
+    spec = FFNSpec("no_backup", T=200, d=512, I=768, mean_active=6, outlier_frac=0.0, W=64, C=12, R=96, seed=9)
+    inp = make_inputs(spec, with_dy=True)
+    h, y, (dx, dWg, dWu, dWd) = _run_hybrid(spec, inp, backup_cap=backup_cap)
+    assert int(h.saved.n_backup.item()) == 0
+    f = ffn.forward(inp["x"], inp["Wg"], inp["Wu"], inp["Wd"])
+    b = ffn.backward(inp["x"], inp["Wg"], inp["Wu"], inp["Wd"], inp["dy"], spec.l1, fwd=f)
+    assert_close(f64_of(y), f["y"], "y")
+    assert_close(f64_of(dx), b["dx"], "dx")
+    assert_close(dWg.cpu().numpy(), b["dWg"], "dWg")
+    assert_close(dWu.cpu().numpy(), b["dWu"], "dWu")
+    assert_close(dWd.cpu().numpy(), b["dWd"], "dWd")
+
+
 def test_hybrid_l1_only_gradient_closed_form():
     """dy = 0, l1 = 1: dWg[j] = sum of x_t over tokens where neuron j fires,
     dx_t = sum of Wg[j] over the neurons token t fires, dWu = dWd = 0."""
