@@ -9,7 +9,7 @@ pages' 1.5B-model FFN shape (see synthetic/workloads.py for the recipe).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--tokens T] [--no-cpu-baseline]
-                    [--no-dense] [--no-inference] [--sweep]
+                    [--no-dense] [--no-inference] [--no-stack] [--sweep]
 
 Prints ONE JSON line (rank 0). Timing: W untimed warm-up steps, then K steps each
 bracketed by CUDA events on the launching stream with a 256 MiB L2 flush between
@@ -183,6 +183,26 @@ def kernel_work(label: str, spec, stats: dict) -> tuple[str, float] | None:
     return None
 
 
+# L2 bandwidth the row gathers can reach: ncu reports lts__throughput at 47-54 % while
+# the token kernels move 11.5-13.1 TB/s of L2 sectors, i.e. 100 % = 24.2 TB/s (both
+# kernels agree to 0.3 %); see profiles/token_kernels_train_d2048_i5632_m29_o1.md.
+L2_GATHER_PEAK_GBS = 24200.0
+
+
+def gathered_bytes(label: str, spec, stats: dict) -> float | None:
+    """Row-slice bytes a gather kernel must pull through L2 per launch: every ELL entry
+    costs whole d-rows of the matrices it touches."""
+    row = spec.d * 2
+    e = stats["nnz_ell"]
+    if label == "sparse_fwd":
+        return float((2 if spec.gated else 1) * e * row)
+    if label == "sparse_bwd_token":
+        return float((3 if spec.gated else 2) * e * row)
+    if label == "ell_weight_grad":
+        return float(2 * e * row)
+    return None
+
+
 # ------------------------------------------------------------------ oracle timing (CPU)
 def oracle_sample_time(spec, inp, n_tokens: int) -> tuple[float, int, str]:
     """Time the fp64 oracle (as it stands) over the whole hot path for a sample of
@@ -286,6 +306,86 @@ def measure_sweep(dev, flush, stream, steps: int) -> list:
     return rows
 
 
+def measure_stack(dev, flush, stream, steps: int, n_layers: int = 28, T: int = 8192) -> dict:
+    """The 28-layer residual stack x_{l+1} = x_l + FFN_l(x_l) at the 1.5B shape, with the
+    per-layer activity profile: forward alone and forward + backward (the backward
+    carries g_l = g_{l+1} + dx_l down the stack), next to the same stack in dense bf16
+    torch (cuBLAS + autograd, same L1 term). The residual adds are bf16 torch adds in
+    both; every FFN step of the sparse stack runs in the library."""
+    import numpy as np
+    import torch
+
+    import activation_sparse_feedforward_gb300 as tw
+    from synthetic import make_stack, stack_layer_spec
+
+    def to_dev(b):
+        return torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    specs = [stack_layer_spec(l, T=T) for l in range(n_layers)]
+    st = make_stack(specs)
+    Ws = [{k: to_dev(v) for k, v in w.items()} for w in st["layers"]]
+    x0, dyt = to_dev(st["x0"]), to_dev(st["dy"])
+    cap = min(T, 128 * int(math.ceil(1.5 * 0.01 * T / 128.0)) + 128)
+    ffns = [tw.HybridFFN(T, sp.d, sp.I, sp.W, sp.C, sp.R, cap, gated=True, device=dev) for sp in specs]
+    xs = [None] * n_layers
+
+    def fwd():
+        x = x0
+        for l in range(n_layers):
+            xs[l] = x
+            x = x + ffns[l].forward(x, Ws[l]["Wg"], Ws[l]["Wu"], Ws[l]["Wd"])
+        return x
+
+    def bwd():
+        g = dyt
+        for l in reversed(range(n_layers)):
+            g = g + ffns[l].backward(g, xs[l], Ws[l]["Wg"], Ws[l]["Wu"], Ws[l]["Wd"], specs[l].l1)[0]
+        return g
+
+    def train():
+        fwd()
+        bwd()
+
+    ms_f = _time_steps(fwd, steps, 3, flush, stream)
+    ms_t = _time_steps(train, steps, 3, flush, stream)
+    for l, f in enumerate(ffns):
+        tw.raise_if_device_error(f.status, f"stack layer {l}")
+    out = {"layers": n_layers, "tokens": T, "fwd_tokens_per_ms": T / ms_f, "train_tokens_per_ms": T / ms_t,
+           "fwd_ms": ms_f, "train_ms": ms_t,
+           "n_backup": [int(f.saved.n_backup.item()) for f in ffns],
+           "nnz_per_token": [round(float(f.saved.row_nnz.float().mean().item()), 2) for f in ffns]}
+    del ffns, xs
+    torch.cuda.empty_cache()
+
+    # dense bf16 stack on the same weights
+    P = [{k: w.detach().clone().requires_grad_(True) for k, w in W.items()} for W in Ws]
+    l1 = specs[0].l1
+
+    def dense_fwd(keep):
+        x, acts = x0, []
+        for W in P:
+            a = torch.relu(x @ W["Wg"].T)
+            acts.append(a)
+            x = x + (a * (x @ W["Wu"].T)) @ W["Wd"]
+        return x, acts
+
+    def dense_fwd_only():
+        with torch.no_grad():
+            dense_fwd(False)
+
+    def dense_train():
+        y, acts = dense_fwd(True)
+        torch.autograd.backward([y] + acts, [dyt] + [torch.full_like(a, l1) for a in acts])
+        for W in P:
+            for w in W.values():
+                w.grad = None
+
+    out["dense_fwd_tokens_per_ms"] = T / _time_steps(dense_fwd_only, steps, 3, flush, stream)
+    out["dense_train_tokens_per_ms"] = T / _time_steps(dense_train, steps, 3, flush, stream)
+    out["dense_impl"] = "torch bf16 matmul + autograd (cuBLAS)"
+    return out
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args, dist: Dist) -> dict | None:
     import numpy as np
@@ -332,20 +432,18 @@ def run_ours(args, dist: Dist) -> dict | None:
     arr = (ctypes.c_void_p * len(tev))(*[e.cuda_event for e in tev])
     L = tw.load()
 
+    # ---- headline: K steps, L2 flushed (untimed) before each, no trace events
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     clocks = ClockSampler(dist.local_rank)
     dist.barrier()
     torch.cuda.synchronize(dev)
     clocks.start()
-    _lib_check = L.tw_trace_begin(arr, len(tev))
-    assert _lib_check == 0
     for i in range(args.steps):
         flush.zero_()
         starts[i].record(stream)
         step()
         ends[i].record(stream)
-    n_ev = L.tw_trace_end()
     torch.cuda.synchronize(dev)
     dist.barrier()
     clk = clocks.stop()
@@ -355,6 +453,29 @@ def run_ours(args, dist: Dist) -> dict | None:
     ms_per_step = total_ms / args.steps
     value = spec.T * dist.world * args.steps / total_ms
 
+    # ---- warm L2: the same K steps back to back
+    ws_, we_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    ws_.record(stream)
+    for i in range(args.steps):
+        step()
+    we_.record(stream)
+    torch.cuda.synchronize(dev)
+    warm_ms = dist.max(ws_.elapsed_time(we_), dev)
+    warm = {"value": spec.T * dist.world * args.steps / warm_ms, "ms_per_step": warm_ms / args.steps,
+            "l2": "no flush between steps"}
+
+    # ---- kernel trace: K more flushed steps with an event after every library launch
+    tstarts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    assert L.tw_trace_begin(arr, len(tev)) == 0
+    for i in range(args.steps):
+        flush.zero_()
+        tstarts[i].record(stream)
+        step()
+    n_ev = L.tw_trace_end()
+    torch.cuda.synchronize(dev)
+    tw.raise_if_device_error(h.status, "traced steps")
+
     # per-kernel durations: event i ends launch i; the step's start event precedes launch 0
     labels = [L.tw_trace_label(i).decode() for i in range(n_ev)]
     if n_ev % args.steps != 0 or n_ev == len(tev):
@@ -363,7 +484,7 @@ def run_ours(args, dist: Dist) -> dict | None:
     per_kernel: dict[str, list[float]] = {}
     launches = 0
     for i in range(args.steps):
-        prev = starts[i]
+        prev = tstarts[i]
         for k in range(i * per_step, (i + 1) * per_step):
             per_kernel.setdefault(labels[k], []).append(prev.elapsed_time(tev[k]))
             launches += labels[k] != "memset"
@@ -393,6 +514,16 @@ def run_ours(args, dist: Dist) -> dict | None:
             b, w = kw
             v["bound"] = b
             v["achieved"] = (w / (v["avg_us"] * 1e-6)) / (1e12 if b == "tensor" else 1e9)
+        gb = gathered_bytes(lab, spec, stats)
+        if gb:
+            v["l2_gather_gbs"] = gb / (v["avg_us"] * 1e-6) / 1e9
+            v["l2_gather_frac"] = v["l2_gather_gbs"] / L2_GATHER_PEAK_GBS
+    gb = gathered_bytes(dom, spec, stats)
+    if gb:
+        # what actually bounds a gather kernel: row slices through L2
+        roofline["l2_gather"] = {"achieved": gb / avg_s / 1e9, "peak": L2_GATHER_PEAK_GBS, "unit": "GB/s",
+                                 "frac": gb / avg_s / 1e9 / L2_GATHER_PEAK_GBS, "bytes": gb,
+                                 "peak_source": "derived from ncu lts__throughput (100 % = 24.2 TB/s)"}
 
     # step roofline: slower of (gate + backup + sparse FLOPs at tensor peak) and
     # (algorithmic bytes at HBM peak)
@@ -461,9 +592,27 @@ def run_ours(args, dist: Dist) -> dict | None:
         dense = {"value": spec.T * max(3, args.steps // 2) / ds.elapsed_time(de), "unit": UNIT,
                  "impl": "torch bf16 matmul + autograd (cuBLAS)"}
 
+    # memory one layer's training step holds beyond x, dy and the weights: for the
+    # library, everything HybridFFN preallocates (saved Hybrid, workspaces, y, dx, dW);
+    # for dense torch, the peak its forward + backward allocates
+    def nbytes(o):
+        return sum(t.numel() * t.element_size() for t in vars(o).values() if isinstance(t, torch.Tensor))
+    ours_bytes = nbytes(h) + nbytes(h.saved)
+    memory = {"hybrid_saved_bytes": nbytes(h.saved), "layer_bytes": ours_bytes,
+              "dense_saved_bytes_bf16_a_u": 2 * spec.T * spec.I * 2}
+    if dense is not None:
+        torch.cuda.synchronize(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        m0 = torch.cuda.memory_allocated(dev)
+        dense_step()
+        torch.cuda.synchronize(dev)
+        memory["dense_step_peak_bytes"] = torch.cuda.max_memory_allocated(dev) - m0
+        memory["layer_bytes_vs_dense"] = ours_bytes / memory["dense_step_peak_bytes"]
+
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "ms_per_step_median": statistics.median(step_ms),
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": spec.name, "tokens": spec.T, "d": spec.d, "I": spec.I, "gated": spec.gated,
                    "mean_active": spec.mean_active, "outlier_frac": spec.outlier_frac, "W": spec.W, "C": spec.C,
@@ -480,11 +629,15 @@ def run_ours(args, dist: Dist) -> dict | None:
                     for k_, v in sorted(kernels.items(), key=lambda kv: -kv[1]["total_ms"])},
         "clocks": clk,
         "dense_bf16": dense,
+        "warm_l2": warm,
+        "memory": memory,
     }
     if not args.no_inference:
         line["inference"] = measure_inference(dev, flush, stream, max(3, args.steps // 2))
     if args.sweep:
         line["sweep"] = measure_sweep(dev, flush, stream, max(3, args.steps // 4))
+    if not args.no_stack:
+        line["stack"] = measure_stack(dev, flush, stream, 3)
     if dist.rank == 0 and not args.no_cpu_baseline:
         n_s = args.cpu_sample_tokens
         dt, cores, sample = oracle_sample_time(spec, inp, n_s)
@@ -531,6 +684,7 @@ def main():
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-inference", action="store_true", help="skip the TwELL inference forward figures")
     ap.add_argument("--sweep", action="store_true", help="also time the training sparsity sweep")
+    ap.add_argument("--no-stack", action="store_true", help="skip the 28-layer residual stack figures")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the workload's token count (small cases for profiler captures)")
     ap.add_argument("--cpu-sample-tokens", type=int, default=2048)

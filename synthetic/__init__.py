@@ -5,6 +5,7 @@ from .workloads import (  # noqa: F401
     bf16_bits_to_float32,
     make_dy,
     make_inputs,
+    make_stack,
     make_weights,
     make_x,
     outlier_rows,

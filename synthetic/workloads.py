@@ -127,10 +127,37 @@ for _m in (29, 108, 911):
                                 W=128, C=16, R=_sweep_R(_m), l1=2e-5, cfg_id=4)
 
 
-def stack_layer_spec(layer: int, T: int = 8192, seed: int = 0) -> FFNSpec:
-    m = stack_layer_mean_active(layer)
-    return FFNSpec(f"stack28_l{layer}", T=T, d=2048, I=5632, mean_active=m,
-                   outlier_frac=0.01, W=128, C=16, R=_sweep_R(m), cfg_id=5, seed=seed)
+def stack_layer_spec(layer: int, T: int = 8192, seed: int = 0, d: int = 2048, I: int = 5632, W: int = 128,
+                     C: int = 16, profile_layer: int | None = None) -> FFNSpec:
+    """Layer `layer` of the residual stack workload. Its mean actives follow the
+    28-layer profile at `profile_layer` (default: the same index), scaled by I / 5632
+    for narrower test shapes."""
+    m = stack_layer_mean_active(layer if profile_layer is None else profile_layer) * I / 5632.0
+    return FFNSpec(f"stack28_l{layer}", T=T, d=d, I=I, mean_active=m,
+                   outlier_frac=0.01, W=W, C=C, R=_sweep_R(m), cfg_id=5, seed=seed)
+
+
+STACK_WD_SCALE = 1.0 / 16.0
+
+
+def make_stack(specs: list[FFNSpec]) -> dict:
+    """Inputs of a residual stack x_{l+1} = x_l + FFN_l(x_l): the first layer's x (with
+    its outlier tokens), every layer's weights, and the gradient arriving at the top.
+    Column 0 of every Wd is zero, so feature 0 of the residual stream stays exactly 1
+    and each layer's bias (Wg[:, 0]) keeps its meaning. Wd is scaled by 1/16
+    (variance 1/(256 I)): a gated FFN is quadratic in its input, and without the
+    branch scaling the outlier tokens (3x inputs) grow without bound within a few
+    layers; with it their |x| stays below ~13 over 28 layers while the ordinary
+    tokens' residual stream keeps unit variance."""
+    layers = []
+    for l, sp in enumerate(specs):
+        w = make_weights(sp, l)
+        wd = bf16_bits_to_float32(w["Wd"]) * np.float32(STACK_WD_SCALE)
+        wd[:, 0] = 0.0
+        w["Wd"] = round_to_bf16_bits(wd)
+        layers.append(w)
+    return {"x0": make_x(specs[0], 0), "outliers": outlier_rows(specs[0], 0), "layers": layers,
+            "dy": make_dy(specs[-1], len(specs) - 1)}
 
 
 def _rng(spec: FFNSpec, layer: int, tid: int) -> np.random.Generator:

@@ -56,3 +56,28 @@ def test_mean_actives_match_closed_form(name, T):
     if out.size:
         p_out = _expected_active_fraction(spec, scale=spec.outlier_scale)
         assert abs(act[out].mean() - p_out * spec.I) < 0.15 * p_out * spec.I + 10
+
+
+def test_stack_generator_structure_and_profile():
+    """The residual stack: Wd column 0 is zero (feature 0 of the stream stays 1), Wd is
+    the layer's N(0, 1/I) draw scaled by 1/16, and the ordinary tokens' activity follows
+    the 28-layer profile through the residual stream (checked over three layers)."""
+    from synthetic import make_stack, round_to_bf16_bits, stack_layer_mean_active, stack_layer_spec
+
+    profile = (0, 9, 27)
+    specs = [stack_layer_spec(l, T=512, d=512, I=1408, W=64, C=16, profile_layer=p)
+             for l, p in enumerate(profile)]
+    st = make_stack(specs)
+    ordinary = np.setdiff1d(np.arange(512), st["outliers"])
+    x = st["x0"]
+    for l, (sp, w) in enumerate(zip(specs, st["layers"])):
+        wd = bf16_bits_to_float32(w["Wd"])
+        assert (wd[:, 0] == 0).all()
+        assert abs(wd[:, 1:].std() * 16 * math.sqrt(sp.I) - 1) < 0.02
+        assert sp.mean_active == stack_layer_mean_active(profile[l]) * sp.I / 5632
+        f = ffn.forward(x, w["Wg"], w["Wu"], w["Wd"])
+        act = (f["g"] > 0).sum(1)[ordinary].mean()
+        assert abs(act - sp.mean_active) < 0.15 * sp.mean_active + 1, (l, act, sp.mean_active)
+        y = round_to_bf16_bits(np.asarray(f["y"], dtype=np.float32))
+        x = round_to_bf16_bits(bf16_bits_to_float32(x) + bf16_bits_to_float32(y))
+        assert (bf16_bits_to_float32(x)[:, 0] == 1.0).all()
