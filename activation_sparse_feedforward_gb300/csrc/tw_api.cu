@@ -223,8 +223,7 @@ tw_status twell_pack(const uint16_t* A, int T, int I, int W, int C, const tw_twe
 static tw_status gate_pack_impl(const uint16_t* x, const uint16_t* Wg, int T, int d, int I, int W, int C,
                                 const tw_twell& o, uint16_t* a_dense, int cap_check, int32_t* dev_status,
                                 cudaStream_t s, bool list_overflow = true) {
-  TW_TRY(tw::memset_async(o.row_nnz, 0, sizeof(int32_t) * T, s));
-  TW_TRY(tw::memset_async(o.ovf, 0, static_cast<size_t>(T), s));
+  TW_TRY(tw::launch_zero(o.row_nnz, sizeof(int32_t) * T, o.ovf, static_cast<size_t>(T), s));
   TW_TRY(tw::gemm_gate_pack(x, Wg, T, d, I, W, C, o, a_dense, dev_status, s));
   if (list_overflow)
     TW_TRY(tw::launch_compact_rows(o.ovf, nullptr, 0, T, o.ovf_rows, T, o.n_ovf, nullptr, nullptr, cap_check,

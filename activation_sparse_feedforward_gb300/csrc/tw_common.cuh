@@ -23,6 +23,15 @@
 namespace tw {
 
 // ------------------------------------------------------------------ status
+// Programmatic dependent launch: wait until the grids this one depends on have
+// completed and their writes are visible; then let the next grid start its launch.
+TW_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+TW_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+TW_DEV void pdl_enter() {
+  pdl_wait();
+  pdl_trigger();
+}
+
 TW_DEV void raise_status(int32_t* status, int code) {
   if (status != nullptr) atomicMax(status, code);
 }

@@ -59,9 +59,9 @@ static cudaError_t run_gemm(const GemmMaps& maps, const GemmShape& sh, const typ
   const long tiles = static_cast<long>((max_rows + GEMM_BM - 1) / GEMM_BM) * (sh.N / BN);
   if (tiles <= 0) return cudaSuccess;
   const int grid = static_cast<int>(std::min<long>(tiles, device_sm_count()));
-  kern<<<grid, GEMM_THREADS, Tr::SMEM_BYTES, s>>>(maps, sh, ep);
+  e = launch(kern, dim3(grid), dim3(GEMM_THREADS), Tr::SMEM_BYTES, s, maps, sh, ep);
   trace_mark(s, label);
-  return cudaGetLastError();
+  return e;
 }
 
 static GemmShape shape_static(int M, int N, int K, int32_t* status) {
@@ -148,7 +148,7 @@ cudaError_t gemm_rows_times_nmajor_splitk(const uint16_t* const* A, const uint16
                                           int32_t* status, cudaStream_t s) {
   if (cap <= 0) return cudaSuccess;
   if (segments < 1 || segments > GEMM_MAX_SEGMENTS || N % 256 != 0) return cudaErrorInvalidValue;
-  cudaError_t e = memset_async(acc, 0, sizeof(float) * static_cast<size_t>(cap) * N, s);
+  cudaError_t e = launch_zero(acc, sizeof(float) * static_cast<size_t>(cap) * N, nullptr, 0, s);
   if (e != cudaSuccess) return e;
   GemmShape sh = shape_static(0, N, K, status);
   sh.m_dev = n_dev;

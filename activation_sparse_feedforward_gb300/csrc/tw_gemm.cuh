@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_enter();  // the setup above overlaps the previous kernel's tail
 
   int M = shape.M;
   if (shape.m_dev != nullptr) M = min(max(*shape.m_dev, 0), shape.m_cap);

@@ -19,8 +19,27 @@ int trace_end();
 const char* trace_label(int i);
 void trace_mark(cudaStream_t s, const char* label);
 
-// cudaMemsetAsync followed by a trace mark
-cudaError_t memset_async(void* p, int v, size_t bytes, cudaStream_t s);
+// Zeroes [p0, p0 + b0) and [p1, p1 + b1) (16-byte aligned starts, any sizes; p1 may
+// be null) with one kernel, followed by a trace mark.
+cudaError_t launch_zero(void* p0, size_t b0, void* p1, size_t b1, cudaStream_t s);
+
+// Every library kernel is launched with programmatic stream serialization: it may
+// start (and run its prologue) while the kernel before it on the stream finishes,
+// and it calls pdl_wait() (griddepcontrol.wait) before touching global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
 
 // ---------------------------------------------------------------- tw_kernels.cu
 // Dense bf16 [T, I] -> TwELL counts/slots/row_nnz/ovf (not the overflow list).

@@ -55,9 +55,29 @@ void trace_mark(cudaStream_t s, const char* label) {
   if (g_trace.n < kTraceLabels) g_trace.labels[g_trace.n] = label;
   ++g_trace.n;
 }
-cudaError_t memset_async(void* p, int v, size_t bytes, cudaStream_t s) {
-  cudaError_t e = cudaMemsetAsync(p, v, bytes, s);
-  trace_mark(s, "memset");
+// ---------------------------------------------------------------- zero fill
+// Zeroes two byte ranges (16-byte aligned starts): 16-byte stores, then the tails
+// byte by byte.
+__global__ void __launch_bounds__(256) zero_kernel(uint8_t* __restrict__ p0, size_t b0, uint8_t* __restrict__ p1,
+                                                  size_t b1) {
+  pdl_enter();
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  const size_t i0 = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const size_t n0 = b0 / 16, n1 = b1 / 16;
+  for (size_t i = i0; i < n0; i += stride) reinterpret_cast<uint4*>(p0)[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (size_t i = i0; i < n1; i += stride) reinterpret_cast<uint4*>(p1)[i] = make_uint4(0u, 0u, 0u, 0u);
+  if (i0 < b0 % 16) p0[n0 * 16 + i0] = 0;
+  if (i0 < b1 % 16) p1[n1 * 16 + i0] = 0;
+}
+
+cudaError_t launch_zero(void* p0, size_t b0, void* p1, size_t b1, cudaStream_t s) {
+  if (p1 == nullptr) b1 = 0;
+  if (b0 == 0 && b1 == 0) return cudaSuccess;
+  const size_t most = std::max(std::max(b0, b1) / 16, static_cast<size_t>(16));
+  const int grid = static_cast<int>(std::min<size_t>((most + 255) / 256, static_cast<size_t>(device_sm_count()) * 4));
+  cudaError_t e = launch(zero_kernel, dim3(std::max(grid, 1)), dim3(256), 0, s, static_cast<uint8_t*>(p0), b0,
+                         static_cast<uint8_t*>(p1), b1);
+  trace_mark(s, "zero");
   return e;
 }
 
@@ -76,6 +96,7 @@ __global__ void __launch_bounds__(256) pack_dense_kernel(const uint16_t* __restr
                                                          uint16_t* __restrict__ cnt, uint16_t* __restrict__ val,
                                                          uint8_t* __restrict__ idx, int32_t* __restrict__ row_nnz,
                                                          uint8_t* __restrict__ ovf) {
+  pdl_enter();
   constexpr int W = 32 * VPL;
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
@@ -125,12 +146,12 @@ cudaError_t launch_pack_dense(const uint16_t* A, int T, int I, int W, int C, con
   if (T == 0) return cudaSuccess;
   const int nT = I / W;
   const int grid = warp_grid(T, 8);
-  if (W == 128)
-    pack_dense_kernel<4><<<grid, 256, 0, s>>>(A, T, I, C, nT, o.cnt, o.val, o.idx, o.row_nnz, o.ovf);
-  else
-    pack_dense_kernel<2><<<grid, 256, 0, s>>>(A, T, I, C, nT, o.cnt, o.val, o.idx, o.row_nnz, o.ovf);
+  cudaError_t e = (W == 128) ? launch(pack_dense_kernel<4>, dim3(grid), dim3(256), 0, s, A, T, I, C, nT, o.cnt, o.val,
+                                      o.idx, o.row_nnz, o.ovf)
+                             : launch(pack_dense_kernel<2>, dim3(grid), dim3(256), 0, s, A, T, I, C, nT, o.cnt, o.val,
+                                      o.idx, o.row_nnz, o.ovf);
   trace_mark(s, "pack_dense");
-  return cudaGetLastError();
+  return e;
 }
 
 // ================================================================ ordered compaction
@@ -169,6 +190,7 @@ __global__ void __launch_bounds__(1024) compact_rows_kernel(const uint8_t* __res
                                                             int32_t* __restrict__ count, int32_t* __restrict__ slot_of,
                                                             int32_t* __restrict__ ell_nnz, int cap_check,
                                                             int32_t* status) {
+  pdl_enter();
   __shared__ int warp_tot[32];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int nwarps = blockDim.x >> 5;
@@ -240,10 +262,10 @@ __global__ void __launch_bounds__(1024) compact_rows_kernel(const uint8_t* __res
 cudaError_t launch_compact_rows(const uint8_t* ovf, const int32_t* row_nnz, int R, int T, int32_t* list,
                                 int list_cap, int32_t* count, int32_t* slot_of, int32_t* ell_nnz, int cap_check,
                                 int32_t* status, cudaStream_t s) {
-  compact_rows_kernel<<<1, 1024, 0, s>>>(ovf, row_nnz, R, T, list, list_cap, count, slot_of, ell_nnz, cap_check,
-                                         status);
+  cudaError_t e = launch(compact_rows_kernel, dim3(1), dim3(1024), 0, s, ovf, row_nnz, R, T, list, list_cap, count,
+                         slot_of, ell_nnz, cap_check, status);
   trace_mark(s, "compact_rows");
-  return cudaGetLastError();
+  return e;
 }
 
 // ================================================================ row gather
@@ -251,6 +273,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
                                                           const int32_t* __restrict__ rows,
                                                           const int32_t* __restrict__ n_dev, int cap, int rows_alloc,
                                                           uint16_t* __restrict__ out) {
+  pdl_enter();
   const int n = min(max(*n_dev, 0), cap);
   const int limit = min(rows_alloc, (n + 127) / 128 * 128);
   const int lane = threadIdx.x & 31;
@@ -273,6 +296,7 @@ __global__ void __launch_bounds__(256) scatter_rows_bf16_kernel(const float* __r
                                                                 const int32_t* __restrict__ n_dev, int cap,
                                                                 const int32_t* __restrict__ row_map,
                                                                 uint16_t* __restrict__ out, int ldo) {
+  pdl_enter();
   const int n = min(max(*n_dev, 0), cap);
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
@@ -290,19 +314,20 @@ __global__ void __launch_bounds__(256) scatter_rows_bf16_kernel(const float* __r
 cudaError_t launch_scatter_rows_bf16(const float* acc, int N, const int32_t* n_dev, int cap, const int32_t* row_map,
                                      uint16_t* out, int ldo, cudaStream_t s) {
   if (cap <= 0) return cudaSuccess;
-  scatter_rows_bf16_kernel<<<std::min(warp_grid(cap, 8), device_sm_count() * 2), 256, 0, s>>>(acc, N, n_dev, cap,
-                                                                                              row_map, out, ldo);
+  cudaError_t e = launch(scatter_rows_bf16_kernel, dim3(std::min(warp_grid(cap, 8), device_sm_count() * 2)), dim3(256),
+                         0, s, acc, N, n_dev, cap, row_map, out, ldo);
   trace_mark(s, "scatter_rows");
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_gather_rows(const uint16_t* src, int d, const int32_t* rows, const int32_t* n, int cap,
                                int rows_alloc, uint16_t* out, cudaStream_t s) {
   if (rows_alloc <= 0) return cudaSuccess;
   const int grid = warp_grid(rows_alloc, 8);
-  gather_rows_kernel<<<std::min(grid, device_sm_count() * 4), 256, 0, s>>>(src, d, rows, n, cap, rows_alloc, out);
+  cudaError_t e = launch(gather_rows_kernel, dim3(std::min(grid, device_sm_count() * 4)), dim3(256), 0, s, src, d, rows,
+                         n, cap, rows_alloc, out);
   trace_mark(s, "gather_rows");
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace tw

@@ -89,6 +89,7 @@ int grid_for(long items, int per_block, int blocks_per_sm) {
 // neurons): col_ptr[0..I], col_cur = col_ptr.
 __global__ void __launch_bounds__(1024) csc_scan_kernel(const int32_t* __restrict__ col_cnt, int I,
                                                         int32_t* __restrict__ col_ptr, int32_t* __restrict__ col_cur) {
+  pdl_enter();
   __shared__ int warp_tot[32];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int per = (I + blockDim.x - 1) / blockDim.x;
@@ -118,6 +119,7 @@ __global__ void __launch_bounds__(1024) csc_scan_kernel(const int32_t* __restric
 // but the gathered rows.
 template <bool GATED>
 __global__ void __launch_bounds__(256) csc_fill_kernel(const SparseBwdArgs a) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
   const uint32_t row16 = static_cast<uint32_t>(a.d / 8);
@@ -151,6 +153,7 @@ __global__ void __launch_bounds__(256) csc_fill_kernel(const SparseBwdArgs a) {
 // the inner loop has no predication and keeps kWgradUnroll row slices in flight.
 template <bool GATED>
 __global__ void __launch_bounds__(256, 3) ell_weight_grad_kernel(const SparseBwdArgs a) {
+  pdl_enter();
   constexpr int U = kWgradUnroll;
   static_assert(32 % U == 0, "the unroll must divide the staging chunk");
   __shared__ float4 stage[8][2][32];
@@ -222,17 +225,17 @@ __global__ void __launch_bounds__(256, 3) ell_weight_grad_kernel(const SparseBwd
 // ====================================================================== launchers
 template <bool GATED>
 static cudaError_t token_side(const SparseBwdArgs& a, cudaStream_t s) {
-  cudaError_t e = memset_async(a.col_cnt, 0, sizeof(int32_t) * (a.I + 1), s);
+  cudaError_t e = launch_zero(a.col_cnt, sizeof(int32_t) * (a.I + 1), nullptr, 0, s);
   if (e != cudaSuccess) return e;
   e = launch_token_bwd(a, s);  // dh, dg, du, column counts, dx
   if (e != cudaSuccess) return e;
-  csc_scan_kernel<<<1, 1024, 0, s>>>(a.col_cnt, a.I, a.col_ptr, a.col_cur);
+  e = launch(csc_scan_kernel, dim3(1), dim3(1024), 0, s, static_cast<const int32_t*>(a.col_cnt), a.I, a.col_ptr,
+             a.col_cur);
   trace_mark(s, "csc_scan");
-  if (a.T > 0) {
-    csc_fill_kernel<GATED><<<grid_for(a.T, 8, 8), 256, 0, s>>>(a);
-    trace_mark(s, "csc_fill");
-  }
-  return cudaGetLastError();
+  if (e != cudaSuccess || a.T == 0) return e;
+  e = launch(csc_fill_kernel<GATED>, dim3(grid_for(a.T, 8, 8)), dim3(256), 0, s, a);
+  trace_mark(s, "csc_fill");
+  return e;
 }
 
 cudaError_t launch_sparse_bwd_tokens(const SparseBwdArgs& a, cudaStream_t s) {
@@ -241,12 +244,11 @@ cudaError_t launch_sparse_bwd_tokens(const SparseBwdArgs& a, cudaStream_t s) {
 
 cudaError_t launch_sparse_bwd_weights(const SparseBwdArgs& a, cudaStream_t s) {
   const long items = static_cast<long>(a.d / 256) * a.I * 2;
-  if (a.Wu != nullptr)
-    ell_weight_grad_kernel<true><<<grid_for(items, 8, 3), 256, 0, s>>>(a);
-  else
-    ell_weight_grad_kernel<false><<<grid_for(items, 8, 3), 256, 0, s>>>(a);
+  const dim3 grid(grid_for(items, 8, 3));
+  const cudaError_t e = a.Wu != nullptr ? launch(ell_weight_grad_kernel<true>, grid, dim3(256), 0, s, a)
+                                        : launch(ell_weight_grad_kernel<false>, grid, dim3(256), 0, s, a);
   trace_mark(s, "ell_weight_grad");
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace tw

@@ -183,6 +183,7 @@ __host__ __device__ inline uint32_t token_smem_bytes(int nch, int cap, int ncoef
 // writes, and token t + 2 writes it only after barriers every warp passes.
 template <int NCH, bool GATED, bool HYBRID>
 __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_fwd_kernel(const SparseFwdArgs a) {
+  pdl_enter();
   constexpr uint32_t row16 = NCH * 32;  // uint4 per d-row
   extern __shared__ __align__(16) uint8_t tsm[];
   const int lane = threadIdx.x & 31, c = threadIdx.x >> 5;
@@ -286,6 +287,7 @@ __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_fwd_kernel(c
 // path afterwards). The window lists are double-buffered like the forward's.
 template <int NCH, bool GATED>
 __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_bwd_kernel(const SparseBwdArgs a) {
+  pdl_enter();
   constexpr uint32_t row16 = NCH * 32;
   constexpr uint32_t lp = rup(kWin + kGroup, kGroup);
   constexpr uint32_t list_bytes = rup(2u * lp, 16u) + 2u * 8u * lp;
@@ -388,16 +390,17 @@ static cudaError_t token_fwd(const SparseFwdArgs& a, cudaStream_t s) {
   const int nch = a.d / 256;
   const size_t smem = token_smem_bytes(nch, a.L, 1);
   const int grid = token_grid(a.T, nch);
-#define TW_TF(n)                                                            \
-  {                                                                         \
-    cudaError_t e = set_smem(token_fwd_kernel<n, GATED, HYBRID>, smem);     \
-    if (e != cudaSuccess) return e;                                         \
-    token_fwd_kernel<n, GATED, HYBRID><<<grid, n * 32, smem, s>>>(a);       \
+  cudaError_t e = cudaSuccess;
+#define TW_TF(n)                                                                            \
+  {                                                                                         \
+    e = set_smem(token_fwd_kernel<n, GATED, HYBRID>, smem);                                 \
+    if (e != cudaSuccess) return e;                                                         \
+    e = launch(token_fwd_kernel<n, GATED, HYBRID>, dim3(grid), dim3(n * 32), smem, s, a); \
   }
   switch (nch) { TW_NCH_CASES(TW_TF) }
 #undef TW_TF
   trace_mark(s, "sparse_fwd");
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_token_fwd(const SparseFwdArgs& a, cudaStream_t s) {
@@ -414,16 +417,17 @@ static cudaError_t token_bwd(const SparseBwdArgs& a, cudaStream_t s) {
   const int nch = a.d / 256;
   const size_t smem = token_smem_bytes(nch, kWin, 2);
   const int grid = token_grid(a.T, nch);
-#define TW_TB(n)                                                   \
-  {                                                                \
-    cudaError_t e = set_smem(token_bwd_kernel<n, GATED>, smem);    \
-    if (e != cudaSuccess) return e;                                \
-    token_bwd_kernel<n, GATED><<<grid, n * 32, smem, s>>>(a);      \
+  cudaError_t e = cudaSuccess;
+#define TW_TB(n)                                                                    \
+  {                                                                                 \
+    e = set_smem(token_bwd_kernel<n, GATED>, smem);                                 \
+    if (e != cudaSuccess) return e;                                                 \
+    e = launch(token_bwd_kernel<n, GATED>, dim3(grid), dim3(n * 32), smem, s, a); \
   }
   switch (nch) { TW_NCH_CASES(TW_TB) }
 #undef TW_TB
   trace_mark(s, "sparse_bwd_token");
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_token_bwd(const SparseBwdArgs& a, cudaStream_t s) {
