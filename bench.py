@@ -189,6 +189,27 @@ def kernel_work(label: str, spec, stats: dict) -> tuple[str, float] | None:
 L2_GATHER_PEAK_GBS = 24200.0
 
 
+def measured_traffic(label: str, workload: str) -> float | None:
+    """DRAM bytes per launch of `label` from the committed ncu summary for `workload`
+    (profiles/dram_traffic_<workload>.txt), or None when there is none or the
+    kernel's sources changed since it was taken (their sha256 no longer matches)."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", f"dram_traffic_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        f = line.split()
+        if not f or f[0].startswith("#") or f[0] != label or len(f) != 5:
+            continue
+        m = hashlib.sha256()
+        for src in f[3].split(","):
+            with open(os.path.join(ROOT, "activation_sparse_feedforward_gb300", "csrc", src), "rb") as fh:
+                m.update(fh.read())
+        return float(f[1]) + float(f[2]) if m.hexdigest()[:16] == f[4] else None
+    return None
+
+
 def gathered_bytes(label: str, spec, stats: dict) -> float | None:
     """Row-slice bytes a gather kernel must pull through L2 per launch: every ELL entry
     costs whole d-rows of the matrices it touches."""
@@ -506,7 +527,8 @@ def run_ours(args, dist: Dist) -> dict | None:
         peak = peaks["hbm_gbs"]
         unit = "GB/s"
     roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": None,
+                "frac": achieved / peak,
+                "traffic": measured_traffic(dom, spec.name) if not args.tokens else None,
                 "peak_source": f"{peaks['source']} ({'bf16 sustained' if bound == 'tensor' else 'HBM copy'})"}
     for lab, v in kernels.items():
         kw = kernel_work(lab, spec, stats)

@@ -1,0 +1,47 @@
+"""Host-side pieces of bench.py that need no GPU: the committed DRAM-traffic
+figures are reported only while the kernel sources they were measured on are
+unchanged, and the algorithmic work formulas count what they say."""
+import hashlib
+import os
+
+import bench
+
+
+def _tree(tmp_path, src_text):
+    csrc = tmp_path / "activation_sparse_feedforward_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "k.cu").write_text(src_text)
+    (tmp_path / "profiles").mkdir()
+    sha = hashlib.sha256(src_text.encode()).hexdigest()[:16]
+    (tmp_path / "profiles" / "dram_traffic_wl.txt").write_text(
+        "# comment\nkern 100 23 k.cu " + sha + "\n")
+    return csrc
+
+
+def test_traffic_reported_while_sources_match(tmp_path, monkeypatch):
+    csrc = _tree(tmp_path, "kernel v1\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.measured_traffic("kern", "wl") == 123.0
+    assert bench.measured_traffic("other", "wl") is None
+    assert bench.measured_traffic("kern", "missing") is None
+    (csrc / "k.cu").write_text("kernel v2\n")
+    assert bench.measured_traffic("kern", "wl") is None
+
+
+def test_committed_traffic_file_parses():
+    path = os.path.join(bench.ROOT, "profiles", "dram_traffic_train_d2048_i5632_m29_o1.txt")
+    rows = [l.split() for l in open(path) if l.strip() and not l.startswith("#")]
+    assert rows and all(len(r) == 5 and int(r[1]) > 0 and int(r[2]) >= 0 for r in rows)
+
+
+def test_gathered_bytes_counts_rows_per_entry():
+    from synthetic import WORKLOADS
+    spec = WORKLOADS["train_d2048_i5632_m29_o1"]
+    stats = {"nnz_ell": 1000, "n_backup": 0, "nnz": 1000}
+    row = spec.d * 2
+    assert bench.gathered_bytes("sparse_fwd", spec, stats) == 2 * 1000 * row
+    assert bench.gathered_bytes("sparse_bwd_token", spec, stats) == 3 * 1000 * row
+    assert bench.gathered_bytes("ell_weight_grad", spec, stats) == 2 * 1000 * row
+    assert bench.gathered_bytes("gate_pack", spec, stats) is None
+    ng = spec.with_(gated=False)
+    assert bench.gathered_bytes("sparse_fwd", ng, stats) == 1000 * row
