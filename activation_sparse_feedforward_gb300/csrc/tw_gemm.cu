@@ -49,6 +49,8 @@ static bool tmap_mnmajor(CUtensorMap* m, const uint16_t* p, int K, int cols) {
   return make_tmap_bf16(m, p, cols, K, static_cast<uint64_t>(cols) * 2, 64, 64);
 }
 
+// max_rows bounds the rows of D (the grid has at most one CTA per tile); a device-
+// chosen split (sh.ksplit < 0) gets one CTA per SM.
 template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES, class Epi>
 static cudaError_t run_gemm(const GemmMaps& maps, const GemmShape& sh, const typename Epi::Params& ep, int max_rows,
                             cudaStream_t s, const char* label) {
@@ -58,7 +60,7 @@ static cudaError_t run_gemm(const GemmMaps& maps, const GemmShape& sh, const typ
   if (e != cudaSuccess) return e;
   const long tiles = static_cast<long>((max_rows + GEMM_BM - 1) / GEMM_BM) * (sh.N / BN);
   if (tiles <= 0) return cudaSuccess;
-  const int grid = static_cast<int>(std::min<long>(tiles, device_sm_count()));
+  const int grid = sh.ksplit < 0 ? device_sm_count() : static_cast<int>(std::min<long>(tiles, device_sm_count()));
   e = launch(kern, dim3(grid), dim3(GEMM_THREADS), Tr::SMEM_BYTES, s, maps, sh, ep);
   trace_mark(s, label);
   return e;
@@ -154,19 +156,14 @@ cudaError_t gemm_rows_times_nmajor_splitk(const uint16_t* const* A, const uint16
   sh.m_dev = n_dev;
   sh.m_cap = cap;
   sh.segments = segments;
-  const int tiles = ((cap + GEMM_BM - 1) / GEMM_BM) * (N / 256);
-  const int kb_total = ((K + GEMM_BK - 1) / GEMM_BK) * segments;
-  sh.ksplit = std::max(1, std::min(kb_total, (2 * device_sm_count() + tiles - 1) / tiles));
+  sh.ksplit = -1;  // the row count is on the device: the kernel picks the split
   GemmMaps maps;
   for (int i = 0; i < segments; ++i)
     if (!tmap_kmajor(&maps.a[i], A[i], rows_alloc, K, 128) || !tmap_mnmajor(&maps.b[i], B[i], K, N))
       return cudaErrorInvalidValue;
   fill_unused(maps, segments, segments);
   EpiRedF32::Params ep{acc, N};
-  const int units = tiles * sh.ksplit;
-  // rows of work units instead of rows of D: run_gemm sizes the grid from max_rows
-  return run_gemm<256, false, true, false, 4, EpiRedF32>(maps, sh, ep, units * GEMM_BM / (N / 256), s,
-                                                          "backup_rows_gemm");
+  return run_gemm<256, false, true, false, 4, EpiRedF32>(maps, sh, ep, cap, s, "backup_rows_gemm");
 }
 
 // ------------------------------------------------------------------ dense backup, backward

@@ -38,7 +38,9 @@ struct GemmShape {
   int k_cap;
   int segments;      // 1 to 4 (A, B) pairs
   int ksplit;        // >= 1: each output tile's K loop is cut into ksplit work units
-                     // (only for epilogues that accumulate, e.g. EpiRedF32)
+                     // (only for epilogues that accumulate, e.g. EpiRedF32); < 0:
+                     // chosen on the device from the actual tile count so that the
+                     // units fill the grid once (grid / tiles slices per tile)
   int32_t* status;
 };
 
@@ -126,7 +128,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const int kb_total = kb_per_seg * shape.segments;
   // work unit = (output tile, slice of its K loop); empty slices are skipped by
   // every role alike
-  const int ksplit = max(1, shape.ksplit);
+  const int ksplit = shape.ksplit >= 0 ? max(1, shape.ksplit)
+                                      : (num_tiles > 0 ? max(1, min(kb_total, static_cast<int>(gridDim.x) / num_tiles)) : 1);
   const int kb_chunk = (kb_total + ksplit - 1) / ksplit;
   const int num_units = num_tiles * ksplit;
 
