@@ -14,9 +14,11 @@ Modules
              packing and unpacking, as the pages define the formats.
 ``sparse``   the same forward/backward computed entry by entry from the packed
              formats (the method is exact: it only skips multiplications by zero).
+``neurons``  per-neuron activity counts and the dead-neuron re-initialisation of
+             the gate projection (a counter-based SplitMix64 / Irwin-Hall draw).
 
 Every function here is pinned by ``-m "not gpu"`` tests against something other
 than itself (brute force, closed forms, finite differences, a hand-worked fixture,
 invariants, torch autograd); see the test files ``tests/test_oracle_*.py``.
 """
-from . import ffn, formats, sparse  # noqa: F401
+from . import ffn, formats, neurons, sparse  # noqa: F401

@@ -1,0 +1,75 @@
+"""Pins of oracle/neurons.py: the SplitMix64 outputs its reference implementation
+gives for seed 0, the Irwin-Hall draw's moments and support, counts against brute
+force and against the Hybrid packing, and re-initialisation touching dead rows only."""
+import numpy as np
+
+from oracle import ffn, formats, neurons
+from synthetic import FFNSpec, make_inputs
+
+
+def test_splitmix64_reference_outputs_seed_zero():
+    # first three outputs of SplitMix64 seeded with 0 (the reference implementation's
+    # next() called three times)
+    got = neurons.splitmix64_at(0, np.arange(3, dtype=np.uint64))
+    assert [int(v) for v in got] == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+
+
+def test_splitmix64_counter_form_matches_sequential_generator():
+    seed = 0x1234_5678_9ABC_DEF0
+    M = (1 << 64) - 1
+    state, seq = seed, []
+    for _ in range(40):       # the generator written out step by step in Python integers
+        state = (state + 0x9E3779B97F4A7C15) & M
+        z = state
+        z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & M
+        z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & M
+        seq.append(z ^ (z >> 31))
+    assert [int(v) for v in neurons.splitmix64_at(seed, np.arange(40, dtype=np.uint64))] == seq
+
+
+def test_irwin_hall_draw_moments_and_support():
+    w = neurons.reinit_values(7, np.arange(64), 1024, 1.0)
+    z = ffn.bf16_to_f64(w)
+    assert abs(z.mean()) < 0.01 and abs(z.var() - 1.0) < 0.02
+    assert np.abs(z).max() <= 6.0
+    # fourth moment of Irwin-Hall(12) - 6 is 3 - 1.2/12 = 2.9 (normal: 3)
+    assert abs((z ** 4).mean() - 2.9) < 0.06
+
+
+def test_reinit_values_are_a_pure_function_of_seed_and_position():
+    a = neurons.reinit_values(3, np.array([5, 9]), 256, 0.02)
+    b = neurons.reinit_values(3, np.array([9, 5]), 256, 0.02)
+    assert np.array_equal(a, b[::-1])
+    c = neurons.reinit_values(4, np.array([5, 9]), 256, 0.02)
+    assert (a != c).mean() > 0.9
+    # scaling: std 0.02 values are 0.02 x the std 1 values up to one bf16 rounding
+    one = ffn.bf16_to_f64(neurons.reinit_values(3, np.array([5]), 256, 1.0))
+    small = ffn.bf16_to_f64(a[:1])
+    assert np.allclose(small, 0.02 * one, rtol=2 ** -7, atol=0)
+
+
+def test_counts_brute_force_and_hybrid_packing():
+    spec = FFNSpec("counts", T=96, d=256, I=448, mean_active=6, outlier_frac=0.05, W=64, C=4, R=8, seed=3)
+    inp = make_inputs(spec)
+    f = ffn.forward(inp["x"], inp["Wg"], inp["Wu"], inp["Wd"])
+    a = f["a"]
+    brute = np.array([sum(1 for t in range(spec.T) if a[t, j] > 0) for j in range(spec.I)])
+    assert np.array_equal(neurons.neuron_counts(a), brute)
+    # the same counts from the Hybrid: ELL entries plus backup rows
+    h = formats.hybrid_pack(a, f["u"], spec.W, spec.C, spec.R)
+    from_hybrid = np.zeros(spec.I, dtype=np.int64)
+    np.add.at(from_hybrid, h["ell_idx"][h["ell_valid"]], 1)
+    from_hybrid += (np.asarray(h["backup_a"]) > 0).sum(axis=0)
+    assert (h["backup_slot"] >= 0).sum() > 0
+    assert np.array_equal(from_hybrid, brute)
+
+
+def test_reinit_touches_dead_rows_only():
+    rng = np.random.default_rng(0)
+    W = rng.integers(0, 1 << 16, size=(32, 64), dtype=np.uint16)
+    counts = np.arange(32) % 3   # rows 0, 3, 6, ... are dead
+    W2, n = neurons.reinit_dead_rows(W, counts, seed=11, std=0.05)
+    dead = counts == 0
+    assert n == dead.sum()
+    assert np.array_equal(W2[~dead], W[~dead])
+    assert np.array_equal(W2[dead], neurons.reinit_values(11, np.flatnonzero(dead), 64, 0.05))
