@@ -10,8 +10,10 @@ from .ops import (  # noqa: F401
     Hybrid,
     TwellFFN,
     dense_gemm,
+    hybrid_neuron_counts,
     new_status,
     raise_if_device_error,
+    reinit_dead_rows,
     twell_ffn_fwd,
     twell_gate_pack,
     twell_pack,

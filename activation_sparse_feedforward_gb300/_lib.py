@@ -52,6 +52,8 @@ SIGNATURES = {
     "hybrid_ffn_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
                                ctypes.POINTER(TwHybrid), c_float, c_void_p, c_void_p, c_void_p, c_void_p,
                                c_void_p, c_size_t, c_void_p, c_void_p]),
+    "hybrid_neuron_counts": (c_int, [ctypes.POINTER(TwHybrid), c_void_p, c_void_p]),
+    "tw_reinit_dead_rows": (c_int, [c_void_p, c_int, c_int, c_void_p, ctypes.c_uint64, c_float, c_void_p, c_void_p]),
     "tw_dense_gemm": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p,
                               c_void_p]),
     "tw_trace_begin": (c_int, [ctypes.POINTER(c_void_p), c_int]),

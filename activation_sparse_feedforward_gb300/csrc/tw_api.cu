@@ -1,6 +1,7 @@
 // extern "C" entry points declared in include/twell.h: host-side validation,
 // workspace layout and the launch sequence of each operation. Everything is
 // enqueued on the caller's stream; nothing is allocated, freed or synchronised.
+#include <cmath>
 #include <stdint.h>
 #include <string.h>
 
@@ -418,6 +419,34 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
   }
   a.dW_base_rows = backup ? saved->n_backup : nullptr;
   TW_TRY(tw::launch_sparse_bwd_weights(a, s));
+  return TW_OK;
+}
+
+tw_status hybrid_neuron_counts(const tw_hybrid* saved, int32_t* counts, void* stream) {
+  if (saved == nullptr) return TW_EINVAL;
+  if (saved->T < 0 || saved->I < 1 || saved->R < 1 || saved->backup_cap < 0 || saved->backup_cap > saved->T)
+    return TW_EINVAL;
+  if (saved->T == 0) return TW_OK;
+  tw_status st = check_ptrs({counts, saved->ell_nnz, saved->ell_idx, saved->n_backup});
+  if (st != TW_OK) return st;
+  if (saved->backup_cap > 0) {
+    st = check_ptrs({saved->backup_a});
+    if (st != TW_OK) return st;
+  }
+  TW_TRY(tw::launch_neuron_counts(*saved, counts, as_stream(stream)));
+  return TW_OK;
+}
+
+tw_status tw_reinit_dead_rows(uint16_t* W, int I, int d, const int32_t* counts, uint64_t seed, float std_dev,
+                              int32_t* n_reinit, void* stream) {
+  if (I < 0 || d < 1 || !std::isfinite(std_dev)) return TW_EINVAL;
+  tw_status st = check_ptrs({n_reinit});
+  if (st != TW_OK) return st;
+  if (I > 0) {
+    if (W == nullptr || counts == nullptr) return TW_EINVAL;
+    if (reinterpret_cast<uintptr_t>(W) % 2 != 0 || reinterpret_cast<uintptr_t>(counts) % 4 != 0) return TW_EALIGN;
+  }
+  TW_TRY(tw::launch_reinit_rows(W, I, d, counts, seed, std_dev, n_reinit, as_stream(stream)));
   return TW_OK;
 }
 

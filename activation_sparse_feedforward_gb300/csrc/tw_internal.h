@@ -54,6 +54,11 @@ cudaError_t launch_compact_rows(const uint8_t* ovf, const int32_t* row_nnz, int 
                                 int list_cap, int32_t* count, int32_t* slot_of, int32_t* ell_nnz, int cap_check,
                                 int32_t* status, cudaStream_t s);
 
+// ---------------------------------------------------------------- tw_neurons.cu
+cudaError_t launch_neuron_counts(const tw_hybrid& h, int32_t* counts, cudaStream_t s);
+cudaError_t launch_reinit_rows(uint16_t* W, int I, int d, const int32_t* counts, uint64_t seed, float stdv,
+                               int32_t* n_reinit, cudaStream_t s);
+
 // out[i] = src[rows[i]] for i < min(*n, cap); rows [n, round_up(n, 128)) (below
 // rows_alloc) are zero-filled. Row length d bf16.
 cudaError_t launch_gather_rows(const uint16_t* src, int d, const int32_t* rows, const int32_t* n, int cap,

@@ -7,6 +7,7 @@ int32 status tensor; ``raise_if_device_error(status)`` synchronises and checks i
 """
 from __future__ import annotations
 
+import ctypes
 from dataclasses import dataclass
 
 import torch
@@ -225,6 +226,31 @@ class HybridFFN:
                                           _ptr(self.status), _stream())
         _lib.check(code, "hybrid_ffn_bwd")
         return self.dx, self.dWg, self.dWu, self.dWd
+
+
+def hybrid_neuron_counts(saved: "Hybrid", counts: torch.Tensor | None = None) -> torch.Tensor:
+    """counts[j] += tokens with a_tj != 0 in the saved Hybrid (ELL entries and dense
+    backup rows). A new zeroed [I] int32 tensor is used when none is given."""
+    if counts is None:
+        counts = torch.zeros(saved.I, dtype=torch.int32, device=saved.row_nnz.device)
+    if counts.dtype != torch.int32 or counts.numel() != saved.I or not counts.is_contiguous():
+        raise ValueError("counts must be a contiguous int32 tensor of I elements")
+    s = saved.struct()
+    _lib.check(_lib.load().hybrid_neuron_counts(ctypes.byref(s), _ptr(counts), _stream()), "hybrid_neuron_counts")
+    return counts
+
+
+def reinit_dead_rows(W: torch.Tensor, counts: torch.Tensor, seed: int, std: float) -> torch.Tensor:
+    """Redraw (in place) every row j of the bf16 matrix W [I, d] with counts[j] == 0
+    (see tw_reinit_dead_rows). Returns the device int32 count of rows redrawn."""
+    _check_bf16("W", W)
+    I, d = W.shape
+    if counts.dtype != torch.int32 or counts.numel() != I:
+        raise ValueError("counts must be an int32 tensor of I elements")
+    n = torch.zeros(1, dtype=torch.int32, device=W.device)
+    _lib.check(_lib.load().tw_reinit_dead_rows(_ptr(W), I, d, _ptr(counts), int(seed) & ((1 << 64) - 1), float(std),
+                                               _ptr(n), _stream()), "tw_reinit_dead_rows")
+    return n
 
 
 def dense_gemm(A: torch.Tensor, B: torch.Tensor, M: int, N: int, K: int, a_mn: bool, b_mn: bool,

@@ -654,6 +654,20 @@ def run_ours(args, dist: Dist) -> dict | None:
         "warm_l2": warm,
         "memory": memory,
     }
+    # per-neuron activity counts of the step's forward and dead-neuron re-initialisation
+    # of (a copy of) the gate projection
+    counts = torch.zeros(spec.I, dtype=torch.int32, device=dev)
+    Wg_copy = Wg.clone()
+
+    def neuron_pass():
+        counts.zero_()
+        tw.hybrid_neuron_counts(h.saved, counts)
+        return tw.reinit_dead_rows(Wg_copy, counts, 1234, 1.0 / math.sqrt(spec.d))
+
+    n_dead = neuron_pass()
+    ms_neur = _time_steps(neuron_pass, max(3, args.steps // 2), 3, flush, stream)
+    line["dead_neurons"] = {"counts_and_reinit_us": 1e3 * ms_neur, "dead": int(n_dead.item()),
+                            "min_count": int(counts.min().item()), "max_count": int(counts.max().item())}
     if not args.no_inference:
         line["inference"] = measure_inference(dev, flush, stream, max(3, args.steps // 2))
     if args.sweep:

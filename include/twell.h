@@ -202,6 +202,26 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
                          float* dWu, float* dWd, void* ws, size_t ws_bytes,
                          int32_t* dev_status, void* stream);
 
+/* Per-neuron activity counts of one Hybrid training forward (the statistic behind
+ * the pages' dead-neuron analysis: thelatestinai listing, Figure 8, Table 5):
+ * counts[j] += the number of tokens t with a_tj != 0, over the saved Hybrid's ELL
+ * entries and its dense backup rows (fp32 a > 0). counts is [I] int32 on the
+ * device, accumulated (zero it to start a window). Enqueues on `stream` after the
+ * forward that filled `saved`. */
+tw_status hybrid_neuron_counts(const tw_hybrid* saved, int32_t* counts, void* stream);
+
+/* Dead-neuron re-initialisation of a weight matrix W [I, d] bf16 (the pages apply
+ * it to the gate projection, Table 5 "Dead neuron reinit."): every row j with
+ * counts[j] == 0 is overwritten with std * z, z = (sum of 12 uniforms) - 6
+ * (Irwin-Hall: mean 0, variance 1, |z| <= 6). The uniforms are the top 24 bits of
+ * SplitMix64 outputs number 12 (j d + k) + i (i < 12) of a generator seeded with
+ * `seed`, so the values depend only on (seed, j, k). z is exact in float64; the value
+ * is rounded once to float32, then to bf16 (nearest even). *n_reinit (device int32)
+ * receives the number of rows rewritten. Rows with counts[j] != 0 are untouched.
+ * Requires I >= 0, d > 0, std finite. */
+tw_status tw_reinit_dead_rows(uint16_t* W, int I, int d, const int32_t* counts, uint64_t seed,
+                              float std_dev, int32_t* n_reinit, void* stream);
+
 /* Dense bf16 GEMM on the tensor cores, D[M, N] (fp32) = A B, the engine of the
  * dense backup path, exposed to check its operand layouts. a_mn == 0: A is [M, K]
  * (K contiguous); a_mn == 1: A is stored [K, M]. b_mn == 0: B is stored [N, K];

@@ -81,6 +81,17 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.tw_dense_gemm(16, 16, 64, 60, 64, 0, 0, 16, 16, None) == _lib.TW_EINVAL
 
 
+def test_neuron_functions_validate_on_the_host(lib):
+    import math
+    assert lib.hybrid_neuron_counts(None, 16, None) == _lib.TW_EINVAL
+    assert lib.tw_reinit_dead_rows(16, 4, 0, 16, 1, 0.1, 16, None) == _lib.TW_EINVAL          # d = 0
+    assert lib.tw_reinit_dead_rows(16, 4, 8, 16, 1, math.inf, 16, None) == _lib.TW_EINVAL     # std not finite
+    assert lib.tw_reinit_dead_rows(None, 4, 8, 16, 1, 0.1, 16, None) == _lib.TW_EINVAL        # no W
+    assert lib.tw_reinit_dead_rows(16, 4, 8, 18, 1, 0.1, 16, None) == _lib.TW_EALIGN          # counts misaligned
+    h = _lib.TwHybrid(0, 64, 8, 0)
+    assert lib.hybrid_neuron_counts(ctypes.byref(h), 16, None) == _lib.TW_OK                  # T = 0: nothing to do
+
+
 def test_trace_hook_host_side(lib):
     assert lib.tw_trace_begin(None, 4) == _lib.TW_EINVAL
     assert lib.tw_trace_end() == 0
