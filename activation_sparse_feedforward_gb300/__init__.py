@@ -9,7 +9,9 @@ from .ops import (  # noqa: F401
     TwELL,
     Hybrid,
     TwellFFN,
+    TwellSparseFFN,
     dense_gemm,
+    gate_relu_dense,
     hybrid_neuron_counts,
     new_status,
     raise_if_device_error,

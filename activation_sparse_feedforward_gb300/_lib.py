@@ -52,6 +52,9 @@ SIGNATURES = {
     "hybrid_ffn_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
                                ctypes.POINTER(TwHybrid), c_float, c_void_p, c_void_p, c_void_p, c_void_p,
                                c_void_p, c_size_t, c_void_p, c_void_p]),
+    "twell_ffn_sparse_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_int,
+                                     ctypes.POINTER(TwTwell), c_void_p, c_size_t, c_void_p, c_void_p, c_void_p]),
+    "tw_gate_relu_dense": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]),
     "hybrid_neuron_counts": (c_int, [ctypes.POINTER(TwHybrid), c_void_p, c_void_p]),
     "tw_reinit_dead_rows": (c_int, [c_void_p, c_int, c_int, c_void_p, ctypes.c_uint64, c_float, c_void_p, c_void_p]),
     "tw_dense_gemm": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p,

@@ -256,9 +256,36 @@ size_t twell_ffn_fwd_workspace_size(int T, int d, int I, int W, int C, int ovf_c
   return c.off + 256;
 }
 
-tw_status twell_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, int T, int d,
-                        int I, int W, int C, int ovf_cap, const tw_twell* tw_out, void* ws, size_t ws_bytes,
-                        uint16_t* y, int32_t* dev_status, void* stream) {
+// The sparse part of the TwELL forward, given a packed TwELL with its overflow list:
+// the token kernel on the non-overflow rows, the dense tensor-core path on the
+// overflow rows (TW_ECAPACITY when more than ovf_cap rows overflowed).
+static tw_status twell_sparse_impl(const uint16_t* x, const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd,
+                                   int T, int d, int I, int W, int C, int ovf_cap, const tw_twell& o, void* ws,
+                                   uint16_t* y, int32_t* dev_status, cudaStream_t s) {
+  Carve c(reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(ws) + 255) & ~static_cast<uintptr_t>(255)));
+  const FwdWs w = carve_twell_fwd(c, d, I, ovf_cap);
+  const int ra = round_up(ovf_cap, 128);
+  tw::SparseFwdArgs a{};
+  a.x = x; a.Wu = Wu; a.Wd = Wd;
+  a.T = T; a.d = d; a.I = I; a.W = W; a.C = C; a.nT = I / W; a.L = (I / W) * C;
+  a.cnt = o.cnt; a.val = o.val; a.idx = o.idx; a.ovf = o.ovf;
+  a.backup_slot = nullptr;
+  a.y = y;
+  TW_TRY(tw::launch_token_fwd(a, s));
+  if (ovf_cap > 0) {
+    TW_TRY(tw::launch_gather_rows(x, d, o.ovf_rows, o.n_ovf, ovf_cap, ra, w.X, s, dev_status));
+    TW_TRY(tw::gemm_backup_hidden(w.X, Wg, Wu, ra, o.n_ovf, ovf_cap, d, I, w.H, w.H_lo, nullptr, nullptr,
+                                  dev_status, s));
+    const uint16_t* A[2] = {w.H, w.H_lo};
+    const uint16_t* B[2] = {Wd, Wd};
+    TW_TRY(tw::gemm_rows_times_nmajor(A, B, 2, ra, o.n_ovf, ovf_cap, I, d, y, d, o.ovf_rows, dev_status, s));
+  }
+  return TW_OK;
+}
+
+static tw_status check_twell_fwd_args(const uint16_t* x, const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd,
+                                      int T, int d, int I, int W, int C, int ovf_cap, const tw_twell* tw_out,
+                                      void* ws, size_t ws_bytes, uint16_t* y, int32_t* dev_status) {
   tw_status st = check_tile_geometry(T, I, W, C);
   if (st != TW_OK) return st;
   st = check_model_width(d);
@@ -272,29 +299,37 @@ tw_status twell_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* W
   if (Wu != nullptr && !aligned16(Wu)) return TW_EALIGN;
   if (ws_bytes < twell_ffn_fwd_workspace_size(T, d, I, W, C, ovf_cap)) return TW_EWORKSPACE;
   if (ovf_cap > 0 && ws == nullptr) return TW_EINVAL;
-  cudaStream_t s = as_stream(stream);
-  const tw_twell& o = *tw_out;
-  Carve c(reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(ws) + 255) & ~static_cast<uintptr_t>(255)));
-  const FwdWs w = carve_twell_fwd(c, d, I, ovf_cap);
-  const int ra = round_up(ovf_cap, 128);
+  return TW_OK;
+}
 
-  st = gate_pack_impl(x, Wg, T, d, I, W, C, o, nullptr, ovf_cap, dev_status, s);
+tw_status twell_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, int T, int d,
+                        int I, int W, int C, int ovf_cap, const tw_twell* tw_out, void* ws, size_t ws_bytes,
+                        uint16_t* y, int32_t* dev_status, void* stream) {
+  tw_status st = check_twell_fwd_args(x, Wg, Wu, Wd, T, d, I, W, C, ovf_cap, tw_out, ws, ws_bytes, y, dev_status);
+  if (st != TW_OK || T == 0) return st;
+  cudaStream_t s = as_stream(stream);
+  st = gate_pack_impl(x, Wg, T, d, I, W, C, *tw_out, nullptr, ovf_cap, dev_status, s);
   if (st != TW_OK) return st;
-  tw::SparseFwdArgs a{};
-  a.x = x; a.Wu = Wu; a.Wd = Wd;
-  a.T = T; a.d = d; a.I = I; a.W = W; a.C = C; a.nT = I / W; a.L = (I / W) * C;
-  a.cnt = o.cnt; a.val = o.val; a.idx = o.idx; a.ovf = o.ovf;
-  a.backup_slot = nullptr;
-  a.y = y;
-  TW_TRY(tw::launch_token_fwd(a, s));
-  if (ovf_cap > 0) {
-    TW_TRY(tw::launch_gather_rows(x, d, o.ovf_rows, o.n_ovf, ovf_cap, ra, w.X, s));
-    TW_TRY(tw::gemm_backup_hidden(w.X, Wg, Wu, ra, o.n_ovf, ovf_cap, d, I, w.H, w.H_lo, nullptr, nullptr,
-                                  dev_status, s));
-    const uint16_t* A[2] = {w.H, w.H_lo};
-    const uint16_t* B[2] = {Wd, Wd};
-    TW_TRY(tw::gemm_rows_times_nmajor(A, B, 2, ra, o.n_ovf, ovf_cap, I, d, y, d, o.ovf_rows, dev_status, s));
-  }
+  return twell_sparse_impl(x, Wg, Wu, Wd, T, d, I, W, C, ovf_cap, *tw_out, ws, y, dev_status, s);
+}
+
+tw_status twell_ffn_sparse_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, int T,
+                               int d, int I, int W, int C, int ovf_cap, const tw_twell* packed, void* ws,
+                               size_t ws_bytes, uint16_t* y, int32_t* dev_status, void* stream) {
+  tw_status st = check_twell_fwd_args(x, Wg, Wu, Wd, T, d, I, W, C, ovf_cap, packed, ws, ws_bytes, y, dev_status);
+  if (st != TW_OK || T == 0) return st;
+  return twell_sparse_impl(x, Wg, Wu, Wd, T, d, I, W, C, ovf_cap, *packed, ws, y, dev_status, as_stream(stream));
+}
+
+tw_status tw_gate_relu_dense(const uint16_t* x, const uint16_t* Wg, int T, int d, int I, uint16_t* a,
+                             int32_t* dev_status, void* stream) {
+  if (T < 0 || I < 64 || I > 65536 || I % 64 != 0) return TW_EUNSUPPORTED;
+  tw_status st = check_model_width(d);
+  if (st != TW_OK) return st;
+  if (T == 0) return TW_OK;
+  st = check_ptrs({x, Wg, a, dev_status});
+  if (st != TW_OK) return st;
+  TW_TRY(tw::gemm_gate_relu_dense(x, Wg, T, d, I, a, dev_status, as_stream(stream)));
   return TW_OK;
 }
 

@@ -101,6 +101,21 @@ cudaError_t gemm_gate_pack(const uint16_t* x, const uint16_t* Wg, int T, int d, 
   return run_gemm<64, false, false, false, 8, EpiTwellPack>(maps, sh, ep, T, s, "gate_pack");
 }
 
+// ------------------------------------------------------------------ unfused gate
+cudaError_t gemm_gate_relu_dense(const uint16_t* x, const uint16_t* Wg, int T, int d, int I, uint16_t* a,
+                                 int32_t* status, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  EpiReluBf16::Params ep{a, I};
+  const GemmShape sh = shape_static(T, I, d, status);
+  GemmMaps maps;
+  const int bn = (I % 256 == 0) ? 256 : (I % 128 == 0) ? 128 : 64;
+  if (!tmap_kmajor(&maps.a[0], x, T, d, 128) || !tmap_kmajor(&maps.b[0], Wg, I, d, bn)) return cudaErrorInvalidValue;
+  fill_unused(maps, 1, 1);
+  if (bn == 256) return run_gemm<256, false, false, false, 4, EpiReluBf16>(maps, sh, ep, T, s, "gate_dense");
+  if (bn == 128) return run_gemm<128, false, false, false, 6, EpiReluBf16>(maps, sh, ep, T, s, "gate_dense");
+  return run_gemm<64, false, false, false, 8, EpiReluBf16>(maps, sh, ep, T, s, "gate_dense");
+}
+
 // ------------------------------------------------------------------ dense backup, forward
 cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint16_t* Wu, int rows_alloc,
                                const int32_t* n_dev, int cap, int d, int I, uint16_t* H, uint16_t* H_lo,

@@ -321,6 +321,31 @@ struct EpiStoreF32 {
   TW_DEV void finish() {}
 };
 
+// a[m][n] = bf16(ReLU(acc)) (round to nearest even), row stride lda: the dense
+// activation matrix of an unfused pipeline (pack in a separate pass).
+struct EpiReluBf16 {
+  struct Params {
+    uint16_t* a;
+    int lda;
+  };
+  const Params& p;
+  int m, M, n0;
+  TW_DEV EpiReluBf16(const Params& p_, int m_, int M_, int n0_) : p(p_), m(m_), M(M_), n0(n0_) {}
+  TW_DEV void chunk(int c, const uint32_t (&v)[32], const uint32_t (&)[32]) {
+    if (m >= M) return;
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float g0 = __uint_as_float(v[2 * i]), g1 = __uint_as_float(v[2 * i + 1]);
+      w[i] = pack_bf16x2(g0 > 0.f ? g0 : 0.f, g1 > 0.f ? g1 : 0.f);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(p.a + static_cast<size_t>(m) * p.lda + n0 + c * 32);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  }
+  TW_DEV void finish() {}
+};
+
 // D[m][n] += acc (fp32 read-modify-write), row stride ldd.
 struct EpiAddF32 {
   struct Params {

@@ -61,8 +61,9 @@ cudaError_t launch_reinit_rows(uint16_t* W, int I, int d, const int32_t* counts,
 
 // out[i] = src[rows[i]] for i < min(*n, cap); rows [n, round_up(n, 128)) (below
 // rows_alloc) are zero-filled. Row length d bf16.
+// Raises TW_ECAPACITY into `status` (when non-null) if *n > cap.
 cudaError_t launch_gather_rows(const uint16_t* src, int d, const int32_t* rows, const int32_t* n, int cap,
-                               int rows_alloc, uint16_t* out, cudaStream_t s);
+                               int rows_alloc, uint16_t* out, cudaStream_t s, int32_t* status = nullptr);
 
 // Largest per-token entry list of the sparse forward, (I / W) * C: two lists of
 // 10 bytes an entry live in one CTA's shared memory.
@@ -125,6 +126,10 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t o
 // gate projection + ReLU + TwELL pack
 cudaError_t gemm_gate_pack(const uint16_t* x, const uint16_t* Wg, int T, int d, int I, int W, int C,
                            const tw_twell& o, uint16_t* a_dense, int32_t* status, cudaStream_t s);
+
+// unfused gate: a = bf16(ReLU(x Wg^T)) written densely [T, I]
+cudaError_t gemm_gate_relu_dense(const uint16_t* x, const uint16_t* Wg, int T, int d, int I, uint16_t* a,
+                                 int32_t* status, cudaStream_t s);
 
 // dense backup forward: h(X Wg^T, X Wu^T) over n (device) rows of X [rows_alloc, d],
 // written as the bf16 pair H + H_lo; optional saved fp32 a / u.

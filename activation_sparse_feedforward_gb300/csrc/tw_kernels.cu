@@ -272,8 +272,9 @@ cudaError_t launch_compact_rows(const uint8_t* ovf, const int32_t* row_nnz, int 
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ src, int d,
                                                           const int32_t* __restrict__ rows,
                                                           const int32_t* __restrict__ n_dev, int cap, int rows_alloc,
-                                                          uint16_t* __restrict__ out) {
+                                                          uint16_t* __restrict__ out, int32_t* status) {
   pdl_enter();
+  if (status != nullptr && blockIdx.x == 0 && threadIdx.x == 0 && *n_dev > cap) raise_status(status, TW_ECAPACITY);
   const int n = min(max(*n_dev, 0), cap);
   const int limit = min(rows_alloc, (n + 127) / 128 * 128);
   const int lane = threadIdx.x & 31;
@@ -321,11 +322,11 @@ cudaError_t launch_scatter_rows_bf16(const float* acc, int N, const int32_t* n_d
 }
 
 cudaError_t launch_gather_rows(const uint16_t* src, int d, const int32_t* rows, const int32_t* n, int cap,
-                               int rows_alloc, uint16_t* out, cudaStream_t s) {
+                               int rows_alloc, uint16_t* out, cudaStream_t s, int32_t* status) {
   if (rows_alloc <= 0) return cudaSuccess;
   const int grid = warp_grid(rows_alloc, 8);
   cudaError_t e = launch(gather_rows_kernel, dim3(std::min(grid, device_sm_count() * 4)), dim3(256), 0, s, src, d, rows,
-                         n, cap, rows_alloc, out);
+                         n, cap, rows_alloc, out, status);
   trace_mark(s, "gather_rows");
   return e;
 }

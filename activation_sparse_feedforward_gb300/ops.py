@@ -125,11 +125,12 @@ def _workspace(nbytes: int, device) -> torch.Tensor:
 
 # ---------------------------------------------------------------------------- ops
 
-def twell_pack(A: torch.Tensor, W: int, C: int, status: torch.Tensor | None = None) -> TwELL:
-    """TwELL of a dense bf16 [T, I] matrix."""
+def twell_pack(A: torch.Tensor, W: int, C: int, status: torch.Tensor | None = None, out: TwELL | None = None) -> TwELL:
+    """TwELL of a dense bf16 [T, I] matrix (into `out` when given)."""
     _check_bf16("A", A)
     T, I = A.shape
-    out = TwELL.empty(T, I, W, C, A.device)
+    if out is None:
+        out = TwELL.empty(T, I, W, C, A.device)
     st = status if status is not None else new_status(A.device)
     s = out.struct()
     _lib.check(_lib.load().twell_pack(_ptr(A), T, I, W, C, s, _ptr(st), _stream()), "twell_pack")
@@ -226,6 +227,41 @@ class HybridFFN:
                                           _ptr(self.status), _stream())
         _lib.check(code, "hybrid_ffn_bwd")
         return self.dx, self.dWg, self.dWu, self.dWd
+
+
+def gate_relu_dense(x: torch.Tensor, Wg: torch.Tensor, status: torch.Tensor | None = None) -> torch.Tensor:
+    """Dense a = bf16(ReLU(x Wg^T)) [T, I]: the first stage of the unfused pipeline."""
+    _check_bf16("x", x)
+    _check_bf16("Wg", Wg)
+    T, d = x.shape
+    I = Wg.shape[0]
+    a = torch.empty((T, I), dtype=BF16, device=x.device)
+    st = status if status is not None else new_status(x.device)
+    _lib.check(_lib.load().tw_gate_relu_dense(_ptr(x), _ptr(Wg), T, d, I, _ptr(a), _ptr(st), _stream()),
+               "tw_gate_relu_dense")
+    return a
+
+
+class TwellSparseFFN:
+    """Preallocated sparse part of the inference forward on an already packed TwELL
+    (the unfused pipeline's last stage; see twell_ffn_sparse_fwd)."""
+
+    def __init__(self, T: int, d: int, I: int, W: int, C: int, ovf_cap: int | None = None, device="cuda"):
+        self.T, self.d, self.I, self.W, self.C = T, d, I, W, C
+        self.ovf_cap = T if ovf_cap is None else ovf_cap
+        self.ws_bytes = int(_lib.load().twell_ffn_fwd_workspace_size(T, d, I, W, C, self.ovf_cap))
+        self.ws = _workspace(self.ws_bytes, device)
+        self.y = torch.empty((T, d), dtype=BF16, device=device)
+        self.status = new_status(device)
+
+    def __call__(self, x, Wg, Wu, Wd, packed: "TwELL") -> torch.Tensor:
+        _check_bf16("x", x, (self.T, self.d))
+        s = packed.struct()
+        code = _lib.load().twell_ffn_sparse_fwd(_ptr(x), _ptr(Wg), _ptr(Wu), _ptr(Wd), self.T, self.d, self.I, self.W,
+                                                self.C, self.ovf_cap, ctypes.byref(s), _ptr(self.ws), self.ws_bytes,
+                                                _ptr(self.y), _ptr(self.status), _stream())
+        _lib.check(code, "twell_ffn_sparse_fwd")
+        return self.y
 
 
 def hybrid_neuron_counts(saved: "Hybrid", counts: torch.Tensor | None = None) -> torch.Tensor:

@@ -290,9 +290,28 @@ def measure_inference(dev, flush, stream, steps: int) -> dict:
             return h @ Wd
 
         ms_d = _time_steps(dense, steps, 3, flush, stream)
+
+        # the unfused pipeline: dense a through HBM, standalone packer, sparse part
+        a_buf = torch.empty((spec.T, spec.I), dtype=torch.bfloat16, device=dev)
+        packed = tw.TwELL.empty(spec.T, spec.I, spec.W, spec.C, dev)
+        st = tw.new_status(dev)
+        sp = tw.TwellSparseFFN(spec.T, spec.d, spec.I, spec.W, spec.C, ovf_cap=512, device=dev)
+
+        def unfused():
+            L = tw.load()
+            L.tw_gate_relu_dense(x.data_ptr(), Wg.data_ptr(), spec.T, spec.d, spec.I, a_buf.data_ptr(), st.data_ptr(),
+                                 torch.cuda.current_stream().cuda_stream)
+            tw.twell_pack(a_buf, spec.W, spec.C, status=st, out=packed)
+            return sp(x, Wg, Wu, Wd, packed)
+
+        ms_u = _time_steps(unfused, steps, 3, flush, stream)
+        tw.raise_if_device_error(st, name + " unfused")
+        tw.raise_if_device_error(sp.status, name + " unfused")
         out[name] = {"tokens_per_ms": spec.T / ms, "ms": ms, "dense_bf16_tokens_per_ms": spec.T / ms_d,
+                     "unfused_tokens_per_ms": spec.T / ms_u, "unfused_ms": ms_u,
                      "n_overflow_rows": int(f.tw.n_ovf.item()),
                      "nnz_per_token": float(f.tw.row_nnz.float().mean().item())}
+        del a_buf, packed, sp
     return out
 
 

@@ -202,6 +202,25 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
                          float* dWu, float* dWd, void* ws, size_t ws_bytes,
                          int32_t* dev_status, void* stream);
 
+/* The sparse part of the TwELL inference forward on an already packed TwELL (from
+ * twell_pack or twell_gate_pack, including its overflow list): y for the rows
+ * without overflow from the CUDA-core kernel, y for the overflow rows from the
+ * dense tensor-core path. Together with tw_gate_relu_dense and twell_pack this is
+ * the unfused pipeline (dense a through HBM, separate conversion, sparse matmuls)
+ * that the pages argue against (explainer 1 "Problem Statement"; blog "1. TwELL");
+ * twell_ffn_fwd is the fused form. Arguments as twell_ffn_fwd, with `packed` read
+ * instead of written; TW_ECAPACITY when the packed TwELL lists more than ovf_cap
+ * overflow rows. */
+tw_status twell_ffn_sparse_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* Wu,
+                               const uint16_t* Wd, int T, int d, int I, int W, int C, int ovf_cap,
+                               const tw_twell* packed, void* ws, size_t ws_bytes, uint16_t* y,
+                               int32_t* dev_status, void* stream);
+
+/* Dense gate activations a = bf16(ReLU(x Wg^T)) [T, I] (round to nearest even), the
+ * first stage of the unfused pipeline. Shapes as twell_gate_pack (I % 64 == 0). */
+tw_status tw_gate_relu_dense(const uint16_t* x, const uint16_t* Wg, int T, int d, int I,
+                             uint16_t* a, int32_t* dev_status, void* stream);
+
 /* Per-neuron activity counts of one Hybrid training forward (the statistic behind
  * the pages' dead-neuron analysis: thelatestinai listing, Figure 8, Table 5):
  * counts[j] += the number of tokens t with a_tj != 0, over the saved Hybrid's ELL

@@ -184,3 +184,43 @@ def test_hybrid_full_size_sampled(name, backup_cap):
     assert_close(dWu[J].cpu().numpy(), r["dWu"], "dWu (sampled neurons)")
     assert_close(dWd[J].cpu().numpy(), r["dWd"], "dWd (sampled neurons)")
     assert int(h.saved.n_backup.item()) >= len(inp["outliers"])
+
+
+@pytest.mark.parametrize("spec", [MEDIUM[0], MEDIUM[2], WORKLOADS["gated_fwd_d2048_i5632"]], ids=lambda s: s.name)
+def test_unfused_pipeline_equals_fused_forward(spec):
+    """Dense a through memory, then the standalone packer, then the sparse part give
+    the fused forward's y bit for bit (same GEMM, same canonical TwELL, same sparse
+    kernels), and both match the oracle."""
+    inp = make_inputs(spec)
+    dv = _dev_inputs(inp)
+    f = tw.TwellFFN(spec.T, spec.d, spec.I, spec.W, spec.C)
+    y_fused = f(dv["x"], dv["Wg"], dv["Wu"], dv["Wd"]).clone()
+    st = tw.new_status()
+    a = tw.gate_relu_dense(dv["x"], dv["Wg"], status=st)
+    packed = tw.twell_pack(a, spec.W, spec.C, status=st)
+    sp = tw.TwellSparseFFN(spec.T, spec.d, spec.I, spec.W, spec.C)
+    y_unfused = sp(dv["x"], dv["Wg"], dv["Wu"], dv["Wd"], packed)
+    torch.cuda.synchronize()
+    for s_ in (f.status, st, sp.status):
+        tw.raise_if_device_error(s_)
+    assert torch.equal(y_unfused, y_fused)
+    for name in ("cnt", "row_nnz", "ovf"):
+        assert torch.equal(getattr(packed, name), getattr(f.tw, name)), name
+    # slots past a tile's count are padding (unspecified)
+    valid = torch.arange(spec.C, device="cuda")[None, None, :] < packed.cnt.long().clamp(max=spec.C)[:, :, None]
+    for name in ("val", "idx"):
+        assert torch.equal(getattr(packed, name)[valid], getattr(f.tw, name)[valid]), name
+    rows = np.unique(np.concatenate([np.arange(0, spec.T, max(1, spec.T // 300)), inp["outliers"][:8]]))
+    ref = ffn.forward(inp["x"][rows], inp["Wg"], inp["Wu"], inp["Wd"])
+    assert_close(f64_of(y_unfused)[rows], ref["y"], "y (unfused)")
+
+
+def test_sparse_part_reports_overflow_beyond_capacity():
+    spec = WORKLOADS["tiny_fwd"]
+    inp = make_inputs(spec)
+    dv = _dev_inputs(inp)
+    packed = tw.twell_pack(tw.gate_relu_dense(dv["x"], dv["Wg"]), spec.W, spec.C)
+    sp = tw.TwellSparseFFN(spec.T, spec.d, spec.I, spec.W, spec.C, ovf_cap=2)   # 5 rows overflow
+    sp(dv["x"], dv["Wg"], dv["Wu"], dv["Wd"], packed)
+    with pytest.raises(tw.TwellError, match="TW_ECAPACITY"):
+        tw.raise_if_device_error(sp.status)
