@@ -32,6 +32,8 @@ MEDIUM = [
     FFNSpec("med_w64_d2048", T=300, d=2048, I=704, mean_active=10, outlier_frac=0.02, W=64, C=6, R=24, seed=7),
     # dense-ish regime: long ELL rows (R = 320) and wide TwELL tiles (C = 32)
     FFNSpec("med_long_rows", T=513, d=512, I=1280, mean_active=200, outlier_frac=0.02, W=128, C=32, R=320, seed=8),
+    # C = 16 on 128-wide tiles (the vector slot loads of the forward's list building)
+    FFNSpec("med_c16", T=700, d=512, I=1024, mean_active=14, outlier_frac=0.02, W=128, C=16, R=64, seed=12),
 ]
 
 
