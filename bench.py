@@ -575,37 +575,60 @@ def run_ours(args, dist: Dist) -> dict | None:
     step_roof = {"tokens_per_ms": spec.T / (t_roof * 1e3), "frac": (spec.T / ms_per_step) / (spec.T / (t_roof * 1e3)),
                  "flops": F, "bytes": B}
 
-    # end to end through the public API with host buffers (pinned), per step:
-    # H2D of x and dy, the step, D2H of y and dx
+    # end to end through the public API with host buffers (pinned): every step uploads
+    # its x and dy and downloads its y and dx. The steps are pipelined the way a
+    # training loop would run them: two sets of device buffers and layer state, step
+    # i + 1's upload on one copy stream and step i - 1's download on another while
+    # step i computes.
     hx = x.cpu().pin_memory()
     hdy = dy.cpu().pin_memory()
     hy = torch.empty_like(hx).pin_memory()
     hdx = torch.empty_like(hx).pin_memory()
-    xd = torch.empty_like(x)
-    dyd = torch.empty_like(dy)
+    hs = [h, tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, backup_cap, gated=spec.gated, device=dev)]
+    xin = [torch.empty_like(x) for _ in range(2)]
+    dyin = [torch.empty_like(dy) for _ in range(2)]
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "done", "out")}
 
-    def e2e_step():
-        xd.copy_(hx, non_blocking=True)
-        dyd.copy_(hdy, non_blocking=True)
-        h.forward(xd, Wg, Wu, Wd)
-        h.backward(dyd, xd, Wg, Wu, Wd, spec.l1)
-        hy.copy_(h.y, non_blocking=True)
-        hdx.copy_(h.dx, non_blocking=True)
+    def e2e_steps(nsteps):
+        for i in range(nsteps):
+            b = i % 2
+            with torch.cuda.stream(up):
+                if i >= 2:
+                    up.wait_event(ev["done"][b])      # step i - 2 no longer reads slot b
+                xin[b].copy_(hx, non_blocking=True)
+                dyin[b].copy_(hdy, non_blocking=True)
+                ev["in"][b].record(up)
+            stream.wait_event(ev["in"][b])
+            if i >= 2:
+                stream.wait_event(ev["out"][b])       # step i - 2's outputs have left the device
+            hs[b].forward(xin[b], Wg, Wu, Wd)
+            hs[b].backward(dyin[b], xin[b], Wg, Wu, Wd, spec.l1)
+            ev["done"][b].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(ev["done"][b])
+                hy.copy_(hs[b].y, non_blocking=True)
+                hdx.copy_(hs[b].dx, non_blocking=True)
+                ev["out"][b].record(down)
+        stream.wait_stream(down)
 
-    for _ in range(2):
-        e2e_step()
+    e2e_steps(2)
     torch.cuda.synchronize(dev)
     e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     dist.barrier()
     e_s.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    up.wait_stream(stream)
+    e2e_steps(args.steps)
     e_e.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = dist.max(e_s.elapsed_time(e_e), dev)
+    for f in hs:
+        tw.raise_if_device_error(f.status, "e2e steps")
     e2e = {"value": spec.T * dist.world * args.steps / e2e_ms, "unit": UNIT,
            "h2d_bytes_per_step": int(hx.numel() * 2 + hdy.numel() * 2),
-           "d2h_bytes_per_step": int(hy.numel() * 2 + hdx.numel() * 2)}
+           "d2h_bytes_per_step": int(hy.numel() * 2 + hdx.numel() * 2),
+           "pipelining": "uploads and downloads on two copy streams, overlapped with the neighbouring steps"}
+    del hs[1]
 
     # dense bf16 FFN (torch/cuBLAS) forward + backward with the same L1 term, same run
     dense = None
