@@ -116,18 +116,6 @@ TW_DEV void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, i
       : "memory");
 }
 
-// 1D bulk copy global -> shared memory (both addresses 16-byte aligned, bytes a
-// multiple of 16); completion is signalled on `bar` as transaction bytes.
-TW_DEV void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_addr(smem_dst)),
-      "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-// Orders this thread's earlier generic-proxy shared-memory accesses before later
-// async-proxy (bulk copy) accesses to the same memory.
-TW_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Bounded wait used only while draining after an abort: ignores the abort flag.
 TW_DEV bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
@@ -139,38 +127,6 @@ TW_DEV bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
-// Per-warp ring of S row slots filled by bulk copies that lane 0 issues ahead of
-// use. Row k of a warp's stream lives in slot k % S; its barrier phase parity is
-// (k / S) & 1. All lanes wait on a slot themselves and agree on the outcome with a
-// warp vote, so a timeout takes every lane out of the loop together.
-template <int S>
-struct WarpRing {
-  uint8_t* buf;       // S * row_bytes
-  uint64_t* bar;      // S barriers
-  uint32_t row_bytes;
-  TW_DEV uint8_t* slot(uint32_t k) const { return buf + (k % S) * row_bytes; }
-  TW_DEV void init(int lane) {
-    if (lane == 0) {
-      for (int s = 0; s < S; ++s) mbar_init(bar + s, 1);
-      fence_barrier_init();
-    }
-    __syncwarp();
-  }
-  // lane 0 only
-  TW_DEV void issue(uint32_t k, const void* src) {
-    uint64_t* b = bar + (k % S);
-    mbar_arrive_expect_tx(b, row_bytes);
-    bulk_load(slot(k), src, row_bytes, b);
-  }
-  TW_DEV bool wait(uint32_t k, volatile int* abort_flag, int32_t* status) {
-    const bool ok = mbar_wait(bar + (k % S), (k / S) & 1u, abort_flag, status);
-    return __all_sync(0xFFFFFFFFu, ok);
-  }
-  // lane 0 only: let rows [consumed, issued) land before the CTA exits after an abort
-  TW_DEV void drain(uint32_t consumed, uint32_t issued) {
-    for (uint32_t k = consumed; k < issued; ++k) mbar_wait_drain(bar + (k % S), (k / S) & 1u);
-  }
-};
 
 // ------------------------------------------------------------------ tcgen05
 // TMEM allocation: executed by one whole warp. The allocated base address is
@@ -248,11 +204,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
 }
 
 // ------------------------------------------------------------------ warp helpers
-TW_DEV float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  return v;
-}
 TW_DEV int warp_inclusive_scan(int v) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
