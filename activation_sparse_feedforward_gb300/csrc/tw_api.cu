@@ -271,6 +271,7 @@ static tw_status twell_sparse_impl(const uint16_t* x, const uint16_t* Wg, const 
   a.cnt = o.cnt; a.val = o.val; a.idx = o.idx; a.ovf = o.ovf;
   a.backup_slot = nullptr;
   a.y = y;
+  a.status = dev_status;
   TW_TRY(tw::launch_token_fwd(a, s));
   if (ovf_cap > 0) {
     TW_TRY(tw::launch_gather_rows(x, d, o.ovf_rows, o.n_ovf, ovf_cap, ra, w.X, s, dev_status));
@@ -375,6 +376,7 @@ tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* 
   a.backup_slot = saved->backup_slot;
   a.ell_idx = saved->ell_idx; a.ell_a = saved->ell_a; a.ell_u = saved->ell_u; a.R = R;
   a.y = y;
+  a.status = dev_status;
   TW_TRY(tw::launch_token_fwd(a, s));
   if (cap > 0) {
     TW_TRY(tw::launch_gather_rows(x, d, saved->backup_tok, saved->n_backup, cap, ra, w.X, s));

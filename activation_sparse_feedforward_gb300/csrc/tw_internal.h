@@ -83,6 +83,7 @@ struct SparseFwdArgs {
   int R;
   int L;                          // per-token entry list capacity: nT * C (<= kMaxList)
   uint16_t* y;
+  int32_t* status;                // device status word (TW_ETIMEOUT from a bounded wait)
 };
 // TwELL / Hybrid forward of the non-dense rows (tw_token.cu)
 cudaError_t launch_token_fwd(const SparseFwdArgs& a, cudaStream_t s);
