@@ -11,6 +11,7 @@ from .ops import (  # noqa: F401
     TwellFFN,
     TwellSparseFFN,
     dense_gemm,
+    fma_probe,
     gate_relu_dense,
     hybrid_neuron_counts,
     new_status,

@@ -487,6 +487,15 @@ tw_status tw_reinit_dead_rows(uint16_t* W, int I, int d, const int32_t* counts, 
   return TW_OK;
 }
 
+tw_status tw_fma_probe(float* out, int blocks, int iters, double* flops, void* stream) {
+  if (blocks < 1 || iters < 1 || blocks > (1 << 20)) return TW_EINVAL;
+  tw_status st = check_ptrs({out});
+  if (st != TW_OK) return st;
+  if (reinterpret_cast<uintptr_t>(out) % 4 != 0) return TW_EALIGN;
+  if (flops != nullptr) *flops = static_cast<double>(tw::fma_probe_flops(blocks, iters));
+  return from_cuda(tw::launch_fma_probe(out, blocks, iters, as_stream(stream)));
+}
+
 tw_status tw_dense_gemm(const uint16_t* A, const uint16_t* B, int M, int N, int K, int a_mn, int b_mn, float* D,
                         int32_t* dev_status, void* stream) {
   if (M < 1 || N < 1 || K < 1 || N % 64 != 0 || K % 64 != 0) return TW_EINVAL;

@@ -22,6 +22,10 @@ void trace_mark(cudaStream_t s, const char* label);
 // Zeroes [p0, p0 + b0) and [p1, p1 + b1) (16-byte aligned starts, any sizes; p1 may
 // be null) with one kernel, followed by a trace mark.
 cudaError_t launch_zero(void* p0, size_t b0, void* p1, size_t b1, cudaStream_t s);
+// fp32 FMA throughput probe (tw_kernels.cu): blocks x 256 threads, `iters` steps;
+// out holds blocks * 256 floats
+cudaError_t launch_fma_probe(float* out, int blocks, int iters, cudaStream_t s);
+long fma_probe_flops(int blocks, int iters);
 
 // Every library kernel is launched with programmatic stream serialization: it may
 // start (and run its prologue) while the kernel before it on the stream finishes,

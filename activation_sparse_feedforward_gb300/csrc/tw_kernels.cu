@@ -81,6 +81,50 @@ cudaError_t launch_zero(void* p0, size_t b0, void* p1, size_t b1, cudaStream_t s
   return e;
 }
 
+// ---------------------------------------------------------------- fp32 FMA probe
+// CUDA-core throughput of the packed two-lane fp32 FMA (`fma.rn.f32x2`), the
+// instruction of the sparse kernels' accumulations: every thread runs kProbeChains
+// independent chains of `iters` dependent FMAs each, on values that stay finite
+// (|m| < 1), and stores the sum so no chain is dead code.
+constexpr int kProbeChains = 8;
+__global__ void __launch_bounds__(256) fma_probe_kernel(float* __restrict__ out, int iters) {
+  pdl_enter();
+  const uint32_t tid = blockIdx.x * blockDim.x + threadIdx.x;
+  const float seed = static_cast<float>(tid & 1023u) * 0x1p-12f;
+  uint64_t acc[kProbeChains], mul, add;
+  {
+    const float m = 0.5f + seed * 0.25f, c = 0.25f - seed;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(mul) : "f"(m), "f"(m * 0.5f));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(add) : "f"(c), "f"(-c));
+  }
+#pragma unroll
+  for (int c = 0; c < kProbeChains; ++c) {
+    const float v = seed + static_cast<float>(c);
+    asm("mov.b64 %0, {%1, %2};" : "=l"(acc[c]) : "f"(v), "f"(-v));
+  }
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int c = 0; c < kProbeChains; ++c) asm volatile("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(acc[c]) : "l"(mul), "l"(add));
+  }
+  float sum = 0.f;
+#pragma unroll
+  for (int c = 0; c < kProbeChains; ++c) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(acc[c]));
+    sum += lo + hi;
+  }
+  out[tid] = sum;
+}
+
+cudaError_t launch_fma_probe(float* out, int blocks, int iters, cudaStream_t s) {
+  cudaError_t e = launch(fma_probe_kernel, dim3(blocks), dim3(256), 0, s, out, iters);
+  trace_mark(s, "fma_probe");
+  return e;
+}
+long fma_probe_flops(int blocks, int iters) {
+  return static_cast<long>(blocks) * 256L * iters * kProbeChains * 2L * 2L;  // 2 lanes, 2 FLOP per FMA
+}
+
 static int warp_grid(long rows, int warps_per_block) {
   const long blocks = (rows + warps_per_block - 1) / warps_per_block;
   const long cap = static_cast<long>(device_sm_count()) * 32;

@@ -300,3 +300,15 @@ def dense_gemm(A: torch.Tensor, B: torch.Tensor, M: int, N: int, K: int, a_mn: b
     _lib.check(_lib.load().tw_dense_gemm(_ptr(A), _ptr(B), M, N, K, int(a_mn), int(b_mn), _ptr(D), _ptr(st),
                                          _stream()), "tw_dense_gemm")
     return D
+
+
+def fma_probe(out: torch.Tensor, blocks: int, iters: int) -> float:
+    """Launch the fp32 FMA throughput probe (see tw_fma_probe) on the current stream;
+    `out` is a float32 device tensor of at least blocks * 256 elements. Returns the
+    FLOPs the launch performs."""
+    if out.dtype != torch.float32 or not out.is_cuda or out.numel() < blocks * 256:
+        raise ValueError("out must be a float32 CUDA tensor of at least blocks * 256 elements")
+    flops = ctypes.c_double(0.0)
+    _lib.check(_lib.load().tw_fma_probe(_ptr(out), int(blocks), int(iters), ctypes.byref(flops), _stream()),
+               "tw_fma_probe")
+    return flops.value

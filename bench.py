@@ -264,6 +264,33 @@ def _time_steps(fn, steps: int, warmup: int, flush, stream) -> float:
     return total / steps
 
 
+def measure_fma_peak(dev, stream) -> dict:
+    """CUDA-core fp32 FMA rate of this GPU from the library's probe kernel (packed
+    two-lane FMAs, 2048 threads per SM): the median of 5 timed launches."""
+    import torch
+
+    import activation_sparse_feedforward_gb300 as tw
+
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks, iters = sms * 8, 16384
+    out = torch.empty(blocks * 256, dtype=torch.float32, device=dev)
+    for _ in range(2):
+        flops = tw.fma_probe(out, blocks, iters)
+    ts = []
+    for _ in range(5):
+        s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_.record(stream)
+        tw.fma_probe(out, blocks, iters)
+        e_.record(stream)
+        torch.cuda.synchronize(dev)
+        ts.append(s_.elapsed_time(e_))
+    ms = statistics.median(ts)
+    if not bool(torch.isfinite(out).all()):
+        raise RuntimeError("fma probe produced non-finite values")
+    return {"tflops": flops / (ms * 1e-3) / 1e12, "ms": ms, "blocks": blocks, "threads": 256, "iters": iters,
+            "instruction": "fma.rn.f32x2"}
+
+
 def measure_inference(dev, flush, stream, steps: int) -> dict:
     """TwELL inference forward at the gated and non-gated 1.5B FFN shapes, next to the
     dense bf16 forward (cuBLAS through torch) on the same inputs."""
@@ -574,6 +601,15 @@ def run_ours(args, dist: Dist) -> dict | None:
     t_roof = max(F / (peaks["bf16_tflops_sustained"] * 1e12), B / (peaks["hbm_gbs"] * 1e9))
     step_roof = {"tokens_per_ms": spec.T / (t_roof * 1e3), "frac": (spec.T / ms_per_step) / (spec.T / (t_roof * 1e3)),
                  "flops": F, "bytes": B}
+    # secondary: the sparse FLOPs priced at the measured CUDA-core fp32 FMA rate (they
+    # run on CUDA cores), the gate and backup FLOPs at the tensor peak
+    fma = measure_fma_peak(dev, stream)
+    F_sparse = 16.0 * spec.d * stats["nnz_ell"]
+    t_roof2 = max((F - F_sparse) / (peaks["bf16_tflops_sustained"] * 1e12) + F_sparse / (fma["tflops"] * 1e12),
+                  B / (peaks["hbm_gbs"] * 1e9))
+    step_roof["cuda_core_sparse"] = {"tokens_per_ms": spec.T / (t_roof2 * 1e3),
+                                     "frac": (spec.T / ms_per_step) / (spec.T / (t_roof2 * 1e3)),
+                                     "sparse_flops": F_sparse, "fp32_fma": fma}
 
     # end to end through the public API with host buffers (pinned): every step uploads
     # its x and dy and downloads its y and dx. The steps are pipelined the way a

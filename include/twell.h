@@ -249,6 +249,15 @@ tw_status tw_reinit_dead_rows(uint16_t* W, int I, int d, const int32_t* counts, 
 tw_status tw_dense_gemm(const uint16_t* A, const uint16_t* B, int M, int N, int K,
                         int a_mn, int b_mn, float* D, int32_t* dev_status, void* stream);
 
+/* CUDA-core fp32 throughput probe for measurement tools (no counterpart on the
+ * pages): `blocks` CTAs of 256 threads each run 8 independent chains of `iters`
+ * packed two-lane FMAs (fma.rn.f32x2, the sparse kernels' accumulation
+ * instruction) and write one float per thread to out [blocks * 256] (device,
+ * caller-owned). *flops (host, may be NULL) receives the FLOPs the launch performs
+ * (4 per packed FMA); FLOPs / device time = the fp32 FMA rate. Requires
+ * 1 <= blocks <= 2^20, iters >= 1; enqueued on `stream`. */
+tw_status tw_fma_probe(float* out, int blocks, int iters, double* flops, void* stream);
+
 /* Kernel-level timing hook for measurement tools (no counterpart on the pages).
  * While a trace is active, every kernel or memset the library enqueues is followed
  * by cudaEventRecord(events[i], stream) with the next caller-created event, and its
