@@ -56,12 +56,14 @@ static cudaError_t run_gemm(const GemmMaps& maps, const GemmShape& sh, const typ
                             cudaStream_t s, const char* label) {
   using Tr = GemmTraits<BN, A_MN, B_MN, DUAL, STAGES>;
   auto kern = gemm_tc_kernel<BN, A_MN, B_MN, DUAL, STAGES, Epi>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Tr::SMEM_BYTES);
+  constexpr int smem = Tr::SMEM_BYTES + Epi::kStageBytes;
+  static_assert(smem <= 232448, "GEMM shared memory above the 227 KiB opt-in limit");
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const long tiles = static_cast<long>((max_rows + GEMM_BM - 1) / GEMM_BM) * (sh.N / BN);
   if (tiles <= 0) return cudaSuccess;
   const int grid = sh.ksplit < 0 ? device_sm_count() : static_cast<int>(std::min<long>(tiles, device_sm_count()));
-  e = launch(kern, dim3(grid), dim3(GEMM_THREADS), Tr::SMEM_BYTES, s, maps, sh, ep);
+  e = launch(kern, dim3(grid), dim3(GEMM_THREADS), smem, s, maps, sh, ep);
   trace_mark(s, label);
   return e;
 }

@@ -27,6 +27,10 @@ namespace tw {
 constexpr int GEMM_BM = 128;
 constexpr int GEMM_BK = 64;
 constexpr int GEMM_THREADS = 192;
+// per-warp transpose buffer of the fp32 row epilogues (`transposed_rows`): 32 rows of
+// kEpiStageStride floats, for each of the four epilogue warps
+constexpr int kEpiStageStride = 36;
+constexpr int kEpiTransposeBytes = 4 * 32 * kEpiStageStride * 4;
 
 struct GemmShape {
   int M;             // rows of D when m_dev == nullptr
@@ -272,6 +276,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const int m = (tile / n_tiles) * GEMM_BM + row;
       const int n0 = (tile % n_tiles) * BN;
       Epi e(ep, m, M, n0);
+      if constexpr (Epi::kStageBytes > 0)
+        e.stage = reinterpret_cast<float*>(tiles + STAGES * Tr::STAGE_BYTES + Tr::BAR_BYTES) + quarter * 32 * kEpiStageStride;
       const uint32_t tbase =
           tmem_base + static_cast<uint32_t>(buf * Tr::ACC_COLS) + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
@@ -298,25 +304,53 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 }
 
 // ======================================================================= epilogues
+// Row-to-column transpose through shared memory for epilogues that write fp32 rows:
+// each epilogue warp holds 32 accumulator rows (one per lane) x 32 columns. Each lane
+// writes its row as eight 16-byte vectors; the warp then reads back four rows per
+// step, eight lanes per row, so one 16-byte-per-lane instruction covers four whole
+// 128-byte row segments instead of 16 bytes in each of 32 rows. The buffer is
+// 32 x 36 floats per warp: with a row stride of 36 floats, every group of eight
+// lanes touches all 32 banks once in both phases. `put(r, c4, x)` stores the four
+// columns 4 c4 .. 4 c4 + 3 of output row r; rows at or past M are skipped. Every
+// lane of the warp must call it.
+template <class Put>
+TW_DEV void transposed_rows(float* stage, const uint32_t (&v)[32], int m, int M, Put put) {
+  const int lane = threadIdx.x & 31;
+  float4* mine = reinterpret_cast<float4*>(stage + lane * kEpiStageStride);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    mine[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
+                          __uint_as_float(v[4 * i + 3]));
+  __syncwarp();
+  const int m0 = m - lane;  // the warp's first row
+  const int sub = lane >> 3, c4 = lane & 7;
+#pragma unroll
+  for (int r0 = 0; r0 < 32; r0 += 4) {
+    const int r = r0 + sub;
+    if (m0 + r < M) put(m0 + r, c4, *reinterpret_cast<const float4*>(stage + r * kEpiStageStride + 4 * c4));
+  }
+  __syncwarp();
+}
+
 // Each epilogue object lives in one thread for one tile: it owns accumulator row m
 // (valid when m < M) and columns [n0, n0 + BN), delivered 32 columns at a time.
 
 // D[m][n] = acc (fp32), row stride ldd.
 struct EpiStoreF32 {
+  static constexpr int kStageBytes = kEpiTransposeBytes;
   struct Params {
     float* D;
     int ldd;
   };
   const Params& p;
   int m, M, n0;
+  float* stage = nullptr;  // this warp's transpose buffer
   TW_DEV EpiStoreF32(const Params& p_, int m_, int M_, int n0_) : p(p_), m(m_), M(M_), n0(n0_) {}
   TW_DEV void chunk(int c, const uint32_t (&v)[32], const uint32_t (&)[32]) {
-    if (m >= M) return;
-    float4* dst = reinterpret_cast<float4*>(p.D + static_cast<size_t>(m) * p.ldd + n0 + c * 32);
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
-                           __uint_as_float(v[4 * i + 3]));
+    float* col = p.D + n0 + c * 32;
+    transposed_rows(stage, v, m, M, [&](int r, int c4, float4 x) {
+      reinterpret_cast<float4*>(col + static_cast<size_t>(r) * p.ldd)[c4] = x;
+    });
   }
   TW_DEV void finish() {}
 };
@@ -324,6 +358,7 @@ struct EpiStoreF32 {
 // a[m][n] = bf16(ReLU(acc)) (round to nearest even), row stride lda: the dense
 // activation matrix of an unfused pipeline (pack in a separate pass).
 struct EpiReluBf16 {
+  static constexpr int kStageBytes = 0;
   struct Params {
     uint16_t* a;
     int lda;
@@ -348,6 +383,7 @@ struct EpiReluBf16 {
 
 // D[m][n] += acc (fp32 read-modify-write), row stride ldd.
 struct EpiAddF32 {
+  static constexpr int kStageBytes = 0;
   struct Params {
     float* D;
     int ldd;
@@ -374,26 +410,27 @@ struct EpiAddF32 {
 // acc[m][n] += D with fp32 vector atomics: one K slice of a split-K product (acc is
 // zeroed beforehand, and every slice of the tile adds its part).
 struct EpiRedF32 {
+  static constexpr int kStageBytes = kEpiTransposeBytes;
   struct Params {
     float* acc;
     int ld;
   };
   const Params& p;
   int m, M, n0;
+  float* stage = nullptr;  // this warp's transpose buffer
   TW_DEV EpiRedF32(const Params& p_, int m_, int M_, int n0_) : p(p_), m(m_), M(M_), n0(n0_) {}
   TW_DEV void chunk(int c, const uint32_t (&v)[32], const uint32_t (&)[32]) {
-    if (m >= M) return;
-    float4* dst = reinterpret_cast<float4*>(p.acc + static_cast<size_t>(m) * p.ld + n0 + c * 32);
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      atomicAdd(dst + i, make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                     __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
+    float* col = p.acc + n0 + c * 32;
+    transposed_rows(stage, v, m, M, [&](int r, int c4, float4 x) {
+      atomicAdd(reinterpret_cast<float4*>(col + static_cast<size_t>(r) * p.ld) + c4, x);
+    });
   }
   TW_DEV void finish() {}
 };
 
 // out[row_map[m]][n] = bf16(acc) (row_map == nullptr: row m), row stride ldo.
 struct EpiScatterBf16 {
+  static constexpr int kStageBytes = 0;
   struct Params {
     uint16_t* out;
     int ldo;
@@ -425,6 +462,7 @@ struct EpiScatterBf16 {
 // stored (padding slots stay untouched); cnt is always written; row_nnz and ovf
 // are combined across column tiles with one atomic per (row, CTA tile).
 struct EpiTwellPack {
+  static constexpr int kStageBytes = 0;
   struct Params {
     int T, W, C, nT;
     uint16_t* cnt;
@@ -510,6 +548,7 @@ TW_DEV void split8(const float (&v)[8], uint4& hi, uint4& lo) {
 // over these rows read zeros.
 template <bool GATED>
 struct EpiBackupHidden {
+  static constexpr int kStageBytes = 0;
   struct Params {
     uint16_t* H;
     uint16_t* H_lo;
@@ -561,6 +600,7 @@ struct EpiBackupHidden {
 // [M, end of tile) become zeros.
 template <bool GATED>
 struct EpiBackupGrad {
+  static constexpr int kStageBytes = 0;
   struct Params {
     const float* a;
     const float* u;
