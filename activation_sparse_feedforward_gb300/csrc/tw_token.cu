@@ -129,6 +129,19 @@ TW_DEV float reduce8(float (&p)[8], int lane) {
 
 TW_DEV uint4 ldg16(const uint4* p) { return __ldg(p); }
 
+// Lists are read from shared memory sixteen bytes at a time (one broadcast
+// wavefront for the whole warp): eight neuron indices, or two coefficient pairs.
+// jsel(jv, q) is index q of a 16-byte block of eight; hsel(hv, odd) is pair `odd` of
+// a block of two.
+TW_DEV uint4 lds16(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+TW_DEV uint32_t jsel(const uint4& jv, int q) {
+  const uint32_t w = q < 2 ? jv.x : q < 4 ? jv.y : q < 6 ? jv.z : jv.w;
+  return (q & 1) ? (w >> 16) : (w & 0xFFFFu);
+}
+TW_DEV f32x2 hsel(const uint4& hv, int odd) {
+  return odd ? ((static_cast<uint64_t>(hv.w) << 32) | hv.z) : ((static_cast<uint64_t>(hv.y) << 32) | hv.x);
+}
+
 // Block-wide exclusive scan of one int per thread; *total gets the sum. One
 // __syncthreads, plus a trailing one when `reuse` (scratch is rewritten before the
 // caller's next barrier); scratch holds one int per warp.
@@ -151,12 +164,21 @@ TW_DEV int block_exclusive_scan(int v, int* scratch, int* total, bool reuse) {
 // Pass A over the list window [w0, w0 + m): part[k - w0] = this warp's slice of
 // vec . W[j_k] for every k of the window rounded up to kGroup (entries past the list
 // end repeat its last neuron; their sums are never read).
+// VEC reads the group's eight indices in one 16-byte load (faster in the forward,
+// slower in the backward, by measurement).
+template <bool VEC>
 TW_DEV void pass_dot(const uint4* Wslice, uint32_t row16, const uint16_t* lj, int w0, int m, const uint4& vec,
                      float* part, int lane) {
   for (int k0 = 0; k0 < m; k0 += kGroup) {
     uint4 v[kGroup];
+    if (VEC) {
+      const uint4 jv = lds16(lj + w0 + k0);
 #pragma unroll
-    for (int q = 0; q < kGroup; ++q) v[q] = ldg16(Wslice + static_cast<uint32_t>(lj[w0 + k0 + q]) * row16);
+      for (int q = 0; q < kGroup; ++q) v[q] = ldg16(Wslice + jsel(jv, q) * row16);
+    } else {
+#pragma unroll
+      for (int q = 0; q < kGroup; ++q) v[q] = ldg16(Wslice + static_cast<uint32_t>(lj[w0 + k0 + q]) * row16);
+    }
     float p[kGroup];
 #pragma unroll
     for (int q = 0; q < kGroup; ++q) p[q] = dot8(vec, v[q]);
@@ -257,7 +279,7 @@ __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_fwd_kernel(c
       const int m = min(kWin, n - w0);
       if (GATED) {
         // -------------------------------------------------------- up: h = a (x_t . Wu[j])
-        pass_dot(Wu4, row16, lj, w0, m, xs, part + c * kWin, lane);
+        pass_dot<true>(Wu4, row16, lj, w0, m, xs, part + c * kWin, lane);
         __syncthreads();
         for (int k = threadIdx.x; k < m; k += blockDim.x) {
           float u = 0.f;
@@ -271,11 +293,16 @@ __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_fwd_kernel(c
       }
       // ---------------------------------------------------------- down: y_t += sum h Wd[j]
       for (int k0 = 0; k0 < m; k0 += kGroup) {
+        const uint4 jv = lds16(lj + w0 + k0);
         uint4 v[kGroup];
 #pragma unroll
-        for (int q = 0; q < kGroup; ++q) v[q] = ldg16(Wd4 + static_cast<uint32_t>(lj[w0 + k0 + q]) * row16);
+        for (int q = 0; q < kGroup; ++q) v[q] = ldg16(Wd4 + jsel(jv, q) * row16);
 #pragma unroll
-        for (int q = 0; q < kGroup; ++q) y.axpy(lh[w0 + k0 + q], v[q]);
+        for (int q = 0; q < kGroup; q += 2) {
+          const uint4 hv = lds16(lh + w0 + k0 + q);
+          y.axpy(hsel(hv, 0), v[q]);
+          y.axpy(hsel(hv, 1), v[q + 1]);
+        }
       }
     }
     reinterpret_cast<uint4*>(a.y)[static_cast<size_t>(t) * row16 + c * 32 + lane] = y.to_bf16();
@@ -436,7 +463,7 @@ __global__ void __launch_bounds__((NCH + 1) * 32, ws_ctas_per_sm(NCH))
     for (int w0 = 0; w0 < n; w0 += kWin) {
       const int m = min(kWin, n - w0);
       if (GATED) {
-        pass_dot(Wu4, row16, lj, w0, m, xs, part + c * kWin, lane);
+        pass_dot<true>(Wu4, row16, lj, w0, m, xs, part + c * kWin, lane);
         consumers_sync(kConsumers);
         for (int kk = threadIdx.x; kk < m; kk += kConsumers) {
           float u = 0.f;
@@ -507,7 +534,7 @@ __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_bwd_kernel(c
       }
       __syncthreads();
       // ---------------------------------------------------------- dh = dy_t . Wd[j]
-      pass_dot(Wd4, row16, lj, 0, m, dys, part + c * kWin, lane);
+      pass_dot<false>(Wd4, row16, lj, 0, m, dys, part + c * kWin, lane);
       __syncthreads();
       for (int k = threadIdx.x; k < m; k += blockDim.x) {
         float dh = 0.f;
@@ -565,18 +592,19 @@ int token_grid(int T, int nch) {
   case 8: CALL(8); break;  \
   default: return cudaErrorInvalidValue;
 
-// Kernel choice, by measurement on GB300 at d 2048: the warp-specialised forward is
-// faster for the Hybrid training forward (7 %) and the non-gated TwELL forward (1 %);
-// the single-role kernel, with one more consumer warp per producer, is faster
-// (3 %) for the gated TwELL forward.
+// Kernel choice, by measurement on GB300 at d 2048: the gated forward (training and
+// inference) runs the single-role kernel; with its list reads vectorised it matches
+// the warp-specialised kernel in training and is 4 % faster in inference. The
+// warp-specialised kernel, which runs out of registers for vectorised reads, is
+// 2.5 % faster for the non-gated forward.
 template <bool GATED, bool HYBRID>
 static cudaError_t token_fwd(const SparseFwdArgs& a, cudaStream_t s) {
   const int nch = a.d / 256;
-  constexpr bool kSpecialised = HYBRID || !GATED;
+  constexpr bool kSpecialised = !GATED;
   const size_t smem = kSpecialised ? fwd_ws_smem_bytes(nch, a.L) : token_smem_bytes(nch, a.L, 1);
   cudaError_t e = cudaSuccess;
 #define TW_TF(n)                                                                                        \
-  if (kSpecialised) {                                                                                   \
+  if constexpr (kSpecialised) {                                                                         \
     const int grid = std::max(1, std::min(a.T, device_sm_count() * ws_ctas_per_sm(n)));                \
     e = set_smem(token_fwd_ws_kernel<n, GATED, HYBRID>, smem);                                          \
     if (e != cudaSuccess) return e;                                                                     \
