@@ -101,6 +101,7 @@ struct FwdWs {
   uint16_t* X;
   uint16_t* H;
   uint16_t* H_lo;
+  int32_t* sched;  // token scheduling counter of the sparse forward
 };
 FwdWs carve_twell_fwd(Carve& c, int d, int I, int ovf_cap) {
   const int ra = round_up(ovf_cap, 128);
@@ -108,6 +109,7 @@ FwdWs carve_twell_fwd(Carve& c, int d, int I, int ovf_cap) {
   w.X = c.take<uint16_t>(static_cast<size_t>(ra) * d);
   w.H = c.take<uint16_t>(static_cast<size_t>(ra) * I);
   w.H_lo = c.take<uint16_t>(static_cast<size_t>(ra) * I);
+  w.sched = c.take<int32_t>(4);
   return w;
 }
 
@@ -122,6 +124,7 @@ struct HybFwdWs {
   uint16_t* H;
   uint16_t* H_lo;
   float* acc;  // split-K accumulator of the down projection [ra, d]
+  int32_t* sched;  // token scheduling counter of the sparse forward
 };
 HybFwdWs carve_hybrid_fwd(Carve& c, int T, int d, int I, int W, int C, int backup_cap) {
   const size_t nT = static_cast<size_t>(I / W);
@@ -137,6 +140,7 @@ HybFwdWs carve_hybrid_fwd(Carve& c, int T, int d, int I, int W, int C, int backu
   w.H = c.take<uint16_t>(static_cast<size_t>(ra) * I);
   w.H_lo = c.take<uint16_t>(static_cast<size_t>(ra) * I);
   w.acc = c.take<float>(static_cast<size_t>(ra) * d);
+  w.sched = c.take<int32_t>(4);
   return w;
 }
 
@@ -151,6 +155,7 @@ struct HybBwdWs {
   uint16_t* X;
   tw::BackupGradOut g;  // dG, dU, H as (hi, lo) bf16 pairs
   float* acc;           // split-K accumulator of dx for the backup rows [ra, d]
+  int32_t* sched;       // token scheduling counter of the token pass
 };
 HybBwdWs carve_hybrid_bwd(Carve& c, int T, int d, int I, int R, int backup_cap) {
   const size_t TR = static_cast<size_t>(T) * R;
@@ -172,6 +177,7 @@ HybBwdWs carve_hybrid_bwd(Carve& c, int T, int d, int I, int R, int backup_cap) 
   w.g.H = c.take<uint16_t>(rI);
   w.g.H_lo = c.take<uint16_t>(rI);
   w.acc = c.take<float>(static_cast<size_t>(ra) * d);
+  w.sched = c.take<int32_t>(4);
   return w;
 }
 
@@ -272,6 +278,8 @@ static tw_status twell_sparse_impl(const uint16_t* x, const uint16_t* Wg, const 
   a.backup_slot = nullptr;
   a.y = y;
   a.status = dev_status;
+  a.sched = w.sched;
+  a.sched_zeroed = false;
   TW_TRY(tw::launch_token_fwd(a, s));
   if (ovf_cap > 0) {
     TW_TRY(tw::launch_gather_rows(x, d, o.ovf_rows, o.n_ovf, ovf_cap, ra, w.X, s, dev_status));
@@ -368,7 +376,7 @@ tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* 
   st = gate_pack_impl(x, Wg, T, d, I, W, C, o, nullptr, T, dev_status, s, false);
   if (st != TW_OK) return st;
   TW_TRY(tw::launch_compact_rows(o.ovf, saved->row_nnz, R, T, saved->backup_tok, cap, saved->n_backup,
-                                 saved->backup_slot, saved->ell_nnz, cap, dev_status, s));
+                                 saved->backup_slot, saved->ell_nnz, cap, dev_status, s, w.sched));
   tw::SparseFwdArgs a{};
   a.x = x; a.Wu = Wu; a.Wd = Wd;
   a.T = T; a.d = d; a.I = I; a.W = W; a.C = C; a.nT = I / W; a.L = (I / W) * C;
@@ -377,6 +385,8 @@ tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* 
   a.ell_idx = saved->ell_idx; a.ell_a = saved->ell_a; a.ell_u = saved->ell_u; a.R = R;
   a.y = y;
   a.status = dev_status;
+  a.sched = w.sched;
+  a.sched_zeroed = true;  // by compact_rows above
   TW_TRY(tw::launch_token_fwd(a, s));
   if (cap > 0) {
     TW_TRY(tw::launch_gather_rows(x, d, saved->backup_tok, saved->n_backup, cap, ra, w.X, s));
@@ -434,6 +444,7 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
   a.dg = w.dg; a.du = w.du; a.dx = dx;
   a.col_cnt = w.col_cnt; a.col_ptr = w.col_ptr; a.col_cur = w.col_cur; a.csc = w.csc;
   a.dWg = dWg; a.dWu = dWu; a.dWd = dWd;
+  a.sched = w.sched;
   TW_TRY(tw::launch_sparse_bwd_tokens(a, s));
   const bool backup = cap > 0 && T > 0;
   if (backup) {

@@ -54,9 +54,11 @@ cudaError_t launch_pack_dense(const uint16_t* A, int T, int I, int W, int C, con
 // *count = n, slot_of[t] (rank, -1 when unflagged, -2 when past list_cap) and
 // ell_nnz[t] (row_nnz when unflagged, else 0) when those pointers are non-null.
 // Raises TW_ECAPACITY when n > cap_check.
+// zero_word (optional) is set to 0 by the kernel, for a scheduling counter used later
+// in the stream.
 cudaError_t launch_compact_rows(const uint8_t* ovf, const int32_t* row_nnz, int R, int T, int32_t* list,
                                 int list_cap, int32_t* count, int32_t* slot_of, int32_t* ell_nnz, int cap_check,
-                                int32_t* status, cudaStream_t s);
+                                int32_t* status, cudaStream_t s, int32_t* zero_word = nullptr);
 
 // ---------------------------------------------------------------- tw_neurons.cu
 cudaError_t launch_neuron_counts(const tw_hybrid& h, int32_t* counts, cudaStream_t s);
@@ -88,6 +90,12 @@ struct SparseFwdArgs {
   int L;                          // per-token entry list capacity: nT * C (<= kMaxList)
   uint16_t* y;
   int32_t* status;                // device status word (TW_ETIMEOUT from a bounded wait)
+  // token scheduling counter (device int): CTAs take their first token by index and
+  // the rest from this counter; nullptr = static round-robin. It must read 0 when the
+  // kernel starts: the launcher zeroes it unless sched_zeroed says an earlier kernel
+  // in the stream did.
+  int32_t* sched;
+  bool sched_zeroed;
 };
 // TwELL / Hybrid forward of the non-dense rows (tw_token.cu)
 cudaError_t launch_token_fwd(const SparseFwdArgs& a, cudaStream_t s);
@@ -113,6 +121,9 @@ struct SparseBwdArgs {
   // when non-null and *dW_base_rows > 0, dW already holds the dense backup rows'
   // part and the ELL part is added to it; otherwise dW is overwritten
   const int32_t* dW_base_rows;
+  // token scheduling counter of the token pass (as SparseFwdArgs::sched); zeroed
+  // together with col_cnt
+  int32_t* sched;
 };
 // Token side of the ELL backward (tw_token.cu): dh, dg and du per entry, column
 // counts of the transposed Hybrid (col_cnt must be zero), dx.

@@ -233,8 +233,9 @@ __global__ void __launch_bounds__(1024) compact_rows_kernel(const uint8_t* __res
                                                             int32_t* __restrict__ list, int list_cap,
                                                             int32_t* __restrict__ count, int32_t* __restrict__ slot_of,
                                                             int32_t* __restrict__ ell_nnz, int cap_check,
-                                                            int32_t* status) {
+                                                            int32_t* status, int32_t* zero_word) {
   pdl_enter();
+  if (zero_word != nullptr && threadIdx.x == 0) *zero_word = 0;
   __shared__ int warp_tot[32];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int nwarps = blockDim.x >> 5;
@@ -305,9 +306,9 @@ __global__ void __launch_bounds__(1024) compact_rows_kernel(const uint8_t* __res
 
 cudaError_t launch_compact_rows(const uint8_t* ovf, const int32_t* row_nnz, int R, int T, int32_t* list,
                                 int list_cap, int32_t* count, int32_t* slot_of, int32_t* ell_nnz, int cap_check,
-                                int32_t* status, cudaStream_t s) {
+                                int32_t* status, cudaStream_t s, int32_t* zero_word) {
   cudaError_t e = launch(compact_rows_kernel, dim3(1), dim3(1024), 0, s, ovf, row_nnz, R, T, list, list_cap, count,
-                         slot_of, ell_nnz, cap_check, status);
+                         slot_of, ell_nnz, cap_check, status, zero_word);
   trace_mark(s, "compact_rows");
   return e;
 }

@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(256, 3) ell_weight_grad_kernel(const SparseBwd
 // ====================================================================== launchers
 template <bool GATED>
 static cudaError_t token_side(const SparseBwdArgs& a, cudaStream_t s) {
-  cudaError_t e = launch_zero(a.col_cnt, sizeof(int32_t) * (a.I + 1), nullptr, 0, s);
+  cudaError_t e = launch_zero(a.col_cnt, sizeof(int32_t) * (a.I + 1), a.sched, a.sched ? sizeof(int32_t) : 0, s);
   if (e != cudaSuccess) return e;
   e = launch_token_bwd(a, s);  // dh, dg, du, column counts, dx
   if (e != cudaSuccess) return e;

@@ -129,6 +129,13 @@ TW_DEV float reduce8(float (&p)[8], int lane) {
 
 TW_DEV uint4 ldg16(const uint4* p) { return __ldg(p); }
 
+// Token scheduling: a CTA's first token is its index; after that it takes the next
+// unclaimed token from a device counter (zero at launch), so CTAs that start late or
+// run slower take fewer tokens. Without a counter the assignment is round-robin.
+TW_DEV int next_token(int32_t* sched, int t) {
+  return sched != nullptr ? static_cast<int>(gridDim.x) + atomicAdd(sched, 1) : t + static_cast<int>(gridDim.x);
+}
+
 // Lists are read from shared memory sixteen bytes at a time (one broadcast
 // wavefront for the whole warp): eight neuron indices, or two coefficient pairs.
 // jsel(jv, q) is index q of a 16-byte block of eight; hsel(hv, odd) is pair `odd` of
@@ -217,10 +224,18 @@ __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_fwd_kernel(c
   const uint4* Wd4 = reinterpret_cast<const uint4*>(a.Wd) + c * 32 + lane;
   const bool vec_slots = a.C % 16 == 0;  // a tile's slots load as 16-byte vectors
   int buf = 0;
+  __shared__ int next_tok[2];  // the CTA's next token, double-buffered like the lists
+  int nb = 0;
 
-  for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
+  for (int t = blockIdx.x; t < a.T; nb ^= 1) {
+    // the next token is fetched now and read after this token's first barrier
+    if (threadIdx.x == 0) next_tok[nb] = next_token(a.sched, t);
     const bool skip = HYBRID ? (a.backup_slot[t] != -1) : (a.ovf[t] != 0);
-    if (skip) continue;
+    if (skip) {
+      __syncthreads();
+      t = next_tok[nb];
+      continue;
+    }
     uint16_t* lj = reinterpret_cast<uint16_t*>(tsm + buf * list_bytes);
     f32x2* lh = reinterpret_cast<f32x2*>(tsm + buf * list_bytes + rup(2u * lp, 16u));
     buf ^= 1;
@@ -306,6 +321,7 @@ __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_fwd_kernel(c
       }
     }
     reinterpret_cast<uint4*>(a.y)[static_cast<size_t>(t) * row16 + c * 32 + lane] = y.to_bf16();
+    t = next_tok[nb];
   }
 }
 
@@ -379,9 +395,13 @@ __global__ void __launch_bounds__((NCH + 1) * 32, ws_ctas_per_sm(NCH))
     const bool vec_slots = a.C % 16 == 0;
     int k = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok; t += gridDim.x) {  // the first t past the range sends the end header
+    for (int t = blockIdx.x; ok;) {  // the first t past the range sends the end header
       const bool end = t >= a.T;
-      if (!end && (HYBRID ? (a.backup_slot[t] != -1) : (a.ovf[t] != 0))) continue;
+      const int t_next = end ? t : __shfl_sync(0xFFFFFFFFu, lane == 0 ? next_token(a.sched, t) : 0, 0);
+      if (!end && (HYBRID ? (a.backup_slot[t] != -1) : (a.ovf[t] != 0))) {
+        t = t_next;
+        continue;
+      }
       const int b = k % kListRing;
       const uint32_t use = static_cast<uint32_t>(k / kListRing);
       ++k;
@@ -438,6 +458,7 @@ __global__ void __launch_bounds__((NCH + 1) * 32, ws_ctas_per_sm(NCH))
       __syncwarp();
       if (lane == 0) mbar_arrive(full + b);  // release: the list and header are visible to the waiters
       if (end) break;
+      t = t_next;
     }
     return;
   }
@@ -490,8 +511,9 @@ __global__ void __launch_bounds__((NCH + 1) * 32, ws_ctas_per_sm(NCH))
 }
 
 // ====================================================================== backward
-// Tokens without ELL entries get dx = 0 (backup rows are overwritten by the dense
-// path afterwards). The window lists are double-buffered like the forward's.
+// Tokens without ELL entries get dx = 0; rows in the dense backup (slot >= 0) are
+// left to the dense path, which writes their dx. The window lists are
+// double-buffered like the forward's.
 template <int NCH, bool GATED>
 __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_bwd_kernel(const SparseBwdArgs a) {
   pdl_enter();
@@ -505,8 +527,16 @@ __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_bwd_kernel(c
   const uint4* Wu4 = reinterpret_cast<const uint4*>(a.Wu) + c * 32 + lane;
   const uint4* Wd4 = reinterpret_cast<const uint4*>(a.Wd) + c * 32 + lane;
   int buf = 0;
+  __shared__ int next_tok[2];  // the CTA's next token (read after this token's first barrier)
+  int nb = 0;
 
-  for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
+  for (int t = blockIdx.x; t < a.T; nb ^= 1) {
+    if (threadIdx.x == 0) next_tok[nb] = next_token(a.sched, t);
+    if (a.backup_slot != nullptr && a.backup_slot[t] >= 0) {  // the dense path writes this row's dx
+      __syncthreads();
+      t = next_tok[nb];
+      continue;
+    }
     const int n = a.ell_nnz[t];
     const size_t rb = static_cast<size_t>(t) * a.R;
     const uint4 dys = n > 0 ? ldg16(reinterpret_cast<const uint4*>(a.dy) + static_cast<size_t>(t) * row16 + c * 32 + lane)
@@ -565,7 +595,9 @@ __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_bwd_kernel(c
         }
       }
     }
+    if (n == 0) __syncthreads();  // the windows' barriers publish next_tok otherwise
     reinterpret_cast<uint4*>(a.dx)[static_cast<size_t>(t) * row16 + c * 32 + lane] = dx.to_bf16();
+    t = next_tok[nb];
   }
 }
 
@@ -600,6 +632,10 @@ int token_grid(int T, int nch) {
 template <bool GATED, bool HYBRID>
 static cudaError_t token_fwd(const SparseFwdArgs& a, cudaStream_t s) {
   const int nch = a.d / 256;
+  if (a.sched != nullptr && !a.sched_zeroed) {
+    const cudaError_t z = launch_zero(a.sched, sizeof(int32_t), nullptr, 0, s);
+    if (z != cudaSuccess) return z;
+  }
   constexpr bool kSpecialised = !GATED;
   const size_t smem = kSpecialised ? fwd_ws_smem_bytes(nch, a.L) : token_smem_bytes(nch, a.L, 1);
   cudaError_t e = cudaSuccess;
