@@ -101,6 +101,7 @@ struct FwdWs {
   uint16_t* X;
   uint16_t* H;
   uint16_t* H_lo;
+  float* acc;      // split-K accumulator of the overflow rows' down projection [ra, d]
   int32_t* sched;  // token scheduling counter of the sparse forward
 };
 FwdWs carve_twell_fwd(Carve& c, int d, int I, int ovf_cap) {
@@ -109,6 +110,7 @@ FwdWs carve_twell_fwd(Carve& c, int d, int I, int ovf_cap) {
   w.X = c.take<uint16_t>(static_cast<size_t>(ra) * d);
   w.H = c.take<uint16_t>(static_cast<size_t>(ra) * I);
   w.H_lo = c.take<uint16_t>(static_cast<size_t>(ra) * I);
+  w.acc = c.take<float>(static_cast<size_t>(ra) * d);
   w.sched = c.take<int32_t>(4);
   return w;
 }
@@ -285,9 +287,12 @@ static tw_status twell_sparse_impl(const uint16_t* x, const uint16_t* Wg, const 
     TW_TRY(tw::launch_gather_rows(x, d, o.ovf_rows, o.n_ovf, ovf_cap, ra, w.X, s, dev_status));
     TW_TRY(tw::gemm_backup_hidden(w.X, Wg, Wu, ra, o.n_ovf, ovf_cap, d, I, w.H, w.H_lo, nullptr, nullptr,
                                   dev_status, s));
+    // the down projection spread over every SM (split-K into an fp32 accumulator),
+    // then the rows written out as bf16
     const uint16_t* A[2] = {w.H, w.H_lo};
     const uint16_t* B[2] = {Wd, Wd};
-    TW_TRY(tw::gemm_rows_times_nmajor(A, B, 2, ra, o.n_ovf, ovf_cap, I, d, y, d, o.ovf_rows, dev_status, s));
+    TW_TRY(tw::gemm_rows_times_nmajor_splitk(A, B, 2, ra, o.n_ovf, ovf_cap, I, d, w.acc, dev_status, s));
+    TW_TRY(tw::launch_scatter_rows_bf16(w.acc, d, o.n_ovf, ovf_cap, o.ovf_rows, y, d, s));
   }
   return TW_OK;
 }

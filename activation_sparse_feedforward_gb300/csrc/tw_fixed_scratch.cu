@@ -9,7 +9,7 @@
 // overflow path needs (the gathered overflow rows and their hidden activations)
 // taken from one fixed array in device memory that this file defines.
 //
-// The array is kFixedScratchBytes (16 MiB). Every GPU on which the library's code
+// The array is kFixedScratchBytes (20 MiB). Every GPU on which the library's code
 // is loaded holds it until the process exits. Every call uses the same array, and
 // the array keeps whatever the previous call left in it: nothing in it has to start
 // at zero, because every byte the forward reads from its scratch is written earlier
@@ -21,7 +21,7 @@
 
 namespace {
 
-constexpr size_t kFixedScratchBytes = static_cast<size_t>(16) << 20;
+constexpr size_t kFixedScratchBytes = static_cast<size_t>(20) << 20;
 constexpr int kMaxDevices = 64;
 
 std::mutex g_setup_mutex;

@@ -140,24 +140,6 @@ cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint
   return run_gemm<64, false, false, false, 8, EpiBackupHidden<false>>(maps, sh, ep, cap, s, "backup_hidden");
 }
 
-cudaError_t gemm_rows_times_nmajor(const uint16_t* const* A, const uint16_t* const* B, int segments, int rows_alloc,
-                                   const int32_t* n_dev, int cap, int K, int N, uint16_t* out, int ldo,
-                                   const int32_t* row_map, int32_t* status, cudaStream_t s) {
-  if (cap <= 0) return cudaSuccess;
-  if (segments < 1 || segments > GEMM_MAX_SEGMENTS) return cudaErrorInvalidValue;
-  GemmShape sh = shape_static(0, N, K, status);
-  sh.m_dev = n_dev;
-  sh.m_cap = cap;
-  sh.segments = segments;
-  GemmMaps maps;
-  for (int i = 0; i < segments; ++i)
-    if (!tmap_kmajor(&maps.a[i], A[i], rows_alloc, K, 128) || !tmap_mnmajor(&maps.b[i], B[i], K, N))
-      return cudaErrorInvalidValue;
-  fill_unused(maps, segments, segments);
-  EpiScatterBf16::Params ep{out, ldo, row_map};
-  return run_gemm<64, false, true, false, 8, EpiScatterBf16>(maps, sh, ep, cap, s, "backup_rows_gemm");
-}
-
 // Same product for few rows, spread over every SM: 256-wide column tiles, each tile's
 // K loop (all segments) cut into slices whose partial sums are added into the fp32
 // accumulator acc [cap, N] (zeroed here); launch_scatter_rows_bf16 then writes the

@@ -428,34 +428,6 @@ struct EpiRedF32 {
   TW_DEV void finish() {}
 };
 
-// out[row_map[m]][n] = bf16(acc) (row_map == nullptr: row m), row stride ldo.
-struct EpiScatterBf16 {
-  static constexpr int kStageBytes = 0;
-  struct Params {
-    uint16_t* out;
-    int ldo;
-    const int32_t* row_map;
-  };
-  const Params& p;
-  int m, M, n0;
-  TW_DEV EpiScatterBf16(const Params& p_, int m_, int M_, int n0_) : p(p_), m(m_), M(M_), n0(n0_) {}
-  TW_DEV void chunk(int c, const uint32_t (&v)[32], const uint32_t (&)[32]) {
-    if (m >= M) return;
-    const int r = p.row_map ? p.row_map[m] : m;
-    uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(r) * p.ldo + n0 + c * 32);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint4 q;
-      q.x = pack_bf16x2(__uint_as_float(v[8 * i + 0]), __uint_as_float(v[8 * i + 1]));
-      q.y = pack_bf16x2(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3]));
-      q.z = pack_bf16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5]));
-      q.w = pack_bf16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7]));
-      dst[i] = q;
-    }
-  }
-  TW_DEV void finish() {}
-};
-
 // Gate projection epilogue: a = bf16(ReLU(acc)) packed into TwELL. The thread owns
 // one token row; it walks its columns in ascending order, so every (row, tile)
 // ELL is filled in ascending column order without atomics. Only nonzeros are

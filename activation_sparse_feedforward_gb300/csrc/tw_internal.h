@@ -153,12 +153,6 @@ cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint
                                const int32_t* n_dev, int cap, int d, int I, uint16_t* H, uint16_t* H_lo,
                                float* save_a, float* save_u, int32_t* status, cudaStream_t s);
 
-// out[row_map[m]] = bf16(sum_s A[s] B[s]) over `segments` pairs, A[s] [rows_alloc, K]
-// K-major and B[s] stored [K, N] (N-major); M = n (device) rows, up to cap.
-cudaError_t gemm_rows_times_nmajor(const uint16_t* const* A, const uint16_t* const* B, int segments, int rows_alloc,
-                                   const int32_t* n_dev, int cap, int K, int N, uint16_t* out, int ldo,
-                                   const int32_t* row_map, int32_t* status, cudaStream_t s);
-
 // The same product spread over every SM with split K: partial sums are added into
 // the fp32 accumulator acc [cap, N] (zeroed first); launch_scatter_rows_bf16 writes
 // the finished rows.

@@ -154,11 +154,11 @@ tw_status twell_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* W
  * loop where cudaMalloc is off limits because it can synchronise the device and
  * stall for milliseconds. This call computes exactly what twell_ffn_fwd computes,
  * with the same arguments minus the workspace: the overflow path's scratch comes
- * from one fixed 16 MiB array in device memory that the library defines.
+ * from one fixed 20 MiB array in device memory that the library defines.
  *  - Limit: returns TW_EWORKSPACE (before enqueuing anything) when
- *    twell_ffn_fwd_workspace_size(T, d, I, W, C, ovf_cap) exceeds 16 MiB; at
+ *    twell_ffn_fwd_workspace_size(T, d, I, W, C, ovf_cap) exceeds 20 MiB; at
  *    d = 2048, I = 5632 that allows ovf_cap up to 512 overflow rows.
- *  - The array occupies 16 MiB on every GPU where the library's code is loaded,
+ *  - The array occupies 20 MiB on every GPU where the library's code is loaded,
  *    until the process exits.
  *  - The first call on each device looks up the array's device address (with that
  *    device current); make that first call before any stream capture.

@@ -191,8 +191,10 @@ def test_hybrid_full_size_sampled(name, backup_cap):
 @pytest.mark.parametrize("spec", [MEDIUM[0], MEDIUM[2], WORKLOADS["gated_fwd_d2048_i5632"]], ids=lambda s: s.name)
 def test_unfused_pipeline_equals_fused_forward(spec):
     """Dense a through memory, then the standalone packer, then the sparse part give
-    the fused forward's y bit for bit (same GEMM, same canonical TwELL, same sparse
-    kernels), and both match the oracle."""
+    the fused forward's y: bit for bit on the rows the sparse kernel serves (same
+    GEMM, same canonical TwELL, same sparse kernel), and on the overflow rows up to
+    the order of the split-K fp32 additions of their dense down projection; both
+    match the oracle."""
     inp = make_inputs(spec)
     dv = _dev_inputs(inp)
     f = tw.TwellFFN(spec.T, spec.d, spec.I, spec.W, spec.C)
@@ -205,7 +207,12 @@ def test_unfused_pipeline_equals_fused_forward(spec):
     torch.cuda.synchronize()
     for s_ in (f.status, st, sp.status):
         tw.raise_if_device_error(s_)
-    assert torch.equal(y_unfused, y_fused)
+    sparse_rows = f.tw.ovf == 0
+    assert torch.equal(y_unfused[sparse_rows], y_fused[sparse_rows])
+    dense_rows = ~sparse_rows
+    if bool(dense_rows.any()):
+        # the same fp32 sums in another order, then bf16: a few one-ulp flips at most
+        assert_close(f64_of(y_unfused[dense_rows]), f64_of(y_fused[dense_rows]), "overflow rows", rel_frob=1e-3)
     for name in ("cnt", "row_nnz", "ovf"):
         assert torch.equal(getattr(packed, name), getattr(f.tw, name)), name
     # slots past a tile's count are padding (unspecified)

@@ -65,7 +65,7 @@ def test_fixed_scratch_matches_workspace_entry_point(lib, spec, ovf_cap):
 
 
 def test_fixed_scratch_rejects_shapes_beyond_its_size(lib):
-    # 513 overflow rows at d = 2048, I = 5632 need more than the 16 MiB array: refused on the host
+    # 513 overflow rows at d = 2048, I = 5632 need more than the 20 MiB array: refused on the host
     s = _lib.TwTwell(16384, 5632, 128, 16, 16, 16, 16, 16, 16, 16, 16)
     code = lib.twell_ffn_fwd_fixed_scratch(16, 16, 16, 16, 16384, 2048, 5632, 128, 16, 513, ctypes.byref(s),
                                            16, 16, None)
