@@ -450,6 +450,7 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
   a.col_cnt = w.col_cnt; a.col_ptr = w.col_ptr; a.col_cur = w.col_cur; a.csc = w.csc;
   a.dWg = dWg; a.dWu = dWu; a.dWd = dWd;
   a.sched = w.sched;
+  a.sched_w = w.sched + 1;
   TW_TRY(tw::launch_sparse_bwd_tokens(a, s));
   const bool backup = cap > 0 && T > 0;
   if (backup) {

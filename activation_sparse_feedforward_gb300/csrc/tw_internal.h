@@ -121,9 +121,10 @@ struct SparseBwdArgs {
   // when non-null and *dW_base_rows > 0, dW already holds the dense backup rows'
   // part and the ELL part is added to it; otherwise dW is overwritten
   const int32_t* dW_base_rows;
-  // token scheduling counter of the token pass (as SparseFwdArgs::sched); zeroed
-  // together with col_cnt
+  // scheduling counters (as SparseFwdArgs::sched) of the token pass and of the
+  // weight pass (sched_w = sched + 1); zeroed together with col_cnt
   int32_t* sched;
+  int32_t* sched_w;
 };
 // Token side of the ELL backward (tw_token.cu): dh, dg and du per entry, column
 // counts of the transposed Hybrid (col_cnt must be zero), dx.

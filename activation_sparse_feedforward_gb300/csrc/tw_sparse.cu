@@ -151,6 +151,13 @@ __global__ void __launch_bounds__(256) csc_fill_kernel(const SparseBwdArgs a) {
 // ({dg, dg, du, du}, {h, h, row}); a chunk whose length is not a multiple of the
 // unroll is padded with zero coefficients on the chunk's last row (an L1 hit), so
 // the inner loop has no predication and keeps kWgradUnroll row slices in flight.
+constexpr int kWgradChunk = 4;
+// the first item of a warp's next chunk: from the counter (zero at launch), or
+// round-robin without one
+TW_DEV int next_chunk(int32_t* sched, int prev, int nwarps) {
+  return sched != nullptr ? (nwarps + atomicAdd(sched, 1)) * kWgradChunk : prev + nwarps * kWgradChunk;
+}
+
 template <bool GATED>
 __global__ void __launch_bounds__(256, 3) ell_weight_grad_kernel(const SparseBwdArgs a) {
   pdl_enter();
@@ -165,7 +172,18 @@ __global__ void __launch_bounds__(256, 3) ell_weight_grad_kernel(const SparseBwd
   // dW already holds the dense backup rows' part when there are backup rows
   const bool add = a.dW_base_rows != nullptr && *a.dW_base_rows > 0;
   const int items = (a.d / 256) * a.I * 2;
-  for (int it = blockIdx.x * wpb + warp; it < items; it += gridDim.x * wpb) {
+  // Items are claimed kWgradChunk at a time, in order (slices outermost): a warp's
+  // first chunk by its index, the rest from the scheduling counter, so warps that
+  // drew long columns take fewer chunks.
+  const int nwarps = gridDim.x * wpb;
+  int it = (blockIdx.x * wpb + warp) * kWgradChunk, it_end = it + kWgradChunk;
+  for (; it < items; ++it) {
+    if (it == it_end) {
+      const int c0 = __shfl_sync(0xFFFFFFFFu, lane == 0 ? next_chunk(a.sched_w, it - kWgradChunk, nwarps) : 0, 0);
+      it = c0;
+      it_end = c0 + kWgradChunk;
+      if (it >= items) break;
+    }
     const bool xside = (it & 1) == 0;
     const int cj = it >> 1;
     const int c = cj / a.I;
@@ -225,7 +243,8 @@ __global__ void __launch_bounds__(256, 3) ell_weight_grad_kernel(const SparseBwd
 // ====================================================================== launchers
 template <bool GATED>
 static cudaError_t token_side(const SparseBwdArgs& a, cudaStream_t s) {
-  cudaError_t e = launch_zero(a.col_cnt, sizeof(int32_t) * (a.I + 1), a.sched, a.sched ? sizeof(int32_t) : 0, s);
+  // the token pass's and the weight pass's scheduling counters are adjacent words
+  cudaError_t e = launch_zero(a.col_cnt, sizeof(int32_t) * (a.I + 1), a.sched, a.sched ? 2 * sizeof(int32_t) : 0, s);
   if (e != cudaSuccess) return e;
   e = launch_token_bwd(a, s);  // dh, dg, du, column counts, dx
   if (e != cudaSuccess) return e;
