@@ -179,7 +179,7 @@ HybBwdWs carve_hybrid_bwd(Carve& c, int T, int d, int I, int R, int backup_cap) 
   w.g.H = c.take<uint16_t>(rI);
   w.g.H_lo = c.take<uint16_t>(rI);
   w.acc = c.take<float>(static_cast<size_t>(ra) * d);
-  w.sched = c.take<int32_t>(4);
+  w.sched = c.take<int32_t>(tw::kSchedWords);
   return w;
 }
 
@@ -450,7 +450,7 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
   a.col_cnt = w.col_cnt; a.col_ptr = w.col_ptr; a.col_cur = w.col_cur; a.csc = w.csc;
   a.dWg = dWg; a.dWu = dWu; a.dWd = dWd;
   a.sched = w.sched;
-  a.sched_w = w.sched + 1;
+  a.sched_w = w.sched + tw::kSchedStride;
   TW_TRY(tw::launch_sparse_bwd_tokens(a, s));
   const bool backup = cap > 0 && T > 0;
   if (backup) {

@@ -121,11 +121,15 @@ struct SparseBwdArgs {
   // when non-null and *dW_base_rows > 0, dW already holds the dense backup rows'
   // part and the ELL part is added to it; otherwise dW is overwritten
   const int32_t* dW_base_rows;
-  // scheduling counters (as SparseFwdArgs::sched) of the token pass and of the
-  // weight pass (sched_w = sched + 1); zeroed together with col_cnt
+  // scheduling counters (as SparseFwdArgs::sched): the token pass's at sched[0], the
+  // weight pass's kSchedCounters at sched_w = sched + kSchedStride, each
+  // kSchedStride ints apart; the kSchedWords ints are zeroed together with col_cnt
   int32_t* sched;
   int32_t* sched_w;
 };
+constexpr int kSchedCounters = 8;
+constexpr int kSchedStride = 32;  // ints: one 128-byte line per counter
+constexpr int kSchedWords = (1 + kSchedCounters) * kSchedStride;
 // Token side of the ELL backward (tw_token.cu): dh, dg and du per entry, column
 // counts of the transposed Hybrid (col_cnt must be zero), dx.
 cudaError_t launch_token_bwd(const SparseBwdArgs& a, cudaStream_t s);

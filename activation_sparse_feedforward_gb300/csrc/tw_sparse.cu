@@ -152,10 +152,15 @@ __global__ void __launch_bounds__(256) csc_fill_kernel(const SparseBwdArgs a) {
 // unroll is padded with zero coefficients on the chunk's last row (an L1 hit), so
 // the inner loop has no predication and keeps kWgradUnroll row slices in flight.
 constexpr int kWgradChunk = 4;
-// the first item of a warp's next chunk: from the counter (zero at launch), or
-// round-robin without one
-TW_DEV int next_chunk(int32_t* sched, int prev, int nwarps) {
-  return sched != nullptr ? (nwarps + atomicAdd(sched, 1)) * kWgradChunk : prev + nwarps * kWgradChunk;
+// Chunks after the warps' first ones are handed out by kSchedCounters counters (each
+// in its own 128-byte line, zero at launch): counter q serves chunks
+// nwarps + q, nwarps + q + kSchedCounters, ... to the warps with index = q modulo
+// kSchedCounters, so no single address takes every claim. Returns the first item of
+// the warp's next chunk (round-robin without counters).
+TW_DEV int next_chunk(int32_t* sched, int prev, int nwarps, int gwarp) {
+  if (sched == nullptr) return prev + nwarps * kWgradChunk;
+  const int q = gwarp % kSchedCounters;
+  return (nwarps + q + kSchedCounters * atomicAdd(sched + q * kSchedStride, 1)) * kWgradChunk;
 }
 
 template <bool GATED>
@@ -175,11 +180,13 @@ __global__ void __launch_bounds__(256, 3) ell_weight_grad_kernel(const SparseBwd
   // Items are claimed kWgradChunk at a time, in order (slices outermost): a warp's
   // first chunk by its index, the rest from the scheduling counter, so warps that
   // drew long columns take fewer chunks.
-  const int nwarps = gridDim.x * wpb;
-  int it = (blockIdx.x * wpb + warp) * kWgradChunk, it_end = it + kWgradChunk;
+  const int nwarps = gridDim.x * wpb, gwarp = blockIdx.x * wpb + warp;
+  int32_t* const sched = nwarps >= kSchedCounters ? a.sched_w : nullptr;  // every counter needs its warps
+  int it = gwarp * kWgradChunk, it_end = it + kWgradChunk;
   for (; it < items; ++it) {
     if (it == it_end) {
-      const int c0 = __shfl_sync(0xFFFFFFFFu, lane == 0 ? next_chunk(a.sched_w, it - kWgradChunk, nwarps) : 0, 0);
+      const int c0 =
+          __shfl_sync(0xFFFFFFFFu, lane == 0 ? next_chunk(sched, it - kWgradChunk, nwarps, gwarp) : 0, 0);
       it = c0;
       it_end = c0 + kWgradChunk;
       if (it >= items) break;
@@ -243,8 +250,9 @@ __global__ void __launch_bounds__(256, 3) ell_weight_grad_kernel(const SparseBwd
 // ====================================================================== launchers
 template <bool GATED>
 static cudaError_t token_side(const SparseBwdArgs& a, cudaStream_t s) {
-  // the token pass's and the weight pass's scheduling counters are adjacent words
-  cudaError_t e = launch_zero(a.col_cnt, sizeof(int32_t) * (a.I + 1), a.sched, a.sched ? 2 * sizeof(int32_t) : 0, s);
+  // the token pass's and the weight pass's scheduling counters (kSchedWords ints)
+  cudaError_t e =
+      launch_zero(a.col_cnt, sizeof(int32_t) * (a.I + 1), a.sched, a.sched ? sizeof(int32_t) * kSchedWords : 0, s);
   if (e != cudaSuccess) return e;
   e = launch_token_bwd(a, s);  // dh, dg, du, column counts, dx
   if (e != cudaSuccess) return e;
