@@ -15,7 +15,7 @@ namespace tw {
 
 namespace {
 
-constexpr int kWgradUnroll = 8;
+constexpr int kWgradUnroll = 4;
 
 // ---------------------------------------------------------------- row arithmetic
 // The accumulation is bound by instruction issue, so it uses Blackwell's packed
@@ -164,7 +164,7 @@ TW_DEV int next_chunk(int32_t* sched, int prev, int nwarps, int gwarp) {
 }
 
 template <bool GATED>
-__global__ void __launch_bounds__(256, 3) ell_weight_grad_kernel(const SparseBwdArgs a) {
+__global__ void __launch_bounds__(256, 4) ell_weight_grad_kernel(const SparseBwdArgs a) {
   pdl_enter();
   constexpr int U = kWgradUnroll;
   static_assert(32 % U == 0, "the unroll must divide the staging chunk");
@@ -271,7 +271,7 @@ cudaError_t launch_sparse_bwd_tokens(const SparseBwdArgs& a, cudaStream_t s) {
 
 cudaError_t launch_sparse_bwd_weights(const SparseBwdArgs& a, cudaStream_t s) {
   const long items = static_cast<long>(a.d / 256) * a.I * 2;
-  const dim3 grid(grid_for(items, 8, 3));
+  const dim3 grid(grid_for(items, 8, 4));
   const cudaError_t e = a.Wu != nullptr ? launch(ell_weight_grad_kernel<true>, grid, dim3(256), 0, s, a)
                                         : launch(ell_weight_grad_kernel<false>, grid, dim3(256), 0, s, a);
   trace_mark(s, "ell_weight_grad");
