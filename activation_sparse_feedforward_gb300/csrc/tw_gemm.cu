@@ -142,15 +142,13 @@ cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint
 
 // Same product for few rows, spread over every SM: 256-wide column tiles, each tile's
 // K loop (all segments) cut into slices whose partial sums are added into the fp32
-// accumulator acc [cap, N] (zeroed here); launch_scatter_rows_bf16 then writes the
-// bf16 rows out.
+// accumulator acc [cap, N] (zeroed beforehand, by the row gather); launch_scatter_rows_bf16
+// then writes the bf16 rows out.
 cudaError_t gemm_rows_times_nmajor_splitk(const uint16_t* const* A, const uint16_t* const* B, int segments,
                                           int rows_alloc, const int32_t* n_dev, int cap, int K, int N, float* acc,
                                           int32_t* status, cudaStream_t s) {
   if (cap <= 0) return cudaSuccess;
   if (segments < 1 || segments > GEMM_MAX_SEGMENTS || N % 256 != 0) return cudaErrorInvalidValue;
-  cudaError_t e = launch_zero(acc, sizeof(float) * static_cast<size_t>(cap) * N, nullptr, 0, s);
-  if (e != cudaSuccess) return e;
   GemmShape sh = shape_static(0, N, K, status);
   sh.m_dev = n_dev;
   sh.m_cap = cap;

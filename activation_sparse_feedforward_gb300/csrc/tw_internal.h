@@ -66,10 +66,14 @@ cudaError_t launch_reinit_rows(uint16_t* W, int I, int d, const int32_t* counts,
                                int32_t* n_reinit, cudaStream_t s);
 
 // out[i] = src[rows[i]] for i < min(*n, cap); rows [n, round_up(n, 128)) (below
-// rows_alloc) are zero-filled. Row length d bf16.
+// rows_alloc) are zero-filled. Row length d bf16. With src2/out2 the same rows of a
+// second matrix are gathered in the same launch; with zero_f32 that many floats at
+// `zero` are set to 0 (a split-K accumulator the next kernels add into).
 // Raises TW_ECAPACITY into `status` (when non-null) if *n > cap.
 cudaError_t launch_gather_rows(const uint16_t* src, int d, const int32_t* rows, const int32_t* n, int cap,
-                               int rows_alloc, uint16_t* out, cudaStream_t s, int32_t* status = nullptr);
+                               int rows_alloc, uint16_t* out, cudaStream_t s, int32_t* status = nullptr,
+                               const uint16_t* src2 = nullptr, uint16_t* out2 = nullptr, float* zero = nullptr,
+                               size_t zero_f32 = 0);
 
 // Largest per-token entry list of the sparse forward, (I / W) * C: two lists of
 // 10 bytes an entry live in one CTA's shared memory.
@@ -159,8 +163,8 @@ cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint
                                float* save_a, float* save_u, int32_t* status, cudaStream_t s);
 
 // The same product spread over every SM with split K: partial sums are added into
-// the fp32 accumulator acc [cap, N] (zeroed first); launch_scatter_rows_bf16 writes
-// the finished rows.
+// the fp32 accumulator acc [cap, N], which must hold zeros (launch_gather_rows zeroes
+// it alongside the row gather); launch_scatter_rows_bf16 writes the finished rows.
 cudaError_t gemm_rows_times_nmajor_splitk(const uint16_t* const* A, const uint16_t* const* B, int segments,
                                           int rows_alloc, const int32_t* n_dev, int cap, int K, int N, float* acc,
                                           int32_t* status, cudaStream_t s);

@@ -314,26 +314,42 @@ cudaError_t launch_compact_rows(const uint8_t* ovf, const int32_t* row_nnz, int 
 }
 
 // ================================================================ row gather
-__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ src, int d,
-                                                          const int32_t* __restrict__ rows,
-                                                          const int32_t* __restrict__ n_dev, int cap, int rows_alloc,
-                                                          uint16_t* __restrict__ out, int32_t* status) {
+struct GatherArgs {
+  const uint16_t* src[2];
+  uint16_t* out[2];
+  int nsrc, d;
+  const int32_t* rows;
+  const int32_t* n_dev;
+  int cap, rows_alloc;
+  float* zero;
+  size_t zero_f32;
+  int32_t* status;
+};
+__global__ void __launch_bounds__(256) gather_rows_kernel(const GatherArgs g) {
   pdl_enter();
-  if (status != nullptr && blockIdx.x == 0 && threadIdx.x == 0 && *n_dev > cap) raise_status(status, TW_ECAPACITY);
-  const int n = min(max(*n_dev, 0), cap);
-  const int limit = min(rows_alloc, (n + 127) / 128 * 128);
+  if (g.status != nullptr && blockIdx.x == 0 && threadIdx.x == 0 && *g.n_dev > g.cap)
+    raise_status(g.status, TW_ECAPACITY);
+  const int n = min(max(*g.n_dev, 0), g.cap);
+  const int limit = min(g.rows_alloc, (n + 127) / 128 * 128);
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
-  const int vec = d / 8;
-  for (int i = blockIdx.x * wpb + (threadIdx.x >> 5); i < limit; i += gridDim.x * wpb) {
-    uint4* o = reinterpret_cast<uint4*>(out + static_cast<size_t>(i) * d);
+  const int vec = g.d / 8;
+  // one warp per (row, matrix)
+  for (int w = blockIdx.x * wpb + (threadIdx.x >> 5); w < limit * g.nsrc; w += gridDim.x * wpb) {
+    const int i = w / g.nsrc, which = w - i * g.nsrc;
+    uint4* o = reinterpret_cast<uint4*>(g.out[which] + static_cast<size_t>(i) * g.d);
     if (i < n) {
-      const uint4* r = reinterpret_cast<const uint4*>(src + static_cast<size_t>(rows[i]) * d);
+      const uint4* r = reinterpret_cast<const uint4*>(g.src[which] + static_cast<size_t>(g.rows[i]) * g.d);
       for (int c = lane; c < vec; c += 32) o[c] = __ldg(r + c);
     } else {
       for (int c = lane; c < vec; c += 32) o[c] = make_uint4(0, 0, 0, 0);
     }
   }
+  // the accumulator: 16-byte stores over the grid (zero_f32 is a multiple of 4)
+  const size_t z4 = g.zero_f32 / 4;
+  for (size_t k = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < z4;
+       k += static_cast<size_t>(gridDim.x) * blockDim.x)
+    reinterpret_cast<float4*>(g.zero)[k] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // out[row_map[i]][:] = bf16(acc[i][:]) for i < min(*n, cap): the finished rows of a
@@ -367,11 +383,28 @@ cudaError_t launch_scatter_rows_bf16(const float* acc, int N, const int32_t* n_d
 }
 
 cudaError_t launch_gather_rows(const uint16_t* src, int d, const int32_t* rows, const int32_t* n, int cap,
-                               int rows_alloc, uint16_t* out, cudaStream_t s, int32_t* status) {
+                               int rows_alloc, uint16_t* out, cudaStream_t s, int32_t* status, const uint16_t* src2,
+                               uint16_t* out2, float* zero, size_t zero_f32) {
   if (rows_alloc <= 0) return cudaSuccess;
-  const int grid = warp_grid(rows_alloc, 8);
-  cudaError_t e = launch(gather_rows_kernel, dim3(std::min(grid, device_sm_count() * 4)), dim3(256), 0, s, src, d, rows,
-                         n, cap, rows_alloc, out, status);
+  if (zero_f32 % 4 != 0 || (zero_f32 > 0 && reinterpret_cast<uintptr_t>(zero) % 16 != 0))
+    return cudaErrorInvalidValue;
+  GatherArgs g{};
+  g.src[0] = src;
+  g.out[0] = out;
+  g.src[1] = src2;
+  g.out[1] = out2;
+  g.nsrc = (src2 != nullptr && out2 != nullptr) ? 2 : 1;
+  g.d = d;
+  g.rows = rows;
+  g.n_dev = n;
+  g.cap = cap;
+  g.rows_alloc = rows_alloc;
+  g.zero = zero;
+  g.zero_f32 = zero != nullptr ? zero_f32 : 0;
+  g.status = status;
+  const long work = std::max<long>(static_cast<long>(rows_alloc) * g.nsrc, static_cast<long>(g.zero_f32 / 1024));
+  const int grid = warp_grid(work, 8);
+  cudaError_t e = launch(gather_rows_kernel, dim3(std::min(grid, device_sm_count() * 4)), dim3(256), 0, s, g);
   trace_mark(s, "gather_rows");
   return e;
 }
