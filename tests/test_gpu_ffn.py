@@ -233,3 +233,37 @@ def test_sparse_part_reports_overflow_beyond_capacity():
     sp(dv["x"], dv["Wg"], dv["Wu"], dv["Wd"], packed)
     with pytest.raises(tw.TwellError, match="TW_ECAPACITY"):
         tw.raise_if_device_error(sp.status)
+
+
+@pytest.mark.parametrize("spec", [MEDIUM[0], MEDIUM[1]], ids=lambda s: s.name)
+def test_workspaces_need_no_initial_contents(spec):
+    """The library's workspaces hold, among other scratch, the device counters from
+    which the gather kernels take their tokens and items; kernels earlier in the same
+    call zero them. Workspaces filled with 0xFF bytes (every counter -1, every list
+    garbage) must give the same results as fresh ones, twice in a row."""
+    inp = make_inputs(spec, with_dy=True)
+    dv = _dev_inputs(inp)
+    ref = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, spec.T // 4, gated=spec.gated)
+    y_ref = ref.forward(dv["x"], dv["Wg"], dv["Wu"], dv["Wd"]).clone()
+    g_ref = [t.clone() for t in ref.backward(dv["dy"], dv["x"], dv["Wg"], dv["Wu"], dv["Wd"], spec.l1)]
+    h = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, spec.T // 4, gated=spec.gated)
+    f = tw.TwellFFN(spec.T, spec.d, spec.I, spec.W, spec.C, ovf_cap=spec.T // 4)
+    y_twell_ref = f(dv["x"], dv["Wg"], dv["Wu"], dv["Wd"]).clone()
+    for _ in range(2):
+        for ws in (h.fwd_ws, h.bwd_ws, f.ws):
+            ws.fill_(0xFF)
+        y = h.forward(dv["x"], dv["Wg"], dv["Wu"], dv["Wd"])
+        grads = h.backward(dv["dy"], dv["x"], dv["Wg"], dv["Wu"], dv["Wd"], spec.l1)
+        y_twell = f(dv["x"], dv["Wg"], dv["Wu"], dv["Wd"])
+        torch.cuda.synchronize()
+        for s_ in (ref.status, h.status, f.status):
+            tw.raise_if_device_error(s_)
+        # the sparse rows' arithmetic is fixed; split-K sums of the dense rows and the
+        # column order of the weight-gradient records may differ in the last bits
+        assert_close(f64_of(y), f64_of(y_ref), "y with dirty workspaces", rel_frob=1e-3)
+        assert_close(f64_of(y_twell), f64_of(y_twell_ref), "TwELL y with dirty workspaces", rel_frob=1e-3)
+        for got, want, name in zip(grads, g_ref, ("dx", "dWg", "dWu", "dWd")):
+            if got is None:
+                continue
+            assert_close(got.float().cpu().numpy(), want.float().cpu().numpy(), f"{name} with dirty workspaces",
+                         rel_frob=1e-3)
