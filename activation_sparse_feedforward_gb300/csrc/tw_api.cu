@@ -285,7 +285,7 @@ static tw_status twell_sparse_impl(const uint16_t* x, const uint16_t* Wg, const 
   TW_TRY(tw::launch_token_fwd(a, s));
   if (ovf_cap > 0) {
     TW_TRY(tw::launch_gather_rows(x, d, o.ovf_rows, o.n_ovf, ovf_cap, ra, w.X, s, dev_status, nullptr, nullptr,
-                                  w.acc, static_cast<size_t>(ovf_cap) * d));
+                                  w.acc, d));
     TW_TRY(tw::gemm_backup_hidden(w.X, Wg, Wu, ra, o.n_ovf, ovf_cap, d, I, w.H, w.H_lo, nullptr, nullptr,
                                   dev_status, s));
     // the down projection spread over every SM (split-K into an fp32 accumulator),
@@ -396,7 +396,7 @@ tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* 
   TW_TRY(tw::launch_token_fwd(a, s));
   if (cap > 0) {
     TW_TRY(tw::launch_gather_rows(x, d, saved->backup_tok, saved->n_backup, cap, ra, w.X, s, nullptr, nullptr,
-                                  nullptr, w.acc, static_cast<size_t>(cap) * d));
+                                  nullptr, w.acc, d));
     TW_TRY(tw::gemm_backup_hidden(w.X, Wg, Wu, ra, saved->n_backup, cap, d, I, w.H, w.H_lo, saved->backup_a,
                                   gated ? saved->backup_u : nullptr, dev_status, s));
     const uint16_t* A[2] = {w.H, w.H_lo};
@@ -457,7 +457,7 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
   const bool backup = cap > 0 && T > 0;
   if (backup) {
     TW_TRY(tw::launch_gather_rows(dy, d, saved->backup_tok, saved->n_backup, cap, ra, w.dY, s, nullptr, x, w.X,
-                                  w.acc, static_cast<size_t>(cap) * d));
+                                  w.acc, d));
     const int32_t* nb = saved->n_backup;
     const tw::BackupGradOut& g = w.g;
     TW_TRY(tw::gemm_backup_grad(w.dY, Wd, ra, nb, cap, d, I, saved->backup_a, gated ? saved->backup_u : nullptr,

@@ -67,13 +67,14 @@ cudaError_t launch_reinit_rows(uint16_t* W, int I, int d, const int32_t* counts,
 
 // out[i] = src[rows[i]] for i < min(*n, cap); rows [n, round_up(n, 128)) (below
 // rows_alloc) are zero-filled. Row length d bf16. With src2/out2 the same rows of a
-// second matrix are gathered in the same launch; with zero_f32 that many floats at
-// `zero` are set to 0 (a split-K accumulator the next kernels add into).
+// second matrix are gathered in the same launch; with `zero`, rows [0, min(*n, cap))
+// of that fp32 accumulator (zero_row_f32 floats a row, a multiple of 4) are set to 0
+// for the split-K product that adds into them next.
 // Raises TW_ECAPACITY into `status` (when non-null) if *n > cap.
 cudaError_t launch_gather_rows(const uint16_t* src, int d, const int32_t* rows, const int32_t* n, int cap,
                                int rows_alloc, uint16_t* out, cudaStream_t s, int32_t* status = nullptr,
                                const uint16_t* src2 = nullptr, uint16_t* out2 = nullptr, float* zero = nullptr,
-                               size_t zero_f32 = 0);
+                               int zero_row_f32 = 0);
 
 // Largest per-token entry list of the sparse forward, (I / W) * C: two lists of
 // 10 bytes an entry live in one CTA's shared memory.

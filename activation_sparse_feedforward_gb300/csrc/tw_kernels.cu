@@ -322,7 +322,7 @@ struct GatherArgs {
   const int32_t* n_dev;
   int cap, rows_alloc;
   float* zero;
-  size_t zero_f32;
+  int zero_row_f32;  // floats per accumulator row; rows [0, min(n, cap)) are zeroed
   int32_t* status;
 };
 __global__ void __launch_bounds__(256) gather_rows_kernel(const GatherArgs g) {
@@ -345,8 +345,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const GatherArgs g) {
       for (int c = lane; c < vec; c += 32) o[c] = make_uint4(0, 0, 0, 0);
     }
   }
-  // the accumulator: 16-byte stores over the grid (zero_f32 is a multiple of 4)
-  const size_t z4 = g.zero_f32 / 4;
+  // the accumulator rows the split-K product adds into: 16-byte stores over the grid
+  const size_t z4 = static_cast<size_t>(n) * g.zero_row_f32 / 4;
   for (size_t k = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < z4;
        k += static_cast<size_t>(gridDim.x) * blockDim.x)
     reinterpret_cast<float4*>(g.zero)[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -384,9 +384,9 @@ cudaError_t launch_scatter_rows_bf16(const float* acc, int N, const int32_t* n_d
 
 cudaError_t launch_gather_rows(const uint16_t* src, int d, const int32_t* rows, const int32_t* n, int cap,
                                int rows_alloc, uint16_t* out, cudaStream_t s, int32_t* status, const uint16_t* src2,
-                               uint16_t* out2, float* zero, size_t zero_f32) {
+                               uint16_t* out2, float* zero, int zero_row_f32) {
   if (rows_alloc <= 0) return cudaSuccess;
-  if (zero_f32 % 4 != 0 || (zero_f32 > 0 && reinterpret_cast<uintptr_t>(zero) % 16 != 0))
+  if (zero_row_f32 % 4 != 0 || (zero != nullptr && reinterpret_cast<uintptr_t>(zero) % 16 != 0))
     return cudaErrorInvalidValue;
   GatherArgs g{};
   g.src[0] = src;
@@ -400,9 +400,9 @@ cudaError_t launch_gather_rows(const uint16_t* src, int d, const int32_t* rows, 
   g.cap = cap;
   g.rows_alloc = rows_alloc;
   g.zero = zero;
-  g.zero_f32 = zero != nullptr ? zero_f32 : 0;
+  g.zero_row_f32 = zero != nullptr ? zero_row_f32 : 0;
   g.status = status;
-  const long work = std::max<long>(static_cast<long>(rows_alloc) * g.nsrc, static_cast<long>(g.zero_f32 / 1024));
+  const long work = static_cast<long>(rows_alloc) * g.nsrc;
   const int grid = warp_grid(work, 8);
   cudaError_t e = launch(gather_rows_kernel, dim3(std::min(grid, device_sm_count() * 4)), dim3(256), 0, s, g);
   trace_mark(s, "gather_rows");
