@@ -23,7 +23,8 @@
  *   give each warp of a token's CTA one 256-wide slice of d); W in {64, 128};
  *   I % W == 0, 64 <= I <= 65536; 1 <= C <= W; (I / W) * C <= 10240 (a token's
  *   entry list lives in shared memory); 1 <= R <= I; 0 <= backup_cap <= T.
- *   T == 0 is a valid no-op. Other shapes return TW_EUNSUPPORTED.
+ *   T == 0 is valid: the forwards and packers do nothing, and hybrid_ffn_bwd
+ *   writes dW = 0 (sums over no tokens). Other shapes return TW_EUNSUPPORTED.
  * - Alignment: every pointer must be 16-byte aligned (TMA and 128-bit accesses).
  * - Ownership: the caller allocates and frees every buffer, including the
  *   workspace whose size the *_workspace_size() functions return. The library
