@@ -44,6 +44,11 @@ TW_DEV uint16_t f32_to_bf16(float v) { return __bfloat16_as_ushort(__float2bfloa
 TW_DEV uint32_t pack_bf16x2(float lo, float hi) {
   return static_cast<uint32_t>(f32_to_bf16(lo)) | (static_cast<uint32_t>(f32_to_bf16(hi)) << 16);
 }
+// the same with one paired conversion (round to nearest even on both halves)
+TW_DEV uint32_t pack_bf16x2_rn(float lo, float hi) {
+  const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
 
 // ------------------------------------------------------------------ smem / timers
 TW_DEV uint32_t smem_addr(const void* p) {

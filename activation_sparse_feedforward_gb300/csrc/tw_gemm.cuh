@@ -433,8 +433,15 @@ struct EpiRedF32 {
 // ELL is filled in ascending column order without atomics. Only nonzeros are
 // stored (padding slots stay untouched); cnt is always written; row_nnz and ovf
 // are combined across column tiles with one atomic per (row, CTA tile).
+// Per 32-column chunk the thread converts its values two at a time, forms a bit mask
+// of the nonzero bf16 results and visits only the set bits; the chunk's bf16 words
+// sit in the thread's part of the staging buffer so a set bit's value is read by
+// index (a register array indexed at run time would go to local memory). Most rows
+// have one or two nonzeros in a chunk, so the loop is short and has no per-column
+// branch.
 struct EpiTwellPack {
-  static constexpr int kStageBytes = 0;
+  static constexpr int kStageBytes = kEpiTransposeBytes;  // 20 words a thread (80 B) fit a warp's region
+  static constexpr int kWordsPerLane = 20;
   struct Params {
     int T, W, C, nT;
     uint16_t* cnt;
@@ -451,6 +458,7 @@ struct EpiTwellPack {
   int c_tile;   // nonzeros seen so far in the current TwELL tile
   int total;    // nonzeros of this row in this CTA tile
   bool any_ovf;
+  float* stage = nullptr;  // this warp's staging buffer
   TW_DEV EpiTwellPack(const Params& p_, int m_, int M_, int n0_)
       : p(p_), m(m_), n0(n0_), valid(m_ < M_), c_tile(0), total(0), any_ovf(false) {}
   TW_DEV void chunk(int c, const uint32_t (&v)[32], const uint32_t (&)[32]) {
@@ -458,28 +466,35 @@ struct EpiTwellPack {
     const int col0 = n0 + c * 32;
     const int k = col0 / p.W;
     const int local0 = col0 - k * p.W;
-    const size_t slot_base = (static_cast<size_t>(m) * p.nT + k) * p.C;
-    uint32_t packed[16];
+    uint32_t w[16];
+    uint32_t mask = 0u;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float g = __uint_as_float(v[i]);
-      const uint16_t a = f32_to_bf16(g > 0.0f ? g : 0.0f);
-      if (i & 1)
-        packed[i >> 1] |= static_cast<uint32_t>(a) << 16;
-      else
-        packed[i >> 1] = a;
-      if (a & 0x7FFFu) {
-        if (c_tile < p.C) {
-          p.val[slot_base + c_tile] = a;
-          p.idx[slot_base + c_tile] = static_cast<uint8_t>(local0 + i);
-        }
-        ++c_tile;
-      }
+    for (int q = 0; q < 16; ++q) {
+      const float g0 = __uint_as_float(v[2 * q]), g1 = __uint_as_float(v[2 * q + 1]);
+      w[q] = pack_bf16x2_rn(g0 > 0.0f ? g0 : 0.0f, g1 > 0.0f ? g1 : 0.0f);
+      mask |= ((w[q] & 0x7FFFu) != 0u ? 1u : 0u) << (2 * q);
+      mask |= ((w[q] & 0x7FFF0000u) != 0u ? 1u : 0u) << (2 * q + 1);
     }
     if (p.a_dense != nullptr) {
       uint4* dst = reinterpret_cast<uint4*>(p.a_dense + static_cast<size_t>(m) * p.lda + col0);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+      for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    }
+    const int before = c_tile;
+    c_tile += __popc(mask);
+    if (mask != 0u && before < p.C) {
+      uint32_t* mine = reinterpret_cast<uint32_t*>(stage) + (threadIdx.x & 31) * kWordsPerLane;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        reinterpret_cast<uint4*>(mine)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      const size_t slot_base = (static_cast<size_t>(m) * p.nT + k) * p.C;
+      for (int s = before; mask != 0u && s < p.C; ++s) {
+        const int i = __ffs(mask) - 1;
+        mask &= mask - 1u;
+        const uint32_t word = mine[i >> 1];
+        p.val[slot_base + s] = static_cast<uint16_t>((i & 1) ? (word >> 16) : (word & 0xFFFFu));
+        p.idx[slot_base + s] = static_cast<uint8_t>(local0 + i);
+      }
     }
     if (local0 + 32 == p.W) {  // last chunk of this TwELL tile
       p.cnt[static_cast<size_t>(m) * p.nT + k] = static_cast<uint16_t>(c_tile);
@@ -494,6 +509,8 @@ struct EpiTwellPack {
     if (any_ovf) p.ovf[m] = 1;
   }
 };
+static_assert(EpiTwellPack::kWordsPerLane * 4 * 32 <= kEpiStageStride * 32 * 4,
+              "a warp's staging region holds 32 lanes of 20 words");
 
 // Eight fp32 values as an exact-to-2^-16 pair of bf16 vectors: hi = bf16(v),
 // lo = bf16(v - hi). A GEMM run over both halves (two K segments against the same
