@@ -469,9 +469,11 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
     TW_TRY(tw::launch_scatter_rows_bf16(w.acc, d, nb, cap, saved->backup_tok, dx, d, s));
     // the backup rows' weight gradients are written first (when there are any);
     // the ELL part is then added to them
-    TW_TRY(tw::gemm_weight_grad(g.dG, g.dG_lo, w.X, ra, nb, cap, I, d, dWg, dev_status, s));
-    if (gated) TW_TRY(tw::gemm_weight_grad(g.dU, g.dU_lo, w.X, ra, nb, cap, I, d, dWu, dev_status, s));
-    TW_TRY(tw::gemm_weight_grad(g.H, g.H_lo, w.dY, ra, nb, cap, I, d, dWd, dev_status, s));
+    // all (two or three) in one launch
+    const tw::WeightGradProblem probs[3] = {{g.dG, g.dG_lo, w.X, dWg},
+                                            {g.H, g.H_lo, w.dY, dWd},
+                                            {g.dU, g.dU_lo, w.X, dWu}};
+    TW_TRY(tw::gemm_weight_grads(probs, gated ? 3 : 2, ra, nb, cap, I, d, dev_status, s));
   }
   a.dW_base_rows = backup ? saved->n_backup : nullptr;
   TW_TRY(tw::launch_sparse_bwd_weights(a, s));

@@ -78,6 +78,7 @@ static GemmShape shape_static(int M, int N, int K, int32_t* status) {
   g.k_dev = nullptr;
   g.k_cap = K;
   g.segments = 1;
+  g.problems = 1;
   g.status = status;
   return g;
 }
@@ -183,22 +184,31 @@ cudaError_t gemm_backup_grad(const uint16_t* dY, const uint16_t* Wd, int rows_al
   return run_gemm<64, false, false, false, 8, EpiBackupGrad<false>>(maps, sh, ep, cap, s, "backup_grad");
 }
 
-cudaError_t gemm_weight_grad(const uint16_t* P_hi, const uint16_t* P_lo, const uint16_t* Q, int rows_alloc,
-                             const int32_t* n_dev, int cap, int I, int d, float* D, int32_t* status, cudaStream_t s) {
-  if (cap <= 0) return cudaSuccess;
+cudaError_t gemm_weight_grads(const WeightGradProblem* probs, int n_probs, int rows_alloc, const int32_t* n_dev,
+                              int cap, int I, int d, int32_t* status, cudaStream_t s) {
+  if (cap <= 0 || n_probs <= 0) return cudaSuccess;
+  if (n_probs > EpiStoreF32Grouped::kMaxProblems || d % 256 != 0) return cudaErrorInvalidValue;
   GemmShape sh = shape_static(I, d, 0, status);
   sh.k_dev = n_dev;
   sh.k_cap = cap;
-  sh.segments = 2;
+  sh.segments = 2;  // P = P_hi + P_lo
+  sh.problems = n_probs;
   GemmMaps maps;
-  if (!tmap_mnmajor(&maps.a[0], P_hi, rows_alloc, I) || !tmap_mnmajor(&maps.a[1], P_lo, rows_alloc, I) ||
-      !tmap_mnmajor(&maps.b[0], Q, rows_alloc, d))
-    return cudaErrorInvalidValue;
-  maps.b[1] = maps.b[0];
-  fill_unused(maps, 2, 2);
-  EpiStoreF32::Params ep{D, d};
-  if (d % 256 == 0) return run_gemm<256, true, true, false, 4, EpiStoreF32>(maps, sh, ep, I, s, "backup_weight_grad");
-  return run_gemm<64, true, true, false, 8, EpiStoreF32>(maps, sh, ep, I, s, "backup_weight_grad");
+  EpiStoreF32Grouped::Params ep{};
+  for (int p = 0; p < n_probs; ++p) {
+    if (!tmap_mnmajor(&maps.a[2 * p], probs[p].P_hi, rows_alloc, I) ||
+        !tmap_mnmajor(&maps.a[2 * p + 1], probs[p].P_lo, rows_alloc, I) ||
+        !tmap_mnmajor(&maps.b[2 * p], probs[p].Q, rows_alloc, d))
+      return cudaErrorInvalidValue;
+    maps.b[2 * p + 1] = maps.b[2 * p];
+    ep.D[p] = probs[p].D;
+  }
+  fill_unused(maps, 2 * n_probs, 2 * n_probs);
+  ep.ldd = d;
+  // each problem takes whole 128-row tiles; rows I .. of its last tile are skipped
+  ep.rows_per_problem = (I + GEMM_BM - 1) / GEMM_BM * GEMM_BM;
+  return run_gemm<256, true, true, false, 4, EpiStoreF32Grouped>(maps, sh, ep, ep.rows_per_problem * n_probs, s,
+                                                                  "backup_weight_grad");
 }
 
 // ------------------------------------------------------------------ layout test GEMM

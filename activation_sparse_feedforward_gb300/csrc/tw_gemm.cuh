@@ -40,7 +40,10 @@ struct GemmShape {
   int K;             // reduction length when k_dev == nullptr
   const int* k_dev;  // optional device K, clamped to [0, k_cap]; memory past K must read as zero
   int k_cap;
-  int segments;      // 1 to 4 (A, B) pairs
+  int segments;      // (A, B) pairs summed into each output tile
+  int problems;      // 1, or several products of the same shape in one launch: problem
+                     // p reads maps a/b[p * segments + s]; its row tiles follow the
+                     // previous problem's (the epilogue sees rows p * m_tiles * 128 + m)
   int ksplit;        // >= 1: each output tile's K loop is cut into ksplit work units
                      // (only for epilogues that accumulate, e.g. EpiRedF32); < 0:
                      // chosen on the device from the actual tile count so that the
@@ -48,10 +51,10 @@ struct GemmShape {
   int32_t* status;
 };
 
-constexpr int GEMM_MAX_SEGMENTS = 4;
+constexpr int GEMM_MAX_SEGMENTS = 6;  // segments x problems
 
-// Tensor maps of every operand: segment s reads a[s] and b[s]; the DUAL form reads
-// b[0] and b[1] against a[0].
+// Tensor maps of every operand: segment s of problem p reads a[p * segments + s] and
+// b[p * segments + s]; the DUAL form reads b[0] and b[1] against a[0].
 struct GemmMaps {
   CUtensorMap a[GEMM_MAX_SEGMENTS];
   CUtensorMap b[GEMM_MAX_SEGMENTS];
@@ -105,7 +108,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
-    for (int sgi = 0; sgi < shape.segments; ++sgi) {
+    for (int sgi = 0; sgi < shape.segments * max(1, shape.problems); ++sgi) {
       tma_prefetch_desc(&maps.a[sgi]);
       tma_prefetch_desc(&maps.b[sgi]);
     }
@@ -127,7 +130,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (shape.k_dev != nullptr) K = min(max(*shape.k_dev, 0), shape.k_cap);
   const int m_tiles = (M + GEMM_BM - 1) / GEMM_BM;
   const int n_tiles = shape.N / BN;
-  const int num_tiles = (K > 0) ? m_tiles * n_tiles : 0;
+  const int problems = max(1, shape.problems);
+  const int num_tiles = (K > 0) ? problems * m_tiles * n_tiles : 0;
   const int kb_per_seg = (K + GEMM_BK - 1) / GEMM_BK;
   const int kb_total = kb_per_seg * shape.segments;
   // work unit = (output tile, slice of its K loop); empty slices are skipped by
@@ -149,7 +153,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int kb_lo = (unit - tile * ksplit) * kb_chunk;
         const int kb_hi = min(kb_total, kb_lo + kb_chunk);
         if (kb_lo >= kb_hi) continue;
-        const int m0 = (tile / n_tiles) * GEMM_BM;
+        const int row_tile = tile / n_tiles;
+        const int prob = row_tile / m_tiles;
+        const int m0 = (row_tile - prob * m_tiles) * GEMM_BM;  // within the problem
         const int n0 = (tile % n_tiles) * BN;
         for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, shape.status)) {
@@ -160,8 +166,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           uint8_t* sB = sA + Tr::A_BYTES;
           const int seg = kb / kb_per_seg;
           const int k0 = (kb - seg * kb_per_seg) * GEMM_BK;
-          const CUtensorMap* ta = &maps.a[seg];
-          const CUtensorMap* tb = &maps.b[seg];
+          const CUtensorMap* ta = &maps.a[prob * shape.segments + seg];
+          const CUtensorMap* tb = &maps.b[prob * shape.segments + seg];
           mbar_arrive_expect_tx(full + stage, Tr::STAGE_BYTES);
           if (!A_MN) {
             tma_load_2d(sA, ta, full + stage, k0, m0);
@@ -349,6 +355,30 @@ struct EpiStoreF32 {
   TW_DEV void chunk(int c, const uint32_t (&v)[32], const uint32_t (&)[32]) {
     float* col = p.D + n0 + c * 32;
     transposed_rows(stage, v, m, M, [&](int r, int c4, float4 x) {
+      reinterpret_cast<float4*>(col + static_cast<size_t>(r) * p.ldd)[c4] = x;
+    });
+  }
+  TW_DEV void finish() {}
+};
+
+// EpiStoreF32 for a grouped launch: row m of the stacked tiles belongs to problem
+// m / rows_per_problem and is row m % rows_per_problem of that problem's D.
+struct EpiStoreF32Grouped {
+  static constexpr int kStageBytes = kEpiTransposeBytes;
+  static constexpr int kMaxProblems = 3;
+  struct Params {
+    float* D[kMaxProblems];
+    int ldd;
+    int rows_per_problem;  // the problem's row tiles x 128
+  };
+  const Params& p;
+  int m, M, n0;
+  float* stage = nullptr;  // this warp's transpose buffer
+  TW_DEV EpiStoreF32Grouped(const Params& p_, int m_, int M_, int n0_) : p(p_), m(m_), M(M_), n0(n0_) {}
+  TW_DEV void chunk(int c, const uint32_t (&v)[32], const uint32_t (&)[32]) {
+    const int prob = m / p.rows_per_problem;  // the same for the warp's 32 rows
+    float* col = p.D[prob] + n0 + c * 32;
+    transposed_rows(stage, v, m - prob * p.rows_per_problem, M, [&](int r, int c4, float4 x) {
       reinterpret_cast<float4*>(col + static_cast<size_t>(r) * p.ldd)[c4] = x;
     });
   }

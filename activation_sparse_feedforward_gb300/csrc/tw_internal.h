@@ -180,12 +180,18 @@ struct BackupGradOut {
 cudaError_t gemm_backup_grad(const uint16_t* dY, const uint16_t* Wd, int rows_alloc, const int32_t* n_dev, int cap,
                              int d, int I, const float* a, const float* u, float l1, const BackupGradOut& o,
                              int32_t* status, cudaStream_t s);
-
-// D[I, d] = (P_hi + P_lo)^T Q with P [rows_alloc, I] and Q [rows_alloc, d] (both
-// stored with the reduction over rows), K = n (device) rows, up to cap. Writes
-// nothing when n == 0.
-cudaError_t gemm_weight_grad(const uint16_t* P_hi, const uint16_t* P_lo, const uint16_t* Q, int rows_alloc,
-                             const int32_t* n_dev, int cap, int I, int d, float* D, int32_t* status, cudaStream_t s);
+// The dense backup rows' weight gradients, D_p = (P_hi,p + P_lo,p)^T Q_p for up to
+// three problems in one launch (P [rows, I] bf16 hi/lo pairs, Q [rows, d] bf16, K =
+// the device row count), written (overwritten) as fp32 [I, d]; nothing is written
+// when the row count is 0. Requires d % 256 == 0.
+struct WeightGradProblem {
+  const uint16_t* P_hi;
+  const uint16_t* P_lo;
+  const uint16_t* Q;
+  float* D;
+};
+cudaError_t gemm_weight_grads(const WeightGradProblem* probs, int n_probs, int rows_alloc, const int32_t* n_dev,
+                              int cap, int I, int d, int32_t* status, cudaStream_t s);
 
 cudaError_t gemm_dense_test(const uint16_t* A, const uint16_t* B, int M, int N, int K, int a_mn, int b_mn, float* D,
                             int32_t* status, cudaStream_t s);
