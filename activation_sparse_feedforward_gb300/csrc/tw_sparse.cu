@@ -168,12 +168,11 @@ __global__ void __launch_bounds__(256, 4) ell_weight_grad_kernel(const SparseBwd
   pdl_enter();
   constexpr int U = kWgradUnroll;
   static_assert(32 % U == 0, "the unroll must divide the staging chunk");
-  __shared__ float4 stage[8][2][32];
+  __shared__ float4 stage[8][32];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int wpb = blockDim.x >> 5;
-  float4(&cgu)[32] = stage[warp][0];
-  float4(&chr)[32] = stage[warp][1];
+  float4(&rec)[32] = stage[warp];  // {dg, du, h, row offset}: one 16-byte read a record
   // dW already holds the dense backup rows' part when there are backup rows
   const bool add = a.dW_base_rows != nullptr && *a.dW_base_rows > 0;
   const int items = (a.d / 256) * a.I * 2;
@@ -206,34 +205,39 @@ __global__ void __launch_bounds__(256, 4) ell_weight_grad_kernel(const SparseBwd
       const uint32_t last = __shfl_sync(0xFFFFFFFFu, r.x, m - 1);
       if (lane >= m) r.x = last;
       __syncwarp();  // the previous chunk's reads of the stage are done
-      const float cg = __uint_as_float(r.y), cu = __uint_as_float(r.z), ch = __uint_as_float(r.w);
-      cgu[lane] = make_float4(cg, cg, cu, cu);
-      chr[lane] = make_float4(ch, ch, __uint_as_float(r.x), 0.f);
+      rec[lane] = make_float4(__uint_as_float(r.y), __uint_as_float(r.z), __uint_as_float(r.w), __uint_as_float(r.x));
       __syncwarp();
       if (xside) {
         for (int k = 0; k < m; k += U) {
           uint4 v[U];
-#pragma unroll
-          for (int q = 0; q < U; ++q) v[q] = ldg16(src + __float_as_uint(chr[k + q].z));
+          float cg[U], cu[U];
 #pragma unroll
           for (int q = 0; q < U; ++q) {
-            const float4 e = cgu[k + q];
+            const float4 e = rec[k + q];
+            cg[q] = e.x;
+            cu[q] = e.y;
+            v[q] = ldg16(src + __float_as_uint(e.w));
+          }
+#pragma unroll
+          for (int q = 0; q < U; ++q) {
             if (GATED)
-              axpy8_two(p, f2(e.x, e.y), q2, f2(e.z, e.w), v[q]);
+              axpy8_two(p, f2(cg[q], cg[q]), q2, f2(cu[q], cu[q]), v[q]);
             else
-              axpy8(p, f2(e.x, e.y), v[q]);
+              axpy8(p, f2(cg[q], cg[q]), v[q]);
           }
         }
       } else {
         for (int k = 0; k < m; k += U) {
           uint4 v[U];
-#pragma unroll
-          for (int q = 0; q < U; ++q) v[q] = ldg16(src + __float_as_uint(chr[k + q].z));
+          float ch[U];
 #pragma unroll
           for (int q = 0; q < U; ++q) {
-            const float2 hh = *reinterpret_cast<const float2*>(&chr[k + q]);
-            axpy8(p, f2(hh.x, hh.y), v[q]);
+            const float4 e = rec[k + q];
+            ch[q] = e.z;
+            v[q] = ldg16(src + __float_as_uint(e.w));
           }
+#pragma unroll
+          for (int q = 0; q < U; ++q) axpy8(p, f2(ch[q], ch[q]), v[q]);
         }
       }
     }
