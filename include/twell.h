@@ -28,9 +28,15 @@
  * - Alignment: every pointer must be 16-byte aligned (TMA and 128-bit accesses).
  * - Ownership: the caller allocates and frees every buffer, including the
  *   workspace whose size the *_workspace_size() functions return. The library
- *   never allocates, frees or synchronises; it only enqueues kernels (and small
- *   cudaMemsetAsync calls) on `stream`, a cudaStream_t passed as void* (NULL =
- *   the legacy default stream).
+ *   never allocates, frees or synchronises; it only enqueues kernels on `stream`,
+ *   a cudaStream_t passed as void* (NULL = the legacy default stream).
+ * - Workspaces need no initial contents: every call zeroes, on its stream, what it
+ *   reads before writing (list counters, column counts, split-K accumulators, the
+ *   counters from which the sparse kernels take their tokens).
+ * - Determinism: TwELL and Hybrid contents, the ELL rows' y and dx, and every count
+ *   are the same on every run. The weight gradients and the dense rows' y and dx
+ *   (overflow / backup rows) are fp32 sums whose order depends on the order of
+ *   atomic updates, so they can differ in the last bits from run to run.
  * - Errors found on the host (bad shape, NULL or misaligned pointer, workspace too
  *   small) are returned synchronously before anything is enqueued. Launch errors
  *   return TW_ECUDA. Conditions only the GPU can see (a capacity exceeded, a
