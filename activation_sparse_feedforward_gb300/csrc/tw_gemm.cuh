@@ -13,11 +13,14 @@
 // A is [M, K] with K contiguous ("K-major") or stored [K, M] ("MN-major"); the same
 // for B with N in place of M. DUAL issues a second MMA with a second B operand into
 // its own accumulator (gate and up projections of the same rows in one pass).
-// `segments == S` (up to 4) continues the K loop over S (A, B) pairs into the same
+// `segments == S` continues the K loop over S (A, B) pairs into the same
 // accumulator: a second product (dx = dG Wg + dU Wu) or the low half of an operand
-// split into two bf16 parts (x = hi + lo) to keep fp32-level precision. M and K may
-// be read from device memory (counts produced by earlier kernels in the stream), so
-// the launch does not need them on the host.
+// split into two bf16 parts (x = hi + lo) to keep fp32-level precision.
+// `problems == P` runs P products of the same shape in one launch, their row tiles
+// one after the other (the backup rows' two or three weight gradients), so the
+// tiles of all of them share the persistent grid. M and K may be read from device
+// memory (counts produced by earlier kernels in the stream), so the launch does not
+// need them on the host.
 #pragma once
 
 #include "tw_common.cuh"
@@ -407,32 +410,6 @@ struct EpiReluBf16 {
     uint4* dst = reinterpret_cast<uint4*>(p.a + static_cast<size_t>(m) * p.lda + n0 + c * 32);
 #pragma unroll
     for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-  }
-  TW_DEV void finish() {}
-};
-
-// D[m][n] += acc (fp32 read-modify-write), row stride ldd.
-struct EpiAddF32 {
-  static constexpr int kStageBytes = 0;
-  struct Params {
-    float* D;
-    int ldd;
-  };
-  const Params& p;
-  int m, M, n0;
-  TW_DEV EpiAddF32(const Params& p_, int m_, int M_, int n0_) : p(p_), m(m_), M(M_), n0(n0_) {}
-  TW_DEV void chunk(int c, const uint32_t (&v)[32], const uint32_t (&)[32]) {
-    if (m >= M) return;
-    float4* dst = reinterpret_cast<float4*>(p.D + static_cast<size_t>(m) * p.ldd + n0 + c * 32);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float4 o = dst[i];
-      o.x += __uint_as_float(v[4 * i]);
-      o.y += __uint_as_float(v[4 * i + 1]);
-      o.z += __uint_as_float(v[4 * i + 2]);
-      o.w += __uint_as_float(v[4 * i + 3]);
-      dst[i] = o;
-    }
   }
   TW_DEV void finish() {}
 };
