@@ -165,23 +165,35 @@ cudaError_t gemm_rows_times_nmajor_splitk(const uint16_t* const* A, const uint16
 }
 
 // ------------------------------------------------------------------ dense backup, backward
-cudaError_t gemm_backup_grad(const uint16_t* dY, const uint16_t* Wd, int rows_alloc, const int32_t* n_dev, int cap,
-                             int d, int I, const float* a, const float* u, float l1, const BackupGradOut& o,
-                             int32_t* status, cudaStream_t s) {
-  if (cap <= 0) return cudaSuccess;
+// 128-wide column tiles when I allows them (one round of tiles on 152 SMs at the
+// common sizes), else 64-wide.
+template <int BN, bool GATED>
+static cudaError_t backup_grad_bn(const uint16_t* dY, const uint16_t* Wd, int rows_alloc, const int32_t* n_dev,
+                                  int cap, int d, int I, const float* a, const float* u, float l1,
+                                  const BackupGradOut& o, int32_t* status, cudaStream_t s) {
   GemmShape sh = shape_static(0, I, d, status);
   sh.m_dev = n_dev;
   sh.m_cap = cap;
   GemmMaps maps;
-  if (!tmap_kmajor(&maps.a[0], dY, rows_alloc, d, 128) || !tmap_kmajor(&maps.b[0], Wd, I, d, 64))
+  if (!tmap_kmajor(&maps.a[0], dY, rows_alloc, d, 128) || !tmap_kmajor(&maps.b[0], Wd, I, d, BN))
     return cudaErrorInvalidValue;
   fill_unused(maps, 1, 1);
-  if (u != nullptr) {
-    typename EpiBackupGrad<true>::Params ep{a, u, o.dG, o.dG_lo, o.dU, o.dU_lo, o.H, o.H_lo, l1, I, rows_alloc};
-    return run_gemm<64, false, false, false, 8, EpiBackupGrad<true>>(maps, sh, ep, cap, s, "backup_grad");
-  }
-  typename EpiBackupGrad<false>::Params ep{a, nullptr, o.dG, o.dG_lo, nullptr, nullptr, o.H, o.H_lo, l1, I, rows_alloc};
-  return run_gemm<64, false, false, false, 8, EpiBackupGrad<false>>(maps, sh, ep, cap, s, "backup_grad");
+  typename EpiBackupGrad<GATED>::Params ep{a,    u,  o.dG, o.dG_lo, GATED ? o.dU : nullptr, GATED ? o.dU_lo : nullptr,
+                                           o.H,  o.H_lo, l1,  I,       rows_alloc};
+  constexpr int kStages = BN == 128 ? 4 : 8;
+  return run_gemm<BN, false, false, false, kStages, EpiBackupGrad<GATED>>(maps, sh, ep, cap, s, "backup_grad");
+}
+
+cudaError_t gemm_backup_grad(const uint16_t* dY, const uint16_t* Wd, int rows_alloc, const int32_t* n_dev, int cap,
+                             int d, int I, const float* a, const float* u, float l1, const BackupGradOut& o,
+                             int32_t* status, cudaStream_t s) {
+  if (cap <= 0) return cudaSuccess;
+  const bool gated = u != nullptr;
+  if (I % 128 == 0)
+    return gated ? backup_grad_bn<128, true>(dY, Wd, rows_alloc, n_dev, cap, d, I, a, u, l1, o, status, s)
+                 : backup_grad_bn<128, false>(dY, Wd, rows_alloc, n_dev, cap, d, I, a, u, l1, o, status, s);
+  return gated ? backup_grad_bn<64, true>(dY, Wd, rows_alloc, n_dev, cap, d, I, a, u, l1, o, status, s)
+               : backup_grad_bn<64, false>(dY, Wd, rows_alloc, n_dev, cap, d, I, a, u, l1, o, status, s);
 }
 
 cudaError_t gemm_weight_grads(const WeightGradProblem* probs, int n_probs, int rows_alloc, const int32_t* n_dev,

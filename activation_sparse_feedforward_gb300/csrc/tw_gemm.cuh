@@ -596,7 +596,7 @@ struct EpiBackupHidden {
 // [M, end of tile) become zeros.
 template <bool GATED>
 struct EpiBackupGrad {
-  static constexpr int kStageBytes = 0;
+  static constexpr int kStageBytes = kEpiTransposeBytes;
   struct Params {
     const float* a;
     const float* u;
@@ -607,49 +607,96 @@ struct EpiBackupGrad {
   };
   const Params& p;
   int m, M, n0;
+  float* stage = nullptr;  // this warp's staging buffer
   TW_DEV EpiBackupGrad(const Params& p_, int m_, int M_, int n0_) : p(p_), m(m_), M(M_), n0(n0_) {}
+
+  // The warp's 32 rows x 32 fp32 columns of a saved matrix, read four rows per
+  // instruction (whole 128-byte row segments) and handed back one row per lane.
+  // Rows at or past `rows` read as 0.
+  TW_DEV void rows_in(const float* src, int m0, int rows, int col, float (&out)[32]) {
+    const int lane = threadIdx.x & 31, sub = lane >> 3, c4 = lane & 7;
+#pragma unroll
+    for (int r0 = 0; r0 < 32; r0 += 4) {
+      const int r = r0 + sub;
+      const float4 x = r < rows ? *reinterpret_cast<const float4*>(src + static_cast<size_t>(m0 + r) * p.ld + col + 4 * c4)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(stage + r * kEpiStageStride + 4 * c4) = x;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 x = *reinterpret_cast<const float4*>(stage + lane * kEpiStageStride + 4 * i);
+      out[4 * i] = x.x;
+      out[4 * i + 1] = x.y;
+      out[4 * i + 2] = x.z;
+      out[4 * i + 3] = x.w;
+    }
+    __syncwarp();
+  }
+  // One bf16 output block: the lane's row of 32 values (16 words) goes through the
+  // stage and leaves as four 16-byte stores per lane, eight rows per instruction.
+  // Rows at or past `rows` are not written.
+  TW_DEV void rows_out(uint16_t* dst, int m0, int rows, int col, const uint32_t (&w)[16]) {
+    const int lane = threadIdx.x & 31;
+    uint32_t* st = reinterpret_cast<uint32_t*>(stage);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      *reinterpret_cast<uint4*>(st + lane * 20 + 4 * i) = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    __syncwarp();
+    const int sub = lane >> 2, c4 = lane & 3;
+#pragma unroll
+    for (int r0 = 0; r0 < 32; r0 += 8) {
+      const int r = r0 + sub;
+      if (r < rows)
+        *reinterpret_cast<uint4*>(dst + static_cast<size_t>(m0 + r) * p.ld + col + 8 * c4) =
+            *reinterpret_cast<const uint4*>(st + r * 20 + 4 * c4);
+    }
+    __syncwarp();
+  }
+
+  // Every lane of the warp calls it (the loads and stores are warp-cooperative).
   TW_DEV void chunk(int c, const uint32_t (&dh)[32], const uint32_t (&)[32]) {
-    if (m >= p.rows_alloc) return;
-    const bool live = m < M;
-    const size_t off = static_cast<size_t>(m) * p.ld + n0 + c * 32;
+    const int lane = threadIdx.x & 31;
+    const int m0 = m - lane;                           // the warp's first row
+    const int rows_out_n = min(32, p.rows_alloc - m0);  // rows of the outputs (zeros past M)
+    if (rows_out_n <= 0) return;                       // uniform over the warp
+    const int live = max(0, min(32, M - m0));          // rows with saved a and u
+    const int col = n0 + c * 32;
+    float av[32], uv[32];
+    rows_in(p.a, m0, live, col, av);
+    if (GATED) {
+      rows_in(p.u, m0, live, col, uv);
+    } else {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float av[8], uv[8];
+      for (int i = 0; i < 32; ++i) uv[i] = 0.f;
+    }
+    // the six outputs, each a bf16 (hi, lo) half of dg, du or h, one at a time
 #pragma unroll
-      for (int i = 0; i < 8; ++i) av[i] = uv[i] = 0.f;
-      if (live) {
-        const float4* pa = reinterpret_cast<const float4*>(p.a + off) + 2 * q;
-        const float4 a0 = pa[0], a1 = pa[1];
-        av[0] = a0.x; av[1] = a0.y; av[2] = a0.z; av[3] = a0.w;
-        av[4] = a1.x; av[5] = a1.y; av[6] = a1.z; av[7] = a1.w;
-        if (GATED) {
-          const float4* pu = reinterpret_cast<const float4*>(p.u + off) + 2 * q;
-          const float4 u0 = pu[0], u1 = pu[1];
-          uv[0] = u0.x; uv[1] = u0.y; uv[2] = u0.z; uv[3] = u0.w;
-          uv[4] = u1.x; uv[5] = u1.y; uv[6] = u1.z; uv[7] = u1.w;
+    for (int o = 0; o < 6; ++o) {
+      if (!GATED && (o == 2 || o == 3)) continue;
+      uint32_t w[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float v2[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int k = 2 * i + e;
+          const float d = __uint_as_float(dh[k]);
+          const bool act = av[k] > 0.f;
+          float v;
+          if (o < 2)
+            v = act ? (GATED ? d * uv[k] : d) + p.l1 : 0.f;  // dg
+          else if (o < 4)
+            v = act ? d * av[k] : 0.f;                       // du
+          else
+            v = GATED ? av[k] * uv[k] : av[k];               // h
+          if (o & 1) v = v - bf16_lo(pack_bf16x2_rn(v, 0.f));  // the low half: v - bf16(v)
+          v2[e] = v;
         }
+        w[i] = pack_bf16x2_rn(v2[0], v2[1]);
       }
-      float dg[8], du[8], h[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float d = __uint_as_float(dh[8 * q + i]);
-        const bool act = av[i] > 0.f;
-        dg[i] = act ? (GATED ? d * uv[i] : d) + p.l1 : 0.f;
-        du[i] = act ? d * av[i] : 0.f;
-        h[i] = GATED ? av[i] * uv[i] : av[i];
-      }
-      uint4 hi, lo;
-      split8(dg, hi, lo);
-      reinterpret_cast<uint4*>(p.dG + off)[q] = hi;
-      reinterpret_cast<uint4*>(p.dG_lo + off)[q] = lo;
-      split8(h, hi, lo);
-      reinterpret_cast<uint4*>(p.H + off)[q] = hi;
-      reinterpret_cast<uint4*>(p.H_lo + off)[q] = lo;
-      if (GATED) {
-        split8(du, hi, lo);
-        reinterpret_cast<uint4*>(p.dU + off)[q] = hi;
-        reinterpret_cast<uint4*>(p.dU_lo + off)[q] = lo;
-      }
+      uint16_t* dst = o == 0 ? p.dG : o == 1 ? p.dG_lo : o == 2 ? p.dU : o == 3 ? p.dU_lo : o == 4 ? p.H : p.H_lo;
+      rows_out(dst, m0, rows_out_n, col, w);
     }
   }
   TW_DEV void finish() {}
