@@ -120,25 +120,36 @@ cudaError_t gemm_gate_relu_dense(const uint16_t* x, const uint16_t* Wg, int T, i
 }
 
 // ------------------------------------------------------------------ dense backup, forward
-cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint16_t* Wu, int rows_alloc,
-                               const int32_t* n_dev, int cap, int d, int I, uint16_t* H, uint16_t* H_lo,
-                               float* save_a, float* save_u, int32_t* status, cudaStream_t s) {
-  if (cap <= 0) return cudaSuccess;
+// 128-wide column tiles when I allows them (one round of tiles on 152 SMs at the
+// common sizes), else 64-wide; as many stages as fit about 192 KB.
+template <int BN, bool GATED>
+static cudaError_t backup_hidden_bn(const uint16_t* X, const uint16_t* Wg, const uint16_t* Wu, int rows_alloc,
+                                    const int32_t* n_dev, int cap, int d, int I, uint16_t* H, uint16_t* H_lo,
+                                    float* save_a, float* save_u, int32_t* status, cudaStream_t s) {
   GemmShape sh = shape_static(0, I, d, status);
   sh.m_dev = n_dev;
   sh.m_cap = cap;
   GemmMaps maps;
-  if (!tmap_kmajor(&maps.a[0], X, rows_alloc, d, 128) || !tmap_kmajor(&maps.b[0], Wg, I, d, 64))
+  if (!tmap_kmajor(&maps.a[0], X, rows_alloc, d, 128) || !tmap_kmajor(&maps.b[0], Wg, I, d, BN))
     return cudaErrorInvalidValue;
-  if (Wu != nullptr) {
-    if (!tmap_kmajor(&maps.b[1], Wu, I, d, 64)) return cudaErrorInvalidValue;
-    fill_unused(maps, 1, 2);
-    typename EpiBackupHidden<true>::Params ep{H, H_lo, save_a, save_u, I, rows_alloc};
-    return run_gemm<64, false, false, true, 6, EpiBackupHidden<true>>(maps, sh, ep, cap, s, "backup_hidden");
-  }
-  fill_unused(maps, 1, 1);
-  typename EpiBackupHidden<false>::Params ep{H, H_lo, save_a, nullptr, I, rows_alloc};
-  return run_gemm<64, false, false, false, 8, EpiBackupHidden<false>>(maps, sh, ep, cap, s, "backup_hidden");
+  if (GATED && !tmap_kmajor(&maps.b[1], Wu, I, d, BN)) return cudaErrorInvalidValue;
+  fill_unused(maps, 1, GATED ? 2 : 1);
+  typename EpiBackupHidden<GATED>::Params ep{H, H_lo, save_a, GATED ? save_u : nullptr, I, rows_alloc};
+  constexpr int kStageBytes = (128 + (GATED ? 2 : 1) * BN) * 64 * 2;
+  constexpr int kStages = (192 * 1024) / kStageBytes < 8 ? (192 * 1024) / kStageBytes : 8;
+  return run_gemm<BN, false, false, GATED, kStages, EpiBackupHidden<GATED>>(maps, sh, ep, cap, s, "backup_hidden");
+}
+
+cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint16_t* Wu, int rows_alloc,
+                               const int32_t* n_dev, int cap, int d, int I, uint16_t* H, uint16_t* H_lo,
+                               float* save_a, float* save_u, int32_t* status, cudaStream_t s) {
+  if (cap <= 0) return cudaSuccess;
+  const bool gated = Wu != nullptr;
+  if (I % 128 == 0)
+    return gated ? backup_hidden_bn<128, true>(X, Wg, Wu, rows_alloc, n_dev, cap, d, I, H, H_lo, save_a, save_u, status, s)
+                 : backup_hidden_bn<128, false>(X, Wg, Wu, rows_alloc, n_dev, cap, d, I, H, H_lo, save_a, save_u, status, s);
+  return gated ? backup_hidden_bn<64, true>(X, Wg, Wu, rows_alloc, n_dev, cap, d, I, H, H_lo, save_a, save_u, status, s)
+               : backup_hidden_bn<64, false>(X, Wg, Wu, rows_alloc, n_dev, cap, d, I, H, H_lo, save_a, save_u, status, s);
 }
 
 // Same product for few rows, spread over every SM: 256-wide column tiles, each tile's
@@ -165,8 +176,8 @@ cudaError_t gemm_rows_times_nmajor_splitk(const uint16_t* const* A, const uint16
 }
 
 // ------------------------------------------------------------------ dense backup, backward
-// 128-wide column tiles when I allows them (one round of tiles on 152 SMs at the
-// common sizes), else 64-wide.
+// 128-wide column tiles when I allows them, else 64-wide; as many stages as fit
+// about 192 KB.
 template <int BN, bool GATED>
 static cudaError_t backup_grad_bn(const uint16_t* dY, const uint16_t* Wd, int rows_alloc, const int32_t* n_dev,
                                   int cap, int d, int I, const float* a, const float* u, float l1,
@@ -180,7 +191,8 @@ static cudaError_t backup_grad_bn(const uint16_t* dY, const uint16_t* Wd, int ro
   fill_unused(maps, 1, 1);
   typename EpiBackupGrad<GATED>::Params ep{a,    u,  o.dG, o.dG_lo, GATED ? o.dU : nullptr, GATED ? o.dU_lo : nullptr,
                                            o.H,  o.H_lo, l1,  I,       rows_alloc};
-  constexpr int kStages = BN == 128 ? 4 : 8;
+  constexpr int kStageBytes = (128 + BN) * 64 * 2;
+  constexpr int kStages = (192 * 1024) / kStageBytes < 8 ? (192 * 1024) / kStageBytes : 8;
   return run_gemm<BN, false, false, false, kStages, EpiBackupGrad<GATED>>(maps, sh, ep, cap, s, "backup_grad");
 }
 

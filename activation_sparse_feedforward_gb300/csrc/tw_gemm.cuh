@@ -23,6 +23,8 @@
 // need them on the host.
 #pragma once
 
+#include <type_traits>
+
 #include "tw_common.cuh"
 
 namespace tw {
@@ -62,6 +64,14 @@ struct GemmMaps {
   CUtensorMap a[GEMM_MAX_SEGMENTS];
   CUtensorMap b[GEMM_MAX_SEGMENTS];
 };
+
+// An epilogue that reads global memory for its tile may define prefetch(BN); the
+// epilogue warps call it before they wait for the tile's accumulator, so the reads
+// overlap the K loop.
+template <class E, class = void>
+struct epi_prefetches : std::false_type {};
+template <class E>
+struct epi_prefetches<E, std::void_t<decltype(&E::prefetch)>> : std::true_type {};
 
 template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES>
 struct GemmTraits {
@@ -277,14 +287,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       ++local;
+      const int m = (tile / n_tiles) * GEMM_BM + row;
+      const int n0 = (tile % n_tiles) * BN;
+      Epi e(ep, m, M, n0);
+      if constexpr (epi_prefetches<Epi>::value) e.prefetch(BN);  // while the tile's K loop runs
       int ok = 0;
       if (lane == 0) ok = mbar_wait(tfull + buf, use & 1u, abort_flag, shape.status) ? 1 : 0;
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       tc_fence_after_sync();
-      const int m = (tile / n_tiles) * GEMM_BM + row;
-      const int n0 = (tile % n_tiles) * BN;
-      Epi e(ep, m, M, n0);
       if constexpr (Epi::kStageBytes > 0)
         e.stage = reinterpret_cast<float*>(tiles + STAGES * Tr::STAGE_BYTES + Tr::BAR_BYTES) + quarter * 32 * kEpiStageStride;
       const uint32_t tbase =
@@ -337,6 +348,28 @@ TW_DEV void transposed_rows(float* stage, const uint32_t (&v)[32], int m, int M,
   for (int r0 = 0; r0 < 32; r0 += 4) {
     const int r = r0 + sub;
     if (m0 + r < M) put(m0 + r, c4, *reinterpret_cast<const float4*>(stage + r * kEpiStageStride + 4 * c4));
+  }
+  __syncwarp();
+}
+
+// The bf16 counterpart for one 32-column output block: the lane's row arrives as 16
+// packed words (two columns each); the warp then writes eight rows per step, four
+// lanes x 16 bytes covering each row's 64-byte segment. Rows m0 + r with r < rows
+// are written to dst + (m0 + r) * ld. Every lane of the warp must call it.
+TW_DEV void transposed_rows_bf16(float* stage, const uint32_t (&w)[16], int m0, int rows, uint16_t* dst, int ld) {
+  const int lane = threadIdx.x & 31;
+  uint32_t* st = reinterpret_cast<uint32_t*>(stage);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    *reinterpret_cast<uint4*>(st + lane * 20 + 4 * i) = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  __syncwarp();
+  const int sub = lane >> 2, c4 = lane & 3;
+#pragma unroll
+  for (int r0 = 0; r0 < 32; r0 += 8) {
+    const int r = r0 + sub;
+    if (r < rows)
+      *reinterpret_cast<uint4*>(dst + static_cast<size_t>(m0 + r) * ld + 8 * c4) =
+          *reinterpret_cast<const uint4*>(st + r * 20 + 4 * c4);
   }
   __syncwarp();
 }
@@ -544,7 +577,7 @@ TW_DEV void split8(const float (&v)[8], uint4& hi, uint4& lo) {
 // over these rows read zeros.
 template <bool GATED>
 struct EpiBackupHidden {
-  static constexpr int kStageBytes = 0;
+  static constexpr int kStageBytes = kEpiTransposeBytes;
   struct Params {
     uint16_t* H;
     uint16_t* H_lo;
@@ -555,35 +588,53 @@ struct EpiBackupHidden {
   };
   const Params& p;
   int m, M, n0;
+  float* stage = nullptr;  // this warp's staging buffer
   TW_DEV EpiBackupHidden(const Params& p_, int m_, int M_, int n0_) : p(p_), m(m_), M(M_), n0(n0_) {}
+  // Every lane of the warp calls it (the stores are warp-cooperative).
   TW_DEV void chunk(int c, const uint32_t (&g)[32], const uint32_t (&u)[32]) {
-    if (m >= p.rows_alloc) return;
+    const int lane = threadIdx.x & 31;
+    const int m0 = m - lane;                      // the warp's first row
+    const int rows = min(32, p.rows_alloc - m0);  // rows of H / H_lo (zeros past M)
+    if (rows <= 0) return;                        // uniform over the warp
     const bool live = m < M;
-    const size_t off = static_cast<size_t>(m) * p.ld + n0 + c * 32;
+    const int col = n0 + c * 32;
+    uint32_t av[32], uv[32];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float a[8], uv[8], h[8];
+    for (int i = 0; i < 32; ++i) {
+      const float gv = __uint_as_float(g[i]);
+      av[i] = __float_as_uint((live && gv > 0.f) ? gv : 0.f);
+      uv[i] = (GATED && live) ? u[i] : 0u;
+    }
+    // h = a u (or a), then its two bf16 halves
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float gv = __uint_as_float(g[8 * q + i]);
-        a[i] = (live && gv > 0.f) ? gv : 0.f;
-        uv[i] = (GATED && live) ? __uint_as_float(u[8 * q + i]) : 0.f;
-        h[i] = GATED ? a[i] * uv[i] : a[i];
+    for (int half = 0; half < 2; ++half) {
+      uint32_t w[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float h2[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int k = 2 * i + e;
+          float h = __uint_as_float(av[k]);
+          if (GATED) h *= __uint_as_float(uv[k]);
+          if (half) h = h - bf16_lo(pack_bf16x2_rn(h, 0.f));  // the low half: h - bf16(h)
+          h2[e] = h;
+        }
+        w[i] = pack_bf16x2_rn(h2[0], h2[1]);
       }
-      uint4 hi, lo;
-      split8(h, hi, lo);
-      reinterpret_cast<uint4*>(p.H + off)[q] = hi;
-      reinterpret_cast<uint4*>(p.H_lo + off)[q] = lo;
-      if (p.save_a != nullptr && live) {
-        float4* da = reinterpret_cast<float4*>(p.save_a + off) + 2 * q;
-        da[0] = make_float4(a[0], a[1], a[2], a[3]);
-        da[1] = make_float4(a[4], a[5], a[6], a[7]);
-      }
-      if (GATED && p.save_u != nullptr && live) {
-        float4* du = reinterpret_cast<float4*>(p.save_u + off) + 2 * q;
-        du[0] = make_float4(uv[0], uv[1], uv[2], uv[3]);
-        du[1] = make_float4(uv[4], uv[5], uv[6], uv[7]);
-      }
+      transposed_rows_bf16(stage, w, m0, rows, (half ? p.H_lo : p.H) + col, p.ld);
+    }
+    if (p.save_a != nullptr) {
+      float* dst = p.save_a + col;
+      transposed_rows(stage, av, m, M, [&](int r, int c4, float4 x) {
+        reinterpret_cast<float4*>(dst + static_cast<size_t>(r) * p.ld)[c4] = x;
+      });
+    }
+    if (GATED && p.save_u != nullptr) {
+      float* dst = p.save_u + col;
+      transposed_rows(stage, uv, m, M, [&](int r, int c4, float4 x) {
+        reinterpret_cast<float4*>(dst + static_cast<size_t>(r) * p.ld)[c4] = x;
+      });
     }
   }
   TW_DEV void finish() {}
@@ -610,46 +661,39 @@ struct EpiBackupGrad {
   float* stage = nullptr;  // this warp's staging buffer
   TW_DEV EpiBackupGrad(const Params& p_, int m_, int M_, int n0_) : p(p_), m(m_), M(M_), n0(n0_) {}
 
+  // Row m's saved a and u over the tile's columns into L2 (rows with saved values).
+  TW_DEV void prefetch(int bn) const {
+    if (m >= M) return;
+    const size_t off = static_cast<size_t>(m) * p.ld + n0;
+    for (int i = 0; i < bn; i += 32) {
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p.a + off + i));
+      if (GATED) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.u + off + i));
+    }
+  }
   // The warp's 32 rows x 32 fp32 columns of a saved matrix, read four rows per
-  // instruction (whole 128-byte row segments) and handed back one row per lane.
-  // Rows at or past `rows` read as 0.
-  TW_DEV void rows_in(const float* src, int m0, int rows, int col, float (&out)[32]) {
+  // instruction (whole 128-byte row segments); rows at or past `rows` read as 0.
+  TW_DEV void load_block(const float* src, int m0, int rows, int col, float4 (&x)[8]) const {
     const int lane = threadIdx.x & 31, sub = lane >> 3, c4 = lane & 7;
 #pragma unroll
-    for (int r0 = 0; r0 < 32; r0 += 4) {
-      const int r = r0 + sub;
-      const float4 x = r < rows ? *reinterpret_cast<const float4*>(src + static_cast<size_t>(m0 + r) * p.ld + col + 4 * c4)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-      *reinterpret_cast<float4*>(stage + r * kEpiStageStride + 4 * c4) = x;
+    for (int i = 0; i < 8; ++i) {
+      const int r = 4 * i + sub;
+      x[i] = r < rows ? *reinterpret_cast<const float4*>(src + static_cast<size_t>(m0 + r) * p.ld + col + 4 * c4)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+  }
+  // ... then handed back one row per lane through the staging buffer.
+  TW_DEV void block_to_rows(const float4 (&x)[8], float (&out)[32]) {
+    const int lane = threadIdx.x & 31, sub = lane >> 3, c4 = lane & 7;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) *reinterpret_cast<float4*>(stage + (4 * i + sub) * kEpiStageStride + 4 * c4) = x[i];
     __syncwarp();
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float4 x = *reinterpret_cast<const float4*>(stage + lane * kEpiStageStride + 4 * i);
-      out[4 * i] = x.x;
-      out[4 * i + 1] = x.y;
-      out[4 * i + 2] = x.z;
-      out[4 * i + 3] = x.w;
-    }
-    __syncwarp();
-  }
-  // One bf16 output block: the lane's row of 32 values (16 words) goes through the
-  // stage and leaves as four 16-byte stores per lane, eight rows per instruction.
-  // Rows at or past `rows` are not written.
-  TW_DEV void rows_out(uint16_t* dst, int m0, int rows, int col, const uint32_t (&w)[16]) {
-    const int lane = threadIdx.x & 31;
-    uint32_t* st = reinterpret_cast<uint32_t*>(stage);
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      *reinterpret_cast<uint4*>(st + lane * 20 + 4 * i) = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-    __syncwarp();
-    const int sub = lane >> 2, c4 = lane & 3;
-#pragma unroll
-    for (int r0 = 0; r0 < 32; r0 += 8) {
-      const int r = r0 + sub;
-      if (r < rows)
-        *reinterpret_cast<uint4*>(dst + static_cast<size_t>(m0 + r) * p.ld + col + 8 * c4) =
-            *reinterpret_cast<const uint4*>(st + r * 20 + 4 * c4);
+      const float4 v = *reinterpret_cast<const float4*>(stage + lane * kEpiStageStride + 4 * i);
+      out[4 * i] = v.x;
+      out[4 * i + 1] = v.y;
+      out[4 * i + 2] = v.z;
+      out[4 * i + 3] = v.w;
     }
     __syncwarp();
   }
@@ -663,12 +707,17 @@ struct EpiBackupGrad {
     const int live = max(0, min(32, M - m0));          // rows with saved a and u
     const int col = n0 + c * 32;
     float av[32], uv[32];
-    rows_in(p.a, m0, live, col, av);
-    if (GATED) {
-      rows_in(p.u, m0, live, col, uv);
-    } else {
+    {
+      float4 xa[8], xu[8];  // both blocks' loads in flight together
+      load_block(p.a, m0, live, col, xa);
+      if (GATED) load_block(p.u, m0, live, col, xu);
+      block_to_rows(xa, av);
+      if (GATED) {
+        block_to_rows(xu, uv);
+      } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) uv[i] = 0.f;
+        for (int i = 0; i < 32; ++i) uv[i] = 0.f;
+      }
     }
     // the six outputs, each a bf16 (hi, lo) half of dg, du or h, one at a time
 #pragma unroll
@@ -696,7 +745,7 @@ struct EpiBackupGrad {
         w[i] = pack_bf16x2_rn(v2[0], v2[1]);
       }
       uint16_t* dst = o == 0 ? p.dG : o == 1 ? p.dG_lo : o == 2 ? p.dU : o == 3 ? p.dU_lo : o == 4 ? p.H : p.H_lo;
-      rows_out(dst, m0, rows_out_n, col, w);
+      transposed_rows_bf16(stage, w, m0, rows_out_n, dst + col, p.ld);
     }
   }
   TW_DEV void finish() {}
