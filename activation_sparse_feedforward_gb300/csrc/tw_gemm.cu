@@ -51,11 +51,11 @@ static bool tmap_mnmajor(CUtensorMap* m, const uint16_t* p, int K, int cols) {
 
 // max_rows bounds the rows of D (the grid has at most one CTA per tile); a device-
 // chosen split (sh.ksplit < 0) gets one CTA per SM.
-template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES, class Epi>
+template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES, class Epi, int NA = 1>
 static cudaError_t run_gemm(const GemmMaps& maps, const GemmShape& sh, const typename Epi::Params& ep, int max_rows,
                             cudaStream_t s, const char* label) {
-  using Tr = GemmTraits<BN, A_MN, B_MN, DUAL, STAGES>;
-  auto kern = gemm_tc_kernel<BN, A_MN, B_MN, DUAL, STAGES, Epi>;
+  using Tr = GemmTraits<BN, A_MN, B_MN, DUAL, STAGES, NA>;
+  auto kern = gemm_tc_kernel<BN, A_MN, B_MN, DUAL, STAGES, Epi, NA>;
   constexpr int smem = Tr::SMEM_BYTES + Epi::kStageBytes;
   static_assert(smem <= 232448, "GEMM shared memory above the 227 KiB opt-in limit");
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -153,7 +153,8 @@ cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint
 }
 
 // Same product for few rows, spread over every SM: 256-wide column tiles, each tile's
-// K loop (all segments) cut into slices whose partial sums are added into the fp32
+// K loop (all segments; a pair of segments over the same B is one K step) cut into
+// slices whose partial sums are added into the fp32
 // accumulator acc [cap, N] (zeroed beforehand, by the row gather); launch_scatter_rows_bf16
 // then writes the bf16 rows out.
 cudaError_t gemm_rows_times_nmajor_splitk(const uint16_t* const* A, const uint16_t* const* B, int segments,
@@ -172,6 +173,11 @@ cudaError_t gemm_rows_times_nmajor_splitk(const uint16_t* const* A, const uint16
       return cudaErrorInvalidValue;
   fill_unused(maps, segments, segments);
   EpiRedF32::Params ep{acc, N};
+  // segments that come in pairs over one B (the hi / lo halves of a split operand)
+  // load that B tile once for both
+  bool paired = segments % 2 == 0;
+  for (int i = 0; paired && i < segments; i += 2) paired = B[i] == B[i + 1];
+  if (paired) return run_gemm<256, false, true, false, 3, EpiRedF32, 2>(maps, sh, ep, cap, s, "backup_rows_gemm");
   return run_gemm<256, false, true, false, 4, EpiRedF32>(maps, sh, ep, cap, s, "backup_rows_gemm");
 }
 

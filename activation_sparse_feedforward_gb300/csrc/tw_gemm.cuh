@@ -73,12 +73,15 @@ struct epi_prefetches : std::false_type {};
 template <class E>
 struct epi_prefetches<E, std::void_t<decltype(&E::prefetch)>> : std::true_type {};
 
-template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES>
+// NA = 2 pairs the segments: segments 2i and 2i + 1 share one B operand (b[2i]), so
+// a stage holds both A tiles and one B tile, and both products go into the same
+// accumulator (the hi / lo halves of a split fp32 operand against one weight).
+template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES, int NA = 1>
 struct GemmTraits {
   static constexpr int NB = DUAL ? 2 : 1;
   static constexpr int A_BYTES = GEMM_BM * GEMM_BK * 2;
   static constexpr int B_BYTES = BN * GEMM_BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + NB * B_BYTES;
+  static constexpr int STAGE_BYTES = NA * A_BYTES + NB * B_BYTES;
   static constexpr int ACC_COLS = BN * NB;
   static constexpr int TMEM_COLS = 2 * ACC_COLS;
   static constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, BN, A_MN, B_MN);
@@ -88,13 +91,14 @@ struct GemmTraits {
   static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of two");
   static_assert((2 * STAGES + 4) * 8 + 8 <= BAR_BYTES, "barrier area");
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+  static_assert(NA == 1 || (NA == 2 && !DUAL), "paired A segments take one B operand");
 };
 
-template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES, class Epi>
+template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES, class Epi, int NA = 1>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ GemmMaps maps, const GemmShape shape,
                    const __grid_constant__ typename Epi::Params ep) {
-  using Tr = GemmTraits<BN, A_MN, B_MN, DUAL, STAGES>;
+  using Tr = GemmTraits<BN, A_MN, B_MN, DUAL, STAGES, NA>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
   uint8_t* tiles = smem_raw + pad;
@@ -146,7 +150,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const int problems = max(1, shape.problems);
   const int num_tiles = (K > 0) ? problems * m_tiles * n_tiles : 0;
   const int kb_per_seg = (K + GEMM_BK - 1) / GEMM_BK;
-  const int kb_total = kb_per_seg * shape.segments;
+  const int kb_total = kb_per_seg * (shape.segments / NA);  // one K step covers NA segments
   // work unit = (output tile, slice of its K loop); empty slices are skipped by
   // every role alike
   const int ksplit = shape.ksplit >= 0 ? max(1, shape.ksplit)
@@ -176,17 +180,22 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             break;
           }
           uint8_t* sA = tiles + stage * Tr::STAGE_BYTES;
-          uint8_t* sB = sA + Tr::A_BYTES;
-          const int seg = kb / kb_per_seg;
-          const int k0 = (kb - seg * kb_per_seg) * GEMM_BK;
-          const CUtensorMap* ta = &maps.a[prob * shape.segments + seg];
+          uint8_t* sB = sA + NA * Tr::A_BYTES;
+          const int grp = kb / kb_per_seg;
+          const int seg = grp * NA;
+          const int k0 = (kb - grp * kb_per_seg) * GEMM_BK;
           const CUtensorMap* tb = &maps.b[prob * shape.segments + seg];
           mbar_arrive_expect_tx(full + stage, Tr::STAGE_BYTES);
-          if (!A_MN) {
-            tma_load_2d(sA, ta, full + stage, k0, m0);
-          } else {
-            tma_load_2d(sA, ta, full + stage, m0, k0);
-            tma_load_2d(sA + 8192, ta, full + stage, m0 + 64, k0);
+#pragma unroll
+          for (int na = 0; na < NA; ++na) {
+            const CUtensorMap* ta = &maps.a[prob * shape.segments + seg + na];
+            uint8_t* dA = sA + na * Tr::A_BYTES;
+            if (!A_MN) {
+              tma_load_2d(dA, ta, full + stage, k0, m0);
+            } else {
+              tma_load_2d(dA, ta, full + stage, m0, k0);
+              tma_load_2d(dA + 8192, ta, full + stage, m0 + 64, k0);
+            }
           }
 #pragma unroll
           for (int nb = 0; nb < Tr::NB; ++nb) {
@@ -243,18 +252,22 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
           tc_fence_after_sync();
           const uint32_t a_base = smem_addr(tiles + stage * Tr::STAGE_BYTES);
-          const uint32_t b_base = a_base + Tr::A_BYTES;
+          const uint32_t b_base = a_base + NA * Tr::A_BYTES;
 #pragma unroll
           for (int k16 = 0; k16 < GEMM_BK / 16; ++k16) {
-            const uint64_t ad = A_MN ? smem_desc_sw128(a_base + k16 * 2048, 8192, 1024)
-                                     : smem_desc_sw128(a_base + k16 * 32, 16, 1024);
-            const uint32_t acc = (kb > kb_lo || k16 > 0) ? 1u : 0u;
 #pragma unroll
-            for (int nb = 0; nb < Tr::NB; ++nb) {
-              const uint32_t bb = b_base + nb * Tr::B_BYTES;
-              const uint64_t bd = B_MN ? smem_desc_sw128(bb + k16 * 2048, 8192, 1024)
-                                       : smem_desc_sw128(bb + k16 * 32, 16, 1024);
-              tc_mma_bf16(d0 + nb * BN, ad, bd, Tr::IDESC, acc);
+            for (int na = 0; na < NA; ++na) {
+              const uint32_t ab = a_base + na * Tr::A_BYTES;
+              const uint64_t ad = A_MN ? smem_desc_sw128(ab + k16 * 2048, 8192, 1024)
+                                       : smem_desc_sw128(ab + k16 * 32, 16, 1024);
+              const uint32_t acc = (kb > kb_lo || k16 > 0 || na > 0) ? 1u : 0u;
+#pragma unroll
+              for (int nb = 0; nb < Tr::NB; ++nb) {
+                const uint32_t bb = b_base + nb * Tr::B_BYTES;
+                const uint64_t bd = B_MN ? smem_desc_sw128(bb + k16 * 2048, 8192, 1024)
+                                         : smem_desc_sw128(bb + k16 * 32, 16, 1024);
+                tc_mma_bf16(d0 + nb * BN, ad, bd, Tr::IDESC, acc);
+              }
             }
           }
           issued_any = true;
