@@ -237,8 +237,9 @@ cudaError_t gemm_weight_grads(const WeightGradProblem* probs, int n_probs, int r
   ep.ldd = d;
   // each problem takes whole 128-row tiles; rows I .. of its last tile are skipped
   ep.rows_per_problem = (I + GEMM_BM - 1) / GEMM_BM * GEMM_BM;
-  return run_gemm<256, true, true, false, 4, EpiStoreF32Grouped>(maps, sh, ep, ep.rows_per_problem * n_probs, s,
-                                                                  "backup_weight_grad");
+  // the hi and lo segments share Q: one Q tile a K step for both
+  return run_gemm<256, true, true, false, 3, EpiStoreF32Grouped, 2>(maps, sh, ep, ep.rows_per_problem * n_probs, s,
+                                                                     "backup_weight_grad");
 }
 
 // ------------------------------------------------------------------ layout test GEMM
