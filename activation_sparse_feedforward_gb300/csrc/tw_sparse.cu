@@ -85,32 +85,67 @@ int grid_for(long items, int per_block, int blocks_per_sm) {
 }  // namespace
 
 // ====================================================================== transposed Hybrid
-// Exclusive scan of the per-neuron counts (one CTA, each thread a run of consecutive
-// neurons): col_ptr[0..I], col_cur = col_ptr.
+// Exclusive scan of the per-neuron counts: col_ptr[0..I], col_cur = col_ptr. One CTA
+// walks the counts in chunks of 16 x blockDim neurons; each thread takes 16
+// consecutive counts (four 16-byte loads, issued together, when I is a multiple of
+// 4), so a chunk costs one round trip to memory instead of one per count.
 __global__ void __launch_bounds__(1024) csc_scan_kernel(const int32_t* __restrict__ col_cnt, int I,
                                                         int32_t* __restrict__ col_ptr, int32_t* __restrict__ col_cur) {
   pdl_enter();
   __shared__ int warp_tot[32];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int per = (I + blockDim.x - 1) / blockDim.x;
-  const int lo = min(I, tid * per), hi = min(I, lo + per);
-  int sum = 0;
-  for (int j = lo; j < hi; ++j) sum += col_cnt[j];
-  const int incl = warp_inclusive_scan(sum);
-  if (lane == 31) warp_tot[wid] = incl;
-  __syncthreads();
-  if (wid == 0) {
-    const int v = lane < (blockDim.x >> 5) ? warp_tot[lane] : 0;
-    warp_tot[lane] = warp_inclusive_scan(v);
+  const bool vec = I % 4 == 0;
+  int carry = 0;
+  for (int base = 0; base < I; base += 16 * blockDim.x) {
+    const int j0 = base + 16 * tid;
+    int v[16];
+    if (vec && j0 + 16 <= I) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int4 c = reinterpret_cast<const int4*>(col_cnt + j0)[q];
+        v[4 * q] = c.x;
+        v[4 * q + 1] = c.y;
+        v[4 * q + 2] = c.z;
+        v[4 * q + 3] = c.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = j0 + i < I ? col_cnt[j0 + i] : 0;
+    }
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sum += v[i];
+    const int incl = warp_inclusive_scan(sum);
+    if (lane == 31) warp_tot[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+      const int w = lane < (blockDim.x >> 5) ? warp_tot[lane] : 0;
+      warp_tot[lane] = warp_inclusive_scan(w);
+    }
+    __syncthreads();
+    int run = carry + (wid ? warp_tot[wid - 1] : 0) + incl - sum;
+    carry += warp_tot[(blockDim.x >> 5) - 1];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int e = run;
+      run += v[i];
+      v[i] = e;
+    }
+    if (vec && j0 + 16 <= I) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int4 e = make_int4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        reinterpret_cast<int4*>(col_ptr + j0)[q] = e;
+        reinterpret_cast<int4*>(col_cur + j0)[q] = e;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (j0 + i < I) col_ptr[j0 + i] = col_cur[j0 + i] = v[i];
+    }
+    __syncthreads();  // warp_tot is rewritten by the next chunk
   }
-  __syncthreads();
-  int run = (wid ? warp_tot[wid - 1] : 0) + incl - sum;
-  for (int j = lo; j < hi; ++j) {
-    col_ptr[j] = run;
-    col_cur[j] = run;
-    run += col_cnt[j];
-  }
-  if (tid == blockDim.x - 1) col_ptr[I] = warp_tot[(blockDim.x >> 5) - 1];
+  if (tid == 0) col_ptr[I] = carry;
 }
 
 // Scatters every ELL entry into its column of the transposed Hybrid as one
