@@ -147,8 +147,6 @@ HybFwdWs carve_hybrid_fwd(Carve& c, int T, int d, int I, int W, int C, int backu
 }
 
 struct HybBwdWs {
-  float* dg;
-  float* du;
   int32_t* col_cnt;
   int32_t* col_ptr;
   int32_t* col_cur;
@@ -164,8 +162,6 @@ HybBwdWs carve_hybrid_bwd(Carve& c, int T, int d, int I, int R, int backup_cap) 
   const int ra = round_up(backup_cap, 128);
   const size_t rI = static_cast<size_t>(ra) * I;
   HybBwdWs w{};
-  w.dg = c.take<float>(TR);
-  w.du = c.take<float>(TR);
   w.col_cnt = c.take<int32_t>(static_cast<size_t>(I) + 1);
   w.col_ptr = c.take<int32_t>(static_cast<size_t>(I) + 1);
   w.col_cur = c.take<int32_t>(static_cast<size_t>(I));
@@ -448,7 +444,7 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
   a.T = T; a.d = d; a.I = I; a.R = R; a.l1 = l1;
   a.ell_nnz = saved->ell_nnz; a.backup_slot = saved->backup_slot;
   a.ell_idx = saved->ell_idx; a.ell_a = saved->ell_a; a.ell_u = saved->ell_u;
-  a.dg = w.dg; a.du = w.du; a.dx = dx;
+  a.dx = dx;
   a.col_cnt = w.col_cnt; a.col_ptr = w.col_ptr; a.col_cur = w.col_cur; a.csc = w.csc;
   a.dWg = dWg; a.dWu = dWu; a.dWd = dWd;
   a.sched = w.sched;

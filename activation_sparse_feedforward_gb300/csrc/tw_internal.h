@@ -114,8 +114,6 @@ struct SparseBwdArgs {
   const uint16_t* ell_idx;
   const uint16_t* ell_a;
   const uint16_t* ell_u;
-  float* dg;        // [T, R] per-entry dg (workspace)
-  float* du;        // [T, R] per-entry du (workspace, gated)
   uint16_t* dx;
   // transposed Hybrid (workspace)
   int32_t* col_cnt;   // [I + 1]
@@ -128,18 +126,21 @@ struct SparseBwdArgs {
   const int32_t* dW_base_rows;
   // scheduling counters (as SparseFwdArgs::sched): the token pass's at sched[0], the
   // weight pass's kSchedCounters at sched_w = sched + kSchedStride, each
-  // kSchedStride ints apart; the kSchedWords ints are zeroed together with col_cnt
+  // kSchedStride ints apart, and the count pass's ticket at sched + kSchedTicket;
+  // the kSchedWords ints are zeroed together with col_cnt
   int32_t* sched;
   int32_t* sched_w;
 };
 constexpr int kSchedCounters = 8;
 constexpr int kSchedStride = 32;  // ints: one 128-byte line per counter
-constexpr int kSchedWords = (1 + kSchedCounters) * kSchedStride;
-// Token side of the ELL backward (tw_token.cu): dh, dg and du per entry, column
-// counts of the transposed Hybrid (col_cnt must be zero), dx.
+constexpr int kSchedTicket = (1 + kSchedCounters) * kSchedStride;
+constexpr int kSchedWords = (2 + kSchedCounters) * kSchedStride;
+// Token side of the ELL backward (tw_token.cu): dh, dg and du per entry, each
+// entry's record of the transposed Hybrid written at a slot claimed from col_cur
+// (set by the count pass), dx.
 cudaError_t launch_token_bwd(const SparseBwdArgs& a, cudaStream_t s);
-// ELL backward (tw_sparse.cu), token side: zeroes col_cnt, launch_token_bwd,
-// transposed Hybrid (column pointers and records).
+// ELL backward (tw_sparse.cu), token side: zeroes the counters, counts and scans the
+// columns of the transposed Hybrid, then launch_token_bwd fills in its records.
 cudaError_t launch_sparse_bwd_tokens(const SparseBwdArgs& a, cudaStream_t s);
 // ELL backward, column side: weight gradients over the transposed Hybrid (see
 // SparseBwdArgs::dW_base_rows for overwrite / accumulate).

@@ -75,6 +75,11 @@ TW_DEV void out_f32x8(float* p, const F8& y, bool add) {
     stcs_f32x8(p, y);
 }
 TW_DEV uint4 ldg16(const uint4* p) { return __ldg(p); }
+constexpr int kCountHistMaxBins = 48 * 1024;  // 192 KB of shared memory
+template <class K>
+cudaError_t set_smem_bytes(K kern, size_t bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+}
 int grid_for(long items, int per_block, int blocks_per_sm) {
   const long blocks = (items + per_block - 1) / per_block;
   return static_cast<int>(
@@ -85,13 +90,12 @@ int grid_for(long items, int per_block, int blocks_per_sm) {
 }  // namespace
 
 // ====================================================================== transposed Hybrid
-// Exclusive scan of the per-neuron counts: col_ptr[0..I], col_cur = col_ptr. One CTA
+// Exclusive scan of the per-neuron counts: col_ptr[0..I], col_cur = col_ptr. The CTA
 // walks the counts in chunks of 16 x blockDim neurons; each thread takes 16
 // consecutive counts (four 16-byte loads, issued together, when I is a multiple of
 // 4), so a chunk costs one round trip to memory instead of one per count.
-__global__ void __launch_bounds__(1024) csc_scan_kernel(const int32_t* __restrict__ col_cnt, int I,
-                                                        int32_t* __restrict__ col_ptr, int32_t* __restrict__ col_cur) {
-  pdl_enter();
+TW_DEV void scan_counts(const int32_t* __restrict__ col_cnt, int I, int32_t* __restrict__ col_ptr,
+                        int32_t* __restrict__ col_cur) {
   __shared__ int warp_tot[32];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const bool vec = I % 4 == 0;
@@ -102,7 +106,7 @@ __global__ void __launch_bounds__(1024) csc_scan_kernel(const int32_t* __restric
     if (vec && j0 + 16 <= I) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const int4 c = reinterpret_cast<const int4*>(col_cnt + j0)[q];
+        const int4 c = __ldcg(reinterpret_cast<const int4*>(col_cnt + j0) + q);
         v[4 * q] = c.x;
         v[4 * q + 1] = c.y;
         v[4 * q + 2] = c.z;
@@ -110,7 +114,7 @@ __global__ void __launch_bounds__(1024) csc_scan_kernel(const int32_t* __restric
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = j0 + i < I ? col_cnt[j0 + i] : 0;
+      for (int i = 0; i < 16; ++i) v[i] = j0 + i < I ? __ldcg(col_cnt + j0 + i) : 0;
     }
     int sum = 0;
 #pragma unroll
@@ -148,27 +152,61 @@ __global__ void __launch_bounds__(1024) csc_scan_kernel(const int32_t* __restric
   if (tid == 0) col_ptr[I] = carry;
 }
 
-// Scatters every ELL entry into its column of the transposed Hybrid as one
-// 16-byte record {token row offset in 16-byte units, dg, du, h = a u (non-gated: a)},
-// so the weight-gradient pass reads one coalesced record per entry and nothing else
-// but the gathered rows.
-template <bool GATED>
-__global__ void __launch_bounds__(256) csc_fill_kernel(const SparseBwdArgs a) {
+// Column counts of the transposed Hybrid, then their scan. Every CTA counts the
+// entries of its tokens (four tokens a warp) into a shared-memory histogram of the I
+// columns, then adds its nonzero bins to col_cnt (zero at launch): a neuron that is
+// active in many tokens then takes one global atomic per CTA, not one per entry.
+// With hist_bins == 0 (I too large for shared memory) entries go to col_cnt
+// directly. The CTA that finishes last, as told by a ticket counter (zero at
+// launch), scans the counts. The token pass then claims each entry's slot from
+// col_cur and writes its record there.
+__global__ void __launch_bounds__(1024) csc_count_scan_kernel(const SparseBwdArgs a, int32_t* ticket, int hist_bins) {
   pdl_enter();
+  extern __shared__ int hist[];
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
-  const uint32_t row16 = static_cast<uint32_t>(a.d / 8);
-  for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < a.T; t += gridDim.x * wpb) {
-    const int n = a.ell_nnz[t];
-    for (int s = lane; s < n; s += 32) {
-      const size_t e = static_cast<size_t>(t) * a.R + s;
-      const float av = bf16_to_f32(a.ell_a[e]);
-      const float h = GATED ? av * bf16_to_f32(a.ell_u[e]) : av;
-      const uint4 rec = make_uint4(static_cast<uint32_t>(t) * row16, __float_as_uint(a.dg[e]),
-                                   GATED ? __float_as_uint(a.du[e]) : 0u, __float_as_uint(h));
-      a.csc[atomicAdd(a.col_cur + a.ell_idx[e], 1)] = rec;
+  for (int j = threadIdx.x; j < hist_bins; j += blockDim.x) hist[j] = 0;
+  __syncthreads();
+  int* cnt = hist_bins > 0 ? hist : a.col_cnt;
+  // a warp takes four tokens at a time: their lengths in one round trip, then their
+  // neuron indices in another
+  const int gwarp = blockIdx.x * wpb + (threadIdx.x >> 5), nwarps = gridDim.x * wpb;
+  for (int t0 = 4 * gwarp; t0 < a.T; t0 += 4 * nwarps) {
+    int len = 0;
+    if (lane < 4 && t0 + lane < a.T) {
+      const int t = t0 + lane;
+      const int slot = a.backup_slot != nullptr ? a.backup_slot[t] : -1;
+      const int n = a.ell_nnz[t];
+      len = slot >= 0 ? 0 : n;  // exactly the entries the token pass writes: none of a backup row's
+    }
+    int n[4], nmax = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      n[q] = __shfl_sync(0xFFFFFFFFu, len, q);
+      nmax = max(nmax, n[q]);
+    }
+    for (int k = lane; k < nmax; k += 32) {
+      int j[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) j[q] = k < n[q] ? a.ell_idx[static_cast<size_t>(t0 + q) * a.R + k] : -1;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (j[q] >= 0) atomicAdd(cnt + j[q], 1);
     }
   }
+  __syncthreads();
+  for (int j = threadIdx.x; j < hist_bins; j += blockDim.x) {
+    const int c = hist[j];
+    if (c != 0) atomicAdd(a.col_cnt + j, c);
+  }
+  __threadfence();  // this thread's counts are visible before the CTA takes its ticket
+  __syncthreads();
+  __shared__ int last;
+  if (threadIdx.x == 0) last = atomicAdd(ticket, 1) == static_cast<int>(gridDim.x) - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  scan_counts(a.col_cnt, a.I, a.col_ptr, a.col_cur);
 }
 
 // ====================================================================== backward: dW
@@ -287,25 +325,26 @@ __global__ void __launch_bounds__(256, 4) ell_weight_grad_kernel(const SparseBwd
 }
 
 // ====================================================================== launchers
-template <bool GATED>
 static cudaError_t token_side(const SparseBwdArgs& a, cudaStream_t s) {
-  // the token pass's and the weight pass's scheduling counters (kSchedWords ints)
+  // column counts, the scheduling counters of both passes and the count pass's ticket
   cudaError_t e =
       launch_zero(a.col_cnt, sizeof(int32_t) * (a.I + 1), a.sched, a.sched ? sizeof(int32_t) * kSchedWords : 0, s);
   if (e != cudaSuccess) return e;
-  e = launch_token_bwd(a, s);  // dh, dg, du, column counts, dx
+  int32_t* ticket = a.sched + kSchedTicket;
+  // one CTA per SM; a shared-memory histogram of the columns when it fits
+  const int bins = a.I <= kCountHistMaxBins ? a.I : 0;
+  const size_t smem = sizeof(int) * static_cast<size_t>(bins);
+  e = set_smem_bytes(csc_count_scan_kernel, smem);
   if (e != cudaSuccess) return e;
-  e = launch(csc_scan_kernel, dim3(1), dim3(1024), 0, s, static_cast<const int32_t*>(a.col_cnt), a.I, a.col_ptr,
-             a.col_cur);
-  trace_mark(s, "csc_scan");
-  if (e != cudaSuccess || a.T == 0) return e;
-  e = launch(csc_fill_kernel<GATED>, dim3(grid_for(a.T, 8, 8)), dim3(256), 0, s, a);
-  trace_mark(s, "csc_fill");
-  return e;
+  e = launch(csc_count_scan_kernel, dim3(grid_for(a.T, 32, 1)), dim3(1024), smem, s, a, ticket, bins);
+  trace_mark(s, "csc_count_scan");
+  if (e != cudaSuccess) return e;
+  return launch_token_bwd(a, s);  // dh, dg, du, the records of the transposed Hybrid, dx
 }
 
 cudaError_t launch_sparse_bwd_tokens(const SparseBwdArgs& a, cudaStream_t s) {
-  return a.Wu != nullptr ? token_side<true>(a, s) : token_side<false>(a, s);
+  if (a.sched == nullptr) return cudaErrorInvalidValue;  // holds the count pass's ticket
+  return token_side(a, s);
 }
 
 cudaError_t launch_sparse_bwd_weights(const SparseBwdArgs& a, cudaStream_t s) {

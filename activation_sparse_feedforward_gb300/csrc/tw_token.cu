@@ -20,8 +20,9 @@
 //            ELL row (idx, a, u).
 //  backward  list = the token's ELL row (j, a, u),
 //            pass A: dh = dy_t . Wd[j]; dg = dh u + l1 (non-gated: dh + l1), du = dh a,
-//            pass B: dx_t = sum dg Wg[j] + du Wu[j]; also counts every neuron
-//            column for the transposed Hybrid.
+//            pass B: dx_t = sum dg Wg[j] + du Wu[j]; between the passes every entry's
+//            record {token row, dg, du, h} goes to its neuron column of the
+//            transposed Hybrid, at a slot claimed from that column's cursor.
 #include <algorithm>
 
 #include "tw_common.cuh"
@@ -518,6 +519,8 @@ template <int NCH, bool GATED>
 __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_bwd_kernel(const SparseBwdArgs a) {
   pdl_enter();
   constexpr uint32_t row16 = NCH * 32;
+  constexpr int kPerThread = (kWin + NCH * 32 - 1) / (NCH * 32);  // window entries per thread, at most
+  static_assert(rup(kWin, kGroup) == kWin, "a window is whole groups");
   constexpr uint32_t lp = rup(kWin + kGroup, kGroup);
   constexpr uint32_t list_bytes = rup(2u * lp, 16u) + 2u * 8u * lp;
   extern __shared__ __align__(16) uint8_t tsm[];
@@ -549,12 +552,20 @@ __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_bwd_kernel(c
       f32x2* lg = reinterpret_cast<f32x2*>(tsm + buf * list_bytes + rup(2u * lp, 16u));  // a, then dg
       f32x2* lu = lg + lp;                                                                // u, then du
       buf ^= 1;
-      for (int k = threadIdx.x; k < rup(m, kGroup); k += blockDim.x) {
+      // each thread takes entries threadIdx.x + i * blockDim.x. It claims the slot of
+      // its first one in the transposed Hybrid here and fills it after pass A, which
+      // hides the claim's round trip (further entries, when a window has more than
+      // blockDim of them, claim theirs when they are filled)
+      int slot0 = 0;
+#pragma unroll
+      for (int i = 0; i < kPerThread; ++i) {
+        const int k = threadIdx.x + i * static_cast<int>(blockDim.x);
+        if (k >= rup(m, kGroup)) break;
         const int e = min(k, m - 1);
         const int j = a.ell_idx[rb + w0 + e];
         lj[k] = static_cast<uint16_t>(j);
         if (k < m) {
-          atomicAdd(a.col_cnt + j, 1);
+          if (i == 0) slot0 = atomicAdd(a.col_cur + j, 1);
           lg[k] = pair(bf16_to_f32(a.ell_a[rb + w0 + k]), 0.f);
           lu[k] = pair(GATED ? bf16_to_f32(a.ell_u[rb + w0 + k]) : 1.f, 0.f);
         } else {
@@ -566,15 +577,20 @@ __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_bwd_kernel(c
       // ---------------------------------------------------------- dh = dy_t . Wd[j]
       pass_dot<false>(Wd4, row16, lj, 0, m, dys, part + c * kWin, lane);
       __syncthreads();
-      for (int k = threadIdx.x; k < m; k += blockDim.x) {
+#pragma unroll
+      for (int i = 0; i < kPerThread; ++i) {
+        const int k = threadIdx.x + i * static_cast<int>(blockDim.x);
+        if (k >= m) break;
         float dh = 0.f;
 #pragma unroll
         for (int w = 0; w < NCH; ++w) dh += part[w * kWin + k];
         const float av = unpair(lg[k]).x, uv = unpair(lu[k]).x;
         const float dg = (GATED ? dh * uv : dh) + a.l1;
         const float du = dh * av;
-        a.dg[rb + w0 + k] = dg;
-        if (GATED) a.du[rb + w0 + k] = du;
+        // the entry's record {token row offset in 16-byte units, dg, du, h = a u (or a)}
+        const int sl = i == 0 ? slot0 : atomicAdd(a.col_cur + lj[k], 1);
+        a.csc[sl] = make_uint4(static_cast<uint32_t>(t) * row16, __float_as_uint(dg),
+                                    GATED ? __float_as_uint(du) : 0u, __float_as_uint(GATED ? av * uv : av));
         lg[k] = pair(dg, dg);
         lu[k] = pair(du, du);
       }
