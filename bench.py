@@ -167,11 +167,13 @@ def kernel_work(label: str, spec, stats: dict) -> tuple[str, float] | None:
         b = (T * d * 2 if spec.gated else 0) + T * d * 2 + T * nT * 2 + nnz_ell * 3 + nnz_ell * 6 + g * I * d * 2
         return "hbm", float(b)
     if label == "sparse_bwd_token":
-        # dy + dx + ELL read (idx, a, u) + dg/du written + three weight matrices
-        return "hbm", float(2 * T * d * 2 + nnz_ell * 6 + nnz_ell * 8 + 3 * I * d * 2)
+        # dy + dx + ELL read (idx, a, u) + one 16-byte column record written per
+        # entry + three weight matrices
+        return "hbm", float(2 * T * d * 2 + nnz_ell * 6 + nnz_ell * 16 + 3 * I * d * 2)
     if label == "ell_weight_grad":
-        # x and dy read + dW written (fp32, 3 matrices) + csc, dg/du, a/u per entry
-        return "hbm", float(2 * T * d * 2 + 3 * I * d * 4 + nnz_ell * (4 + 8 + 4))
+        # x and dy read + dW written (fp32, 3 matrices) + one 16-byte column record
+        # read per entry
+        return "hbm", float(2 * T * d * 2 + 3 * I * d * 4 + nnz_ell * 16)
     if label == "backup_hidden":
         return "tensor", 2.0 * 2 * nb * d * I
     if label == "backup_grad":
