@@ -72,6 +72,13 @@ template <class E, class = void>
 struct epi_prefetches : std::false_type {};
 template <class E>
 struct epi_prefetches<E, std::void_t<decltype(&E::prefetch)>> : std::true_type {};
+// An epilogue with kOverlapLoads = true (single accumulator only) has each chunk's
+// TMEM load issued before the previous chunk is written out, at the cost of a
+// second 32-register buffer.
+template <class E, class = void>
+struct epi_overlaps_loads : std::false_type {};
+template <class E>
+struct epi_overlaps_loads<E, std::void_t<decltype(E::kOverlapLoads)>> : std::bool_constant<E::kOverlapLoads> {};
 
 // NA = 2 pairs the segments: segments 2i and 2i + 1 share one B operand (b[2i]), so
 // a stage holds both A tiles and one B tile, and both products go into the same
@@ -313,14 +320,32 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         e.stage = reinterpret_cast<float*>(tiles + STAGES * Tr::STAGE_BYTES + Tr::BAR_BYTES) + quarter * 32 * kEpiStageStride;
       const uint32_t tbase =
           tmem_base + static_cast<uint32_t>(buf * Tr::ACC_COLS) + (static_cast<uint32_t>(quarter * 32) << 16);
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t v0[32];
-        uint32_t v1[32];
-        tmem_ld32(tbase + c * 32, v0);
-        if (DUAL) tmem_ld32(tbase + BN + c * 32, v1);
+      if constexpr (!DUAL && epi_overlaps_loads<Epi>::value) {
+        // the next chunk's TMEM load is in flight while this chunk is written out
+        uint32_t va[32], vb[32];
+        tmem_ld32(tbase, va);
         tmem_wait_ld();
-        e.chunk(c, v0, v1);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; c += 2) {
+          if (c + 1 < BN / 32) tmem_ld32(tbase + (c + 1) * 32, vb);
+          e.chunk(c, va, va);
+          tmem_wait_ld();
+          if (c + 1 < BN / 32) {
+            if (c + 2 < BN / 32) tmem_ld32(tbase + (c + 2) * 32, va);
+            e.chunk(c + 1, vb, vb);
+            tmem_wait_ld();
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v0[32];
+          uint32_t v1[32];
+          tmem_ld32(tbase + c * 32, v0);
+          if (DUAL) tmem_ld32(tbase + BN + c * 32, v1);
+          tmem_wait_ld();
+          e.chunk(c, v0, v1);
+        }
       }
       tc_fence_before_sync();
       __syncwarp();
@@ -393,6 +418,7 @@ TW_DEV void transposed_rows_bf16(float* stage, const uint32_t (&w)[16], int m0, 
 // D[m][n] = acc (fp32), row stride ldd.
 struct EpiStoreF32 {
   static constexpr int kStageBytes = kEpiTransposeBytes;
+  static constexpr bool kOverlapLoads = true;
   struct Params {
     float* D;
     int ldd;
@@ -414,6 +440,7 @@ struct EpiStoreF32 {
 // m / rows_per_problem and is row m % rows_per_problem of that problem's D.
 struct EpiStoreF32Grouped {
   static constexpr int kStageBytes = kEpiTransposeBytes;
+  static constexpr bool kOverlapLoads = true;
   static constexpr int kMaxProblems = 3;
   struct Params {
     float* D[kMaxProblems];
@@ -464,6 +491,7 @@ struct EpiReluBf16 {
 // zeroed beforehand, and every slice of the tile adds its part).
 struct EpiRedF32 {
   static constexpr int kStageBytes = kEpiTransposeBytes;
+  static constexpr bool kOverlapLoads = true;
   struct Params {
     float* acc;
     int ld;
