@@ -1,7 +1,8 @@
 """Edge cases of the whole path against the fp64 oracle: an empty batch, a single
-token, tokens without any active neuron, and the longest per-token entry lists the
+token, tokens without any active neuron, the longest per-token entry lists the
 sparse forward accepts ((I / W) * C = 10240 entries with every neuron active, which
-fills one CTA's shared memory and runs the backward in 40 windows)."""
+fills one CTA's shared memory and runs the backward in 40 windows), and a hidden
+layer too wide for the backward's shared-memory column histogram."""
 import numpy as np
 import pytest
 
@@ -86,6 +87,18 @@ def test_tokens_without_active_neurons():
     empty = int((h.saved.row_nnz[:spec.T] == 0).sum().item())
     assert empty >= spec.T - 20
     _check_against_oracle(spec, inp, y_twell, y, grads, "idle tokens")
+
+
+def test_wide_hidden_layer():
+    # I = 49216 (769 tiles of 64) is past the 48K columns of the backward count
+    # pass's shared-memory histogram, so its column counts go to global atomics;
+    # three outlier tokens overflow a tile and go to the dense backup (checked on the
+    # oracle's activations when the case was chosen).
+    spec = FFNSpec("wide", T=128, d=256, I=49216, mean_active=60, outlier_frac=0.02, W=64, C=8, R=256, seed=8)
+    inp = make_inputs(spec, with_dy=True)
+    f, h, y_twell, y, grads = _run(spec, inp, ovf_cap=8, backup_cap=8)
+    assert int(h.saved.n_backup.item()) == 3
+    _check_against_oracle(spec, inp, y_twell, y, grads, "wide hidden layer")
 
 
 def _bf16(v):
