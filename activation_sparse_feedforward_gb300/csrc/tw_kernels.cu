@@ -314,6 +314,9 @@ cudaError_t launch_compact_rows(const uint8_t* ovf, const int32_t* row_nnz, int 
 }
 
 // ================================================================ row gather
+// 16-byte pieces a lane moves per row of the row gather and scatter: rows of up to
+// 2048 bf16 (d at most 2048) are 256 pieces, eight per lane.
+constexpr int kRowVecs = 8;
 struct GatherArgs {
   const uint16_t* src[2];
   uint16_t* out[2];
@@ -334,16 +337,24 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const GatherArgs g) {
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
   const int vec = g.d / 8;
-  // one warp per (row, matrix)
+  // one warp per (row, matrix); a lane's (at most kRowVecs) 16-byte pieces of the
+  // row are all loaded before any is stored, so their round trips overlap
   for (int w = blockIdx.x * wpb + (threadIdx.x >> 5); w < limit * g.nsrc; w += gridDim.x * wpb) {
     const int i = w / g.nsrc, which = w - i * g.nsrc;
-    uint4* o = reinterpret_cast<uint4*>(g.out[which] + static_cast<size_t>(i) * g.d);
+    uint4* o = reinterpret_cast<uint4*>((which ? g.out[1] : g.out[0]) + static_cast<size_t>(i) * g.d);
+    uint4 v[kRowVecs];
+#pragma unroll
+    for (int q = 0; q < kRowVecs; ++q) v[q] = make_uint4(0, 0, 0, 0);
     if (i < n) {
-      const uint4* r = reinterpret_cast<const uint4*>(g.src[which] + static_cast<size_t>(g.rows[i]) * g.d);
-      for (int c = lane; c < vec; c += 32) o[c] = __ldg(r + c);
-    } else {
-      for (int c = lane; c < vec; c += 32) o[c] = make_uint4(0, 0, 0, 0);
+      const uint4* r =
+          reinterpret_cast<const uint4*>((which ? g.src[1] : g.src[0]) + static_cast<size_t>(g.rows[i]) * g.d);
+#pragma unroll
+      for (int q = 0; q < kRowVecs; ++q)
+        if (lane + 32 * q < vec) v[q] = __ldg(r + lane + 32 * q);
     }
+#pragma unroll
+    for (int q = 0; q < kRowVecs; ++q)
+      if (lane + 32 * q < vec) o[lane + 32 * q] = v[q];
   }
   // the accumulator rows the split-K product adds into: 16-byte stores over the grid
   const size_t z4 = static_cast<size_t>(n) * g.zero_row_f32 / 4;
@@ -365,10 +376,22 @@ __global__ void __launch_bounds__(256) scatter_rows_bf16_kernel(const float* __r
   for (int i = blockIdx.x * wpb + (threadIdx.x >> 5); i < n; i += gridDim.x * wpb) {
     const float4* src = reinterpret_cast<const float4*>(acc + static_cast<size_t>(i) * N);
     uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(row_map[i]) * ldo);
-    for (int c = lane; c < N / 8; c += 32) {
-      const float4 a = src[2 * c], b = src[2 * c + 1];
-      dst[c] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
-                          pack_bf16x2(b.z, b.w));
+    // all of the lane's (at most kRowVecs) pieces are loaded before any is stored
+    float4 a[kRowVecs], b[kRowVecs];
+#pragma unroll
+    for (int q = 0; q < kRowVecs; ++q) {
+      const int c = lane + 32 * q;
+      if (c < N / 8) {
+        a[q] = src[2 * c];
+        b[q] = src[2 * c + 1];
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kRowVecs; ++q) {
+      const int c = lane + 32 * q;
+      if (c < N / 8)
+        dst[c] = make_uint4(pack_bf16x2(a[q].x, a[q].y), pack_bf16x2(a[q].z, a[q].w), pack_bf16x2(b[q].x, b[q].y),
+                            pack_bf16x2(b[q].z, b[q].w));
     }
   }
 }
@@ -376,6 +399,7 @@ __global__ void __launch_bounds__(256) scatter_rows_bf16_kernel(const float* __r
 cudaError_t launch_scatter_rows_bf16(const float* acc, int N, const int32_t* n_dev, int cap, const int32_t* row_map,
                                      uint16_t* out, int ldo, cudaStream_t s) {
   if (cap <= 0) return cudaSuccess;
+  if (N % 8 != 0 || N > 8 * 32 * kRowVecs) return cudaErrorInvalidValue;
   cudaError_t e = launch(scatter_rows_bf16_kernel, dim3(std::min(warp_grid(cap, 8), device_sm_count() * 2)), dim3(256),
                          0, s, acc, N, n_dev, cap, row_map, out, ldo);
   trace_mark(s, "scatter_rows");
@@ -386,6 +410,7 @@ cudaError_t launch_gather_rows(const uint16_t* src, int d, const int32_t* rows, 
                                int rows_alloc, uint16_t* out, cudaStream_t s, int32_t* status, const uint16_t* src2,
                                uint16_t* out2, float* zero, int zero_row_f32) {
   if (rows_alloc <= 0) return cudaSuccess;
+  if (d % 8 != 0 || d > 8 * 32 * kRowVecs) return cudaErrorInvalidValue;
   if (zero_row_f32 % 4 != 0 || (zero != nullptr && reinterpret_cast<uintptr_t>(zero) % 16 != 0))
     return cudaErrorInvalidValue;
   GatherArgs g{};
