@@ -199,32 +199,45 @@ cudaError_t launch_pack_dense(const uint16_t* A, int T, int I, int W, int C, con
 }
 
 // ================================================================ ordered compaction
-// One CTA of 1024 threads; thread i owns a run of consecutive rows. It counts the
-// flagged rows of its run, a block-wide exclusive scan of the counts gives the run's
-// first rank, and a second walk over the run writes the ranks, so the list comes out
-// in ascending row order. Runs are a multiple of 16 rows where T allows it, so both
-// walks move 16 rows at a time with vector loads and stores.
+// One CTA of 1024 threads walks the rows in rounds of 4 x 1024: in a round, thread i
+// owns rows base + 4 i .. base + 4 i + 3, so a warp's loads and stores cover 128
+// consecutive rows (one 512-byte line run per int32 array, 128 bytes of flags). A
+// block-wide exclusive scan of the threads' flagged counts, plus the rounds before,
+// gives each flagged row its rank, so the list comes out in ascending row order. The
+// next round's rows are loaded before the current round's scan.
 namespace {
-// flags of rows t0 .. t0 + 15 as a bit mask; z receives their row_nnz (0 without it)
-TW_DEV uint32_t flags16(const uint8_t* __restrict__ ovf, const int32_t* __restrict__ row_nnz, int R, int t0,
-                        int (&z)[16]) {
-  const uint4 f = *reinterpret_cast<const uint4*>(ovf + t0);
-  const uint32_t fw[4] = {f.x, f.y, f.z, f.w};
+struct Rows4 {
+  uint32_t flags;  // bit b: row base + 4 tid + b is flagged
+  int z[4];        // their row_nnz (0 without it)
+};
+TW_DEV Rows4 load_rows4(const uint8_t* __restrict__ ovf, const int32_t* __restrict__ row_nnz, int R, int T, int t,
+                        bool vec) {
+  Rows4 r{0u, {0, 0, 0, 0}};
+  uint32_t o4 = 0;
+  if (vec && t + 3 < T) {
+    o4 = *reinterpret_cast<const uint32_t*>(ovf + t);
+    if (row_nnz != nullptr) {
+      const int4 z = *reinterpret_cast<const int4*>(row_nnz + t);
+      r.z[0] = z.x;
+      r.z[1] = z.y;
+      r.z[2] = z.z;
+      r.z[3] = z.w;
+    }
+  } else {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int4 v = row_nnz != nullptr ? reinterpret_cast<const int4*>(row_nnz + t0)[q] : make_int4(0, 0, 0, 0);
-    z[4 * q] = v.x;
-    z[4 * q + 1] = v.y;
-    z[4 * q + 2] = v.z;
-    z[4 * q + 3] = v.w;
+    for (int b = 0; b < 4; ++b) {
+      if (t + b < T) {
+        o4 |= static_cast<uint32_t>(ovf[t + b] != 0) << (8 * b);
+        if (row_nnz != nullptr) r.z[b] = row_nnz[t + b];
+      }
+    }
   }
-  uint32_t m = 0;
 #pragma unroll
-  for (int b = 0; b < 16; ++b) {
-    const bool o = ((fw[b >> 2] >> (8 * (b & 3))) & 0xFFu) != 0;
-    m |= ((o || (row_nnz != nullptr && z[b] > R)) ? 1u : 0u) << b;
+  for (int b = 0; b < 4; ++b) {
+    const bool f = ((o4 >> (8 * b)) & 0xFFu) != 0 || (row_nnz != nullptr && r.z[b] > R);
+    r.flags |= (f && t + b < T ? 1u : 0u) << b;
   }
-  return m;
+  return r;
 }
 }  // namespace
 
@@ -236,71 +249,57 @@ __global__ void __launch_bounds__(1024) compact_rows_kernel(const uint8_t* __res
                                                             int32_t* status, int32_t* zero_word) {
   pdl_enter();
   if (zero_word != nullptr && threadIdx.x == 0) *zero_word = 0;
-  __shared__ int warp_tot[32];
+  __shared__ int warp_tot[2][32];  // by round parity: a round's totals are read while the next round's are written
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int nwarps = blockDim.x >> 5;
-  int per = (T + blockDim.x - 1) / blockDim.x;
-  per = (per + 15) / 16 * 16;
-  const int lo = min(T, tid * per), hi = min(T, lo + per);
-  const bool vec = (hi - lo) % 16 == 0;
-  auto flagged = [&](int t) {
-    const int o = ovf[t];
-    const int z = row_nnz != nullptr ? row_nnz[t] : 0;
-    return (o != 0) | (z > R && row_nnz != nullptr);
-  };
-  int n = 0;
-  if (vec) {
-    int z[16];
-    for (int t0 = lo; t0 < hi; t0 += 16) n += __popc(flags16(ovf, row_nnz, R, t0, z));
-  } else {
-    for (int t = lo; t < hi; ++t) n += flagged(t) ? 1 : 0;
-  }
-  const int incl = warp_inclusive_scan(n);
-  if (lane == 31) warp_tot[wid] = incl;
-  __syncthreads();
-  if (wid == 0) {
-    int v = lane < nwarps ? warp_tot[lane] : 0;
-    warp_tot[lane] = warp_inclusive_scan(v);
-  }
-  __syncthreads();
-  int pos = (wid ? warp_tot[wid - 1] : 0) + incl - n;
-  if (vec) {
-    for (int t0 = lo; t0 < hi; t0 += 16) {
-      int z[16], sl[16], en[16];
-      const uint32_t m = flags16(ovf, row_nnz, R, t0, z);
+  const int per_round = 4 * static_cast<int>(blockDim.x);
+  const bool vec_in = reinterpret_cast<uintptr_t>(ovf) % 4 == 0 &&
+                      (row_nnz == nullptr || reinterpret_cast<uintptr_t>(row_nnz) % 16 == 0);
+  const bool vec_out = (slot_of == nullptr || reinterpret_cast<uintptr_t>(slot_of) % 16 == 0) &&
+                       (ell_nnz == nullptr || reinterpret_cast<uintptr_t>(ell_nnz) % 16 == 0);
+  int carry = 0;  // flagged rows in the rounds before
+  Rows4 next = load_rows4(ovf, row_nnz, R, T, 4 * tid, vec_in);
+  for (int base = 0, round = 0; base < T; base += per_round, ++round) {
+    const Rows4 cur = next;
+    if (base + per_round < T) next = load_rows4(ovf, row_nnz, R, T, base + per_round + 4 * tid, vec_in);
+    const int c = __popc(cur.flags);
+    const int incl = warp_inclusive_scan(c);
+    int* wt = warp_tot[round & 1];
+    if (lane == 31) wt[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+      const int v = lane < nwarps ? wt[lane] : 0;
+      wt[lane] = warp_inclusive_scan(v);
+    }
+    __syncthreads();
+    int pos = carry + (wid ? wt[wid - 1] : 0) + incl - c;
+    carry += wt[nwarps - 1];
+    const int t = base + 4 * tid;
+    int sl[4], en[4];
 #pragma unroll
-      for (int b = 0; b < 16; ++b) {
-        const bool f = (m >> b) & 1u;
-        if (f && pos < list_cap) list[pos] = t0 + b;
-        sl[b] = f ? (pos < list_cap ? pos : -2) : -1;
-        en[b] = f ? 0 : z[b];
-        pos += f ? 1 : 0;
-      }
+    for (int b = 0; b < 4; ++b) {
+      const bool f = (cur.flags >> b) & 1u;
+      if (f && pos < list_cap) list[pos] = t + b;
+      sl[b] = f ? (pos < list_cap ? pos : -2) : -1;
+      en[b] = f ? 0 : cur.z[b];
+      pos += f ? 1 : 0;
+    }
+    if (vec_out && t + 3 < T) {
+      if (slot_of) *reinterpret_cast<int4*>(slot_of + t) = make_int4(sl[0], sl[1], sl[2], sl[3]);
+      if (ell_nnz) *reinterpret_cast<int4*>(ell_nnz + t) = make_int4(en[0], en[1], en[2], en[3]);
+    } else {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (slot_of)
-          reinterpret_cast<int4*>(slot_of + t0)[q] = make_int4(sl[4 * q], sl[4 * q + 1], sl[4 * q + 2], sl[4 * q + 3]);
-        if (ell_nnz)
-          reinterpret_cast<int4*>(ell_nnz + t0)[q] = make_int4(en[4 * q], en[4 * q + 1], en[4 * q + 2], en[4 * q + 3]);
+      for (int b = 0; b < 4; ++b) {
+        if (t + b < T) {
+          if (slot_of) slot_of[t + b] = sl[b];
+          if (ell_nnz) ell_nnz[t + b] = en[b];
+        }
       }
     }
-  } else {
-    for (int t = lo; t < hi; ++t) {
-      const bool f = flagged(t);
-      if (f) {
-        if (pos < list_cap) list[pos] = t;
-        if (slot_of) slot_of[t] = pos < list_cap ? pos : -2;
-        ++pos;
-      } else if (slot_of) {
-        slot_of[t] = -1;
-      }
-      if (ell_nnz) ell_nnz[t] = f ? 0 : row_nnz[t];
-    }
   }
-  if (tid == blockDim.x - 1) {
-    const int total = warp_tot[nwarps - 1];
-    *count = total;
-    if (total > cap_check) raise_status(status, TW_ECAPACITY);
+  if (tid == 0) {
+    *count = carry;
+    if (carry > cap_check) raise_status(status, TW_ECAPACITY);
   }
 }
 
