@@ -213,9 +213,15 @@ def make_inputs(spec: FFNSpec, layer: int = 0, with_dy: bool = False) -> dict:
     return out
 
 
-def random_bf16_matrix(shape, density: float, seed: int, negative_zero_frac: float = 0.0) -> np.ndarray:
+def random_bf16_matrix(shape, density: float, seed: int, negative_zero_frac: float = 0.0,
+                       signed: bool = False, subnormal_frac: float = 0.0) -> np.ndarray:
     """A bf16 matrix whose entries are nonzero with probability ``density`` (values ~ |N(0,1)|,
-    i.e. post-ReLU-like). A fraction of the zero entries can be written as -0.0 (0x8000)."""
+    i.e. post-ReLU-like). A fraction of the zero entries can be written as -0.0 (0x8000).
+
+    ``signed`` gives each nonzero a random sign (a general matrix for the standalone
+    packer, whose nonzero test is on the magnitude bits); ``subnormal_frac`` of the
+    nonzeros become bf16 subnormals: the smallest (0x0001) and the largest (0x007F)
+    magnitudes, with the sign the entry had."""
     rng = np.random.default_rng([seed, 9001])
     vals = np.abs(rng.standard_normal(shape, dtype=np.float32)) + np.float32(1e-3)
     keep = rng.random(shape) < density
@@ -223,4 +229,10 @@ def random_bf16_matrix(shape, density: float, seed: int, negative_zero_frac: flo
     if negative_zero_frac > 0:
         negz = (~keep) & (rng.random(shape) < negative_zero_frac)
         bits[negz] = 0x8000
+    if subnormal_frac > 0:
+        sub = keep & (rng.random(shape) < subnormal_frac)
+        bits[sub] = np.where(rng.random(shape) < 0.5, 0x0001, 0x007F).astype(np.uint16)[sub]
+    if signed:
+        neg = keep & (rng.random(shape) < 0.5)
+        bits[neg] |= np.uint16(0x8000)
     return bits

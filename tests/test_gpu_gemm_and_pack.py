@@ -65,11 +65,14 @@ def _assert_twell_equal(gpu: "tw.TwELL", ref: dict, rows=None):
     assert T == gpu.T
 
 
-@pytest.mark.parametrize("T,I,W,C,density", [(1, 64, 64, 1, 0.5), (77, 640, 64, 8, 0.05),
-                                             (300, 1024, 128, 16, 0.1), (513, 768, 128, 4, 0.02),
-                                             (64, 256, 128, 128, 1.0), (50, 256, 64, 8, 0.0)])
-def test_twell_pack_bit_exact(T, I, W, C, density):
-    A = random_bf16_matrix((T, I), density, seed=T + I, negative_zero_frac=0.3)
+@pytest.mark.parametrize("T,I,W,C,density,signed", [(1, 64, 64, 1, 0.5, False), (77, 640, 64, 8, 0.05, False),
+                                                    (300, 1024, 128, 16, 0.1, False), (513, 768, 128, 4, 0.02, False),
+                                                    (64, 256, 128, 128, 1.0, False), (50, 256, 64, 8, 0.0, False),
+                                                    # negative nonzeros and bf16 subnormals count, -0.0 does not
+                                                    (129, 512, 64, 8, 0.1, True), (200, 1024, 128, 16, 0.3, True)])
+def test_twell_pack_bit_exact(T, I, W, C, density, signed):
+    A = random_bf16_matrix((T, I), density, seed=T + I, negative_zero_frac=0.3, signed=signed,
+                           subnormal_frac=0.2 if signed else 0.0)
     out = tw.twell_pack(to_dev(A), W, C)
     torch.cuda.synchronize()
     _assert_twell_equal(out, formats.twell_pack(A, W, C))

@@ -91,15 +91,21 @@ def brute_force_twell(A, W, C):
     return cnt, slots, ovf
 
 
-@pytest.mark.parametrize("shape,W,C,density,seed", [
-    ((7, 16), 4, 2, 0.3, 1),
-    ((5, 64), 64, 8, 0.1, 2),
-    ((9, 256), 128, 16, 0.08, 3),
-    ((3, 12), 4, 4, 0.9, 4),
-    ((6, 8), 8, 1, 0.2, 5),
+@pytest.mark.parametrize("shape,W,C,density,seed,signed", [
+    ((7, 16), 4, 2, 0.3, 1, False),
+    ((5, 64), 64, 8, 0.1, 2, False),
+    ((9, 256), 128, 16, 0.08, 3, False),
+    ((3, 12), 4, 4, 0.9, 4, False),
+    ((6, 8), 8, 1, 0.2, 5, False),
+    # a general matrix: negative nonzeros and bf16 subnormals count, -0.0 does not
+    ((8, 128), 64, 6, 0.3, 6, True),
+    ((5, 256), 128, 16, 0.15, 7, True),
 ])
-def test_twell_matches_brute_force(shape, W, C, density, seed):
-    A = random_bf16_matrix(shape, density, seed, negative_zero_frac=0.3)
+def test_twell_matches_brute_force(shape, W, C, density, seed, signed):
+    A = random_bf16_matrix(shape, density, seed, negative_zero_frac=0.3, signed=signed,
+                           subnormal_frac=0.2 if signed else 0.0)
+    if signed:
+        assert ((A & 0x8000) != 0)[(A & 0x7FFF) != 0].any() and (((A & 0x7F80) == 0) & ((A & 0x7FFF) != 0)).any()
     tw = formats.twell_pack(A, W, C)
     cnt, slots, ovf = brute_force_twell(A, W, C)
     np.testing.assert_array_equal(tw["cnt"], np.array(cnt))
@@ -115,7 +121,7 @@ def test_twell_matches_brute_force(shape, W, C, density, seed):
 @pytest.mark.parametrize("density", [0.0, 0.005, 0.05, 0.3, 1.0])
 def test_twell_invariants(density):
     W, C = 64, 8
-    A = random_bf16_matrix((40, 320), density, seed=11, negative_zero_frac=0.5)
+    A = random_bf16_matrix((40, 320), density, seed=11, negative_zero_frac=0.5, signed=True, subnormal_frac=0.1)
     tw = formats.twell_pack(A, W, C)
     nz = (A & 0x7FFF) != 0
     assert tw["cnt"].sum() == nz.sum() == tw["row_nnz"].sum()

@@ -91,6 +91,8 @@ FORMAT_MUTANTS = [
     ("-0.0 counted as nonzero", "return (A & 0x7FFF) != 0", "return A != 0"),
     ("routing ignores TwELL overflow", "backup = tw[\"ovf\"] | (tw[\"row_nnz\"] > R)", "backup = tw[\"row_nnz\"] > R"),
     ("capped count stored", "cnt = nz.sum(axis=2).astype(np.int64)", "cnt = np.minimum(nz.sum(axis=2), C).astype(np.int64)"),
+    ("negative values not counted", "return (A & 0x7FFF) != 0", "return ((A & 0x7FFF) != 0) & ((A & 0x8000) == 0)"),
+    ("subnormals not counted", "return (A & 0x7FFF) != 0", "return (A & 0x7F80) != 0"),
 ]
 
 
@@ -102,7 +104,8 @@ def _format_pins(fm):
         tf.test_twell_golden_worked_example()
         tf.test_hybrid_golden_worked_example()
         tf.test_twell_capacity_boundary()
-        for args in [((7, 16), 4, 2, 0.3, 1), ((9, 256), 128, 16, 0.08, 3)]:
+        for args in [((7, 16), 4, 2, 0.3, 1, False), ((9, 256), 128, 16, 0.08, 3, False),
+                     ((8, 128), 64, 6, 0.3, 6, True)]:
             tf.test_twell_matches_brute_force(*args)
     finally:
         tf.formats = orig
@@ -117,3 +120,41 @@ def test_format_mutant_is_caught(desc, old, new):
 def test_unmutated_formats_pass():
     _format_pins(oracle.formats)
     assert random_bf16_matrix((2, 2), 0.5, 0).dtype == np.uint16
+
+
+NEURON_MUTANTS = [
+    ("bf16 by truncation", "return ((bits + np.uint64(0x7FFF) + lsb) >> np.uint64(16)).astype(np.uint16)",
+     "return (bits >> np.uint64(16)).astype(np.uint16)"),
+    ("product in float32", "w = (np.float64(np.float32(std)) * z).astype(np.float32)",
+     "w = np.float32(std) * z.astype(np.float32)"),
+    # bf16 straight from the float64 product (round half to even at 8 significant
+    # bits), skipping the float32 rounding the definition states
+    ("no float32 step", "w = (np.float64(np.float32(std)) * z).astype(np.float32)",
+     "w = np.float64(np.float32(std)) * z\n"
+     "    e = np.floor(np.log2(np.abs(np.where(w == 0, 1.0, w))))\n"
+     "    w = (np.round(np.ldexp(w, (7 - e).astype(np.int64))) * np.exp2(e - 7)).astype(np.float32)"),
+    ("uniforms from the wrong bits", ">> np.uint64(40)).astype(np.int64)", ">> np.uint64(41)).astype(np.int64)"),
+    ("counter offset", "base + np.uint64(i)", "base + np.uint64(i + 1)"),
+]
+
+
+def _neuron_pins(nm):
+    import test_oracle_neurons as tn
+    orig = tn.neurons
+    tn.neurons = nm
+    try:
+        tn.test_reinit_known_answers()
+        tn.test_irwin_hall_draw_moments_and_support()
+        tn.test_reinit_touches_dead_rows_only()
+    finally:
+        tn.neurons = orig
+
+
+@pytest.mark.parametrize("desc,old,new", NEURON_MUTANTS, ids=[m[0] for m in NEURON_MUTANTS])
+def test_neuron_mutant_is_caught(desc, old, new):
+    m = _mutant("neurons", old, new)
+    assert _fails(_neuron_pins, m), f"not caught: {desc}"
+
+
+def test_unmutated_neurons_pass():
+    _neuron_pins(oracle.neurons)

@@ -1,6 +1,12 @@
 """Pins of oracle/neurons.py: the SplitMix64 outputs its reference implementation
 gives for seed 0, the Irwin-Hall draw's moments and support, counts against brute
-force and against the Hybrid packing, and re-initialisation touching dead rows only."""
+force and against the Hybrid packing, re-initialisation touching dead rows only, and
+hand-derived known answers of the draw at bf16 rounding midpoints
+(tests/golden/reinit_splitmix64_pins.json)."""
+import json
+import os
+from fractions import Fraction
+
 import numpy as np
 
 from oracle import ffn, formats, neurons
@@ -73,3 +79,36 @@ def test_reinit_touches_dead_rows_only():
     assert n == dead.sum()
     assert np.array_equal(W2[~dead], W[~dead])
     assert np.array_equal(W2[dead], neurons.reinit_values(11, np.flatnonzero(dead), 64, 0.05))
+
+
+REINIT_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "reinit_splitmix64_pins.json")
+
+
+def _f32_of_hex(h: str) -> float:
+    return float(np.array([int(h, 16)], dtype=np.uint32).view(np.float32)[0])
+
+
+def test_reinit_known_answers():
+    """The draw against a hand-derived fixture: three elements whose float32 value is a
+    bf16 midpoint or near one, so that truncation, skipping the float32 step, or a
+    float32 product gives other bits than the rounding the definition states."""
+    with open(REINIT_GOLDEN) as f:
+        g = json.load(f)
+    outs = [int(h, 16) for h in g["outputs_hex"]]
+    # the fixture's first three outputs are SplitMix64's published ones for seed 0
+    assert outs[:3] == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+    d = g["d"]
+    for case in g["cases"]:
+        first = 12 * (case["row"] * d + case["col"])
+        # the derivation chain, step by step, in exact integer / rational arithmetic
+        assert [o >> 40 for o in outs[first:first + 12]] == case["top24"]
+        assert sum(case["top24"]) == case["sum"]
+        z = Fraction(case["sum"], 1 << 24) - 6
+        assert z == Fraction(*case["z"])
+        std = _f32_of_hex(case["std_f32_hex"])
+        if "w_exact" in case:
+            assert Fraction(std) * z == Fraction(*case["w_exact"])
+        w32 = np.float32(float(Fraction(std) * z))
+        assert int(np.array([w32]).view(np.uint32)[0]) == int(case["w_f32_hex"], 16)
+        got = neurons.reinit_values(g["seed"], np.array([case["row"]]), d, std)[0, case["col"]]
+        assert int(got) == int(case["bf16_rne_of_f32"], 16), (case["note"], hex(int(got)))
