@@ -294,9 +294,13 @@ static tw_status twell_sparse_impl(const uint16_t* x, const uint16_t* Wg, const 
   return TW_OK;
 }
 
-static tw_status check_twell_fwd_args(const uint16_t* x, const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd,
-                                      int T, int d, int I, int W, int C, int ovf_cap, const tw_twell* tw_out,
-                                      void* ws, size_t ws_bytes, uint16_t* y, int32_t* dev_status) {
+}  // extern "C"
+
+namespace tw {
+// Every argument check of twell_ffn_fwd except the workspace's.
+tw_status check_twell_fwd_operands(const uint16_t* x, const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd,
+                                   int T, int d, int I, int W, int C, int ovf_cap, const tw_twell* tw_out,
+                                   uint16_t* y, int32_t* dev_status) {
   tw_status st = check_tile_geometry(T, I, W, C);
   if (st != TW_OK) return st;
   st = check_model_width(d);
@@ -308,6 +312,17 @@ static tw_status check_twell_fwd_args(const uint16_t* x, const uint16_t* Wg, con
   st = check_ptrs({x, Wg, Wd, y, dev_status});
   if (st != TW_OK) return st;
   if (Wu != nullptr && !aligned16(Wu)) return TW_EALIGN;
+  return TW_OK;
+}
+}  // namespace tw
+
+extern "C" {
+
+static tw_status check_twell_fwd_args(const uint16_t* x, const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd,
+                                      int T, int d, int I, int W, int C, int ovf_cap, const tw_twell* tw_out,
+                                      void* ws, size_t ws_bytes, uint16_t* y, int32_t* dev_status) {
+  tw_status st = tw::check_twell_fwd_operands(x, Wg, Wu, Wd, T, d, I, W, C, ovf_cap, tw_out, y, dev_status);
+  if (st != TW_OK || T == 0) return st;
   if (ws_bytes < twell_ffn_fwd_workspace_size(T, d, I, W, C, ovf_cap)) return TW_EWORKSPACE;
   if (ovf_cap > 0 && ws == nullptr) return TW_EINVAL;
   return TW_OK;

@@ -50,6 +50,25 @@ TW_DEV uint32_t pack_bf16x2_rn(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
+// ------------------------------------------------------------------ packed fp32 pairs
+// Two fp32 lanes in one 64-bit register, the operand form of Blackwell's packed
+// `fma.rn.f32x2`, which the CUDA-core accumulations use (half the FMA instructions).
+typedef unsigned long long f32x2;
+TW_DEV f32x2 pair(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+TW_DEV float2 unpair(f32x2 v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return make_float2(lo, hi);
+}
+// acc += a * b on both lanes (round to nearest even, one rounding per lane)
+TW_DEV void fma2(f32x2& acc, f32x2 a, f32x2 b) { asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b)); }
+// a packed bf16 pair (low half = element 0) widened exactly to two fp32 lanes
+TW_DEV f32x2 widen(uint32_t w) { return pair(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)); }
+
 // ------------------------------------------------------------------ smem / timers
 TW_DEV uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

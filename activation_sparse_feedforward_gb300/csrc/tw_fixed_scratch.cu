@@ -15,6 +15,13 @@
 // at zero, because every byte the forward reads from its scratch is written earlier
 // in the same call. Two calls whose work overlaps on the GPU (different streams,
 // no ordering between them) race on the array.
+//
+// The array's device address is looked up once per device, in the context that is
+// current on the first call (the CUDA runtime's primary context for that device),
+// and kept for the life of the process. The call therefore assumes that every later
+// call on that device runs in the same context, and that the device is not reset
+// (cudaDeviceReset) in between: after a reset the kept address would point into a
+// context that no longer exists.
 #include <mutex>
 
 #include "tw_internal.h"
@@ -38,7 +45,10 @@ extern "C" tw_status twell_ffn_fwd_fixed_scratch(const uint16_t* x, const uint16
                                                  const uint16_t* Wd, int T, int d, int I, int W, int C, int ovf_cap,
                                                  const tw_twell* tw_out, uint16_t* y, int32_t* dev_status,
                                                  void* stream) {
-  if (T < 0 || d <= 0 || I <= 0 || W <= 0 || C <= 0 || ovf_cap < 0) return TW_EINVAL;
+  // the arguments are checked as twell_ffn_fwd checks them, so a bad argument gets the
+  // same error code from both entry points; then the size against the fixed array
+  const tw_status st = tw::check_twell_fwd_operands(x, Wg, Wu, Wd, T, d, I, W, C, ovf_cap, tw_out, y, dev_status);
+  if (st != TW_OK || T == 0) return st;
   if (twell_ffn_fwd_workspace_size(T, d, I, W, C, ovf_cap) > kFixedScratchBytes) return TW_EWORKSPACE;
 
   // one-time set-up per device, with that device current: look up the device

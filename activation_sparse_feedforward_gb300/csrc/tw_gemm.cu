@@ -120,8 +120,9 @@ cudaError_t gemm_gate_relu_dense(const uint16_t* x, const uint16_t* Wg, int T, i
 }
 
 // ------------------------------------------------------------------ dense backup, forward
-// 128-wide column tiles when I allows them (one round of tiles on 152 SMs at the
-// common sizes), else 64-wide; as many stages as fit about 192 KB.
+// The gated form (two B operands, gate and up, into two accumulators) runs 64-wide
+// column tiles; the non-gated form 128-wide tiles when I allows them, else 64-wide;
+// as many stages as fit about 192 KB.
 template <int BN, bool GATED>
 static cudaError_t backup_hidden_bn(const uint16_t* X, const uint16_t* Wg, const uint16_t* Wu, int rows_alloc,
                                     const int32_t* n_dev, int cap, int d, int I, uint16_t* H, uint16_t* H_lo,
@@ -144,12 +145,11 @@ cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint
                                const int32_t* n_dev, int cap, int d, int I, uint16_t* H, uint16_t* H_lo,
                                float* save_a, float* save_u, int32_t* status, cudaStream_t s) {
   if (cap <= 0) return cudaSuccess;
-  const bool gated = Wu != nullptr;
+  if (Wu != nullptr)
+    return backup_hidden_bn<64, true>(X, Wg, Wu, rows_alloc, n_dev, cap, d, I, H, H_lo, save_a, save_u, status, s);
   if (I % 128 == 0)
-    return gated ? backup_hidden_bn<128, true>(X, Wg, Wu, rows_alloc, n_dev, cap, d, I, H, H_lo, save_a, save_u, status, s)
-                 : backup_hidden_bn<128, false>(X, Wg, Wu, rows_alloc, n_dev, cap, d, I, H, H_lo, save_a, save_u, status, s);
-  return gated ? backup_hidden_bn<64, true>(X, Wg, Wu, rows_alloc, n_dev, cap, d, I, H, H_lo, save_a, save_u, status, s)
-               : backup_hidden_bn<64, false>(X, Wg, Wu, rows_alloc, n_dev, cap, d, I, H, H_lo, save_a, save_u, status, s);
+    return backup_hidden_bn<128, false>(X, Wg, Wu, rows_alloc, n_dev, cap, d, I, H, H_lo, save_a, save_u, status, s);
+  return backup_hidden_bn<64, false>(X, Wg, Wu, rows_alloc, n_dev, cap, d, I, H, H_lo, save_a, save_u, status, s);
 }
 
 // Same product for few rows, spread over every SM: 256-wide column tiles, each tile's

@@ -13,6 +13,12 @@ namespace tw {
 
 int device_sm_count();
 
+// Every host-side argument check of twell_ffn_fwd except the workspace size
+// (tw_api.cu), shared with the fixed-scratch entry point.
+tw_status check_twell_fwd_operands(const uint16_t* x, const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd,
+                                   int T, int d, int I, int W, int C, int ovf_cap, const tw_twell* tw_out,
+                                   uint16_t* y, int32_t* dev_status);
+
 // Timing trace (tw_trace_begin): records the next caller event on `s` after a launch.
 void trace_begin(void* const* events, int capacity);
 int trace_end();

@@ -20,34 +20,21 @@ constexpr int kWgradUnroll = 4;
 // ---------------------------------------------------------------- row arithmetic
 // The accumulation is bound by instruction issue, so it uses Blackwell's packed
 // fp32x2 FMA. Eight fp32 accumulators live as four packed pairs.
-typedef unsigned long long f32x2;
 struct F8 {
   f32x2 v[4];
 };
 TW_DEV void f8_zero(F8& a) { a.v[0] = a.v[1] = a.v[2] = a.v[3] = 0ull; }
-TW_DEV f32x2 f2(float lo, float hi) {
-  f32x2 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-TW_DEV float2 f2_split(f32x2 v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-  return make_float2(lo, hi);
-}
-TW_DEV f32x2 bf16x2_to_f32x2(uint32_t w) { return f2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)); }
-TW_DEV void fma2(f32x2& acc, f32x2 a, f32x2 b) { asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b)); }
 // y += h * w over 8 bf16 elements (h2 = {h, h})
 TW_DEV void axpy8(F8& y, f32x2 h2, const uint4& w) {
-  fma2(y.v[0], h2, bf16x2_to_f32x2(w.x));
-  fma2(y.v[1], h2, bf16x2_to_f32x2(w.y));
-  fma2(y.v[2], h2, bf16x2_to_f32x2(w.z));
-  fma2(y.v[3], h2, bf16x2_to_f32x2(w.w));
+  fma2(y.v[0], h2, widen(w.x));
+  fma2(y.v[1], h2, widen(w.y));
+  fma2(y.v[2], h2, widen(w.z));
+  fma2(y.v[3], h2, widen(w.w));
 }
 // g += cg * x and u += cu * x sharing one conversion of x
 TW_DEV void axpy8_two(F8& g, f32x2 cg2, F8& u, f32x2 cu2, const uint4& x) {
-  const f32x2 x0 = bf16x2_to_f32x2(x.x), x1 = bf16x2_to_f32x2(x.y), x2 = bf16x2_to_f32x2(x.z),
-              x3 = bf16x2_to_f32x2(x.w);
+  const f32x2 x0 = widen(x.x), x1 = widen(x.y), x2 = widen(x.z),
+              x3 = widen(x.w);
   fma2(g.v[0], cg2, x0);
   fma2(g.v[1], cg2, x1);
   fma2(g.v[2], cg2, x2);
@@ -58,13 +45,13 @@ TW_DEV void axpy8_two(F8& g, f32x2 cg2, F8& u, f32x2 cu2, const uint4& x) {
   fma2(u.v[3], cu2, x3);
 }
 TW_DEV void stcs_f32x8(float* p, const F8& y) {
-  const float2 a = f2_split(y.v[0]), b = f2_split(y.v[1]), c = f2_split(y.v[2]), d = f2_split(y.v[3]);
+  const float2 a = unpair(y.v[0]), b = unpair(y.v[1]), c = unpair(y.v[2]), d = unpair(y.v[3]);
   __stcs(reinterpret_cast<float4*>(p), make_float4(a.x, a.y, b.x, b.y));
   __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(c.x, c.y, d.x, d.y));
 }
 // y added into p with fp32 vector reductions (the L2 does the adds; no round trip)
 TW_DEV void red_f32x8(float* p, const F8& y) {
-  const float2 a = f2_split(y.v[0]), b = f2_split(y.v[1]), c = f2_split(y.v[2]), d = f2_split(y.v[3]);
+  const float2 a = unpair(y.v[0]), b = unpair(y.v[1]), c = unpair(y.v[2]), d = unpair(y.v[3]);
   atomicAdd(reinterpret_cast<float4*>(p), make_float4(a.x, a.y, b.x, b.y));
   atomicAdd(reinterpret_cast<float4*>(p) + 1, make_float4(c.x, c.y, d.x, d.y));
 }
@@ -294,9 +281,9 @@ __global__ void __launch_bounds__(256, 4) ell_weight_grad_kernel(const SparseBwd
 #pragma unroll
           for (int q = 0; q < U; ++q) {
             if (GATED)
-              axpy8_two(p, f2(cg[q], cg[q]), q2, f2(cu[q], cu[q]), v[q]);
+              axpy8_two(p, pair(cg[q], cg[q]), q2, pair(cu[q], cu[q]), v[q]);
             else
-              axpy8(p, f2(cg[q], cg[q]), v[q]);
+              axpy8(p, pair(cg[q], cg[q]), v[q]);
           }
         }
       } else {
@@ -310,7 +297,7 @@ __global__ void __launch_bounds__(256, 4) ell_weight_grad_kernel(const SparseBwd
             v[q] = ldg16(src + __float_as_uint(e.w));
           }
 #pragma unroll
-          for (int q = 0; q < U; ++q) axpy8(p, f2(ch[q], ch[q]), v[q]);
+          for (int q = 0; q < U; ++q) axpy8(p, pair(ch[q], ch[q]), v[q]);
         }
       }
     }

@@ -41,20 +41,6 @@ __host__ __device__ constexpr int ctas_per_sm(int nch) { return 48 / nch < 32 ? 
 
 __host__ __device__ constexpr uint32_t rup(uint32_t v, uint32_t m) { return (v + m - 1) / m * m; }
 
-typedef unsigned long long f32x2;
-TW_DEV f32x2 pair(float lo, float hi) {
-  f32x2 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-TW_DEV float2 unpair(f32x2 v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-  return make_float2(lo, hi);
-}
-TW_DEV void fma2(f32x2& acc, f32x2 a, f32x2 b) { asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b)); }
-TW_DEV f32x2 widen(uint32_t w) { return pair(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)); }
-
 // eight fp32 accumulators as four packed pairs
 struct Acc8 {
   f32x2 v[4];

@@ -168,7 +168,12 @@ tw_status twell_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* W
  *  - The array occupies 20 MiB on every GPU where the library's code is loaded,
  *    until the process exits.
  *  - The first call on each device looks up the array's device address (with that
- *    device current); make that first call before any stream capture.
+ *    device current); make that first call before any stream capture. The address
+ *    is kept for the life of the process, so every call on that device must run in
+ *    the same context as the first one (the runtime's primary context), and the
+ *    device must not be reset (cudaDeviceReset) between calls.
+ *  - Arguments are checked as twell_ffn_fwd checks them (same error codes); only
+ *    then is the size compared with the array.
  *  - All calls share the one array and it keeps the previous call's contents;
  *    nothing in it needs to start at zero. Calls whose GPU work overlaps (on
  *    unordered streams) race on it: order them on one stream.

@@ -65,8 +65,26 @@ def test_fixed_scratch_matches_workspace_entry_point(lib, spec, ovf_cap):
 
 
 def test_fixed_scratch_rejects_shapes_beyond_its_size(lib):
-    # 513 overflow rows at d = 2048, I = 5632 need more than the 20 MiB array: refused on the host
-    s = _lib.TwTwell(16384, 5632, 128, 16, 16, 16, 16, 16, 16, 16, 16)
-    code = lib.twell_ffn_fwd_fixed_scratch(16, 16, 16, 16, 16384, 2048, 5632, 128, 16, 513, ctypes.byref(s),
-                                           16, 16, None)
-    assert code == _lib.TW_EWORKSPACE
+    # 513 overflow rows at d = 2048, I = 5632 need more than the 20 MiB array: refused on the
+    # host before anything is enqueued. Every buffer is a real device buffer of its full
+    # size, so even a call that did run would stay inside them.
+    T, d, I, W, C = 600, 2048, 5632, 128, 16
+    dv = {k: torch.zeros(shape, dtype=torch.bfloat16, device="cuda")
+          for k, shape in (("x", (T, d)), ("Wg", (I, d)), ("Wu", (I, d)), ("Wd", (I, d)))}
+    twl = tw.TwELL.empty(T, I, W, C)
+    y = torch.full((T, d), 7.0, dtype=torch.bfloat16, device="cuda")
+    status = tw.new_status()
+    s = twl.struct()
+    torch.cuda.synchronize()
+    code = lib.twell_ffn_fwd_fixed_scratch(dv["x"].data_ptr(), dv["Wg"].data_ptr(), dv["Wu"].data_ptr(),
+                                           dv["Wd"].data_ptr(), T, d, I, W, C, 513, ctypes.byref(s), y.data_ptr(),
+                                           status.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert code == _lib.TW_EWORKSPACE, lib.tw_status_str(code)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0                   # nothing ran: no device condition raised
+    assert bool((y == 7.0).all())                    # and y was not written
+    # an argument twell_ffn_fwd rejects gets the same code here, whatever the size
+    code = lib.twell_ffn_fwd_fixed_scratch(dv["x"].data_ptr(), dv["Wg"].data_ptr(), dv["Wu"].data_ptr(),
+                                           dv["Wd"].data_ptr(), T, d, I, W, C, T + 1, ctypes.byref(s), y.data_ptr(),
+                                           status.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert code == _lib.TW_EINVAL, lib.tw_status_str(code)
