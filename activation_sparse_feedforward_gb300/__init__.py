@@ -14,10 +14,14 @@ from .ops import (  # noqa: F401
     fma_probe,
     gate_relu_dense,
     hybrid_neuron_counts,
+    hybrid_pack,
+    hybrid_unpack,
+    l2_gather_probe,
     new_status,
     raise_if_device_error,
     reinit_dead_rows,
     twell_ffn_fwd,
     twell_gate_pack,
     twell_pack,
+    twell_unpack,
 )

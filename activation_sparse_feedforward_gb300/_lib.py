@@ -9,14 +9,16 @@ import ctypes
 import os
 import threading
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtwell.so")
+# TW_LIB_PATH selects another build of the same library (the bounds-checked one)
+LIB_PATH = os.environ.get("TW_LIB_PATH") or os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtwell.so")
 
 c_void_p = ctypes.c_void_p
 c_int = ctypes.c_int
 c_size_t = ctypes.c_size_t
 c_float = ctypes.c_float
 
-TW_OK, TW_EINVAL, TW_EALIGN, TW_EUNSUPPORTED, TW_ECAPACITY, TW_ETIMEOUT, TW_ECUDA, TW_EWORKSPACE = range(8)
+(TW_OK, TW_EINVAL, TW_EALIGN, TW_EUNSUPPORTED, TW_ECAPACITY, TW_ETIMEOUT, TW_ECUDA, TW_EWORKSPACE,
+ TW_EBOUNDS) = range(9)
 
 
 class TwTwell(ctypes.Structure):
@@ -38,6 +40,11 @@ SIGNATURES = {
     "tw_status_str": (ctypes.c_char_p, [c_int]),
     "tw_abi_version": (c_int, []),
     "twell_pack": (c_int, [c_void_p, c_int, c_int, c_int, c_int, ctypes.POINTER(TwTwell), c_void_p, c_void_p]),
+    "twell_unpack": (c_int, [ctypes.POINTER(TwTwell), c_void_p, c_void_p]),
+    "hybrid_pack_workspace_size": (c_size_t, [c_int]),
+    "hybrid_pack": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, ctypes.POINTER(TwHybrid), c_void_p,
+                            c_size_t, c_void_p, c_void_p]),
+    "hybrid_unpack": (c_int, [ctypes.POINTER(TwHybrid), c_void_p, c_void_p, c_void_p]),
     "twell_gate_pack": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, ctypes.POINTER(TwTwell),
                                 c_void_p, c_void_p, c_void_p]),
     "twell_ffn_fwd_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int, c_int]),
@@ -59,6 +66,10 @@ SIGNATURES = {
     "tw_reinit_dead_rows": (c_int, [c_void_p, c_int, c_int, c_void_p, ctypes.c_uint64, c_float, c_void_p, c_void_p]),
     "tw_dense_gemm": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p,
                               c_void_p]),
+    "tw_l2_gather_probe": (c_int, [c_void_p, c_int, c_int, c_void_p, c_int, c_void_p, c_int,
+                                   ctypes.POINTER(ctypes.c_double), c_void_p]),
+    "tw_l2_gather_probe_blocks": (c_int, [c_int]),
+    "tw_wait_timeout_probe": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]),
     "tw_fma_probe": (c_int, [c_void_p, c_int, c_int, ctypes.POINTER(ctypes.c_double), c_void_p]),
     "tw_trace_begin": (c_int, [ctypes.POINTER(c_void_p), c_int]),
     "tw_trace_end": (c_int, []),

@@ -193,6 +193,7 @@ const char* tw_status_str(int status) {
     case TW_ETIMEOUT: return "TW_ETIMEOUT: a bounded pipeline wait gave up";
     case TW_ECUDA: return "TW_ECUDA: CUDA runtime error";
     case TW_EWORKSPACE: return "TW_EWORKSPACE: workspace too small";
+    case TW_EBOUNDS: return "TW_EBOUNDS: an index read from the data fell outside its buffer (checked build)";
     default: return "unknown tw_status";
   }
 }
@@ -280,7 +281,7 @@ static tw_status twell_sparse_impl(const uint16_t* x, const uint16_t* Wg, const 
   a.sched_zeroed = false;
   TW_TRY(tw::launch_token_fwd(a, s));
   if (ovf_cap > 0) {
-    TW_TRY(tw::launch_gather_rows(x, d, o.ovf_rows, o.n_ovf, ovf_cap, ra, w.X, s, dev_status, nullptr, nullptr,
+    TW_TRY(tw::launch_gather_rows(x, d, T, o.ovf_rows, o.n_ovf, ovf_cap, ra, w.X, s, dev_status, nullptr, nullptr,
                                   w.acc, d));
     TW_TRY(tw::gemm_backup_hidden(w.X, Wg, Wu, ra, o.n_ovf, ovf_cap, d, I, w.H, w.H_lo, nullptr, nullptr,
                                   dev_status, s));
@@ -289,7 +290,7 @@ static tw_status twell_sparse_impl(const uint16_t* x, const uint16_t* Wg, const 
     const uint16_t* A[2] = {w.H, w.H_lo};
     const uint16_t* B[2] = {Wd, Wd};
     TW_TRY(tw::gemm_rows_times_nmajor_splitk(A, B, 2, ra, o.n_ovf, ovf_cap, I, d, w.acc, dev_status, s));
-    TW_TRY(tw::launch_scatter_rows_bf16(w.acc, d, o.n_ovf, ovf_cap, o.ovf_rows, y, d, s));
+    TW_TRY(tw::launch_scatter_rows_bf16(w.acc, d, o.n_ovf, ovf_cap, o.ovf_rows, y, d, T, s));
   }
   return TW_OK;
 }
@@ -406,14 +407,14 @@ tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* 
   a.sched_zeroed = true;  // by compact_rows above
   TW_TRY(tw::launch_token_fwd(a, s));
   if (cap > 0) {
-    TW_TRY(tw::launch_gather_rows(x, d, saved->backup_tok, saved->n_backup, cap, ra, w.X, s, nullptr, nullptr,
+    TW_TRY(tw::launch_gather_rows(x, d, T, saved->backup_tok, saved->n_backup, cap, ra, w.X, s, dev_status, nullptr,
                                   nullptr, w.acc, d));
     TW_TRY(tw::gemm_backup_hidden(w.X, Wg, Wu, ra, saved->n_backup, cap, d, I, w.H, w.H_lo, saved->backup_a,
                                   gated ? saved->backup_u : nullptr, dev_status, s));
     const uint16_t* A[2] = {w.H, w.H_lo};
     const uint16_t* B[2] = {Wd, Wd};
     TW_TRY(tw::gemm_rows_times_nmajor_splitk(A, B, 2, ra, saved->n_backup, cap, I, d, w.acc, dev_status, s));
-    TW_TRY(tw::launch_scatter_rows_bf16(w.acc, d, saved->n_backup, cap, saved->backup_tok, y, d, s));
+    TW_TRY(tw::launch_scatter_rows_bf16(w.acc, d, saved->n_backup, cap, saved->backup_tok, y, d, T, s));
   }
   return TW_OK;
 }
@@ -461,13 +462,15 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
   a.ell_idx = saved->ell_idx; a.ell_a = saved->ell_a; a.ell_u = saved->ell_u;
   a.dx = dx;
   a.col_cnt = w.col_cnt; a.col_ptr = w.col_ptr; a.col_cur = w.col_cur; a.csc = w.csc;
+  a.csc_cap = static_cast<long long>(T) * R;
+  a.status = dev_status;
   a.dWg = dWg; a.dWu = dWu; a.dWd = dWd;
   a.sched = w.sched;
   a.sched_w = w.sched + tw::kSchedStride;
   TW_TRY(tw::launch_sparse_bwd_tokens(a, s));
   const bool backup = cap > 0 && T > 0;
   if (backup) {
-    TW_TRY(tw::launch_gather_rows(dy, d, saved->backup_tok, saved->n_backup, cap, ra, w.dY, s, nullptr, x, w.X,
+    TW_TRY(tw::launch_gather_rows(dy, d, T, saved->backup_tok, saved->n_backup, cap, ra, w.dY, s, dev_status, x, w.X,
                                   w.acc, d));
     const int32_t* nb = saved->n_backup;
     const tw::BackupGradOut& g = w.g;
@@ -477,7 +480,7 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
     const uint16_t* A[4] = {g.dG, g.dG_lo, g.dU, g.dU_lo};
     const uint16_t* B[4] = {Wg, Wg, Wu, Wu};
     TW_TRY(tw::gemm_rows_times_nmajor_splitk(A, B, gated ? 4 : 2, ra, nb, cap, I, d, w.acc, dev_status, s));
-    TW_TRY(tw::launch_scatter_rows_bf16(w.acc, d, nb, cap, saved->backup_tok, dx, d, s));
+    TW_TRY(tw::launch_scatter_rows_bf16(w.acc, d, nb, cap, saved->backup_tok, dx, d, T, s));
     // the backup rows' weight gradients are written first (when there are any);
     // the ELL part is then added to them
     // all (two or three) in one launch
@@ -488,6 +491,55 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
   }
   a.dW_base_rows = backup ? saved->n_backup : nullptr;
   TW_TRY(tw::launch_sparse_bwd_weights(a, s));
+  return TW_OK;
+}
+
+tw_status twell_unpack(const tw_twell* in, uint16_t* A, void* stream) {
+  if (in == nullptr) return TW_EINVAL;
+  tw_status st = check_tile_geometry(in->T, in->I, in->W, in->C);
+  if (st != TW_OK) return st;
+  st = check_twell(in, in->T, in->I, in->W, in->C);
+  if (st != TW_OK || in->T == 0) return st;
+  st = check_ptrs({A});
+  if (st != TW_OK) return st;
+  TW_TRY(tw::launch_twell_unpack(*in, A, as_stream(stream)));
+  return TW_OK;
+}
+
+size_t hybrid_pack_workspace_size(int T) {
+  if (T < 0) return 0;
+  Carve c(nullptr);
+  c.take<uint8_t>(static_cast<size_t>(T));
+  return c.off + 256;
+}
+
+tw_status hybrid_pack(const uint16_t* A, const uint16_t* U, int T, int I, int W, int C, const tw_hybrid* out, void* ws,
+                      size_t ws_bytes, int32_t* dev_status, void* stream) {
+  tw_status st = check_tile_geometry(T, I, W, C);
+  if (st != TW_OK) return st;
+  const bool gated = U != nullptr;
+  st = check_hybrid(out, T, I, gated);
+  if (st != TW_OK) return st;
+  if (T == 0) return TW_OK;
+  st = check_ptrs({A, dev_status, ws});
+  if (st != TW_OK) return st;
+  if (gated && !aligned16(U)) return TW_EALIGN;
+  if (ws_bytes < hybrid_pack_workspace_size(T)) return TW_EWORKSPACE;
+  Carve c(reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(ws) + 255) & ~static_cast<uintptr_t>(255)));
+  uint8_t* ovf = c.take<uint8_t>(static_cast<size_t>(T));
+  TW_TRY(tw::launch_hybrid_pack(A, U, T, I, W, C, *out, ovf, dev_status, as_stream(stream)));
+  return TW_OK;
+}
+
+tw_status hybrid_unpack(const tw_hybrid* in, float* A, float* U, void* stream) {
+  if (in == nullptr) return TW_EINVAL;
+  if (in->T < 0 || in->I < 64 || in->I > 65536 || in->I % 64 != 0) return TW_EUNSUPPORTED;
+  tw_status st = check_hybrid(in, in->T, in->I, U != nullptr);
+  if (st != TW_OK || in->T == 0) return st;
+  st = check_ptrs({A});
+  if (st != TW_OK) return st;
+  if (U != nullptr && !aligned16(U)) return TW_EALIGN;
+  TW_TRY(tw::launch_hybrid_unpack(*in, A, U, as_stream(stream)));
   return TW_OK;
 }
 
@@ -526,6 +578,31 @@ tw_status tw_fma_probe(float* out, int blocks, int iters, double* flops, void* s
   if (reinterpret_cast<uintptr_t>(out) % 4 != 0) return TW_EALIGN;
   if (flops != nullptr) *flops = static_cast<double>(tw::fma_probe_flops(blocks, iters));
   return from_cuda(tw::launch_fma_probe(out, blocks, iters, as_stream(stream)));
+}
+
+int tw_l2_gather_probe_blocks(int d) {
+  if (d < 256 || d > 2048 || d % 256 != 0) return 0;
+  return tw::l2_gather_probe_blocks(d);
+}
+
+tw_status tw_l2_gather_probe(const uint16_t* table, int rows, int d, const int32_t* idx, int n_idx, float* out,
+                             int blocks, double* bytes, void* stream) {
+  tw_status st = check_model_width(d);
+  if (st != TW_OK) return st;
+  if (rows < 1 || n_idx < 8 || n_idx % 8 != 0 || blocks < 1 || blocks > (1 << 20)) return TW_EINVAL;
+  st = check_ptrs({table, idx, out});
+  if (st != TW_OK) return st;
+  if (bytes != nullptr) *bytes = static_cast<double>(n_idx) * d * 2.0;
+  return from_cuda(tw::launch_l2_gather_probe(table, rows, d, idx, n_idx, out, blocks, as_stream(stream)));
+}
+
+tw_status tw_wait_timeout_probe(const uint16_t* A, const uint16_t* B, int M, int N, int K, int withhold_kb, float* D,
+                                int32_t* dev_status, void* stream) {
+  if (M < 1 || M > 128 || N < 64 || N > 256 || N % 64 != 0 || K < 64 || K % 64 != 0) return TW_EINVAL;
+  if (withhold_kb < 0 || withhold_kb >= K / 64) return TW_EINVAL;
+  tw_status st = check_ptrs({A, B, D, dev_status});
+  if (st != TW_OK) return st;
+  return from_cuda(tw::gemm_dense_test(A, B, M, N, K, 0, 0, D, dev_status, as_stream(stream), withhold_kb));
 }
 
 tw_status tw_dense_gemm(const uint16_t* A, const uint16_t* B, int M, int N, int K, int a_mn, int b_mn, float* D,

@@ -11,6 +11,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdio.h>
 
 #include "../../include/twell.h"
 
@@ -35,6 +36,28 @@ TW_DEV void pdl_enter() {
 TW_DEV void raise_status(int32_t* status, int code) {
   if (status != nullptr) atomicMax(status, code);
 }
+
+// ------------------------------------------------------------------ checked builds
+// A build with -DTW_CHECK compares every index that a kernel computes from data it
+// reads (neuron indices of the formats, token rows of the row gathers and scatters,
+// record slots of the transposed Hybrid, counts that size a loop) with the size of
+// the buffer it addresses. TW_CHECKED(cond, status) is then false when the index
+// does not fit: TW_EBOUNDS is raised in *status (when non-null), the first few
+// violations of each translation unit print their source line, and the caller skips
+// the access. Without TW_CHECK it is the constant true and costs nothing.
+#ifdef TW_CHECK
+static __device__ unsigned int tw_check_prints;
+TW_DEV bool check_bound(bool ok, int32_t* status, const char* file, int line) {
+  if (!ok) {
+    raise_status(status, TW_EBOUNDS);
+    if (atomicAdd(&tw_check_prints, 1u) < 16u) printf("TW_CHECK: index out of bounds at %s:%d\n", file, line);
+  }
+  return ok;
+}
+#define TW_CHECKED(cond, status) (::tw::check_bound((cond), (status), __FILE__, __LINE__))
+#else
+#define TW_CHECKED(cond, status) (true)
+#endif
 
 // ------------------------------------------------------------------ bf16 bits
 TW_DEV float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }

@@ -80,6 +80,7 @@ static GemmShape shape_static(int M, int N, int K, int32_t* status) {
   g.segments = 1;
   g.problems = 1;
   g.status = status;
+  g.withhold_kb = -1;
   return g;
 }
 
@@ -244,8 +245,9 @@ cudaError_t gemm_weight_grads(const WeightGradProblem* probs, int n_probs, int r
 
 // ------------------------------------------------------------------ layout test GEMM
 cudaError_t gemm_dense_test(const uint16_t* A, const uint16_t* B, int M, int N, int K, int a_mn, int b_mn, float* D,
-                            int32_t* status, cudaStream_t s) {
-  const GemmShape sh = shape_static(M, N, K, status);
+                            int32_t* status, cudaStream_t s, int withhold_kb) {
+  GemmShape sh = shape_static(M, N, K, status);
+  sh.withhold_kb = withhold_kb;
   EpiStoreF32::Params ep{D, N};
   GemmMaps maps;
   const bool oka = a_mn ? tmap_mnmajor(&maps.a[0], A, K, M) : tmap_kmajor(&maps.a[0], A, M, K, 128);

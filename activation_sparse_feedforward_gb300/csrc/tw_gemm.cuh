@@ -54,6 +54,9 @@ struct GemmShape {
                      // chosen on the device from the actual tile count so that the
                      // units fill the grid once (grid / tiles slices per tile)
   int32_t* status;
+  int withhold_kb;   // test hook, -1 normally: in a CTA's first work unit, the TMA loads of
+                     // this K block are never issued, so the MMA issuer's bounded wait for
+                     // that stage runs out (TW_ETIMEOUT) and every role drains and returns
 };
 
 constexpr int GEMM_MAX_SEGMENTS = 6;  // segments x problems
@@ -185,6 +188,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, shape.status)) {
             ok = false;
             break;
+          }
+          if (kb == shape.withhold_kb && unit == static_cast<int>(blockIdx.x)) {
+            // test hook: this stage is never filled (its "full" barrier gets no arrival)
+            ++issued;
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
           }
           uint8_t* sA = tiles + stage * Tr::STAGE_BYTES;
           uint8_t* sB = sA + NA * Tr::A_BYTES;
@@ -547,6 +559,7 @@ struct EpiTwellPack {
     const int col0 = n0 + c * 32;
     const int k = col0 / p.W;
     const int local0 = col0 - k * p.W;
+    if (!TW_CHECKED(k < p.nT && m < p.T, nullptr)) return;
     uint32_t w[16];
     uint32_t mask = 0u;
 #pragma unroll

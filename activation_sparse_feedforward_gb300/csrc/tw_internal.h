@@ -32,6 +32,13 @@ cudaError_t launch_zero(void* p0, size_t b0, void* p1, size_t b1, cudaStream_t s
 // out holds blocks * 256 floats
 cudaError_t launch_fma_probe(float* out, int blocks, int iters, cudaStream_t s);
 long fma_probe_flops(int blocks, int iters);
+// L2 row-gather probe (tw_kernels.cu): `blocks` CTAs of d / 8 threads gather the
+// rows idx[0 .. n_idx) of table [rows, d] (n_idx % 8 == 0); out holds blocks * d / 8
+// floats. l2_gather_probe_blocks(d) is the grid the bench uses (the token kernels'
+// residency).
+cudaError_t launch_l2_gather_probe(const uint16_t* table, int rows, int d, const int32_t* idx, int n_idx, float* out,
+                                   int blocks, cudaStream_t s);
+int l2_gather_probe_blocks(int d);
 
 // Every library kernel is launched with programmatic stream serialization: it may
 // start (and run its prologue) while the kernel before it on the stream finishes,
@@ -66,18 +73,29 @@ cudaError_t launch_compact_rows(const uint8_t* ovf, const int32_t* row_nnz, int 
                                 int list_cap, int32_t* count, int32_t* slot_of, int32_t* ell_nnz, int cap_check,
                                 int32_t* status, cudaStream_t s, int32_t* zero_word = nullptr);
 
+// ---------------------------------------------------------------- tw_formats.cu
+// TwELL slots scattered into a dense bf16 [T, I] matrix (zeros elsewhere).
+cudaError_t launch_twell_unpack(const tw_twell& tw, uint16_t* A, cudaStream_t s);
+// Hybrid of a dense bf16 A (and U) with tile width W and capacity C for the overflow
+// test: every field of h; ovf_ws holds T bytes of per-row overflow flags.
+cudaError_t launch_hybrid_pack(const uint16_t* A, const uint16_t* U, int T, int I, int W, int C, const tw_hybrid& h,
+                               uint8_t* ovf_ws, int32_t* status, cudaStream_t s);
+// Dense fp32 A [T, I] (and U when non-null) from a Hybrid.
+cudaError_t launch_hybrid_unpack(const tw_hybrid& h, float* A, float* U, cudaStream_t s);
+
 // ---------------------------------------------------------------- tw_neurons.cu
 cudaError_t launch_neuron_counts(const tw_hybrid& h, int32_t* counts, cudaStream_t s);
 cudaError_t launch_reinit_rows(uint16_t* W, int I, int d, const int32_t* counts, uint64_t seed, float stdv,
                                int32_t* n_reinit, cudaStream_t s);
 
-// out[i] = src[rows[i]] for i < min(*n, cap); rows [n, round_up(n, 128)) (below
+// out[i] = src[rows[i]] for i < min(*n, cap) (src holds src_rows rows, and so does
+// src2); rows [n, round_up(n, 128)) (below
 // rows_alloc) are zero-filled. Row length d bf16. With src2/out2 the same rows of a
 // second matrix are gathered in the same launch; with `zero`, rows [0, min(*n, cap))
 // of that fp32 accumulator (zero_row_f32 floats a row, a multiple of 4) are set to 0
 // for the split-K product that adds into them next.
 // Raises TW_ECAPACITY into `status` (when non-null) if *n > cap.
-cudaError_t launch_gather_rows(const uint16_t* src, int d, const int32_t* rows, const int32_t* n, int cap,
+cudaError_t launch_gather_rows(const uint16_t* src, int d, int src_rows, const int32_t* rows, const int32_t* n, int cap,
                                int rows_alloc, uint16_t* out, cudaStream_t s, int32_t* status = nullptr,
                                const uint16_t* src2 = nullptr, uint16_t* out2 = nullptr, float* zero = nullptr,
                                int zero_row_f32 = 0);
@@ -125,7 +143,9 @@ struct SparseBwdArgs {
   int32_t* col_cnt;   // [I + 1]
   int32_t* col_ptr;   // [I + 1]
   int32_t* col_cur;   // [I]
-  uint4* csc;         // [T * R] column-ordered entry records
+  uint4* csc;         // [csc_cap] column-ordered entry records
+  long long csc_cap;  // T * R
+  int32_t* status;    // device status word (TW_EBOUNDS in bounds-checked builds)
   float *dWg, *dWu, *dWd;
   // when non-null and *dW_base_rows > 0, dW already holds the dense backup rows'
   // part and the ELL part is added to it; otherwise dW is overwritten
@@ -177,7 +197,7 @@ cudaError_t gemm_rows_times_nmajor_splitk(const uint16_t* const* A, const uint16
                                           int rows_alloc, const int32_t* n_dev, int cap, int K, int N, float* acc,
                                           int32_t* status, cudaStream_t s);
 cudaError_t launch_scatter_rows_bf16(const float* acc, int N, const int32_t* n_dev, int cap, const int32_t* row_map,
-                                     uint16_t* out, int ldo, cudaStream_t s);
+                                     uint16_t* out, int ldo, int out_rows, cudaStream_t s);
 
 // dense backup backward part 1: dh = dY Wd^T and the epilogue producing dG, dU and H,
 // each as a (hi, lo) bf16 pair [rows_alloc, I].
@@ -200,7 +220,8 @@ struct WeightGradProblem {
 cudaError_t gemm_weight_grads(const WeightGradProblem* probs, int n_probs, int rows_alloc, const int32_t* n_dev,
                               int cap, int I, int d, int32_t* status, cudaStream_t s);
 
+// withhold_kb >= 0: the test hook of GemmShape::withhold_kb (a bounded wait runs out)
 cudaError_t gemm_dense_test(const uint16_t* A, const uint16_t* B, int M, int N, int K, int a_mn, int b_mn, float* D,
-                            int32_t* status, cudaStream_t s);
+                            int32_t* status, cudaStream_t s, int withhold_kb = -1);
 
 }  // namespace tw

@@ -125,6 +125,57 @@ long fma_probe_flops(int blocks, int iters) {
   return static_cast<long>(blocks) * 256L * iters * kProbeChains * 2L * 2L;  // 2 lanes, 2 FLOP per FMA
 }
 
+// ---------------------------------------------------------------- L2 gather probe
+// Row-slice gather rate from an L2-resident table, the access pattern of the sparse
+// kernels: a CTA of d / 256 warps takes groups of eight row indices; warp c loads the
+// 512-byte slice c of each of the eight rows (16 bytes a lane, all eight loads in
+// flight together) and accumulates them with packed fp32 FMAs. Six CTAs per SM at
+// d = 2048 (48 warps), like the token kernels. Each thread writes its sum.
+__global__ void __launch_bounds__(256) l2_gather_probe_kernel(const uint16_t* __restrict__ table, int rows, int d,
+                                                             const int32_t* __restrict__ idx, int n_groups,
+                                                             float* __restrict__ out) {
+  pdl_enter();
+  const int lane = threadIdx.x & 31, c = threadIdx.x >> 5;
+  const uint32_t row16 = static_cast<uint32_t>(d / 8);
+  const uint4* base = reinterpret_cast<const uint4*>(table) + c * 32 + lane;
+  f32x2 acc[4] = {0ull, 0ull, 0ull, 0ull};
+  const f32x2 one = pair(1.f, 1.f);
+  for (int g = blockIdx.x; g < n_groups; g += gridDim.x) {
+    const int4 i0 = reinterpret_cast<const int4*>(idx)[2 * g];
+    const int4 i1 = reinterpret_cast<const int4*>(idx)[2 * g + 1];
+    const int r[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
+    uint4 v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const uint32_t rr = static_cast<uint32_t>(min(max(r[q], 0), rows - 1));
+      v[q] = __ldg(base + rr * row16);
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      fma2(acc[0], one, widen(v[q].x));
+      fma2(acc[1], one, widen(v[q].y));
+      fma2(acc[2], one, widen(v[q].z));
+      fma2(acc[3], one, widen(v[q].w));
+    }
+  }
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 p = unpair(acc[i]);
+    sum += p.x + p.y;
+  }
+  out[static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x] = sum;
+}
+
+cudaError_t launch_l2_gather_probe(const uint16_t* table, int rows, int d, const int32_t* idx, int n_idx, float* out,
+                                   int blocks, cudaStream_t s) {
+  cudaError_t e = launch(l2_gather_probe_kernel, dim3(blocks), dim3(d / 8), 0, s, table, rows, d, idx, n_idx / 8, out);
+  trace_mark(s, "l2_gather_probe");
+  return e;
+}
+
+int l2_gather_probe_blocks(int d) { return device_sm_count() * std::max(1, std::min(32, 48 / (d / 256))); }
+
 static int warp_grid(long rows, int warps_per_block) {
   const long blocks = (rows + warps_per_block - 1) / warps_per_block;
   const long cap = static_cast<long>(device_sm_count()) * 32;
@@ -320,6 +371,7 @@ struct GatherArgs {
   const uint16_t* src[2];
   uint16_t* out[2];
   int nsrc, d;
+  int src_rows;  // rows of src (and src2): the bound of rows[i]
   const int32_t* rows;
   const int32_t* n_dev;
   int cap, rows_alloc;
@@ -344,7 +396,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const GatherArgs g) {
     uint4 v[kRowVecs];
 #pragma unroll
     for (int q = 0; q < kRowVecs; ++q) v[q] = make_uint4(0, 0, 0, 0);
-    if (i < n) {
+    if (i < n && TW_CHECKED(g.rows[i] >= 0 && g.rows[i] < g.src_rows, g.status)) {
       const uint4* r =
           reinterpret_cast<const uint4*>((which ? g.src[1] : g.src[0]) + static_cast<size_t>(g.rows[i]) * g.d);
 #pragma unroll
@@ -367,12 +419,13 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const GatherArgs g) {
 __global__ void __launch_bounds__(256) scatter_rows_bf16_kernel(const float* __restrict__ acc, int N,
                                                                 const int32_t* __restrict__ n_dev, int cap,
                                                                 const int32_t* __restrict__ row_map,
-                                                                uint16_t* __restrict__ out, int ldo) {
+                                                                uint16_t* __restrict__ out, int ldo, int out_rows) {
   pdl_enter();
   const int n = min(max(*n_dev, 0), cap);
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
   for (int i = blockIdx.x * wpb + (threadIdx.x >> 5); i < n; i += gridDim.x * wpb) {
+    if (!TW_CHECKED(row_map[i] >= 0 && row_map[i] < out_rows, nullptr)) continue;
     const float4* src = reinterpret_cast<const float4*>(acc + static_cast<size_t>(i) * N);
     uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(row_map[i]) * ldo);
     // all of the lane's (at most kRowVecs) pieces are loaded before any is stored
@@ -396,16 +449,16 @@ __global__ void __launch_bounds__(256) scatter_rows_bf16_kernel(const float* __r
 }
 
 cudaError_t launch_scatter_rows_bf16(const float* acc, int N, const int32_t* n_dev, int cap, const int32_t* row_map,
-                                     uint16_t* out, int ldo, cudaStream_t s) {
+                                     uint16_t* out, int ldo, int out_rows, cudaStream_t s) {
   if (cap <= 0) return cudaSuccess;
   if (N % 8 != 0 || N > 8 * 32 * kRowVecs) return cudaErrorInvalidValue;
   cudaError_t e = launch(scatter_rows_bf16_kernel, dim3(std::min(warp_grid(cap, 8), device_sm_count() * 2)), dim3(256),
-                         0, s, acc, N, n_dev, cap, row_map, out, ldo);
+                         0, s, acc, N, n_dev, cap, row_map, out, ldo, out_rows);
   trace_mark(s, "scatter_rows");
   return e;
 }
 
-cudaError_t launch_gather_rows(const uint16_t* src, int d, const int32_t* rows, const int32_t* n, int cap,
+cudaError_t launch_gather_rows(const uint16_t* src, int d, int src_rows, const int32_t* rows, const int32_t* n, int cap,
                                int rows_alloc, uint16_t* out, cudaStream_t s, int32_t* status, const uint16_t* src2,
                                uint16_t* out2, float* zero, int zero_row_f32) {
   if (rows_alloc <= 0) return cudaSuccess;
@@ -419,6 +472,7 @@ cudaError_t launch_gather_rows(const uint16_t* src, int d, const int32_t* rows, 
   g.out[1] = out2;
   g.nsrc = (src2 != nullptr && out2 != nullptr) ? 2 : 1;
   g.d = d;
+  g.src_rows = src_rows;
   g.rows = rows;
   g.n_dev = n;
   g.cap = cap;

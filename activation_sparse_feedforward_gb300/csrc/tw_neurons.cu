@@ -38,8 +38,12 @@ __global__ void __launch_bounds__(256) neuron_counts_kernel(const int32_t* __res
   const int wpb = blockDim.x >> 5;
   if (static_cast<int>(blockIdx.x) < token_blocks) {
     for (int t = blockIdx.x * wpb + (threadIdx.x >> 5); t < T; t += token_blocks * wpb) {
-      const int n = ell_nnz[t];
-      for (int e = lane; e < n; e += 32) atomicAdd(counts + ell_idx[static_cast<size_t>(t) * R + e], 1);
+      int n = ell_nnz[t];
+      if (!TW_CHECKED(n >= 0 && n <= R, nullptr)) n = 0;
+      for (int e = lane; e < n; e += 32) {
+        const int j = ell_idx[static_cast<size_t>(t) * R + e];
+        if (TW_CHECKED(j < I, nullptr)) atomicAdd(counts + j, 1);
+      }
     }
   } else if (backup_a != nullptr) {
     const int nb = min(max(*n_backup, 0), cap);

@@ -163,7 +163,8 @@ __global__ void __launch_bounds__(1024) csc_count_scan_kernel(const SparseBwdArg
     if (lane < 4 && t0 + lane < a.T) {
       const int t = t0 + lane;
       const int slot = a.backup_slot != nullptr ? a.backup_slot[t] : -1;
-      const int n = a.ell_nnz[t];
+      int n = a.ell_nnz[t];
+      if (!TW_CHECKED(n >= 0 && n <= a.R, a.status)) n = 0;
       len = slot >= 0 ? 0 : n;  // exactly the entries the token pass writes: none of a backup row's
     }
     int n[4], nmax = 0;
@@ -178,7 +179,7 @@ __global__ void __launch_bounds__(1024) csc_count_scan_kernel(const SparseBwdArg
       for (int q = 0; q < 4; ++q) j[q] = k < n[q] ? a.ell_idx[static_cast<size_t>(t0 + q) * a.R + k] : -1;
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        if (j[q] >= 0) atomicAdd(cnt + j[q], 1);
+        if (j[q] >= 0 && TW_CHECKED(j[q] < a.I, a.status)) atomicAdd(cnt + j[q], 1);
     }
   }
   __syncthreads();
@@ -255,13 +256,16 @@ __global__ void __launch_bounds__(256, 4) ell_weight_grad_kernel(const SparseBwd
     const int c = cj / a.I;
     const int j = cj - c * a.I;
     const uint4* src = reinterpret_cast<const uint4*>(xside ? a.x : a.dy) + c * 32 + lane;
-    const int lo = a.col_ptr[j], hi = a.col_ptr[j + 1];
+    int lo = a.col_ptr[j], hi = a.col_ptr[j + 1];
+    if (!TW_CHECKED(lo >= 0 && lo <= hi && hi <= a.csc_cap, a.status)) lo = hi = 0;
+    const uint32_t rows16 = static_cast<uint32_t>(a.T) * static_cast<uint32_t>(a.d / 8);  // bound of a record's row
     F8 p, q2;
     f8_zero(p);
     f8_zero(q2);
     for (int e0 = lo; e0 < hi; e0 += 32) {
       const int m = min(32, hi - e0);
       uint4 r = lane < m ? a.csc[e0 + lane] : make_uint4(0u, 0u, 0u, 0u);
+      if (!TW_CHECKED(r.x < rows16, a.status)) r = make_uint4(0u, 0u, 0u, 0u);
       const uint32_t last = __shfl_sync(0xFFFFFFFFu, r.x, m - 1);
       if (lane >= m) r.x = last;
       __syncwarp();  // the previous chunk's reads of the stage are done

@@ -162,16 +162,22 @@ TW_DEV int block_exclusive_scan(int v, int* scratch, int* total, bool reuse) {
 // slower in the backward, by measurement).
 template <bool VEC>
 TW_DEV void pass_dot(const uint4* Wslice, uint32_t row16, const uint16_t* lj, int w0, int m, const uint4& vec,
-                     float* part, int lane) {
+                     float* part, int lane, int I, int32_t* status) {
   for (int k0 = 0; k0 < m; k0 += kGroup) {
     uint4 v[kGroup];
     if (VEC) {
       const uint4 jv = lds16(lj + w0 + k0);
 #pragma unroll
-      for (int q = 0; q < kGroup; ++q) v[q] = ldg16(Wslice + jsel(jv, q) * row16);
+      for (int q = 0; q < kGroup; ++q) {
+        const uint32_t j = jsel(jv, q);
+        v[q] = TW_CHECKED(j < static_cast<uint32_t>(I), status) ? ldg16(Wslice + j * row16) : make_uint4(0u, 0u, 0u, 0u);
+      }
     } else {
 #pragma unroll
-      for (int q = 0; q < kGroup; ++q) v[q] = ldg16(Wslice + static_cast<uint32_t>(lj[w0 + k0 + q]) * row16);
+      for (int q = 0; q < kGroup; ++q) {
+        const uint32_t j = lj[w0 + k0 + q];
+        v[q] = TW_CHECKED(j < static_cast<uint32_t>(I), status) ? ldg16(Wslice + j * row16) : make_uint4(0u, 0u, 0u, 0u);
+      }
     }
     float p[kGroup];
 #pragma unroll
@@ -244,10 +250,11 @@ __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_fwd_kernel(c
       const int off = n + block_exclusive_scan(cnt, scratch, &tot, kb + static_cast<int>(blockDim.x) < a.nT);
       auto put = [&](int i, int jj, uint16_t ab) {
         const int j = k * a.W + jj;
+        if (!TW_CHECKED(off + i < a.L && jj < a.W, a.status)) return;
         const float av = bf16_to_f32(ab);
         lj[off + i] = static_cast<uint16_t>(j);
         lh[off + i] = pair(av, av);
-        if (HYBRID) {
+        if (HYBRID && TW_CHECKED(off + i < a.R, a.status)) {
           a.ell_idx[rb + off + i] = static_cast<uint16_t>(j);
           a.ell_a[rb + off + i] = ab;
         }
@@ -281,7 +288,7 @@ __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_fwd_kernel(c
       const int m = min(kWin, n - w0);
       if (GATED) {
         // -------------------------------------------------------- up: h = a (x_t . Wu[j])
-        pass_dot<true>(Wu4, row16, lj, w0, m, xs, part + c * kWin, lane);
+        pass_dot<true>(Wu4, row16, lj, w0, m, xs, part + c * kWin, lane, a.I, a.status);
         __syncthreads();
         for (int k = threadIdx.x; k < m; k += blockDim.x) {
           float u = 0.f;
@@ -289,7 +296,7 @@ __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_fwd_kernel(c
           for (int w = 0; w < NCH; ++w) u += part[w * kWin + k];
           const float h = unpair(lh[w0 + k]).x * u;
           lh[w0 + k] = pair(h, h);
-          if (HYBRID) a.ell_u[rb + w0 + k] = f32_to_bf16(u);
+          if (HYBRID && TW_CHECKED(w0 + k < a.R, a.status)) a.ell_u[rb + w0 + k] = f32_to_bf16(u);
         }
         __syncthreads();
       }
@@ -298,7 +305,10 @@ __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_fwd_kernel(c
         const uint4 jv = lds16(lj + w0 + k0);
         uint4 v[kGroup];
 #pragma unroll
-        for (int q = 0; q < kGroup; ++q) v[q] = ldg16(Wd4 + jsel(jv, q) * row16);
+        for (int q = 0; q < kGroup; ++q) {
+          const uint32_t j = jsel(jv, q);
+          v[q] = TW_CHECKED(j < static_cast<uint32_t>(a.I), a.status) ? ldg16(Wd4 + j * row16) : make_uint4(0u, 0u, 0u, 0u);
+        }
 #pragma unroll
         for (int q = 0; q < kGroup; q += 2) {
           const uint4 hv = lds16(lh + w0 + k0 + q);
@@ -409,10 +419,11 @@ __global__ void __launch_bounds__((NCH + 1) * 32, ws_ctas_per_sm(NCH))
           const int off = n + incl - cnt;
           auto put = [&](int i, int jj, uint16_t ab) {
             const int j = kt * a.W + jj;
+            if (!TW_CHECKED(off + i < a.L && jj < a.W, status)) return;
             const float av = bf16_to_f32(ab);
             lj[off + i] = static_cast<uint16_t>(j);
             lh[off + i] = pair(av, av);
-            if (HYBRID) {
+            if (HYBRID && TW_CHECKED(off + i < a.R, status)) {
               a.ell_idx[rb + off + i] = static_cast<uint16_t>(j);
               a.ell_a[rb + off + i] = ab;
             }
@@ -471,7 +482,7 @@ __global__ void __launch_bounds__((NCH + 1) * 32, ws_ctas_per_sm(NCH))
     for (int w0 = 0; w0 < n; w0 += kWin) {
       const int m = min(kWin, n - w0);
       if (GATED) {
-        pass_dot<true>(Wu4, row16, lj, w0, m, xs, part + c * kWin, lane);
+        pass_dot<true>(Wu4, row16, lj, w0, m, xs, part + c * kWin, lane, a.I, status);
         consumers_sync(kConsumers);
         for (int kk = threadIdx.x; kk < m; kk += kConsumers) {
           float u = 0.f;
@@ -479,14 +490,17 @@ __global__ void __launch_bounds__((NCH + 1) * 32, ws_ctas_per_sm(NCH))
           for (int w = 0; w < NCH; ++w) u += part[w * kWin + kk];
           const float h = unpair(lh[w0 + kk]).x * u;
           lh[w0 + kk] = pair(h, h);
-          if (HYBRID) a.ell_u[rb + w0 + kk] = f32_to_bf16(u);
+          if (HYBRID && TW_CHECKED(w0 + kk < a.R, status)) a.ell_u[rb + w0 + kk] = f32_to_bf16(u);
         }
         consumers_sync(kConsumers);
       }
       for (int k0 = 0; k0 < m; k0 += kGroup) {
         uint4 v[kGroup];
 #pragma unroll
-        for (int q = 0; q < kGroup; ++q) v[q] = ldg16(Wd4 + static_cast<uint32_t>(lj[w0 + k0 + q]) * row16);
+        for (int q = 0; q < kGroup; ++q) {
+          const uint32_t j = lj[w0 + k0 + q];
+          v[q] = TW_CHECKED(j < static_cast<uint32_t>(a.I), status) ? ldg16(Wd4 + j * row16) : make_uint4(0u, 0u, 0u, 0u);
+        }
 #pragma unroll
         for (int q = 0; q < kGroup; ++q) y.axpy(lh[w0 + k0 + q], v[q]);
       }
@@ -526,7 +540,8 @@ __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_bwd_kernel(c
       t = next_tok[nb];
       continue;
     }
-    const int n = a.ell_nnz[t];
+    int n = a.ell_nnz[t];
+    if (!TW_CHECKED(n >= 0 && n <= a.R, a.status)) n = 0;
     const size_t rb = static_cast<size_t>(t) * a.R;
     const uint4 dys = n > 0 ? ldg16(reinterpret_cast<const uint4*>(a.dy) + static_cast<size_t>(t) * row16 + c * 32 + lane)
                             : make_uint4(0u, 0u, 0u, 0u);
@@ -548,7 +563,8 @@ __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_bwd_kernel(c
         const int k = threadIdx.x + i * static_cast<int>(blockDim.x);
         if (k >= rup(m, kGroup)) break;
         const int e = min(k, m - 1);
-        const int j = a.ell_idx[rb + w0 + e];
+        int j = a.ell_idx[rb + w0 + e];
+        if (!TW_CHECKED(j < a.I, a.status)) j = 0;
         lj[k] = static_cast<uint16_t>(j);
         if (k < m) {
           if (i == 0) slot0 = atomicAdd(a.col_cur + j, 1);
@@ -561,7 +577,7 @@ __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_bwd_kernel(c
       }
       __syncthreads();
       // ---------------------------------------------------------- dh = dy_t . Wd[j]
-      pass_dot<false>(Wd4, row16, lj, 0, m, dys, part + c * kWin, lane);
+      pass_dot<false>(Wd4, row16, lj, 0, m, dys, part + c * kWin, lane, a.I, a.status);
       __syncthreads();
 #pragma unroll
       for (int i = 0; i < kPerThread; ++i) {
@@ -575,7 +591,8 @@ __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_bwd_kernel(c
         const float du = dh * av;
         // the entry's record {token row offset in 16-byte units, dg, du, h = a u (or a)}
         const int sl = i == 0 ? slot0 : atomicAdd(a.col_cur + lj[k], 1);
-        a.csc[sl] = make_uint4(static_cast<uint32_t>(t) * row16, __float_as_uint(dg),
+        if (TW_CHECKED(sl >= 0 && sl < a.csc_cap, a.status))
+          a.csc[sl] = make_uint4(static_cast<uint32_t>(t) * row16, __float_as_uint(dg),
                                     GATED ? __float_as_uint(du) : 0u, __float_as_uint(GATED ? av * uv : av));
         lg[k] = pair(dg, dg);
         lu[k] = pair(du, du);

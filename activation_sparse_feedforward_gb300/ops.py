@@ -137,6 +137,44 @@ def twell_pack(A: torch.Tensor, W: int, C: int, status: torch.Tensor | None = No
     return out
 
 
+def twell_unpack(tw_in: TwELL) -> torch.Tensor:
+    """Dense bf16 [T, I] matrix of the stored TwELL slots (zeros elsewhere)."""
+    A = torch.empty((max(tw_in.T, 1), tw_in.I), dtype=BF16, device=tw_in.cnt.device)
+    s = tw_in.struct()
+    _lib.check(_lib.load().twell_unpack(s, _ptr(A), _stream()), "twell_unpack")
+    return A[:tw_in.T]
+
+
+def hybrid_pack(A: torch.Tensor, U: torch.Tensor | None, W: int, C: int, R: int, backup_cap: int,
+                status: torch.Tensor | None = None) -> "Hybrid":
+    """Hybrid of a dense bf16 A [T, I] (and U, gated form) with ELL row capacity R,
+    TwELL tile width W and capacity C for the overflow rule, and room for backup_cap
+    backup rows."""
+    _check_bf16("A", A)
+    T, I = A.shape
+    if U is not None:
+        _check_bf16("U", U, (T, I))
+    out = Hybrid.empty(T, I, R, backup_cap, U is not None, A.device)
+    st = status if status is not None else new_status(A.device)
+    L = _lib.load()
+    ws = _workspace(L.hybrid_pack_workspace_size(T), A.device)
+    s = out.struct()
+    _lib.check(L.hybrid_pack(_ptr(A), _ptr(U), T, I, W, C, s, _ptr(ws), ws.numel(), _ptr(st), _stream()),
+               "hybrid_pack")
+    return out
+
+
+def hybrid_unpack(h: "Hybrid", with_u: bool | None = None) -> tuple[torch.Tensor, torch.Tensor | None]:
+    """Dense fp32 A (and U when the Hybrid is gated, or with_u) [T, I] from a Hybrid."""
+    want_u = (h.ell_u is not None) if with_u is None else with_u
+    dev = h.row_nnz.device
+    A = torch.empty((max(h.T, 1), h.I), dtype=torch.float32, device=dev)
+    U = torch.empty((max(h.T, 1), h.I), dtype=torch.float32, device=dev) if want_u else None
+    s = h.struct()
+    _lib.check(_lib.load().hybrid_unpack(s, _ptr(A), _ptr(U), _stream()), "hybrid_unpack")
+    return A[:h.T], (U[:h.T] if U is not None else None)
+
+
 def twell_gate_pack(x: torch.Tensor, Wg: torch.Tensor, W: int, C: int, want_dense: bool = False,
                     status: torch.Tensor | None = None, out: TwELL | None = None):
     """a = bf16(ReLU(x Wg^T)) packed into TwELL by the fused tensor-core kernel.
@@ -312,3 +350,19 @@ def fma_probe(out: torch.Tensor, blocks: int, iters: int) -> float:
     _lib.check(_lib.load().tw_fma_probe(_ptr(out), int(blocks), int(iters), ctypes.byref(flops), _stream()),
                "tw_fma_probe")
     return flops.value
+
+
+def l2_gather_probe(table: torch.Tensor, idx: torch.Tensor, out: torch.Tensor | None = None,
+                    blocks: int | None = None) -> tuple[torch.Tensor, float]:
+    """Launch the L2 row-gather probe (see tw_l2_gather_probe) on the current stream
+    over table [rows, d] bf16 and idx [n] int32; returns (out, bytes gathered)."""
+    _check_bf16("table", table)
+    rows, d = table.shape
+    L = _lib.load()
+    nb = blocks if blocks is not None else L.tw_l2_gather_probe_blocks(d)
+    if out is None:
+        out = torch.empty(nb * d // 8, dtype=torch.float32, device=table.device)
+    b = ctypes.c_double(0.0)
+    _lib.check(L.tw_l2_gather_probe(_ptr(table), rows, d, _ptr(idx), idx.numel(), _ptr(out), nb, ctypes.byref(b),
+                                    _stream()), "tw_l2_gather_probe")
+    return out, b.value

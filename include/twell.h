@@ -64,7 +64,10 @@ typedef enum {
   TW_ECAPACITY = 4,     /* device: more overflow/backup rows than the buffers hold */
   TW_ETIMEOUT = 5,      /* device: a bounded pipeline wait gave up */
   TW_ECUDA = 6,         /* a CUDA runtime call or launch failed */
-  TW_EWORKSPACE = 7     /* workspace smaller than *_workspace_size() */
+  TW_EWORKSPACE = 7,    /* workspace smaller than *_workspace_size() */
+  TW_EBOUNDS = 8        /* device, bounds-checked builds only (-DTW_CHECK): an index
+                           computed from the inputs or workspaces did not fit its
+                           buffer; the access was skipped */
 } tw_status;
 
 /* TwELL (tile-wise ELLPACK) of a [T, I] activation matrix with tile width W and
@@ -130,6 +133,43 @@ int tw_abi_version(void);
  * Defines the format of explainer 2.A; used standalone and as a test hook. */
 tw_status twell_pack(const uint16_t* A, int T, int I, int W, int C,
                      const tw_twell* out, int32_t* dev_status, void* stream);
+
+/* TwELL unpack (explainer 2.A "New Sparse Data Format: TwELL"; wispaper blog,
+ * "1. TwELL: Tile-wise ELLPACK"): A [in->T, in->I] bf16 (device, caller-owned) is
+ * overwritten with zeros and every stored slot s < min(cnt, C) of tile k of row t is
+ * written at column k W + idx. On a row without overflow this gives back exactly the
+ * packed row; on an overflow row only its first C nonzeros of each tile. Slot indices
+ * >= W are skipped. Reads cnt, val and idx only. Enqueued on `stream`. */
+tw_status twell_unpack(const tw_twell* in, uint16_t* A, void* stream);
+
+/* Workspace bytes hybrid_pack needs (one byte a row). */
+size_t hybrid_pack_workspace_size(int T);
+
+/* Hybrid pack of a given dense bf16 activation matrix A [T, I] and, in the gated
+ * form, the up-projection U [T, I] (NULL: non-gated, ell_u / backup_u unused)
+ * (explainer 2.A "Hybrid Format for Training"; wispaper blog, "2. The Hybrid
+ * Training Algorithm"). Fills every field of *out exactly as the training forward
+ * does from its own a and u: row_nnz = nonzeros of row t (bf16 magnitude bits
+ * nonzero); the row goes to the dense backup when some W-column tile of it holds
+ * more than C nonzeros (its TwELL overflows) or row_nnz > out->R; backup slots are
+ * given by ascending row (backup_tok, backup_slot, n_backup; more than
+ * out->backup_cap backup rows raise TW_ECAPACITY in *dev_status, the extra rows get
+ * slot -2 and are not stored); ELL rows store their nonzeros in ascending column
+ * order (ell_idx, ell_a, ell_u; ell_nnz = row_nnz, 0 for backup rows); backup rows
+ * store the full rows of A and U widened exactly to fp32. Shapes as twell_pack; ws
+ * holds hybrid_pack_workspace_size(T) bytes. Enqueued on `stream`. */
+tw_status hybrid_pack(const uint16_t* A, const uint16_t* U, int T, int I, int W, int C,
+                      const tw_hybrid* out, void* ws, size_t ws_bytes, int32_t* dev_status,
+                      void* stream);
+
+/* Hybrid unpack (explainer 2.A "Hybrid Format for Training"): dense fp32 A [T, I]
+ * and, when U != NULL (gated Hybrid), U [T, I] (device, caller-owned). A row with a
+ * backup slot is its backup row; an ELL row is zeros with its ell_nnz entries written
+ * at their columns (bf16 widened exactly); a row past the backup capacity (slot -2)
+ * is zeros. Unpacking a hybrid_pack result gives A back on every row and U on the
+ * support of ELL rows and on all of backup rows. I % 64 == 0, 64 <= I <= 65536.
+ * Enqueued on `stream`. */
+tw_status hybrid_unpack(const tw_hybrid* in, float* A, float* U, void* stream);
 
 /* Gate projection with the TwELL pack fused into its epilogue (explainer 2.B
  * "Inference Kernels", "Gate Projection"): a = bf16(ReLU(x Wg^T)) with fp32
@@ -260,6 +300,35 @@ tw_status tw_reinit_dead_rows(uint16_t* W, int I, int d, const int32_t* counts, 
  * and M % 64 == 0 when a_mn == 1. */
 tw_status tw_dense_gemm(const uint16_t* A, const uint16_t* B, int M, int N, int K,
                         int a_mn, int b_mn, float* D, int32_t* dev_status, void* stream);
+
+/* L2 row-gather throughput probe for measurement tools (no counterpart on the pages):
+ * the access pattern of the sparse kernels, with nothing else. `blocks` CTAs of d / 8
+ * threads (one warp per 256-wide slice of d) take groups of eight indices from idx
+ * [n_idx] (int32, device; values clamped to [0, rows)) and gather the eight rows'
+ * slices of table [rows, d] bf16 (device) into registers, 16 bytes a lane, all eight
+ * loads in flight together, summing them with packed fp32 FMAs; out [blocks * d / 8]
+ * fp32 (device) receives each thread's sum. *bytes (host, may be NULL) = the row
+ * bytes gathered (n_idx * d * 2); bytes / device time = the gather rate, from L2 when
+ * the table fits in it. d as the FFN calls; n_idx a positive multiple of 8;
+ * 1 <= blocks <= 2^20. Enqueued on `stream`. */
+tw_status tw_l2_gather_probe(const uint16_t* table, int rows, int d, const int32_t* idx, int n_idx, float* out,
+                             int blocks, double* bytes, void* stream);
+
+/* The grid tw_l2_gather_probe is measured with: as many CTAs as the token kernels keep
+ * resident (48 warps per SM at d = 2048) on every SM of the current device; 0 when d
+ * is unsupported. */
+int tw_l2_gather_probe_blocks(int d);
+
+/* Test hook for the bounded waits (no counterpart on the pages): the GEMM of
+ * tw_dense_gemm (a_mn = b_mn = 0; M <= 128, one 128-row tile; N in 64..256, a multiple
+ * of 64; K a multiple of 64) with the TMA loads of K block `withhold_kb` (0 <=
+ * withhold_kb < K / 64) never issued. The MMA issuer's wait for that pipeline stage
+ * therefore runs out after the library's wait limit (1 s): the kernel raises
+ * TW_ETIMEOUT in *dev_status, every role drains the copies and MMAs it issued, TMEM
+ * is freed, and the kernel returns, leaving the context usable. D [M, N] fp32 is
+ * left unspecified. Nothing faults, traps or spins without a limit. */
+tw_status tw_wait_timeout_probe(const uint16_t* A, const uint16_t* B, int M, int N, int K, int withhold_kb,
+                                float* D, int32_t* dev_status, void* stream);
 
 /* CUDA-core fp32 throughput probe for measurement tools (no counterpart on the
  * pages): `blocks` CTAs of 256 threads each run 8 independent chains of `iters`

@@ -43,7 +43,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_abi_version_and_status_strings(lib):
     assert lib.tw_abi_version() == 1
-    for code in range(8):
+    for code in range(9):
         assert lib.tw_status_str(code).decode().startswith("TW_")
 
 

@@ -57,3 +57,24 @@ def test_fma_probe_rejects_bad_arguments():
         tw.fma_probe(out, 2, 1)          # out too small for 2 blocks
     with pytest.raises(tw.TwellError):
         tw.fma_probe(out, 1, 0)          # iters < 1
+
+
+def test_l2_gather_probe_sums_the_gathered_rows():
+    """Each thread's output is the sum of the eight bf16 columns it owns over every
+    row index its CTA took, so the bytes it reports were gathered."""
+    rng = np.random.default_rng(9)
+    rows, d, n_idx, blocks = 300, 512, 8 * 37, 5
+    tab = rng.integers(-8, 8, size=(rows, d)).astype(np.float32)   # small integers: every sum is exact
+    bits = (tab.view(np.uint32) >> 16).astype(np.uint16)
+    table = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    idx_np = rng.integers(0, rows, size=n_idx).astype(np.int32)
+    idx = torch.from_numpy(idx_np).cuda()
+    out, nbytes = tw.l2_gather_probe(table, idx, blocks=blocks)
+    torch.cuda.synchronize()
+    assert nbytes == n_idx * d * 2
+    exp = np.zeros((blocks, d // 8), dtype=np.float64)
+    for g in range(n_idx // 8):
+        b = g % blocks
+        for r in idx_np[8 * g:8 * g + 8]:
+            exp[b] += tab[r].reshape(d // 8, 8).sum(axis=1)
+    np.testing.assert_array_equal(out.cpu().numpy().reshape(blocks, d // 8), exp.astype(np.float32))
