@@ -9,13 +9,15 @@ pages' 1.5B-model FFN shape (see synthetic/workloads.py for the recipe).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--tokens T] [--no-cpu-baseline]
-                    [--no-dense] [--no-inference] [--no-stack] [--sweep]
+                    [--no-dense] [--no-inference] [--no-stack] [--no-sweep] [--clock-soak S]
 
 Prints ONE JSON line (rank 0). Timing: W untimed warm-up steps, then K steps each
 bracketed by CUDA events on the launching stream with a 256 MiB L2 flush between
 steps (outside the events); barrier + synchronize around the timed region and the
-max over ranks. Per-kernel durations come from events the library records after
-each of its launches during the timed steps (tw_trace_begin).
+max over ranks. The same K-step region is then repeated until the clock sampler has
+seen a few seconds of it (the `clocks` record and `repeats`); `value` is the first
+one. Per-kernel durations come from events the library records after each of its
+launches during further timed steps (tw_trace_begin).
 """
 from __future__ import annotations
 
@@ -185,10 +187,11 @@ def kernel_work(label: str, spec, stats: dict) -> tuple[str, float] | None:
     return None
 
 
-# L2 bandwidth the row gathers can reach: ncu reports lts__throughput at 47-54 % while
-# the token kernels move 11.5-13.1 TB/s of L2 sectors, i.e. 100 % = 24.2 TB/s (both
-# kernels agree to 0.3 %); see profiles/token_kernels_train_d2048_i5632_m29_o1.md.
-L2_GATHER_PEAK_GBS = 24200.0
+# L2 figure derived from ncu: lts__throughput read 47-54 % while the token kernels
+# moved 11.5-13.1 TB/s of L2 sectors, i.e. 100 % = 24.2 TB/s (see
+# profiles/token_kernels_train_d2048_i5632_m29_o1.md). Reported beside the gather
+# rate the library's probe measures in the same run, which is the denominator.
+L2_NCU_DERIVED_GBS = 24200.0
 
 
 def measured_traffic(label: str, workload: str) -> float | None:
@@ -244,6 +247,74 @@ def oracle_sample_time(spec, inp, n_tokens: int) -> tuple[float, int, str]:
     dt = time.perf_counter() - t0
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     return dt, cores, f"first {n_tokens} tokens of {spec.name}, full weights, fp64 numpy (BLAS threads: all cores)"
+
+
+# ------------------------------------------------------------------ step roofline
+def step_roofline(spec, stats: dict, ms_per_step: float, peaks: dict) -> dict:
+    """The whole training step's roofline: the slower of (gate + dense backup + sparse
+    FLOPs at the sustained bf16 peak) and (algorithmic bytes at HBM peak), from the
+    step's measured ELL entries and backup rows."""
+    T, d, I = spec.T, spec.d, spec.I
+    nw = 3 if spec.gated else 2
+    F = (2.0 * T * d * I + (14.0 if spec.gated else 10.0) * d * I * stats["n_backup"]
+         + (16.0 if spec.gated else 10.0) * d * stats["nnz_ell"])
+    B = (3 * T * d * 2 + 2 * T * d * 2 + 2 * nw * I * d * 2 + nw * I * d * 4 + stats["nnz_ell"] * (6 + 6 + 8 + 4))
+    t_roof = max(F / (peaks["bf16_tflops_sustained"] * 1e12), B / (peaks["hbm_gbs"] * 1e9))
+    return {"tokens_per_ms": T / (t_roof * 1e3), "frac": (T / ms_per_step) / (T / (t_roof * 1e3)), "flops": F,
+            "bytes": B}
+
+
+def dense_train_step(x, Wg, Wu, Wd, dy, l1):
+    """The dense bf16 FFN (torch / cuBLAS) forward + backward with the same L1 term,
+    as a closure over fresh leaf copies of the inputs."""
+    import torch
+
+    ws = [w.detach().clone().requires_grad_(True) for w in (Wg, Wu, Wd) if w is not None]
+    Wg_, Wd_ = ws[0], ws[-1]
+    Wu_ = ws[1] if Wu is not None else None
+    x_ = x.detach().clone().requires_grad_(True)
+
+    def step():
+        a = torch.relu(x_ @ Wg_.T)
+        h = a * (x_ @ Wu_.T) if Wu_ is not None else a
+        torch.autograd.backward([h @ Wd_, a], [dy, torch.full_like(a, l1)])
+        x_.grad = None
+        for w in ws:
+            w.grad = None
+
+    return step
+
+
+def measure_l2_gather(dev, stream, d: int = 2048, table_rows: int = 3 * 5632, n_idx: int = 1 << 22) -> dict:
+    """Row-slice gather rate of this GPU from an L2-resident table the size of the three
+    gated weight matrices at d 2048, I 5632 (66 MiB), with the access pattern and
+    residency of the token kernels (tw_l2_gather_probe): the median of 5 timed
+    launches after two untimed ones."""
+    import torch
+
+    import activation_sparse_feedforward_gb300 as tw
+
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    table = torch.randn((table_rows, d), generator=g, device=dev).to(torch.bfloat16)
+    idx = torch.randint(0, table_rows, (n_idx,), generator=g, device=dev, dtype=torch.int32)
+    out, nbytes = tw.l2_gather_probe(table, idx)
+    for _ in range(2):
+        tw.l2_gather_probe(table, idx, out=out)
+    ts = []
+    for _ in range(5):
+        s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_.record(stream)
+        tw.l2_gather_probe(table, idx, out=out)
+        e_.record(stream)
+        torch.cuda.synchronize(dev)
+        ts.append(s_.elapsed_time(e_))
+    ms = statistics.median(ts)
+    if not bool(torch.isfinite(out).all()):
+        raise RuntimeError("l2 gather probe produced non-finite values")
+    return {"gbs": nbytes / (ms * 1e-3) / 1e9, "ms": ms, "bytes": nbytes, "table_mib": table_rows * d * 2 / 2**20,
+            "row_slice_bytes": 512, "loads_in_flight_per_warp": 8,
+            "ncu_derived_gbs": L2_NCU_DERIVED_GBS}
 
 
 # ------------------------------------------------------------------ secondary measurements
@@ -344,34 +415,47 @@ def measure_inference(dev, flush, stream, steps: int) -> dict:
     return out
 
 
-def measure_sweep(dev, flush, stream, steps: int) -> list:
-    """The training step over the sparsity sweep (mean actives x outlier fraction)."""
+def measure_sweep(dev, flush, stream, steps: int, peaks: dict) -> list:
+    """The training step over the sparsity sweep (mean actives x outlier fraction) and
+    the non-gated training step, each next to the dense bf16 step on the same inputs,
+    with its ELL / backup split and step roofline fraction."""
     import numpy as np
     import torch
 
     import activation_sparse_feedforward_gb300 as tw
     from synthetic import WORKLOADS, make_inputs
 
+    names = [f"train_d2048_i5632_m{m}_o{o}" for m in (29, 108, 911) for o in (0, 1, 5)]
+    names.append("train_nongated_d2048_i8192_m40_o1")
     rows = []
-    for m in (29, 108, 911):
-        for o in (0, 1, 5):
-            spec = WORKLOADS[f"train_d2048_i5632_m{m}_o{o}"]
-            inp = make_inputs(spec, with_dy=True)
-            x, Wg, Wu, Wd, dy = (torch.from_numpy(inp[k].view(np.int16)).view(torch.bfloat16).to(dev)
-                                 for k in ("x", "Wg", "Wu", "Wd", "dy"))
-            h = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, spec.T, gated=True, device=dev)
+    for name in names:
+        spec = WORKLOADS[name]
+        inp = make_inputs(spec, with_dy=True)
+        x, Wg, Wu, Wd, dy = (None if inp[k] is None else torch.from_numpy(inp[k].view(np.int16)).view(torch.bfloat16).to(dev)
+                             for k in ("x", "Wg", "Wu", "Wd", "dy"))
+        h = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, spec.T, gated=spec.gated, device=dev)
 
-            def step():
-                h.forward(x, Wg, Wu, Wd)
-                h.backward(dy, x, Wg, Wu, Wd, spec.l1)
+        def step():
+            h.forward(x, Wg, Wu, Wd)
+            h.backward(dy, x, Wg, Wu, Wd, spec.l1)
 
-            ms = _time_steps(step, steps, 3, flush, stream)
-            tw.raise_if_device_error(h.status, spec.name)
-            rows.append({"workload": spec.name, "tokens_per_ms": spec.T / ms, "ms": ms,
-                         "n_backup": int(h.saved.n_backup.item()),
-                         "nnz_per_token": float(h.saved.row_nnz.float().mean().item())})
-            del h
-            torch.cuda.empty_cache()
+        ms = _time_steps(step, steps, 3, flush, stream)
+        tw.raise_if_device_error(h.status, spec.name)
+        stats = {"n_backup": int(h.saved.n_backup.item()), "nnz_ell": int(h.saved.ell_nnz.sum().item()),
+                 "nnz": float(h.saved.row_nnz[:spec.T].float().mean().item())}
+        del h
+        torch.cuda.empty_cache()
+        ms_d = _time_steps(dense_train_step(x, Wg, Wu, Wd, dy, spec.l1), steps, 3, flush, stream)
+        roof = step_roofline(spec, stats, ms, peaks)
+        rows.append({"workload": spec.name, "tokens_per_ms": spec.T / ms, "ms": ms,
+                     "dense_bf16_tokens_per_ms": spec.T / ms_d, "vs_dense": ms_d / ms,
+                     "n_backup": stats["n_backup"], "backup_rows_frac": stats["n_backup"] / spec.T,
+                     "nnz_ell": stats["nnz_ell"],
+                     "nnz_per_token": stats["nnz"],
+                     "ell_entries_per_token": stats["nnz_ell"] / spec.T, "C": spec.C, "R": spec.R,
+                     "step_roofline_frac": roof["frac"], "step_roofline_tokens_per_ms": roof["tokens_per_ms"]})
+        del x, Wg, Wu, Wd, dy
+        torch.cuda.empty_cache()
     return rows
 
 
@@ -395,6 +479,11 @@ def measure_stack(dev, flush, stream, steps: int, n_layers: int = 28, T: int = 8
     Ws = [{k: to_dev(v) for k, v in w.items()} for w in st["layers"]]
     x0, dyt = to_dev(st["x0"]), to_dev(st["dy"])
     cap = min(T, 128 * int(math.ceil(1.5 * 0.01 * T / 128.0)) + 128)
+    # memory: the peak allocated above the inputs and weights, through the stack's
+    # buffers (saved Hybrids, workspaces, outputs, dW of every layer) and one step
+    torch.cuda.synchronize(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    mem0 = torch.cuda.memory_allocated(dev)
     ffns = [tw.HybridFFN(T, sp.d, sp.I, sp.W, sp.C, sp.R, cap, gated=True, device=dev) for sp in specs]
     xs = [None] * n_layers
 
@@ -415,6 +504,9 @@ def measure_stack(dev, flush, stream, steps: int, n_layers: int = 28, T: int = 8
         fwd()
         bwd()
 
+    train()
+    torch.cuda.synchronize(dev)
+    peak_ours = torch.cuda.max_memory_allocated(dev) - mem0
     ms_f = _time_steps(fwd, steps, 3, flush, stream)
     ms_t = _time_steps(train, steps, 3, flush, stream)
     for l, f in enumerate(ffns):
@@ -449,6 +541,18 @@ def measure_stack(dev, flush, stream, steps: int, n_layers: int = 28, T: int = 8
             for w in W.values():
                 w.grad = None
 
+    torch.cuda.synchronize(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    mem0 = torch.cuda.memory_allocated(dev)
+    dense_train()
+    torch.cuda.synchronize(dev)
+    peak_dense = torch.cuda.max_memory_allocated(dev) - mem0
+    out["memory"] = {"hybrid_stack_peak_bytes": peak_ours, "dense_stack_peak_bytes": peak_dense,
+                     "ratio": peak_ours / peak_dense,
+                     "what": "torch.cuda.max_memory_allocated during one training step minus the memory held "
+                             "before it (inputs, weights); ours includes every layer's preallocated library "
+                             "buffers (saved Hybrid, workspaces, y, dx, dW), dense its autograd activations "
+                             "and gradients"}
     out["dense_fwd_tokens_per_ms"] = T / _time_steps(dense_fwd_only, steps, 3, flush, stream)
     out["dense_train_tokens_per_ms"] = T / _time_steps(dense_train, steps, 3, flush, stream)
     out["dense_impl"] = "torch bf16 matmul + autograd (cuBLAS)"
@@ -501,26 +605,43 @@ def run_ours(args, dist: Dist) -> dict | None:
     arr = (ctypes.c_void_p * len(tev))(*[e.cuda_event for e in tev])
     L = tw.load()
 
-    # ---- headline: K steps, L2 flushed (untimed) before each, no trace events
+    # ---- headline: K steps, L2 flushed (untimed) before each, no trace events. The
+    # same K-step region is repeated until the clock sampler has watched it for
+    # --clock-soak seconds; `value` is the first region, the others give the spread.
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     clocks = ClockSampler(dist.local_rank)
-    dist.barrier()
-    torch.cuda.synchronize(dev)
+    regions = []
     clocks.start()
-    for i in range(args.steps):
-        flush.zero_()
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-    torch.cuda.synchronize(dev)
-    dist.barrier()
+    t_soak = time.monotonic()
+    while True:
+        dist.barrier()
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        dist.barrier()
+        regions.append([s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)])
+        # every rank takes the same decision (rank 0's clock)
+        done = dist.max(1.0 if time.monotonic() - t_soak >= args.clock_soak else 0.0, dev) > 0
+        if done or len(regions) >= 10000:
+            break
     clk = clocks.stop()
     tw.raise_if_device_error(h.status, "timed steps")
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    step_ms = regions[0]
     total_ms = dist.max(sum(step_ms), dev)
     ms_per_step = total_ms / args.steps
     value = spec.T * dist.world * args.steps / total_ms
+    region_values = [spec.T * args.steps / sum(r) for r in regions]
+    repeats = {"regions": len(regions), "value_median": statistics.median(region_values),
+               "value_min": min(region_values), "value_max": max(region_values),
+               "seconds": time.monotonic() - t_soak}
+    if clk.get("sm_mhz") and clk.get("sm_max_mhz"):
+        # the first region's time scaled to the maximum SM clock (time x median MHz)
+        repeats["ms_per_step_at_max_clock"] = ms_per_step * clk["sm_mhz"] / clk["sm_max_mhz"]
 
     # ---- warm L2: the same K steps back to back
     ws_, we_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -578,35 +699,35 @@ def run_ours(args, dist: Dist) -> dict | None:
                 "frac": achieved / peak,
                 "traffic": measured_traffic(dom, spec.name) if not args.tokens else None,
                 "peak_source": f"{peaks['source']} ({'bf16 sustained' if bound == 'tensor' else 'HBM copy'})"}
+    l2 = measure_l2_gather(dev, stream, d=spec.d, table_rows=(3 if spec.gated else 2) * spec.I)
     for lab, v in kernels.items():
         kw = kernel_work(lab, spec, stats)
         if kw:
             b, w = kw
             v["bound"] = b
             v["achieved"] = (w / (v["avg_us"] * 1e-6)) / (1e12 if b == "tensor" else 1e9)
+            if b == "hbm":
+                v["hbm_frac"] = v["achieved"] / peaks["hbm_gbs"]
         gb = gathered_bytes(lab, spec, stats)
         if gb:
             v["l2_gather_gbs"] = gb / (v["avg_us"] * 1e-6) / 1e9
-            v["l2_gather_frac"] = v["l2_gather_gbs"] / L2_GATHER_PEAK_GBS
+            v["l2_gather_frac"] = v["l2_gather_gbs"] / l2["gbs"]
     gb = gathered_bytes(dom, spec, stats)
     if gb:
-        # what actually bounds a gather kernel: row slices through L2
-        roofline["l2_gather"] = {"achieved": gb / avg_s / 1e9, "peak": L2_GATHER_PEAK_GBS, "unit": "GB/s",
-                                 "frac": gb / avg_s / 1e9 / L2_GATHER_PEAK_GBS, "bytes": gb,
-                                 "peak_source": "derived from ncu lts__throughput (100 % = 24.2 TB/s)"}
+        # what actually bounds a gather kernel: row slices through L2, against the rate
+        # the library's gather probe reaches in this run
+        roofline["l2_gather"] = {"achieved": gb / avg_s / 1e9, "peak": l2["gbs"], "unit": "GB/s",
+                                 "frac": gb / avg_s / 1e9 / l2["gbs"], "bytes": gb,
+                                 "peak_source": "measured: tw_l2_gather_probe in this run",
+                                 "ncu_derived_peak": L2_NCU_DERIVED_GBS}
 
-    # step roofline: slower of (gate + backup + sparse FLOPs at tensor peak) and
-    # (algorithmic bytes at HBM peak)
-    F = 2.0 * spec.T * spec.d * spec.I + 14.0 * spec.d * spec.I * stats["n_backup"] + 16.0 * spec.d * stats["nnz_ell"]
-    B = (3 * spec.T * spec.d * 2 + 2 * spec.T * spec.d * 2 + 2 * 3 * spec.I * spec.d * 2 + 3 * spec.I * spec.d * 4
-         + stats["nnz_ell"] * (6 + 6 + 8 + 4))
-    t_roof = max(F / (peaks["bf16_tflops_sustained"] * 1e12), B / (peaks["hbm_gbs"] * 1e9))
-    step_roof = {"tokens_per_ms": spec.T / (t_roof * 1e3), "frac": (spec.T / ms_per_step) / (spec.T / (t_roof * 1e3)),
-                 "flops": F, "bytes": B}
+    step_roof = step_roofline(spec, stats, ms_per_step, peaks)
+    F = step_roof["flops"]
+    B = step_roof["bytes"]
     # secondary: the sparse FLOPs priced at the measured CUDA-core fp32 FMA rate (they
     # run on CUDA cores), the gate and backup FLOPs at the tensor peak
     fma = measure_fma_peak(dev, stream)
-    F_sparse = 16.0 * spec.d * stats["nnz_ell"]
+    F_sparse = (16.0 if spec.gated else 10.0) * spec.d * stats["nnz_ell"]
     t_roof2 = max((F - F_sparse) / (peaks["bf16_tflops_sustained"] * 1e12) + F_sparse / (fma["tflops"] * 1e12),
                   B / (peaks["hbm_gbs"] * 1e9))
     step_roof["cuda_core_sparse"] = {"tokens_per_ms": spec.T / (t_roof2 * 1e3),
@@ -671,17 +792,7 @@ def run_ours(args, dist: Dist) -> dict | None:
     # dense bf16 FFN (torch/cuBLAS) forward + backward with the same L1 term, same run
     dense = None
     if not args.no_dense:
-        Wg_, Wu_, Wd_ = (w.detach().clone().requires_grad_(True) for w in (Wg, Wu, Wd))
-        x_ = x.detach().clone().requires_grad_(True)
-
-        def dense_step():
-            g = x_ @ Wg_.T
-            a = torch.relu(g)
-            yy = (a * (x_ @ Wu_.T)) @ Wd_
-            loss_like = yy
-            torch.autograd.backward([loss_like, a], [dy, torch.full_like(a, spec.l1)])
-            x_.grad = Wg_.grad = Wu_.grad = Wd_.grad = None
-
+        dense_step = dense_train_step(x, Wg, Wu, Wd, dy, spec.l1)
         for _ in range(2):
             dense_step()
         torch.cuda.synchronize(dev)
@@ -700,7 +811,20 @@ def run_ours(args, dist: Dist) -> dict | None:
     def nbytes(o):
         return sum(t.numel() * t.element_size() for t in vars(o).values() if isinstance(t, torch.Tensor))
     ours_bytes = nbytes(h) + nbytes(h.saved)
-    memory = {"hybrid_saved_bytes": nbytes(h.saved), "layer_bytes": ours_bytes,
+    # the library side as a measured peak: a fresh layer object (its preallocated saved
+    # Hybrid, workspaces, y, dx, dW) and one training step, above what was held before
+    torch.cuda.synchronize(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    m0 = torch.cuda.memory_allocated(dev)
+    h_m = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, backup_cap, gated=spec.gated, device=dev)
+    h_m.forward(x, Wg, Wu, Wd)
+    h_m.backward(dy, x, Wg, Wu, Wd, spec.l1)
+    torch.cuda.synchronize(dev)
+    ours_peak = torch.cuda.max_memory_allocated(dev) - m0
+    tw.raise_if_device_error(h_m.status, "memory step")
+    del h_m
+    torch.cuda.empty_cache()
+    memory = {"hybrid_saved_bytes": nbytes(h.saved), "layer_bytes": ours_bytes, "layer_peak_bytes": ours_peak,
               "dense_saved_bytes_bf16_a_u": 2 * spec.T * spec.I * 2}
     if dense is not None:
         torch.cuda.synchronize(dev)
@@ -710,6 +834,7 @@ def run_ours(args, dist: Dist) -> dict | None:
         torch.cuda.synchronize(dev)
         memory["dense_step_peak_bytes"] = torch.cuda.max_memory_allocated(dev) - m0
         memory["layer_bytes_vs_dense"] = ours_bytes / memory["dense_step_peak_bytes"]
+        memory["layer_peak_vs_dense_peak"] = ours_peak / memory["dense_step_peak_bytes"]
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
@@ -730,6 +855,8 @@ def run_ours(args, dist: Dist) -> dict | None:
         "kernels": {k_: {kk: (round(vv, 4) if isinstance(vv, float) else vv) for kk, vv in v.items()}
                     for k_, v in sorted(kernels.items(), key=lambda kv: -kv[1]["total_ms"])},
         "clocks": clk,
+        "repeats": repeats,
+        "l2_gather_probe": l2,
         "dense_bf16": dense,
         "warm_l2": warm,
         "memory": memory,
@@ -750,8 +877,8 @@ def run_ours(args, dist: Dist) -> dict | None:
                             "min_count": int(counts.min().item()), "max_count": int(counts.max().item())}
     if not args.no_inference:
         line["inference"] = measure_inference(dev, flush, stream, max(3, args.steps // 2))
-    if args.sweep:
-        line["sweep"] = measure_sweep(dev, flush, stream, max(3, args.steps // 4))
+    if not args.no_sweep:
+        line["sweep"] = measure_sweep(dev, flush, stream, max(3, min(10, args.steps // 2)), peaks)
     if not args.no_stack:
         line["stack"] = measure_stack(dev, flush, stream, 3)
     if dist.rank == 0 and not args.no_cpu_baseline:
@@ -799,7 +926,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-inference", action="store_true", help="skip the TwELL inference forward figures")
-    ap.add_argument("--sweep", action="store_true", help="also time the training sparsity sweep")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the training sparsity sweep")
+    ap.add_argument("--clock-soak", type=float, default=4.0,
+                    help="seconds over which the K-step timed region is repeated for the clock record")
     ap.add_argument("--no-stack", action="store_true", help="skip the 28-layer residual stack figures")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the workload's token count (small cases for profiler captures)")

@@ -119,6 +119,10 @@ WORKLOADS: dict[str, FFNSpec] = {
                                         gated=False, mean_active=40, outlier_frac=0.01,
                                         W=128, C=16, R=96, cfg_id=3),
 }
+# Hybrid training step of the non-gated form (shapes and inputs of the non-gated forward)
+WORKLOADS["train_nongated_d2048_i8192_m40_o1"] = FFNSpec(
+    "train_nongated_d2048_i8192_m40_o1", T=16384, d=2048, I=8192, gated=False, mean_active=40, outlier_frac=0.01,
+    W=128, C=16, R=96, l1=2e-5, cfg_id=3)
 # Hybrid training step sweep at the 1.5B gated shape
 for _m in (29, 108, 911):
     for _f in (0.0, 0.01, 0.05):
