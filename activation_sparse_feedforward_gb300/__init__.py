@@ -6,6 +6,7 @@ The computation runs in ``libtwell.so`` (CUDA kernels behind the C ABI of
 from ._lib import TwellError, lib_path, load  # noqa: F401
 from .ops import (  # noqa: F401
     HybridFFN,
+    HybridScratch,
     TwELL,
     Hybrid,
     TwellFFN,

@@ -32,7 +32,12 @@ class TwHybrid(ctypes.Structure):
                 ("backup_cap", ctypes.c_int32),
                 ("row_nnz", c_void_p), ("ell_nnz", c_void_p), ("ell_idx", c_void_p), ("ell_a", c_void_p),
                 ("ell_u", c_void_p), ("backup_slot", c_void_p), ("backup_tok", c_void_p),
-                ("backup_a", c_void_p), ("backup_u", c_void_p), ("n_backup", c_void_p)]
+                ("backup_a", c_void_p), ("backup_u", c_void_p), ("n_backup", c_void_p),
+                ("route", ctypes.c_int32), ("dense_above", ctypes.c_float), ("route_taken", c_void_p)]
+
+
+TW_ROUTE_SPARSE, TW_ROUTE_DENSE, TW_ROUTE_AUTO = 0, 1, 2
+ROUTES = {"sparse": TW_ROUTE_SPARSE, "dense": TW_ROUTE_DENSE, "auto": TW_ROUTE_AUTO}
 
 
 # name -> (restype, argtypes); every symbol declared in include/twell.h
@@ -52,10 +57,10 @@ SIGNATURES = {
                               ctypes.POINTER(TwTwell), c_void_p, c_size_t, c_void_p, c_void_p, c_void_p]),
     "twell_ffn_fwd_fixed_scratch": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
                                             c_int, c_int, ctypes.POINTER(TwTwell), c_void_p, c_void_p, c_void_p]),
-    "hybrid_ffn_fwd_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int, c_int, c_int]),
+    "hybrid_ffn_fwd_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int]),
     "hybrid_ffn_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
                                ctypes.POINTER(TwHybrid), c_void_p, c_size_t, c_void_p, c_void_p, c_void_p]),
-    "hybrid_ffn_bwd_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+    "hybrid_ffn_bwd_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int, c_int]),
     "hybrid_ffn_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
                                ctypes.POINTER(TwHybrid), c_float, c_void_p, c_void_p, c_void_p, c_void_p,
                                c_void_p, c_size_t, c_void_p, c_void_p]),

@@ -11,7 +11,7 @@
 
 namespace {
 
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -79,6 +79,11 @@ tw_status check_ptrs(std::initializer_list<const void*> ptrs) {
 tw_status check_hybrid(const tw_hybrid* h, int T, int I, bool gated) {
   if (h == nullptr) return TW_EINVAL;
   if (h->T != T || h->I != I || h->R < 1 || h->R > I || h->backup_cap < 0 || h->backup_cap > T) return TW_EINVAL;
+  if (h->route < TW_ROUTE_SPARSE || h->route > TW_ROUTE_AUTO) return TW_EINVAL;
+  if (h->route != TW_ROUTE_SPARSE) {
+    if (!(h->dense_above >= 0.f) || h->route_taken == nullptr) return TW_EINVAL;
+    if (reinterpret_cast<uintptr_t>(h->route_taken) % 4 != 0) return TW_EALIGN;
+  }
   tw_status st = check_ptrs({h->row_nnz, h->ell_nnz, h->ell_idx, h->ell_a, h->backup_slot, h->n_backup});
   if (st != TW_OK) return st;
   if (gated) {
@@ -127,8 +132,9 @@ struct HybFwdWs {
   uint16_t* H_lo;
   float* acc;  // split-K accumulator of the down projection [ra, d]
   int32_t* sched;  // token scheduling counter of the sparse forward
+  uint16_t* Hd;    // dense route: h of every row [T, I] (null for the sparse route)
 };
-HybFwdWs carve_hybrid_fwd(Carve& c, int T, int d, int I, int W, int C, int backup_cap) {
+HybFwdWs carve_hybrid_fwd(Carve& c, int T, int d, int I, int W, int C, int backup_cap, int route) {
   const size_t nT = static_cast<size_t>(I / W);
   const int ra = round_up(backup_cap, 128);
   HybFwdWs w{};
@@ -143,6 +149,7 @@ HybFwdWs carve_hybrid_fwd(Carve& c, int T, int d, int I, int W, int C, int backu
   w.H_lo = c.take<uint16_t>(static_cast<size_t>(ra) * I);
   w.acc = c.take<float>(static_cast<size_t>(ra) * d);
   w.sched = c.take<int32_t>(4);
+  w.Hd = route != TW_ROUTE_SPARSE ? c.take<uint16_t>(static_cast<size_t>(T) * I) : nullptr;
   return w;
 }
 
@@ -156,8 +163,9 @@ struct HybBwdWs {
   tw::BackupGradOut g;  // dG, dU, H as (hi, lo) bf16 pairs
   float* acc;           // split-K accumulator of dx for the backup rows [ra, d]
   int32_t* sched;       // token scheduling counter of the token pass
+  uint16_t *dGd, *dUd, *Hd;  // dense route: dg, du, h of every row [T, I] (null for the sparse route)
 };
-HybBwdWs carve_hybrid_bwd(Carve& c, int T, int d, int I, int R, int backup_cap) {
+HybBwdWs carve_hybrid_bwd(Carve& c, int T, int d, int I, int R, int backup_cap, int route) {
   const size_t TR = static_cast<size_t>(T) * R;
   const int ra = round_up(backup_cap, 128);
   const size_t rI = static_cast<size_t>(ra) * I;
@@ -176,6 +184,14 @@ HybBwdWs carve_hybrid_bwd(Carve& c, int T, int d, int I, int R, int backup_cap) 
   w.g.H_lo = c.take<uint16_t>(rI);
   w.acc = c.take<float>(static_cast<size_t>(ra) * d);
   w.sched = c.take<int32_t>(tw::kSchedWords);
+  if (route != TW_ROUTE_SPARSE) {
+    const size_t TI = static_cast<size_t>(T) * I;
+    w.dGd = c.take<uint16_t>(TI);
+    w.dUd = c.take<uint16_t>(TI);
+    w.Hd = c.take<uint16_t>(TI);
+  } else {
+    w.dGd = w.dUd = w.Hd = nullptr;
+  }
   return w;
 }
 
@@ -360,11 +376,11 @@ tw_status tw_gate_relu_dense(const uint16_t* x, const uint16_t* Wg, int T, int d
   return TW_OK;
 }
 
-size_t hybrid_ffn_fwd_workspace_size(int T, int d, int I, int W, int C, int R, int backup_cap) {
+size_t hybrid_ffn_fwd_workspace_size(int T, int d, int I, int W, int C, int R, int backup_cap, int route) {
   (void)R;
   if (T < 0 || W <= 0 || C <= 0) return 0;
   Carve c(nullptr);
-  carve_hybrid_fwd(c, T, d, I, W, C, backup_cap < 0 ? 0 : backup_cap);
+  carve_hybrid_fwd(c, T, d, I, W, C, backup_cap < 0 ? 0 : backup_cap, route);
   return c.off + 256;
 }
 
@@ -383,18 +399,23 @@ tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* 
   if (st != TW_OK) return st;
   if (gated && !aligned16(Wu)) return TW_EALIGN;
   const int R = saved->R, cap = saved->backup_cap;
-  if (ws_bytes < hybrid_ffn_fwd_workspace_size(T, d, I, W, C, R, cap)) return TW_EWORKSPACE;
+  const int route = saved->route;
+  if (ws_bytes < hybrid_ffn_fwd_workspace_size(T, d, I, W, C, R, cap, route)) return TW_EWORKSPACE;
   cudaStream_t s = as_stream(stream);
   Carve c(reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(ws) + 255) & ~static_cast<uintptr_t>(255)));
-  const HybFwdWs w = carve_hybrid_fwd(c, T, d, I, W, C, cap);
+  const HybFwdWs w = carve_hybrid_fwd(c, T, d, I, W, C, cap, route);
   const int ra = round_up(cap, 128);
   tw_twell o{T, I, W, C, w.cnt, w.val, w.idx, saved->row_nnz, w.ovf, w.ovf_rows, w.n_ovf};
+  // the route this call takes, decided on the device by the row compaction (it is
+  // known on the host only for the fixed routes); kernels of the other route return
+  const int32_t* taken = route == TW_ROUTE_SPARSE ? nullptr : saved->route_taken;
 
   // the backup list below covers the overflow rows, so the TwELL's own list is not built
   st = gate_pack_impl(x, Wg, T, d, I, W, C, o, nullptr, T, dev_status, s, false);
   if (st != TW_OK) return st;
   TW_TRY(tw::launch_compact_rows(o.ovf, saved->row_nnz, R, T, saved->backup_tok, cap, saved->n_backup,
-                                 saved->backup_slot, saved->ell_nnz, cap, dev_status, s, w.sched));
+                                 saved->backup_slot, saved->ell_nnz, cap, dev_status, s, w.sched, route,
+                                 saved->dense_above, saved->route_taken));
   tw::SparseFwdArgs a{};
   a.x = x; a.Wu = Wu; a.Wd = Wd;
   a.T = T; a.d = d; a.I = I; a.W = W; a.C = C; a.nT = I / W; a.L = (I / W) * C;
@@ -405,7 +426,21 @@ tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* 
   a.status = dev_status;
   a.sched = w.sched;
   a.sched_zeroed = true;  // by compact_rows above
-  TW_TRY(tw::launch_token_fwd(a, s));
+  a.route = taken;
+  if (route != TW_ROUTE_DENSE) TW_TRY(tw::launch_token_fwd(a, s));
+  if (route != TW_ROUTE_SPARSE) {
+    // the dense route: h of every ELL row on the tensor cores (and the ELL rows of the
+    // saved Hybrid), then y = h Wd over all rows; the backup rows' y follows below
+    if (gated)
+      TW_TRY(tw::gemm_up_hybrid(x, Wu, T, d, I, o, R, saved->backup_slot, w.Hd, saved->ell_idx, saved->ell_a,
+                                saved->ell_u, taken, dev_status, s));
+    else
+      TW_TRY(tw::launch_twell_to_dense_ell(o, saved->backup_slot, R, w.Hd, saved->ell_idx, saved->ell_a, taken,
+                                           dev_status, s));
+    const uint16_t* A[1] = {w.Hd};
+    const uint16_t* B[1] = {Wd};
+    TW_TRY(tw::gemm_rows_nmajor_bf16(A, B, 1, T, I, d, y, d, taken, dev_status, s));
+  }
   if (cap > 0) {
     TW_TRY(tw::launch_gather_rows(x, d, T, saved->backup_tok, saved->n_backup, cap, ra, w.X, s, dev_status, nullptr,
                                   nullptr, w.acc, d));
@@ -419,10 +454,10 @@ tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* 
   return TW_OK;
 }
 
-size_t hybrid_ffn_bwd_workspace_size(int T, int d, int I, int R, int backup_cap) {
+size_t hybrid_ffn_bwd_workspace_size(int T, int d, int I, int R, int backup_cap, int route) {
   if (T < 0 || R < 1) return 0;
   Carve c(nullptr);
-  carve_hybrid_bwd(c, T, d, I, R, backup_cap < 0 ? 0 : backup_cap);
+  carve_hybrid_bwd(c, T, d, I, R, backup_cap < 0 ? 0 : backup_cap, route);
   return c.off + 256;
 }
 
@@ -449,11 +484,15 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
     if (st != TW_OK) return st;
   }
   const int R = saved->R, cap = saved->backup_cap;
-  if (ws_bytes < hybrid_ffn_bwd_workspace_size(T, d, I, R, cap)) return TW_EWORKSPACE;
+  const int route = saved->route;
+  if (ws_bytes < hybrid_ffn_bwd_workspace_size(T, d, I, R, cap, route)) return TW_EWORKSPACE;
   cudaStream_t s = as_stream(stream);
   Carve c(reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(ws) + 255) & ~static_cast<uintptr_t>(255)));
-  const HybBwdWs w = carve_hybrid_bwd(c, T, d, I, R, cap);
+  const HybBwdWs w = carve_hybrid_bwd(c, T, d, I, R, cap, route);
   const int ra = round_up(cap, 128);
+  // the route the forward took (T == 0: no forward ran, the sparse path writes dW = 0)
+  const bool dense_possible = route != TW_ROUTE_SPARSE && T > 0;
+  const int32_t* taken = dense_possible ? saved->route_taken : nullptr;
 
   tw::SparseBwdArgs a{};
   a.dy = dy; a.x = x; a.Wg = Wg; a.Wu = Wu; a.Wd = Wd;
@@ -467,7 +506,17 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
   a.dWg = dWg; a.dWu = dWu; a.dWd = dWd;
   a.sched = w.sched;
   a.sched_w = w.sched + tw::kSchedStride;
-  TW_TRY(tw::launch_sparse_bwd_tokens(a, s));
+  a.route = taken;
+  const bool sparse_possible = route != TW_ROUTE_DENSE || T == 0;
+  if (sparse_possible) TW_TRY(tw::launch_sparse_bwd_tokens(a, s));
+  if (dense_possible) {
+    // the dense route: dg, du, h of every ELL row from dh = dY Wd^T on the tensor
+    // cores, then dx = dg Wg + du Wu over all rows (the backup rows' dx follows below)
+    TW_TRY(tw::gemm_dense_grad(dy, Wd, T, d, I, *saved, gated, l1, w.dGd, w.dUd, w.Hd, taken, dev_status, s));
+    const uint16_t* A[2] = {w.dGd, w.dUd};
+    const uint16_t* B[2] = {Wg, Wu};
+    TW_TRY(tw::gemm_rows_nmajor_bf16(A, B, gated ? 2 : 1, T, I, d, dx, d, taken, dev_status, s));
+  }
   const bool backup = cap > 0 && T > 0;
   if (backup) {
     TW_TRY(tw::launch_gather_rows(dy, d, T, saved->backup_tok, saved->n_backup, cap, ra, w.dY, s, dev_status, x, w.X,
@@ -490,7 +539,14 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
     TW_TRY(tw::gemm_weight_grads(probs, gated ? 3 : 2, ra, nb, cap, I, d, dev_status, s));
   }
   a.dW_base_rows = backup ? saved->n_backup : nullptr;
-  TW_TRY(tw::launch_sparse_bwd_weights(a, s));
+  if (sparse_possible) TW_TRY(tw::launch_sparse_bwd_weights(a, s));
+  if (dense_possible) {
+    // dense route weight gradients over all rows (the backup rows' dg, du, h are 0 in
+    // these operands): added to the backup rows' part when there is one
+    const tw::DenseWeightGradProblem probs[3] = {{w.dGd, x, dWg}, {w.Hd, dy, dWd}, {w.dUd, x, dWu}};
+    TW_TRY(tw::gemm_dense_weight_grads(probs, gated ? 3 : 2, T, I, d, backup ? saved->n_backup : nullptr, taken,
+                                       dev_status, s));
+  }
   return TW_OK;
 }
 

@@ -224,4 +224,54 @@ cudaError_t launch_hybrid_unpack(const tw_hybrid& h, float* A, float* U, cudaStr
   return e;
 }
 
+// ------------------------------------------------------------------ dense route, non-gated
+// Row t without a backup slot: H[t] = its TwELL activations (zeros elsewhere), and its
+// ELL row: the slots of tile k go to ELL offsets starting at the nonzeros of tiles
+// 0 .. k - 1 (a warp scan over the tiles, 32 at a time). Backup rows: H[t] = 0.
+__global__ void __launch_bounds__(256) twell_to_dense_ell_kernel(const tw_twell tw, const int32_t* __restrict__ backup_slot,
+                                                                int R, uint16_t* __restrict__ H,
+                                                                uint16_t* __restrict__ ell_idx,
+                                                                uint16_t* __restrict__ ell_a, const int32_t* route,
+                                                                int32_t* status) {
+  pdl_enter();
+  if (route != nullptr && *route != 1) return;  // the call took the sparse route
+  const int lane = threadIdx.x & 31;
+  const int nT = tw.I / tw.W;
+  for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < tw.T; t += gridDim.x * 8) {
+    uint4* row = reinterpret_cast<uint4*>(H + static_cast<size_t>(t) * tw.I);
+    for (int c = lane; c < tw.I / 8; c += 32) row[c] = make_uint4(0u, 0u, 0u, 0u);
+    if (backup_slot[t] != -1) continue;
+    __syncwarp();  // the zeros land before any lane's slots
+    const size_t rb = static_cast<size_t>(t) * R;
+    int base = 0;
+    for (int k0 = 0; k0 < nT; k0 += 32) {
+      const int k = k0 + lane;
+      const size_t tk = static_cast<size_t>(t) * nT + k;
+      const int n = k < nT ? min(static_cast<int>(tw.cnt[tk]), tw.C) : 0;
+      const int incl = warp_inclusive_scan(n);
+      int off = base + incl - n;
+      for (int s = 0; s < n; ++s, ++off) {
+        const int li = tw.idx[tk * tw.C + s];
+        if (!TW_CHECKED(li < tw.W && off < R, status)) continue;
+        const int j = k * tw.W + li;
+        const uint16_t v = tw.val[tk * tw.C + s];
+        H[static_cast<size_t>(t) * tw.I + j] = v;
+        ell_idx[rb + off] = static_cast<uint16_t>(j);
+        ell_a[rb + off] = v;
+      }
+      base += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+  }
+}
+
+cudaError_t launch_twell_to_dense_ell(const tw_twell& tw, const int32_t* backup_slot, int R, uint16_t* H,
+                                      uint16_t* ell_idx, uint16_t* ell_a, const int32_t* route, int32_t* status,
+                                      cudaStream_t s) {
+  if (tw.T == 0) return cudaSuccess;
+  cudaError_t e = launch(twell_to_dense_ell_kernel, dim3(rows_grid(tw.T)), dim3(256), 0, s, tw, backup_slot, R, H,
+                         ell_idx, ell_a, route, status);
+  trace_mark(s, "twell_to_dense_ell");
+  return e;
+}
+
 }  // namespace tw

@@ -81,6 +81,8 @@ static GemmShape shape_static(int M, int N, int K, int32_t* status) {
   g.problems = 1;
   g.status = status;
   g.withhold_kb = -1;
+  g.route_dev = nullptr;
+  g.route_want = 0;
   return g;
 }
 
@@ -241,6 +243,99 @@ cudaError_t gemm_weight_grads(const WeightGradProblem* probs, int n_probs, int r
   // the hi and lo segments share Q: one Q tile a K step for both
   return run_gemm<256, true, true, false, 3, EpiStoreF32Grouped, 2>(maps, sh, ep, ep.rows_per_problem * n_probs, s,
                                                                      "backup_weight_grad");
+}
+
+// ------------------------------------------------------------------ dense route
+static void set_route(GemmShape& sh, const int32_t* route) {
+  sh.route_dev = route;
+  sh.route_want = 1;
+}
+
+cudaError_t gemm_up_hybrid(const uint16_t* x, const uint16_t* Wu, int T, int d, int I, const tw_twell& tw, int R,
+                           const int32_t* backup_slot, uint16_t* H, uint16_t* ell_idx, uint16_t* ell_a,
+                           uint16_t* ell_u, const int32_t* route, int32_t* status, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  GemmShape sh = shape_static(T, I, d, status);
+  set_route(sh, route);
+  EpiUpHybrid::Params ep{T, tw.W, tw.C, I / tw.W, R, tw.cnt, tw.val, tw.idx, backup_slot, H, I,
+                         ell_idx, ell_a, ell_u, status};
+  GemmMaps maps;
+  const int bn = (I % 256 == 0) ? 256 : (I % 128 == 0) ? 128 : 64;
+  if (!tmap_kmajor(&maps.a[0], x, T, d, 128) || !tmap_kmajor(&maps.b[0], Wu, I, d, bn)) return cudaErrorInvalidValue;
+  fill_unused(maps, 1, 1);
+  if (bn == 256) return run_gemm<256, false, false, false, 4, EpiUpHybrid>(maps, sh, ep, T, s, "dense_up");
+  if (bn == 128) return run_gemm<128, false, false, false, 6, EpiUpHybrid>(maps, sh, ep, T, s, "dense_up");
+  return run_gemm<64, false, false, false, 8, EpiUpHybrid>(maps, sh, ep, T, s, "dense_up");
+}
+
+cudaError_t gemm_rows_nmajor_bf16(const uint16_t* const* A, const uint16_t* const* B, int segments, int M, int K,
+                                  int N, uint16_t* out, int ld, const int32_t* route, int32_t* status,
+                                  cudaStream_t s) {
+  if (M == 0) return cudaSuccess;
+  if (segments < 1 || segments > GEMM_MAX_SEGMENTS || N % 256 != 0) return cudaErrorInvalidValue;
+  GemmShape sh = shape_static(M, N, K, status);
+  sh.segments = segments;
+  set_route(sh, route);
+  GemmMaps maps;
+  for (int i = 0; i < segments; ++i)
+    if (!tmap_kmajor(&maps.a[i], A[i], M, K, 128) || !tmap_mnmajor(&maps.b[i], B[i], K, N))
+      return cudaErrorInvalidValue;
+  fill_unused(maps, segments, segments);
+  EpiStoreBf16::Params ep{out, ld};
+  return run_gemm<256, false, true, false, 4, EpiStoreBf16>(maps, sh, ep, M, s, "dense_rows_gemm");
+}
+
+template <int BN, bool GATED>
+static cudaError_t dense_grad_bn(const uint16_t* dY, const uint16_t* Wd, int T, int d, int I, const tw_hybrid& h,
+                                 float l1, uint16_t* dG, uint16_t* dU, uint16_t* H, const int32_t* route,
+                                 int32_t* status, cudaStream_t s) {
+  GemmShape sh = shape_static(T, I, d, status);
+  set_route(sh, route);
+  GemmMaps maps;
+  if (!tmap_kmajor(&maps.a[0], dY, T, d, 128) || !tmap_kmajor(&maps.b[0], Wd, I, d, BN)) return cudaErrorInvalidValue;
+  fill_unused(maps, 1, 1);
+  typename EpiDenseGrad<GATED>::Params ep{h.R, I, h.ell_nnz, h.backup_slot, h.ell_idx, h.ell_a, GATED ? h.ell_u : nullptr,
+                                          l1, dG, GATED ? dU : nullptr, H, I, status};
+  constexpr int kStageBytes = (128 + BN) * 64 * 2;
+  constexpr int kBudget = 232448 - 1280 - EpiDenseGrad<GATED>::kStageBytes;
+  constexpr int kStages = kBudget / kStageBytes < 8 ? kBudget / kStageBytes : 8;
+  return run_gemm<BN, false, false, false, kStages, EpiDenseGrad<GATED>>(maps, sh, ep, T, s, "dense_grad");
+}
+
+cudaError_t gemm_dense_grad(const uint16_t* dY, const uint16_t* Wd, int T, int d, int I, const tw_hybrid& h,
+                            bool gated, float l1, uint16_t* dG, uint16_t* dU, uint16_t* H, const int32_t* route,
+                            int32_t* status, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  if (I % 256 == 0)
+    return gated ? dense_grad_bn<256, true>(dY, Wd, T, d, I, h, l1, dG, dU, H, route, status, s)
+                 : dense_grad_bn<256, false>(dY, Wd, T, d, I, h, l1, dG, dU, H, route, status, s);
+  if (I % 128 == 0)
+    return gated ? dense_grad_bn<128, true>(dY, Wd, T, d, I, h, l1, dG, dU, H, route, status, s)
+                 : dense_grad_bn<128, false>(dY, Wd, T, d, I, h, l1, dG, dU, H, route, status, s);
+  return gated ? dense_grad_bn<64, true>(dY, Wd, T, d, I, h, l1, dG, dU, H, route, status, s)
+               : dense_grad_bn<64, false>(dY, Wd, T, d, I, h, l1, dG, dU, H, route, status, s);
+}
+
+cudaError_t gemm_dense_weight_grads(const DenseWeightGradProblem* probs, int n_probs, int T, int I, int d,
+                                    const int32_t* add_if, const int32_t* route, int32_t* status, cudaStream_t s) {
+  if (T == 0 || n_probs <= 0) return cudaSuccess;
+  if (n_probs > EpiF32GroupedStoreOrAdd::kMaxProblems || d % 256 != 0) return cudaErrorInvalidValue;
+  GemmShape sh = shape_static(I, d, T, status);
+  sh.problems = n_probs;
+  set_route(sh, route);
+  GemmMaps maps;
+  EpiF32GroupedStoreOrAdd::Params ep{};
+  for (int p = 0; p < n_probs; ++p) {
+    if (!tmap_mnmajor(&maps.a[p], probs[p].P, T, I) || !tmap_mnmajor(&maps.b[p], probs[p].Q, T, d))
+      return cudaErrorInvalidValue;
+    ep.D[p] = probs[p].D;
+  }
+  fill_unused(maps, n_probs, n_probs);
+  ep.ldd = d;
+  ep.rows_per_problem = (I + GEMM_BM - 1) / GEMM_BM * GEMM_BM;
+  ep.add_if = add_if;
+  return run_gemm<256, true, true, false, 4, EpiF32GroupedStoreOrAdd>(maps, sh, ep, ep.rows_per_problem * n_probs, s,
+                                                                      "dense_weight_grad");
 }
 
 // ------------------------------------------------------------------ layout test GEMM

@@ -57,6 +57,8 @@ struct GemmShape {
   int withhold_kb;   // test hook, -1 normally: in a CTA's first work unit, the TMA loads of
                      // this K block are never issued, so the MMA issuer's bounded wait for
                      // that stage runs out (TW_ETIMEOUT) and every role drains and returns
+  const int* route_dev;  // optional: the launch does its work only when *route_dev == route_want
+  int route_want;        // (the route a call took, decided on the device by an earlier kernel)
 };
 
 constexpr int GEMM_MAX_SEGMENTS = 6;  // segments x problems
@@ -155,6 +157,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (shape.m_dev != nullptr) M = min(max(*shape.m_dev, 0), shape.m_cap);
   int K = shape.K;
   if (shape.k_dev != nullptr) K = min(max(*shape.k_dev, 0), shape.k_cap);
+  if (shape.route_dev != nullptr && *shape.route_dev != shape.route_want) K = 0;  // not this call's route: no work
   const int m_tiles = (M + GEMM_BM - 1) / GEMM_BM;
   const int n_tiles = shape.N / BN;
   const int problems = max(1, shape.problems);
@@ -329,7 +332,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if (!ok) break;
       tc_fence_after_sync();
       if constexpr (Epi::kStageBytes > 0)
-        e.stage = reinterpret_cast<float*>(tiles + STAGES * Tr::STAGE_BYTES + Tr::BAR_BYTES) + quarter * 32 * kEpiStageStride;
+        e.stage = reinterpret_cast<float*>(tiles + STAGES * Tr::STAGE_BYTES + Tr::BAR_BYTES) + quarter * (Epi::kStageBytes / 16);
       const uint32_t tbase =
           tmem_base + static_cast<uint32_t>(buf * Tr::ACC_COLS) + (static_cast<uint32_t>(quarter * 32) << 16);
       if constexpr (!DUAL && epi_overlaps_loads<Epi>::value) {
@@ -469,6 +472,272 @@ struct EpiStoreF32Grouped {
     transposed_rows(stage, v, m - prob * p.rows_per_problem, M, [&](int r, int c4, float4 x) {
       reinterpret_cast<float4*>(col + static_cast<size_t>(r) * p.ldd)[c4] = x;
     });
+  }
+  TW_DEV void finish() {}
+};
+
+// EpiStoreF32Grouped that adds instead of storing when *add_if (a device count, read
+// once a thread) is positive: the dense route's weight gradients, added to the dense
+// backup rows' part when there are backup rows, else written.
+struct EpiF32GroupedStoreOrAdd {
+  static constexpr int kStageBytes = kEpiTransposeBytes;
+  static constexpr bool kOverlapLoads = true;
+  static constexpr int kMaxProblems = 3;
+  struct Params {
+    float* D[kMaxProblems];
+    int ldd;
+    int rows_per_problem;
+    const int32_t* add_if;
+  };
+  const Params& p;
+  int m, M, n0;
+  bool add;
+  float* stage = nullptr;
+  TW_DEV EpiF32GroupedStoreOrAdd(const Params& p_, int m_, int M_, int n0_)
+      : p(p_), m(m_), M(M_), n0(n0_), add(p_.add_if != nullptr && *p_.add_if > 0) {}
+  TW_DEV void chunk(int c, const uint32_t (&v)[32], const uint32_t (&)[32]) {
+    const int prob = m / p.rows_per_problem;
+    float* col = p.D[prob] + n0 + c * 32;
+    transposed_rows(stage, v, m - prob * p.rows_per_problem, M, [&](int r, int c4, float4 x) {
+      float4* dst = reinterpret_cast<float4*>(col + static_cast<size_t>(r) * p.ldd) + c4;
+      if (add)
+        atomicAdd(dst, x);
+      else
+        *dst = x;
+    });
+  }
+  TW_DEV void finish() {}
+};
+
+// D[m][n] = bf16(acc) (round to nearest even) for rows m < M, row stride ld: the dense
+// route's y and dx (rows of the dense backup are written again by its row scatter).
+struct EpiStoreBf16 {
+  static constexpr int kStageBytes = kEpiTransposeBytes;
+  static constexpr bool kOverlapLoads = true;
+  struct Params {
+    uint16_t* D;
+    int ld;
+  };
+  const Params& p;
+  int m, M, n0;
+  float* stage = nullptr;
+  TW_DEV EpiStoreBf16(const Params& p_, int m_, int M_, int n0_) : p(p_), m(m_), M(M_), n0(n0_) {}
+  // Every lane of the warp calls it (the stores are warp-cooperative).
+  TW_DEV void chunk(int c, const uint32_t (&v)[32], const uint32_t (&)[32]) {
+    const int lane = threadIdx.x & 31;
+    const int m0 = m - lane;
+    const int rows = min(32, M - m0);
+    if (rows <= 0) return;
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+    transposed_rows_bf16(stage, w, m0, rows, p.D + n0 + c * 32, p.ld);
+  }
+  TW_DEV void finish() {}
+};
+
+// Dense route, gated forward: the accumulator is u = x Wu^T for token row m over the
+// columns [n0, n0 + BN). With the row's TwELL slots of a (the gate kernel's output;
+// a row served here never overflowed, so its slots hold all its nonzeros) the
+// epilogue forms h = a u at the active columns and writes
+//   H[m][:]        bf16(h) at active columns, 0 elsewhere (the down GEMM's operand),
+//   the ELL row    global index, a and bf16(u) per nonzero, at the row's ELL offset
+//                  (the nonzeros of the row's tiles before this CTA tile),
+// the same ELL the sparse route's token kernel writes. Rows of the dense backup
+// (backup_slot != -1) get H = 0 and no ELL entries.
+// The accumulator's 32 columns of a chunk go through the thread's part of the
+// staging buffer (a row of kUpStride floats, an odd stride, so lanes reading the same
+// column hit distinct banks), where active columns are looked up by index.
+struct EpiUpHybrid {
+  static constexpr int kUpStride = 33;
+  static constexpr int kStageBytes = 4 * 32 * kUpStride * 4;
+  struct Params {
+    int T, W, C, nT, R;
+    const uint16_t* cnt;
+    const uint16_t* val;
+    const uint8_t* idx;
+    const int32_t* backup_slot;
+    uint16_t* H;
+    int ldh;
+    uint16_t* ell_idx;
+    uint16_t* ell_a;
+    uint16_t* ell_u;
+    int32_t* status;
+  };
+  const Params& p;
+  int m, n0;
+  bool valid, ell_row;
+  int off;      // ELL slot of the next nonzero of this row
+  int k_cur;    // TwELL tile of the slot cursor, and the cursor within it
+  int s_cur;
+  float* stage = nullptr;
+  TW_DEV EpiUpHybrid(const Params& p_, int m_, int M_, int n0_)
+      : p(p_), m(m_), n0(n0_), valid(m_ < M_), ell_row(false), off(0), k_cur(-1), s_cur(0) {}
+  // before the accumulator is ready: the routing of the row and the ELL offset of its
+  // first tile in [n0, n0 + BN) (a sum over the counts of the row's earlier tiles)
+  TW_DEV void prefetch(int) {
+    if (!valid) return;
+    ell_row = p.backup_slot[m] == -1;
+    if (!ell_row) return;
+    const int k0 = n0 / p.W;
+    const uint16_t* cr = p.cnt + static_cast<size_t>(m) * p.nT;
+    int o = 0;
+    for (int k = 0; k < k0; ++k) o += min(static_cast<int>(cr[k]), p.C);
+    off = o;
+  }
+  TW_DEV void chunk(int c, const uint32_t (&v)[32], const uint32_t (&)[32]) {
+    if (!valid) return;
+    const int col0 = n0 + c * 32;
+    uint4* hdst = reinterpret_cast<uint4*>(p.H + static_cast<size_t>(m) * p.ldh + col0);
+    if (!ell_row) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) hdst[i] = make_uint4(0u, 0u, 0u, 0u);
+      return;
+    }
+    float* mine = stage + (threadIdx.x & 31) * kUpStride;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) mine[i] = __uint_as_float(v[i]);
+    const int k = col0 / p.W;
+    const int local0 = col0 - k * p.W;
+    if (k != k_cur) {
+      k_cur = k;
+      s_cur = 0;
+    }
+    const size_t tk = static_cast<size_t>(m) * p.nT + k;
+    const int n = min(static_cast<int>(p.cnt[tk]), p.C);
+    uint32_t mask = 0u;
+    const size_t rb = static_cast<size_t>(m) * p.R;
+    // the tile's slots are in ascending column order: take those inside this chunk
+    for (; s_cur < n; ++s_cur) {
+      const int li = p.idx[tk * p.C + s_cur];
+      if (li >= local0 + 32) break;
+      const int i = li - local0;
+      if (!TW_CHECKED(i >= 0 && i < 32, p.status)) continue;
+      const uint16_t ab = p.val[tk * p.C + s_cur];
+      const float u = mine[i];
+      mine[i] = bf16_to_f32(ab) * u;  // h, in place of u
+      mask |= 1u << i;
+      if (TW_CHECKED(off < p.R, p.status)) {
+        p.ell_idx[rb + off] = static_cast<uint16_t>(col0 + i);
+        p.ell_a[rb + off] = ab;
+        p.ell_u[rb + off] = f32_to_bf16(u);
+      }
+      ++off;
+    }
+    uint32_t w[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const float h0 = ((mask >> (2 * q)) & 1u) ? mine[2 * q] : 0.f;
+      const float h1 = ((mask >> (2 * q + 1)) & 1u) ? mine[2 * q + 1] : 0.f;
+      w[q] = pack_bf16x2_rn(h0, h1);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) hdst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  }
+  TW_DEV void finish() {}
+};
+
+// Dense route, backward: the accumulator is dh = dY Wd^T for token row m over the
+// columns [n0, n0 + BN). The row's saved ELL entries (global index ascending, a, u)
+// give the support; on it
+//   dg = dh u + l1 (non-gated: dh + l1),  du = dh a,  h = a u (non-gated: a),
+// and the epilogue writes bf16 dG, dU (gated) and H over the tile's columns, 0 off
+// the support, as the operands of the dx and weight-gradient GEMMs. Rows of the dense
+// backup get zeros (their gradients come from the backup GEMMs). The entries of a
+// chunk are placed in the thread's staging row (a at column i, u at 32 + i; stride
+// kGradStride, odd) and read back by column.
+template <bool GATED>
+struct EpiDenseGrad {
+  static constexpr int kGradStride = 65;
+  static constexpr int kStageBytes = 4 * 32 * kGradStride * 4;
+  struct Params {
+    int R, I;
+    const int32_t* ell_nnz;
+    const int32_t* backup_slot;
+    const uint16_t* ell_idx;
+    const uint16_t* ell_a;
+    const uint16_t* ell_u;
+    float l1;
+    uint16_t *dG, *dU, *H;
+    int ld;
+    int32_t* status;
+  };
+  const Params& p;
+  int m, n0;
+  bool valid, ell_row;
+  int cur, end;  // ELL entry cursor and end of the row
+  float* stage = nullptr;
+  TW_DEV EpiDenseGrad(const Params& p_, int m_, int M_, int n0_)
+      : p(p_), m(m_), n0(n0_), valid(m_ < M_), ell_row(false), cur(0), end(0) {}
+  // before the accumulator is ready: the first ELL entry at or past column n0
+  // (binary search over the row's ascending indices)
+  TW_DEV void prefetch(int) {
+    if (!valid) return;
+    ell_row = p.backup_slot[m] == -1;
+    if (!ell_row) return;
+    int n = p.ell_nnz[m];
+    if (!TW_CHECKED(n >= 0 && n <= p.R, p.status)) n = 0;
+    const uint16_t* ri = p.ell_idx + static_cast<size_t>(m) * p.R;
+    int lo = 0, hi = n;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (static_cast<int>(ri[mid]) < n0)
+        lo = mid + 1;
+      else
+        hi = mid;
+    }
+    cur = lo;
+    end = n;
+  }
+  TW_DEV void chunk(int c, const uint32_t (&dh)[32], const uint32_t (&)[32]) {
+    if (!valid) return;
+    const int col0 = n0 + c * 32;
+    const size_t o = static_cast<size_t>(m) * p.ld + col0;
+    uint32_t mask = 0u;
+    float* mine = stage + (threadIdx.x & 31) * kGradStride;
+    if (ell_row) {
+      const size_t rb = static_cast<size_t>(m) * p.R;
+      for (; cur < end; ++cur) {
+        const int j = p.ell_idx[rb + cur];
+        if (j >= col0 + 32) break;
+        const int i = j - col0;
+        if (!TW_CHECKED(i >= 0, p.status)) continue;
+        mine[i] = bf16_to_f32(p.ell_a[rb + cur]);
+        if (GATED) mine[32 + i] = bf16_to_f32(p.ell_u[rb + cur]);
+        mask |= 1u << i;
+      }
+    }
+    uint32_t wg[16], wu[16], wh[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      float g2[2], u2[2], h2[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int i = 2 * q + e;
+        const bool act = (mask >> i) & 1u;
+        const float a = act ? mine[i] : 0.f;
+        const float u = GATED ? (act ? mine[32 + i] : 0.f) : 1.f;
+        const float d = __uint_as_float(dh[i]);
+        g2[e] = act ? (GATED ? d * u : d) + p.l1 : 0.f;
+        u2[e] = act ? d * a : 0.f;
+        h2[e] = GATED ? a * u : a;
+      }
+      wg[q] = pack_bf16x2_rn(g2[0], g2[1]);
+      wu[q] = pack_bf16x2_rn(u2[0], u2[1]);
+      wh[q] = pack_bf16x2_rn(h2[0], h2[1]);
+    }
+    uint4* dg = reinterpret_cast<uint4*>(p.dG + o);
+    uint4* hh = reinterpret_cast<uint4*>(p.H + o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      dg[i] = make_uint4(wg[4 * i], wg[4 * i + 1], wg[4 * i + 2], wg[4 * i + 3]);
+      hh[i] = make_uint4(wh[4 * i], wh[4 * i + 1], wh[4 * i + 2], wh[4 * i + 3]);
+    }
+    if (GATED) {
+      uint4* du = reinterpret_cast<uint4*>(p.dU + o);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) du[i] = make_uint4(wu[4 * i], wu[4 * i + 1], wu[4 * i + 2], wu[4 * i + 3]);
+    }
   }
   TW_DEV void finish() {}
 };

@@ -69,9 +69,13 @@ cudaError_t launch_pack_dense(const uint16_t* A, int T, int I, int W, int C, con
 // Raises TW_ECAPACITY when n > cap_check.
 // zero_word (optional) is set to 0 by the kernel, for a scheduling counter used later
 // in the stream.
+// Route decision (when route_out != nullptr): *route_out = 1 (dense) when route_mode
+// is TW_ROUTE_DENSE, or TW_ROUTE_AUTO and the unflagged rows' mean row_nnz exceeds
+// dense_above; else 0.
 cudaError_t launch_compact_rows(const uint8_t* ovf, const int32_t* row_nnz, int R, int T, int32_t* list,
                                 int list_cap, int32_t* count, int32_t* slot_of, int32_t* ell_nnz, int cap_check,
-                                int32_t* status, cudaStream_t s, int32_t* zero_word = nullptr);
+                                int32_t* status, cudaStream_t s, int32_t* zero_word = nullptr,
+                                int route_mode = TW_ROUTE_SPARSE, float dense_above = 0.f, int32_t* route_out = nullptr);
 
 // ---------------------------------------------------------------- tw_formats.cu
 // TwELL slots scattered into a dense bf16 [T, I] matrix (zeros elsewhere).
@@ -82,6 +86,12 @@ cudaError_t launch_hybrid_pack(const uint16_t* A, const uint16_t* U, int T, int 
                                uint8_t* ovf_ws, int32_t* status, cudaStream_t s);
 // Dense fp32 A [T, I] (and U when non-null) from a Hybrid.
 cudaError_t launch_hybrid_unpack(const tw_hybrid& h, float* A, float* U, cudaStream_t s);
+// Dense route, non-gated forward (only when *route == 1): H [T, I] bf16 = the TwELL's
+// activations on rows without a backup slot (0 on backup rows), and those rows' ELL
+// entries (idx, a) written at their ELL offsets.
+cudaError_t launch_twell_to_dense_ell(const tw_twell& tw, const int32_t* backup_slot, int R, uint16_t* H,
+                                      uint16_t* ell_idx, uint16_t* ell_a, const int32_t* route, int32_t* status,
+                                      cudaStream_t s);
 
 // ---------------------------------------------------------------- tw_neurons.cu
 cudaError_t launch_neuron_counts(const tw_hybrid& h, int32_t* counts, cudaStream_t s);
@@ -125,6 +135,7 @@ struct SparseFwdArgs {
   // in the stream did.
   int32_t* sched;
   bool sched_zeroed;
+  const int32_t* route;  // optional: the kernel does nothing when *route == 1 (the dense route)
 };
 // TwELL / Hybrid forward of the non-dense rows (tw_token.cu)
 cudaError_t launch_token_fwd(const SparseFwdArgs& a, cudaStream_t s);
@@ -156,6 +167,7 @@ struct SparseBwdArgs {
   // the kSchedWords ints are zeroed together with col_cnt
   int32_t* sched;
   int32_t* sched_w;
+  const int32_t* route;  // optional: the kernels do nothing when *route == 1 (the dense route)
 };
 constexpr int kSchedCounters = 8;
 constexpr int kSchedStride = 32;  // ints: one 128-byte line per counter
@@ -221,6 +233,33 @@ cudaError_t gemm_weight_grads(const WeightGradProblem* probs, int n_probs, int r
                               int cap, int I, int d, int32_t* status, cudaStream_t s);
 
 // withhold_kb >= 0: the test hook of GemmShape::withhold_kb (a bounded wait runs out)
+// ---------------------------------------------------------------- dense route (tw_gemm.cu)
+// Every launch below does its work only when *route == 1 (route may be null: always).
+// Gated forward: u = x Wu^T over all T rows, with h = a u at the TwELL's active columns
+// written densely into H [T, I] bf16 and the Hybrid's ELL rows (idx, a, bf16 u) of
+// the rows without a backup slot; backup rows get H = 0.
+cudaError_t gemm_up_hybrid(const uint16_t* x, const uint16_t* Wu, int T, int d, int I, const tw_twell& tw, int R,
+                           const int32_t* backup_slot, uint16_t* H, uint16_t* ell_idx, uint16_t* ell_a,
+                           uint16_t* ell_u, const int32_t* route, int32_t* status, cudaStream_t s);
+// out [M, N] bf16 (row stride ld) = sum over segments of A_s [M, K] (K-major) B_s [K, N]
+// (N contiguous).
+cudaError_t gemm_rows_nmajor_bf16(const uint16_t* const* A, const uint16_t* const* B, int segments, int M, int K,
+                                  int N, uint16_t* out, int ld, const int32_t* route, int32_t* status, cudaStream_t s);
+// Backward: dh = dY Wd^T over all T rows; dG, dU (gated) and H [T, I] bf16 from the
+// saved Hybrid's ELL rows (zeros off the support and on backup rows).
+cudaError_t gemm_dense_grad(const uint16_t* dY, const uint16_t* Wd, int T, int d, int I, const tw_hybrid& h,
+                            bool gated, float l1, uint16_t* dG, uint16_t* dU, uint16_t* H, const int32_t* route,
+                            int32_t* status, cudaStream_t s);
+// D_p = P_p^T Q_p (P [T, I] bf16, Q [T, d] bf16, K = T) for up to three problems,
+// written as fp32 [I, d], or added when *add_if > 0 (the dense backup's part is there).
+struct DenseWeightGradProblem {
+  const uint16_t* P;
+  const uint16_t* Q;
+  float* D;
+};
+cudaError_t gemm_dense_weight_grads(const DenseWeightGradProblem* probs, int n_probs, int T, int I, int d,
+                                    const int32_t* add_if, const int32_t* route, int32_t* status, cudaStream_t s);
+
 cudaError_t gemm_dense_test(const uint16_t* A, const uint16_t* B, int M, int N, int K, int a_mn, int b_mn, float* D,
                             int32_t* status, cudaStream_t s, int withhold_kb = -1);
 

@@ -297,8 +297,11 @@ __global__ void __launch_bounds__(1024) compact_rows_kernel(const uint8_t* __res
                                                             int32_t* __restrict__ list, int list_cap,
                                                             int32_t* __restrict__ count, int32_t* __restrict__ slot_of,
                                                             int32_t* __restrict__ ell_nnz, int cap_check,
-                                                            int32_t* status, int32_t* zero_word) {
+                                                            int32_t* status, int32_t* zero_word, int route_mode,
+                                                            float dense_above, int32_t* route_out) {
   pdl_enter();
+  long long ell_sum = 0;  // row_nnz over the unflagged rows, and their number (the route decision)
+  int ell_rows = 0;
   if (zero_word != nullptr && threadIdx.x == 0) *zero_word = 0;
   __shared__ int warp_tot[2][32];  // by round parity: a round's totals are read while the next round's are written
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -334,6 +337,10 @@ __global__ void __launch_bounds__(1024) compact_rows_kernel(const uint8_t* __res
       sl[b] = f ? (pos < list_cap ? pos : -2) : -1;
       en[b] = f ? 0 : cur.z[b];
       pos += f ? 1 : 0;
+      if (!f && t + b < T) {
+        ell_sum += cur.z[b];
+        ++ell_rows;
+      }
     }
     if (vec_out && t + 3 < T) {
       if (slot_of) *reinterpret_cast<int4*>(slot_of + t) = make_int4(sl[0], sl[1], sl[2], sl[3]);
@@ -352,13 +359,40 @@ __global__ void __launch_bounds__(1024) compact_rows_kernel(const uint8_t* __res
     *count = carry;
     if (carry > cap_check) raise_status(status, TW_ECAPACITY);
   }
+  if (route_out != nullptr) {
+    __shared__ long long sum_w[32];
+    __shared__ int rows_w[32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      ell_sum += __shfl_xor_sync(0xFFFFFFFFu, ell_sum, o);
+      ell_rows += __shfl_xor_sync(0xFFFFFFFFu, ell_rows, o);
+    }
+    if (lane == 0) {
+      sum_w[wid] = ell_sum;
+      rows_w[wid] = ell_rows;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      long long tot = 0;
+      long long nr = 0;
+      for (int w = 0; w < nwarps; ++w) {
+        tot += sum_w[w];
+        nr += rows_w[w];
+      }
+      const bool dense = route_mode == TW_ROUTE_DENSE ||
+                         (route_mode == TW_ROUTE_AUTO && nr > 0 &&
+                          static_cast<double>(tot) > static_cast<double>(dense_above) * static_cast<double>(nr));
+      *route_out = dense ? 1 : 0;
+    }
+  }
 }
 
 cudaError_t launch_compact_rows(const uint8_t* ovf, const int32_t* row_nnz, int R, int T, int32_t* list,
                                 int list_cap, int32_t* count, int32_t* slot_of, int32_t* ell_nnz, int cap_check,
-                                int32_t* status, cudaStream_t s, int32_t* zero_word) {
+                                int32_t* status, cudaStream_t s, int32_t* zero_word, int route_mode,
+                                float dense_above, int32_t* route_out) {
   cudaError_t e = launch(compact_rows_kernel, dim3(1), dim3(1024), 0, s, ovf, row_nnz, R, T, list, list_cap, count,
-                         slot_of, ell_nnz, cap_check, status, zero_word);
+                         slot_of, ell_nnz, cap_check, status, zero_word, route_mode, dense_above, route_out);
   trace_mark(s, "compact_rows");
   return e;
 }

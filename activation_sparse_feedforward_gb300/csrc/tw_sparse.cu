@@ -149,6 +149,7 @@ TW_DEV void scan_counts(const int32_t* __restrict__ col_cnt, int I, int32_t* __r
 // col_cur and writes its record there.
 __global__ void __launch_bounds__(1024) csc_count_scan_kernel(const SparseBwdArgs a, int32_t* ticket, int hist_bins) {
   pdl_enter();
+  if (a.route != nullptr && *a.route == 1) return;  // the call took the dense route
   extern __shared__ int hist[];
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
@@ -227,6 +228,7 @@ TW_DEV int next_chunk(int32_t* sched, int prev, int nwarps, int gwarp) {
 template <bool GATED>
 __global__ void __launch_bounds__(256, 4) ell_weight_grad_kernel(const SparseBwdArgs a) {
   pdl_enter();
+  if (a.route != nullptr && *a.route == 1) return;  // the call took the dense route
   constexpr int U = kWgradUnroll;
   static_assert(32 % U == 0, "the unroll must divide the staging chunk");
   __shared__ float4 stage[8][32];

@@ -206,6 +206,7 @@ __host__ __device__ inline uint32_t token_smem_bytes(int nch, int cap, int ncoef
 template <int NCH, bool GATED, bool HYBRID>
 __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_fwd_kernel(const SparseFwdArgs a) {
   pdl_enter();
+  if (a.route != nullptr && *a.route == 1) return;  // the call took the dense route
   constexpr uint32_t row16 = NCH * 32;  // uint4 per d-row
   extern __shared__ __align__(16) uint8_t tsm[];
   const int lane = threadIdx.x & 31, c = threadIdx.x >> 5;
@@ -386,6 +387,7 @@ __global__ void __launch_bounds__((NCH + 1) * 32, ws_ctas_per_sm(NCH))
   }
   __syncthreads();
   pdl_enter();
+  if (a.route != nullptr && *a.route == 1) return;  // the call took the dense route (uniform over the CTA)
 
   if (warp == NCH) {
     // ------------------------------------------------------------ producer warp
@@ -518,6 +520,7 @@ __global__ void __launch_bounds__((NCH + 1) * 32, ws_ctas_per_sm(NCH))
 template <int NCH, bool GATED>
 __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_bwd_kernel(const SparseBwdArgs a) {
   pdl_enter();
+  if (a.route != nullptr && *a.route == 1) return;  // the call took the dense route
   constexpr uint32_t row16 = NCH * 32;
   constexpr int kPerThread = (kWin + NCH * 32 - 1) / (NCH * 32);  // window entries per thread, at most
   static_assert(rup(kWin, kGroup) == kWin, "a window is whole groups");

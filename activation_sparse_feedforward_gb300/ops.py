@@ -96,9 +96,13 @@ class Hybrid:
     backup_a: torch.Tensor     # [max(cap,1), I] fp32
     backup_u: torch.Tensor | None  # [max(cap,1), I] fp32
     n_backup: torch.Tensor     # [1] int32
+    route: int = _lib.TW_ROUTE_SPARSE
+    dense_above: float = 0.0
+    route_taken: torch.Tensor | None = None  # [1] int32: 0 sparse, 1 dense (written by the forward)
 
     @staticmethod
-    def empty(T: int, I: int, R: int, backup_cap: int, gated: bool, device="cuda") -> "Hybrid":
+    def empty(T: int, I: int, R: int, backup_cap: int, gated: bool, device="cuda", route: str = "sparse",
+              dense_above: float = 64.0) -> "Hybrid":
         cap1 = max(backup_cap, 1)
         return Hybrid(T, I, R, backup_cap,
                       row_nnz=torch.empty(max(T, 1), dtype=torch.int32, device=device),
@@ -110,13 +114,19 @@ class Hybrid:
                       backup_tok=torch.empty(cap1, dtype=torch.int32, device=device),
                       backup_a=torch.empty((cap1, I), dtype=torch.float32, device=device),
                       backup_u=torch.empty((cap1, I), dtype=torch.float32, device=device) if gated else None,
-                      n_backup=torch.zeros(1, dtype=torch.int32, device=device))
+                      n_backup=torch.zeros(1, dtype=torch.int32, device=device),
+                      route=_lib.ROUTES[route], dense_above=float(dense_above),
+                      route_taken=torch.zeros(1, dtype=torch.int32, device=device))
 
     def struct(self) -> _lib.TwHybrid:
         return _lib.TwHybrid(self.T, self.I, self.R, self.backup_cap, _ptr(self.row_nnz), _ptr(self.ell_nnz),
                              _ptr(self.ell_idx), _ptr(self.ell_a), _ptr(self.ell_u), _ptr(self.backup_slot),
                              _ptr(self.backup_tok), _ptr(self.backup_a), _ptr(self.backup_u),
-                             _ptr(self.n_backup))
+                             _ptr(self.n_backup), self.route, self.dense_above, _ptr(self.route_taken))
+
+    def took_dense_route(self) -> bool:
+        """Whether the last forward took the dense route (synchronises)."""
+        return self.route_taken is not None and int(self.route_taken.item()) == 1
 
 
 def _workspace(nbytes: int, device) -> torch.Tensor:
@@ -225,46 +235,100 @@ def twell_ffn_fwd(x, Wg, Wu, Wd, W: int, C: int, ovf_cap: int | None = None):
     return y, f.tw, f.status
 
 
+class HybridScratch:
+    """Buffers several HybridFFN layers can share because each call is done with them
+    when the next layer's call starts on the same stream: the forward and backward
+    workspaces and the y and dx outputs (a layer's y must be consumed, e.g. by a
+    residual add, before the next layer's forward overwrites it). Sized for the
+    largest of the layers it serves."""
+
+    def __init__(self, device="cuda"):
+        self.device = device
+        self.fwd_ws = _workspace(0, device)
+        self.bwd_ws = _workspace(0, device)
+        self.y = None
+        self.dx = None
+
+    def reserve(self, fwd_bytes: int, bwd_bytes: int, T: int, d: int) -> None:
+        if self.fwd_ws.numel() < fwd_bytes:
+            self.fwd_ws = _workspace(fwd_bytes, self.device)
+        if self.bwd_ws.numel() < bwd_bytes:
+            self.bwd_ws = _workspace(bwd_bytes, self.device)
+        if self.y is None or self.y.shape != (T, d):
+            self.y = torch.empty((T, d), dtype=BF16, device=self.device)
+            self.dx = torch.empty((T, d), dtype=BF16, device=self.device)
+
+
 class HybridFFN:
-    """Preallocated training forward + backward through the Hybrid format."""
+    """Preallocated training forward + backward through the Hybrid format.
+
+    route: "sparse" (the pages' CUDA-core gathers for the ELL rows), "dense" (the ELL
+    rows' projections as dense tensor-core GEMMs) or "auto" (decided on the device per
+    forward: dense when the ELL rows' mean nonzeros exceed dense_above). scratch: a
+    HybridScratch shared with other layers (workspaces, y and dx), or None for own
+    buffers."""
 
     def __init__(self, T: int, d: int, I: int, W: int, C: int, R: int, backup_cap: int, gated: bool = True,
-                 device="cuda"):
+                 device="cuda", route: str = "sparse", dense_above: float = 64.0,
+                 scratch: HybridScratch | None = None):
         self.T, self.d, self.I, self.W, self.C, self.R = T, d, I, W, C, R
         self.backup_cap = backup_cap
         self.gated = gated
         L = _lib.load()
-        self.saved = Hybrid.empty(T, I, R, backup_cap, gated, device)
+        self.saved = Hybrid.empty(T, I, R, backup_cap, gated, device, route=route, dense_above=dense_above)
         self._hs = self.saved.struct()
-        self.fwd_ws_bytes = int(L.hybrid_ffn_fwd_workspace_size(T, d, I, W, C, R, backup_cap))
-        self.bwd_ws_bytes = int(L.hybrid_ffn_bwd_workspace_size(T, d, I, R, backup_cap))
-        self.fwd_ws = _workspace(self.fwd_ws_bytes, device)
-        self.bwd_ws = _workspace(self.bwd_ws_bytes, device)
-        self.y = torch.empty((T, d), dtype=BF16, device=device)
-        self.dx = torch.empty((T, d), dtype=BF16, device=device)
+        rc = _lib.ROUTES[route]
+        fwd_bytes = int(L.hybrid_ffn_fwd_workspace_size(T, d, I, W, C, R, backup_cap, rc))
+        bwd_bytes = int(L.hybrid_ffn_bwd_workspace_size(T, d, I, R, backup_cap, rc))
+        self.scratch = scratch
+        if scratch is None:
+            self.fwd_ws = _workspace(fwd_bytes, device)
+            self.bwd_ws = _workspace(bwd_bytes, device)
+            self.y = torch.empty((T, d), dtype=BF16, device=device)
+            self.dx = torch.empty((T, d), dtype=BF16, device=device)
+        else:
+            scratch.reserve(fwd_bytes, bwd_bytes, T, d)
         self.dWg = torch.empty((I, d), dtype=torch.float32, device=device)
         self.dWu = torch.empty((I, d), dtype=torch.float32, device=device) if gated else None
         self.dWd = torch.empty((I, d), dtype=torch.float32, device=device)
         self.status = new_status(device)
 
+    # the buffers a layer may share with others (see HybridScratch)
+    @property
+    def _fwd_ws(self):
+        return self.scratch.fwd_ws if self.scratch is not None else self.fwd_ws
+
+    @property
+    def _bwd_ws(self):
+        return self.scratch.bwd_ws if self.scratch is not None else self.bwd_ws
+
+    @property
+    def _y(self):
+        return self.scratch.y if self.scratch is not None else self.y
+
+    @property
+    def _dx(self):
+        return self.scratch.dx if self.scratch is not None else self.dx
+
     def forward(self, x, Wg, Wu, Wd) -> torch.Tensor:
         _check_bf16("x", x, (self.T, self.d))
         if (Wu is not None) != self.gated:
             raise ValueError("Wu must be given exactly for the gated form")
+        ws, y = self._fwd_ws, self._y
         code = _lib.load().hybrid_ffn_fwd(_ptr(x), _ptr(Wg), _ptr(Wu), _ptr(Wd), self.T, self.d, self.I, self.W,
-                                          self.C, self._hs, _ptr(self.fwd_ws), self.fwd_ws_bytes, _ptr(self.y),
-                                          _ptr(self.status), _stream())
+                                          self.C, self._hs, _ptr(ws), ws.numel(), _ptr(y), _ptr(self.status),
+                                          _stream())
         _lib.check(code, "hybrid_ffn_fwd")
-        return self.y
+        return y
 
     def backward(self, dy, x, Wg, Wu, Wd, l1: float):
         _check_bf16("dy", dy, (self.T, self.d))
+        ws, dx = self._bwd_ws, self._dx
         code = _lib.load().hybrid_ffn_bwd(_ptr(dy), _ptr(x), _ptr(Wg), _ptr(Wu), _ptr(Wd), self.T, self.d, self.I,
-                                          self._hs, float(l1), _ptr(self.dx), _ptr(self.dWg), _ptr(self.dWu),
-                                          _ptr(self.dWd), _ptr(self.bwd_ws), self.bwd_ws_bytes,
-                                          _ptr(self.status), _stream())
+                                          self._hs, float(l1), _ptr(dx), _ptr(self.dWg), _ptr(self.dWu),
+                                          _ptr(self.dWd), _ptr(ws), ws.numel(), _ptr(self.status), _stream())
         _lib.check(code, "hybrid_ffn_bwd")
-        return self.dx, self.dWg, self.dWu, self.dWd
+        return dx, self.dWg, self.dWu, self.dWd
 
 
 def gate_relu_dense(x: torch.Tensor, Wg: torch.Tensor, status: torch.Tensor | None = None) -> torch.Tensor:

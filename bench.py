@@ -38,6 +38,9 @@ if ROOT not in sys.path:
 METRIC = "sparse gated-FFN fwd+bwd input tokens/ms (d2048,I5632) and % of roofline"
 UNIT = "tokens/ms"
 DEFAULT_WORKLOAD = "train_d2048_i5632_m29_o1"
+# the automatic route takes the dense tensor-core path above this many nonzeros per ELL
+# row (the crossover of the two routes measured across the sweep)
+DENSE_ABOVE = 64.0
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -433,27 +436,39 @@ def measure_sweep(dev, flush, stream, steps: int, peaks: dict) -> list:
         inp = make_inputs(spec, with_dy=True)
         x, Wg, Wu, Wd, dy = (None if inp[k] is None else torch.from_numpy(inp[k].view(np.int16)).view(torch.bfloat16).to(dev)
                              for k in ("x", "Wg", "Wu", "Wd", "dy"))
-        h = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, spec.T, gated=spec.gated, device=dev)
+        # backup capacity: the outliers with room to spare (ordinary rows fit the ELL)
+        cap = min(spec.T, 128 * int(math.ceil(1.5 * spec.outlier_frac * spec.T / 128.0)) + 128)
+        row = {"workload": spec.name, "C": spec.C, "R": spec.R, "backup_cap": cap, "dense_above": DENSE_ABOVE}
+        for route in ("auto", "sparse", "dense"):
+            h = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, cap, gated=spec.gated, device=dev,
+                             route=route, dense_above=DENSE_ABOVE)
 
-        def step():
-            h.forward(x, Wg, Wu, Wd)
-            h.backward(dy, x, Wg, Wu, Wd, spec.l1)
+            def step():
+                h.forward(x, Wg, Wu, Wd)
+                h.backward(dy, x, Wg, Wu, Wd, spec.l1)
 
-        ms = _time_steps(step, steps, 3, flush, stream)
-        tw.raise_if_device_error(h.status, spec.name)
-        stats = {"n_backup": int(h.saved.n_backup.item()), "nnz_ell": int(h.saved.ell_nnz.sum().item()),
-                 "nnz": float(h.saved.row_nnz[:spec.T].float().mean().item())}
-        del h
-        torch.cuda.empty_cache()
+            # the sparse route at high activity takes tens of ms a step: fewer steps
+            n = steps if route != "sparse" or spec.mean_active < 200 else 3
+            ms = _time_steps(step, n, 3 if n > 3 else 1, flush, stream)
+            tw.raise_if_device_error(h.status, f"{spec.name} {route}")
+            if route == "auto":
+                stats = {"n_backup": int(h.saved.n_backup.item()), "nnz_ell": int(h.saved.ell_nnz.sum().item()),
+                         "nnz": float(h.saved.row_nnz[:spec.T].float().mean().item())}
+                roof = step_roofline(spec, stats, ms, peaks)
+                row.update({"tokens_per_ms": spec.T / ms, "ms": ms,
+                            "route_taken": "dense" if h.saved.took_dense_route() else "sparse",
+                            "n_backup": stats["n_backup"], "backup_rows_frac": stats["n_backup"] / spec.T,
+                            "nnz_ell": stats["nnz_ell"], "nnz_per_token": stats["nnz"],
+                            "ell_entries_per_ell_row": stats["nnz_ell"] / max(1, spec.T - stats["n_backup"]),
+                            "step_roofline_frac": roof["frac"], "step_roofline_tokens_per_ms": roof["tokens_per_ms"]})
+            else:
+                row[f"{route}_route_tokens_per_ms"] = spec.T / ms
+            del h
+            torch.cuda.empty_cache()
         ms_d = _time_steps(dense_train_step(x, Wg, Wu, Wd, dy, spec.l1), steps, 3, flush, stream)
-        roof = step_roofline(spec, stats, ms, peaks)
-        rows.append({"workload": spec.name, "tokens_per_ms": spec.T / ms, "ms": ms,
-                     "dense_bf16_tokens_per_ms": spec.T / ms_d, "vs_dense": ms_d / ms,
-                     "n_backup": stats["n_backup"], "backup_rows_frac": stats["n_backup"] / spec.T,
-                     "nnz_ell": stats["nnz_ell"],
-                     "nnz_per_token": stats["nnz"],
-                     "ell_entries_per_token": stats["nnz_ell"] / spec.T, "C": spec.C, "R": spec.R,
-                     "step_roofline_frac": roof["frac"], "step_roofline_tokens_per_ms": roof["tokens_per_ms"]})
+        row["dense_bf16_tokens_per_ms"] = spec.T / ms_d
+        row["vs_dense"] = row["tokens_per_ms"] / row["dense_bf16_tokens_per_ms"]
+        rows.append(row)
         del x, Wg, Wu, Wd, dy
         torch.cuda.empty_cache()
     return rows
@@ -484,7 +499,9 @@ def measure_stack(dev, flush, stream, steps: int, n_layers: int = 28, T: int = 8
     torch.cuda.synchronize(dev)
     torch.cuda.reset_peak_memory_stats(dev)
     mem0 = torch.cuda.memory_allocated(dev)
-    ffns = [tw.HybridFFN(T, sp.d, sp.I, sp.W, sp.C, sp.R, cap, gated=True, device=dev) for sp in specs]
+    scratch = tw.HybridScratch(dev)
+    ffns = [tw.HybridFFN(T, sp.d, sp.I, sp.W, sp.C, sp.R, cap, gated=True, device=dev, route="auto",
+                         dense_above=DENSE_ABOVE, scratch=scratch) for sp in specs]
     xs = [None] * n_layers
 
     def fwd():
@@ -512,10 +529,12 @@ def measure_stack(dev, flush, stream, steps: int, n_layers: int = 28, T: int = 8
     for l, f in enumerate(ffns):
         tw.raise_if_device_error(f.status, f"stack layer {l}")
     out = {"layers": n_layers, "tokens": T, "fwd_tokens_per_ms": T / ms_f, "train_tokens_per_ms": T / ms_t,
-           "fwd_ms": ms_f, "train_ms": ms_t,
+           "fwd_ms": ms_f, "train_ms": ms_t, "route": f"auto (dense above {DENSE_ABOVE:g} nonzeros per ELL row)",
+           "routes_taken": ["dense" if f.saved.took_dense_route() else "sparse" for f in ffns],
+           "layer_buffers": "one shared scratch (workspaces, y, dx) for all layers; per layer: saved Hybrid, dW",
            "n_backup": [int(f.saved.n_backup.item()) for f in ffns],
            "nnz_per_token": [round(float(f.saved.row_nnz.float().mean().item()), 2) for f in ffns]}
-    del ffns, xs
+    del ffns, xs, scratch
     torch.cuda.empty_cache()
 
     # dense bf16 stack on the same weights
@@ -580,7 +599,8 @@ def run_ours(args, dist: Dist) -> dict | None:
 
     x, Wg, Wu, Wd, dy = (to_dev(inp[k]) for k in ("x", "Wg", "Wu", "Wd", "dy"))
     backup_cap = min(spec.T, max(128, int(math.ceil(spec.outlier_frac * spec.T * 1.5 / 128.0)) * 128 + 128))
-    h = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, backup_cap, gated=spec.gated, device=dev)
+    h = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, backup_cap, gated=spec.gated, device=dev,
+                     route="auto", dense_above=DENSE_ABOVE)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -593,7 +613,8 @@ def run_ours(args, dist: Dist) -> dict | None:
     torch.cuda.synchronize(dev)
     tw.raise_if_device_error(h.status, "warm-up")
     stats = {"n_backup": int(h.saved.n_backup.item()), "nnz_ell": int(h.saved.ell_nnz.sum().item()),
-             "nnz": int(h.saved.row_nnz[:spec.T].sum().item())}
+             "nnz": int(h.saved.row_nnz[:spec.T].sum().item()),
+             "route": "dense" if h.saved.took_dense_route() else "sparse"}
 
     # kernel trace events (materialised once so their handles exist)
     per_step_cap = 64
@@ -743,7 +764,8 @@ def run_ours(args, dist: Dist) -> dict | None:
     hdy = dy.cpu().pin_memory()
     hy = torch.empty_like(hx).pin_memory()
     hdx = torch.empty_like(hx).pin_memory()
-    hs = [h, tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, backup_cap, gated=spec.gated, device=dev)]
+    hs = [h, tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, backup_cap, gated=spec.gated, device=dev,
+                          route="auto", dense_above=DENSE_ABOVE)]
     xin = [torch.empty_like(x) for _ in range(2)]
     dyin = [torch.empty_like(dy) for _ in range(2)]
     up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -816,7 +838,8 @@ def run_ours(args, dist: Dist) -> dict | None:
     torch.cuda.synchronize(dev)
     torch.cuda.reset_peak_memory_stats(dev)
     m0 = torch.cuda.memory_allocated(dev)
-    h_m = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, backup_cap, gated=spec.gated, device=dev)
+    h_m = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, backup_cap, gated=spec.gated, device=dev,
+                       route="auto", dense_above=DENSE_ABOVE)
     h_m.forward(x, Wg, Wu, Wd)
     h_m.backward(dy, x, Wg, Wu, Wd, spec.l1)
     torch.cuda.synchronize(dev)
@@ -847,7 +870,8 @@ def run_ours(args, dist: Dist) -> dict | None:
                    "step": "hybrid_ffn_fwd + hybrid_ffn_bwd", "l2": "256 MiB flush between steps (untimed)",
                    "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "single GPU"},
         "measured": {"nnz_per_token": stats["nnz"] / spec.T, "nnz_ell": stats["nnz_ell"],
-                     "n_backup": stats["n_backup"]},
+                     "n_backup": stats["n_backup"], "route_taken": stats["route"],
+                     "route": f"auto (dense above {DENSE_ABOVE:g} nonzeros per ELL row)"},
         "roofline": roofline,
         "step_roofline": step_roof,
         "e2e": e2e,

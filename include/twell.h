@@ -120,7 +120,32 @@ typedef struct {
   float* backup_a;
   float* backup_u;
   int32_t* n_backup;
+  int32_t route;          /* how the ELL rows' projections run: TW_ROUTE_* below */
+  float dense_above;      /* TW_ROUTE_AUTO: the dense route when the ELL rows' mean
+                             number of nonzeros exceeds this */
+  int32_t* route_taken;   /* device int32: the forward writes the route it took (0 sparse,
+                             1 dense); the backward takes the same one. May be NULL only
+                             with TW_ROUTE_SPARSE */
 } tw_hybrid;
+
+/* Routes of the Hybrid's ELL rows (the backup rows always take the dense tensor-core
+ * path with split fp32 operands):
+ *  TW_ROUTE_SPARSE  the pages' method: CUDA-core gathers over the active neurons only
+ *                   (explainer 2.B "Training Kernels", "Backpropagation");
+ *  TW_ROUTE_DENSE   the ELL rows' up / down projections and their backward as dense
+ *                   bf16 tensor-core GEMMs over all neurons, with the TwELL / Hybrid
+ *                   masks applied in the GEMM epilogues (h, dg, du are rounded once to
+ *                   bf16, as in a dense bf16 FFN); the saved Hybrid is the same;
+ *  TW_ROUTE_AUTO    decided on the device by each forward, after the gate kernel: dense
+ *                   when the ELL rows' mean nonzeros per row exceeds dense_above. A
+ *                   row's gathers cost L2 traffic in proportion to its nonzeros, the
+ *                   dense GEMMs a fixed amount, so above some activity the dense route
+ *                   is faster; the tunx.ai announcement calls the dense backup a
+ *                   "safety valve" for high activity, and this extends it to a whole
+ *                   call. */
+#define TW_ROUTE_SPARSE 0
+#define TW_ROUTE_DENSE 1
+#define TW_ROUTE_AUTO 2
 
 /* Human-readable name of a tw_status code. */
 const char* tw_status_str(int status);
@@ -223,8 +248,9 @@ tw_status twell_ffn_fwd_fixed_scratch(const uint16_t* x, const uint16_t* Wg, con
                                       int ovf_cap, const tw_twell* tw, uint16_t* y,
                                       int32_t* dev_status, void* stream);
 
-/* Workspace bytes hybrid_ffn_fwd needs. */
-size_t hybrid_ffn_fwd_workspace_size(int T, int d, int I, int W, int C, int R, int backup_cap);
+/* Workspace bytes hybrid_ffn_fwd needs for a Hybrid with the given route (any route
+ * other than TW_ROUTE_SPARSE adds the dense route's [T, I] bf16 hidden matrix). */
+size_t hybrid_ffn_fwd_workspace_size(int T, int d, int I, int W, int C, int R, int backup_cap, int route);
 
 /* Training forward (explainer 2.B "Training Kernels"): gate+pack into TwELL,
  * conversion of TwELL into the Hybrid *saved (sizes taken from saved->R and
@@ -236,8 +262,9 @@ tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* 
                          const tw_hybrid* saved, void* ws, size_t ws_bytes,
                          uint16_t* y, int32_t* dev_status, void* stream);
 
-/* Workspace bytes hybrid_ffn_bwd needs. */
-size_t hybrid_ffn_bwd_workspace_size(int T, int d, int I, int R, int backup_cap);
+/* Workspace bytes hybrid_ffn_bwd needs (routes other than TW_ROUTE_SPARSE add the
+ * dense route's [T, I] bf16 dG, dU and h). */
+size_t hybrid_ffn_bwd_workspace_size(int T, int d, int I, int R, int backup_cap, int route);
 
 /* Training backward over the saved Hybrid (explainer 2.B "Backpropagation"):
  * gradient of L = sum(dy * y) + l1 * sum(a):

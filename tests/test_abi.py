@@ -42,7 +42,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.tw_abi_version() == 1
+    assert lib.tw_abi_version() == 2
     for code in range(9):
         assert lib.tw_status_str(code).decode().startswith("TW_")
 
@@ -102,10 +102,10 @@ def test_workspace_sizes_grow_with_capacity(lib):
     a = lib.twell_ffn_fwd_workspace_size(16384, 2048, 5632, 128, 16, 0)
     b = lib.twell_ffn_fwd_workspace_size(16384, 2048, 5632, 128, 16, 200)
     assert b - a >= 256 * (2048 + 5632) * 2
-    h0 = lib.hybrid_ffn_fwd_workspace_size(16384, 2048, 5632, 128, 16, 64, 0)
+    h0 = lib.hybrid_ffn_fwd_workspace_size(16384, 2048, 5632, 128, 16, 64, 0, 0)
     assert h0 >= 16384 * 44 * (2 + 16 * 3)
-    assert lib.hybrid_ffn_bwd_workspace_size(16384, 2048, 5632, 64, 256) > \
-        lib.hybrid_ffn_bwd_workspace_size(16384, 2048, 5632, 64, 0)
+    assert lib.hybrid_ffn_bwd_workspace_size(16384, 2048, 5632, 64, 256, 0) > \
+        lib.hybrid_ffn_bwd_workspace_size(16384, 2048, 5632, 64, 0, 0)
 
 
 def test_package_fails_loudly_without_library(monkeypatch, tmp_path):

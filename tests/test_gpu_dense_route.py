@@ -1,0 +1,141 @@
+"""GPU parity of the dense route of the Hybrid training step: the ELL rows' up and
+down projections and their backward as dense tensor-core GEMMs over all neurons,
+with the TwELL / Hybrid masks applied in the GEMM epilogues, against the fp64
+oracle at the usual tolerances; the saved Hybrid equals the sparse route's; the
+automatic route is decided on the device from the ELL rows' mean activity."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import activation_sparse_feedforward_gb300 as tw  # noqa: E402
+from gpu_util import assert_close, bits_of, f64_of, to_dev  # noqa: E402
+from oracle import ffn  # noqa: E402
+from synthetic import FFNSpec, WORKLOADS, make_inputs  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    tw.load()
+
+
+CASES = [
+    FFNSpec("dense_gated", T=777, d=512, I=1280, mean_active=40, outlier_frac=0.03, W=128, C=16, R=96, seed=21),
+    FFNSpec("dense_nongated", T=600, d=768, I=1024, gated=False, mean_active=30, outlier_frac=0.02, W=64, C=8,
+            R=64, seed=22),
+    # I = 704: 64-wide column tiles in the up and grad GEMMs; d = 2048
+    FFNSpec("dense_i704_d2048", T=300, d=2048, I=704, mean_active=20, outlier_frac=0.02, W=64, C=8, R=48, seed=23),
+    # long ELL rows (the grad epilogue's row search and walk over many entries per tile)
+    FFNSpec("dense_long_rows", T=513, d=512, I=1280, mean_active=200, outlier_frac=0.02, W=128, C=40, R=320,
+            seed=24),
+]
+
+
+def _dev(inp):
+    return {k: to_dev(v) for k, v in inp.items() if k in ("x", "Wg", "Wu", "Wd", "dy")}
+
+
+def _step(spec, dv, route, l1, backup_cap, dense_above=64.0):
+    h = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, backup_cap, gated=spec.gated, route=route,
+                     dense_above=dense_above)
+    y = h.forward(dv["x"], dv["Wg"], dv["Wu"], dv["Wd"]).clone()
+    grads = [None if g is None else g.clone()
+             for g in h.backward(dv["dy"], dv["x"], dv["Wg"], dv["Wu"], dv["Wd"], l1)]
+    torch.cuda.synchronize()
+    tw.raise_if_device_error(h.status, f"{route} route")
+    return h, y, grads
+
+
+def _check_oracle(spec, inp, y, grads, l1, rows=None):
+    dx, dWg, dWu, dWd = grads
+    x, dyi = (inp["x"], inp["dy"]) if rows is None else (inp["x"][rows], inp["dy"][rows])
+    f = ffn.forward(x, inp["Wg"], inp["Wu"], inp["Wd"])
+    b = ffn.backward(x, inp["Wg"], inp["Wu"], inp["Wd"], dyi, l1, fwd=f)
+    yy, dd = (f64_of(y), f64_of(dx)) if rows is None else (f64_of(y)[rows], f64_of(dx)[rows])
+    assert_close(yy, f["y"], "y")
+    assert_close(dd, b["dx"], "dx")
+    if rows is None:
+        assert_close(dWg.cpu().numpy(), b["dWg"], "dWg")
+        assert_close(dWd.cpu().numpy(), b["dWd"], "dWd")
+        if spec.gated:
+            assert_close(dWu.cpu().numpy(), b["dWu"], "dWu")
+
+
+@pytest.mark.parametrize("spec", CASES, ids=lambda s: s.name)
+@pytest.mark.parametrize("l1", [2e-5, 0.05])
+def test_dense_route_matches_oracle(spec, l1):
+    inp = make_inputs(spec, with_dy=True)
+    h, y, grads = _step(spec, _dev(inp), "dense", l1, spec.T // 4)
+    assert h.saved.took_dense_route()
+    assert 0 < int(h.saved.n_backup.item()) <= spec.T // 4
+    _check_oracle(spec, inp, y, grads, l1)
+
+
+@pytest.mark.parametrize("spec", CASES[:2], ids=lambda s: s.name)
+def test_dense_route_without_backup_capacity_rows(spec):
+    """No backup rows: the dense weight-gradient GEMM writes dW instead of adding."""
+    spec = spec.with_(outlier_frac=0.0, R=spec.I)
+    inp = make_inputs(spec, with_dy=True)
+    h, y, grads = _step(spec, _dev(inp), "dense", spec.l1, 0)
+    assert int(h.saved.n_backup.item()) == 0
+    _check_oracle(spec, inp, y, grads, spec.l1)
+
+
+@pytest.mark.parametrize("spec", CASES, ids=lambda s: s.name)
+def test_dense_route_saves_the_sparse_routes_hybrid(spec):
+    inp = make_inputs(spec, with_dy=True)
+    dv = _dev(inp)
+    hs, ys, gs = _step(spec, dv, "sparse", spec.l1, spec.T // 4)
+    hd, yd, gd = _step(spec, dv, "dense", spec.l1, spec.T // 4)
+    for name in ("row_nnz", "ell_nnz", "backup_slot", "n_backup"):
+        assert torch.equal(getattr(hs.saved, name), getattr(hd.saved, name)), name
+    nb = int(hs.saved.n_backup.item())
+    assert torch.equal(hs.saved.backup_tok[:nb], hd.saved.backup_tok[:nb])
+    n = hs.saved.ell_nnz[:spec.T].long()
+    valid = (torch.arange(spec.R, device="cuda")[None, :] < n[:, None]).cpu().numpy()
+    for name in ("ell_idx", "ell_a"):
+        np.testing.assert_array_equal(bits_of(getattr(hs.saved, name))[valid], bits_of(getattr(hd.saved, name))[valid])
+    if spec.gated:
+        # u: the same fp32 dot product summed in another order, rounded to bf16 once
+        us = ffn.bf16_to_f64(bits_of(hs.saved.ell_u)[valid])
+        ud = ffn.bf16_to_f64(bits_of(hd.saved.ell_u)[valid])
+        assert np.all(np.abs(us - ud) <= 2.0 ** -7 * np.abs(us) + 1e-30)
+    # the two routes' outputs agree with each other as closely as each with the oracle
+    assert_close(f64_of(yd), f64_of(ys), "y: dense vs sparse route")
+    assert_close(f64_of(gd[0]), f64_of(gs[0]), "dx: dense vs sparse route")
+
+
+@pytest.mark.parametrize("dense_above,expect_dense", [(10.0, True), (1000.0, False)])
+def test_auto_route_is_decided_on_the_device(dense_above, expect_dense):
+    spec = CASES[0]                                   # ELL rows hold ~40 nonzeros on average
+    inp = make_inputs(spec, with_dy=True)
+    h, y, grads = _step(spec, _dev(inp), "auto", spec.l1, spec.T // 4, dense_above=dense_above)
+    assert h.saved.took_dense_route() == expect_dense
+    ell = h.saved.ell_nnz[:spec.T].float()
+    rows = (h.saved.backup_slot[:spec.T] == -1)
+    mean = float(ell[rows].mean())
+    assert (mean > dense_above) == expect_dense
+    _check_oracle(spec, inp, y, grads, spec.l1)
+
+
+@pytest.mark.parametrize("name,backup_cap", [("train_d2048_i5632_m108_o5", 1280),
+                                             ("train_d2048_i5632_m911_o1", 512)])
+def test_dense_route_full_size_sampled(name, backup_cap):
+    spec = WORKLOADS[name]
+    inp = make_inputs(spec, with_dy=True)
+    h, y, grads = _step(spec, _dev(inp), "dense", spec.l1, backup_cap)
+    assert h.saved.took_dense_route()
+    nb = int(h.saved.n_backup.item())
+    assert len(inp["outliers"]) <= nb <= backup_cap
+    rows = np.unique(np.concatenate([np.arange(7, spec.T, 1031), inp["outliers"][:10], [spec.T - 1]]))
+    _check_oracle(spec, inp, y, grads, spec.l1, rows=rows)
+    J = np.array([0, 3, 999, 2048, 4095, 5631])
+    r = ffn.backward_weight_rows(inp["x"], inp["Wg"], inp["Wu"], inp["Wd"], inp["dy"], spec.l1, J)
+    dx, dWg, dWu, dWd = grads
+    assert_close(dWg[J].cpu().numpy(), r["dWg"], "dWg (sampled neurons)")
+    assert_close(dWu[J].cpu().numpy(), r["dWu"], "dWu (sampled neurons)")
+    assert_close(dWd[J].cpu().numpy(), r["dWd"], "dWd (sampled neurons)")

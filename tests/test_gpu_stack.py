@@ -28,7 +28,11 @@ def _bf16_sum(a_bits, b_f64):
     return round_to_bf16_bits((ffn.bf16_to_f64(a_bits) + ffn.bf16_to_f64(b_bits)).astype(np.float32))
 
 
-def test_residual_stack_matches_oracle():
+@pytest.mark.parametrize("route,shared", [("sparse", False), ("auto", True)], ids=["sparse", "auto_shared_scratch"])
+def test_residual_stack_matches_oracle(route, shared):
+    """With the automatic route the two middle layers (ELL rows of ~13-15 nonzeros, above
+    the threshold of 8) take the dense route and the outer ones (~2) the sparse route;
+    with a shared scratch every layer uses the same workspaces and y / dx buffers."""
     # four layers sampling the 28-layer activity profile (rising, plateau, falling)
     specs = [stack_layer_spec(l, T=300, d=256, I=704, W=64, C=8, profile_layer=p)
              for l, p in enumerate((0, 9, 18, 27))]
@@ -37,9 +41,11 @@ def test_residual_stack_matches_oracle():
     # ---------------------------------------------------------------- library
     x = to_dev(st["x0"])
     layers, xs = [], []
+    scratch = tw.HybridScratch() if shared else None
     for sp, w in zip(specs, st["layers"]):
         W = {k: to_dev(v) for k, v in w.items()}
-        h = tw.HybridFFN(sp.T, sp.d, sp.I, sp.W, sp.C, sp.R, sp.T // 4, gated=True)
+        h = tw.HybridFFN(sp.T, sp.d, sp.I, sp.W, sp.C, sp.R, sp.T // 4, gated=True, route=route, dense_above=8.0,
+                         scratch=scratch)
         y = h.forward(x, W["Wg"], W["Wu"], W["Wd"])
         xs.append(x)
         layers.append((h, W))
@@ -56,6 +62,8 @@ def test_residual_stack_matches_oracle():
     for h, _ in layers:
         tw.raise_if_device_error(h.status)
         assert int(h.saved.n_backup.item()) >= 3   # the outlier tokens stay outliers up the stack
+    if route == "auto":
+        assert [h.saved.took_dense_route() for h, _ in layers] == [False, True, True, False]
     # ---------------------------------------------------------------- oracle
     xo = st["x0"]
     xos, fs = [], []
