@@ -163,7 +163,9 @@ struct HybBwdWs {
   tw::BackupGradOut g;  // dG, dU, H as (hi, lo) bf16 pairs
   float* acc;           // split-K accumulator of dx for the backup rows [ra, d]
   int32_t* sched;       // token scheduling counter of the token pass
-  uint16_t *dGd, *dUd, *Hd;  // dense route: dg, du, h of every row [T, I] (null for the sparse route)
+  uint16_t *dGd, *dUd, *Hd;  // dense route: fp16 dg, du, h of every row [T, I] (null for the sparse route)
+  uint16_t *Wg16, *Wu16;     // dense route: fp16 copies of the weights [I, d] (the dx GEMM's operands)
+  uint16_t *X16, *dY16;      // and of x and dy [T, d] (the weight-gradient GEMMs' operands)
 };
 HybBwdWs carve_hybrid_bwd(Carve& c, int T, int d, int I, int R, int backup_cap, int route) {
   const size_t TR = static_cast<size_t>(T) * R;
@@ -189,8 +191,12 @@ HybBwdWs carve_hybrid_bwd(Carve& c, int T, int d, int I, int R, int backup_cap, 
     w.dGd = c.take<uint16_t>(TI);
     w.dUd = c.take<uint16_t>(TI);
     w.Hd = c.take<uint16_t>(TI);
+    w.Wg16 = c.take<uint16_t>(static_cast<size_t>(I) * d);
+    w.Wu16 = c.take<uint16_t>(static_cast<size_t>(I) * d);
+    w.X16 = c.take<uint16_t>(static_cast<size_t>(T) * d);
+    w.dY16 = c.take<uint16_t>(static_cast<size_t>(T) * d);
   } else {
-    w.dGd = w.dUd = w.Hd = nullptr;
+    w.dGd = w.dUd = w.Hd = w.Wg16 = w.Wu16 = w.X16 = w.dY16 = nullptr;
   }
   return w;
 }
@@ -510,12 +516,18 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
   const bool sparse_possible = route != TW_ROUTE_DENSE || T == 0;
   if (sparse_possible) TW_TRY(tw::launch_sparse_bwd_tokens(a, s));
   if (dense_possible) {
-    // the dense route: dg, du, h of every ELL row from dh = dY Wd^T on the tensor
-    // cores, then dx = dg Wg + du Wu over all rows (the backup rows' dx follows below)
+    // the dense route: dg, du, h of every ELL row (fp16) from dh = dY Wd^T on the
+    // tensor cores, then dx = dg Wg + du Wu over all rows on fp16 operands (the backup
+    // rows' dx follows below)
+    const uint16_t* src[4] = {Wg, x, dy, Wu};
+    uint16_t* dst[4] = {w.Wg16, w.X16, w.dY16, w.Wu16};
+    const size_t n[4] = {static_cast<size_t>(I) * d, static_cast<size_t>(T) * d, static_cast<size_t>(T) * d,
+                         static_cast<size_t>(I) * d};
+    TW_TRY(tw::launch_to_f16(src, dst, n, gated ? 4 : 3, taken, s));
     TW_TRY(tw::gemm_dense_grad(dy, Wd, T, d, I, *saved, gated, l1, w.dGd, w.dUd, w.Hd, taken, dev_status, s));
     const uint16_t* A[2] = {w.dGd, w.dUd};
-    const uint16_t* B[2] = {Wg, Wu};
-    TW_TRY(tw::gemm_rows_nmajor_bf16(A, B, gated ? 2 : 1, T, I, d, dx, d, taken, dev_status, s));
+    const uint16_t* B[2] = {w.Wg16, w.Wu16};
+    TW_TRY(tw::gemm_rows_nmajor_bf16(A, B, gated ? 2 : 1, T, I, d, dx, d, taken, dev_status, s, true));
   }
   const bool backup = cap > 0 && T > 0;
   if (backup) {
@@ -543,7 +555,7 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
   if (dense_possible) {
     // dense route weight gradients over all rows (the backup rows' dg, du, h are 0 in
     // these operands): added to the backup rows' part when there is one
-    const tw::DenseWeightGradProblem probs[3] = {{w.dGd, x, dWg}, {w.Hd, dy, dWd}, {w.dUd, x, dWu}};
+    const tw::DenseWeightGradProblem probs[3] = {{w.dGd, w.X16, dWg}, {w.Hd, w.dY16, dWd}, {w.dUd, w.X16, dWu}};
     TW_TRY(tw::gemm_dense_weight_grads(probs, gated ? 3 : 2, T, I, d, backup ? saved->n_backup : nullptr, taken,
                                        dev_status, s));
   }

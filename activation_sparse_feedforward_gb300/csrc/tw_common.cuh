@@ -9,6 +9,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -71,6 +72,14 @@ TW_DEV uint32_t pack_bf16x2(float lo, float hi) {
 TW_DEV uint32_t pack_bf16x2_rn(float lo, float hi) {
   const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&b);
+}
+// fp16 (IEEE binary16) bits: the Hybrid's stored u and the dense route's backward
+// operands, which need 11 significant bits where bf16 has 8
+TW_DEV uint16_t f32_to_f16(float v) { return __half_as_ushort(__float2half_rn(v)); }
+TW_DEV float f16_to_f32(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+TW_DEV uint32_t pack_f16x2_rn(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // ------------------------------------------------------------------ packed fp32 pairs
@@ -241,11 +250,12 @@ TW_DEV uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo
   return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, fp32 D.
-//  bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format (1 = bf16),
+// Instruction descriptor of tcgen05.mma kind::f16: A and B both bf16 (or, with f16,
+// both fp16), fp32 D.
+//  bits 4-5 D format (1 = f32), 7-9 A format and 10-12 B format (0 = f16, 1 = bf16),
 //  bit 15 A major (1 = MN), bit 16 B major (1 = MN), bits 17-22 N >> 3, bits 24-28 M >> 4.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn, bool f16 = false) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) | (static_cast<uint32_t>(a_mn) << 15) |
          (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }

@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(256) hybrid_fill_kernel(const uint16_t* __rest
             if (off < h.R) {  // an ELL row has at most R nonzeros; the bound keeps stores inside the row
               h.ell_idx[rb + off] = static_cast<uint16_t>(col + i);
               h.ell_a[rb + off] = elem8(v, i);
-              if (urow != nullptr) h.ell_u[rb + off] = elem8(w, i);
+              if (urow != nullptr) h.ell_u[rb + off] = f32_to_f16(bf16_to_f32(elem8(w, i)));
             }
             ++off;
           }
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(256) hybrid_unpack_kernel(const tw_hybrid h, f
       const int j = h.ell_idx[rb + s];
       if (j >= I) continue;  // not a column of this matrix: nothing to write
       A[static_cast<size_t>(t) * I + j] = bf16_to_f32(h.ell_a[rb + s]);
-      if (U != nullptr) U[static_cast<size_t>(t) * I + j] = bf16_to_f32(h.ell_u[rb + s]);
+      if (U != nullptr) U[static_cast<size_t>(t) * I + j] = f16_to_f32(h.ell_u[rb + s]);
     }
   }
 }

@@ -270,7 +270,7 @@ cudaError_t gemm_up_hybrid(const uint16_t* x, const uint16_t* Wu, int T, int d, 
 
 cudaError_t gemm_rows_nmajor_bf16(const uint16_t* const* A, const uint16_t* const* B, int segments, int M, int K,
                                   int N, uint16_t* out, int ld, const int32_t* route, int32_t* status,
-                                  cudaStream_t s) {
+                                  cudaStream_t s, bool f16) {
   if (M == 0) return cudaSuccess;
   if (segments < 1 || segments > GEMM_MAX_SEGMENTS || N % 256 != 0) return cudaErrorInvalidValue;
   GemmShape sh = shape_static(M, N, K, status);
@@ -282,6 +282,7 @@ cudaError_t gemm_rows_nmajor_bf16(const uint16_t* const* A, const uint16_t* cons
       return cudaErrorInvalidValue;
   fill_unused(maps, segments, segments);
   EpiStoreBf16::Params ep{out, ld};
+  if (f16) return run_gemm<256, false, true, false, 4, F16Operands<EpiStoreBf16>>(maps, sh, ep, M, s, "dense_rows_gemm");
   return run_gemm<256, false, true, false, 4, EpiStoreBf16>(maps, sh, ep, M, s, "dense_rows_gemm");
 }
 
@@ -334,8 +335,8 @@ cudaError_t gemm_dense_weight_grads(const DenseWeightGradProblem* probs, int n_p
   ep.ldd = d;
   ep.rows_per_problem = (I + GEMM_BM - 1) / GEMM_BM * GEMM_BM;
   ep.add_if = add_if;
-  return run_gemm<256, true, true, false, 4, EpiF32GroupedStoreOrAdd>(maps, sh, ep, ep.rows_per_problem * n_probs, s,
-                                                                      "dense_weight_grad");
+  return run_gemm<256, true, true, false, 4, F16Operands<EpiF32GroupedStoreOrAdd>>(
+      maps, sh, ep, ep.rows_per_problem * n_probs, s, "dense_weight_grad");
 }
 
 // ------------------------------------------------------------------ layout test GEMM

@@ -85,10 +85,18 @@ struct epi_overlaps_loads : std::false_type {};
 template <class E>
 struct epi_overlaps_loads<E, std::void_t<decltype(E::kOverlapLoads)>> : std::bool_constant<E::kOverlapLoads> {};
 
+// An epilogue wrapped in F16Operands<> runs its GEMM on fp16 operands (A and B both
+// fp16; the tensor maps copy the bits as they are): the dense route's backward, whose
+// operands need 11 significant bits.
+template <class E, class = void>
+struct epi_f16_operands : std::false_type {};
+template <class E>
+struct epi_f16_operands<E, std::void_t<decltype(E::kF16Operands)>> : std::bool_constant<E::kF16Operands> {};
+
 // NA = 2 pairs the segments: segments 2i and 2i + 1 share one B operand (b[2i]), so
 // a stage holds both A tiles and one B tile, and both products go into the same
 // accumulator (the hi / lo halves of a split fp32 operand against one weight).
-template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES, int NA = 1>
+template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES, int NA = 1, bool F16 = false>
 struct GemmTraits {
   static constexpr int NB = DUAL ? 2 : 1;
   static constexpr int A_BYTES = GEMM_BM * GEMM_BK * 2;
@@ -96,7 +104,7 @@ struct GemmTraits {
   static constexpr int STAGE_BYTES = NA * A_BYTES + NB * B_BYTES;
   static constexpr int ACC_COLS = BN * NB;
   static constexpr int TMEM_COLS = 2 * ACC_COLS;
-  static constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, BN, A_MN, B_MN);
+  static constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, BN, A_MN, B_MN, F16);
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64, 128, 192 or 256");
@@ -110,7 +118,7 @@ template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES, class Epi, int NA
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ GemmMaps maps, const GemmShape shape,
                    const __grid_constant__ typename Epi::Params ep) {
-  using Tr = GemmTraits<BN, A_MN, B_MN, DUAL, STAGES, NA>;
+  using Tr = GemmTraits<BN, A_MN, B_MN, DUAL, STAGES, NA, epi_f16_operands<Epi>::value>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
   uint8_t* tiles = smem_raw + pad;
@@ -476,6 +484,13 @@ struct EpiStoreF32Grouped {
   TW_DEV void finish() {}
 };
 
+// Any epilogue, with its GEMM run on fp16 operands.
+template <class E>
+struct F16Operands : E {
+  static constexpr bool kF16Operands = true;
+  using E::E;
+};
+
 // EpiStoreF32Grouped that adds instead of storing when *add_if (a device count, read
 // once a thread) is positive: the dense route's weight gradients, added to the dense
 // backup rows' part when there are backup rows, else written.
@@ -541,7 +556,7 @@ struct EpiStoreBf16 {
 // a row served here never overflowed, so its slots hold all its nonzeros) the
 // epilogue forms h = a u at the active columns and writes
 //   H[m][:]        bf16(h) at active columns, 0 elsewhere (the down GEMM's operand),
-//   the ELL row    global index, a and bf16(u) per nonzero, at the row's ELL offset
+//   the ELL row    global index, a and fp16(u) per nonzero, at the row's ELL offset
 //                  (the nonzeros of the row's tiles before this CTA tile),
 // the same ELL the sparse route's token kernel writes. Rows of the dense backup
 // (backup_slot != -1) get H = 0 and no ELL entries.
@@ -620,7 +635,7 @@ struct EpiUpHybrid {
       if (TW_CHECKED(off < p.R, p.status)) {
         p.ell_idx[rb + off] = static_cast<uint16_t>(col0 + i);
         p.ell_a[rb + off] = ab;
-        p.ell_u[rb + off] = f32_to_bf16(u);
+        p.ell_u[rb + off] = f32_to_f16(u);
       }
       ++off;
     }
@@ -641,8 +656,11 @@ struct EpiUpHybrid {
 // columns [n0, n0 + BN). The row's saved ELL entries (global index ascending, a, u)
 // give the support; on it
 //   dg = dh u + l1 (non-gated: dh + l1),  du = dh a,  h = a u (non-gated: a),
-// and the epilogue writes bf16 dG, dU (gated) and H over the tile's columns, 0 off
-// the support, as the operands of the dx and weight-gradient GEMMs. Rows of the dense
+// and the epilogue writes fp16 dG, dU (gated) and H over the tile's columns, 0 off
+// the support, as the operands of the dx and weight-gradient GEMMs (run on fp16: a
+// weight-gradient element sums thousands of these products at high activity, and
+// bf16's 8 significant bits then leave errors above the parity bound where the sum
+// cancels). Rows of the dense
 // backup get zeros (their gradients come from the backup GEMMs). The entries of a
 // chunk are placed in the thread's staging row (a at column i, u at 32 + i; stride
 // kGradStride, odd) and read back by column.
@@ -703,7 +721,7 @@ struct EpiDenseGrad {
         const int i = j - col0;
         if (!TW_CHECKED(i >= 0, p.status)) continue;
         mine[i] = bf16_to_f32(p.ell_a[rb + cur]);
-        if (GATED) mine[32 + i] = bf16_to_f32(p.ell_u[rb + cur]);
+        if (GATED) mine[32 + i] = f16_to_f32(p.ell_u[rb + cur]);
         mask |= 1u << i;
       }
     }
@@ -722,9 +740,9 @@ struct EpiDenseGrad {
         u2[e] = act ? d * a : 0.f;
         h2[e] = GATED ? a * u : a;
       }
-      wg[q] = pack_bf16x2_rn(g2[0], g2[1]);
-      wu[q] = pack_bf16x2_rn(u2[0], u2[1]);
-      wh[q] = pack_bf16x2_rn(h2[0], h2[1]);
+      wg[q] = pack_f16x2_rn(g2[0], g2[1]);
+      wu[q] = pack_f16x2_rn(u2[0], u2[1]);
+      wh[q] = pack_f16x2_rn(h2[0], h2[1]);
     }
     uint4* dg = reinterpret_cast<uint4*>(p.dG + o);
     uint4* hh = reinterpret_cast<uint4*>(p.H + o);

@@ -28,6 +28,10 @@ void trace_mark(cudaStream_t s, const char* label);
 // Zeroes [p0, p0 + b0) and [p1, p1 + b1) (16-byte aligned starts, any sizes; p1 may
 // be null) with one kernel, followed by a trace mark.
 cudaError_t launch_zero(void* p0, size_t b0, void* p1, size_t b1, cudaStream_t s);
+// bf16 -> fp16 conversion of up to four tensors of n[k] elements (multiples of 8),
+// only when *route == 1 (route may be null): the dense route backward's operands.
+cudaError_t launch_to_f16(const uint16_t* const* src, uint16_t* const* dst, const size_t* n, int count,
+                          const int32_t* route, cudaStream_t s);
 // fp32 FMA throughput probe (tw_kernels.cu): blocks x 256 threads, `iters` steps;
 // out holds blocks * 256 floats
 cudaError_t launch_fma_probe(float* out, int blocks, int iters, cudaStream_t s);
@@ -242,15 +246,16 @@ cudaError_t gemm_up_hybrid(const uint16_t* x, const uint16_t* Wu, int T, int d, 
                            const int32_t* backup_slot, uint16_t* H, uint16_t* ell_idx, uint16_t* ell_a,
                            uint16_t* ell_u, const int32_t* route, int32_t* status, cudaStream_t s);
 // out [M, N] bf16 (row stride ld) = sum over segments of A_s [M, K] (K-major) B_s [K, N]
-// (N contiguous).
+// (N contiguous); operands bf16, or fp16 when f16.
 cudaError_t gemm_rows_nmajor_bf16(const uint16_t* const* A, const uint16_t* const* B, int segments, int M, int K,
-                                  int N, uint16_t* out, int ld, const int32_t* route, int32_t* status, cudaStream_t s);
-// Backward: dh = dY Wd^T over all T rows; dG, dU (gated) and H [T, I] bf16 from the
+                                  int N, uint16_t* out, int ld, const int32_t* route, int32_t* status, cudaStream_t s,
+                                  bool f16 = false);
+// Backward: dh = dY Wd^T over all T rows; dG, dU (gated) and H [T, I] fp16 from the
 // saved Hybrid's ELL rows (zeros off the support and on backup rows).
 cudaError_t gemm_dense_grad(const uint16_t* dY, const uint16_t* Wd, int T, int d, int I, const tw_hybrid& h,
                             bool gated, float l1, uint16_t* dG, uint16_t* dU, uint16_t* H, const int32_t* route,
                             int32_t* status, cudaStream_t s);
-// D_p = P_p^T Q_p (P [T, I] bf16, Q [T, d] bf16, K = T) for up to three problems,
+// D_p = P_p^T Q_p (P [T, I] fp16, Q [T, d] fp16, K = T) for up to three problems,
 // written as fp32 [I, d], or added when *add_if > 0 (the dense backup's part is there).
 struct DenseWeightGradProblem {
   const uint16_t* P;

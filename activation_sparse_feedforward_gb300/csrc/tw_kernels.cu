@@ -81,6 +81,53 @@ cudaError_t launch_zero(void* p0, size_t b0, void* p1, size_t b1, cudaStream_t s
   return e;
 }
 
+// ---------------------------------------------------------------- bf16 -> fp16
+// Up to four tensors converted element by element, round to nearest even (exact for
+// magnitudes in fp16's normal range, 2^-14 to 65504; smaller ones become fp16
+// subnormals, larger ones infinity). Only when *route == 1 (route may be null).
+struct ToF16Args {
+  const uint16_t* src[4];
+  uint16_t* dst[4];
+  size_t n8[4];  // elements / 8
+  int count;
+  const int32_t* route;
+};
+__global__ void __launch_bounds__(256) to_f16_kernel(const ToF16Args a) {
+  pdl_enter();
+  if (a.route != nullptr && *a.route != 1) return;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (int k = 0; k < a.count; ++k) {
+    const uint4* s = reinterpret_cast<const uint4*>(a.src[k]);
+    uint4* d = reinterpret_cast<uint4*>(a.dst[k]);
+    for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < a.n8[k]; i += stride) {
+      const uint4 v = s[i];
+      d[i] = make_uint4(pack_f16x2_rn(bf16_lo(v.x), bf16_hi(v.x)), pack_f16x2_rn(bf16_lo(v.y), bf16_hi(v.y)),
+                        pack_f16x2_rn(bf16_lo(v.z), bf16_hi(v.z)), pack_f16x2_rn(bf16_lo(v.w), bf16_hi(v.w)));
+    }
+  }
+}
+
+cudaError_t launch_to_f16(const uint16_t* const* src, uint16_t* const* dst, const size_t* n, int count,
+                          const int32_t* route, cudaStream_t s) {
+  if (count < 1 || count > 4) return cudaErrorInvalidValue;
+  ToF16Args a{};
+  size_t most = 0;
+  for (int k = 0; k < count; ++k) {
+    if (n[k] % 8 != 0) return cudaErrorInvalidValue;
+    a.src[k] = src[k];
+    a.dst[k] = dst[k];
+    a.n8[k] = n[k] / 8;
+    most = std::max(most, a.n8[k]);
+  }
+  a.count = count;
+  a.route = route;
+  if (most == 0) return cudaSuccess;
+  const int grid = static_cast<int>(std::min<size_t>((most + 255) / 256, static_cast<size_t>(device_sm_count()) * 8));
+  cudaError_t e = launch(to_f16_kernel, dim3(grid), dim3(256), 0, s, a);
+  trace_mark(s, "to_f16");
+  return e;
+}
+
 // ---------------------------------------------------------------- fp32 FMA probe
 // CUDA-core throughput of the packed two-lane fp32 FMA (`fma.rn.f32x2`), the
 // instruction of the sparse kernels' accumulations: every thread runs kProbeChains

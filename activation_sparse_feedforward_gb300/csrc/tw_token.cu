@@ -17,7 +17,7 @@
 //  forward   list = the token's TwELL entries (j, a) in ascending neuron order,
 //            pass A: u = x_t . Wu[j], h = a u (gated; non-gated h = a),
 //            pass B: y_t = sum h Wd[j]; in training the list is also the Hybrid
-//            ELL row (idx, a, u).
+//            ELL row (idx, bf16 a, fp16 u).
 //  backward  list = the token's ELL row (j, a, u),
 //            pass A: dh = dy_t . Wd[j]; dg = dh u + l1 (non-gated: dh + l1), du = dh a,
 //            pass B: dx_t = sum dg Wg[j] + du Wu[j]; between the passes every entry's
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_fwd_kernel(c
           for (int w = 0; w < NCH; ++w) u += part[w * kWin + k];
           const float h = unpair(lh[w0 + k]).x * u;
           lh[w0 + k] = pair(h, h);
-          if (HYBRID && TW_CHECKED(w0 + k < a.R, a.status)) a.ell_u[rb + w0 + k] = f32_to_bf16(u);
+          if (HYBRID && TW_CHECKED(w0 + k < a.R, a.status)) a.ell_u[rb + w0 + k] = f32_to_f16(u);
         }
         __syncthreads();
       }
@@ -492,7 +492,7 @@ __global__ void __launch_bounds__((NCH + 1) * 32, ws_ctas_per_sm(NCH))
           for (int w = 0; w < NCH; ++w) u += part[w * kWin + kk];
           const float h = unpair(lh[w0 + kk]).x * u;
           lh[w0 + kk] = pair(h, h);
-          if (HYBRID && TW_CHECKED(w0 + kk < a.R, status)) a.ell_u[rb + w0 + kk] = f32_to_bf16(u);
+          if (HYBRID && TW_CHECKED(w0 + kk < a.R, status)) a.ell_u[rb + w0 + kk] = f32_to_f16(u);
         }
         consumers_sync(kConsumers);
       }
@@ -572,7 +572,7 @@ __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_bwd_kernel(c
         if (k < m) {
           if (i == 0) slot0 = atomicAdd(a.col_cur + j, 1);
           lg[k] = pair(bf16_to_f32(a.ell_a[rb + w0 + k]), 0.f);
-          lu[k] = pair(GATED ? bf16_to_f32(a.ell_u[rb + w0 + k]) : 1.f, 0.f);
+          lu[k] = pair(GATED ? f16_to_f32(a.ell_u[rb + w0 + k]) : 1.f, 0.f);
         } else {
           lg[k] = 0ull;
           lu[k] = 0ull;

@@ -90,7 +90,7 @@ class Hybrid:
     ell_nnz: torch.Tensor      # [T] int32
     ell_idx: torch.Tensor      # [T, R] int16 bits of uint16
     ell_a: torch.Tensor        # [T, R] bf16
-    ell_u: torch.Tensor | None  # [T, R] bf16
+    ell_u: torch.Tensor | None  # [T, R] fp16
     backup_slot: torch.Tensor  # [T] int32
     backup_tok: torch.Tensor   # [max(cap,1)] int32
     backup_a: torch.Tensor     # [max(cap,1), I] fp32
@@ -109,7 +109,7 @@ class Hybrid:
                       ell_nnz=torch.empty(max(T, 1), dtype=torch.int32, device=device),
                       ell_idx=torch.empty((max(T, 1), R), dtype=torch.int16, device=device),
                       ell_a=torch.empty((max(T, 1), R), dtype=BF16, device=device),
-                      ell_u=torch.empty((max(T, 1), R), dtype=BF16, device=device) if gated else None,
+                      ell_u=torch.empty((max(T, 1), R), dtype=torch.float16, device=device) if gated else None,
                       backup_slot=torch.empty(max(T, 1), dtype=torch.int32, device=device),
                       backup_tok=torch.empty(cap1, dtype=torch.int32, device=device),
                       backup_a=torch.empty((cap1, I), dtype=torch.float32, device=device),

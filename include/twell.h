@@ -98,7 +98,12 @@ typedef struct {
  *   row_nnz[t]                      active neurons of row t
  *   ell_nnz[t]                      entries stored in the ELL (0 for backup rows)
  *   ell_idx[t*R + s]                global neuron index, ascending in s
- *   ell_a[t*R + s], ell_u[t*R + s]  bf16 a and u at that neuron (ell_u unused when non-gated)
+ *   ell_a[t*R + s]                  bf16 a at that neuron (the TwELL's value)
+ *   ell_u[t*R + s]                  u at that neuron as fp16 bits (IEEE binary16: 11
+ *                                   significant bits where bf16 has 8, for the weight
+ *                                   gradients' long sums; |u| must stay below 65504,
+ *                                   which the backup rows' fp32 storage covers for the
+ *                                   largest activations); unused when non-gated
  *   backup_slot[t]                  slot of row t in the backup, or -1
  *   backup_tok[b]                   token of backup slot b, ascending in b
  *   backup_a[b*I + j], backup_u[b*I + j]   full fp32 rows of a = ReLU(g) and u (the
@@ -133,9 +138,12 @@ typedef struct {
  *  TW_ROUTE_SPARSE  the pages' method: CUDA-core gathers over the active neurons only
  *                   (explainer 2.B "Training Kernels", "Backpropagation");
  *  TW_ROUTE_DENSE   the ELL rows' up / down projections and their backward as dense
- *                   bf16 tensor-core GEMMs over all neurons, with the TwELL / Hybrid
- *                   masks applied in the GEMM epilogues (h, dg, du are rounded once to
- *                   bf16, as in a dense bf16 FFN); the saved Hybrid is the same;
+ *                   tensor-core GEMMs over all neurons, with the TwELL / Hybrid masks
+ *                   applied in the GEMM epilogues: the forward on bf16 operands (h
+ *                   rounded once to bf16), the backward's dx and dW on fp16 operands
+ *                   (dg, du, h rounded once to fp16; fp16 copies of Wg, Wu, x, dy,
+ *                   whose magnitudes must stay below 65504); the saved Hybrid is the
+ *                   same;
  *  TW_ROUTE_AUTO    decided on the device by each forward, after the gate kernel: dense
  *                   when the ELL rows' mean nonzeros per row exceeds dense_above. A
  *                   row's gathers cost L2 traffic in proportion to its nonzeros, the
@@ -180,7 +188,8 @@ size_t hybrid_pack_workspace_size(int T);
  * given by ascending row (backup_tok, backup_slot, n_backup; more than
  * out->backup_cap backup rows raise TW_ECAPACITY in *dev_status, the extra rows get
  * slot -2 and are not stored); ELL rows store their nonzeros in ascending column
- * order (ell_idx, ell_a, ell_u; ell_nnz = row_nnz, 0 for backup rows); backup rows
+ * order (ell_idx, ell_a, ell_u as fp16 of U's values; ell_nnz = row_nnz, 0 for backup
+ * rows); backup rows
  * store the full rows of A and U widened exactly to fp32. Shapes as twell_pack; ws
  * holds hybrid_pack_workspace_size(T) bytes. Enqueued on `stream`. */
 tw_status hybrid_pack(const uint16_t* A, const uint16_t* U, int T, int I, int W, int C,
@@ -263,7 +272,7 @@ tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* 
                          uint16_t* y, int32_t* dev_status, void* stream);
 
 /* Workspace bytes hybrid_ffn_bwd needs (routes other than TW_ROUTE_SPARSE add the
- * dense route's [T, I] bf16 dG, dU and h). */
+ * dense route's [T, I] fp16 dG, dU and h and fp16 copies of Wg, Wu, x and dy). */
 size_t hybrid_ffn_bwd_workspace_size(int T, int d, int I, int R, int backup_cap, int route);
 
 /* Training backward over the saved Hybrid (explainer 2.B "Backpropagation"):

