@@ -127,9 +127,8 @@ WORKLOADS["train_nongated_d2048_i8192_m40_o1"] = FFNSpec(
 for _m in (29, 108, 911):
     for _f in (0.0, 0.01, 0.05):
         _n = f"train_d2048_i5632_m{_m}_o{int(round(_f * 100))}"
-        # C holds an ordinary row's busiest tile: ~21 nonzeros a 128-wide tile at m = 911
         WORKLOADS[_n] = FFNSpec(_n, T=16384, d=2048, I=5632, mean_active=_m, outlier_frac=_f,
-                                W=128, C=64 if _m > 200 else 16, R=_sweep_R(_m), l1=2e-5, cfg_id=4)
+                                W=128, C=16, R=_sweep_R(_m), l1=2e-5, cfg_id=4)
 
 
 def stack_layer_spec(layer: int, T: int = 8192, seed: int = 0, d: int = 2048, I: int = 5632, W: int = 128,

@@ -100,10 +100,18 @@ def test_dense_route_saves_the_sparse_routes_hybrid(spec):
     for name in ("ell_idx", "ell_a"):
         np.testing.assert_array_equal(bits_of(getattr(hs.saved, name))[valid], bits_of(getattr(hd.saved, name))[valid])
     if spec.gated:
-        # u: the same fp32 dot product summed in another order, rounded to fp16 once
+        # u: the same fp32 dot product of d terms summed in another order, rounded to
+        # fp16 once: one fp16 unit in the last place apart (adjacent fp16 values of one
+        # sign have adjacent bit patterns), or, where the sum cancels to a small value,
+        # apart by no more than the summation-order error of terms of size ~|x||Wu|
+        bs = hs.saved.ell_u.view(torch.int16).cpu().numpy().astype(np.int32)[valid]
+        bd = hd.saved.ell_u.view(torch.int16).cpu().numpy().astype(np.int32)[valid]
         us = hs.saved.ell_u.double().cpu().numpy()[valid]
         ud = hd.saved.ell_u.double().cpu().numpy()[valid]
-        assert np.all(np.abs(us - ud) <= 2.0 ** -10 * np.abs(us) + 2.0 ** -24)
+        ok = (np.abs(bs - bd) <= 1) | (np.abs(us - ud) <= 1e-5)
+        bad = np.flatnonzero(~ok)
+        assert bad.size == 0, (f"{bad.size} of {ok.size} u values differ by more than one fp16 ulp; first: "
+                               f"{[(float(us[i]), float(ud[i])) for i in bad[:5]]}")
     # the two routes' outputs agree with each other as closely as each with the oracle
     assert_close(f64_of(yd), f64_of(ys), "y: dense vs sparse route")
     assert_close(f64_of(gd[0]), f64_of(gs[0]), "dx: dense vs sparse route")
@@ -123,7 +131,7 @@ def test_auto_route_is_decided_on_the_device(dense_above, expect_dense):
 
 
 @pytest.mark.parametrize("name,backup_cap", [("train_d2048_i5632_m108_o5", 1280),
-                                             ("train_d2048_i5632_m911_o1", 512)])
+                                             ("train_d2048_i5632_m108_o0", 128)])
 def test_dense_route_full_size_sampled(name, backup_cap):
     spec = WORKLOADS[name]
     inp = make_inputs(spec, with_dy=True)
@@ -131,6 +139,7 @@ def test_dense_route_full_size_sampled(name, backup_cap):
     assert h.saved.took_dense_route()
     nb = int(h.saved.n_backup.item())
     assert len(inp["outliers"]) <= nb <= backup_cap
+    assert int(h.saved.ell_nnz.sum().item()) > 100 * (spec.T - nb)     # ELL rows of ~108 nonzeros
     rows = np.unique(np.concatenate([np.arange(7, spec.T, 1031), inp["outliers"][:10], [spec.T - 1]]))
     _check_oracle(spec, inp, y, grads, spec.l1, rows=rows)
     J = np.array([0, 3, 999, 2048, 4095, 5631])
