@@ -105,6 +105,11 @@ def _bf16(v):
     return ffn.bf16_to_f64(round_to_bf16_bits(np.asarray(v, dtype=np.float32)))
 
 
+def _f16(v):
+    """fp16 (IEEE binary16) rounding, round to nearest even: the Hybrid's storage of u."""
+    return np.asarray(v, dtype=np.float64).astype(np.float16).astype(np.float64)
+
+
 def _close_to_stored_precision(got, ref, what):
     """|got - ref| <= 2^-8 |ref| (the bf16 output) + 2e-3 rms(ref) (fp32 sums, and a
     rare one-ulp difference where the GPU's fp32 g rounds to another bf16 a)."""
@@ -129,11 +134,11 @@ def test_longest_entry_lists(gated):
     b = ffn.backward(inp["x"], inp["Wg"], inp["Wu"], inp["Wd"], inp["dy"], spec.l1, fwd=o)
     x, Wg, Wu, Wd, dyv = (ffn.as_f64(inp[k]) for k in ("x", "Wg", "Wu", "Wd", "dy"))
     # With every one of 10240 neurons active, a ~ 3 and the sums are long: the bf16
-    # storage of a (TwELL values, Hybrid ELL a) and, in the backward, of u (Hybrid
-    # ELL u) moves y, dx and dW by ~0.2 % of their terms' scale, more than
-    # 1e-2 (1 + |ref|) allows where an element nearly cancels. The reference
-    # therefore stores a and u in bf16 as the formats do; the rest is the plain
-    # definition in fp64.
+    # storage of a (TwELL values, Hybrid ELL a) and, in the backward, the fp16 storage
+    # of u (Hybrid ELL u) move y, dx and dW by ~0.2 % of their terms' scale, more
+    # than 1e-2 (1 + |ref|) allows where an element nearly cancels. The reference
+    # therefore stores a in bf16 and u in fp16 as the formats do; the rest is the
+    # plain definition in fp64.
     a16 = _bf16(o["a"])
     u = o["u"]
     y_ref = (a16 * u if gated else a16) @ Wd
@@ -143,7 +148,7 @@ def test_longest_entry_lists(gated):
     dh = dyv @ Wd.T
     dx, dWg, dWu, dWd = grads
     if gated:
-        u16 = _bf16(u)
+        u16 = _f16(u)
         dg = (dh * u16 + spec.l1) * active
         du = dh * a16
         dx_ref = dg @ Wg + du @ Wu
