@@ -436,8 +436,13 @@ def measure_sweep(dev, flush, stream, steps: int, peaks: dict) -> list:
         inp = make_inputs(spec, with_dy=True)
         x, Wg, Wu, Wd, dy = (None if inp[k] is None else torch.from_numpy(inp[k].view(np.int16)).view(torch.bfloat16).to(dev)
                              for k in ("x", "Wg", "Wu", "Wd", "dy"))
-        # backup capacity: the outliers with room to spare (ordinary rows fit the ELL)
-        cap = min(spec.T, 128 * int(math.ceil(1.5 * spec.outlier_frac * spec.T / 128.0)) + 128)
+        # the dense backup sized to hold the backup rows (counted by one forward with room
+        # for every row), rounded up to whole 128-row tiles with one spare tile
+        probe = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, spec.T, gated=spec.gated, device=dev)
+        probe.forward(x, Wg, Wu, Wd)
+        cap = min(spec.T, 128 * int(math.ceil(int(probe.saved.n_backup.item()) / 128.0)) + 128)
+        del probe
+        torch.cuda.empty_cache()
         row = {"workload": spec.name, "C": spec.C, "R": spec.R, "backup_cap": cap, "dense_above": DENSE_ABOVE}
         for route in ("auto", "sparse", "dense"):
             h = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, cap, gated=spec.gated, device=dev,
