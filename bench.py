@@ -605,7 +605,7 @@ def run_ours(args, dist: Dist) -> dict | None:
     x, Wg, Wu, Wd, dy = (to_dev(inp[k]) for k in ("x", "Wg", "Wu", "Wd", "dy"))
     backup_cap = min(spec.T, max(128, int(math.ceil(spec.outlier_frac * spec.T * 1.5 / 128.0)) * 128 + 128))
     h = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, backup_cap, gated=spec.gated, device=dev,
-                     route="auto", dense_above=DENSE_ABOVE)
+                     route=args.route, dense_above=DENSE_ABOVE)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -770,7 +770,7 @@ def run_ours(args, dist: Dist) -> dict | None:
     hy = torch.empty_like(hx).pin_memory()
     hdx = torch.empty_like(hx).pin_memory()
     hs = [h, tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, backup_cap, gated=spec.gated, device=dev,
-                          route="auto", dense_above=DENSE_ABOVE)]
+                          route=args.route, dense_above=DENSE_ABOVE)]
     xin = [torch.empty_like(x) for _ in range(2)]
     dyin = [torch.empty_like(dy) for _ in range(2)]
     up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -844,7 +844,7 @@ def run_ours(args, dist: Dist) -> dict | None:
     torch.cuda.reset_peak_memory_stats(dev)
     m0 = torch.cuda.memory_allocated(dev)
     h_m = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, backup_cap, gated=spec.gated, device=dev,
-                       route="auto", dense_above=DENSE_ABOVE)
+                       route=args.route, dense_above=DENSE_ABOVE)
     h_m.forward(x, Wg, Wu, Wd)
     h_m.backward(dy, x, Wg, Wu, Wd, spec.l1)
     torch.cuda.synchronize(dev)
@@ -876,7 +876,8 @@ def run_ours(args, dist: Dist) -> dict | None:
                    "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "single GPU"},
         "measured": {"nnz_per_token": stats["nnz"] / spec.T, "nnz_ell": stats["nnz_ell"],
                      "n_backup": stats["n_backup"], "route_taken": stats["route"],
-                     "route": f"auto (dense above {DENSE_ABOVE:g} nonzeros per ELL row)"},
+                     "route": args.route + (f" (dense above {DENSE_ABOVE:g} nonzeros per ELL row)"
+                                            if args.route == "auto" else "")},
         "roofline": roofline,
         "step_roofline": step_roof,
         "e2e": e2e,
@@ -956,6 +957,8 @@ def main():
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-inference", action="store_true", help="skip the TwELL inference forward figures")
     ap.add_argument("--no-sweep", action="store_true", help="skip the training sparsity sweep")
+    ap.add_argument("--route", choices=["sparse", "dense", "auto"], default="sparse",
+                    help="route of the headline step's ELL rows (the sweep and the stack report all of them)")
     ap.add_argument("--clock-soak", type=float, default=4.0,
                     help="seconds over which the K-step timed region is repeated for the clock record")
     ap.add_argument("--no-stack", action="store_true", help="skip the 28-layer residual stack figures")
