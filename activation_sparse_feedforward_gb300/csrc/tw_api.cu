@@ -445,7 +445,7 @@ tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* 
                                            dev_status, s));
     const uint16_t* A[1] = {w.Hd};
     const uint16_t* B[1] = {Wd};
-    TW_TRY(tw::gemm_rows_nmajor_bf16(A, B, 1, T, I, d, y, d, taken, dev_status, s));
+    TW_TRY(tw::gemm_rows_nmajor_bf16(A, B, 1, T, I, d, y, d, taken, dev_status, s, false, "dense_down"));
   }
   if (cap > 0) {
     TW_TRY(tw::launch_gather_rows(x, d, T, saved->backup_tok, saved->n_backup, cap, ra, w.X, s, dev_status, nullptr,
@@ -527,7 +527,7 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
     TW_TRY(tw::gemm_dense_grad(dy, Wd, T, d, I, *saved, gated, l1, w.dGd, w.dUd, w.Hd, taken, dev_status, s));
     const uint16_t* A[2] = {w.dGd, w.dUd};
     const uint16_t* B[2] = {w.Wg16, w.Wu16};
-    TW_TRY(tw::gemm_rows_nmajor_bf16(A, B, gated ? 2 : 1, T, I, d, dx, d, taken, dev_status, s, true));
+    TW_TRY(tw::gemm_rows_nmajor_bf16(A, B, gated ? 2 : 1, T, I, d, dx, d, taken, dev_status, s, true, "dense_dx"));
   }
   const bool backup = cap > 0 && T > 0;
   if (backup) {

@@ -270,7 +270,7 @@ cudaError_t gemm_up_hybrid(const uint16_t* x, const uint16_t* Wu, int T, int d, 
 
 cudaError_t gemm_rows_nmajor_bf16(const uint16_t* const* A, const uint16_t* const* B, int segments, int M, int K,
                                   int N, uint16_t* out, int ld, const int32_t* route, int32_t* status,
-                                  cudaStream_t s, bool f16) {
+                                  cudaStream_t s, bool f16, const char* label) {
   if (M == 0) return cudaSuccess;
   if (segments < 1 || segments > GEMM_MAX_SEGMENTS || N % 256 != 0) return cudaErrorInvalidValue;
   GemmShape sh = shape_static(M, N, K, status);
@@ -282,8 +282,8 @@ cudaError_t gemm_rows_nmajor_bf16(const uint16_t* const* A, const uint16_t* cons
       return cudaErrorInvalidValue;
   fill_unused(maps, segments, segments);
   EpiStoreBf16::Params ep{out, ld};
-  if (f16) return run_gemm<256, false, true, false, 4, F16Operands<EpiStoreBf16>>(maps, sh, ep, M, s, "dense_rows_gemm");
-  return run_gemm<256, false, true, false, 4, EpiStoreBf16>(maps, sh, ep, M, s, "dense_rows_gemm");
+  if (f16) return run_gemm<256, false, true, false, 4, F16Operands<EpiStoreBf16>>(maps, sh, ep, M, s, label);
+  return run_gemm<256, false, true, false, 4, EpiStoreBf16>(maps, sh, ep, M, s, label);
 }
 
 template <int BN, bool GATED>

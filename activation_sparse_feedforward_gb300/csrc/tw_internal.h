@@ -249,7 +249,7 @@ cudaError_t gemm_up_hybrid(const uint16_t* x, const uint16_t* Wu, int T, int d, 
 // (N contiguous); operands bf16, or fp16 when f16.
 cudaError_t gemm_rows_nmajor_bf16(const uint16_t* const* A, const uint16_t* const* B, int segments, int M, int K,
                                   int N, uint16_t* out, int ld, const int32_t* route, int32_t* status, cudaStream_t s,
-                                  bool f16 = false);
+                                  bool f16, const char* label);
 // Backward: dh = dY Wd^T over all T rows; dG, dU (gated) and H [T, I] fp16 from the
 // saved Hybrid's ELL rows (zeros off the support and on backup rows).
 cudaError_t gemm_dense_grad(const uint16_t* dY, const uint16_t* Wd, int T, int d, int I, const tw_hybrid& h,

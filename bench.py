@@ -179,6 +179,12 @@ def kernel_work(label: str, spec, stats: dict) -> tuple[str, float] | None:
         # x and dy read + dW written (fp32, 3 matrices) + one 16-byte column record
         # read per entry
         return "hbm", float(2 * T * d * 2 + 3 * I * d * 4 + nnz_ell * 16)
+    if label in ("dense_up", "dense_down", "dense_grad"):
+        return "tensor", 2.0 * T * d * I
+    if label == "dense_dx":
+        return "tensor", 2.0 * g * T * d * I
+    if label == "dense_weight_grad":
+        return "tensor", 2.0 * (g + 1) * T * d * I
     if label == "backup_hidden":
         return "tensor", 2.0 * 2 * nb * d * I
     if label == "backup_grad":
