@@ -551,6 +551,16 @@ struct EpiStoreBf16 {
   TW_DEV void finish() {}
 };
 
+// Element q (0..7) of eight 16-bit values held in a uint4, and byte q (0..15) of a uint4.
+TW_DEV uint32_t sel16(const uint4& v, int q) {
+  const uint32_t w = q < 2 ? v.x : q < 4 ? v.y : q < 6 ? v.z : v.w;
+  return (q & 1) ? (w >> 16) : (w & 0xFFFFu);
+}
+TW_DEV uint32_t sel8(const uint4& v, int q) {
+  const uint32_t w = q < 4 ? v.x : q < 8 ? v.y : q < 12 ? v.z : v.w;
+  return (w >> (8 * (q & 3))) & 0xFFu;
+}
+
 // Dense route, gated forward: the accumulator is u = x Wu^T for token row m over the
 // columns [n0, n0 + BN). With the row's TwELL slots of a (the gate kernel's output;
 // a row served here never overflowed, so its slots hold all its nonzeros) the
@@ -560,12 +570,17 @@ struct EpiStoreBf16 {
 //                  (the nonzeros of the row's tiles before this CTA tile),
 // the same ELL the sparse route's token kernel writes. Rows of the dense backup
 // (backup_slot != -1) get H = 0 and no ELL entries.
-// The accumulator's 32 columns of a chunk go through the thread's part of the
-// staging buffer (a row of kUpStride floats, an odd stride, so lanes reading the same
-// column hit distinct banks), where active columns are looked up by index.
+// A TwELL tile's slots are read sixteen at a time (one 16-byte load of indices and
+// two of values, all issued together; the first tile's before the accumulator is
+// ready), not one dependent load per slot. The accumulator's 32 columns of a chunk go
+// through the thread's part of the staging buffer (a row of kUpStride floats, an odd
+// stride, so lanes reading the same column hit distinct banks), where active columns
+// are looked up by index; H leaves through the per-warp transpose, whole 64-byte row
+// segments per store.
 struct EpiUpHybrid {
   static constexpr int kUpStride = 33;
-  static constexpr int kStageBytes = 4 * 32 * kUpStride * 4;
+  static constexpr int kWarpFloats = 32 * kUpStride + 32 * 20;  // u staging + bf16 transpose
+  static constexpr int kStageBytes = 4 * kWarpFloats * 4;
   struct Params {
     int T, W, C, nT, R;
     const uint16_t* cnt;
@@ -580,16 +595,45 @@ struct EpiUpHybrid {
     int32_t* status;
   };
   const Params& p;
-  int m, n0;
+  int m, M, n0;
   bool valid, ell_row;
   int off;      // ELL slot of the next nonzero of this row
-  int k_cur;    // TwELL tile of the slot cursor, and the cursor within it
+  int k_cur;    // TwELL tile of the slot cursor, its count, the cursor within it
+  int n_cur;
   int s_cur;
+  int g_cur;    // first slot of the group of sixteen held in iv / v0 / v1
+  uint4 iv, v0, v1;
   float* stage = nullptr;
   TW_DEV EpiUpHybrid(const Params& p_, int m_, int M_, int n0_)
-      : p(p_), m(m_), n0(n0_), valid(m_ < M_), ell_row(false), off(0), k_cur(-1), s_cur(0) {}
-  // before the accumulator is ready: the routing of the row and the ELL offset of its
-  // first tile in [n0, n0 + BN) (a sum over the counts of the row's earlier tiles)
+      : p(p_), m(m_), M(M_), n0(n0_), valid(m_ < M_), ell_row(false), off(0), k_cur(-1), n_cur(0), s_cur(0),
+        g_cur(-16) {}
+  TW_DEV void load_group(int k, int g) {
+    const size_t base = (static_cast<size_t>(m) * p.nT + k) * p.C + g;
+    if (p.C % 16 == 0) {
+      iv = *reinterpret_cast<const uint4*>(p.idx + base);
+      v0 = *reinterpret_cast<const uint4*>(p.val + base);
+      v1 = *reinterpret_cast<const uint4*>(p.val + base + 8);
+    } else {
+      uint32_t b[4] = {0u, 0u, 0u, 0u}, w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+      for (int q = 0; q < 16 && g + q < p.C; ++q) {
+        b[q >> 2] |= static_cast<uint32_t>(p.idx[base + q]) << (8 * (q & 3));
+        w[q >> 1] |= static_cast<uint32_t>(p.val[base + q]) << (16 * (q & 1));
+      }
+      iv = make_uint4(b[0], b[1], b[2], b[3]);
+      v0 = make_uint4(w[0], w[1], w[2], w[3]);
+      v1 = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+    g_cur = g;
+  }
+  TW_DEV void open_tile(int k) {
+    k_cur = k;
+    s_cur = 0;
+    n_cur = min(static_cast<int>(p.cnt[static_cast<size_t>(m) * p.nT + k]), p.C);
+    if (n_cur > 0) load_group(k, 0);
+  }
+  // before the accumulator is ready: the routing of the row, the ELL offset of its
+  // first tile in [n0, n0 + BN) (a sum over the counts of the row's earlier tiles) and
+  // that tile's first sixteen slots
   TW_DEV void prefetch(int) {
     if (!valid) return;
     ell_row = p.backup_slot[m] == -1;
@@ -599,45 +643,43 @@ struct EpiUpHybrid {
     int o = 0;
     for (int k = 0; k < k0; ++k) o += min(static_cast<int>(cr[k]), p.C);
     off = o;
+    open_tile(k0);
   }
+  // Every lane of the warp calls it (H's stores are warp-cooperative).
   TW_DEV void chunk(int c, const uint32_t (&v)[32], const uint32_t (&)[32]) {
-    if (!valid) return;
+    const int lane = threadIdx.x & 31;
+    const int m0 = m - lane;
+    const int rows = min(32, M - m0);
+    if (rows <= 0) return;  // uniform over the warp
     const int col0 = n0 + c * 32;
-    uint4* hdst = reinterpret_cast<uint4*>(p.H + static_cast<size_t>(m) * p.ldh + col0);
-    if (!ell_row) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) hdst[i] = make_uint4(0u, 0u, 0u, 0u);
-      return;
-    }
-    float* mine = stage + (threadIdx.x & 31) * kUpStride;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) mine[i] = __uint_as_float(v[i]);
-    const int k = col0 / p.W;
-    const int local0 = col0 - k * p.W;
-    if (k != k_cur) {
-      k_cur = k;
-      s_cur = 0;
-    }
-    const size_t tk = static_cast<size_t>(m) * p.nT + k;
-    const int n = min(static_cast<int>(p.cnt[tk]), p.C);
     uint32_t mask = 0u;
-    const size_t rb = static_cast<size_t>(m) * p.R;
-    // the tile's slots are in ascending column order: take those inside this chunk
-    for (; s_cur < n; ++s_cur) {
-      const int li = p.idx[tk * p.C + s_cur];
-      if (li >= local0 + 32) break;
-      const int i = li - local0;
-      if (!TW_CHECKED(i >= 0 && i < 32, p.status)) continue;
-      const uint16_t ab = p.val[tk * p.C + s_cur];
-      const float u = mine[i];
-      mine[i] = bf16_to_f32(ab) * u;  // h, in place of u
-      mask |= 1u << i;
-      if (TW_CHECKED(off < p.R, p.status)) {
-        p.ell_idx[rb + off] = static_cast<uint16_t>(col0 + i);
-        p.ell_a[rb + off] = ab;
-        p.ell_u[rb + off] = f32_to_f16(u);
+    float* mine = stage + lane * kUpStride;
+    if (valid && ell_row) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) mine[i] = __uint_as_float(v[i]);
+      const int k = col0 / p.W;
+      const int local0 = col0 - k * p.W;
+      if (k != k_cur) open_tile(k);
+      const size_t rb = static_cast<size_t>(m) * p.R;
+      // the tile's slots are in ascending column order: take those inside this chunk
+      for (; s_cur < n_cur; ++s_cur) {
+        if (s_cur - g_cur >= 16) load_group(k, s_cur);
+        const int q = s_cur - g_cur;
+        const int li = static_cast<int>(sel8(iv, q));
+        if (li >= local0 + 32) break;
+        const int i = li - local0;
+        if (!TW_CHECKED(i >= 0 && i < 32, p.status)) continue;
+        const uint16_t ab = static_cast<uint16_t>(q < 8 ? sel16(v0, q) : sel16(v1, q - 8));
+        const float u = mine[i];
+        mine[i] = bf16_to_f32(ab) * u;  // h, in place of u
+        mask |= 1u << i;
+        if (TW_CHECKED(off < p.R, p.status)) {
+          p.ell_idx[rb + off] = static_cast<uint16_t>(col0 + i);
+          p.ell_a[rb + off] = ab;
+          p.ell_u[rb + off] = f32_to_f16(u);
+        }
+        ++off;
       }
-      ++off;
     }
     uint32_t w[16];
 #pragma unroll
@@ -646,8 +688,7 @@ struct EpiUpHybrid {
       const float h1 = ((mask >> (2 * q + 1)) & 1u) ? mine[2 * q + 1] : 0.f;
       w[q] = pack_bf16x2_rn(h0, h1);
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) hdst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    transposed_rows_bf16(stage + 32 * kUpStride, w, m0, rows, p.H + col0, p.ldh);
   }
   TW_DEV void finish() {}
 };
@@ -660,14 +701,19 @@ struct EpiUpHybrid {
 // the support, as the operands of the dx and weight-gradient GEMMs (run on fp16: a
 // weight-gradient element sums thousands of these products at high activity, and
 // bf16's 8 significant bits then leave errors above the parity bound where the sum
-// cancels). Rows of the dense
-// backup get zeros (their gradients come from the backup GEMMs). The entries of a
-// chunk are placed in the thread's staging row (a at column i, u at 32 + i; stride
-// kGradStride, odd) and read back by column.
+// cancels). Rows of the dense backup get zeros (their gradients come from the backup
+// GEMMs).
+// The row's entries are read eight at a time (16-byte loads of indices, a and u,
+// issued together; the tile's first eight before the accumulator is ready, after a
+// binary search for the tile's first entry), not one dependent load per entry. A
+// chunk's entries are placed in the thread's staging row (a at column i, u at
+// 32 + i; stride kGradStride, odd) and read back by column; the three outputs leave
+// through the per-warp transpose, whole 64-byte row segments per store.
 template <bool GATED>
 struct EpiDenseGrad {
   static constexpr int kGradStride = 65;
-  static constexpr int kStageBytes = 4 * 32 * kGradStride * 4;
+  static constexpr int kWarpFloats = 32 * kGradStride + 32 * 20;  // a / u staging + transpose
+  static constexpr int kStageBytes = 4 * kWarpFloats * 4;
   struct Params {
     int R, I;
     const int32_t* ell_nnz;
@@ -681,14 +727,35 @@ struct EpiDenseGrad {
     int32_t* status;
   };
   const Params& p;
-  int m, n0;
+  int m, M, n0;
   bool valid, ell_row;
   int cur, end;  // ELL entry cursor and end of the row
+  int b_cur;     // first entry of the batch of eight held in bi / ba / bu
+  uint4 bi, ba, bu;
   float* stage = nullptr;
   TW_DEV EpiDenseGrad(const Params& p_, int m_, int M_, int n0_)
-      : p(p_), m(m_), n0(n0_), valid(m_ < M_), ell_row(false), cur(0), end(0) {}
-  // before the accumulator is ready: the first ELL entry at or past column n0
-  // (binary search over the row's ascending indices)
+      : p(p_), m(m_), M(M_), n0(n0_), valid(m_ < M_), ell_row(false), cur(0), end(0), b_cur(-8) {}
+  TW_DEV void load_batch(int e) {
+    const size_t base = static_cast<size_t>(m) * p.R + e;
+    if (p.R % 8 == 0) {
+      bi = *reinterpret_cast<const uint4*>(p.ell_idx + base);
+      ba = *reinterpret_cast<const uint4*>(p.ell_a + base);
+      bu = GATED ? *reinterpret_cast<const uint4*>(p.ell_u + base) : make_uint4(0u, 0u, 0u, 0u);
+    } else {
+      uint32_t wi[4] = {0u, 0u, 0u, 0u}, wa[4] = {0u, 0u, 0u, 0u}, wu[4] = {0u, 0u, 0u, 0u};
+      for (int q = 0; q < 8 && e + q < end; ++q) {
+        wi[q >> 1] |= static_cast<uint32_t>(p.ell_idx[base + q]) << (16 * (q & 1));
+        wa[q >> 1] |= static_cast<uint32_t>(p.ell_a[base + q]) << (16 * (q & 1));
+        if (GATED) wu[q >> 1] |= static_cast<uint32_t>(p.ell_u[base + q]) << (16 * (q & 1));
+      }
+      bi = make_uint4(wi[0], wi[1], wi[2], wi[3]);
+      ba = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+      bu = make_uint4(wu[0], wu[1], wu[2], wu[3]);
+    }
+    b_cur = e;
+  }
+  // before the accumulator is ready: the first ELL entry at or past column n0 (binary
+  // search over the row's ascending indices) and the batch holding it
   TW_DEV void prefetch(int) {
     if (!valid) return;
     ell_row = p.backup_slot[m] == -1;
@@ -706,22 +773,27 @@ struct EpiDenseGrad {
     }
     cur = lo;
     end = n;
+    if (cur < end) load_batch(p.R % 8 == 0 ? (cur & ~7) : cur);
   }
+  // Every lane of the warp calls it (the stores are warp-cooperative).
   TW_DEV void chunk(int c, const uint32_t (&dh)[32], const uint32_t (&)[32]) {
-    if (!valid) return;
+    const int lane = threadIdx.x & 31;
+    const int m0 = m - lane;
+    const int rows = min(32, M - m0);
+    if (rows <= 0) return;  // uniform over the warp
     const int col0 = n0 + c * 32;
-    const size_t o = static_cast<size_t>(m) * p.ld + col0;
     uint32_t mask = 0u;
-    float* mine = stage + (threadIdx.x & 31) * kGradStride;
-    if (ell_row) {
-      const size_t rb = static_cast<size_t>(m) * p.R;
+    float* mine = stage + lane * kGradStride;
+    if (valid && ell_row) {
       for (; cur < end; ++cur) {
-        const int j = p.ell_idx[rb + cur];
+        if (cur - b_cur >= 8) load_batch(p.R % 8 == 0 ? (cur & ~7) : cur);
+        const int q = cur - b_cur;
+        const int j = static_cast<int>(sel16(bi, q));
         if (j >= col0 + 32) break;
         const int i = j - col0;
         if (!TW_CHECKED(i >= 0, p.status)) continue;
-        mine[i] = bf16_to_f32(p.ell_a[rb + cur]);
-        if (GATED) mine[32 + i] = f16_to_f32(p.ell_u[rb + cur]);
+        mine[i] = bf16_to_f32(static_cast<uint16_t>(sel16(ba, q)));
+        if (GATED) mine[32 + i] = f16_to_f32(static_cast<uint16_t>(sel16(bu, q)));
         mask |= 1u << i;
       }
     }
@@ -744,18 +816,10 @@ struct EpiDenseGrad {
       wu[q] = pack_f16x2_rn(u2[0], u2[1]);
       wh[q] = pack_f16x2_rn(h2[0], h2[1]);
     }
-    uint4* dg = reinterpret_cast<uint4*>(p.dG + o);
-    uint4* hh = reinterpret_cast<uint4*>(p.H + o);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      dg[i] = make_uint4(wg[4 * i], wg[4 * i + 1], wg[4 * i + 2], wg[4 * i + 3]);
-      hh[i] = make_uint4(wh[4 * i], wh[4 * i + 1], wh[4 * i + 2], wh[4 * i + 3]);
-    }
-    if (GATED) {
-      uint4* du = reinterpret_cast<uint4*>(p.dU + o);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) du[i] = make_uint4(wu[4 * i], wu[4 * i + 1], wu[4 * i + 2], wu[4 * i + 3]);
-    }
+    float* tr = stage + 32 * kGradStride;
+    transposed_rows_bf16(tr, wg, m0, rows, p.dG + col0, p.ld);
+    transposed_rows_bf16(tr, wh, m0, rows, p.H + col0, p.ld);
+    if (GATED) transposed_rows_bf16(tr, wu, m0, rows, p.dU + col0, p.ld);
   }
   TW_DEV void finish() {}
 };
