@@ -56,14 +56,14 @@ static cudaError_t run_gemm(const GemmMaps& maps, const GemmShape& sh, const typ
                             cudaStream_t s, const char* label) {
   using Tr = GemmTraits<BN, A_MN, B_MN, DUAL, STAGES, NA>;
   auto kern = gemm_tc_kernel<BN, A_MN, B_MN, DUAL, STAGES, Epi, NA>;
-  constexpr int smem = Tr::SMEM_BYTES + Epi::kStageBytes;
+  constexpr int smem = Tr::SMEM_BYTES + Epi::kStageBytes * (epi_warps<BN, Epi>() / 4);
   static_assert(smem <= 232448, "GEMM shared memory above the 227 KiB opt-in limit");
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const long tiles = static_cast<long>((max_rows + GEMM_BM - 1) / GEMM_BM) * (sh.N / BN);
   if (tiles <= 0) return cudaSuccess;
   const int grid = sh.ksplit < 0 ? device_sm_count() : static_cast<int>(std::min<long>(tiles, device_sm_count()));
-  e = launch(kern, dim3(grid), dim3(GEMM_THREADS), smem, s, maps, sh, ep);
+  e = launch(kern, dim3(grid), dim3(gemm_threads<BN, Epi>()), smem, s, maps, sh, ep);
   trace_mark(s, label);
   return e;
 }
@@ -298,7 +298,7 @@ static cudaError_t dense_grad_bn(const uint16_t* dY, const uint16_t* Wd, int T, 
   typename EpiDenseGrad<GATED>::Params ep{h.R, I, h.ell_nnz, h.backup_slot, h.ell_idx, h.ell_a, GATED ? h.ell_u : nullptr,
                                           l1, dG, GATED ? dU : nullptr, H, I, status};
   constexpr int kStageBytes = (128 + BN) * 64 * 2;
-  constexpr int kBudget = 232448 - 1280 - EpiDenseGrad<GATED>::kStageBytes;
+  constexpr int kBudget = 232448 - 1280 - EpiDenseGrad<GATED>::kStageBytes * (epi_warps<BN, EpiDenseGrad<GATED>>() / 4);
   constexpr int kStages = kBudget / kStageBytes < 8 ? kBudget / kStageBytes : 8;
   return run_gemm<BN, false, false, false, kStages, EpiDenseGrad<GATED>>(maps, sh, ep, T, s, "dense_grad");
 }

@@ -8,7 +8,9 @@
 //    into one of two accumulator buffers and commits each ring slot back to the
 //    producer when its MMAs retire.
 //  * Warps 2-5 (128 threads, one accumulator row each) run the epilogue of tile i
-//    while the MMAs of tile i + 1 fill the other TMEM buffer.
+//    while the MMAs of tile i + 1 fill the other TMEM buffer. An epilogue that does
+//    much per element (kSplitColumns) gets eight warps on 256-wide tiles: two per
+//    TMEM lane quarter, each taking one half of the tile's columns.
 //
 // A is [M, K] with K contiguous ("K-major") or stored [K, M] ("MN-major"); the same
 // for B with N in place of M. DUAL issues a second MMA with a second B operand into
@@ -31,7 +33,6 @@ namespace tw {
 
 constexpr int GEMM_BM = 128;
 constexpr int GEMM_BK = 64;
-constexpr int GEMM_THREADS = 192;
 // per-warp transpose buffer of the fp32 row epilogues (`transposed_rows`): 32 rows of
 // kEpiStageStride floats, for each of the four epilogue warps
 constexpr int kEpiStageStride = 36;
@@ -93,6 +94,22 @@ struct epi_f16_operands : std::false_type {};
 template <class E>
 struct epi_f16_operands<E, std::void_t<decltype(E::kF16Operands)>> : std::bool_constant<E::kF16Operands> {};
 
+// An epilogue with kSplitColumns = true runs on eight warps when BN == 256 (each warp
+// sees an epilogue object over its 128 columns); the others on four. kStageBytes is
+// an epilogue's staging for four warps, so eight warps take twice as much.
+template <class E, class = void>
+struct epi_splits : std::false_type {};
+template <class E>
+struct epi_splits<E, std::void_t<decltype(E::kSplitColumns)>> : std::bool_constant<E::kSplitColumns> {};
+template <int BN, class Epi>
+__host__ __device__ constexpr int epi_warps() {
+  return (epi_splits<Epi>::value && BN == 256) ? 8 : 4;
+}
+template <int BN, class Epi>
+__host__ __device__ constexpr int gemm_threads() {
+  return 64 + 32 * epi_warps<BN, Epi>();
+}
+
 // NA = 2 pairs the segments: segments 2i and 2i + 1 share one B operand (b[2i]), so
 // a stage holds both A tiles and one B tile, and both products go into the same
 // accumulator (the hi / lo halves of a split fp32 operand against one weight).
@@ -115,7 +132,7 @@ struct GemmTraits {
 };
 
 template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES, class Epi, int NA = 1>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+__global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
     gemm_tc_kernel(const __grid_constant__ GemmMaps maps, const GemmShape shape,
                    const __grid_constant__ typename Epi::Params ep) {
   using Tr = GemmTraits<BN, A_MN, B_MN, DUAL, STAGES, NA, epi_f16_operands<Epi>::value>;
@@ -139,7 +156,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull + b, 1);
-      mbar_init(tempty + b, 4);
+      mbar_init(tempty + b, epi_warps<BN, Epi>());
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -320,7 +337,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue warps
+    constexpr int kEW = epi_warps<BN, Epi>();
+    constexpr int kCols = BN * 4 / kEW;  // the columns of the tile one epilogue warp takes
+    const int ew = warp - 2;
     const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
+    const int half = ew >> 2;      // which kCols columns of the tile (0 with four warps)
     const int row = quarter * 32 + lane;
     int local = 0;
     for (int unit = blockIdx.x; unit < num_units; unit += gridDim.x) {
@@ -331,37 +352,37 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       ++local;
       const int m = (tile / n_tiles) * GEMM_BM + row;
-      const int n0 = (tile % n_tiles) * BN;
+      const int n0 = (tile % n_tiles) * BN + half * kCols;
       Epi e(ep, m, M, n0);
-      if constexpr (epi_prefetches<Epi>::value) e.prefetch(BN);  // while the tile's K loop runs
+      if constexpr (epi_prefetches<Epi>::value) e.prefetch(kCols);  // while the tile's K loop runs
       int ok = 0;
       if (lane == 0) ok = mbar_wait(tfull + buf, use & 1u, abort_flag, shape.status) ? 1 : 0;
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       tc_fence_after_sync();
       if constexpr (Epi::kStageBytes > 0)
-        e.stage = reinterpret_cast<float*>(tiles + STAGES * Tr::STAGE_BYTES + Tr::BAR_BYTES) + quarter * (Epi::kStageBytes / 16);
-      const uint32_t tbase =
-          tmem_base + static_cast<uint32_t>(buf * Tr::ACC_COLS) + (static_cast<uint32_t>(quarter * 32) << 16);
+        e.stage = reinterpret_cast<float*>(tiles + STAGES * Tr::STAGE_BYTES + Tr::BAR_BYTES) + ew * (Epi::kStageBytes / 16);
+      const uint32_t tbase = tmem_base + static_cast<uint32_t>(buf * Tr::ACC_COLS + half * kCols) +
+                             (static_cast<uint32_t>(quarter * 32) << 16);
       if constexpr (!DUAL && epi_overlaps_loads<Epi>::value) {
         // the next chunk's TMEM load is in flight while this chunk is written out
         uint32_t va[32], vb[32];
         tmem_ld32(tbase, va);
         tmem_wait_ld();
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; c += 2) {
-          if (c + 1 < BN / 32) tmem_ld32(tbase + (c + 1) * 32, vb);
+        for (int c = 0; c < kCols / 32; c += 2) {
+          if (c + 1 < kCols / 32) tmem_ld32(tbase + (c + 1) * 32, vb);
           e.chunk(c, va, va);
           tmem_wait_ld();
-          if (c + 1 < BN / 32) {
-            if (c + 2 < BN / 32) tmem_ld32(tbase + (c + 2) * 32, va);
+          if (c + 1 < kCols / 32) {
+            if (c + 2 < kCols / 32) tmem_ld32(tbase + (c + 2) * 32, va);
             e.chunk(c + 1, vb, vb);
             tmem_wait_ld();
           }
         }
       } else {
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < kCols / 32; ++c) {
           uint32_t v0[32];
           uint32_t v1[32];
           tmem_ld32(tbase + c * 32, v0);
@@ -575,12 +596,12 @@ TW_DEV uint32_t sel8(const uint4& v, int q) {
 // ready), not one dependent load per slot. The accumulator's 32 columns of a chunk go
 // through the thread's part of the staging buffer (a row of kUpStride floats, an odd
 // stride, so lanes reading the same column hit distinct banks), where active columns
-// are looked up by index; H leaves through the per-warp transpose, whole 64-byte row
-// segments per store.
+// are looked up by index; H leaves through the per-warp transpose (in the same
+// buffer, once every lane has read its row), whole 64-byte row segments per store.
 struct EpiUpHybrid {
   static constexpr int kUpStride = 33;
-  static constexpr int kWarpFloats = 32 * kUpStride + 32 * 20;  // u staging + bf16 transpose
-  static constexpr int kStageBytes = 4 * kWarpFloats * 4;
+  static constexpr int kStageBytes = 4 * 32 * kUpStride * 4;
+  static constexpr bool kSplitColumns = true;  // eight epilogue warps on 256-wide tiles
   struct Params {
     int T, W, C, nT, R;
     const uint16_t* cnt;
@@ -688,7 +709,8 @@ struct EpiUpHybrid {
       const float h1 = ((mask >> (2 * q + 1)) & 1u) ? mine[2 * q + 1] : 0.f;
       w[q] = pack_bf16x2_rn(h0, h1);
     }
-    transposed_rows_bf16(stage + 32 * kUpStride, w, m0, rows, p.H + col0, p.ldh);
+    __syncwarp();  // every lane has read its staging row: the transpose reuses the buffer
+    transposed_rows_bf16(stage, w, m0, rows, p.H + col0, p.ldh);
   }
   TW_DEV void finish() {}
 };
@@ -706,14 +728,15 @@ struct EpiUpHybrid {
 // The row's entries are read eight at a time (16-byte loads of indices, a and u,
 // issued together; the tile's first eight before the accumulator is ready, after a
 // binary search for the tile's first entry), not one dependent load per entry. A
-// chunk's entries are placed in the thread's staging row (a at column i, u at
-// 32 + i; stride kGradStride, odd) and read back by column; the three outputs leave
-// through the per-warp transpose, whole 64-byte row segments per store.
+// chunk's entries are placed in the thread's staging row, word i = a's bf16 bits |
+// u's fp16 bits << 16 (stride kGradStride, odd), and read back by column; the three
+// outputs leave through the per-warp transpose (in the same buffer, once every lane
+// has read its row), whole 64-byte row segments per store.
 template <bool GATED>
 struct EpiDenseGrad {
-  static constexpr int kGradStride = 65;
-  static constexpr int kWarpFloats = 32 * kGradStride + 32 * 20;  // a / u staging + transpose
-  static constexpr int kStageBytes = 4 * kWarpFloats * 4;
+  static constexpr int kGradStride = 33;
+  static constexpr int kStageBytes = 4 * 32 * kGradStride * 4;
+  static constexpr bool kSplitColumns = true;  // eight epilogue warps on 256-wide tiles
   struct Params {
     int R, I;
     const int32_t* ell_nnz;
@@ -783,7 +806,7 @@ struct EpiDenseGrad {
     if (rows <= 0) return;  // uniform over the warp
     const int col0 = n0 + c * 32;
     uint32_t mask = 0u;
-    float* mine = stage + lane * kGradStride;
+    uint32_t* mine = reinterpret_cast<uint32_t*>(stage) + lane * kGradStride;
     if (valid && ell_row) {
       for (; cur < end; ++cur) {
         if (cur - b_cur >= 8) load_batch(p.R % 8 == 0 ? (cur & ~7) : cur);
@@ -792,8 +815,7 @@ struct EpiDenseGrad {
         if (j >= col0 + 32) break;
         const int i = j - col0;
         if (!TW_CHECKED(i >= 0, p.status)) continue;
-        mine[i] = bf16_to_f32(static_cast<uint16_t>(sel16(ba, q)));
-        if (GATED) mine[32 + i] = f16_to_f32(static_cast<uint16_t>(sel16(bu, q)));
+        mine[i] = sel16(ba, q) | (GATED ? sel16(bu, q) << 16 : 0u);
         mask |= 1u << i;
       }
     }
@@ -805,8 +827,9 @@ struct EpiDenseGrad {
       for (int e = 0; e < 2; ++e) {
         const int i = 2 * q + e;
         const bool act = (mask >> i) & 1u;
-        const float a = act ? mine[i] : 0.f;
-        const float u = GATED ? (act ? mine[32 + i] : 0.f) : 1.f;
+        const uint32_t au = act ? mine[i] : 0u;
+        const float a = bf16_to_f32(static_cast<uint16_t>(au & 0xFFFFu));
+        const float u = GATED ? f16_to_f32(static_cast<uint16_t>(au >> 16)) : 1.f;
         const float d = __uint_as_float(dh[i]);
         g2[e] = act ? (GATED ? d * u : d) + p.l1 : 0.f;
         u2[e] = act ? d * a : 0.f;
@@ -816,10 +839,10 @@ struct EpiDenseGrad {
       wu[q] = pack_f16x2_rn(u2[0], u2[1]);
       wh[q] = pack_f16x2_rn(h2[0], h2[1]);
     }
-    float* tr = stage + 32 * kGradStride;
-    transposed_rows_bf16(tr, wg, m0, rows, p.dG + col0, p.ld);
-    transposed_rows_bf16(tr, wh, m0, rows, p.H + col0, p.ld);
-    if (GATED) transposed_rows_bf16(tr, wu, m0, rows, p.dU + col0, p.ld);
+    __syncwarp();  // every lane has read its staging row: the transposes reuse the buffer
+    transposed_rows_bf16(stage, wg, m0, rows, p.dG + col0, p.ld);
+    transposed_rows_bf16(stage, wh, m0, rows, p.H + col0, p.ld);
+    if (GATED) transposed_rows_bf16(stage, wu, m0, rows, p.dU + col0, p.ld);
   }
   TW_DEV void finish() {}
 };
@@ -884,8 +907,9 @@ struct EpiRedF32 {
 // have one or two nonzeros in a chunk, so the loop is short and has no per-column
 // branch.
 struct EpiTwellPack {
-  static constexpr int kStageBytes = kEpiTransposeBytes;  // 20 words a thread (80 B) fit a warp's region
-  static constexpr int kWordsPerLane = 20;
+  static constexpr int kWordsPerLane = 20;                      // a thread's chunk of bf16 words
+  static constexpr int kStageBytes = 4 * 32 * kWordsPerLane * 4;
+  static constexpr bool kSplitColumns = true;  // eight epilogue warps on 256-wide tiles (W <= 128)
   struct Params {
     int T, W, C, nT;
     uint16_t* cnt;
@@ -954,7 +978,7 @@ struct EpiTwellPack {
     if (any_ovf) p.ovf[m] = 1;
   }
 };
-static_assert(EpiTwellPack::kWordsPerLane * 4 * 32 <= kEpiStageStride * 32 * 4,
+static_assert(EpiTwellPack::kWordsPerLane * 4 * 32 * 4 <= EpiTwellPack::kStageBytes,
               "a warp's staging region holds 32 lanes of 20 words");
 
 // Eight fp32 values as an exact-to-2^-16 pair of bf16 vectors: hi = bf16(v),
