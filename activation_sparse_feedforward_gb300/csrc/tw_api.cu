@@ -516,9 +516,9 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
   const bool sparse_possible = route != TW_ROUTE_DENSE || T == 0;
   if (sparse_possible) TW_TRY(tw::launch_sparse_bwd_tokens(a, s));
   if (dense_possible) {
-    // the dense route: dg, du, h of every ELL row (fp16) from dh = dY Wd^T on the
-    // tensor cores, then dx = dg Wg + du Wu over all rows on fp16 operands (the backup
-    // rows' dx follows below)
+    // the dense route: dg, du, h of every row (fp16; the backup rows' from their saved
+    // fp32 a and u) from dh = dY Wd^T on the tensor cores, then dx = dg Wg + du Wu over
+    // all rows on fp16 operands
     const uint16_t* src[4] = {Wg, x, dy, Wu};
     uint16_t* dst[4] = {w.Wg16, w.X16, w.dY16, w.Wu16};
     const size_t n[4] = {static_cast<size_t>(I) * d, static_cast<size_t>(T) * d, static_cast<size_t>(T) * d,
@@ -530,34 +530,34 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
     TW_TRY(tw::gemm_rows_nmajor_bf16(A, B, gated ? 2 : 1, T, I, d, dx, d, taken, dev_status, s, true, "dense_dx"));
   }
   const bool backup = cap > 0 && T > 0;
-  if (backup) {
+  if (backup && route != TW_ROUTE_DENSE) {
+    // the sparse route's dense backup (the dense route's GEMMs above cover the backup
+    // rows, so these launches do nothing when the call took that route)
     TW_TRY(tw::launch_gather_rows(dy, d, T, saved->backup_tok, saved->n_backup, cap, ra, w.dY, s, dev_status, x, w.X,
-                                  w.acc, d));
+                                  w.acc, d, taken));
     const int32_t* nb = saved->n_backup;
     const tw::BackupGradOut& g = w.g;
     TW_TRY(tw::gemm_backup_grad(w.dY, Wd, ra, nb, cap, d, I, saved->backup_a, gated ? saved->backup_u : nullptr,
-                                l1, g, dev_status, s));
+                                l1, g, dev_status, s, taken));
     // dx = (dG + dG_lo) Wg + (dU + dU_lo) Wu, scattered back to the backup tokens
     const uint16_t* A[4] = {g.dG, g.dG_lo, g.dU, g.dU_lo};
     const uint16_t* B[4] = {Wg, Wg, Wu, Wu};
-    TW_TRY(tw::gemm_rows_times_nmajor_splitk(A, B, gated ? 4 : 2, ra, nb, cap, I, d, w.acc, dev_status, s));
-    TW_TRY(tw::launch_scatter_rows_bf16(w.acc, d, nb, cap, saved->backup_tok, dx, d, T, s));
+    TW_TRY(tw::gemm_rows_times_nmajor_splitk(A, B, gated ? 4 : 2, ra, nb, cap, I, d, w.acc, dev_status, s, taken));
+    TW_TRY(tw::launch_scatter_rows_bf16(w.acc, d, nb, cap, saved->backup_tok, dx, d, T, s, taken));
     // the backup rows' weight gradients are written first (when there are any);
     // the ELL part is then added to them
     // all (two or three) in one launch
     const tw::WeightGradProblem probs[3] = {{g.dG, g.dG_lo, w.X, dWg},
                                             {g.H, g.H_lo, w.dY, dWd},
                                             {g.dU, g.dU_lo, w.X, dWu}};
-    TW_TRY(tw::gemm_weight_grads(probs, gated ? 3 : 2, ra, nb, cap, I, d, dev_status, s));
+    TW_TRY(tw::gemm_weight_grads(probs, gated ? 3 : 2, ra, nb, cap, I, d, dev_status, s, taken));
   }
   a.dW_base_rows = backup ? saved->n_backup : nullptr;
   if (sparse_possible) TW_TRY(tw::launch_sparse_bwd_weights(a, s));
   if (dense_possible) {
-    // dense route weight gradients over all rows (the backup rows' dg, du, h are 0 in
-    // these operands): added to the backup rows' part when there is one
+    // dense route weight gradients over all rows, the backup rows included: written
     const tw::DenseWeightGradProblem probs[3] = {{w.dGd, w.X16, dWg}, {w.Hd, w.dY16, dWd}, {w.dUd, w.X16, dWu}};
-    TW_TRY(tw::gemm_dense_weight_grads(probs, gated ? 3 : 2, T, I, d, backup ? saved->n_backup : nullptr, taken,
-                                       dev_status, s));
+    TW_TRY(tw::gemm_dense_weight_grads(probs, gated ? 3 : 2, T, I, d, nullptr, taken, dev_status, s));
   }
   return TW_OK;
 }

@@ -162,7 +162,7 @@ cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint
 // then writes the bf16 rows out.
 cudaError_t gemm_rows_times_nmajor_splitk(const uint16_t* const* A, const uint16_t* const* B, int segments,
                                           int rows_alloc, const int32_t* n_dev, int cap, int K, int N, float* acc,
-                                          int32_t* status, cudaStream_t s) {
+                                          int32_t* status, cudaStream_t s, const int32_t* sparse_only) {
   if (cap <= 0) return cudaSuccess;
   if (segments < 1 || segments > GEMM_MAX_SEGMENTS || N % 256 != 0) return cudaErrorInvalidValue;
   GemmShape sh = shape_static(0, N, K, status);
@@ -170,6 +170,8 @@ cudaError_t gemm_rows_times_nmajor_splitk(const uint16_t* const* A, const uint16
   sh.m_cap = cap;
   sh.segments = segments;
   sh.ksplit = -1;  // the row count is on the device: the kernel picks the split
+  sh.route_dev = sparse_only;
+  sh.route_want = 0;
   GemmMaps maps;
   for (int i = 0; i < segments; ++i)
     if (!tmap_kmajor(&maps.a[i], A[i], rows_alloc, K, 128) || !tmap_mnmajor(&maps.b[i], B[i], K, N))
@@ -190,10 +192,12 @@ cudaError_t gemm_rows_times_nmajor_splitk(const uint16_t* const* A, const uint16
 template <int BN, bool GATED>
 static cudaError_t backup_grad_bn(const uint16_t* dY, const uint16_t* Wd, int rows_alloc, const int32_t* n_dev,
                                   int cap, int d, int I, const float* a, const float* u, float l1,
-                                  const BackupGradOut& o, int32_t* status, cudaStream_t s) {
+                                  const BackupGradOut& o, int32_t* status, cudaStream_t s, const int32_t* sparse_only) {
   GemmShape sh = shape_static(0, I, d, status);
   sh.m_dev = n_dev;
   sh.m_cap = cap;
+  sh.route_dev = sparse_only;
+  sh.route_want = 0;
   GemmMaps maps;
   if (!tmap_kmajor(&maps.a[0], dY, rows_alloc, d, 128) || !tmap_kmajor(&maps.b[0], Wd, I, d, BN))
     return cudaErrorInvalidValue;
@@ -207,18 +211,18 @@ static cudaError_t backup_grad_bn(const uint16_t* dY, const uint16_t* Wd, int ro
 
 cudaError_t gemm_backup_grad(const uint16_t* dY, const uint16_t* Wd, int rows_alloc, const int32_t* n_dev, int cap,
                              int d, int I, const float* a, const float* u, float l1, const BackupGradOut& o,
-                             int32_t* status, cudaStream_t s) {
+                             int32_t* status, cudaStream_t s, const int32_t* sparse_only) {
   if (cap <= 0) return cudaSuccess;
   const bool gated = u != nullptr;
   if (I % 128 == 0)
-    return gated ? backup_grad_bn<128, true>(dY, Wd, rows_alloc, n_dev, cap, d, I, a, u, l1, o, status, s)
-                 : backup_grad_bn<128, false>(dY, Wd, rows_alloc, n_dev, cap, d, I, a, u, l1, o, status, s);
-  return gated ? backup_grad_bn<64, true>(dY, Wd, rows_alloc, n_dev, cap, d, I, a, u, l1, o, status, s)
-               : backup_grad_bn<64, false>(dY, Wd, rows_alloc, n_dev, cap, d, I, a, u, l1, o, status, s);
+    return gated ? backup_grad_bn<128, true>(dY, Wd, rows_alloc, n_dev, cap, d, I, a, u, l1, o, status, s, sparse_only)
+                 : backup_grad_bn<128, false>(dY, Wd, rows_alloc, n_dev, cap, d, I, a, u, l1, o, status, s, sparse_only);
+  return gated ? backup_grad_bn<64, true>(dY, Wd, rows_alloc, n_dev, cap, d, I, a, u, l1, o, status, s, sparse_only)
+               : backup_grad_bn<64, false>(dY, Wd, rows_alloc, n_dev, cap, d, I, a, u, l1, o, status, s, sparse_only);
 }
 
 cudaError_t gemm_weight_grads(const WeightGradProblem* probs, int n_probs, int rows_alloc, const int32_t* n_dev,
-                              int cap, int I, int d, int32_t* status, cudaStream_t s) {
+                              int cap, int I, int d, int32_t* status, cudaStream_t s, const int32_t* sparse_only) {
   if (cap <= 0 || n_probs <= 0) return cudaSuccess;
   if (n_probs > EpiStoreF32Grouped::kMaxProblems || d % 256 != 0) return cudaErrorInvalidValue;
   GemmShape sh = shape_static(I, d, 0, status);
@@ -226,6 +230,8 @@ cudaError_t gemm_weight_grads(const WeightGradProblem* probs, int n_probs, int r
   sh.k_cap = cap;
   sh.segments = 2;  // P = P_hi + P_lo
   sh.problems = n_probs;
+  sh.route_dev = sparse_only;
+  sh.route_want = 0;
   GemmMaps maps;
   EpiStoreF32Grouped::Params ep{};
   for (int p = 0; p < n_probs; ++p) {
@@ -295,8 +301,22 @@ static cudaError_t dense_grad_bn(const uint16_t* dY, const uint16_t* Wd, int T, 
   GemmMaps maps;
   if (!tmap_kmajor(&maps.a[0], dY, T, d, 128) || !tmap_kmajor(&maps.b[0], Wd, I, d, BN)) return cudaErrorInvalidValue;
   fill_unused(maps, 1, 1);
-  typename EpiDenseGrad<GATED>::Params ep{h.R, I, h.ell_nnz, h.backup_slot, h.ell_idx, h.ell_a, GATED ? h.ell_u : nullptr,
-                                          l1, dG, GATED ? dU : nullptr, H, I, status};
+  typename EpiDenseGrad<GATED>::Params ep{h.R,
+                                          I,
+                                          h.ell_nnz,
+                                          h.backup_slot,
+                                          h.ell_idx,
+                                          h.ell_a,
+                                          GATED ? h.ell_u : nullptr,
+                                          h.backup_cap > 0 ? h.backup_a : nullptr,
+                                          GATED && h.backup_cap > 0 ? h.backup_u : nullptr,
+                                          h.backup_cap,
+                                          l1,
+                                          dG,
+                                          GATED ? dU : nullptr,
+                                          H,
+                                          I,
+                                          status};
   constexpr int kStageBytes = (128 + BN) * 64 * 2;
   constexpr int kBudget = 232448 - 1280 - EpiDenseGrad<GATED>::kStageBytes * (epi_warps<BN, EpiDenseGrad<GATED>>() / 4);
   constexpr int kStages = kBudget / kStageBytes < 8 ? kBudget / kStageBytes : 8;

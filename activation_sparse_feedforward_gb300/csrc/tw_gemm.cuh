@@ -723,8 +723,9 @@ struct EpiUpHybrid {
 // the support, as the operands of the dx and weight-gradient GEMMs (run on fp16: a
 // weight-gradient element sums thousands of these products at high activity, and
 // bf16's 8 significant bits then leave errors above the parity bound where the sum
-// cancels). Rows of the dense backup get zeros (their gradients come from the backup
-// GEMMs).
+// cancels). Rows of the dense backup take their a and u from the saved fp32 backup
+// rows (support a > 0), so the dense GEMMs cover them too and the backup's own
+// backward GEMMs do not run; a row past the backup capacity gets zeros.
 // The row's entries are read eight at a time (16-byte loads of indices, a and u,
 // issued together; the tile's first eight before the accumulator is ready, after a
 // binary search for the tile's first entry), not one dependent load per entry. A
@@ -744,6 +745,9 @@ struct EpiDenseGrad {
     const uint16_t* ell_idx;
     const uint16_t* ell_a;
     const uint16_t* ell_u;
+    const float* backup_a;  // [cap, I] fp32 (may be null when cap == 0)
+    const float* backup_u;
+    int cap;
     float l1;
     uint16_t *dG, *dU, *H;
     int ld;
@@ -752,12 +756,13 @@ struct EpiDenseGrad {
   const Params& p;
   int m, M, n0;
   bool valid, ell_row;
+  int bslot;     // backup slot of the row when it has one below the capacity, else -1
   int cur, end;  // ELL entry cursor and end of the row
   int b_cur;     // first entry of the batch of eight held in bi / ba / bu
   uint4 bi, ba, bu;
   float* stage = nullptr;
   TW_DEV EpiDenseGrad(const Params& p_, int m_, int M_, int n0_)
-      : p(p_), m(m_), M(M_), n0(n0_), valid(m_ < M_), ell_row(false), cur(0), end(0), b_cur(-8) {}
+      : p(p_), m(m_), M(M_), n0(n0_), valid(m_ < M_), ell_row(false), bslot(-1), cur(0), end(0), b_cur(-8) {}
   TW_DEV void load_batch(int e) {
     const size_t base = static_cast<size_t>(m) * p.R + e;
     if (p.R % 8 == 0) {
@@ -781,7 +786,9 @@ struct EpiDenseGrad {
   // search over the row's ascending indices) and the batch holding it
   TW_DEV void prefetch(int) {
     if (!valid) return;
-    ell_row = p.backup_slot[m] == -1;
+    const int slot = p.backup_slot[m];
+    ell_row = slot == -1;
+    if (slot >= 0 && TW_CHECKED(slot < p.cap, p.status)) bslot = slot;
     if (!ell_row) return;
     int n = p.ell_nnz[m];
     if (!TW_CHECKED(n >= 0 && n <= p.R, p.status)) n = 0;
@@ -819,6 +826,30 @@ struct EpiDenseGrad {
         mask |= 1u << i;
       }
     }
+    // a backup row's a and u over the chunk: its saved fp32 rows
+    float ba_[32], bu_[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) ba_[i] = bu_[i] = 0.f;
+    const bool bk = valid && bslot >= 0;
+    if (bk) {
+      const float4* ra = reinterpret_cast<const float4*>(p.backup_a + static_cast<size_t>(bslot) * p.I + col0);
+      const float4* ru = reinterpret_cast<const float4*>(p.backup_u + static_cast<size_t>(bslot) * p.I + col0);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 x = ra[i];
+        ba_[4 * i] = x.x;
+        ba_[4 * i + 1] = x.y;
+        ba_[4 * i + 2] = x.z;
+        ba_[4 * i + 3] = x.w;
+        if (GATED) {
+          const float4 y = ru[i];
+          bu_[4 * i] = y.x;
+          bu_[4 * i + 1] = y.y;
+          bu_[4 * i + 2] = y.z;
+          bu_[4 * i + 3] = y.w;
+        }
+      }
+    }
     uint32_t wg[16], wu[16], wh[16];
 #pragma unroll
     for (int q = 0; q < 16; ++q) {
@@ -826,14 +857,14 @@ struct EpiDenseGrad {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int i = 2 * q + e;
-        const bool act = (mask >> i) & 1u;
-        const uint32_t au = act ? mine[i] : 0u;
-        const float a = bf16_to_f32(static_cast<uint16_t>(au & 0xFFFFu));
-        const float u = GATED ? f16_to_f32(static_cast<uint16_t>(au >> 16)) : 1.f;
+        const uint32_t au = ((mask >> i) & 1u) ? mine[i] : 0u;
+        const bool act = bk ? ba_[i] > 0.f : ((mask >> i) & 1u) != 0u;
+        const float a = bk ? ba_[i] : bf16_to_f32(static_cast<uint16_t>(au & 0xFFFFu));
+        const float u = GATED ? (bk ? bu_[i] : f16_to_f32(static_cast<uint16_t>(au >> 16))) : 1.f;
         const float d = __uint_as_float(dh[i]);
         g2[e] = act ? (GATED ? d * u : d) + p.l1 : 0.f;
         u2[e] = act ? d * a : 0.f;
-        h2[e] = GATED ? a * u : a;
+        h2[e] = act ? (GATED ? a * u : a) : 0.f;
       }
       wg[q] = pack_f16x2_rn(g2[0], g2[1]);
       wu[q] = pack_f16x2_rn(u2[0], u2[1]);

@@ -112,7 +112,7 @@ cudaError_t launch_reinit_rows(uint16_t* W, int I, int d, const int32_t* counts,
 cudaError_t launch_gather_rows(const uint16_t* src, int d, int src_rows, const int32_t* rows, const int32_t* n, int cap,
                                int rows_alloc, uint16_t* out, cudaStream_t s, int32_t* status = nullptr,
                                const uint16_t* src2 = nullptr, uint16_t* out2 = nullptr, float* zero = nullptr,
-                               int zero_row_f32 = 0);
+                               int zero_row_f32 = 0, const int32_t* sparse_only = nullptr);
 
 // Largest per-token entry list of the sparse forward, (I / W) * C: two lists of
 // 10 bytes an entry live in one CTA's shared memory.
@@ -211,9 +211,13 @@ cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint
 // it alongside the row gather); launch_scatter_rows_bf16 writes the finished rows.
 cudaError_t gemm_rows_times_nmajor_splitk(const uint16_t* const* A, const uint16_t* const* B, int segments,
                                           int rows_alloc, const int32_t* n_dev, int cap, int K, int N, float* acc,
-                                          int32_t* status, cudaStream_t s);
+                                          int32_t* status, cudaStream_t s, const int32_t* sparse_only = nullptr);
+// sparse_only (optional, here and below): the launch does its work only when
+// *sparse_only != 1, i.e. when the call took the sparse route (the dense route's
+// backward folds the backup rows into its own GEMMs).
 cudaError_t launch_scatter_rows_bf16(const float* acc, int N, const int32_t* n_dev, int cap, const int32_t* row_map,
-                                     uint16_t* out, int ldo, int out_rows, cudaStream_t s);
+                                     uint16_t* out, int ldo, int out_rows, cudaStream_t s,
+                                     const int32_t* sparse_only = nullptr);
 
 // dense backup backward part 1: dh = dY Wd^T and the epilogue producing dG, dU and H,
 // each as a (hi, lo) bf16 pair [rows_alloc, I].
@@ -222,7 +226,7 @@ struct BackupGradOut {
 };
 cudaError_t gemm_backup_grad(const uint16_t* dY, const uint16_t* Wd, int rows_alloc, const int32_t* n_dev, int cap,
                              int d, int I, const float* a, const float* u, float l1, const BackupGradOut& o,
-                             int32_t* status, cudaStream_t s);
+                             int32_t* status, cudaStream_t s, const int32_t* sparse_only = nullptr);
 // The dense backup rows' weight gradients, D_p = (P_hi,p + P_lo,p)^T Q_p for up to
 // three problems in one launch (P [rows, I] bf16 hi/lo pairs, Q [rows, d] bf16, K =
 // the device row count), written (overwritten) as fp32 [I, d]; nothing is written
@@ -234,7 +238,8 @@ struct WeightGradProblem {
   float* D;
 };
 cudaError_t gemm_weight_grads(const WeightGradProblem* probs, int n_probs, int rows_alloc, const int32_t* n_dev,
-                              int cap, int I, int d, int32_t* status, cudaStream_t s);
+                              int cap, int I, int d, int32_t* status, cudaStream_t s,
+                              const int32_t* sparse_only = nullptr);
 
 // withhold_kb >= 0: the test hook of GemmShape::withhold_kb (a bounded wait runs out)
 // ---------------------------------------------------------------- dense route (tw_gemm.cu)

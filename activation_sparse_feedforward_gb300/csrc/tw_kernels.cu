@@ -459,9 +459,11 @@ struct GatherArgs {
   float* zero;
   int zero_row_f32;  // floats per accumulator row; rows [0, min(n, cap)) are zeroed
   int32_t* status;
+  const int32_t* sparse_only;  // optional: nothing to do when *sparse_only == 1 (the dense route)
 };
 __global__ void __launch_bounds__(256) gather_rows_kernel(const GatherArgs g) {
   pdl_enter();
+  if (g.sparse_only != nullptr && *g.sparse_only == 1) return;
   if (g.status != nullptr && blockIdx.x == 0 && threadIdx.x == 0 && *g.n_dev > g.cap)
     raise_status(g.status, TW_ECAPACITY);
   const int n = min(max(*g.n_dev, 0), g.cap);
@@ -500,8 +502,10 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const GatherArgs g) {
 __global__ void __launch_bounds__(256) scatter_rows_bf16_kernel(const float* __restrict__ acc, int N,
                                                                 const int32_t* __restrict__ n_dev, int cap,
                                                                 const int32_t* __restrict__ row_map,
-                                                                uint16_t* __restrict__ out, int ldo, int out_rows) {
+                                                                uint16_t* __restrict__ out, int ldo, int out_rows,
+                                                                const int32_t* sparse_only) {
   pdl_enter();
+  if (sparse_only != nullptr && *sparse_only == 1) return;
   const int n = min(max(*n_dev, 0), cap);
   const int lane = threadIdx.x & 31;
   const int wpb = blockDim.x >> 5;
@@ -530,18 +534,18 @@ __global__ void __launch_bounds__(256) scatter_rows_bf16_kernel(const float* __r
 }
 
 cudaError_t launch_scatter_rows_bf16(const float* acc, int N, const int32_t* n_dev, int cap, const int32_t* row_map,
-                                     uint16_t* out, int ldo, int out_rows, cudaStream_t s) {
+                                     uint16_t* out, int ldo, int out_rows, cudaStream_t s, const int32_t* sparse_only) {
   if (cap <= 0) return cudaSuccess;
   if (N % 8 != 0 || N > 8 * 32 * kRowVecs) return cudaErrorInvalidValue;
   cudaError_t e = launch(scatter_rows_bf16_kernel, dim3(std::min(warp_grid(cap, 8), device_sm_count() * 2)), dim3(256),
-                         0, s, acc, N, n_dev, cap, row_map, out, ldo, out_rows);
+                         0, s, acc, N, n_dev, cap, row_map, out, ldo, out_rows, sparse_only);
   trace_mark(s, "scatter_rows");
   return e;
 }
 
 cudaError_t launch_gather_rows(const uint16_t* src, int d, int src_rows, const int32_t* rows, const int32_t* n, int cap,
                                int rows_alloc, uint16_t* out, cudaStream_t s, int32_t* status, const uint16_t* src2,
-                               uint16_t* out2, float* zero, int zero_row_f32) {
+                               uint16_t* out2, float* zero, int zero_row_f32, const int32_t* sparse_only) {
   if (rows_alloc <= 0) return cudaSuccess;
   if (d % 8 != 0 || d > 8 * 32 * kRowVecs) return cudaErrorInvalidValue;
   if (zero_row_f32 % 4 != 0 || (zero != nullptr && reinterpret_cast<uintptr_t>(zero) % 16 != 0))
@@ -561,6 +565,7 @@ cudaError_t launch_gather_rows(const uint16_t* src, int d, int src_rows, const i
   g.zero = zero;
   g.zero_row_f32 = zero != nullptr ? zero_row_f32 : 0;
   g.status = status;
+  g.sparse_only = sparse_only;
   const long work = static_cast<long>(rows_alloc) * g.nsrc;
   const int grid = warp_grid(work, 8);
   cudaError_t e = launch(gather_rows_kernel, dim3(std::min(grid, device_sm_count() * 4)), dim3(256), 0, s, g);
