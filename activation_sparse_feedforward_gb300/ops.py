@@ -293,6 +293,16 @@ class HybridFFN:
         self.dWd = torch.empty((I, d), dtype=torch.float32, device=device)
         self.status = new_status(device)
 
+    def fix_route(self) -> str:
+        """Keep the route the last forward took for the following calls (synchronises
+        once): a training loop whose layers change activity slowly decides each layer's
+        route on the device in one step and then launches only that route's kernels.
+        The workspaces sized for the automatic route serve either fixed route."""
+        taken = _lib.TW_ROUTE_DENSE if self.saved.took_dense_route() else _lib.TW_ROUTE_SPARSE
+        self.saved.route = taken
+        self._hs = self.saved.struct()
+        return "dense" if taken == _lib.TW_ROUTE_DENSE else "sparse"
+
     # the buffers a layer may share with others (see HybridScratch)
     @property
     def _fwd_ws(self):

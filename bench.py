@@ -535,13 +535,17 @@ def measure_stack(dev, flush, stream, steps: int, n_layers: int = 28, T: int = 8
     train()
     torch.cuda.synchronize(dev)
     peak_ours = torch.cuda.max_memory_allocated(dev) - mem0
+    # each layer keeps the route the device chose for it in that first step
+    routes = [f.fix_route() for f in ffns]
     ms_f = _time_steps(fwd, steps, 3, flush, stream)
     ms_t = _time_steps(train, steps, 3, flush, stream)
     for l, f in enumerate(ffns):
         tw.raise_if_device_error(f.status, f"stack layer {l}")
     out = {"layers": n_layers, "tokens": T, "fwd_tokens_per_ms": T / ms_f, "train_tokens_per_ms": T / ms_t,
-           "fwd_ms": ms_f, "train_ms": ms_t, "route": f"auto (dense above {DENSE_ABOVE:g} nonzeros per ELL row)",
-           "routes_taken": ["dense" if f.saved.took_dense_route() else "sparse" for f in ffns],
+           "fwd_ms": ms_f, "train_ms": ms_t,
+           "route": f"auto (dense above {DENSE_ABOVE:g} nonzeros per ELL row) in the first step, then each "
+                    "layer's route kept (fix_route)",
+           "routes_taken": routes,
            "layer_buffers": "one shared scratch (workspaces, y, dx) for all layers; per layer: saved Hybrid, dW",
            "n_backup": [int(f.saved.n_backup.item()) for f in ffns],
            "nnz_per_token": [round(float(f.saved.row_nnz.float().mean().item()), 2) for f in ffns]}
