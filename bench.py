@@ -41,6 +41,8 @@ DEFAULT_WORKLOAD = "train_d2048_i5632_m29_o1"
 # the automatic route takes the dense tensor-core path above this many nonzeros per ELL
 # row (the crossover of the two routes measured across the sweep)
 DENSE_ABOVE = 64.0
+# seconds of fp64 oracle work the cpu_baseline sample is sized to
+CPU_TARGET_S = 12.0
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -922,8 +924,14 @@ def run_ours(args, dist: Dist) -> dict | None:
     if not args.no_stack:
         line["stack"] = measure_stack(dev, flush, stream, 3)
     if dist.rank == 0 and not args.no_cpu_baseline:
+        # a probe sample sizes the timed one to about CPU_TARGET_S of oracle work
+        # (capped at the whole batch)
         n_s = args.cpu_sample_tokens
         dt, cores, sample = oracle_sample_time(spec, inp, n_s)
+        grow = min(spec.T, 256 * int(n_s * CPU_TARGET_S / max(dt, 1e-3) / 256))
+        if grow > n_s:
+            n_s = grow
+            dt, cores, sample = oracle_sample_time(spec, inp, n_s)
         line["cpu_baseline"] = {"value": n_s / (dt * 1e3), "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": sample, "seconds": dt}
     return line
@@ -975,7 +983,7 @@ def main():
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the workload's token count (small cases for profiler captures)")
     ap.add_argument("--cpu-sample-tokens", type=int, default=2048)
-    ap.add_argument("--reference-sample-tokens", type=int, default=256)
+    ap.add_argument("--reference-sample-tokens", type=int, default=1024)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
