@@ -132,7 +132,8 @@ struct HybFwdWs {
   uint16_t* H_lo;
   float* acc;  // split-K accumulator of the down projection [ra, d]
   int32_t* sched;  // token scheduling counter of the sparse forward
-  uint16_t* Hd;    // dense route: h of every row [T, I] (null for the sparse route)
+  uint16_t* Hd;    // dense route: fp16 h of every row [T, I] (null for the sparse route)
+  uint16_t* Wd16;  // dense route: fp16 copy of Wd [I, d] (the down GEMM's operand)
 };
 HybFwdWs carve_hybrid_fwd(Carve& c, int T, int d, int I, int W, int C, int backup_cap, int route) {
   const size_t nT = static_cast<size_t>(I / W);
@@ -150,6 +151,7 @@ HybFwdWs carve_hybrid_fwd(Carve& c, int T, int d, int I, int W, int C, int backu
   w.acc = c.take<float>(static_cast<size_t>(ra) * d);
   w.sched = c.take<int32_t>(4);
   w.Hd = route != TW_ROUTE_SPARSE ? c.take<uint16_t>(static_cast<size_t>(T) * I) : nullptr;
+  w.Wd16 = route != TW_ROUTE_SPARSE ? c.take<uint16_t>(static_cast<size_t>(I) * d) : nullptr;
   return w;
 }
 
@@ -434,28 +436,39 @@ tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* 
   a.sched_zeroed = true;  // by compact_rows above
   a.route = taken;
   if (route != TW_ROUTE_DENSE) TW_TRY(tw::launch_token_fwd(a, s));
-  if (route != TW_ROUTE_SPARSE) {
-    // the dense route: h of every ELL row on the tensor cores (and the ELL rows of the
-    // saved Hybrid), then y = h Wd over all rows; the backup rows' y follows below
-    if (gated)
-      TW_TRY(tw::gemm_up_hybrid(x, Wu, T, d, I, o, R, saved->backup_slot, w.Hd, saved->ell_idx, saved->ell_a,
-                                saved->ell_u, taken, dev_status, s));
-    else
-      TW_TRY(tw::launch_twell_to_dense_ell(o, saved->backup_slot, R, w.Hd, saved->ell_idx, saved->ell_a, taken,
-                                           dev_status, s));
-    const uint16_t* A[1] = {w.Hd};
-    const uint16_t* B[1] = {Wd};
-    TW_TRY(tw::gemm_rows_nmajor_bf16(A, B, 1, T, I, d, y, d, taken, dev_status, s, false, "dense_down"));
-  }
+  // the backup rows' fp32 a and u (saved for the backward) on the tensor cores; the
+  // sparse route also takes the hi/lo bf16 pair of their h here and their y below
   if (cap > 0) {
     TW_TRY(tw::launch_gather_rows(x, d, T, saved->backup_tok, saved->n_backup, cap, ra, w.X, s, dev_status, nullptr,
                                   nullptr, w.acc, d));
     TW_TRY(tw::gemm_backup_hidden(w.X, Wg, Wu, ra, saved->n_backup, cap, d, I, w.H, w.H_lo, saved->backup_a,
-                                  gated ? saved->backup_u : nullptr, dev_status, s));
+                                  gated ? saved->backup_u : nullptr, dev_status, s, taken));
+  }
+  if (route != TW_ROUTE_SPARSE) {
+    // the dense route: h of every row on the tensor cores (the ELL rows from the TwELL,
+    // writing the saved Hybrid's ELL; the backup rows from their fp32 a), then
+    // y = h Wd over all rows on fp16 operands
+    {
+      const uint16_t* src[1] = {Wd};
+      uint16_t* dst[1] = {w.Wd16};
+      const size_t n[1] = {static_cast<size_t>(I) * d};
+      TW_TRY(tw::launch_to_f16(src, dst, n, 1, taken, s));
+    }
+    if (gated)
+      TW_TRY(tw::gemm_up_hybrid(x, Wu, T, d, I, o, R, saved->backup_slot, saved->backup_a, cap, w.Hd,
+                                saved->ell_idx, saved->ell_a, saved->ell_u, taken, dev_status, s));
+    else
+      TW_TRY(tw::launch_twell_to_dense_ell(o, saved->backup_slot, saved->backup_a, cap, R, w.Hd, saved->ell_idx,
+                                           saved->ell_a, taken, dev_status, s));
+    const uint16_t* A[1] = {w.Hd};
+    const uint16_t* B[1] = {w.Wd16};
+    TW_TRY(tw::gemm_rows_nmajor_bf16(A, B, 1, T, I, d, y, d, taken, dev_status, s, true, "dense_down"));
+  }
+  if (cap > 0 && route != TW_ROUTE_DENSE) {
     const uint16_t* A[2] = {w.H, w.H_lo};
     const uint16_t* B[2] = {Wd, Wd};
-    TW_TRY(tw::gemm_rows_times_nmajor_splitk(A, B, 2, ra, saved->n_backup, cap, I, d, w.acc, dev_status, s));
-    TW_TRY(tw::launch_scatter_rows_bf16(w.acc, d, saved->n_backup, cap, saved->backup_tok, y, d, T, s));
+    TW_TRY(tw::gemm_rows_times_nmajor_splitk(A, B, 2, ra, saved->n_backup, cap, I, d, w.acc, dev_status, s, taken));
+    TW_TRY(tw::launch_scatter_rows_bf16(w.acc, d, saved->n_backup, cap, saved->backup_tok, y, d, T, s, taken));
   }
   return TW_OK;
 }

@@ -225,11 +225,14 @@ cudaError_t launch_hybrid_unpack(const tw_hybrid& h, float* A, float* U, cudaStr
 }
 
 // ------------------------------------------------------------------ dense route, non-gated
-// Row t without a backup slot: H[t] = its TwELL activations (zeros elsewhere), and its
-// ELL row: the slots of tile k go to ELL offsets starting at the nonzeros of tiles
-// 0 .. k - 1 (a warp scan over the tiles, 32 at a time). Backup rows: H[t] = 0.
+// H is fp16 (the down GEMM's operand). Row t without a backup slot: H[t] = its TwELL
+// activations (zeros elsewhere), and its ELL row: the slots of tile k go to ELL offsets
+// starting at the nonzeros of tiles 0 .. k - 1 (a warp scan over the tiles, 32 at a
+// time). Backup rows: H[t] = fp16 of the saved fp32 a row; rows past the backup
+// capacity: 0.
 __global__ void __launch_bounds__(256) twell_to_dense_ell_kernel(const tw_twell tw, const int32_t* __restrict__ backup_slot,
-                                                                int R, uint16_t* __restrict__ H,
+                                                                const float* __restrict__ backup_a, int cap, int R,
+                                                                uint16_t* __restrict__ H,
                                                                 uint16_t* __restrict__ ell_idx,
                                                                 uint16_t* __restrict__ ell_a, const int32_t* route,
                                                                 int32_t* status) {
@@ -239,8 +242,18 @@ __global__ void __launch_bounds__(256) twell_to_dense_ell_kernel(const tw_twell 
   const int nT = tw.I / tw.W;
   for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < tw.T; t += gridDim.x * 8) {
     uint4* row = reinterpret_cast<uint4*>(H + static_cast<size_t>(t) * tw.I);
+    const int slot = backup_slot[t];
+    if (slot >= 0 && TW_CHECKED(slot < cap, status)) {
+      const float4* src = reinterpret_cast<const float4*>(backup_a + static_cast<size_t>(slot) * tw.I);
+      for (int c = lane; c < tw.I / 8; c += 32) {
+        const float4 x0 = src[2 * c], x1 = src[2 * c + 1];
+        row[c] = make_uint4(pack_f16x2_rn(x0.x, x0.y), pack_f16x2_rn(x0.z, x0.w), pack_f16x2_rn(x1.x, x1.y),
+                            pack_f16x2_rn(x1.z, x1.w));
+      }
+      continue;
+    }
     for (int c = lane; c < tw.I / 8; c += 32) row[c] = make_uint4(0u, 0u, 0u, 0u);
-    if (backup_slot[t] != -1) continue;
+    if (slot != -1) continue;
     __syncwarp();  // the zeros land before any lane's slots
     const size_t rb = static_cast<size_t>(t) * R;
     int base = 0;
@@ -255,7 +268,7 @@ __global__ void __launch_bounds__(256) twell_to_dense_ell_kernel(const tw_twell 
         if (!TW_CHECKED(li < tw.W && off < R, status)) continue;
         const int j = k * tw.W + li;
         const uint16_t v = tw.val[tk * tw.C + s];
-        H[static_cast<size_t>(t) * tw.I + j] = v;
+        H[static_cast<size_t>(t) * tw.I + j] = f32_to_f16(bf16_to_f32(v));
         ell_idx[rb + off] = static_cast<uint16_t>(j);
         ell_a[rb + off] = v;
       }
@@ -264,12 +277,12 @@ __global__ void __launch_bounds__(256) twell_to_dense_ell_kernel(const tw_twell 
   }
 }
 
-cudaError_t launch_twell_to_dense_ell(const tw_twell& tw, const int32_t* backup_slot, int R, uint16_t* H,
-                                      uint16_t* ell_idx, uint16_t* ell_a, const int32_t* route, int32_t* status,
-                                      cudaStream_t s) {
+cudaError_t launch_twell_to_dense_ell(const tw_twell& tw, const int32_t* backup_slot, const float* backup_a, int cap,
+                                      int R, uint16_t* H, uint16_t* ell_idx, uint16_t* ell_a, const int32_t* route,
+                                      int32_t* status, cudaStream_t s) {
   if (tw.T == 0) return cudaSuccess;
-  cudaError_t e = launch(twell_to_dense_ell_kernel, dim3(rows_grid(tw.T)), dim3(256), 0, s, tw, backup_slot, R, H,
-                         ell_idx, ell_a, route, status);
+  cudaError_t e = launch(twell_to_dense_ell_kernel, dim3(rows_grid(tw.T)), dim3(256), 0, s, tw, backup_slot, backup_a,
+                         cap, R, H, ell_idx, ell_a, route, status);
   trace_mark(s, "twell_to_dense_ell");
   return e;
 }

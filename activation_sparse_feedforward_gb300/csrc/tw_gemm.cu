@@ -129,7 +129,8 @@ cudaError_t gemm_gate_relu_dense(const uint16_t* x, const uint16_t* Wg, int T, i
 template <int BN, bool GATED>
 static cudaError_t backup_hidden_bn(const uint16_t* X, const uint16_t* Wg, const uint16_t* Wu, int rows_alloc,
                                     const int32_t* n_dev, int cap, int d, int I, uint16_t* H, uint16_t* H_lo,
-                                    float* save_a, float* save_u, int32_t* status, cudaStream_t s) {
+                                    float* save_a, float* save_u, int32_t* status, cudaStream_t s,
+                                    const int32_t* route) {
   GemmShape sh = shape_static(0, I, d, status);
   sh.m_dev = n_dev;
   sh.m_cap = cap;
@@ -138,7 +139,7 @@ static cudaError_t backup_hidden_bn(const uint16_t* X, const uint16_t* Wg, const
     return cudaErrorInvalidValue;
   if (GATED && !tmap_kmajor(&maps.b[1], Wu, I, d, BN)) return cudaErrorInvalidValue;
   fill_unused(maps, 1, GATED ? 2 : 1);
-  typename EpiBackupHidden<GATED>::Params ep{H, H_lo, save_a, GATED ? save_u : nullptr, I, rows_alloc};
+  typename EpiBackupHidden<GATED>::Params ep{H, H_lo, save_a, GATED ? save_u : nullptr, I, rows_alloc, route};
   constexpr int kStageBytes = (128 + (GATED ? 2 : 1) * BN) * 64 * 2;
   constexpr int kStages = (192 * 1024) / kStageBytes < 8 ? (192 * 1024) / kStageBytes : 8;
   return run_gemm<BN, false, false, GATED, kStages, EpiBackupHidden<GATED>>(maps, sh, ep, cap, s, "backup_hidden");
@@ -146,13 +147,17 @@ static cudaError_t backup_hidden_bn(const uint16_t* X, const uint16_t* Wg, const
 
 cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint16_t* Wu, int rows_alloc,
                                const int32_t* n_dev, int cap, int d, int I, uint16_t* H, uint16_t* H_lo,
-                               float* save_a, float* save_u, int32_t* status, cudaStream_t s) {
+                               float* save_a, float* save_u, int32_t* status, cudaStream_t s,
+                               const int32_t* route) {
   if (cap <= 0) return cudaSuccess;
   if (Wu != nullptr)
-    return backup_hidden_bn<64, true>(X, Wg, Wu, rows_alloc, n_dev, cap, d, I, H, H_lo, save_a, save_u, status, s);
+    return backup_hidden_bn<64, true>(X, Wg, Wu, rows_alloc, n_dev, cap, d, I, H, H_lo, save_a, save_u, status, s,
+                                      route);
   if (I % 128 == 0)
-    return backup_hidden_bn<128, false>(X, Wg, Wu, rows_alloc, n_dev, cap, d, I, H, H_lo, save_a, save_u, status, s);
-  return backup_hidden_bn<64, false>(X, Wg, Wu, rows_alloc, n_dev, cap, d, I, H, H_lo, save_a, save_u, status, s);
+    return backup_hidden_bn<128, false>(X, Wg, Wu, rows_alloc, n_dev, cap, d, I, H, H_lo, save_a, save_u, status, s,
+                                        route);
+  return backup_hidden_bn<64, false>(X, Wg, Wu, rows_alloc, n_dev, cap, d, I, H, H_lo, save_a, save_u, status, s,
+                                     route);
 }
 
 // Same product for few rows, spread over every SM: 256-wide column tiles, each tile's
@@ -258,13 +263,14 @@ static void set_route(GemmShape& sh, const int32_t* route) {
 }
 
 cudaError_t gemm_up_hybrid(const uint16_t* x, const uint16_t* Wu, int T, int d, int I, const tw_twell& tw, int R,
-                           const int32_t* backup_slot, uint16_t* H, uint16_t* ell_idx, uint16_t* ell_a,
-                           uint16_t* ell_u, const int32_t* route, int32_t* status, cudaStream_t s) {
+                           const int32_t* backup_slot, const float* backup_a, int cap, uint16_t* H,
+                           uint16_t* ell_idx, uint16_t* ell_a, uint16_t* ell_u, const int32_t* route,
+                           int32_t* status, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   GemmShape sh = shape_static(T, I, d, status);
   set_route(sh, route);
-  EpiUpHybrid::Params ep{T, tw.W, tw.C, I / tw.W, R, tw.cnt, tw.val, tw.idx, backup_slot, H, I,
-                         ell_idx, ell_a, ell_u, status};
+  EpiUpHybrid::Params ep{T,       tw.W,     tw.C, I / tw.W, R,       tw.cnt,  tw.val,
+                         tw.idx,  backup_slot, backup_a, cap, H, I, ell_idx, ell_a, ell_u, status};
   GemmMaps maps;
   const int bn = (I % 256 == 0) ? 256 : (I % 128 == 0) ? 128 : 64;
   if (!tmap_kmajor(&maps.a[0], x, T, d, 128) || !tmap_kmajor(&maps.b[0], Wu, I, d, bn)) return cudaErrorInvalidValue;

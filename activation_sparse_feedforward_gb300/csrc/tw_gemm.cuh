@@ -586,11 +586,15 @@ TW_DEV uint32_t sel8(const uint4& v, int q) {
 // columns [n0, n0 + BN). With the row's TwELL slots of a (the gate kernel's output;
 // a row served here never overflowed, so its slots hold all its nonzeros) the
 // epilogue forms h = a u at the active columns and writes
-//   H[m][:]        bf16(h) at active columns, 0 elsewhere (the down GEMM's operand),
+//   H[m][:]        fp16(h) at active columns, 0 elsewhere (the down GEMM's operand;
+//                  fp16's 11 significant bits, because the backup rows' large
+//                  activations put bf16's rounding of h above the parity bound),
 //   the ELL row    global index, a and fp16(u) per nonzero, at the row's ELL offset
 //                  (the nonzeros of the row's tiles before this CTA tile),
-// the same ELL the sparse route's token kernel writes. Rows of the dense backup
-// (backup_slot != -1) get H = 0 and no ELL entries.
+// the same ELL the sparse route's token kernel writes. Rows of the dense backup get
+// no ELL entries and H = fp16(a u) from their saved fp32 a (the backup's own GEMM has
+// run before this one) and this accumulator's u, so the down GEMM covers them too; a
+// row past the backup capacity gets H = 0.
 // A TwELL tile's slots are read sixteen at a time (one 16-byte load of indices and
 // two of values, all issued together; the first tile's before the accumulator is
 // ready), not one dependent load per slot. The accumulator's 32 columns of a chunk go
@@ -608,8 +612,10 @@ struct EpiUpHybrid {
     const uint16_t* val;
     const uint8_t* idx;
     const int32_t* backup_slot;
+    const float* backup_a;  // [cap, I] fp32 (may be null when cap == 0)
+    int cap;
     uint16_t* H;
-    int ldh;
+    int ldh;  // row stride of H and backup_a (= I)
     uint16_t* ell_idx;
     uint16_t* ell_a;
     uint16_t* ell_u;
@@ -618,6 +624,7 @@ struct EpiUpHybrid {
   const Params& p;
   int m, M, n0;
   bool valid, ell_row;
+  int bslot;    // backup slot of the row when it has one below the capacity, else -1
   int off;      // ELL slot of the next nonzero of this row
   int k_cur;    // TwELL tile of the slot cursor, its count, the cursor within it
   int n_cur;
@@ -626,8 +633,8 @@ struct EpiUpHybrid {
   uint4 iv, v0, v1;
   float* stage = nullptr;
   TW_DEV EpiUpHybrid(const Params& p_, int m_, int M_, int n0_)
-      : p(p_), m(m_), M(M_), n0(n0_), valid(m_ < M_), ell_row(false), off(0), k_cur(-1), n_cur(0), s_cur(0),
-        g_cur(-16) {}
+      : p(p_), m(m_), M(M_), n0(n0_), valid(m_ < M_), ell_row(false), bslot(-1), off(0), k_cur(-1), n_cur(0),
+        s_cur(0), g_cur(-16) {}
   TW_DEV void load_group(int k, int g) {
     const size_t base = (static_cast<size_t>(m) * p.nT + k) * p.C + g;
     if (p.C % 16 == 0) {
@@ -657,7 +664,9 @@ struct EpiUpHybrid {
   // that tile's first sixteen slots
   TW_DEV void prefetch(int) {
     if (!valid) return;
-    ell_row = p.backup_slot[m] == -1;
+    const int slot = p.backup_slot[m];
+    ell_row = slot == -1;
+    if (slot >= 0 && TW_CHECKED(slot < p.cap, p.status)) bslot = slot;
     if (!ell_row) return;
     const int k0 = n0 / p.W;
     const uint16_t* cr = p.cnt + static_cast<size_t>(m) * p.nT;
@@ -701,13 +710,24 @@ struct EpiUpHybrid {
         }
         ++off;
       }
+    } else if (valid && bslot >= 0) {
+      // a backup row: h = a u with its saved fp32 a (0 off the support)
+      const float4* ra = reinterpret_cast<const float4*>(p.backup_a + static_cast<size_t>(bslot) * p.ldh + col0);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 x = ra[i];
+        const float av[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) mine[4 * i + e] = av[e] > 0.f ? av[e] * __uint_as_float(v[4 * i + e]) : 0.f;
+      }
+      mask = 0xFFFFFFFFu;
     }
     uint32_t w[16];
 #pragma unroll
     for (int q = 0; q < 16; ++q) {
       const float h0 = ((mask >> (2 * q)) & 1u) ? mine[2 * q] : 0.f;
       const float h1 = ((mask >> (2 * q + 1)) & 1u) ? mine[2 * q + 1] : 0.f;
-      w[q] = pack_bf16x2_rn(h0, h1);
+      w[q] = pack_f16x2_rn(h0, h1);
     }
     __syncwarp();  // every lane has read its staging row: the transpose reuses the buffer
     transposed_rows_bf16(stage, w, m0, rows, p.H + col0, p.ldh);
@@ -1045,11 +1065,16 @@ struct EpiBackupHidden {
     float* save_u;  // optional
     int ld;         // row stride of every buffer (= I)
     int rows_alloc; // rows H / H_lo hold
+    // optional route word: when it reads 1 (the dense route, whose own GEMMs take the
+    // backup rows' y) only the saved a and u are written, not H / H_lo
+    const int32_t* route;
   };
   const Params& p;
   int m, M, n0;
+  bool want_h;
   float* stage = nullptr;  // this warp's staging buffer
-  TW_DEV EpiBackupHidden(const Params& p_, int m_, int M_, int n0_) : p(p_), m(m_), M(M_), n0(n0_) {}
+  TW_DEV EpiBackupHidden(const Params& p_, int m_, int M_, int n0_)
+      : p(p_), m(m_), M(M_), n0(n0_), want_h(p_.route == nullptr || *p_.route != 1) {}
   // Every lane of the warp calls it (the stores are warp-cooperative).
   TW_DEV void chunk(int c, const uint32_t (&g)[32], const uint32_t (&u)[32]) {
     const int lane = threadIdx.x & 31;
@@ -1067,7 +1092,7 @@ struct EpiBackupHidden {
     }
     // h = a u (or a), then its two bf16 halves
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
+    for (int half = 0; half < 2 && want_h; ++half) {
       uint32_t w[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {

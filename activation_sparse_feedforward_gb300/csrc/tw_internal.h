@@ -90,12 +90,13 @@ cudaError_t launch_hybrid_pack(const uint16_t* A, const uint16_t* U, int T, int 
                                uint8_t* ovf_ws, int32_t* status, cudaStream_t s);
 // Dense fp32 A [T, I] (and U when non-null) from a Hybrid.
 cudaError_t launch_hybrid_unpack(const tw_hybrid& h, float* A, float* U, cudaStream_t s);
-// Dense route, non-gated forward (only when *route == 1): H [T, I] bf16 = the TwELL's
-// activations on rows without a backup slot (0 on backup rows), and those rows' ELL
-// entries (idx, a) written at their ELL offsets.
-cudaError_t launch_twell_to_dense_ell(const tw_twell& tw, const int32_t* backup_slot, int R, uint16_t* H,
-                                      uint16_t* ell_idx, uint16_t* ell_a, const int32_t* route, int32_t* status,
-                                      cudaStream_t s);
+// Dense route, non-gated forward (only when *route == 1): H [T, I] fp16 = the TwELL's
+// activations on rows without a backup slot, and those rows' ELL entries (idx, a)
+// written at their ELL offsets; backup rows get fp16 of their saved fp32 a (backup_a
+// [cap, I], written by the backup's GEMM before this launch), rows past the capacity 0.
+cudaError_t launch_twell_to_dense_ell(const tw_twell& tw, const int32_t* backup_slot, const float* backup_a, int cap,
+                                      int R, uint16_t* H, uint16_t* ell_idx, uint16_t* ell_a, const int32_t* route,
+                                      int32_t* status, cudaStream_t s);
 
 // ---------------------------------------------------------------- tw_neurons.cu
 cudaError_t launch_neuron_counts(const tw_hybrid& h, int32_t* counts, cudaStream_t s);
@@ -201,10 +202,12 @@ cudaError_t gemm_gate_relu_dense(const uint16_t* x, const uint16_t* Wg, int T, i
                                  int32_t* status, cudaStream_t s);
 
 // dense backup forward: h(X Wg^T, X Wu^T) over n (device) rows of X [rows_alloc, d],
-// written as the bf16 pair H + H_lo; optional saved fp32 a / u.
+// written as the bf16 pair H + H_lo; optional saved fp32 a / u. With a route word
+// that reads 1 (the dense route) only a and u are written.
 cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint16_t* Wu, int rows_alloc,
                                const int32_t* n_dev, int cap, int d, int I, uint16_t* H, uint16_t* H_lo,
-                               float* save_a, float* save_u, int32_t* status, cudaStream_t s);
+                               float* save_a, float* save_u, int32_t* status, cudaStream_t s,
+                               const int32_t* route = nullptr);
 
 // The same product spread over every SM with split K: partial sums are added into
 // the fp32 accumulator acc [cap, N], which must hold zeros (launch_gather_rows zeroes
@@ -245,18 +248,22 @@ cudaError_t gemm_weight_grads(const WeightGradProblem* probs, int n_probs, int r
 // ---------------------------------------------------------------- dense route (tw_gemm.cu)
 // Every launch below does its work only when *route == 1 (route may be null: always).
 // Gated forward: u = x Wu^T over all T rows, with h = a u at the TwELL's active columns
-// written densely into H [T, I] bf16 and the Hybrid's ELL rows (idx, a, bf16 u) of
-// the rows without a backup slot; backup rows get H = 0.
+// written densely into H [T, I] fp16 and the Hybrid's ELL rows (idx, a, fp16 u) of
+// the rows without a backup slot; backup rows get H = fp16(a u) from their saved fp32
+// a (backup_a [cap, I], written by the backup's GEMM before this launch), rows past
+// the capacity H = 0.
 cudaError_t gemm_up_hybrid(const uint16_t* x, const uint16_t* Wu, int T, int d, int I, const tw_twell& tw, int R,
-                           const int32_t* backup_slot, uint16_t* H, uint16_t* ell_idx, uint16_t* ell_a,
-                           uint16_t* ell_u, const int32_t* route, int32_t* status, cudaStream_t s);
+                           const int32_t* backup_slot, const float* backup_a, int cap, uint16_t* H,
+                           uint16_t* ell_idx, uint16_t* ell_a, uint16_t* ell_u, const int32_t* route,
+                           int32_t* status, cudaStream_t s);
 // out [M, N] bf16 (row stride ld) = sum over segments of A_s [M, K] (K-major) B_s [K, N]
 // (N contiguous); operands bf16, or fp16 when f16.
 cudaError_t gemm_rows_nmajor_bf16(const uint16_t* const* A, const uint16_t* const* B, int segments, int M, int K,
                                   int N, uint16_t* out, int ld, const int32_t* route, int32_t* status, cudaStream_t s,
                                   bool f16, const char* label);
 // Backward: dh = dY Wd^T over all T rows; dG, dU (gated) and H [T, I] fp16 from the
-// saved Hybrid's ELL rows (zeros off the support and on backup rows).
+// saved Hybrid's ELL rows and fp32 backup rows (zeros off the support and on rows
+// past the backup capacity).
 cudaError_t gemm_dense_grad(const uint16_t* dY, const uint16_t* Wd, int T, int d, int I, const tw_hybrid& h,
                             bool gated, float l1, uint16_t* dG, uint16_t* dU, uint16_t* H, const int32_t* route,
                             int32_t* status, cudaStream_t s);

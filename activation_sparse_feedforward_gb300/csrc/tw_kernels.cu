@@ -426,9 +426,13 @@ __global__ void __launch_bounds__(1024) compact_rows_kernel(const uint8_t* __res
         tot += sum_w[w];
         nr += rows_w[w];
       }
+      // the sparse route's work per row, in ELL entries: an ELL row its entries, a
+      // backup row 2 dense_above (its hi/lo GEMMs cost about twice the dense route's
+      // per-row work, which dense_above entries price); dense when the mean is larger
+      const double work = static_cast<double>(tot) + 2.0 * static_cast<double>(dense_above) * static_cast<double>(T - nr);
       const bool dense = route_mode == TW_ROUTE_DENSE ||
-                         (route_mode == TW_ROUTE_AUTO && nr > 0 &&
-                          static_cast<double>(tot) > static_cast<double>(dense_above) * static_cast<double>(nr));
+                         (route_mode == TW_ROUTE_AUTO && T > 0 &&
+                          work > static_cast<double>(dense_above) * static_cast<double>(T));
       *route_out = dense ? 1 : 0;
     }
   }

@@ -262,9 +262,10 @@ class HybridScratch:
 class HybridFFN:
     """Preallocated training forward + backward through the Hybrid format.
 
-    route: "sparse" (the pages' CUDA-core gathers for the ELL rows), "dense" (the ELL
-    rows' projections as dense tensor-core GEMMs) or "auto" (decided on the device per
-    forward: dense when the ELL rows' mean nonzeros exceed dense_above). scratch: a
+    route: "sparse" (the pages' CUDA-core gathers for the ELL rows), "dense" (every
+    row's projections as dense tensor-core GEMMs) or "auto" (decided on the device per
+    forward: dense when the mean over rows of the ELL nonzeros, a backup row counting
+    2 dense_above, exceeds dense_above). scratch: a
     HybridScratch shared with other layers (workspaces, y and dx), or None for own
     buffers."""
 

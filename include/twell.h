@@ -126,31 +126,37 @@ typedef struct {
   float* backup_u;
   int32_t* n_backup;
   int32_t route;          /* how the ELL rows' projections run: TW_ROUTE_* below */
-  float dense_above;      /* TW_ROUTE_AUTO: the dense route when the ELL rows' mean
-                             number of nonzeros exceeds this */
+  float dense_above;      /* TW_ROUTE_AUTO: the dense route when the mean over all rows
+                             of (ELL row: its nonzeros; backup row: 2 dense_above)
+                             exceeds this */
   int32_t* route_taken;   /* device int32: the forward writes the route it took (0 sparse,
                              1 dense); the backward takes the same one. May be NULL only
                              with TW_ROUTE_SPARSE */
 } tw_hybrid;
 
-/* Routes of the Hybrid's ELL rows (the backup rows always take the dense tensor-core
- * path with split fp32 operands):
- *  TW_ROUTE_SPARSE  the pages' method: CUDA-core gathers over the active neurons only
- *                   (explainer 2.B "Training Kernels", "Backpropagation");
- *  TW_ROUTE_DENSE   the ELL rows' up / down projections and their backward as dense
+/* Routes of a Hybrid layer's projections. The backup rows' fp32 a and u always come
+ * from a dense tensor-core GEMM.
+ *  TW_ROUTE_SPARSE  the pages' method: CUDA-core gathers over the active neurons of
+ *                   the ELL rows (explainer 2.B "Training Kernels",
+ *                   "Backpropagation"); the backup rows' y, dx and dW from dense GEMMs
+ *                   on split fp32 (hi + lo bf16) operands;
+ *  TW_ROUTE_DENSE   every row's up / down projections and their backward as dense
  *                   tensor-core GEMMs over all neurons, with the TwELL / Hybrid masks
- *                   applied in the GEMM epilogues: the forward on bf16 operands (h
- *                   rounded once to bf16), the backward's dx and dW on fp16 operands
- *                   (dg, du, h rounded once to fp16; fp16 copies of Wg, Wu, x, dy,
- *                   whose magnitudes must stay below 65504); the saved Hybrid is the
- *                   same;
+ *                   applied in the GEMM epilogues (the backup rows' h, dg, du from
+ *                   their saved fp32 a and u): the forward's up GEMM on the bf16
+ *                   inputs, its down GEMM and the backward's dx and dW on fp16
+ *                   operands (h, dg, du rounded once to fp16; fp16 copies of Wd, Wg,
+ *                   Wu, x, dy, whose magnitudes must stay below 65504); the saved
+ *                   Hybrid is the same;
  *  TW_ROUTE_AUTO    decided on the device by each forward, after the gate kernel: dense
- *                   when the ELL rows' mean nonzeros per row exceeds dense_above. A
- *                   row's gathers cost L2 traffic in proportion to its nonzeros, the
- *                   dense GEMMs a fixed amount, so above some activity the dense route
- *                   is faster; the tunx.ai announcement calls the dense backup a
- *                   "safety valve" for high activity, and this extends it to a whole
- *                   call. */
+ *                   when the sparse route's work per row, in ELL entries, exceeds
+ *                   dense_above on average, counting an ELL row's nonzeros and
+ *                   2 dense_above for a backup row (whose split-operand GEMMs cost
+ *                   about twice the dense route's work per row). A row's gathers cost
+ *                   L2 traffic in proportion to its nonzeros, the dense GEMMs a fixed
+ *                   amount, so above some activity the dense route is faster; the
+ *                   tunx.ai page has the dense backup take the rows that activity
+ *                   makes expensive, and this extends that choice to a whole call. */
 #define TW_ROUTE_SPARSE 0
 #define TW_ROUTE_DENSE 1
 #define TW_ROUTE_AUTO 2
@@ -258,14 +264,16 @@ tw_status twell_ffn_fwd_fixed_scratch(const uint16_t* x, const uint16_t* Wg, con
                                       int32_t* dev_status, void* stream);
 
 /* Workspace bytes hybrid_ffn_fwd needs for a Hybrid with the given route (any route
- * other than TW_ROUTE_SPARSE adds the dense route's [T, I] bf16 hidden matrix). */
+ * other than TW_ROUTE_SPARSE adds the dense route's [T, I] fp16 hidden matrix and an
+ * fp16 copy of Wd). */
 size_t hybrid_ffn_fwd_workspace_size(int T, int d, int I, int W, int C, int R, int backup_cap, int route);
 
 /* Training forward (explainer 2.B "Training Kernels"): gate+pack into TwELL,
  * conversion of TwELL into the Hybrid *saved (sizes taken from saved->R and
- * saved->backup_cap), u on the support of ELL rows, y from the ELL rows on the CUDA
- * cores and from the backup rows on the tensor cores. *saved holds what the
- * backward needs. */
+ * saved->backup_cap), the backup rows' fp32 a and u on the tensor cores, u on the
+ * support of ELL rows; y from the ELL rows on the CUDA cores and from the backup
+ * rows on the tensor cores, or, when the call takes the dense route, from one
+ * tensor-core GEMM over all rows. *saved holds what the backward needs. */
 tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* Wu,
                          const uint16_t* Wd, int T, int d, int I, int W, int C,
                          const tw_hybrid* saved, void* ws, size_t ws_bytes,
@@ -280,8 +288,10 @@ size_t hybrid_ffn_bwd_workspace_size(int T, int d, int I, int R, int backup_cap,
  *   dh = dy Wd^T on the support;  du = dh * a;  dg = (dh * u + l1) on the support
  *   (non-gated: dg = dh + l1);  dx = dg Wg + du Wu  (bf16 [T, d]);
  *   dWg = dg^T x, dWu = du^T x, dWd = h^T dy  (fp32 [I, d], overwritten).
- * The ELL part runs on the CUDA cores with the weight gradients accumulated over
- * the transposed Hybrid; backup rows use tensor-core GEMMs. dWu is ignored when
+ * The sparse route runs the ELL part on the CUDA cores with the weight gradients
+ * accumulated over the transposed Hybrid and the backup rows as tensor-core GEMMs;
+ * the dense route (the one the forward took) runs all rows as tensor-core GEMMs.
+ * dWu is ignored when
  * Wu == NULL. TW_EUNSUPPORTED when T * d / 8 exceeds 2^32 - 1 (token rows are
  * addressed by 32-bit offsets). */
 tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* Wg,

@@ -2,7 +2,8 @@
 down projections and their backward as dense tensor-core GEMMs over all neurons,
 with the TwELL / Hybrid masks applied in the GEMM epilogues, against the fp64
 oracle at the usual tolerances; the saved Hybrid equals the sparse route's; the
-automatic route is decided on the device from the ELL rows' mean activity."""
+automatic route is decided on the device from the rows' activity (an ELL row counts
+its nonzeros, a backup row twice the threshold)."""
 import numpy as np
 import pytest
 
@@ -117,17 +118,52 @@ def test_dense_route_saves_the_sparse_routes_hybrid(spec):
     assert_close(f64_of(gd[0]), f64_of(gs[0]), "dx: dense vs sparse route")
 
 
+def _route_work(h, T, dense_above):
+    """The automatic route's measure: mean over rows of the ELL nonzeros, a backup row
+    counting 2 dense_above."""
+    ell = h.saved.ell_nnz[:T].double()
+    backup = (h.saved.backup_slot[:T] != -1)
+    return float((torch.where(backup, torch.full_like(ell, 2.0 * dense_above), ell)).mean())
+
+
 @pytest.mark.parametrize("dense_above,expect_dense", [(10.0, True), (1000.0, False)])
 def test_auto_route_is_decided_on_the_device(dense_above, expect_dense):
     spec = CASES[0]                                   # ELL rows hold ~40 nonzeros on average
     inp = make_inputs(spec, with_dy=True)
     h, y, grads = _step(spec, _dev(inp), "auto", spec.l1, spec.T // 4, dense_above=dense_above)
     assert h.saved.took_dense_route() == expect_dense
-    ell = h.saved.ell_nnz[:spec.T].float()
-    rows = (h.saved.backup_slot[:spec.T] == -1)
-    mean = float(ell[rows].mean())
-    assert (mean > dense_above) == expect_dense
+    assert (_route_work(h, spec.T, dense_above) > dense_above) == expect_dense
     _check_oracle(spec, inp, y, grads, spec.l1)
+
+
+# every row overflows its TwELL (~19 nonzeros per 64-wide tile against C = 4): the
+# whole layer is backup rows
+ALL_BACKUP = [
+    FFNSpec("all_backup_gated", T=300, d=512, I=1024, mean_active=300, outlier_frac=0.0, W=64, C=4, R=64, seed=25),
+    FFNSpec("all_backup_nongated", T=260, d=768, I=1024, gated=False, mean_active=300, outlier_frac=0.0, W=64,
+            C=4, R=64, seed=26),
+]
+
+
+@pytest.mark.parametrize("spec", ALL_BACKUP, ids=lambda s: s.name)
+def test_auto_route_takes_the_dense_route_when_every_row_is_backup(spec):
+    """No ELL rows: the sparse route would run the whole layer on the split-operand
+    backup GEMMs; the automatic route takes the dense route, whose forward forms the
+    backup rows' h from their saved fp32 a, and both agree with the oracle."""
+    inp = make_inputs(spec, with_dy=True)
+    dv = _dev(inp)
+    h, y, grads = _step(spec, dv, "auto", spec.l1, spec.T)
+    assert int(h.saved.n_backup.item()) == spec.T
+    assert h.saved.took_dense_route()
+    assert _route_work(h, spec.T, 64.0) == 128.0
+    _check_oracle(spec, inp, y, grads, spec.l1)
+    hs, ys, gs = _step(spec, dv, "sparse", spec.l1, spec.T)
+    assert not hs.saved.took_dense_route()
+    _check_oracle(spec, inp, ys, gs, spec.l1)
+    # the saved fp32 rows do not depend on the route
+    assert torch.equal(hs.saved.backup_a, h.saved.backup_a)
+    if spec.gated:
+        assert torch.equal(hs.saved.backup_u, h.saved.backup_u)
 
 
 @pytest.mark.parametrize("name,backup_cap", [("train_d2048_i5632_m108_o5", 1280),
