@@ -130,7 +130,10 @@ struct HybFwdWs {
   uint16_t* X;
   uint16_t* H;
   uint16_t* H_lo;
-  float* acc;  // split-K accumulator of the down projection [ra, d]
+  float* acc;  // split-K accumulators [ra, acc_ld]: the down projection (columns [0, d)),
+               // and for a small backup the hidden product's g and u ([d, d + 2 I))
+  int acc_ld;
+  bool split;      // backup_cap <= kBackupSplitRows: the hidden product runs split-K
   int32_t* sched;  // token scheduling counter of the sparse forward
   uint16_t* Hd;    // dense route: fp16 h of every row [T, I] (null for the sparse route)
   uint16_t* Wd16;  // dense route: fp16 copy of Wd [I, d] (the down GEMM's operand)
@@ -148,7 +151,9 @@ HybFwdWs carve_hybrid_fwd(Carve& c, int T, int d, int I, int W, int C, int backu
   w.X = c.take<uint16_t>(static_cast<size_t>(ra) * d);
   w.H = c.take<uint16_t>(static_cast<size_t>(ra) * I);
   w.H_lo = c.take<uint16_t>(static_cast<size_t>(ra) * I);
-  w.acc = c.take<float>(static_cast<size_t>(ra) * d);
+  w.split = backup_cap <= tw::kBackupSplitRows;
+  w.acc_ld = d + (w.split ? 2 * I : 0);
+  w.acc = c.take<float>(static_cast<size_t>(ra) * w.acc_ld);
   w.sched = c.take<int32_t>(4);
   w.Hd = route != TW_ROUTE_SPARSE ? c.take<uint16_t>(static_cast<size_t>(T) * I) : nullptr;
   w.Wd16 = route != TW_ROUTE_SPARSE ? c.take<uint16_t>(static_cast<size_t>(I) * d) : nullptr;
@@ -163,7 +168,10 @@ struct HybBwdWs {
   uint16_t* dY;
   uint16_t* X;
   tw::BackupGradOut g;  // dG, dU, H as (hi, lo) bf16 pairs
-  float* acc;           // split-K accumulator of dx for the backup rows [ra, d]
+  float* acc;           // split-K accumulators [ra, acc_ld]: dx of the backup rows (columns
+                        // [0, d)), and for a small backup dh ([d, d + I))
+  int acc_ld;
+  bool split;           // backup_cap <= kBackupSplitRows: the grad product runs split-K
   int32_t* sched;       // token scheduling counter of the token pass
   uint16_t *dGd, *dUd, *Hd;  // dense route: fp16 dg, du, h of every row [T, I] (null for the sparse route)
   uint16_t *Wg16, *Wu16;     // dense route: fp16 copies of the weights [I, d] (the dx GEMM's operands)
@@ -186,7 +194,9 @@ HybBwdWs carve_hybrid_bwd(Carve& c, int T, int d, int I, int R, int backup_cap, 
   w.g.dU_lo = c.take<uint16_t>(rI);
   w.g.H = c.take<uint16_t>(rI);
   w.g.H_lo = c.take<uint16_t>(rI);
-  w.acc = c.take<float>(static_cast<size_t>(ra) * d);
+  w.split = backup_cap <= tw::kBackupSplitRows;
+  w.acc_ld = d + (w.split ? I : 0);
+  w.acc = c.take<float>(static_cast<size_t>(ra) * w.acc_ld);
   w.sched = c.take<int32_t>(tw::kSchedWords);
   if (route != TW_ROUTE_SPARSE) {
     const size_t TI = static_cast<size_t>(T) * I;
@@ -440,9 +450,10 @@ tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* 
   // sparse route also takes the hi/lo bf16 pair of their h here and their y below
   if (cap > 0) {
     TW_TRY(tw::launch_gather_rows(x, d, T, saved->backup_tok, saved->n_backup, cap, ra, w.X, s, dev_status, nullptr,
-                                  nullptr, w.acc, d));
+                                  nullptr, w.acc, w.acc_ld));
     TW_TRY(tw::gemm_backup_hidden(w.X, Wg, Wu, ra, saved->n_backup, cap, d, I, w.H, w.H_lo, saved->backup_a,
-                                  gated ? saved->backup_u : nullptr, dev_status, s, taken));
+                                  gated ? saved->backup_u : nullptr, dev_status, s, taken,
+                                  w.split ? w.acc + d : nullptr, w.acc_ld));
   }
   if (route != TW_ROUTE_SPARSE) {
     // the dense route: h of every row on the tensor cores (the ELL rows from the TwELL,
@@ -467,8 +478,10 @@ tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* 
   if (cap > 0 && route != TW_ROUTE_DENSE) {
     const uint16_t* A[2] = {w.H, w.H_lo};
     const uint16_t* B[2] = {Wd, Wd};
-    TW_TRY(tw::gemm_rows_times_nmajor_splitk(A, B, 2, ra, saved->n_backup, cap, I, d, w.acc, dev_status, s, taken));
-    TW_TRY(tw::launch_scatter_rows_bf16(w.acc, d, saved->n_backup, cap, saved->backup_tok, y, d, T, s, taken));
+    TW_TRY(tw::gemm_rows_times_nmajor_splitk(A, B, 2, ra, saved->n_backup, cap, I, d, w.acc, dev_status, s, taken,
+                                             w.acc_ld));
+    TW_TRY(tw::launch_scatter_rows_bf16(w.acc, d, saved->n_backup, cap, saved->backup_tok, y, d, T, s, taken,
+                                        w.acc_ld));
   }
   return TW_OK;
 }
@@ -547,16 +560,17 @@ tw_status hybrid_ffn_bwd(const uint16_t* dy, const uint16_t* x, const uint16_t* 
     // the sparse route's dense backup (the dense route's GEMMs above cover the backup
     // rows, so these launches do nothing when the call took that route)
     TW_TRY(tw::launch_gather_rows(dy, d, T, saved->backup_tok, saved->n_backup, cap, ra, w.dY, s, dev_status, x, w.X,
-                                  w.acc, d, taken));
+                                  w.acc, w.acc_ld, taken));
     const int32_t* nb = saved->n_backup;
     const tw::BackupGradOut& g = w.g;
     TW_TRY(tw::gemm_backup_grad(w.dY, Wd, ra, nb, cap, d, I, saved->backup_a, gated ? saved->backup_u : nullptr,
-                                l1, g, dev_status, s, taken));
+                                l1, g, dev_status, s, taken, w.split ? w.acc + d : nullptr, w.acc_ld));
     // dx = (dG + dG_lo) Wg + (dU + dU_lo) Wu, scattered back to the backup tokens
     const uint16_t* A[4] = {g.dG, g.dG_lo, g.dU, g.dU_lo};
     const uint16_t* B[4] = {Wg, Wg, Wu, Wu};
-    TW_TRY(tw::gemm_rows_times_nmajor_splitk(A, B, gated ? 4 : 2, ra, nb, cap, I, d, w.acc, dev_status, s, taken));
-    TW_TRY(tw::launch_scatter_rows_bf16(w.acc, d, nb, cap, saved->backup_tok, dx, d, T, s, taken));
+    TW_TRY(tw::gemm_rows_times_nmajor_splitk(A, B, gated ? 4 : 2, ra, nb, cap, I, d, w.acc, dev_status, s, taken,
+                                             w.acc_ld));
+    TW_TRY(tw::launch_scatter_rows_bf16(w.acc, d, nb, cap, saved->backup_tok, dx, d, T, s, taken, w.acc_ld));
     // the backup rows' weight gradients are written first (when there are any);
     // the ELL part is then added to them
     // all (two or three) in one launch

@@ -122,6 +122,51 @@ cudaError_t gemm_gate_relu_dense(const uint16_t* x, const uint16_t* Wg, int T, i
   return run_gemm<64, false, false, false, 8, EpiReluBf16>(maps, sh, ep, T, s, "gate_dense");
 }
 
+// ------------------------------------------------------------------ dense backup, split-K forms
+// For few backup rows the hidden and grad products would run a fraction of a round of
+// tiles on the SMs (2 row tiles x 44 column tiles at 164 rows); instead each output
+// tile's K loop is cut into units spread over every SM (the split chosen on the device
+// from the actual row count by split_by_cost), whose partial sums are added into
+// fp32 accumulators that the row gather zeroed; a finishing kernel then applies the
+// epilogue's arithmetic (tw_kernels.cu).
+template <int BN>
+static cudaError_t rows_split_bn(const GemmMaps& maps, const GemmShape& sh, const EpiRedF32Grouped::Params& ep,
+                                 int max_rows, cudaStream_t s, const char* label) {
+  constexpr int kStageBytes = (128 + BN) * 64 * 2;
+  constexpr int kStages = (192 * 1024) / kStageBytes < 8 ? (192 * 1024) / kStageBytes : 8;
+  return run_gemm<BN, false, false, false, kStages, EpiRedF32Grouped>(maps, sh, ep, max_rows, s, label);
+}
+
+// acc[p][i][:] += X[i] . B_p^T for the n (device) rows i of X [rows_alloc, K] and
+// problems p < n_b (B_p [N, K], K-major); acc rows have stride ld.
+static cudaError_t rows_times_kmajor_split(const uint16_t* X, const uint16_t* const* B, int n_b, int rows_alloc,
+                                           const int32_t* n_dev, int cap, int K, int N, float* const* acc, int ld,
+                                           int32_t* status, cudaStream_t s, const int32_t* sparse_only,
+                                           const char* label) {
+  if (n_b < 1 || n_b > EpiRedF32Grouped::kMaxProblems || N % 64 != 0) return cudaErrorInvalidValue;
+  GemmShape sh = shape_static(0, N, K, status);
+  sh.m_dev = n_dev;
+  sh.m_cap = cap;
+  sh.problems = n_b;
+  sh.ksplit = -2;
+  sh.route_dev = sparse_only;
+  sh.route_want = 0;
+  const int bn = (N % 256 == 0) ? 256 : (N % 128 == 0) ? 128 : 64;
+  GemmMaps maps;
+  EpiRedF32Grouped::Params ep{};
+  for (int p = 0; p < n_b; ++p) {
+    if (!tmap_kmajor(&maps.a[p], X, rows_alloc, K, 128) || !tmap_kmajor(&maps.b[p], B[p], N, K, bn))
+      return cudaErrorInvalidValue;
+    ep.acc[p] = acc[p];
+  }
+  fill_unused(maps, n_b, n_b);
+  ep.ld = ld;
+  const int max_rows = (cap + GEMM_BM - 1) / GEMM_BM * GEMM_BM * n_b;
+  if (bn == 256) return rows_split_bn<256>(maps, sh, ep, max_rows, s, label);
+  if (bn == 128) return rows_split_bn<128>(maps, sh, ep, max_rows, s, label);
+  return rows_split_bn<64>(maps, sh, ep, max_rows, s, label);
+}
+
 // ------------------------------------------------------------------ dense backup, forward
 // The gated form (two B operands, gate and up, into two accumulators) runs 64-wide
 // column tiles; the non-gated form 128-wide tiles when I allows them, else 64-wide;
@@ -148,8 +193,17 @@ static cudaError_t backup_hidden_bn(const uint16_t* X, const uint16_t* Wg, const
 cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint16_t* Wu, int rows_alloc,
                                const int32_t* n_dev, int cap, int d, int I, uint16_t* H, uint16_t* H_lo,
                                float* save_a, float* save_u, int32_t* status, cudaStream_t s,
-                               const int32_t* route) {
+                               const int32_t* route, float* split_acc, int split_ld) {
   if (cap <= 0) return cudaSuccess;
+  if (split_acc != nullptr) {
+    const uint16_t* B[2] = {Wg, Wu};
+    float* acc[2] = {split_acc, split_acc + I};
+    const cudaError_t e = rows_times_kmajor_split(X, B, Wu != nullptr ? 2 : 1, rows_alloc, n_dev, cap, d, I, acc,
+                                                  split_ld, status, s, nullptr, "backup_hidden");
+    if (e != cudaSuccess) return e;
+    return launch_backup_hidden_finish(split_acc, split_ld, n_dev, cap, I, Wu != nullptr, H, H_lo, rows_alloc, save_a,
+                                       save_u, route, s);
+  }
   if (Wu != nullptr)
     return backup_hidden_bn<64, true>(X, Wg, Wu, rows_alloc, n_dev, cap, d, I, H, H_lo, save_a, save_u, status, s,
                                       route);
@@ -167,7 +221,7 @@ cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint
 // then writes the bf16 rows out.
 cudaError_t gemm_rows_times_nmajor_splitk(const uint16_t* const* A, const uint16_t* const* B, int segments,
                                           int rows_alloc, const int32_t* n_dev, int cap, int K, int N, float* acc,
-                                          int32_t* status, cudaStream_t s, const int32_t* sparse_only) {
+                                          int32_t* status, cudaStream_t s, const int32_t* sparse_only, int ld_acc) {
   if (cap <= 0) return cudaSuccess;
   if (segments < 1 || segments > GEMM_MAX_SEGMENTS || N % 256 != 0) return cudaErrorInvalidValue;
   GemmShape sh = shape_static(0, N, K, status);
@@ -182,7 +236,7 @@ cudaError_t gemm_rows_times_nmajor_splitk(const uint16_t* const* A, const uint16
     if (!tmap_kmajor(&maps.a[i], A[i], rows_alloc, K, 128) || !tmap_mnmajor(&maps.b[i], B[i], K, N))
       return cudaErrorInvalidValue;
   fill_unused(maps, segments, segments);
-  EpiRedF32::Params ep{acc, N};
+  EpiRedF32::Params ep{acc, ld_acc > 0 ? ld_acc : N};
   // segments that come in pairs over one B (the hi / lo halves of a split operand)
   // load that B tile once for both
   bool paired = segments % 2 == 0;
@@ -216,9 +270,19 @@ static cudaError_t backup_grad_bn(const uint16_t* dY, const uint16_t* Wd, int ro
 
 cudaError_t gemm_backup_grad(const uint16_t* dY, const uint16_t* Wd, int rows_alloc, const int32_t* n_dev, int cap,
                              int d, int I, const float* a, const float* u, float l1, const BackupGradOut& o,
-                             int32_t* status, cudaStream_t s, const int32_t* sparse_only) {
+                             int32_t* status, cudaStream_t s, const int32_t* sparse_only, float* split_acc,
+                             int split_ld) {
   if (cap <= 0) return cudaSuccess;
   const bool gated = u != nullptr;
+  if (split_acc != nullptr) {
+    const uint16_t* B[1] = {Wd};
+    float* acc[1] = {split_acc};
+    const cudaError_t e =
+        rows_times_kmajor_split(dY, B, 1, rows_alloc, n_dev, cap, d, I, acc, split_ld, status, s, sparse_only,
+                                "backup_grad");
+    if (e != cudaSuccess) return e;
+    return launch_backup_grad_finish(split_acc, split_ld, n_dev, cap, I, a, u, l1, o, rows_alloc, sparse_only, s);
+  }
   if (I % 128 == 0)
     return gated ? backup_grad_bn<128, true>(dY, Wd, rows_alloc, n_dev, cap, d, I, a, u, l1, o, status, s, sparse_only)
                  : backup_grad_bn<128, false>(dY, Wd, rows_alloc, n_dev, cap, d, I, a, u, l1, o, status, s, sparse_only);

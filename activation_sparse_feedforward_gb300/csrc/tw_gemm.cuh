@@ -51,9 +51,11 @@ struct GemmShape {
                      // p reads maps a/b[p * segments + s]; its row tiles follow the
                      // previous problem's (the epilogue sees rows p * m_tiles * 128 + m)
   int ksplit;        // >= 1: each output tile's K loop is cut into ksplit work units
-                     // (only for epilogues that accumulate, e.g. EpiRedF32); < 0:
+                     // (only for epilogues that accumulate, e.g. EpiRedF32); -1:
                      // chosen on the device from the actual tile count so that the
-                     // units fill the grid once (grid / tiles slices per tile)
+                     // units fill the grid once (grid / tiles slices per tile); -2:
+                     // chosen on the device by split_by_cost (for tile counts near
+                     // the SM count, where whole rounds of units matter)
   int32_t* status;
   int withhold_kb;   // test hook, -1 normally: in a CTA's first work unit, the TMA loads of
                      // this K block are never issued, so the MMA issuer's bounded wait for
@@ -131,6 +133,26 @@ struct GemmTraits {
   static_assert(NA == 1 || (NA == 2 && !DUAL), "paired A segments take one B operand");
 };
 
+// The K split of a launch whose units are handed out to `grid` CTAs in rounds: the
+// number of slices s (at most 16) that minimises rounds x (K blocks a unit + 2), the
+// 2 standing for a unit's fixed cost (pipeline fill, the accumulator's drain and its
+// fp32 reductions). Every thread computes the same value.
+TW_DEV int split_by_cost(int tiles, int kb_total, int grid) {
+  if (tiles <= 0 || kb_total <= 0) return 1;
+  int best = 1;
+  long best_cost = -1;
+  for (int s = 1; s <= min(kb_total, 16); ++s) {
+    const long chunk = (kb_total + s - 1) / s;
+    const long rounds = (static_cast<long>(tiles) * s + grid - 1) / grid;
+    const long cost = rounds * (chunk + 2);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
 template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES, class Epi, int NA = 1>
 __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
     gemm_tc_kernel(const __grid_constant__ GemmMaps maps, const GemmShape shape,
@@ -191,8 +213,10 @@ __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
   const int kb_total = kb_per_seg * (shape.segments / NA);  // one K step covers NA segments
   // work unit = (output tile, slice of its K loop); empty slices are skipped by
   // every role alike
-  const int ksplit = shape.ksplit >= 0 ? max(1, shape.ksplit)
-                                      : (num_tiles > 0 ? max(1, min(kb_total, static_cast<int>(gridDim.x) / num_tiles)) : 1);
+  const int ksplit =
+      shape.ksplit >= 0   ? max(1, shape.ksplit)
+      : shape.ksplit == -2 ? split_by_cost(num_tiles, kb_total, static_cast<int>(gridDim.x))
+                           : (num_tiles > 0 ? max(1, min(kb_total, static_cast<int>(gridDim.x) / num_tiles)) : 1);
   const int kb_chunk = (kb_total + ksplit - 1) / ksplit;
   const int num_units = num_tiles * ksplit;
 
@@ -940,6 +964,33 @@ struct EpiRedF32 {
   TW_DEV void chunk(int c, const uint32_t (&v)[32], const uint32_t (&)[32]) {
     float* col = p.acc + n0 + c * 32;
     transposed_rows(stage, v, m, M, [&](int r, int c4, float4 x) {
+      atomicAdd(reinterpret_cast<float4*>(col + static_cast<size_t>(r) * p.ld) + c4, x);
+    });
+  }
+  TW_DEV void finish() {}
+};
+
+// EpiRedF32 for a grouped launch over a device row count M: problem p's row tiles
+// follow problem p - 1's (M rounded up to whole 128-row tiles each), and its partial
+// sums are added into acc[p] (row stride ld).
+struct EpiRedF32Grouped {
+  static constexpr int kStageBytes = kEpiTransposeBytes;
+  static constexpr bool kOverlapLoads = true;
+  static constexpr int kMaxProblems = 2;
+  struct Params {
+    float* acc[kMaxProblems];
+    int ld;
+  };
+  const Params& p;
+  int m, M, n0;
+  float* stage = nullptr;  // this warp's transpose buffer
+  TW_DEV EpiRedF32Grouped(const Params& p_, int m_, int M_, int n0_) : p(p_), m(m_), M(M_), n0(n0_) {}
+  TW_DEV void chunk(int c, const uint32_t (&v)[32], const uint32_t (&)[32]) {
+    const int rows_per_problem = (M + GEMM_BM - 1) / GEMM_BM * GEMM_BM;
+    const int prob = m / rows_per_problem;  // the same for the warp's 32 rows
+    if (prob >= kMaxProblems) return;       // uniform over the warp
+    float* col = p.acc[prob] + n0 + c * 32;
+    transposed_rows(stage, v, m - prob * rows_per_problem, M, [&](int r, int c4, float4 x) {
       atomicAdd(reinterpret_cast<float4*>(col + static_cast<size_t>(r) * p.ld) + c4, x);
     });
   }

@@ -201,35 +201,54 @@ cudaError_t gemm_gate_pack(const uint16_t* x, const uint16_t* Wg, int T, int d, 
 cudaError_t gemm_gate_relu_dense(const uint16_t* x, const uint16_t* Wg, int T, int d, int I, uint16_t* a,
                                  int32_t* status, cudaStream_t s);
 
+// Backup capacities up to this many rows take the split-K forms of the dense backup's
+// hidden and grad products (gemm_backup_hidden / gemm_backup_grad with split_acc):
+// their fp32 accumulators hold (gated) 2 I or I floats a row, zeroed by the row gather.
+constexpr int kBackupSplitRows = 512;
+
 // dense backup forward: h(X Wg^T, X Wu^T) over n (device) rows of X [rows_alloc, d],
 // written as the bf16 pair H + H_lo; optional saved fp32 a / u. With a route word
-// that reads 1 (the dense route) only a and u are written.
+// that reads 1 (the dense route) only a and u are written. With split_acc (rows of
+// stride split_ld holding g in columns [0, I) and, gated, u in [I, 2 I), rows
+// [0, n) zeroed beforehand) the products run split-K and a finishing kernel follows.
 cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint16_t* Wu, int rows_alloc,
                                const int32_t* n_dev, int cap, int d, int I, uint16_t* H, uint16_t* H_lo,
                                float* save_a, float* save_u, int32_t* status, cudaStream_t s,
-                               const int32_t* route = nullptr);
+                               const int32_t* route = nullptr, float* split_acc = nullptr, int split_ld = 0);
 
 // The same product spread over every SM with split K: partial sums are added into
 // the fp32 accumulator acc [cap, N], which must hold zeros (launch_gather_rows zeroes
 // it alongside the row gather); launch_scatter_rows_bf16 writes the finished rows.
 cudaError_t gemm_rows_times_nmajor_splitk(const uint16_t* const* A, const uint16_t* const* B, int segments,
                                           int rows_alloc, const int32_t* n_dev, int cap, int K, int N, float* acc,
-                                          int32_t* status, cudaStream_t s, const int32_t* sparse_only = nullptr);
+                                          int32_t* status, cudaStream_t s, const int32_t* sparse_only = nullptr,
+                                          int ld_acc = 0);
 // sparse_only (optional, here and below): the launch does its work only when
 // *sparse_only != 1, i.e. when the call took the sparse route (the dense route's
 // backward folds the backup rows into its own GEMMs).
 cudaError_t launch_scatter_rows_bf16(const float* acc, int N, const int32_t* n_dev, int cap, const int32_t* row_map,
                                      uint16_t* out, int ldo, int out_rows, cudaStream_t s,
-                                     const int32_t* sparse_only = nullptr);
+                                     const int32_t* sparse_only = nullptr, int ld_acc = 0);
 
 // dense backup backward part 1: dh = dY Wd^T and the epilogue producing dG, dU and H,
 // each as a (hi, lo) bf16 pair [rows_alloc, I].
 struct BackupGradOut {
   uint16_t *dG, *dG_lo, *dU, *dU_lo, *H, *H_lo;
 };
+// With split_acc (rows of stride split_ld, columns [0, I) zeroed beforehand on rows
+// [0, n)) the product runs split-K and a finishing kernel follows.
 cudaError_t gemm_backup_grad(const uint16_t* dY, const uint16_t* Wd, int rows_alloc, const int32_t* n_dev, int cap,
                              int d, int I, const float* a, const float* u, float l1, const BackupGradOut& o,
-                             int32_t* status, cudaStream_t s, const int32_t* sparse_only = nullptr);
+                             int32_t* status, cudaStream_t s, const int32_t* sparse_only = nullptr,
+                             float* split_acc = nullptr, int split_ld = 0);
+// The finishing kernels of the split-K forms (tw_kernels.cu): the arithmetic of the
+// direct forms' epilogues (EpiBackupHidden, EpiBackupGrad) on the accumulated rows.
+cudaError_t launch_backup_hidden_finish(const float* acc, int ld, const int32_t* n_dev, int cap, int I, bool gated,
+                                        uint16_t* H, uint16_t* H_lo, int rows_alloc, float* save_a, float* save_u,
+                                        const int32_t* route, cudaStream_t s);
+cudaError_t launch_backup_grad_finish(const float* acc, int ld, const int32_t* n_dev, int cap, int I, const float* a,
+                                      const float* u, float l1, const BackupGradOut& o, int rows_alloc,
+                                      const int32_t* sparse_only, cudaStream_t s);
 // The dense backup rows' weight gradients, D_p = (P_hi,p + P_lo,p)^T Q_p for up to
 // three problems in one launch (P [rows, I] bf16 hi/lo pairs, Q [rows, d] bf16, K =
 // the device row count), written (overwritten) as fp32 [I, d]; nothing is written

@@ -501,9 +501,10 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const GatherArgs g) {
     reinterpret_cast<float4*>(g.zero)[k] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// out[row_map[i]][:] = bf16(acc[i][:]) for i < min(*n, cap): the finished rows of a
-// split-K product. One warp per row, 8 columns per lane per step.
-__global__ void __launch_bounds__(256) scatter_rows_bf16_kernel(const float* __restrict__ acc, int N,
+// out[row_map[i]][:] = bf16(acc[i][0 .. N)) for i < min(*n, cap) (acc rows of stride
+// lda): the finished rows of a split-K product. One warp per row, 8 columns per lane
+// per step.
+__global__ void __launch_bounds__(256) scatter_rows_bf16_kernel(const float* __restrict__ acc, int N, int lda,
                                                                 const int32_t* __restrict__ n_dev, int cap,
                                                                 const int32_t* __restrict__ row_map,
                                                                 uint16_t* __restrict__ out, int ldo, int out_rows,
@@ -515,7 +516,7 @@ __global__ void __launch_bounds__(256) scatter_rows_bf16_kernel(const float* __r
   const int wpb = blockDim.x >> 5;
   for (int i = blockIdx.x * wpb + (threadIdx.x >> 5); i < n; i += gridDim.x * wpb) {
     if (!TW_CHECKED(row_map[i] >= 0 && row_map[i] < out_rows, nullptr)) continue;
-    const float4* src = reinterpret_cast<const float4*>(acc + static_cast<size_t>(i) * N);
+    const float4* src = reinterpret_cast<const float4*>(acc + static_cast<size_t>(i) * lda);
     uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(row_map[i]) * ldo);
     // all of the lane's (at most kRowVecs) pieces are loaded before any is stored
     float4 a[kRowVecs], b[kRowVecs];
@@ -538,12 +539,149 @@ __global__ void __launch_bounds__(256) scatter_rows_bf16_kernel(const float* __r
 }
 
 cudaError_t launch_scatter_rows_bf16(const float* acc, int N, const int32_t* n_dev, int cap, const int32_t* row_map,
-                                     uint16_t* out, int ldo, int out_rows, cudaStream_t s, const int32_t* sparse_only) {
+                                     uint16_t* out, int ldo, int out_rows, cudaStream_t s, const int32_t* sparse_only,
+                                     int ld_acc) {
   if (cap <= 0) return cudaSuccess;
-  if (N % 8 != 0 || N > 8 * 32 * kRowVecs) return cudaErrorInvalidValue;
+  const int lda = ld_acc > 0 ? ld_acc : N;
+  if (N % 8 != 0 || N > 8 * 32 * kRowVecs || lda < N || lda % 4 != 0) return cudaErrorInvalidValue;
   cudaError_t e = launch(scatter_rows_bf16_kernel, dim3(std::min(warp_grid(cap, 8), device_sm_count() * 2)), dim3(256),
-                         0, s, acc, N, n_dev, cap, row_map, out, ldo, out_rows, sparse_only);
+                         0, s, acc, N, lda, n_dev, cap, row_map, out, ldo, out_rows, sparse_only);
   trace_mark(s, "scatter_rows");
+  return e;
+}
+
+// ------------------------------------------------------------------ split-K backup: finishing kernels
+// Both take eight columns of one row a thread-step over rows [0, round_up(n, 128))
+// (below rows_alloc); rows past n get zeros in the bf16 outputs, as the direct forms'
+// epilogues write them (the later GEMMs read whole 64-row K blocks of them).
+namespace {
+struct Row8 {
+  float v[8];
+};
+TW_DEV Row8 load8(const float* p) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  return Row8{{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w}};
+}
+TW_DEV void store8(float* p, const Row8& r) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(r.v[0], r.v[1], r.v[2], r.v[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(r.v[4], r.v[5], r.v[6], r.v[7]);
+}
+// the bf16 pair of eight values: hi = bf16(v), lo = bf16(v - hi)
+TW_DEV void store_pair8(uint16_t* hi, uint16_t* lo, size_t off, const Row8& r) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float v0 = r.v[2 * q], v1 = r.v[2 * q + 1];
+    h[q] = pack_bf16x2_rn(v0, v1);
+    l[q] = pack_bf16x2_rn(v0 - bf16_lo(h[q]), v1 - bf16_hi(h[q]));
+  }
+  *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+int finish_grid(int rows_alloc, int I) {
+  const long work = static_cast<long>(rows_alloc) * (I / 8);
+  return static_cast<int>(std::max(1L, std::min<long>((work + 255) / 256, device_sm_count() * 4L)));
+}
+}  // namespace
+
+// Forward: row i < n of acc holds g (columns [0, I)) and, gated, u ([I, 2 I)):
+// a = ReLU(g) (strictly positive g), h = a u (non-gated: a) as the pair H + H_lo, and
+// the saved fp32 a and u. A route word reading 1 (the dense route) skips H and H_lo.
+__global__ void __launch_bounds__(256) backup_hidden_finish_kernel(const float* __restrict__ acc, int ld,
+                                                                   const int32_t* __restrict__ n_dev, int cap, int I,
+                                                                   bool gated, uint16_t* __restrict__ H,
+                                                                   uint16_t* __restrict__ H_lo, int rows_alloc,
+                                                                   float* __restrict__ save_a,
+                                                                   float* __restrict__ save_u, const int32_t* route) {
+  pdl_enter();
+  const int n = min(max(*n_dev, 0), cap);
+  const int rows = min(rows_alloc, (n + 127) / 128 * 128);
+  const bool want_h = route == nullptr || *route != 1;
+  const int v8 = I / 8;
+  const long total = static_cast<long>(rows) * v8;
+  for (long k = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; k < total;
+       k += static_cast<long>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(k / v8);
+    const int c = static_cast<int>(k - static_cast<long>(r) * v8) * 8;
+    const size_t o = static_cast<size_t>(r) * I + c;
+    Row8 h{};
+    if (r < n) {
+      const float* row = acc + static_cast<size_t>(r) * ld;
+      Row8 a = load8(row + c);
+      Row8 u{};
+      if (gated) u = load8(row + I + c);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        a.v[e] = a.v[e] > 0.f ? a.v[e] : 0.f;
+        h.v[e] = gated ? a.v[e] * u.v[e] : a.v[e];
+      }
+      if (save_a != nullptr) store8(save_a + o, a);
+      if (gated && save_u != nullptr) store8(save_u + o, u);
+    }
+    if (want_h) store_pair8(H, H_lo, o, h);
+  }
+}
+
+// Backward: row i < n of acc holds dh = dY Wd^T (columns [0, I)); with the saved fp32
+// a and u, dg = (dh u + l1) where a > 0 (non-gated: dh + l1), du = dh a where a > 0,
+// h = a u (non-gated: a), each as a bf16 pair.
+__global__ void __launch_bounds__(256) backup_grad_finish_kernel(const float* __restrict__ acc, int ld,
+                                                                 const int32_t* __restrict__ n_dev, int cap, int I,
+                                                                 const float* __restrict__ a_sv,
+                                                                 const float* __restrict__ u_sv, float l1,
+                                                                 const BackupGradOut o, int rows_alloc,
+                                                                 const int32_t* sparse_only) {
+  pdl_enter();
+  if (sparse_only != nullptr && *sparse_only == 1) return;
+  const bool gated = u_sv != nullptr;
+  const int n = min(max(*n_dev, 0), cap);
+  const int rows = min(rows_alloc, (n + 127) / 128 * 128);
+  const int v8 = I / 8;
+  const long total = static_cast<long>(rows) * v8;
+  for (long k = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; k < total;
+       k += static_cast<long>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(k / v8);
+    const int c = static_cast<int>(k - static_cast<long>(r) * v8) * 8;
+    const size_t off = static_cast<size_t>(r) * I + c;
+    Row8 dg{}, du{}, h{};
+    if (r < n) {
+      const Row8 dh = load8(acc + static_cast<size_t>(r) * ld + c);
+      const Row8 a = load8(a_sv + off);
+      Row8 u{};
+      if (gated) u = load8(u_sv + off);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const bool act = a.v[e] > 0.f;
+        dg.v[e] = act ? (gated ? dh.v[e] * u.v[e] : dh.v[e]) + l1 : 0.f;
+        du.v[e] = act ? dh.v[e] * a.v[e] : 0.f;
+        h.v[e] = gated ? a.v[e] * u.v[e] : a.v[e];
+      }
+    }
+    store_pair8(o.dG, o.dG_lo, off, dg);
+    if (gated) store_pair8(o.dU, o.dU_lo, off, du);
+    store_pair8(o.H, o.H_lo, off, h);
+  }
+}
+
+cudaError_t launch_backup_hidden_finish(const float* acc, int ld, const int32_t* n_dev, int cap, int I, bool gated,
+                                        uint16_t* H, uint16_t* H_lo, int rows_alloc, float* save_a, float* save_u,
+                                        const int32_t* route, cudaStream_t s) {
+  if (cap <= 0 || rows_alloc <= 0) return cudaSuccess;
+  if (I % 8 != 0 || ld % 4 != 0) return cudaErrorInvalidValue;
+  cudaError_t e = launch(backup_hidden_finish_kernel, dim3(finish_grid(rows_alloc, I)), dim3(256), 0, s, acc, ld,
+                         n_dev, cap, I, gated, H, H_lo, rows_alloc, save_a, save_u, route);
+  trace_mark(s, "backup_hidden_finish");
+  return e;
+}
+
+cudaError_t launch_backup_grad_finish(const float* acc, int ld, const int32_t* n_dev, int cap, int I, const float* a,
+                                      const float* u, float l1, const BackupGradOut& o, int rows_alloc,
+                                      const int32_t* sparse_only, cudaStream_t s) {
+  if (cap <= 0 || rows_alloc <= 0) return cudaSuccess;
+  if (I % 8 != 0 || ld % 4 != 0) return cudaErrorInvalidValue;
+  cudaError_t e = launch(backup_grad_finish_kernel, dim3(finish_grid(rows_alloc, I)), dim3(256), 0, s, acc, ld, n_dev,
+                         cap, I, a, u, l1, o, rows_alloc, sparse_only);
+  trace_mark(s, "backup_grad_finish");
   return e;
 }
 

@@ -15,7 +15,7 @@ namespace tw {
 
 namespace {
 
-constexpr int kWgradUnroll = 4;
+constexpr int kWgradUnroll = 8;
 
 // ---------------------------------------------------------------- row arithmetic
 // The accumulation is bound by instruction issue, so it uses Blackwell's packed

@@ -160,10 +160,12 @@ def test_auto_route_takes_the_dense_route_when_every_row_is_backup(spec):
     hs, ys, gs = _step(spec, dv, "sparse", spec.l1, spec.T)
     assert not hs.saved.took_dense_route()
     _check_oracle(spec, inp, ys, gs, spec.l1)
-    # the saved fp32 rows do not depend on the route
-    assert torch.equal(hs.saved.backup_a, h.saved.backup_a)
+    # the saved fp32 rows do not depend on the route (the same sums, whose split-K
+    # partials may be added in another order)
+    nb = spec.T
+    assert torch.allclose(hs.saved.backup_a[:nb], h.saved.backup_a[:nb], rtol=1e-4, atol=1e-5)
     if spec.gated:
-        assert torch.equal(hs.saved.backup_u, h.saved.backup_u)
+        assert torch.allclose(hs.saved.backup_u[:nb], h.saved.backup_u[:nb], rtol=1e-4, atol=1e-5)
 
 
 @pytest.mark.parametrize("name,backup_cap", [("train_d2048_i5632_m108_o5", 1280),

@@ -162,9 +162,17 @@ def test_hybrid_saved_format_matches_oracle_packing():
     np.testing.assert_array_equal(s.ell_idx.cpu().numpy().view(np.uint16).astype(np.int64)[v], ref["ell_idx"][v])
     np.testing.assert_array_equal(bits_of(s.ell_a)[v], ref["ell_a"][v])
     assert_close(s.ell_u.double().cpu().numpy()[v], ref["ell_u"][v], "ell u")
-    # backup rows hold fp32 a = ReLU(g) and u: a rounds to the TwELL value, u matches the oracle
-    a_b = s.backup_a[:nb].to(torch.bfloat16)
-    np.testing.assert_array_equal(bits_of(a_b), ref["backup_a"])
+    # backup rows hold fp32 a = ReLU(g) and u. The backup's own GEMM sums g in another
+    # order than the gate kernel (a few backup rows take split-K units), so a rounds to
+    # the TwELL value except where the two fp32 sums straddle a bf16 rounding boundary:
+    # there the two bf16 values are adjacent (bit patterns one apart, same sign); where
+    # g is within summation-order error of 0, ReLU may keep a tiny a on one side only
+    a32 = s.backup_a[:nb].cpu().numpy()
+    a_b = bits_of(s.backup_a[:nb].to(torch.bfloat16)).astype(np.int32)
+    diff = np.abs(a_b - ref["backup_a"].astype(np.int32))
+    diff[(np.abs(a32) < 1e-6) & (np.abs(ffn.bf16_to_f64(ref["backup_a"])) < 1e-6)] = 0
+    assert diff.max() <= 1 and (diff > 0).mean() < 1e-3, (int(diff.max()), float((diff > 0).mean()))
+    assert_close(s.backup_a[:nb].double().cpu().numpy(), ffn.bf16_to_f64(ref["backup_a"]), "backup a")
     assert_close(s.backup_u[:nb].cpu().numpy(), ref["backup_u"], "backup u")
 
 
