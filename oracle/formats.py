@@ -18,8 +18,9 @@ are silent:
   the dense path, so TwELL is lossless on the rows it does not flag.
 
 Hybrid (explainer 2.A "Hybrid Format for Training"; wispaper blog, "2. The Hybrid
-Training Algorithm"; tunx.ai announcement, "Details" -- the dense backup as a
-"safety valve"): every row goes either to a compact row-wise ELL of capacity R
+Training Algorithm"; tunx.ai announcement, "Details" -- the dense backup as the
+fallback for rows too active for the ELL): every row goes either to a compact
+row-wise ELL of capacity R
 (global column indices, ascending) or to a dense backup matrix that holds the full
 row. The Hybrid is built from the TwELL of the gate activations (explainer 2.B,
 "Hybrid Conversion"), so a row whose TwELL overflowed (values beyond C were never
