@@ -426,6 +426,21 @@ def measure_inference(dev, flush, stream, steps: int) -> dict:
     return out
 
 
+def probe_backup_cap(spec, x, Wg, Wu, Wd, dev) -> int:
+    """The dense backup sized to hold a workload's backup rows: counted by one forward
+    with room for every row, rounded up to whole 128-row tiles with one spare tile."""
+    import torch
+
+    import activation_sparse_feedforward_gb300 as tw
+
+    probe = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, spec.T, gated=spec.gated, device=dev)
+    probe.forward(x, Wg, Wu, Wd)
+    cap = min(spec.T, 128 * int(math.ceil(int(probe.saved.n_backup.item()) / 128.0)) + 128)
+    del probe
+    torch.cuda.empty_cache()
+    return cap
+
+
 def measure_sweep(dev, flush, stream, steps: int, peaks: dict) -> list:
     """The training step over the sparsity sweep (mean actives x outlier fraction) and
     the non-gated training step, each next to the dense bf16 step on the same inputs,
@@ -444,13 +459,7 @@ def measure_sweep(dev, flush, stream, steps: int, peaks: dict) -> list:
         inp = make_inputs(spec, with_dy=True)
         x, Wg, Wu, Wd, dy = (None if inp[k] is None else torch.from_numpy(inp[k].view(np.int16)).view(torch.bfloat16).to(dev)
                              for k in ("x", "Wg", "Wu", "Wd", "dy"))
-        # the dense backup sized to hold the backup rows (counted by one forward with room
-        # for every row), rounded up to whole 128-row tiles with one spare tile
-        probe = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, spec.T, gated=spec.gated, device=dev)
-        probe.forward(x, Wg, Wu, Wd)
-        cap = min(spec.T, 128 * int(math.ceil(int(probe.saved.n_backup.item()) / 128.0)) + 128)
-        del probe
-        torch.cuda.empty_cache()
+        cap = probe_backup_cap(spec, x, Wg, Wu, Wd, dev)
         row = {"workload": spec.name, "C": spec.C, "R": spec.R, "backup_cap": cap, "dense_above": DENSE_ABOVE}
         for route in ("auto", "sparse", "dense"):
             h = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, cap, gated=spec.gated, device=dev,
@@ -615,7 +624,7 @@ def run_ours(args, dist: Dist) -> dict | None:
         return None if b is None else torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(dev)
 
     x, Wg, Wu, Wd, dy = (to_dev(inp[k]) for k in ("x", "Wg", "Wu", "Wd", "dy"))
-    backup_cap = min(spec.T, max(128, int(math.ceil(spec.outlier_frac * spec.T * 1.5 / 128.0)) * 128 + 128))
+    backup_cap = probe_backup_cap(spec, x, Wg, Wu, Wd, dev)
     h = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, backup_cap, gated=spec.gated, device=dev,
                      route=args.route, dense_above=DENSE_ABOVE)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
