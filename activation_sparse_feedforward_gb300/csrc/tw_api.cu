@@ -449,8 +449,10 @@ tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* 
   // the backup rows' fp32 a and u (saved for the backward) on the tensor cores; the
   // sparse route also takes the hi/lo bf16 pair of their h here and their y below
   if (cap > 0) {
+    // the accumulator holds only the sparse route's y unless the hidden product runs
+    // split-K into it too
     TW_TRY(tw::launch_gather_rows(x, d, T, saved->backup_tok, saved->n_backup, cap, ra, w.X, s, dev_status, nullptr,
-                                  nullptr, w.acc, w.acc_ld));
+                                  nullptr, w.acc, w.acc_ld, nullptr, w.split ? nullptr : taken));
     TW_TRY(tw::gemm_backup_hidden(w.X, Wg, Wu, ra, saved->n_backup, cap, d, I, w.H, w.H_lo, saved->backup_a,
                                   gated ? saved->backup_u : nullptr, dev_status, s, taken,
                                   w.split ? w.acc + d : nullptr, w.acc_ld));

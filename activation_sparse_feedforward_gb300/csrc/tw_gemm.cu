@@ -167,6 +167,38 @@ static cudaError_t rows_times_kmajor_split(const uint16_t* X, const uint16_t* co
   return rows_split_bn<64>(maps, sh, ep, max_rows, s, label);
 }
 
+// save_a = ReLU(X Wg^T) and (when Wu) save_u = X Wu^T over the n (device) rows of X
+// [rows_alloc, d]: one grouped launch of one or two problems on 256-wide tiles (128 or
+// 64 when I requires), fp32 rows of stride I.
+template <int BN>
+static cudaError_t rows_store_bn(const GemmMaps& maps, const GemmShape& sh, const EpiStoreF32RowsGrouped::Params& ep,
+                                 int max_rows, cudaStream_t s) {
+  constexpr int kStageBytes = (128 + BN) * 64 * 2;
+  constexpr int kStages = (192 * 1024) / kStageBytes < 8 ? (192 * 1024) / kStageBytes : 8;
+  return run_gemm<BN, false, false, false, kStages, EpiStoreF32RowsGrouped>(maps, sh, ep, max_rows, s, "backup_hidden");
+}
+static cudaError_t rows_store_a_u(const uint16_t* X, const uint16_t* Wg, const uint16_t* Wu, int rows_alloc,
+                                  const int32_t* n_dev, int cap, int d, int I, float* save_a, float* save_u,
+                                  int32_t* status, cudaStream_t s) {
+  const int n_b = Wu != nullptr ? 2 : 1;
+  GemmShape sh = shape_static(0, I, d, status);
+  sh.m_dev = n_dev;
+  sh.m_cap = cap;
+  sh.problems = n_b;
+  const int bn = (I % 256 == 0) ? 256 : (I % 128 == 0) ? 128 : 64;
+  GemmMaps maps;
+  const uint16_t* B[2] = {Wg, Wu};
+  EpiStoreF32RowsGrouped::Params ep{{save_a, save_u}, I, 1u};
+  for (int p = 0; p < n_b; ++p)
+    if (!tmap_kmajor(&maps.a[p], X, rows_alloc, d, 128) || !tmap_kmajor(&maps.b[p], B[p], I, d, bn))
+      return cudaErrorInvalidValue;
+  fill_unused(maps, n_b, n_b);
+  const int max_rows = (cap + GEMM_BM - 1) / GEMM_BM * GEMM_BM * n_b;
+  if (bn == 256) return rows_store_bn<256>(maps, sh, ep, max_rows, s);
+  if (bn == 128) return rows_store_bn<128>(maps, sh, ep, max_rows, s);
+  return rows_store_bn<64>(maps, sh, ep, max_rows, s);
+}
+
 // ------------------------------------------------------------------ dense backup, forward
 // The gated form (two B operands, gate and up, into two accumulators) runs 64-wide
 // column tiles; the non-gated form 128-wide tiles when I allows them, else 64-wide;
@@ -202,7 +234,17 @@ cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint
                                                   split_ld, status, s, nullptr, "backup_hidden");
     if (e != cudaSuccess) return e;
     return launch_backup_hidden_finish(split_acc, split_ld, n_dev, cap, I, Wu != nullptr, H, H_lo, rows_alloc, save_a,
-                                       save_u, route, s);
+                                       save_u, route, s, false);
+  }
+  if (save_a != nullptr && (Wu == nullptr || save_u != nullptr)) {
+    // a large backup in training: a = ReLU(x Wg^T) and u = x Wu^T stored straight into
+    // the saved fp32 rows by one grouped launch on full-width tiles, then h as its hi /
+    // lo pair from them (only when the call takes the sparse route, whose down GEMM
+    // reads it)
+    const cudaError_t e = rows_store_a_u(X, Wg, Wu, rows_alloc, n_dev, cap, d, I, save_a, save_u, status, s);
+    if (e != cudaSuccess) return e;
+    return launch_backup_hidden_finish(save_a, I, n_dev, cap, I, Wu != nullptr, H, H_lo, rows_alloc, save_a, save_u,
+                                       route, s, true);
   }
   if (Wu != nullptr)
     return backup_hidden_bn<64, true>(X, Wg, Wu, rows_alloc, n_dev, cap, d, I, H, H_lo, save_a, save_u, status, s,

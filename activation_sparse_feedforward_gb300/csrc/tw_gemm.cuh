@@ -529,6 +529,41 @@ struct EpiStoreF32Grouped {
   TW_DEV void finish() {}
 };
 
+// D_p[m][n] = acc (fp32), or ReLU(acc) for the problems whose bit is set in relu, for a
+// grouped launch over a device row count M (problem p's row tiles follow problem
+// p - 1's, M rounded up to whole 128-row tiles each); rows at or past M are skipped.
+struct EpiStoreF32RowsGrouped {
+  static constexpr int kStageBytes = kEpiTransposeBytes;
+  static constexpr bool kOverlapLoads = true;
+  static constexpr int kMaxProblems = 2;
+  struct Params {
+    float* D[kMaxProblems];
+    int ldd;
+    unsigned relu;
+  };
+  const Params& p;
+  int m, M, n0;
+  float* stage = nullptr;  // this warp's transpose buffer
+  TW_DEV EpiStoreF32RowsGrouped(const Params& p_, int m_, int M_, int n0_) : p(p_), m(m_), M(M_), n0(n0_) {}
+  TW_DEV void chunk(int c, const uint32_t (&v)[32], const uint32_t (&)[32]) {
+    const int rows_per_problem = (M + GEMM_BM - 1) / GEMM_BM * GEMM_BM;
+    const int prob = m / rows_per_problem;  // the same for the warp's 32 rows
+    if (prob >= kMaxProblems) return;       // uniform over the warp
+    uint32_t w[32];
+    const bool relu = (p.relu >> prob) & 1u;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float x = __uint_as_float(v[i]);
+      w[i] = __float_as_uint(relu ? (x > 0.f ? x : 0.f) : x);
+    }
+    float* col = p.D[prob] + n0 + c * 32;
+    transposed_rows(stage, w, m - prob * rows_per_problem, M, [&](int r, int c4, float4 x) {
+      reinterpret_cast<float4*>(col + static_cast<size_t>(r) * p.ldd)[c4] = x;
+    });
+  }
+  TW_DEV void finish() {}
+};
+
 // Any epilogue, with its GEMM run on fp16 operands.
 template <class E>
 struct F16Operands : E {
@@ -686,11 +721,15 @@ struct EpiUpHybrid {
   // before the accumulator is ready: the routing of the row, the ELL offset of its
   // first tile in [n0, n0 + BN) (a sum over the counts of the row's earlier tiles) and
   // that tile's first sixteen slots
-  TW_DEV void prefetch(int) {
+  TW_DEV void prefetch(int bn) {
     if (!valid) return;
     const int slot = p.backup_slot[m];
     ell_row = slot == -1;
     if (slot >= 0 && TW_CHECKED(slot < p.cap, p.status)) bslot = slot;
+    if (bslot >= 0) {  // the saved fp32 a of a backup row over the tile's columns, into L2
+      const float* ra = p.backup_a + static_cast<size_t>(bslot) * p.ldh + n0;
+      for (int i = 0; i < bn; i += 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(ra + i));
+    }
     if (!ell_row) return;
     const int k0 = n0 / p.W;
     const uint16_t* cr = p.cnt + static_cast<size_t>(m) * p.nT;
@@ -828,11 +867,18 @@ struct EpiDenseGrad {
   }
   // before the accumulator is ready: the first ELL entry at or past column n0 (binary
   // search over the row's ascending indices) and the batch holding it
-  TW_DEV void prefetch(int) {
+  TW_DEV void prefetch(int bn) {
     if (!valid) return;
     const int slot = p.backup_slot[m];
     ell_row = slot == -1;
     if (slot >= 0 && TW_CHECKED(slot < p.cap, p.status)) bslot = slot;
+    if (bslot >= 0) {  // the saved fp32 a and u of a backup row over the tile's columns, into L2
+      const size_t off = static_cast<size_t>(bslot) * p.I + n0;
+      for (int i = 0; i < bn; i += 32) {
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.backup_a + off + i));
+        if (GATED) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.backup_u + off + i));
+      }
+    }
     if (!ell_row) return;
     int n = p.ell_nnz[m];
     if (!TW_CHECKED(n >= 0 && n <= p.R, p.status)) n = 0;

@@ -108,12 +108,14 @@ cudaError_t launch_reinit_rows(uint16_t* W, int I, int d, const int32_t* counts,
 // rows_alloc) are zero-filled. Row length d bf16. With src2/out2 the same rows of a
 // second matrix are gathered in the same launch; with `zero`, rows [0, min(*n, cap))
 // of that fp32 accumulator (zero_row_f32 floats a row, a multiple of 4) are set to 0
-// for the split-K product that adds into them next.
+// for the split-K product that adds into them next (with zero_if_sparse, only when
+// that route word does not read 1: the accumulator serves only the sparse route).
 // Raises TW_ECAPACITY into `status` (when non-null) if *n > cap.
 cudaError_t launch_gather_rows(const uint16_t* src, int d, int src_rows, const int32_t* rows, const int32_t* n, int cap,
                                int rows_alloc, uint16_t* out, cudaStream_t s, int32_t* status = nullptr,
                                const uint16_t* src2 = nullptr, uint16_t* out2 = nullptr, float* zero = nullptr,
-                               int zero_row_f32 = 0, const int32_t* sparse_only = nullptr);
+                               int zero_row_f32 = 0, const int32_t* sparse_only = nullptr,
+                               const int32_t* zero_if_sparse = nullptr);
 
 // Largest per-token entry list of the sparse forward, (I / W) * C: two lists of
 // 10 bytes an entry live in one CTA's shared memory.
@@ -210,7 +212,9 @@ constexpr int kBackupSplitRows = 512;
 // written as the bf16 pair H + H_lo; optional saved fp32 a / u. With a route word
 // that reads 1 (the dense route) only a and u are written. With split_acc (rows of
 // stride split_ld holding g in columns [0, I) and, gated, u in [I, 2 I), rows
-// [0, n) zeroed beforehand) the products run split-K and a finishing kernel follows.
+// [0, n) zeroed beforehand) the products run split-K and a finishing kernel follows;
+// without it but with the saved rows, a and u are stored by a grouped launch on
+// full-width tiles and H / H_lo formed from them by the finishing kernel.
 cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint16_t* Wu, int rows_alloc,
                                const int32_t* n_dev, int cap, int d, int I, uint16_t* H, uint16_t* H_lo,
                                float* save_a, float* save_u, int32_t* status, cudaStream_t s,
@@ -243,9 +247,11 @@ cudaError_t gemm_backup_grad(const uint16_t* dY, const uint16_t* Wd, int rows_al
                              float* split_acc = nullptr, int split_ld = 0);
 // The finishing kernels of the split-K forms (tw_kernels.cu): the arithmetic of the
 // direct forms' epilogues (EpiBackupHidden, EpiBackupGrad) on the accumulated rows.
+// from_saved: acc is save_a, whose rows already hold a = ReLU(g), and u comes from
+// save_u; only H / H_lo are written (nothing when the route word reads 1).
 cudaError_t launch_backup_hidden_finish(const float* acc, int ld, const int32_t* n_dev, int cap, int I, bool gated,
                                         uint16_t* H, uint16_t* H_lo, int rows_alloc, float* save_a, float* save_u,
-                                        const int32_t* route, cudaStream_t s);
+                                        const int32_t* route, cudaStream_t s, bool from_saved);
 cudaError_t launch_backup_grad_finish(const float* acc, int ld, const int32_t* n_dev, int cap, int I, const float* a,
                                       const float* u, float l1, const BackupGradOut& o, int rows_alloc,
                                       const int32_t* sparse_only, cudaStream_t s);

@@ -464,6 +464,7 @@ struct GatherArgs {
   int zero_row_f32;  // floats per accumulator row; rows [0, min(n, cap)) are zeroed
   int32_t* status;
   const int32_t* sparse_only;  // optional: nothing to do when *sparse_only == 1 (the dense route)
+  const int32_t* zero_if_sparse;  // optional: the accumulator rows are zeroed only when this reads != 1
 };
 __global__ void __launch_bounds__(256) gather_rows_kernel(const GatherArgs g) {
   pdl_enter();
@@ -495,7 +496,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const GatherArgs g) {
       if (lane + 32 * q < vec) o[lane + 32 * q] = v[q];
   }
   // the accumulator rows the split-K product adds into: 16-byte stores over the grid
-  const size_t z4 = static_cast<size_t>(n) * g.zero_row_f32 / 4;
+  const bool zero = g.zero_if_sparse == nullptr || *g.zero_if_sparse != 1;
+  const size_t z4 = zero ? static_cast<size_t>(n) * g.zero_row_f32 / 4 : 0;
   for (size_t k = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < z4;
        k += static_cast<size_t>(gridDim.x) * blockDim.x)
     reinterpret_cast<float4*>(g.zero)[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -587,16 +589,18 @@ int finish_grid(int rows_alloc, int I) {
 // Forward: row i < n of acc holds g (columns [0, I)) and, gated, u ([I, 2 I)):
 // a = ReLU(g) (strictly positive g), h = a u (non-gated: a) as the pair H + H_lo, and
 // the saved fp32 a and u. A route word reading 1 (the dense route) skips H and H_lo.
-__global__ void __launch_bounds__(256) backup_hidden_finish_kernel(const float* __restrict__ acc, int ld,
+// from_saved: acc is save_a, already ReLU(g), u is save_u's row; only H, H_lo.
+__global__ void __launch_bounds__(256) backup_hidden_finish_kernel(const float* acc, int ld,
                                                                    const int32_t* __restrict__ n_dev, int cap, int I,
                                                                    bool gated, uint16_t* __restrict__ H,
                                                                    uint16_t* __restrict__ H_lo, int rows_alloc,
-                                                                   float* __restrict__ save_a,
-                                                                   float* __restrict__ save_u, const int32_t* route) {
+                                                                   float* save_a, float* save_u, const int32_t* route,
+                                                                   bool from_saved) {
   pdl_enter();
+  const bool want_h = route == nullptr || *route != 1;
+  if (from_saved && !want_h) return;
   const int n = min(max(*n_dev, 0), cap);
   const int rows = min(rows_alloc, (n + 127) / 128 * 128);
-  const bool want_h = route == nullptr || *route != 1;
   const int v8 = I / 8;
   const long total = static_cast<long>(rows) * v8;
   for (long k = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; k < total;
@@ -609,14 +613,16 @@ __global__ void __launch_bounds__(256) backup_hidden_finish_kernel(const float* 
       const float* row = acc + static_cast<size_t>(r) * ld;
       Row8 a = load8(row + c);
       Row8 u{};
-      if (gated) u = load8(row + I + c);
+      if (gated) u = load8(from_saved ? save_u + o : row + I + c);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         a.v[e] = a.v[e] > 0.f ? a.v[e] : 0.f;
         h.v[e] = gated ? a.v[e] * u.v[e] : a.v[e];
       }
-      if (save_a != nullptr) store8(save_a + o, a);
-      if (gated && save_u != nullptr) store8(save_u + o, u);
+      if (!from_saved) {
+        if (save_a != nullptr) store8(save_a + o, a);
+        if (gated && save_u != nullptr) store8(save_u + o, u);
+      }
     }
     if (want_h) store_pair8(H, H_lo, o, h);
   }
@@ -665,11 +671,11 @@ __global__ void __launch_bounds__(256) backup_grad_finish_kernel(const float* __
 
 cudaError_t launch_backup_hidden_finish(const float* acc, int ld, const int32_t* n_dev, int cap, int I, bool gated,
                                         uint16_t* H, uint16_t* H_lo, int rows_alloc, float* save_a, float* save_u,
-                                        const int32_t* route, cudaStream_t s) {
+                                        const int32_t* route, cudaStream_t s, bool from_saved) {
   if (cap <= 0 || rows_alloc <= 0) return cudaSuccess;
   if (I % 8 != 0 || ld % 4 != 0) return cudaErrorInvalidValue;
   cudaError_t e = launch(backup_hidden_finish_kernel, dim3(finish_grid(rows_alloc, I)), dim3(256), 0, s, acc, ld,
-                         n_dev, cap, I, gated, H, H_lo, rows_alloc, save_a, save_u, route);
+                         n_dev, cap, I, gated, H, H_lo, rows_alloc, save_a, save_u, route, from_saved);
   trace_mark(s, "backup_hidden_finish");
   return e;
 }
@@ -687,7 +693,8 @@ cudaError_t launch_backup_grad_finish(const float* acc, int ld, const int32_t* n
 
 cudaError_t launch_gather_rows(const uint16_t* src, int d, int src_rows, const int32_t* rows, const int32_t* n, int cap,
                                int rows_alloc, uint16_t* out, cudaStream_t s, int32_t* status, const uint16_t* src2,
-                               uint16_t* out2, float* zero, int zero_row_f32, const int32_t* sparse_only) {
+                               uint16_t* out2, float* zero, int zero_row_f32, const int32_t* sparse_only,
+                               const int32_t* zero_if_sparse) {
   if (rows_alloc <= 0) return cudaSuccess;
   if (d % 8 != 0 || d > 8 * 32 * kRowVecs) return cudaErrorInvalidValue;
   if (zero_row_f32 % 4 != 0 || (zero != nullptr && reinterpret_cast<uintptr_t>(zero) % 16 != 0))
@@ -708,6 +715,7 @@ cudaError_t launch_gather_rows(const uint16_t* src, int d, int src_rows, const i
   g.zero_row_f32 = zero != nullptr ? zero_row_f32 : 0;
   g.status = status;
   g.sparse_only = sparse_only;
+  g.zero_if_sparse = zero_if_sparse;
   const long work = static_cast<long>(rows_alloc) * g.nsrc;
   const int grid = warp_grid(work, 8);
   cudaError_t e = launch(gather_rows_kernel, dim3(std::min(grid, device_sm_count() * 4)), dim3(256), 0, s, g);
