@@ -468,8 +468,10 @@ tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* 
       TW_TRY(tw::launch_to_f16(src, dst, n, 1, taken, s));
     }
     if (gated)
-      TW_TRY(tw::gemm_up_hybrid(x, Wu, T, d, I, o, R, saved->backup_slot, saved->backup_a, cap, w.Hd,
-                                saved->ell_idx, saved->ell_a, saved->ell_u, taken, dev_status, s));
+      // u of the backup rows is saved here unless the split-K backup product saved it
+      TW_TRY(tw::gemm_up_hybrid(x, Wu, T, d, I, o, R, saved->backup_slot, saved->backup_a,
+                                w.split ? nullptr : saved->backup_u, cap, w.Hd, saved->ell_idx, saved->ell_a,
+                                saved->ell_u, taken, dev_status, s));
     else
       TW_TRY(tw::launch_twell_to_dense_ell(o, saved->backup_slot, saved->backup_a, cap, R, w.Hd, saved->ell_idx,
                                            saved->ell_a, taken, dev_status, s));

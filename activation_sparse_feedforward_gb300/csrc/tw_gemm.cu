@@ -179,12 +179,14 @@ static cudaError_t rows_store_bn(const GemmMaps& maps, const GemmShape& sh, cons
 }
 static cudaError_t rows_store_a_u(const uint16_t* X, const uint16_t* Wg, const uint16_t* Wu, int rows_alloc,
                                   const int32_t* n_dev, int cap, int d, int I, float* save_a, float* save_u,
-                                  int32_t* status, cudaStream_t s) {
+                                  int32_t* status, cudaStream_t s, const int32_t* route) {
   const int n_b = Wu != nullptr ? 2 : 1;
   GemmShape sh = shape_static(0, I, d, status);
   sh.m_dev = n_dev;
   sh.m_cap = cap;
   sh.problems = n_b;
+  // the dense route's up GEMM saves u for these rows itself
+  if (n_b == 2) sh.drop_last_problem_if = route;
   const int bn = (I % 256 == 0) ? 256 : (I % 128 == 0) ? 128 : 64;
   GemmMaps maps;
   const uint16_t* B[2] = {Wg, Wu};
@@ -241,7 +243,7 @@ cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint
     // the saved fp32 rows by one grouped launch on full-width tiles, then h as its hi /
     // lo pair from them (only when the call takes the sparse route, whose down GEMM
     // reads it)
-    const cudaError_t e = rows_store_a_u(X, Wg, Wu, rows_alloc, n_dev, cap, d, I, save_a, save_u, status, s);
+    const cudaError_t e = rows_store_a_u(X, Wg, Wu, rows_alloc, n_dev, cap, d, I, save_a, save_u, status, s, route);
     if (e != cudaSuccess) return e;
     return launch_backup_hidden_finish(save_a, I, n_dev, cap, I, Wu != nullptr, H, H_lo, rows_alloc, save_a, save_u,
                                        route, s, true);
@@ -369,14 +371,14 @@ static void set_route(GemmShape& sh, const int32_t* route) {
 }
 
 cudaError_t gemm_up_hybrid(const uint16_t* x, const uint16_t* Wu, int T, int d, int I, const tw_twell& tw, int R,
-                           const int32_t* backup_slot, const float* backup_a, int cap, uint16_t* H,
+                           const int32_t* backup_slot, const float* backup_a, float* backup_u, int cap, uint16_t* H,
                            uint16_t* ell_idx, uint16_t* ell_a, uint16_t* ell_u, const int32_t* route,
                            int32_t* status, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   GemmShape sh = shape_static(T, I, d, status);
   set_route(sh, route);
-  EpiUpHybrid::Params ep{T,       tw.W,     tw.C, I / tw.W, R,       tw.cnt,  tw.val,
-                         tw.idx,  backup_slot, backup_a, cap, H, I, ell_idx, ell_a, ell_u, status};
+  EpiUpHybrid::Params ep{T,      tw.W,        tw.C,     I / tw.W, R,   tw.cnt, tw.val,  tw.idx, backup_slot,
+                         backup_a, backup_u, cap,      H,        I,   ell_idx, ell_a, ell_u,  status};
   GemmMaps maps;
   const int bn = (I % 256 == 0) ? 256 : (I % 128 == 0) ? 128 : 64;
   if (!tmap_kmajor(&maps.a[0], x, T, d, 128) || !tmap_kmajor(&maps.b[0], Wu, I, d, bn)) return cudaErrorInvalidValue;

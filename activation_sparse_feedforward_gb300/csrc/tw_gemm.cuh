@@ -62,6 +62,7 @@ struct GemmShape {
                      // that stage runs out (TW_ETIMEOUT) and every role drains and returns
   const int* route_dev;  // optional: the launch does its work only when *route_dev == route_want
   int route_want;        // (the route a call took, decided on the device by an earlier kernel)
+  const int* drop_last_problem_if;  // optional: when it reads 1, the launch runs one problem fewer
 };
 
 constexpr int GEMM_MAX_SEGMENTS = 6;  // segments x problems
@@ -207,7 +208,8 @@ __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
   if (shape.route_dev != nullptr && *shape.route_dev != shape.route_want) K = 0;  // not this call's route: no work
   const int m_tiles = (M + GEMM_BM - 1) / GEMM_BM;
   const int n_tiles = shape.N / BN;
-  const int problems = max(1, shape.problems);
+  const int problems = max(1, shape.problems) -
+                       ((shape.drop_last_problem_if != nullptr && *shape.drop_last_problem_if == 1) ? 1 : 0);
   const int num_tiles = (K > 0) ? problems * m_tiles * n_tiles : 0;
   const int kb_per_seg = (K + GEMM_BK - 1) / GEMM_BK;
   const int kb_total = kb_per_seg * (shape.segments / NA);  // one K step covers NA segments
@@ -652,8 +654,8 @@ TW_DEV uint32_t sel8(const uint4& v, int q) {
 //                  (the nonzeros of the row's tiles before this CTA tile),
 // the same ELL the sparse route's token kernel writes. Rows of the dense backup get
 // no ELL entries and H = fp16(a u) from their saved fp32 a (the backup's own GEMM has
-// run before this one) and this accumulator's u, so the down GEMM covers them too; a
-// row past the backup capacity gets H = 0.
+// run before this one) and this accumulator's u, which is also saved as their fp32 u,
+// so the down GEMM covers them too; a row past the backup capacity gets H = 0.
 // A TwELL tile's slots are read sixteen at a time (one 16-byte load of indices and
 // two of values, all issued together; the first tile's before the accumulator is
 // ready), not one dependent load per slot. The accumulator's 32 columns of a chunk go
@@ -672,9 +674,11 @@ struct EpiUpHybrid {
     const uint8_t* idx;
     const int32_t* backup_slot;
     const float* backup_a;  // [cap, I] fp32 (may be null when cap == 0)
+    float* backup_u;        // [cap, I] fp32: written for the backup rows (this accumulator's u), or
+                            // null when the backup's own GEMM saved u
     int cap;
     uint16_t* H;
-    int ldh;  // row stride of H and backup_a (= I)
+    int ldh;  // row stride of H, backup_a and backup_u (= I)
     uint16_t* ell_idx;
     uint16_t* ell_a;
     uint16_t* ell_u;
@@ -792,7 +796,28 @@ struct EpiUpHybrid {
       const float h1 = ((mask >> (2 * q + 1)) & 1u) ? mine[2 * q + 1] : 0.f;
       w[q] = pack_f16x2_rn(h0, h1);
     }
-    __syncwarp();  // every lane has read its staging row: the transpose reuses the buffer
+    // the backup rows' fp32 u is saved from here (the backup's own GEMM skips u on this
+    // route): the lanes' rows go through the staging buffer, and each backup row leaves
+    // as whole 128-byte segments at its slot
+    const int my_slot = (valid && bslot >= 0 && p.backup_u != nullptr) ? bslot : -1;
+    if (__any_sync(0xFFFFFFFFu, my_slot >= 0)) {
+      __syncwarp();  // every lane has read its h from the staging row
+#pragma unroll
+      for (int i = 0; i < 32; ++i) mine[i] = __uint_as_float(v[i]);
+      __syncwarp();
+      const int sub = lane >> 3, c8 = lane & 7;
+#pragma unroll
+      for (int r0 = 0; r0 < 32; r0 += 4) {
+        const int r = r0 + sub;
+        const int sl = __shfl_sync(0xFFFFFFFFu, my_slot, r);
+        if (sl >= 0 && r < rows) {
+          const float* src = stage + r * kUpStride + 4 * c8;
+          reinterpret_cast<float4*>(p.backup_u + static_cast<size_t>(sl) * p.ldh + col0)[c8] =
+              make_float4(src[0], src[1], src[2], src[3]);
+        }
+      }
+    }
+    __syncwarp();  // every lane has read the staging rows: the transpose reuses the buffer
     transposed_rows_bf16(stage, w, m0, rows, p.H + col0, p.ldh);
   }
   TW_DEV void finish() {}

@@ -214,7 +214,8 @@ constexpr int kBackupSplitRows = 512;
 // stride split_ld holding g in columns [0, I) and, gated, u in [I, 2 I), rows
 // [0, n) zeroed beforehand) the products run split-K and a finishing kernel follows;
 // without it but with the saved rows, a and u are stored by a grouped launch on
-// full-width tiles and H / H_lo formed from them by the finishing kernel.
+// full-width tiles (u only when the route word does not read 1: the dense route's
+// up GEMM saves it) and H / H_lo formed from them by the finishing kernel.
 cudaError_t gemm_backup_hidden(const uint16_t* X, const uint16_t* Wg, const uint16_t* Wu, int rows_alloc,
                                const int32_t* n_dev, int cap, int d, int I, uint16_t* H, uint16_t* H_lo,
                                float* save_a, float* save_u, int32_t* status, cudaStream_t s,
@@ -275,10 +276,10 @@ cudaError_t gemm_weight_grads(const WeightGradProblem* probs, int n_probs, int r
 // Gated forward: u = x Wu^T over all T rows, with h = a u at the TwELL's active columns
 // written densely into H [T, I] fp16 and the Hybrid's ELL rows (idx, a, fp16 u) of
 // the rows without a backup slot; backup rows get H = fp16(a u) from their saved fp32
-// a (backup_a [cap, I], written by the backup's GEMM before this launch), rows past
-// the capacity H = 0.
+// a (backup_a [cap, I], written by the backup's GEMM before this launch) and their u
+// saved into backup_u (unless null), rows past the capacity H = 0.
 cudaError_t gemm_up_hybrid(const uint16_t* x, const uint16_t* Wu, int T, int d, int I, const tw_twell& tw, int R,
-                           const int32_t* backup_slot, const float* backup_a, int cap, uint16_t* H,
+                           const int32_t* backup_slot, const float* backup_a, float* backup_u, int cap, uint16_t* H,
                            uint16_t* ell_idx, uint16_t* ell_a, uint16_t* ell_u, const int32_t* route,
                            int32_t* status, cudaStream_t s);
 // out [M, N] bf16 (row stride ld) = sum over segments of A_s [M, K] (K-major) B_s [K, N]
