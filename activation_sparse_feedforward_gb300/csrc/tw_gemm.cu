@@ -202,9 +202,10 @@ static cudaError_t rows_store_a_u(const uint16_t* X, const uint16_t* Wg, const u
 }
 
 // ------------------------------------------------------------------ dense backup, forward
-// The gated form (two B operands, gate and up, into two accumulators) runs 64-wide
-// column tiles; the non-gated form 128-wide tiles when I allows them, else 64-wide;
-// as many stages as fit about 192 KB.
+// The form without saved rows (the inference forward's overflow rows): h formed in
+// the epilogue from both accumulators. The gated form (two B operands, gate and up,
+// into two accumulators) runs 64-wide column tiles; the non-gated form 128-wide tiles
+// when I allows them, else 64-wide; as many stages as fit about 192 KB.
 template <int BN, bool GATED>
 static cudaError_t backup_hidden_bn(const uint16_t* X, const uint16_t* Wg, const uint16_t* Wu, int rows_alloc,
                                     const int32_t* n_dev, int cap, int d, int I, uint16_t* H, uint16_t* H_lo,
