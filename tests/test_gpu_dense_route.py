@@ -145,6 +145,34 @@ ALL_BACKUP = [
 ]
 
 
+# backups above 512 rows: a and u stored by the grouped full-width launch (the dense
+# route's up GEMM saving u), rather than the split-K form
+LARGE_BACKUP = [
+    FFNSpec("large_backup_gated", T=700, d=512, I=1024, mean_active=300, outlier_frac=0.0, W=64, C=4, R=64, seed=27),
+    FFNSpec("large_backup_nongated", T=660, d=768, I=1024, gated=False, mean_active=300, outlier_frac=0.0, W=64,
+            C=4, R=64, seed=28),
+    # a mix: 60 % outliers over ordinary rows, so ELL rows and backup rows share tiles
+    FFNSpec("large_backup_mixed", T=900, d=512, I=1280, mean_active=40, outlier_frac=0.6, W=128, C=16, R=96,
+            seed=29),
+]
+
+
+@pytest.mark.parametrize("route", ["sparse", "dense"])
+@pytest.mark.parametrize("spec", LARGE_BACKUP, ids=lambda s: s.name)
+def test_large_backup_matches_oracle(spec, route):
+    inp = make_inputs(spec, with_dy=True)
+    h, y, grads = _step(spec, _dev(inp), route, spec.l1, spec.T)
+    nb = int(h.saved.n_backup.item())
+    assert nb > 512, nb
+    _check_oracle(spec, inp, y, grads, spec.l1)
+    # the saved fp32 rows: a = ReLU(g) and u of the backup tokens
+    rows = h.saved.backup_tok[:nb].cpu().numpy()
+    f = ffn.forward(inp["x"][rows], inp["Wg"], inp["Wu"], inp["Wd"])
+    assert_close(h.saved.backup_a[:nb].double().cpu().numpy(), f["a"], "backup a")
+    if spec.gated:
+        assert_close(h.saved.backup_u[:nb].double().cpu().numpy(), f["u"], "backup u")
+
+
 @pytest.mark.parametrize("spec", ALL_BACKUP, ids=lambda s: s.name)
 def test_auto_route_takes_the_dense_route_when_every_row_is_backup(spec):
     """No ELL rows: the sparse route would run the whole layer on the split-operand
