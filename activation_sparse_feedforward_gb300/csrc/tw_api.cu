@@ -439,13 +439,20 @@ tw_status hybrid_ffn_fwd(const uint16_t* x, const uint16_t* Wg, const uint16_t* 
   a.T = T; a.d = d; a.I = I; a.W = W; a.C = C; a.nT = I / W; a.L = (I / W) * C;
   a.cnt = o.cnt; a.val = o.val; a.idx = o.idx; a.ovf = o.ovf;
   a.backup_slot = saved->backup_slot;
+  a.ell_nnz = saved->ell_nnz;
   a.ell_idx = saved->ell_idx; a.ell_a = saved->ell_a; a.ell_u = saved->ell_u; a.R = R;
   a.y = y;
   a.status = dev_status;
   a.sched = w.sched;
   a.sched_zeroed = true;  // by compact_rows above
   a.route = taken;
-  if (route != TW_ROUTE_DENSE) TW_TRY(tw::launch_token_fwd(a, s));
+  if (route != TW_ROUTE_DENSE) {
+    // gated: the ELL rows' idx and a from the TwELL first (a warp a row), which the
+    // token kernel then reads as its entry lists
+    if (gated) TW_TRY(tw::launch_twell_to_ell(o, saved->backup_slot, R, saved->ell_idx, saved->ell_a, taken,
+                                              dev_status, s));
+    TW_TRY(tw::launch_token_fwd(a, s));
+  }
   // the backup rows' fp32 a and u (saved for the backward) on the tensor cores; the
   // sparse route also takes the hi/lo bf16 pair of their h here and their y below
   if (cap > 0) {

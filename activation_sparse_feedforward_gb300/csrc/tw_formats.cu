@@ -277,6 +277,89 @@ __global__ void __launch_bounds__(256) twell_to_dense_ell_kernel(const tw_twell 
   }
 }
 
+// The ELL rows' entries (idx, a) alone, for the sparse route's forward: a warp a row,
+// lane l taking TwELL tiles 2 l and 2 l + 1 of each group of 64; a group's loads (the
+// row's backup slot, the tiles' counts and their first sixteen slots as 16-byte
+// vectors) are issued together before the warp scan that places the tiles' slots at
+// their ELL offsets.
+namespace {
+struct TileSlots {
+  int n;
+  uint4 iv, v0, v1;
+};
+TW_DEV TileSlots load_tile(const tw_twell& tw, size_t tk, bool live, bool vec) {
+  TileSlots r{0, make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+  if (live) {
+    r.n = min(static_cast<int>(tw.cnt[tk]), tw.C);
+    if (vec) {
+      r.iv = *reinterpret_cast<const uint4*>(tw.idx + tk * tw.C);
+      r.v0 = *reinterpret_cast<const uint4*>(tw.val + tk * tw.C);
+      r.v1 = *reinterpret_cast<const uint4*>(tw.val + tk * tw.C + 8);
+    }
+  }
+  return r;
+}
+TW_DEV void put_tile(const tw_twell& tw, const TileSlots& ts, size_t tk, int k, int off, int R, size_t rb,
+                     uint16_t* ell_idx, uint16_t* ell_a, bool vec, int32_t* status) {
+  if (vec) {
+    const uint32_t iw[4] = {ts.iv.x, ts.iv.y, ts.iv.z, ts.iv.w};
+    const uint32_t vw[8] = {ts.v0.x, ts.v0.y, ts.v0.z, ts.v0.w, ts.v1.x, ts.v1.y, ts.v1.z, ts.v1.w};
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+      if (s >= ts.n) break;
+      const int li = static_cast<int>((iw[s >> 2] >> (8 * (s & 3))) & 0xFFu);
+      if (!TW_CHECKED(li < tw.W && off + s < R, status)) continue;
+      ell_idx[rb + off + s] = static_cast<uint16_t>(k * tw.W + li);
+      ell_a[rb + off + s] = static_cast<uint16_t>(vw[s >> 1] >> (16 * (s & 1)));
+    }
+  }
+  for (int s = vec ? 16 : 0; s < ts.n; ++s) {
+    const int li = tw.idx[tk * tw.C + s];
+    if (!TW_CHECKED(li < tw.W && off + s < R, status)) continue;
+    ell_idx[rb + off + s] = static_cast<uint16_t>(k * tw.W + li);
+    ell_a[rb + off + s] = tw.val[tk * tw.C + s];
+  }
+}
+}  // namespace
+
+__global__ void __launch_bounds__(256) twell_to_ell_kernel(const tw_twell tw, const int32_t* __restrict__ backup_slot,
+                                                          int R, uint16_t* __restrict__ ell_idx,
+                                                          uint16_t* __restrict__ ell_a, const int32_t* route,
+                                                          int32_t* status) {
+  pdl_enter();
+  if (route != nullptr && *route == 1) return;  // the call took the dense route
+  const int lane = threadIdx.x & 31;
+  const int nT = tw.I / tw.W;
+  const bool vec = tw.C % 16 == 0;
+  for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < tw.T; t += gridDim.x * 8) {
+    const size_t rb = static_cast<size_t>(t) * R;
+    int base = 0;
+    for (int k0 = 0; k0 < nT; k0 += 64) {
+      const int ka = k0 + 2 * lane, kb = ka + 1;
+      const size_t ta = static_cast<size_t>(t) * nT + ka;
+      const int slot = backup_slot[t];
+      const TileSlots sa = load_tile(tw, ta, ka < nT, vec);
+      const TileSlots sb = load_tile(tw, ta + 1, kb < nT, vec);
+      if (slot != -1) break;  // uniform over the warp: a backup row has no ELL entries
+      const int pair_n = sa.n + sb.n;
+      const int incl = warp_inclusive_scan(pair_n);
+      const int off = base + incl - pair_n;
+      put_tile(tw, sa, ta, ka, off, R, rb, ell_idx, ell_a, vec, status);
+      put_tile(tw, sb, ta + 1, kb, off + sa.n, R, rb, ell_idx, ell_a, vec, status);
+      base += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+  }
+}
+
+cudaError_t launch_twell_to_ell(const tw_twell& tw, const int32_t* backup_slot, int R, uint16_t* ell_idx,
+                                uint16_t* ell_a, const int32_t* route, int32_t* status, cudaStream_t s) {
+  if (tw.T == 0) return cudaSuccess;
+  cudaError_t e = launch(twell_to_ell_kernel, dim3(rows_grid(tw.T)), dim3(256), 0, s, tw, backup_slot, R, ell_idx,
+                         ell_a, route, status);
+  trace_mark(s, "twell_to_ell");
+  return e;
+}
+
 cudaError_t launch_twell_to_dense_ell(const tw_twell& tw, const int32_t* backup_slot, const float* backup_a, int cap,
                                       int R, uint16_t* H, uint16_t* ell_idx, uint16_t* ell_a, const int32_t* route,
                                       int32_t* status, cudaStream_t s) {

@@ -97,6 +97,10 @@ cudaError_t launch_hybrid_unpack(const tw_hybrid& h, float* A, float* U, cudaStr
 cudaError_t launch_twell_to_dense_ell(const tw_twell& tw, const int32_t* backup_slot, const float* backup_a, int cap,
                                       int R, uint16_t* H, uint16_t* ell_idx, uint16_t* ell_a, const int32_t* route,
                                       int32_t* status, cudaStream_t s);
+// The ELL entries (idx, a) of the rows without a backup slot from the TwELL, for the
+// sparse route's forward (nothing when *route == 1; route may be null).
+cudaError_t launch_twell_to_ell(const tw_twell& tw, const int32_t* backup_slot, int R, uint16_t* ell_idx,
+                                uint16_t* ell_a, const int32_t* route, int32_t* status, cudaStream_t s);
 
 // ---------------------------------------------------------------- tw_neurons.cu
 cudaError_t launch_neuron_counts(const tw_hybrid& h, int32_t* counts, cudaStream_t s);
@@ -129,6 +133,8 @@ struct SparseFwdArgs {
   const uint8_t* idx;
   const uint8_t* ovf;             // TwELL mode: skip rows with ovf
   const int32_t* backup_slot;     // Hybrid mode: skip rows with slot != -1
+  const int32_t* ell_nnz;         // Hybrid mode, gated: the ELL rows' lengths (their idx and a
+                                  // written by launch_twell_to_dense_ell beforehand)
   uint16_t* ell_idx;              // Hybrid mode outputs (R slots per row)
   uint16_t* ell_a;
   uint16_t* ell_u;

@@ -197,9 +197,12 @@ __host__ __device__ inline uint32_t token_smem_bytes(int nch, int cap, int ncoef
 }  // namespace
 
 // ====================================================================== forward
-// Rows served by the dense path (TwELL overflow, Hybrid backup) are skipped. The
-// entry list is built by the CTA: thread k takes TwELL tile k, an exclusive scan of
-// the tiles' counts places their slots, so the list is in ascending neuron order.
+// Rows served by the dense path (TwELL overflow, Hybrid backup) are skipped. In
+// TwELL mode the entry list is built by the CTA: thread k takes TwELL tile k, an
+// exclusive scan of the tiles' counts places their slots, so the list is in ascending
+// neuron order. In Hybrid mode it is the row's ELL (idx, a), which a warp-per-row
+// conversion wrote before this kernel: building it here cost the kernel 27 us at the
+// bench workload (a block scan and the TwELL reads per token), the conversion 15.
 // Lists are double-buffered over tokens, so a token needs no closing barrier: a
 // warp still in the down pass of token t reads the other buffer than token t + 1
 // writes, and token t + 2 writes it only after barriers every warp passes.
@@ -236,7 +239,20 @@ __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_fwd_kernel(c
     const size_t rb = static_cast<size_t>(t) * a.R;
     // ------------------------------------------------------------ entry list
     int n = 0, last_pos = -1, last_j = 0;
-    for (int kb = 0; kb < a.nT; kb += blockDim.x) {
+    if (HYBRID) {
+      // the row's ELL entries (written by the ELL conversion before this kernel), padded
+      // to a whole group with its last neuron and zero coefficients
+      n = a.ell_nnz[t];
+      if (!TW_CHECKED(n >= 0 && n <= a.R && n <= a.L, a.status)) n = 0;
+      for (int k = threadIdx.x; k < rup(n, kGroup); k += blockDim.x) {
+        const int e = min(k, n - 1);
+        const uint16_t j = a.ell_idx[rb + e];
+        lj[k] = TW_CHECKED(j < a.I, a.status) ? j : 0;
+        const float av = k < n ? bf16_to_f32(a.ell_a[rb + e]) : 0.f;
+        lh[k] = pair(av, av);
+      }
+    }
+    for (int kb = 0; !HYBRID && kb < a.nT; kb += blockDim.x) {
       const int k = kb + threadIdx.x;
       const int cnt = k < a.nT ? min(static_cast<int>(a.cnt[static_cast<size_t>(t) * a.nT + k]), a.C) : 0;
       const size_t sb = (static_cast<size_t>(t) * a.nT + k) * a.C;
@@ -255,10 +271,6 @@ __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_fwd_kernel(c
         const float av = bf16_to_f32(ab);
         lj[off + i] = static_cast<uint16_t>(j);
         lh[off + i] = pair(av, av);
-        if (HYBRID && TW_CHECKED(off + i < a.R, a.status)) {
-          a.ell_idx[rb + off + i] = static_cast<uint16_t>(j);
-          a.ell_a[rb + off + i] = ab;
-        }
         last_pos = off + i;
         last_j = j;
       };
@@ -273,7 +285,7 @@ __global__ void __launch_bounds__(NCH * 32, ctas_per_sm(NCH)) token_fwd_kernel(c
       for (int i = vec_slots ? 16 : 0; i < cnt; ++i) put(i, a.idx[sb + i], a.val[sb + i]);
       n += tot;
     }
-    if (n > 0 && last_pos == n - 1) {  // the list's last writer pads it to a whole group (zero coefficients)
+    if (!HYBRID && n > 0 && last_pos == n - 1) {  // the list's last writer pads it to a whole group (zero coefficients)
 #pragma unroll
       for (int i = 0; i < kGroup; ++i) {
         lj[n + i] = static_cast<uint16_t>(last_j);
