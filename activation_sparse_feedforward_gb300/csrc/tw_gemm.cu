@@ -97,9 +97,10 @@ cudaError_t gemm_gate_pack(const uint16_t* x, const uint16_t* Wg, int T, int d, 
                            const tw_twell& o, uint16_t* a_dense, int32_t* status, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   EpiTwellPack::Params ep{T, W, C, I / W, o.cnt, o.val, o.idx, o.row_nnz, o.ovf, a_dense, I};
-  const GemmShape sh = shape_static(T, I, d, status);
+  GemmShape sh = shape_static(T, I, d, status);
   GemmMaps maps;
   const int bn = (I % 256 == 0) ? 256 : (I % 128 == 0) ? 128 : 64;
+  sh.split_tail = (bn / 2) % W == 0;  // a half unit must hold whole TwELL tiles
   if (!tmap_kmajor(&maps.a[0], x, T, d, 128) || !tmap_kmajor(&maps.b[0], Wg, I, d, bn)) return cudaErrorInvalidValue;
   fill_unused(maps, 1, 1);
   if (bn == 256) return run_gemm<256, false, false, false, 4, EpiTwellPack>(maps, sh, ep, T, s, "gate_pack");
@@ -112,7 +113,8 @@ cudaError_t gemm_gate_relu_dense(const uint16_t* x, const uint16_t* Wg, int T, i
                                  int32_t* status, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   EpiReluBf16::Params ep{a, I};
-  const GemmShape sh = shape_static(T, I, d, status);
+  GemmShape sh = shape_static(T, I, d, status);
+  sh.split_tail = true;
   GemmMaps maps;
   const int bn = (I % 256 == 0) ? 256 : (I % 128 == 0) ? 128 : 64;
   if (!tmap_kmajor(&maps.a[0], x, T, d, 128) || !tmap_kmajor(&maps.b[0], Wg, I, d, bn)) return cudaErrorInvalidValue;
@@ -378,6 +380,7 @@ cudaError_t gemm_up_hybrid(const uint16_t* x, const uint16_t* Wu, int T, int d, 
   if (T == 0) return cudaSuccess;
   GemmShape sh = shape_static(T, I, d, status);
   set_route(sh, route);
+  sh.split_tail = ((I % 256 == 0 ? 256 : I % 128 == 0 ? 128 : 64) / 2) % tw.W == 0;  // whole TwELL tiles a unit
   EpiUpHybrid::Params ep{T,      tw.W,        tw.C,     I / tw.W, R,   tw.cnt, tw.val,  tw.idx, backup_slot,
                          backup_a, backup_u, cap,      H,        I,   ell_idx, ell_a, ell_u,  status};
   GemmMaps maps;
@@ -396,6 +399,7 @@ cudaError_t gemm_rows_nmajor_bf16(const uint16_t* const* A, const uint16_t* cons
   if (segments < 1 || segments > GEMM_MAX_SEGMENTS || N % 256 != 0) return cudaErrorInvalidValue;
   GemmShape sh = shape_static(M, N, K, status);
   sh.segments = segments;
+  sh.split_tail = true;
   set_route(sh, route);
   GemmMaps maps;
   for (int i = 0; i < segments; ++i)
@@ -413,6 +417,7 @@ static cudaError_t dense_grad_bn(const uint16_t* dY, const uint16_t* Wd, int T, 
                                  int32_t* status, cudaStream_t s) {
   GemmShape sh = shape_static(T, I, d, status);
   set_route(sh, route);
+  sh.split_tail = true;
   GemmMaps maps;
   if (!tmap_kmajor(&maps.a[0], dY, T, d, 128) || !tmap_kmajor(&maps.b[0], Wd, I, d, BN)) return cudaErrorInvalidValue;
   fill_unused(maps, 1, 1);
@@ -479,6 +484,7 @@ cudaError_t gemm_dense_test(const uint16_t* A, const uint16_t* B, int M, int N, 
                             int32_t* status, cudaStream_t s, int withhold_kb) {
   GemmShape sh = shape_static(M, N, K, status);
   sh.withhold_kb = withhold_kb;
+  sh.split_tail = true;
   EpiStoreF32::Params ep{D, N};
   GemmMaps maps;
   const bool oka = a_mn ? tmap_mnmajor(&maps.a[0], A, K, M) : tmap_kmajor(&maps.a[0], A, M, K, 128);

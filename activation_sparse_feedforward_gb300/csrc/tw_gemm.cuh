@@ -63,6 +63,8 @@ struct GemmShape {
   const int* route_dev;  // optional: the launch does its work only when *route_dev == route_want
   int route_want;        // (the route a call took, decided on the device by an earlier kernel)
   const int* drop_last_problem_if;  // optional: when it reads 1, the launch runs one problem fewer
+  bool split_tail;   // tiles of the last round, when they fill at most half the grid, run as
+                     // two half-width units each (launches without a K split, BN >= 128)
 };
 
 constexpr int GEMM_MAX_SEGMENTS = 6;  // segments x problems
@@ -125,6 +127,7 @@ struct GemmTraits {
   static constexpr int ACC_COLS = BN * NB;
   static constexpr int TMEM_COLS = 2 * ACC_COLS;
   static constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, BN, A_MN, B_MN, F16);
+  static constexpr uint32_t IDESC_HALF = idesc_bf16_f32(GEMM_BM, BN / 2, A_MN, B_MN, F16);  // half-width units
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64, 128, 192 or 256");
@@ -152,6 +155,30 @@ TW_DEV int split_by_cost(int tiles, int kb_total, int grid) {
     }
   }
   return best;
+}
+
+// A work unit: an output tile (or, with the tail split, a half of one: half 0 or 1, the
+// columns [0, BN/2) or [BN/2, BN) of the tile; -1 = the whole tile) and the slice of
+// its K loop. Units [0, full_units) are whole tiles cut into ksplit slices each; with
+// the tail split, the units after them are the last tiles' halves (ksplit == 1).
+struct UnitInfo {
+  int tile, kb_lo, kb_hi, half;
+};
+TW_DEV UnitInfo unit_info(int unit, int ksplit, int kb_chunk, int kb_total, int full_units) {
+  UnitInfo u;
+  if (unit < full_units) {
+    u.tile = unit / ksplit;
+    u.kb_lo = (unit - u.tile * ksplit) * kb_chunk;
+    u.kb_hi = min(kb_total, u.kb_lo + kb_chunk);
+    u.half = -1;
+  } else {
+    const int h = unit - full_units;
+    u.tile = full_units + h / 2;
+    u.kb_lo = 0;
+    u.kb_hi = kb_total;
+    u.half = h & 1;
+  }
+  return u;
 }
 
 template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES, class Epi, int NA = 1>
@@ -220,7 +247,13 @@ __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
       : shape.ksplit == -2 ? split_by_cost(num_tiles, kb_total, static_cast<int>(gridDim.x))
                            : (num_tiles > 0 ? max(1, min(kb_total, static_cast<int>(gridDim.x) / num_tiles)) : 1);
   const int kb_chunk = (kb_total + ksplit - 1) / ksplit;
-  const int num_units = num_tiles * ksplit;
+  // the tail split: the last round's tiles as two half-width units each, when they fill
+  // at most half the grid (so the last round takes half a tile's time)
+  const int grid = static_cast<int>(gridDim.x);
+  const int rem = num_tiles % grid;
+  const bool tail = shape.split_tail && !DUAL && BN >= 128 && ksplit == 1 && rem > 0 && 2 * rem <= grid;
+  const int full_units = tail ? num_tiles - rem : num_tiles * ksplit;
+  const int num_units = tail ? full_units + 2 * rem : num_tiles * ksplit;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -230,14 +263,15 @@ __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
       long issued = 0;
       bool ok = true;
       for (int unit = blockIdx.x; ok && unit < num_units; unit += gridDim.x) {
-        const int tile = unit / ksplit;
-        const int kb_lo = (unit - tile * ksplit) * kb_chunk;
-        const int kb_hi = min(kb_total, kb_lo + kb_chunk);
+        const UnitInfo ui = unit_info(unit, ksplit, kb_chunk, kb_total, full_units);
+        const int tile = ui.tile, kb_lo = ui.kb_lo, kb_hi = ui.kb_hi;
         if (kb_lo >= kb_hi) continue;
         const int row_tile = tile / n_tiles;
         const int prob = row_tile / m_tiles;
         const int m0 = (row_tile - prob * m_tiles) * GEMM_BM;  // within the problem
-        const int n0 = (tile % n_tiles) * BN;
+        // a second half's B box starts at its own columns (the box's other half, past
+        // the tile or past N, is loaded but not used)
+        const int n0 = (tile % n_tiles) * BN + (ui.half == 1 ? BN / 2 : 0);
         for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, shape.status)) {
             ok = false;
@@ -305,10 +339,10 @@ __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
       bool ok = true;
       bool issued_any = false;
       for (int unit = blockIdx.x; ok && unit < num_units; unit += gridDim.x) {
-        const int tile = unit / ksplit;
-        const int kb_lo = (unit - tile * ksplit) * kb_chunk;
-        const int kb_hi = min(kb_total, kb_lo + kb_chunk);
+        const UnitInfo ui = unit_info(unit, ksplit, kb_chunk, kb_total, full_units);
+        const int kb_lo = ui.kb_lo, kb_hi = ui.kb_hi;
         if (kb_lo >= kb_hi) continue;
+        const uint32_t idesc = ui.half < 0 ? Tr::IDESC : Tr::IDESC_HALF;
         const int buf = local & 1;
         const uint32_t use = static_cast<uint32_t>(local >> 1);
         ++local;
@@ -339,7 +373,7 @@ __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
                 const uint32_t bb = b_base + nb * Tr::B_BYTES;
                 const uint64_t bd = B_MN ? smem_desc_sw128(bb + k16 * 2048, 8192, 1024)
                                          : smem_desc_sw128(bb + k16 * 32, 16, 1024);
-                tc_mma_bf16(d0 + nb * BN, ad, bd, Tr::IDESC, acc);
+                tc_mma_bf16(d0 + nb * BN, ad, bd, idesc, acc);
               }
             }
           }
@@ -371,16 +405,25 @@ __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
     const int row = quarter * 32 + lane;
     int local = 0;
     for (int unit = blockIdx.x; unit < num_units; unit += gridDim.x) {
-      const int tile = unit / ksplit;
-      const int kb_lo = (unit - tile * ksplit) * kb_chunk;
-      if (kb_lo >= min(kb_total, kb_lo + kb_chunk)) continue;
+      const UnitInfo ui = unit_info(unit, ksplit, kb_chunk, kb_total, full_units);
+      if (ui.kb_lo >= ui.kb_hi) continue;
+      const int tile = ui.tile;
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       ++local;
       const int m = (tile / n_tiles) * GEMM_BM + row;
-      const int n0 = (tile % n_tiles) * BN + half * kCols;
+      // this warp's columns: kCols at half * kCols of a whole tile; of a half unit, its
+      // BN / 2 columns (with eight warps all of them for the first group's warps, none
+      // for the second's), at the start of the accumulator
+      int cols = kCols, col_off = half * kCols;
+      if (ui.half >= 0) {
+        cols = (kEW == 8) ? (half == 0 ? kCols : 0) : kCols / 2;
+        col_off = 0;
+      }
+      const int n0 = (tile % n_tiles) * BN + (ui.half == 1 ? BN / 2 : 0) + col_off;
       Epi e(ep, m, M, n0);
-      if constexpr (epi_prefetches<Epi>::value) e.prefetch(kCols);  // while the tile's K loop runs
+      if constexpr (epi_prefetches<Epi>::value)
+        if (cols > 0) e.prefetch(cols);  // while the tile's K loop runs
       int ok = 0;
       if (lane == 0) ok = mbar_wait(tfull + buf, use & 1u, abort_flag, shape.status) ? 1 : 0;
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -388,27 +431,30 @@ __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
       tc_fence_after_sync();
       if constexpr (Epi::kStageBytes > 0)
         e.stage = reinterpret_cast<float*>(tiles + STAGES * Tr::STAGE_BYTES + Tr::BAR_BYTES) + ew * (Epi::kStageBytes / 16);
-      const uint32_t tbase = tmem_base + static_cast<uint32_t>(buf * Tr::ACC_COLS + half * kCols) +
+      const uint32_t tbase = tmem_base + static_cast<uint32_t>(buf * Tr::ACC_COLS + col_off) +
                              (static_cast<uint32_t>(quarter * 32) << 16);
+      const int nch = cols / 32;
       if constexpr (!DUAL && epi_overlaps_loads<Epi>::value) {
         // the next chunk's TMEM load is in flight while this chunk is written out
-        uint32_t va[32], vb[32];
-        tmem_ld32(tbase, va);
-        tmem_wait_ld();
-#pragma unroll 1
-        for (int c = 0; c < kCols / 32; c += 2) {
-          if (c + 1 < kCols / 32) tmem_ld32(tbase + (c + 1) * 32, vb);
-          e.chunk(c, va, va);
+        if (nch > 0) {
+          uint32_t va[32], vb[32];
+          tmem_ld32(tbase, va);
           tmem_wait_ld();
-          if (c + 1 < kCols / 32) {
-            if (c + 2 < kCols / 32) tmem_ld32(tbase + (c + 2) * 32, va);
-            e.chunk(c + 1, vb, vb);
+#pragma unroll 1
+          for (int c = 0; c < nch; c += 2) {
+            if (c + 1 < nch) tmem_ld32(tbase + (c + 1) * 32, vb);
+            e.chunk(c, va, va);
             tmem_wait_ld();
+            if (c + 1 < nch) {
+              if (c + 2 < nch) tmem_ld32(tbase + (c + 2) * 32, va);
+              e.chunk(c + 1, vb, vb);
+              tmem_wait_ld();
+            }
           }
         }
       } else {
 #pragma unroll 1
-        for (int c = 0; c < kCols / 32; ++c) {
+        for (int c = 0; c < nch; ++c) {
           uint32_t v0[32];
           uint32_t v1[32];
           tmem_ld32(tbase + c * 32, v0);
