@@ -506,16 +506,21 @@ TW_DEV void transposed_rows(float* stage, const uint32_t (&v)[32], int m, int M,
   __syncwarp();
 }
 
-// The bf16 counterpart for one 32-column output block: the lane's row arrives as 16
+// The 16-bit counterpart for one 32-column output block: the lane's row arrives as 16
 // packed words (two columns each); the warp then writes eight rows per step, four
 // lanes x 16 bytes covering each row's 64-byte segment. Rows m0 + r with r < rows
-// are written to dst + (m0 + r) * ld. Every lane of the warp must call it.
+// are written to dst + (m0 + r) * ld. In the staging buffer a row is 16 words and
+// its four 16-byte chunks are XOR-swizzled by (row / 2) mod 4, so both the lanes'
+// row writes and the quarter-warps' two-row reads touch every bank once: the
+// epilogue's shared-memory traffic competes with the MMAs' operand reads. Every lane
+// of the warp must call it.
 TW_DEV void transposed_rows_bf16(float* stage, const uint32_t (&w)[16], int m0, int rows, uint16_t* dst, int ld) {
   const int lane = threadIdx.x & 31;
   uint32_t* st = reinterpret_cast<uint32_t*>(stage);
 #pragma unroll
   for (int i = 0; i < 4; ++i)
-    *reinterpret_cast<uint4*>(st + lane * 20 + 4 * i) = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    *reinterpret_cast<uint4*>(st + lane * 16 + 4 * ((i ^ (lane >> 1)) & 3)) =
+        make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
   __syncwarp();
   const int sub = lane >> 2, c4 = lane & 3;
 #pragma unroll
@@ -523,7 +528,7 @@ TW_DEV void transposed_rows_bf16(float* stage, const uint32_t (&w)[16], int m0, 
     const int r = r0 + sub;
     if (r < rows)
       *reinterpret_cast<uint4*>(dst + static_cast<size_t>(m0 + r) * ld + 8 * c4) =
-          *reinterpret_cast<const uint4*>(st + r * 20 + 4 * c4);
+          *reinterpret_cast<const uint4*>(st + r * 16 + 4 * ((c4 ^ (r >> 1)) & 3));
   }
   __syncwarp();
 }
