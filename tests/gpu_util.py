@@ -46,6 +46,21 @@ def assert_close(got: np.ndarray, ref: np.ndarray, what: str, rel_frob: float = 
     return rel
 
 
+def assert_close_by_row_class(got: np.ndarray, ref: np.ndarray, backup_rows: np.ndarray, what: str):
+    """assert_close over all rows, then separately over the ELL rows and over the dense
+    backup rows, so that an error confined to the few backup (outlier) rows cannot hide
+    in the Frobenius norm of the whole."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert_close(got, ref, what)
+    is_backup = np.zeros(got.shape[0], dtype=bool)
+    is_backup[np.asarray(backup_rows, dtype=np.int64)] = True
+    if (~is_backup).any():
+        assert_close(got[~is_backup], ref[~is_backup], f"{what} (ELL rows)")
+    if is_backup.any():
+        assert_close(got[is_backup], ref[is_backup], f"{what} (backup rows)")
+
+
 def check_active_set(active_gpu: np.ndarray, g_ref: np.ndarray, what: str = "active set"):
     """Every disagreement between the GPU's active set and g_ref > 0 sits at |g_ref| <= 1e-3."""
     diff = active_gpu != (g_ref > 0)

@@ -10,7 +10,7 @@ import pytest
 torch = pytest.importorskip("torch")
 
 import activation_sparse_feedforward_gb300 as tw  # noqa: E402
-from gpu_util import assert_close, bits_of, f64_of, to_dev  # noqa: E402
+from gpu_util import assert_close, assert_close_by_row_class, bits_of, f64_of, to_dev  # noqa: E402
 from oracle import ffn  # noqa: E402
 from synthetic import FFNSpec, WORKLOADS, make_inputs  # noqa: E402
 
@@ -72,8 +72,15 @@ def test_dense_route_matches_oracle(spec, l1):
     inp = make_inputs(spec, with_dy=True)
     h, y, grads = _step(spec, _dev(inp), "dense", l1, spec.T // 4)
     assert h.saved.took_dense_route()
-    assert 0 < int(h.saved.n_backup.item()) <= spec.T // 4
+    nb = int(h.saved.n_backup.item())
+    assert 0 < nb <= spec.T // 4
     _check_oracle(spec, inp, y, grads, l1)
+    # y and dx of the ELL rows and of the backup rows, each class on its own
+    f = ffn.forward(inp["x"], inp["Wg"], inp["Wu"], inp["Wd"])
+    b = ffn.backward(inp["x"], inp["Wg"], inp["Wu"], inp["Wd"], inp["dy"], l1, fwd=f)
+    backup = h.saved.backup_tok[:nb].cpu().numpy()
+    assert_close_by_row_class(f64_of(y), f["y"], backup, "y")
+    assert_close_by_row_class(f64_of(grads[0]), b["dx"], backup, "dx")
 
 
 @pytest.mark.parametrize("spec", CASES[:2], ids=lambda s: s.name)

@@ -6,7 +6,7 @@ import pytest
 torch = pytest.importorskip("torch")
 
 import activation_sparse_feedforward_gb300 as tw  # noqa: E402
-from gpu_util import assert_close, bits_of, f64_of, to_dev  # noqa: E402
+from gpu_util import assert_close, assert_close_by_row_class, bits_of, f64_of, to_dev  # noqa: E402
 from oracle import ffn, formats  # noqa: E402
 from synthetic import FFNSpec, WORKLOADS, make_inputs  # noqa: E402
 
@@ -102,8 +102,9 @@ def test_hybrid_forward_backward_match_oracle(spec, l1):
     h, y, (dx, dWg, dWu, dWd) = _run_hybrid(spec, inp, backup_cap=spec.T // 4, l1=l1)
     f = ffn.forward(inp["x"], inp["Wg"], inp["Wu"], inp["Wd"])
     b = ffn.backward(inp["x"], inp["Wg"], inp["Wu"], inp["Wd"], inp["dy"], l1, fwd=f)
-    assert_close(f64_of(y), f["y"], "y")
-    assert_close(f64_of(dx), b["dx"], "dx")
+    backup = h.saved.backup_tok[:int(h.saved.n_backup.item())].cpu().numpy()
+    assert_close_by_row_class(f64_of(y), f["y"], backup, "y")
+    assert_close_by_row_class(f64_of(dx), b["dx"], backup, "dx")
     assert_close(dWg.cpu().numpy(), b["dWg"], "dWg")
     assert_close(dWd.cpu().numpy(), b["dWd"], "dWd")
     if spec.gated:
