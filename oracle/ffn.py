@@ -22,6 +22,11 @@ gradient ``backward`` returns is
 (``dy`` plays the role of the upstream gradient; no 1/T normalisation is applied
 to the L1 term -- a caller wanting one folds it into ``l1``). ReLU'(0) is taken
 as 0, i.e. the active set is the strict set g > 0.
+
+The pages leave open which activation the penalty acts on. ``penalise="h"`` takes
+the other reading, l1 * sum |h| with h = a * u (sign(0) = 0), for reference only:
+the library implements the penalty on a. Without a gate, h = a and both readings
+coincide.
 """
 from __future__ import annotations
 
@@ -60,13 +65,14 @@ def forward(x, Wg, Wu, Wd) -> dict:
     return {"g": g, "a": a, "u": u, "h": h, "y": y}
 
 
-def loss(x, Wg, Wu, Wd, dy, l1: float) -> float:
-    """L = sum(dy * y) + l1 * sum(a)."""
+def loss(x, Wg, Wu, Wd, dy, l1: float, penalise: str = "a") -> float:
+    """L = sum(dy * y) + l1 * sum(a)  (or + l1 * sum |h| with penalise="h")."""
     f = forward(x, Wg, Wu, Wd)
-    return float(np.sum(as_f64(dy) * f["y"]) + l1 * np.sum(f["a"]))
+    pen = np.sum(f["a"]) if penalise == "a" else np.sum(np.abs(f["h"]))
+    return float(np.sum(as_f64(dy) * f["y"]) + l1 * pen)
 
 
-def backward(x, Wg, Wu, Wd, dy, l1: float, fwd: dict | None = None) -> dict:
+def backward(x, Wg, Wu, Wd, dy, l1: float, fwd: dict | None = None, penalise: str = "a") -> dict:
     """Gradient of L with respect to x and the three weights, by the chain rule:
 
         dh  = dy Wd^T                      dWd = h^T dy
@@ -76,13 +82,22 @@ def backward(x, Wg, Wu, Wd, dy, l1: float, fwd: dict | None = None) -> dict:
 
     The sparse backward of the pages (explainer 2.B "Backpropagation": inject the
     L1 gradient, transpose the hybrid format for the weight gradients) computes
-    exactly these quantities restricted to the active set."""
+    exactly these quantities restricted to the active set.
+
+    With penalise="h" the penalty's gradient enters through h instead:
+    dh' = dh + l1 * sign(h), then du = dh' * a and dg = dh' * u * [g > 0] (gated;
+    non-gated h = a >= 0, the same as the default)."""
     x, Wg, Wu, Wd, dy = (as_f64(t) for t in (x, Wg, Wu, Wd, dy))
     f = fwd if fwd is not None else forward(x, Wg, Wu, Wd)
     g, a, u, h = f["g"], f["a"], f["u"], f["h"]
     active = (g > 0.0).astype(np.float64)
     dh = dy @ Wd.T
     dWd = h.T @ dy
+    if penalise == "h" and Wu is not None:
+        dh_h = dh + l1 * np.sign(h)
+        du = dh_h * a
+        dg = dh_h * u * active
+        return {"dx": dg @ Wg + du @ Wu, "dWg": dg.T @ x, "dWu": du.T @ x, "dWd": dWd, "dh": dh, "dg": dg, "du": du}
     if Wu is None:
         du = None
         dg = (dh + l1) * active

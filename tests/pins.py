@@ -112,6 +112,31 @@ def pin_backward_finite_differences(ffn=_ffn, gated=True, l1=0.3):
         np.testing.assert_allclose(b[name], fd, rtol=1e-6, atol=1e-7, err_msg=name)
 
 
+def pin_backward_l1_on_h(ffn=_ffn, gated=True, l1=0.3):
+    """The reference-only reading with the penalty on |h|: central differences of
+    its loss, and torch autograd of the same loss, against ``backward``."""
+    import torch
+    x, Wg, Wu, Wd, dy = tiny_problem(gated=gated)
+    b = ffn.backward(x, Wg, Wu, Wd, dy, l1, penalise="h")
+    loss = lambda: ffn.loss(x, Wg, Wu, Wd, dy, l1, penalise="h")  # noqa: E731
+    names = [("dx", x), ("dWg", Wg), ("dWd", Wd)] + ([("dWu", Wu)] if gated else [])
+    for name, arr in names:
+        fd = _fd_grad(loss, arr)
+        np.testing.assert_allclose(b[name], fd, rtol=1e-6, atol=1e-7, err_msg=name)
+    tt = {k: torch.tensor(v, dtype=torch.float64, requires_grad=True)
+          for k, v in dict(x=x, Wg=Wg, Wd=Wd, **({"Wu": Wu} if gated else {})).items()}
+    a = torch.relu(tt["x"] @ tt["Wg"].T)
+    h = a * (tt["x"] @ tt["Wu"].T) if gated else a
+    L = (torch.tensor(dy) * (h @ tt["Wd"])).sum() + l1 * h.abs().sum()
+    L.backward()
+    leaf = {"dx": "x", "dWg": "Wg", "dWd": "Wd", "dWu": "Wu"}
+    for name, _ in names:
+        np.testing.assert_allclose(b[name], tt[leaf[name]].grad.numpy(), rtol=1e-10, atol=1e-12, err_msg=name)
+    if gated:
+        # the two readings differ on this problem (u takes both signs)
+        assert not np.allclose(b["dWg"], ffn.backward(x, Wg, Wu, Wd, dy, l1)["dWg"])
+
+
 def pin_backward_l1_closed_form(ffn=_ffn, gated=True):
     """dy = 0, l1 = 1: the gradient is that of sum(a) alone, so dWg[j] = sum of x_t
     over tokens with g_tj > 0, dx_t = sum of Wg[j] over its active neurons, and

@@ -26,6 +26,11 @@ def test_backward_finite_differences(gated):
 
 
 @pytest.mark.parametrize("gated", [True, False])
+def test_backward_l1_on_h_reading(gated):
+    pins.pin_backward_l1_on_h(gated=gated)
+
+
+@pytest.mark.parametrize("gated", [True, False])
 def test_backward_l1_closed_form(gated):
     pins.pin_backward_l1_closed_form(gated=gated)
 
