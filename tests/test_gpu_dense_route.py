@@ -10,7 +10,8 @@ import pytest
 torch = pytest.importorskip("torch")
 
 import activation_sparse_feedforward_gb300 as tw  # noqa: E402
-from gpu_util import assert_close, assert_close_by_row_class, bits_of, f64_of, to_dev  # noqa: E402
+from gpu_util import (assert_close, assert_close_by_row_class, bits_of, f64_of, kernel_active_set,  # noqa: E402
+                      oracle_on_kernel_branch, to_dev)
 from oracle import ffn  # noqa: E402
 from synthetic import FFNSpec, WORKLOADS, make_inputs  # noqa: E402
 
@@ -33,6 +34,10 @@ CASES = [
     # long ELL rows (the grad epilogue's row search and walk over many entries per tile)
     FFNSpec("dense_long_rows", T=513, d=512, I=1280, mean_active=200, outlier_frac=0.02, W=128, C=40, R=320,
             seed=24),
+    # 16 x 22 = 352 tiles in the gate, up and grad GEMMs: 304 whole tiles, then the last
+    # 48 as half-width units (the tail split with both kinds in one launch)
+    FFNSpec("dense_mixed_tail", T=2048, d=256, I=5632, mean_active=100, outlier_frac=0.01, W=128, C=16, R=224,
+            seed=30),
 ]
 
 
@@ -51,11 +56,19 @@ def _step(spec, dv, route, l1, backup_cap, dense_above=64.0):
     return h, y, grads
 
 
-def _check_oracle(spec, inp, y, grads, l1, rows=None):
-    dx, dWg, dWu, dWd = grads
+def _oracle(inp, h, l1, rows=None):
+    """Oracle forward and backward on the kernel's side of the ReLU kink (rows: a
+    sample of the tokens)."""
     x, dyi = (inp["x"], inp["dy"]) if rows is None else (inp["x"][rows], inp["dy"][rows])
-    f = ffn.forward(x, inp["Wg"], inp["Wu"], inp["Wd"])
-    b = ffn.backward(x, inp["Wg"], inp["Wu"], inp["Wd"], dyi, l1, fwd=f)
+    act = kernel_active_set(h.saved)
+    f = oracle_on_kernel_branch(ffn.forward(x, inp["Wg"], inp["Wu"], inp["Wd"]),
+                                act if rows is None else act[rows], inp["Wd"])
+    return f, ffn.backward(x, inp["Wg"], inp["Wu"], inp["Wd"], dyi, l1, fwd=f)
+
+
+def _check_oracle(spec, inp, h, y, grads, l1, rows=None):
+    dx, dWg, dWu, dWd = grads
+    f, b = _oracle(inp, h, l1, rows)
     yy, dd = (f64_of(y), f64_of(dx)) if rows is None else (f64_of(y)[rows], f64_of(dx)[rows])
     assert_close(yy, f["y"], "y")
     assert_close(dd, b["dx"], "dx")
@@ -74,10 +87,9 @@ def test_dense_route_matches_oracle(spec, l1):
     assert h.saved.took_dense_route()
     nb = int(h.saved.n_backup.item())
     assert 0 < nb <= spec.T // 4
-    _check_oracle(spec, inp, y, grads, l1)
+    _check_oracle(spec, inp, h, y, grads, l1)
     # y and dx of the ELL rows and of the backup rows, each class on its own
-    f = ffn.forward(inp["x"], inp["Wg"], inp["Wu"], inp["Wd"])
-    b = ffn.backward(inp["x"], inp["Wg"], inp["Wu"], inp["Wd"], inp["dy"], l1, fwd=f)
+    f, b = _oracle(inp, h, l1)
     backup = h.saved.backup_tok[:nb].cpu().numpy()
     assert_close_by_row_class(f64_of(y), f["y"], backup, "y")
     assert_close_by_row_class(f64_of(grads[0]), b["dx"], backup, "dx")
@@ -90,7 +102,7 @@ def test_dense_route_without_backup_capacity_rows(spec):
     inp = make_inputs(spec, with_dy=True)
     h, y, grads = _step(spec, _dev(inp), "dense", spec.l1, 0)
     assert int(h.saved.n_backup.item()) == 0
-    _check_oracle(spec, inp, y, grads, spec.l1)
+    _check_oracle(spec, inp, h, y, grads, spec.l1)
 
 
 @pytest.mark.parametrize("spec", CASES, ids=lambda s: s.name)
@@ -140,7 +152,7 @@ def test_auto_route_is_decided_on_the_device(dense_above, expect_dense):
     h, y, grads = _step(spec, _dev(inp), "auto", spec.l1, spec.T // 4, dense_above=dense_above)
     assert h.saved.took_dense_route() == expect_dense
     assert (_route_work(h, spec.T, dense_above) > dense_above) == expect_dense
-    _check_oracle(spec, inp, y, grads, spec.l1)
+    _check_oracle(spec, inp, h, y, grads, spec.l1)
 
 
 # every row overflows its TwELL (~19 nonzeros per 64-wide tile against C = 4): the
@@ -171,7 +183,7 @@ def test_large_backup_matches_oracle(spec, route):
     h, y, grads = _step(spec, _dev(inp), route, spec.l1, spec.T)
     nb = int(h.saved.n_backup.item())
     assert nb > 512, nb
-    _check_oracle(spec, inp, y, grads, spec.l1)
+    _check_oracle(spec, inp, h, y, grads, spec.l1)
     # the saved fp32 rows: a = ReLU(g) and u of the backup tokens
     rows = h.saved.backup_tok[:nb].cpu().numpy()
     f = ffn.forward(inp["x"][rows], inp["Wg"], inp["Wu"], inp["Wd"])
@@ -191,10 +203,10 @@ def test_auto_route_takes_the_dense_route_when_every_row_is_backup(spec):
     assert int(h.saved.n_backup.item()) == spec.T
     assert h.saved.took_dense_route()
     assert _route_work(h, spec.T, 64.0) == 128.0
-    _check_oracle(spec, inp, y, grads, spec.l1)
+    _check_oracle(spec, inp, h, y, grads, spec.l1)
     hs, ys, gs = _step(spec, dv, "sparse", spec.l1, spec.T)
     assert not hs.saved.took_dense_route()
-    _check_oracle(spec, inp, ys, gs, spec.l1)
+    _check_oracle(spec, inp, hs, ys, gs, spec.l1)
     # the saved fp32 rows do not depend on the route (the same sums, whose split-K
     # partials may be added in another order)
     nb = spec.T
@@ -214,7 +226,7 @@ def test_dense_route_full_size_sampled(name, backup_cap):
     assert len(inp["outliers"]) <= nb <= backup_cap
     assert int(h.saved.ell_nnz.sum().item()) > 100 * (spec.T - nb)     # ELL rows of ~108 nonzeros
     rows = np.unique(np.concatenate([np.arange(7, spec.T, 1031), inp["outliers"][:10], [spec.T - 1]]))
-    _check_oracle(spec, inp, y, grads, spec.l1, rows=rows)
+    _check_oracle(spec, inp, h, y, grads, spec.l1, rows=rows)
     J = np.array([0, 3, 999, 2048, 4095, 5631])
     r = ffn.backward_weight_rows(inp["x"], inp["Wg"], inp["Wu"], inp["Wd"], inp["dy"], spec.l1, J)
     dx, dWg, dWu, dWd = grads

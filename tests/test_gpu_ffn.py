@@ -6,7 +6,8 @@ import pytest
 torch = pytest.importorskip("torch")
 
 import activation_sparse_feedforward_gb300 as tw  # noqa: E402
-from gpu_util import assert_close, assert_close_by_row_class, bits_of, f64_of, to_dev  # noqa: E402
+from gpu_util import (assert_close, assert_close_by_row_class, bits_of, f64_of, kernel_active_set,  # noqa: E402
+                      oracle_on_kernel_branch, to_dev)
 from oracle import ffn, formats  # noqa: E402
 from synthetic import FFNSpec, WORKLOADS, make_inputs  # noqa: E402
 
@@ -100,7 +101,8 @@ def _run_hybrid(spec, inp, backup_cap, l1=None, dy_zero=False):
 def test_hybrid_forward_backward_match_oracle(spec, l1):
     inp = make_inputs(spec, with_dy=True)
     h, y, (dx, dWg, dWu, dWd) = _run_hybrid(spec, inp, backup_cap=spec.T // 4, l1=l1)
-    f = ffn.forward(inp["x"], inp["Wg"], inp["Wu"], inp["Wd"])
+    f = oracle_on_kernel_branch(ffn.forward(inp["x"], inp["Wg"], inp["Wu"], inp["Wd"]),
+                                kernel_active_set(h.saved), inp["Wd"])
     b = ffn.backward(inp["x"], inp["Wg"], inp["Wu"], inp["Wd"], inp["dy"], l1, fwd=f)
     backup = h.saved.backup_tok[:int(h.saved.n_backup.item())].cpu().numpy()
     assert_close_by_row_class(f64_of(y), f["y"], backup, "y")
@@ -121,7 +123,8 @@ def test_hybrid_without_backup_rows(backup_cap):
     inp = make_inputs(spec, with_dy=True)
     h, y, (dx, dWg, dWu, dWd) = _run_hybrid(spec, inp, backup_cap=backup_cap)
     assert int(h.saved.n_backup.item()) == 0
-    f = ffn.forward(inp["x"], inp["Wg"], inp["Wu"], inp["Wd"])
+    f = oracle_on_kernel_branch(ffn.forward(inp["x"], inp["Wg"], inp["Wu"], inp["Wd"]),
+                                kernel_active_set(h.saved), inp["Wd"])
     b = ffn.backward(inp["x"], inp["Wg"], inp["Wu"], inp["Wd"], inp["dy"], spec.l1, fwd=f)
     assert_close(f64_of(y), f["y"], "y")
     assert_close(f64_of(dx), b["dx"], "dx")
@@ -185,7 +188,8 @@ def test_hybrid_full_size_sampled(name, backup_cap):
     inp = make_inputs(spec, with_dy=True)
     h, y, (dx, dWg, dWu, dWd) = _run_hybrid(spec, inp, backup_cap=backup_cap)
     rows = np.unique(np.concatenate([np.arange(5, spec.T, 1013), inp["outliers"][:10], [spec.T - 1]]))
-    f = ffn.forward(inp["x"][rows], inp["Wg"], inp["Wu"], inp["Wd"])
+    f = oracle_on_kernel_branch(ffn.forward(inp["x"][rows], inp["Wg"], inp["Wu"], inp["Wd"]),
+                                kernel_active_set(h.saved)[rows], inp["Wd"])
     b = ffn.backward(inp["x"][rows], inp["Wg"], inp["Wu"], inp["Wd"], inp["dy"][rows], spec.l1, fwd=f)
     assert_close(f64_of(y)[rows], f["y"], "y (sampled rows)")
     assert_close(f64_of(dx)[rows], b["dx"], "dx (sampled rows)")

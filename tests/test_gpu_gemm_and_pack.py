@@ -26,7 +26,9 @@ def _rand_bf16(shape, seed, scale=1.0):
 
 
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1)])
-@pytest.mark.parametrize("M,N,K", [(256, 192, 320), (192, 64, 64), (512, 256, 1024)])
+# (3072, 1792, 64): 168 tiles of 128 x 256 on 152 SMs, so the last 16 run as half-width
+# units after 152 whole ones (the second half of the last column tile reads past N)
+@pytest.mark.parametrize("M,N,K", [(256, 192, 320), (192, 64, 64), (512, 256, 1024), (3072, 1792, 64)])
 def test_dense_gemm_layouts(a_mn, b_mn, M, N, K):
     A = _rand_bf16((K, M) if a_mn else (M, K), 1)
     B = _rand_bf16((K, N) if b_mn else (N, K), 2)
