@@ -171,6 +171,15 @@ TW_DEV void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1)
       : "memory");
 }
+// The same load for a CTA of a pair: completion is signalled on the barrier at
+// `bar_cluster` (a shared::cluster address, here the pair's rank-0 barrier).
+TW_DEV void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar_cluster, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_addr(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
+      : "memory");
+}
 
 
 // Bounded wait used only while draining after an abort: ignores the abort flag.
@@ -217,6 +226,63 @@ TW_DEV void tc_commit(uint64_t* bar) {
                : "memory");
 }
 TW_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ------------------------------------------------------------------ CTA pairs (cta_group::2)
+// Two CTAs of a cluster share each MMA: the pair's accumulator tile is 256 rows, the
+// first 128 in rank 0's TMEM and the next 128 in rank 1's, and each CTA holds its own
+// A rows and half of the B tile in shared memory at the same offsets. Rank 0 issues
+// the MMAs. Allocation, its permit and deallocation are done by one warp of each CTA.
+TW_DEV uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of both CTAs; orders the shared-memory writes before it (barrier
+// initialisation, the TMEM address) for the other CTA.
+TW_DEV void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The shared::cluster address of the variable at `p` (this CTA's shared memory) in
+// the cluster's CTA `rank`.
+TW_DEV uint32_t peer_smem_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+  return r;
+}
+TW_DEV void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+TW_DEV void tmem_alloc_pair(uint32_t* smem_dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(smem_dst)),
+               "r"(ncols)
+               : "memory");
+}
+TW_DEV void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+TW_DEV void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// The pair's MMA: D rows [0, 128) into rank 0's TMEM at d_tmem and rows [128, 256)
+// into rank 1's; A and B descriptors address this CTA's shared memory, the other
+// CTA's operand halves sit at the same offsets.
+TW_DEV void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on the barrier at `bar`'s offset in both CTAs of the pair when every
+// tcgen05 operation this thread issued so far is done.
+TW_DEV void tc_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
 
 // Each lane of the warp reads 32 consecutive fp32 columns of its own TMEM lane.
 TW_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {

@@ -51,19 +51,31 @@ static bool tmap_mnmajor(CUtensorMap* m, const uint16_t* p, int K, int cols) {
 
 // max_rows bounds the rows of D (the grid has at most one CTA per tile); a device-
 // chosen split (sh.ksplit < 0) gets one CTA per SM.
-template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES, class Epi, int NA = 1>
+//
+// PAIR launches clusters of two CTAs (one 256-row unit per pair at a time), as many
+// pairs as can be resident at once (at most one CTA per SM), without a K split.
+template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES, class Epi, int NA = 1, bool PAIR = false>
 static cudaError_t run_gemm(const GemmMaps& maps, const GemmShape& sh, const typename Epi::Params& ep, int max_rows,
                             cudaStream_t s, const char* label) {
-  using Tr = GemmTraits<BN, A_MN, B_MN, DUAL, STAGES, NA>;
-  auto kern = gemm_tc_kernel<BN, A_MN, B_MN, DUAL, STAGES, Epi, NA>;
+  using Tr = GemmTraits<BN, A_MN, B_MN, DUAL, STAGES, NA, false, PAIR>;
+  auto kern = gemm_tc_kernel<BN, A_MN, B_MN, DUAL, STAGES, Epi, NA, PAIR>;
   constexpr int smem = Tr::SMEM_BYTES + Epi::kStageBytes * (epi_warps<BN, Epi>() / 4);
   static_assert(smem <= 232448, "GEMM shared memory above the 227 KiB opt-in limit");
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const long tiles = static_cast<long>((max_rows + GEMM_BM - 1) / GEMM_BM) * (sh.N / BN);
+  const long tiles = static_cast<long>((max_rows + Tr::UNIT_ROWS - 1) / Tr::UNIT_ROWS) * (sh.N / BN);
   if (tiles <= 0) return cudaSuccess;
-  const int grid = sh.ksplit < 0 ? device_sm_count() : static_cast<int>(std::min<long>(tiles, device_sm_count()));
-  e = launch(kern, dim3(grid), dim3(gemm_threads<BN, Epi>()), smem, s, maps, sh, ep);
+  if constexpr (PAIR) {
+    if (sh.ksplit > 1 || sh.ksplit < 0) return cudaErrorInvalidValue;  // CTA pairs run whole tiles
+    static int resident_pairs = -1;  // per instantiation: the query depends only on the kernel
+    if (resident_pairs < 0) resident_pairs = max_active_clusters(kern, gemm_threads<BN, Epi>(), smem, 2);
+    const int pairs = static_cast<int>(std::min<long>(tiles, std::min(resident_pairs, device_sm_count() / 2)));
+    if (pairs < 1) return cudaErrorInvalidConfiguration;
+    e = launch_clustered(kern, dim3(2 * pairs), dim3(gemm_threads<BN, Epi>()), smem, 2, s, maps, sh, ep);
+  } else {
+    const int grid = sh.ksplit < 0 ? device_sm_count() : static_cast<int>(std::min<long>(tiles, device_sm_count()));
+    e = launch(kern, dim3(grid), dim3(gemm_threads<BN, Epi>()), smem, s, maps, sh, ep);
+  }
   trace_mark(s, label);
   return e;
 }
@@ -101,9 +113,11 @@ cudaError_t gemm_gate_pack(const uint16_t* x, const uint16_t* Wg, int T, int d, 
   GemmMaps maps;
   const int bn = (I % 256 == 0) ? 256 : (I % 128 == 0) ? 128 : 64;
   sh.split_tail = (bn / 2) % W == 0;  // a half unit must hold whole TwELL tiles
-  if (!tmap_kmajor(&maps.a[0], x, T, d, 128) || !tmap_kmajor(&maps.b[0], Wg, I, d, bn)) return cudaErrorInvalidValue;
+  // 256-wide tiles run on CTA pairs, each CTA loading half of the B tile
+  if (!tmap_kmajor(&maps.a[0], x, T, d, 128) || !tmap_kmajor(&maps.b[0], Wg, I, d, bn == 256 ? 128 : bn))
+    return cudaErrorInvalidValue;
   fill_unused(maps, 1, 1);
-  if (bn == 256) return run_gemm<256, false, false, false, 4, EpiTwellPack>(maps, sh, ep, T, s, "gate_pack");
+  if (bn == 256) return run_gemm<256, false, false, false, 6, EpiTwellPack, 1, true>(maps, sh, ep, T, s, "gate_pack");
   if (bn == 128) return run_gemm<128, false, false, false, 6, EpiTwellPack>(maps, sh, ep, T, s, "gate_pack");
   return run_gemm<64, false, false, false, 8, EpiTwellPack>(maps, sh, ep, T, s, "gate_pack");
 }
@@ -117,9 +131,11 @@ cudaError_t gemm_gate_relu_dense(const uint16_t* x, const uint16_t* Wg, int T, i
   sh.split_tail = true;
   GemmMaps maps;
   const int bn = (I % 256 == 0) ? 256 : (I % 128 == 0) ? 128 : 64;
-  if (!tmap_kmajor(&maps.a[0], x, T, d, 128) || !tmap_kmajor(&maps.b[0], Wg, I, d, bn)) return cudaErrorInvalidValue;
+  // 256-wide tiles run on CTA pairs, each CTA loading half of the B tile
+  if (!tmap_kmajor(&maps.a[0], x, T, d, 128) || !tmap_kmajor(&maps.b[0], Wg, I, d, bn == 256 ? 128 : bn))
+    return cudaErrorInvalidValue;
   fill_unused(maps, 1, 1);
-  if (bn == 256) return run_gemm<256, false, false, false, 4, EpiReluBf16>(maps, sh, ep, T, s, "gate_dense");
+  if (bn == 256) return run_gemm<256, false, false, false, 6, EpiReluBf16, 1, true>(maps, sh, ep, T, s, "gate_dense");
   if (bn == 128) return run_gemm<128, false, false, false, 6, EpiReluBf16>(maps, sh, ep, T, s, "gate_dense");
   return run_gemm<64, false, false, false, 8, EpiReluBf16>(maps, sh, ep, T, s, "gate_dense");
 }
@@ -385,9 +401,11 @@ cudaError_t gemm_up_hybrid(const uint16_t* x, const uint16_t* Wu, int T, int d, 
                          backup_a, backup_u, cap,      H,        I,   ell_idx, ell_a, ell_u,  status};
   GemmMaps maps;
   const int bn = (I % 256 == 0) ? 256 : (I % 128 == 0) ? 128 : 64;
-  if (!tmap_kmajor(&maps.a[0], x, T, d, 128) || !tmap_kmajor(&maps.b[0], Wu, I, d, bn)) return cudaErrorInvalidValue;
+  // 256-wide tiles run on CTA pairs, each CTA loading half of the B tile
+  if (!tmap_kmajor(&maps.a[0], x, T, d, 128) || !tmap_kmajor(&maps.b[0], Wu, I, d, bn == 256 ? 128 : bn))
+    return cudaErrorInvalidValue;
   fill_unused(maps, 1, 1);
-  if (bn == 256) return run_gemm<256, false, false, false, 4, EpiUpHybrid>(maps, sh, ep, T, s, "dense_up");
+  if (bn == 256) return run_gemm<256, false, false, false, 6, EpiUpHybrid, 1, true>(maps, sh, ep, T, s, "dense_up");
   if (bn == 128) return run_gemm<128, false, false, false, 6, EpiUpHybrid>(maps, sh, ep, T, s, "dense_up");
   return run_gemm<64, false, false, false, 8, EpiUpHybrid>(maps, sh, ep, T, s, "dense_up");
 }
@@ -407,8 +425,9 @@ cudaError_t gemm_rows_nmajor_bf16(const uint16_t* const* A, const uint16_t* cons
       return cudaErrorInvalidValue;
   fill_unused(maps, segments, segments);
   EpiStoreBf16::Params ep{out, ld};
-  if (f16) return run_gemm<256, false, true, false, 4, F16Operands<EpiStoreBf16>>(maps, sh, ep, M, s, label);
-  return run_gemm<256, false, true, false, 4, EpiStoreBf16>(maps, sh, ep, M, s, label);
+  // CTA pairs (each CTA loads 128 of the tile's 256 B columns)
+  if (f16) return run_gemm<256, false, true, false, 6, F16Operands<EpiStoreBf16>, 1, true>(maps, sh, ep, M, s, label);
+  return run_gemm<256, false, true, false, 6, EpiStoreBf16, 1, true>(maps, sh, ep, M, s, label);
 }
 
 template <int BN, bool GATED>
@@ -419,7 +438,10 @@ static cudaError_t dense_grad_bn(const uint16_t* dY, const uint16_t* Wd, int T, 
   set_route(sh, route);
   sh.split_tail = true;
   GemmMaps maps;
-  if (!tmap_kmajor(&maps.a[0], dY, T, d, 128) || !tmap_kmajor(&maps.b[0], Wd, I, d, BN)) return cudaErrorInvalidValue;
+  // 256-wide tiles run on CTA pairs, each CTA loading half of the B tile
+  constexpr bool kPair = BN == 256;
+  constexpr int kBRows = kPair ? BN / 2 : BN;
+  if (!tmap_kmajor(&maps.a[0], dY, T, d, 128) || !tmap_kmajor(&maps.b[0], Wd, I, d, kBRows)) return cudaErrorInvalidValue;
   fill_unused(maps, 1, 1);
   typename EpiDenseGrad<GATED>::Params ep{h.R,
                                           I,
@@ -437,10 +459,10 @@ static cudaError_t dense_grad_bn(const uint16_t* dY, const uint16_t* Wd, int T, 
                                           H,
                                           I,
                                           status};
-  constexpr int kStageBytes = (128 + BN) * 64 * 2;
+  constexpr int kStageBytes = (128 + kBRows) * 64 * 2;
   constexpr int kBudget = 232448 - 1280 - EpiDenseGrad<GATED>::kStageBytes * (epi_warps<BN, EpiDenseGrad<GATED>>() / 4);
   constexpr int kStages = kBudget / kStageBytes < 8 ? kBudget / kStageBytes : 8;
-  return run_gemm<BN, false, false, false, kStages, EpiDenseGrad<GATED>>(maps, sh, ep, T, s, "dense_grad");
+  return run_gemm<BN, false, false, false, kStages, EpiDenseGrad<GATED>, 1, kPair>(maps, sh, ep, T, s, "dense_grad");
 }
 
 cudaError_t gemm_dense_grad(const uint16_t* dY, const uint16_t* Wd, int T, int d, int I, const tw_hybrid& h,
@@ -473,9 +495,10 @@ cudaError_t gemm_dense_weight_grads(const DenseWeightGradProblem* probs, int n_p
   }
   fill_unused(maps, n_probs, n_probs);
   ep.ldd = d;
-  ep.rows_per_problem = (I + GEMM_BM - 1) / GEMM_BM * GEMM_BM;
+  // CTA pairs: a problem's rows are whole 256-row units
+  ep.rows_per_problem = (I + 2 * GEMM_BM - 1) / (2 * GEMM_BM) * (2 * GEMM_BM);
   ep.add_if = add_if;
-  return run_gemm<256, true, true, false, 4, F16Operands<EpiF32GroupedStoreOrAdd>>(
+  return run_gemm<256, true, true, false, 6, F16Operands<EpiF32GroupedStoreOrAdd>, 1, true>(
       maps, sh, ep, ep.rows_per_problem * n_probs, s, "dense_weight_grad");
 }
 

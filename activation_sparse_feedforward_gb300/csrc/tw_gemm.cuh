@@ -23,6 +23,13 @@
 // tiles of all of them share the persistent grid. M and K may be read from device
 // memory (counts produced by earlier kernels in the stream), so the launch does not
 // need them on the host.
+//
+// PAIR runs the same roles on clusters of two CTAs with the two-SM MMA
+// (tcgen05.mma.cta_group::2, M = 256): each CTA stages its own 128 rows of A and half
+// of the B tile, rank 0's MMA thread issues for both, and each CTA's epilogue reads its
+// own 128 accumulator rows. Per MMA a CTA's shared memory serves 128 + BN / 2 operand
+// rows instead of 128 + BN; at BN = 256 the single-CTA form asks more of shared memory
+// (operand reads plus TMA writes) than one SM delivers at the tensor rate.
 #pragma once
 
 #include <type_traits>
@@ -118,15 +125,21 @@ __host__ __device__ constexpr int gemm_threads() {
 // NA = 2 pairs the segments: segments 2i and 2i + 1 share one B operand (b[2i]), so
 // a stage holds both A tiles and one B tile, and both products go into the same
 // accumulator (the hi / lo halves of a split fp32 operand against one weight).
-template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES, int NA = 1, bool F16 = false>
+// PAIR runs the GEMM on CTA pairs (clusters of two, cta_group::2 MMAs): a unit is a
+// 256-row tile, each CTA loads its 128 A rows and BN / 2 of the tile's B rows, and
+// the pair's shared-memory operand traffic per FLOP is two thirds of a single CTA's
+// at BN = 256, below what one SM's shared memory delivers at the MMA rate.
+template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES, int NA = 1, bool F16 = false, bool PAIR = false>
 struct GemmTraits {
   static constexpr int NB = DUAL ? 2 : 1;
   static constexpr int A_BYTES = GEMM_BM * GEMM_BK * 2;
-  static constexpr int B_BYTES = BN * GEMM_BK * 2;
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B rows (N) of a stage in one CTA
+  static constexpr int B_BYTES = B_ROWS * GEMM_BK * 2;
   static constexpr int STAGE_BYTES = NA * A_BYTES + NB * B_BYTES;
   static constexpr int ACC_COLS = BN * NB;
   static constexpr int TMEM_COLS = 2 * ACC_COLS;
-  static constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, BN, A_MN, B_MN, F16);
+  static constexpr int UNIT_ROWS = PAIR ? 2 * GEMM_BM : GEMM_BM;
+  static constexpr uint32_t IDESC = idesc_bf16_f32(UNIT_ROWS, BN, A_MN, B_MN, F16);
   static constexpr uint32_t IDESC_HALF = idesc_bf16_f32(GEMM_BM, BN / 2, A_MN, B_MN, F16);  // half-width units
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
@@ -135,6 +148,7 @@ struct GemmTraits {
   static_assert((2 * STAGES + 4) * 8 + 8 <= BAR_BYTES, "barrier area");
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
   static_assert(NA == 1 || (NA == 2 && !DUAL), "paired A segments take one B operand");
+  static_assert(!PAIR || (!DUAL && NA == 1 && BN >= 128), "CTA pairs: one B operand, one A tile, BN >= 128");
 };
 
 // The K split of a launch whose units are handed out to `grid` CTAs in rounds: the
@@ -181,11 +195,11 @@ TW_DEV UnitInfo unit_info(int unit, int ksplit, int kb_chunk, int kb_total, int 
   return u;
 }
 
-template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES, class Epi, int NA = 1>
+template <int BN, bool A_MN, bool B_MN, bool DUAL, int STAGES, class Epi, int NA = 1, bool PAIR = false>
 __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
     gemm_tc_kernel(const __grid_constant__ GemmMaps maps, const GemmShape shape,
                    const __grid_constant__ typename Epi::Params ep) {
-  using Tr = GemmTraits<BN, A_MN, B_MN, DUAL, STAGES, NA, epi_f16_operands<Epi>::value>;
+  using Tr = GemmTraits<BN, A_MN, B_MN, DUAL, STAGES, NA, epi_f16_operands<Epi>::value, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
   uint8_t* tiles = smem_raw + pad;
@@ -198,6 +212,10 @@ __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // CTA pairs: rank 0 issues the MMAs and owns the "full" and "accumulator empty"
+  // barriers both CTAs signal; each CTA's own "empty" and "accumulator full" barriers
+  // get the MMA commits of rank 0 (multicast)
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -206,7 +224,7 @@ __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull + b, 1);
-      mbar_init(tempty + b, epi_warps<BN, Epi>());
+      mbar_init(tempty + b, (PAIR ? 2 : 1) * epi_warps<BN, Epi>());
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -219,11 +237,17 @@ __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
     if (DUAL) tma_prefetch_desc(&maps.b[1]);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, Tr::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(tmem_slot, Tr::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, Tr::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // both CTAs' barriers and TMEM exist before either signals the other
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   pdl_enter();  // the setup above overlaps the previous kernel's tail
@@ -233,7 +257,7 @@ __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
   int K = shape.K;
   if (shape.k_dev != nullptr) K = min(max(*shape.k_dev, 0), shape.k_cap);
   if (shape.route_dev != nullptr && *shape.route_dev != shape.route_want) K = 0;  // not this call's route: no work
-  const int m_tiles = (M + GEMM_BM - 1) / GEMM_BM;
+  const int m_tiles = (M + Tr::UNIT_ROWS - 1) / Tr::UNIT_ROWS;
   const int n_tiles = shape.N / BN;
   const int problems = max(1, shape.problems) -
                        ((shape.drop_last_problem_if != nullptr && *shape.drop_last_problem_if == 1) ? 1 : 0);
@@ -242,16 +266,19 @@ __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
   const int kb_total = kb_per_seg * (shape.segments / NA);  // one K step covers NA segments
   // work unit = (output tile, slice of its K loop); empty slices are skipped by
   // every role alike
-  const int ksplit =
-      shape.ksplit >= 0   ? max(1, shape.ksplit)
-      : shape.ksplit == -2 ? split_by_cost(num_tiles, kb_total, static_cast<int>(gridDim.x))
-                           : (num_tiles > 0 ? max(1, min(kb_total, static_cast<int>(gridDim.x) / num_tiles)) : 1);
+  // units are handed out per CTA, or per pair
+  const int grid = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int first_unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int ksplit = PAIR                ? 1
+                     : shape.ksplit >= 0 ? max(1, shape.ksplit)
+                     : shape.ksplit == -2 ? split_by_cost(num_tiles, kb_total, grid)
+                                          : (num_tiles > 0 ? max(1, min(kb_total, grid / num_tiles)) : 1);
   const int kb_chunk = (kb_total + ksplit - 1) / ksplit;
   // the tail split: the last round's tiles as two half-width units each, when they fill
   // at most half the grid (so the last round takes half a tile's time)
-  const int grid = static_cast<int>(gridDim.x);
   const int rem = num_tiles % grid;
-  const bool tail = shape.split_tail && !DUAL && BN >= 128 && ksplit == 1 && rem > 0 && 2 * rem <= grid;
+  const bool tail =
+      !PAIR && shape.split_tail && !DUAL && BN >= 128 && ksplit == 1 && rem > 0 && 2 * rem <= grid;
   const int full_units = tail ? num_tiles - rem : num_tiles * ksplit;
   const int num_units = tail ? full_units + 2 * rem : num_tiles * ksplit;
 
@@ -262,22 +289,24 @@ __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
       uint32_t phase = 0;
       long issued = 0;
       bool ok = true;
-      for (int unit = blockIdx.x; ok && unit < num_units; unit += gridDim.x) {
+      for (int unit = first_unit; ok && unit < num_units; unit += grid) {
         const UnitInfo ui = unit_info(unit, ksplit, kb_chunk, kb_total, full_units);
         const int tile = ui.tile, kb_lo = ui.kb_lo, kb_hi = ui.kb_hi;
         if (kb_lo >= kb_hi) continue;
         const int row_tile = tile / n_tiles;
         const int prob = row_tile / m_tiles;
-        const int m0 = (row_tile - prob * m_tiles) * GEMM_BM;  // within the problem
+        // within the problem; a pair's rank 1 loads the unit's second 128 rows
+        const int m0 = (row_tile - prob * m_tiles) * Tr::UNIT_ROWS + static_cast<int>(rank) * GEMM_BM;
         // a second half's B box starts at its own columns (the box's other half, past
-        // the tile or past N, is loaded but not used)
-        const int n0 = (tile % n_tiles) * BN + (ui.half == 1 ? BN / 2 : 0);
+        // the tile or past N, is loaded but not used); a pair's ranks load one half of
+        // the B tile each
+        const int n0 = (tile % n_tiles) * BN + (ui.half == 1 ? BN / 2 : 0) + static_cast<int>(rank) * Tr::B_ROWS;
         for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, shape.status)) {
             ok = false;
             break;
           }
-          if (kb == shape.withhold_kb && unit == static_cast<int>(blockIdx.x)) {
+          if (kb == shape.withhold_kb && unit == first_unit) {
             // test hook: this stage is never filled (its "full" barrier gets no arrival)
             ++issued;
             if (++stage == STAGES) {
@@ -292,16 +321,24 @@ __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
           const int seg = grp * NA;
           const int k0 = (kb - grp * kb_per_seg) * GEMM_BK;
           const CUtensorMap* tb = &maps.b[prob * shape.segments + seg];
-          mbar_arrive_expect_tx(full + stage, Tr::STAGE_BYTES);
+          // a pair's loads all complete on rank 0's barrier, which expects both CTAs' bytes
+          if (rank == 0) mbar_arrive_expect_tx(full + stage, (PAIR ? 2 : 1) * Tr::STAGE_BYTES);
+          const uint32_t fbar = PAIR ? peer_smem_addr(full + stage, 0) : 0u;
+          auto load = [&](uint8_t* dst, const CUtensorMap* map, int c0, int c1) {
+            if constexpr (PAIR)
+              tma_load_2d_pair(dst, map, fbar, c0, c1);
+            else
+              tma_load_2d(dst, map, full + stage, c0, c1);
+          };
 #pragma unroll
           for (int na = 0; na < NA; ++na) {
             const CUtensorMap* ta = &maps.a[prob * shape.segments + seg + na];
             uint8_t* dA = sA + na * Tr::A_BYTES;
             if (!A_MN) {
-              tma_load_2d(dA, ta, full + stage, k0, m0);
+              load(dA, ta, k0, m0);
             } else {
-              tma_load_2d(dA, ta, full + stage, m0, k0);
-              tma_load_2d(dA + 8192, ta, full + stage, m0 + 64, k0);
+              load(dA, ta, m0, k0);
+              load(dA + 8192, ta, m0 + 64, k0);
             }
           }
 #pragma unroll
@@ -309,10 +346,10 @@ __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
             const CUtensorMap* tbb = (nb == 0) ? tb : &maps.b[1];
             uint8_t* dst = sB + nb * Tr::B_BYTES;
             if (!B_MN) {
-              tma_load_2d(dst, tbb, full + stage, k0, n0);
+              load(dst, tbb, k0, n0);
             } else {
 #pragma unroll
-              for (int c = 0; c < BN / 64; ++c) tma_load_2d(dst + c * 8192, tbb, full + stage, n0 + c * 64, k0);
+              for (int c = 0; c < Tr::B_ROWS / 64; ++c) load(dst + c * 8192, tbb, n0 + c * 64, k0);
             }
           }
           ++issued;
@@ -322,8 +359,10 @@ __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
           }
         }
       }
-      if (!ok) {
-        // let the loads already issued land before the CTA can exit
+      if (!ok && rank == 0) {
+        // let the loads already issued land before the CTA can exit (a pair's rank 1
+        // loads complete on rank 0's barriers, which rank 0 drains; rank 1 stays until
+        // rank 0 reaches the closing cluster barrier)
         for (long i = 0; i < STAGES && i < issued; ++i) {
           const long q = issued - 1 - i;
           mbar_wait_drain(full + (q % STAGES), static_cast<uint32_t>((q / STAGES) & 1));
@@ -332,13 +371,13 @@ __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
       bool issued_any = false;
-      for (int unit = blockIdx.x; ok && unit < num_units; unit += gridDim.x) {
+      for (int unit = first_unit; ok && unit < num_units; unit += grid) {
         const UnitInfo ui = unit_info(unit, ksplit, kb_chunk, kb_total, full_units);
         const int kb_lo = ui.kb_lo, kb_hi = ui.kb_hi;
         if (kb_lo >= kb_hi) continue;
@@ -373,25 +412,37 @@ __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
                 const uint32_t bb = b_base + nb * Tr::B_BYTES;
                 const uint64_t bd = B_MN ? smem_desc_sw128(bb + k16 * 2048, 8192, 1024)
                                          : smem_desc_sw128(bb + k16 * 32, 16, 1024);
-                tc_mma_bf16(d0 + nb * BN, ad, bd, idesc, acc);
+                if constexpr (PAIR)
+                  tc_mma_bf16_pair(d0 + nb * BN, ad, bd, idesc, acc);
+                else
+                  tc_mma_bf16(d0 + nb * BN, ad, bd, idesc, acc);
               }
             }
           }
           issued_any = true;
-          tc_commit(empty + stage);
+          if constexpr (PAIR)
+            tc_commit_pair(empty + stage);
+          else
+            tc_commit(empty + stage);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(tfull + buf);
+        if constexpr (PAIR)
+          tc_commit_pair(tfull + buf);
+        else
+          tc_commit(tfull + buf);
       }
       if (!ok && issued_any) {
         // wait for MMAs in flight before TMEM is released: the commit completes the
         // current phase of this ring slot's "empty" barrier (parity == phase)
         uint64_t* drain = empty + stage;
-        tc_commit(drain);
+        if constexpr (PAIR)
+          tc_commit_pair(drain);
+        else
+          tc_commit(drain);
         mbar_wait_drain(drain, phase);
       }
     }
@@ -404,14 +455,14 @@ __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
     const int half = ew >> 2;      // which kCols columns of the tile (0 with four warps)
     const int row = quarter * 32 + lane;
     int local = 0;
-    for (int unit = blockIdx.x; unit < num_units; unit += gridDim.x) {
+    for (int unit = first_unit; unit < num_units; unit += grid) {
       const UnitInfo ui = unit_info(unit, ksplit, kb_chunk, kb_total, full_units);
       if (ui.kb_lo >= ui.kb_hi) continue;
       const int tile = ui.tile;
       const int buf = local & 1;
       const uint32_t use = static_cast<uint32_t>(local >> 1);
       ++local;
-      const int m = (tile / n_tiles) * GEMM_BM + row;
+      const int m = (tile / n_tiles) * Tr::UNIT_ROWS + static_cast<int>(rank) * GEMM_BM + row;
       // this warp's columns: kCols at half * kCols of a whole tile; of a half unit, its
       // BN / 2 columns (with eight warps all of them for the first group's warps, none
       // for the second's), at the start of the accumulator
@@ -465,15 +516,26 @@ __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
       }
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty + buf);
+      if (lane == 0) {
+        if constexpr (PAIR)
+          mbar_arrive_cluster(peer_smem_addr(tempty + buf, 0));  // rank 0's MMA issuer waits for both CTAs
+        else
+          mbar_arrive(tempty + buf);
+      }
       e.finish();
     }
   }
 
   __syncthreads();
+  // a pair's CTAs leave together: no signal or MMA write of one may reach the other
+  // after it has released its TMEM or exited
+  if constexpr (PAIR) cluster_sync();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, Tr::TMEM_COLS);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem_base, Tr::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, Tr::TMEM_COLS);
   }
 }
 
@@ -634,7 +696,7 @@ struct EpiF32GroupedStoreOrAdd {
   struct Params {
     float* D[kMaxProblems];
     int ldd;
-    int rows_per_problem;
+    int rows_per_problem;  // the problem's rows rounded up to whole units (256 rows on CTA pairs)
     const int32_t* add_if;
   };
   const Params& p;
