@@ -191,9 +191,11 @@ static cudaError_t rows_times_kmajor_split(const uint16_t* X, const uint16_t* co
 template <int BN>
 static cudaError_t rows_store_bn(const GemmMaps& maps, const GemmShape& sh, const EpiStoreF32RowsGrouped::Params& ep,
                                  int max_rows, cudaStream_t s) {
-  constexpr int kStageBytes = (128 + BN) * 64 * 2;
+  constexpr bool kPair = BN == 256;  // CTA pairs, each CTA loading half of the B tile
+  constexpr int kStageBytes = (128 + (kPair ? BN / 2 : BN)) * 64 * 2;
   constexpr int kStages = (192 * 1024) / kStageBytes < 8 ? (192 * 1024) / kStageBytes : 8;
-  return run_gemm<BN, false, false, false, kStages, EpiStoreF32RowsGrouped>(maps, sh, ep, max_rows, s, "backup_hidden");
+  return run_gemm<BN, false, false, false, kStages, EpiStoreF32RowsGrouped, 1, kPair>(maps, sh, ep, max_rows, s,
+                                                                                      "backup_hidden");
 }
 static cudaError_t rows_store_a_u(const uint16_t* X, const uint16_t* Wg, const uint16_t* Wu, int rows_alloc,
                                   const int32_t* n_dev, int cap, int d, int I, float* save_a, float* save_u,
@@ -208,12 +210,13 @@ static cudaError_t rows_store_a_u(const uint16_t* X, const uint16_t* Wg, const u
   const int bn = (I % 256 == 0) ? 256 : (I % 128 == 0) ? 128 : 64;
   GemmMaps maps;
   const uint16_t* B[2] = {Wg, Wu};
-  EpiStoreF32RowsGrouped::Params ep{{save_a, save_u}, I, 1u};
+  const int unit_rows = bn == 256 ? 2 * GEMM_BM : GEMM_BM;  // CTA pairs on 256-wide tiles
+  EpiStoreF32RowsGrouped::Params ep{{save_a, save_u}, I, 1u, unit_rows};
   for (int p = 0; p < n_b; ++p)
-    if (!tmap_kmajor(&maps.a[p], X, rows_alloc, d, 128) || !tmap_kmajor(&maps.b[p], B[p], I, d, bn))
+    if (!tmap_kmajor(&maps.a[p], X, rows_alloc, d, 128) || !tmap_kmajor(&maps.b[p], B[p], I, d, bn == 256 ? 128 : bn))
       return cudaErrorInvalidValue;
   fill_unused(maps, n_b, n_b);
-  const int max_rows = (cap + GEMM_BM - 1) / GEMM_BM * GEMM_BM * n_b;
+  const int max_rows = (cap + unit_rows - 1) / unit_rows * unit_rows * n_b;
   if (bn == 256) return rows_store_bn<256>(maps, sh, ep, max_rows, s);
   if (bn == 128) return rows_store_bn<128>(maps, sh, ep, max_rows, s);
   return rows_store_bn<64>(maps, sh, ep, max_rows, s);

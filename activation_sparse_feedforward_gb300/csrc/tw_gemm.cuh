@@ -140,7 +140,7 @@ struct GemmTraits {
   static constexpr int TMEM_COLS = 2 * ACC_COLS;
   static constexpr int UNIT_ROWS = PAIR ? 2 * GEMM_BM : GEMM_BM;
   static constexpr uint32_t IDESC = idesc_bf16_f32(UNIT_ROWS, BN, A_MN, B_MN, F16);
-  static constexpr uint32_t IDESC_HALF = idesc_bf16_f32(GEMM_BM, BN / 2, A_MN, B_MN, F16);  // half-width units
+  static constexpr uint32_t IDESC_HALF = idesc_bf16_f32(UNIT_ROWS, BN / 2, A_MN, B_MN, F16);  // half-width units
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + BAR_BYTES;
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64, 128, 192 or 256");
@@ -277,6 +277,7 @@ __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
   // the tail split: the last round's tiles as two half-width units each, when they fill
   // at most half the grid (so the last round takes half a tile's time)
   const int rem = num_tiles % grid;
+  // (not on CTA pairs: half-width pair units, measured at T 8192, were slower than whole ones)
   const bool tail =
       !PAIR && shape.split_tail && !DUAL && BN >= 128 && ksplit == 1 && rem > 0 && 2 * rem <= grid;
   const int full_units = tail ? num_tiles - rem : num_tiles * ksplit;
@@ -646,7 +647,8 @@ struct EpiStoreF32Grouped {
 
 // D_p[m][n] = acc (fp32), or ReLU(acc) for the problems whose bit is set in relu, for a
 // grouped launch over a device row count M (problem p's row tiles follow problem
-// p - 1's, M rounded up to whole 128-row tiles each); rows at or past M are skipped.
+// p - 1's, M rounded up to whole units of unit_rows each: 128, or 256 on CTA pairs);
+// rows at or past M are skipped.
 struct EpiStoreF32RowsGrouped {
   static constexpr int kStageBytes = kEpiTransposeBytes;
   static constexpr bool kOverlapLoads = true;
@@ -655,13 +657,14 @@ struct EpiStoreF32RowsGrouped {
     float* D[kMaxProblems];
     int ldd;
     unsigned relu;
+    int unit_rows;
   };
   const Params& p;
   int m, M, n0;
   float* stage = nullptr;  // this warp's transpose buffer
   TW_DEV EpiStoreF32RowsGrouped(const Params& p_, int m_, int M_, int n0_) : p(p_), m(m_), M(M_), n0(n0_) {}
   TW_DEV void chunk(int c, const uint32_t (&v)[32], const uint32_t (&)[32]) {
-    const int rows_per_problem = (M + GEMM_BM - 1) / GEMM_BM * GEMM_BM;
+    const int rows_per_problem = (M + p.unit_rows - 1) / p.unit_rows * p.unit_rows;
     const int prob = m / rows_per_problem;  // the same for the warp's 32 rows
     if (prob >= kMaxProblems) return;       // uniform over the warp
     uint32_t w[32];
