@@ -71,10 +71,13 @@ SIGNATURES = {
     "tw_reinit_dead_rows": (c_int, [c_void_p, c_int, c_int, c_void_p, ctypes.c_uint64, c_float, c_void_p, c_void_p]),
     "tw_dense_gemm": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p,
                               c_void_p]),
+    "tw_dense_gemm_pair": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p,
+                              c_void_p]),
     "tw_l2_gather_probe": (c_int, [c_void_p, c_int, c_int, c_void_p, c_int, c_void_p, c_int,
                                    ctypes.POINTER(ctypes.c_double), c_void_p]),
     "tw_l2_gather_probe_blocks": (c_int, [c_int]),
     "tw_wait_timeout_probe": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]),
+    "tw_wait_timeout_probe_pair": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]),
     "tw_fma_probe": (c_int, [c_void_p, c_int, c_int, ctypes.POINTER(ctypes.c_double), c_void_p]),
     "tw_trace_begin": (c_int, [ctypes.POINTER(c_void_p), c_int]),
     "tw_trace_end": (c_int, []),

@@ -720,4 +720,22 @@ tw_status tw_dense_gemm(const uint16_t* A, const uint16_t* B, int M, int N, int 
   return from_cuda(tw::gemm_dense_test(A, B, M, N, K, a_mn, b_mn, D, dev_status, as_stream(stream)));
 }
 
+tw_status tw_dense_gemm_pair(const uint16_t* A, const uint16_t* B, int M, int N, int K, int a_mn, int b_mn, float* D,
+                             int32_t* dev_status, void* stream) {
+  if (M < 1 || N < 1 || K < 1 || N % 256 != 0 || K % 64 != 0) return TW_EINVAL;
+  if (a_mn && M % 64 != 0) return TW_EINVAL;
+  tw_status st = check_ptrs({A, B, D, dev_status});
+  if (st != TW_OK) return st;
+  return from_cuda(tw::gemm_dense_test(A, B, M, N, K, a_mn, b_mn, D, dev_status, as_stream(stream), -1, true));
+}
+
+tw_status tw_wait_timeout_probe_pair(const uint16_t* A, const uint16_t* B, int M, int N, int K, int withhold_kb,
+                                     float* D, int32_t* dev_status, void* stream) {
+  if (M < 1 || M > 256 || N != 256 || K < 64 || K % 64 != 0) return TW_EINVAL;
+  if (withhold_kb < 0 || withhold_kb >= K / 64) return TW_EINVAL;
+  tw_status st = check_ptrs({A, B, D, dev_status});
+  if (st != TW_OK) return st;
+  return from_cuda(tw::gemm_dense_test(A, B, M, N, K, 0, 0, D, dev_status, as_stream(stream), withhold_kb, true));
+}
+
 }  // extern "C"

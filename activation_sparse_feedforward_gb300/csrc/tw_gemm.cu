@@ -507,16 +507,23 @@ cudaError_t gemm_dense_weight_grads(const DenseWeightGradProblem* probs, int n_p
 
 // ------------------------------------------------------------------ layout test GEMM
 cudaError_t gemm_dense_test(const uint16_t* A, const uint16_t* B, int M, int N, int K, int a_mn, int b_mn, float* D,
-                            int32_t* status, cudaStream_t s, int withhold_kb) {
+                            int32_t* status, cudaStream_t s, int withhold_kb, bool pair) {
   GemmShape sh = shape_static(M, N, K, status);
   sh.withhold_kb = withhold_kb;
   sh.split_tail = true;
   EpiStoreF32::Params ep{D, N};
   GemmMaps maps;
   const bool oka = a_mn ? tmap_mnmajor(&maps.a[0], A, K, M) : tmap_kmajor(&maps.a[0], A, M, K, 128);
-  const bool okb = b_mn ? tmap_mnmajor(&maps.b[0], B, K, N) : tmap_kmajor(&maps.b[0], B, N, K, 64);
+  const bool okb = b_mn ? tmap_mnmajor(&maps.b[0], B, K, N) : tmap_kmajor(&maps.b[0], B, N, K, pair ? 128 : 64);
   if (!oka || !okb) return cudaErrorInvalidValue;
   fill_unused(maps, 1, 1);
+  if (pair) {
+    // 256 x 256 units on CTA pairs (N % 256 == 0)
+    if (!a_mn && !b_mn) return run_gemm<256, false, false, false, 6, EpiStoreF32, 1, true>(maps, sh, ep, M, s, "dense_gemm");
+    if (!a_mn && b_mn) return run_gemm<256, false, true, false, 6, EpiStoreF32, 1, true>(maps, sh, ep, M, s, "dense_gemm");
+    if (a_mn && !b_mn) return run_gemm<256, true, false, false, 6, EpiStoreF32, 1, true>(maps, sh, ep, M, s, "dense_gemm");
+    return run_gemm<256, true, true, false, 6, EpiStoreF32, 1, true>(maps, sh, ep, M, s, "dense_gemm");
+  }
   if (!a_mn && !b_mn) return run_gemm<64, false, false, false, 8, EpiStoreF32>(maps, sh, ep, M, s, "dense_gemm");
   if (!a_mn && b_mn) return run_gemm<64, false, true, false, 8, EpiStoreF32>(maps, sh, ep, M, s, "dense_gemm");
   if (a_mn && !b_mn) return run_gemm<64, true, false, false, 8, EpiStoreF32>(maps, sh, ep, M, s, "dense_gemm");

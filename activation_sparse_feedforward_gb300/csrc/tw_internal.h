@@ -350,7 +350,8 @@ struct DenseWeightGradProblem {
 cudaError_t gemm_dense_weight_grads(const DenseWeightGradProblem* probs, int n_probs, int T, int I, int d,
                                     const int32_t* add_if, const int32_t* route, int32_t* status, cudaStream_t s);
 
+// The layout-test GEMM (fp32 D = A B); pair runs it on CTA pairs (N % 256 == 0).
 cudaError_t gemm_dense_test(const uint16_t* A, const uint16_t* B, int M, int N, int K, int a_mn, int b_mn, float* D,
-                            int32_t* status, cudaStream_t s, int withhold_kb = -1);
+                            int32_t* status, cudaStream_t s, int withhold_kb = -1, bool pair = false);
 
 }  // namespace tw

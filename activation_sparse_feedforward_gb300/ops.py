@@ -403,15 +403,17 @@ def reinit_dead_rows(W: torch.Tensor, counts: torch.Tensor, seed: int, std: floa
 
 
 def dense_gemm(A: torch.Tensor, B: torch.Tensor, M: int, N: int, K: int, a_mn: bool, b_mn: bool,
-               status: torch.Tensor | None = None) -> torch.Tensor:
+               status: torch.Tensor | None = None, pair: bool = False) -> torch.Tensor:
     """D = A B (fp32) on the tcgen05 GEMM engine. A is [M, K] (a_mn False) or stored
-    [K, M]; B is stored [N, K] (b_mn False) or [K, N]."""
+    [K, M]; B is stored [N, K] (b_mn False) or [K, N]. pair: on CTA pairs
+    (tw_dense_gemm_pair, N % 256 == 0)."""
     _check_bf16("A", A)
     _check_bf16("B", B)
     D = torch.empty((M, N), dtype=torch.float32, device=A.device)
     st = status if status is not None else new_status(A.device)
-    _lib.check(_lib.load().tw_dense_gemm(_ptr(A), _ptr(B), M, N, K, int(a_mn), int(b_mn), _ptr(D), _ptr(st),
-                                         _stream()), "tw_dense_gemm")
+    name = "tw_dense_gemm_pair" if pair else "tw_dense_gemm"
+    _lib.check(getattr(_lib.load(), name)(_ptr(A), _ptr(B), M, N, K, int(a_mn), int(b_mn), _ptr(D), _ptr(st),
+                                          _stream()), name)
     return D
 
 

@@ -347,6 +347,13 @@ tw_status tw_reinit_dead_rows(uint16_t* W, int I, int d, const int32_t* counts, 
 tw_status tw_dense_gemm(const uint16_t* A, const uint16_t* B, int M, int N, int K,
                         int a_mn, int b_mn, float* D, int32_t* dev_status, void* stream);
 
+/* tw_dense_gemm on CTA pairs: clusters of two CTAs, each 256 x 256 unit computed by
+ * the two-SM form of the MMA (tcgen05.mma.cta_group::2) with each CTA holding its 128
+ * rows of A and half of the B tile, as the library's 256-wide GEMMs run. Arguments
+ * and layouts as tw_dense_gemm; requires N % 256 == 0 (TW_EINVAL otherwise). */
+tw_status tw_dense_gemm_pair(const uint16_t* A, const uint16_t* B, int M, int N, int K,
+                             int a_mn, int b_mn, float* D, int32_t* dev_status, void* stream);
+
 /* L2 row-gather throughput probe for measurement tools (no counterpart on the pages):
  * the access pattern of the sparse kernels, with nothing else. `blocks` CTAs of d / 8
  * threads (one warp per 256-wide slice of d) take groups of eight indices from idx
@@ -375,6 +382,14 @@ int tw_l2_gather_probe_blocks(int d);
  * left unspecified. Nothing faults, traps or spins without a limit. */
 tw_status tw_wait_timeout_probe(const uint16_t* A, const uint16_t* B, int M, int N, int K, int withhold_kb,
                                 float* D, int32_t* dev_status, void* stream);
+
+/* The same test hook on a CTA pair (tw_dense_gemm_pair with a_mn = b_mn = 0; M <= 256,
+ * one 256-row unit; N == 256; K a multiple of 64): both CTAs leave K block
+ * `withhold_kb` unloaded, the MMA issuer's wait runs out, each CTA's waits end by the
+ * abort flag or their own limit, and the two CTAs meet at the closing cluster barrier
+ * before TMEM is freed. TW_ETIMEOUT in *dev_status; D left unspecified. */
+tw_status tw_wait_timeout_probe_pair(const uint16_t* A, const uint16_t* B, int M, int N, int K, int withhold_kb,
+                                     float* D, int32_t* dev_status, void* stream);
 
 /* CUDA-core fp32 throughput probe for measurement tools (no counterpart on the
  * pages): `blocks` CTAs of 256 threads each run 8 independent chains of `iters`

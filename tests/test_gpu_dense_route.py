@@ -34,10 +34,14 @@ CASES = [
     # long ELL rows (the grad epilogue's row search and walk over many entries per tile)
     FFNSpec("dense_long_rows", T=513, d=512, I=1280, mean_active=200, outlier_frac=0.02, W=128, C=40, R=320,
             seed=24),
-    # 16 x 22 = 352 tiles in the gate, up and grad GEMMs: 304 whole tiles, then the last
-    # 48 as half-width units (the tail split with both kinds in one launch)
+    # 8 x 22 = 176 units of 256 x 256 on CTA pairs in the gate, up and grad GEMMs (more
+    # than one round, the last partly empty); d = 256: one column of units for down, dx
     FFNSpec("dense_mixed_tail", T=2048, d=256, I=5632, mean_active=100, outlier_frac=0.01, W=128, C=16, R=224,
             seed=30),
+    # I = 1152: 128-wide column tiles, one CTA each, in the gate, up and grad GEMMs;
+    # 18 x 9 = 162 tiles on 152 SMs, so the last 10 run as half-width units
+    FFNSpec("dense_i1152_tail", T=2300, d=512, I=1152, mean_active=60, outlier_frac=0.01, W=128, C=16, R=160,
+            seed=31),
 ]
 
 

@@ -25,19 +25,35 @@ def _rand_bf16(shape, seed, scale=1.0):
     return round_to_bf16_bits(rng.standard_normal(shape).astype(np.float32) * scale)
 
 
-@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1)])
-# (3072, 1792, 64): 168 tiles of 128 x 256 on 152 SMs, so the last 16 run as half-width
-# units after 152 whole ones (the second half of the last column tile reads past N)
-@pytest.mark.parametrize("M,N,K", [(256, 192, 320), (192, 64, 64), (512, 256, 1024), (3072, 1792, 64)])
-def test_dense_gemm_layouts(a_mn, b_mn, M, N, K):
+def _check_layout(M, N, K, a_mn, b_mn, pair):
     A = _rand_bf16((K, M) if a_mn else (M, K), 1)
     B = _rand_bf16((K, N) if b_mn else (N, K), 2)
-    D = tw.dense_gemm(to_dev(A), to_dev(B), M, N, K, bool(a_mn), bool(b_mn))
+    D = tw.dense_gemm(to_dev(A), to_dev(B), M, N, K, bool(a_mn), bool(b_mn), pair=pair)
     torch.cuda.synchronize()
     a = ffn.bf16_to_f64(A)
     b = ffn.bf16_to_f64(B)
     ref = (a.T if a_mn else a) @ (b if b_mn else b.T)
     np.testing.assert_allclose(D.cpu().numpy(), ref, rtol=1e-4, atol=1e-4 * np.sqrt(K))
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1)])
+# 128 x 64 tiles, one CTA each; (3072, 1792, 64) is 672 tiles, several rounds
+@pytest.mark.parametrize("M,N,K", [(256, 192, 320), (192, 64, 64), (512, 256, 1024), (3072, 1792, 64)])
+def test_dense_gemm_layouts(a_mn, b_mn, M, N, K):
+    _check_layout(M, N, K, a_mn, b_mn, pair=False)
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 0), (1, 1)])
+# 256 x 256 units on CTA pairs: one unit whose second CTA's rows are all past M
+# (M 192), whole units, and (3072, 1792, 64): 84 units on at most 76 pairs
+@pytest.mark.parametrize("M,N,K", [(192, 256, 64), (512, 512, 1024), (3072, 1792, 64)])
+def test_dense_gemm_pair_layouts(a_mn, b_mn, M, N, K):
+    _check_layout(M, N, K, a_mn, b_mn, pair=True)
+
+
+def test_dense_gemm_pair_ragged_rows():
+    """M = 300: the second unit's first CTA holds rows 256..299, its second CTA none."""
+    _check_layout(300, 256, 192, 0, 0, pair=True)
 
 
 def test_dense_gemm_ragged_rows():
