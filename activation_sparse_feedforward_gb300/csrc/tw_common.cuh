@@ -100,6 +100,8 @@ TW_DEV float2 unpair(f32x2 v) {
 TW_DEV void fma2(f32x2& acc, f32x2 a, f32x2 b) { asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b)); }
 // a packed bf16 pair (low half = element 0) widened exactly to two fp32 lanes
 TW_DEV f32x2 widen(uint32_t w) { return pair(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)); }
+// A 16-byte read-only load through the non-coherent path (the gathers' row slices).
+TW_DEV uint4 ldg16(const uint4* p) { return __ldg(p); }
 
 // ------------------------------------------------------------------ smem / timers
 TW_DEV uint32_t smem_addr(const void* p) {

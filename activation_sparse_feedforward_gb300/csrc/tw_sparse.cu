@@ -61,7 +61,6 @@ TW_DEV void out_f32x8(float* p, const F8& y, bool add) {
   else
     stcs_f32x8(p, y);
 }
-TW_DEV uint4 ldg16(const uint4* p) { return __ldg(p); }
 constexpr int kCountHistMaxBins = 48 * 1024;  // 192 KB of shared memory
 template <class K>
 cudaError_t set_smem_bytes(K kern, size_t bytes) {

@@ -114,7 +114,6 @@ TW_DEV float reduce8(float (&p)[8], int lane) {
   return s;
 }
 
-TW_DEV uint4 ldg16(const uint4* p) { return __ldg(p); }
 
 // Token scheduling: a CTA's first token is its index; after that it takes the next
 // unclaimed token from a device counter (zero at launch), so CTAs that start late or
