@@ -23,11 +23,12 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_tiled_fn() {
   return fn;
 }
 
-// 2D bf16 tensor map with 128-byte swizzle: dims {inner, outer}, rows row_bytes apart,
-// box {box_inner, box_outer} (box_inner * 2 bytes must be <= 128). Out-of-range
-// elements read as zero.
+// 2D bf16 tensor map with 128-byte swizzle (64-byte with swizzle64): dims {inner,
+// outer}, rows row_bytes apart, box {box_inner, box_outer} (box_inner * 2 bytes must
+// be at most the swizzle span). Out-of-range elements read as zero; stores past the
+// dims are clipped.
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
-                    uint32_t box_inner, uint32_t box_outer) {
+                    uint32_t box_inner, uint32_t box_outer, bool swizzle64) {
   auto fn = encode_tiled_fn();
   if (fn == nullptr || inner == 0 || outer == 0) return false;
   cuuint64_t dims[2] = {inner, outer};
@@ -35,8 +36,8 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t o
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -462,6 +463,13 @@ static cudaError_t dense_grad_bn(const uint16_t* dY, const uint16_t* Wd, int T, 
                                           H,
                                           I,
                                           status};
+  // the outputs as 32 x 32 fp16 boxes (the bits are copied as they are; rows past T are
+  // clipped by the stores)
+  const uint64_t row_bytes = static_cast<uint64_t>(I) * 2;
+  if (!make_tmap_bf16(&ep.tm_dG, dG, I, T, row_bytes, 32, 32, true) ||
+      !make_tmap_bf16(&ep.tm_H, H, I, T, row_bytes, 32, 32, true) ||
+      !make_tmap_bf16(&ep.tm_dU, GATED ? dU : dG, I, T, row_bytes, 32, 32, true))
+    return cudaErrorInvalidValue;
   constexpr int kStageBytes = (128 + kBRows) * 64 * 2;
   constexpr int kBudget = 232448 - 1280 - EpiDenseGrad<GATED>::kStageBytes * (epi_warps<BN, EpiDenseGrad<GATED>>() / 4);
   constexpr int kStages = kBudget / kStageBytes < 8 ? kBudget / kStageBytes : 8;

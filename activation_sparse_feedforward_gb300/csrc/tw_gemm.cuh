@@ -541,6 +541,21 @@ __global__ void __launch_bounds__(gemm_threads<BN, Epi>(), 1)
 }
 
 // ======================================================================= epilogues
+// Bulk tensor stores from shared memory (TMA, async proxy). The issuing thread
+// commits its stores as one bulk group and later waits for them: `_read` until the
+// shared-memory sources have been read (the buffer may be rewritten), the plain form
+// until the global writes are done.
+TW_DEV void tma_store_2d(const CUtensorMap* map, const void* smem_src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_addr(smem_src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+TW_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+TW_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+TW_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+TW_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // Row-to-column transpose through shared memory for epilogues that write fp32 rows:
 // each epilogue warp holds 32 accumulator rows (one per lane) x 32 columns. Each lane
 // writes its row as eight 16-byte vectors; the warp then reads back four rows per
@@ -960,7 +975,11 @@ struct EpiUpHybrid {
 template <bool GATED>
 struct EpiDenseGrad {
   static constexpr int kGradStride = 33;
-  static constexpr int kStageBytes = 4 * 32 * kGradStride * 4;
+  // a warp's staging: its lanes' rows of ELL (a, u) words (32 x kGradStride words),
+  // overlapped by the three 2 KB output blocks at the next 512-byte boundary
+  static constexpr int kWarpStageBytes = 7168;
+  static_assert(32 * kGradStride * 4 <= kWarpStageBytes && 511 + 3 * 2048 <= kWarpStageBytes, "grad staging");
+  static constexpr int kStageBytes = 4 * kWarpStageBytes;
   static constexpr bool kSplitColumns = true;  // eight epilogue warps on 256-wide tiles
   struct Params {
     int R, I;
@@ -976,6 +995,9 @@ struct EpiDenseGrad {
     uint16_t *dG, *dU, *H;
     int ld;
     int32_t* status;
+    // dG, dU, H [T, I] fp16 as tensor maps of 32 x 32 boxes with the 64-byte swizzle
+    // (the staging layout): each warp's blocks leave by bulk tensor stores
+    CUtensorMap tm_dG, tm_dU, tm_H;
   };
   const Params& p;
   int m, M, n0;
@@ -1043,6 +1065,10 @@ struct EpiDenseGrad {
     const int rows = min(32, M - m0);
     if (rows <= 0) return;  // uniform over the warp
     const int col0 = n0 + c * 32;
+    // the previous chunk's bulk stores have read their blocks, which the ELL words
+    // below overwrite
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
     uint32_t mask = 0u;
     uint32_t* mine = reinterpret_cast<uint32_t*>(stage) + lane * kGradStride;
     if (valid && ell_row) {
@@ -1101,12 +1127,35 @@ struct EpiDenseGrad {
       wu[q] = pack_f16x2_rn(u2[0], u2[1]);
       wh[q] = pack_f16x2_rn(h2[0], h2[1]);
     }
-    __syncwarp();  // every lane has read its staging row: the transposes reuse the buffer
-    transposed_rows_bf16(stage, wg, m0, rows, p.dG + col0, p.ld);
-    transposed_rows_bf16(stage, wh, m0, rows, p.H + col0, p.ld);
-    if (GATED) transposed_rows_bf16(stage, wu, m0, rows, p.dU + col0, p.ld);
+    __syncwarp();  // every lane has read its staging row: the blocks reuse the buffer
+    // lane r writes row r of each block (64 bytes, 16-byte pieces at piece ^ ((r >> 1) & 3),
+    // the tensor maps' 64-byte swizzle); rows past T are clipped by the stores
+    const uint32_t base = smem_addr(stage);
+    uint8_t* blk = reinterpret_cast<uint8_t*>(stage) + (((base + 511u) & ~511u) - base);
+    auto put_block = [&](uint8_t* b, const uint32_t (&w)[16]) {
+      uint32_t* st = reinterpret_cast<uint32_t*>(b);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<uint4*>(st + lane * 16 + 4 * ((i ^ (lane >> 1)) & 3)) =
+            make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    };
+    put_block(blk, wg);
+    put_block(blk + 2048, wh);
+    if (GATED) put_block(blk + 4096, wu);
+    fence_proxy_async_smem();  // the generic-proxy writes are visible to the bulk copies
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(&p.tm_dG, blk, col0, m0);
+      tma_store_2d(&p.tm_H, blk + 2048, col0, m0);
+      if (GATED) tma_store_2d(&p.tm_dU, blk + 4096, col0, m0);
+      bulk_commit();
+    }
   }
-  TW_DEV void finish() {}
+  // the tile's stores are complete before the warp's staging is reused or the CTA exits
+  TW_DEV void finish() {
+    if ((threadIdx.x & 31) == 0) bulk_wait_all();
+    __syncwarp();
+  }
 };
 
 // a[m][n] = bf16(ReLU(acc)) (round to nearest even), row stride lda: the dense

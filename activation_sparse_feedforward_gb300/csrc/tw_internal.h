@@ -239,8 +239,10 @@ cudaError_t launch_sparse_bwd_tokens(const SparseBwdArgs& a, cudaStream_t s);
 cudaError_t launch_sparse_bwd_weights(const SparseBwdArgs& a, cudaStream_t s);
 
 // ---------------------------------------------------------------- tw_gemm.cu
+// 2D tensor map of 16-bit elements with the 128-byte swizzle (operand loads), or the
+// 64-byte swizzle (swizzle64: the 32 x 32 output boxes of bulk stores).
 bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
-                    uint32_t box_inner, uint32_t box_outer);
+                    uint32_t box_inner, uint32_t box_outer, bool swizzle64 = false);
 
 // gate projection + ReLU + TwELL pack
 cudaError_t gemm_gate_pack(const uint16_t* x, const uint16_t* Wg, int T, int d, int I, int W, int C,
