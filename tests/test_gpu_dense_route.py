@@ -211,12 +211,19 @@ def test_auto_route_takes_the_dense_route_when_every_row_is_backup(spec):
     hs, ys, gs = _step(spec, dv, "sparse", spec.l1, spec.T)
     assert not hs.saved.took_dense_route()
     _check_oracle(spec, inp, hs, ys, gs, spec.l1)
-    # the saved fp32 rows do not depend on the route (the same sums, whose split-K
-    # partials may be added in another order)
+    # the saved fp32 rows do not depend on the route: the same sums, whose split-K
+    # partials are added by atomics in an order that varies between launches, so they
+    # agree to the size of a reordering of d terms (about sqrt(d) fp32 roundings of the
+    # terms' magnitude sum; allowed: eight times that, 2^-16 of it at d = 512-768)
     nb = spec.T
-    assert torch.allclose(hs.saved.backup_a[:nb], h.saved.backup_a[:nb], rtol=1e-4, atol=1e-5)
-    if spec.gated:
-        assert torch.allclose(hs.saved.backup_u[:nb], h.saved.backup_u[:nb], rtol=1e-4, atol=1e-5)
+    x = ffn.as_f64(inp["x"])
+    for got, ref, W in ((hs.saved.backup_a, h.saved.backup_a, inp["Wg"]),
+                        (hs.saved.backup_u, h.saved.backup_u, inp["Wu"] if spec.gated else None)):
+        if W is None:
+            continue
+        terms = np.abs(x) @ np.abs(ffn.as_f64(W)).T
+        g, r = got[:nb].double().cpu().numpy(), ref[:nb].double().cpu().numpy()
+        assert (np.abs(g - r) <= 1e-4 * np.abs(r) + 2 ** -16 * terms[:nb]).all()
 
 
 @pytest.mark.parametrize("name,backup_cap", [("train_d2048_i5632_m108_o5", 1280),
