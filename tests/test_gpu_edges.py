@@ -40,11 +40,11 @@ def _check_against_oracle(spec, inp, y_twell, y, grads, what):
         assert_close(dWu.cpu().numpy(), b["dWu"], f"{what}: dWu")
 
 
-def _run(spec, inp, ovf_cap, backup_cap):
+def _run(spec, inp, ovf_cap, backup_cap, route="sparse"):
     dv = _dev(inp)
     f = tw.TwellFFN(spec.T, spec.d, spec.I, spec.W, spec.C, ovf_cap=ovf_cap)
     y_twell = f(dv["x"], dv["Wg"], dv["Wu"], dv["Wd"]).clone()
-    h = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, backup_cap, gated=spec.gated)
+    h = tw.HybridFFN(spec.T, spec.d, spec.I, spec.W, spec.C, spec.R, backup_cap, gated=spec.gated, route=route)
     y = h.forward(dv["x"], dv["Wg"], dv["Wu"], dv["Wd"]).clone()
     grads = h.backward(dv["dy"], dv["x"], dv["Wg"], dv["Wu"], dv["Wd"], spec.l1)
     torch.cuda.synchronize()
@@ -71,12 +71,17 @@ def test_empty_batch():
         assert not bool(g.any())
 
 
+@pytest.mark.parametrize("route", ["sparse", "dense"])
 @pytest.mark.parametrize("gated", [True, False])
-def test_single_token(gated):
+def test_single_token(gated, route):
+    """One token. On the dense route every GEMM runs one 256-row unit on a CTA pair
+    with a single valid row, and the weight-gradient GEMM has K = 1 (its 64-row K
+    boxes read zeros past the token)."""
     spec = FFNSpec("one_token", T=1, d=512, I=1280, gated=gated, mean_active=40, W=128, C=8, R=64, seed=4)
     inp = make_inputs(spec, with_dy=True)
-    _, _, y_twell, y, grads = _run(spec, inp, ovf_cap=1, backup_cap=1)
-    _check_against_oracle(spec, inp, y_twell, y, grads, "one token")
+    _, h, y_twell, y, grads = _run(spec, inp, ovf_cap=1, backup_cap=1, route=route)
+    assert h.saved.took_dense_route() == (route == "dense")
+    _check_against_oracle(spec, inp, y_twell, y, grads, f"one token, {route} route")
 
 
 def test_tokens_without_active_neurons():

@@ -108,6 +108,10 @@ def _gate_case(spec: FFNSpec):
     WORKLOADS["tiny_fwd"],                                                        # I=704: 64-wide N tiles
     FFNSpec("gate_ragged_128", T=1000, d=512, I=640, mean_active=12, outlier_frac=0.02, W=128, C=8),
     FFNSpec("gate_ragged_256", T=333, d=768, I=1024, mean_active=20, outlier_frac=0.03, W=64, C=8, seed=3),
+    # 256-wide tiles on CTA pairs with one 256-row unit: the second CTA of the pair has
+    # no rows (T = 77), or neither CTA has more than one (T = 1)
+    FFNSpec("gate_pair_77_rows", T=77, d=256, I=512, mean_active=10, outlier_frac=0.03, W=128, C=8, seed=4),
+    FFNSpec("gate_pair_one_row", T=1, d=256, I=256, mean_active=8, outlier_frac=0.0, W=64, C=8, seed=13),
 ], ids=lambda s: s.name)
 def test_gate_pack_values_and_bit_exact_pack(spec):
     inp, out, dense = _gate_case(spec)
