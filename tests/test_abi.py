@@ -79,6 +79,13 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.twell_ffn_fwd(16, 16, 16, 16, 4, 256, 256, 64, 8, 4, ctypes.byref(s), 16, 0, 16, 16,
                              None) == _lib.TW_EWORKSPACE
     assert lib.tw_dense_gemm(16, 16, 64, 60, 64, 0, 0, 16, 16, None) == _lib.TW_EINVAL
+    # the CTA-pair forms: N a multiple of 256; the pair timeout hook one 256 x 256 unit
+    assert lib.tw_dense_gemm_pair(16, 16, 64, 128, 64, 0, 0, 16, 16, None) == _lib.TW_EINVAL      # N % 256
+    assert lib.tw_dense_gemm_pair(16, 16, 60, 256, 64, 1, 0, 16, 16, None) == _lib.TW_EINVAL      # M % 64, MN-major A
+    assert lib.tw_dense_gemm_pair(16, 16, 64, 256, 60, 0, 0, 16, 16, None) == _lib.TW_EINVAL      # K % 64
+    assert lib.tw_wait_timeout_probe_pair(16, 16, 300, 256, 64, 0, 16, 16, None) == _lib.TW_EINVAL  # M > 256
+    assert lib.tw_wait_timeout_probe_pair(16, 16, 256, 512, 64, 0, 16, 16, None) == _lib.TW_EINVAL  # N != 256
+    assert lib.tw_wait_timeout_probe_pair(16, 16, 256, 256, 64, 1, 16, 16, None) == _lib.TW_EINVAL  # K block past K
 
 
 def test_neuron_functions_validate_on_the_host(lib):
