@@ -139,9 +139,16 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+        return self.summarize(self.lines)
+
+    @staticmethod
+    def summarize(lines) -> dict:
+        """Median SM clock, the highest maximum clock, the throttle reasons seen active
+        and the sample count, from nvidia-smi CSV lines of FIELDS (malformed lines and
+        unreadable clocks are skipped)."""
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue

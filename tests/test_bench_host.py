@@ -45,3 +45,16 @@ def test_gathered_bytes_counts_rows_per_entry():
     assert bench.gathered_bytes("gate_pack", spec, stats) is None
     ng = spec.with_(gated=False)
     assert bench.gathered_bytes("sparse_fwd", ng, stats) == 1000 * row
+
+
+def test_clock_record_summary():
+    lines = ["0, 2070, 2070, 900.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+             "0, 1800, 2070, 1390.1, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+             "0, 2010, 2070, 1200.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+             "0, [N/A], 2070, 1200.0, 0x0, Not Active, Not Active, Not Active, Not Active",   # unreadable clock
+             "garbage line"]
+    out = bench.ClockSampler.summarize(lines)
+    assert out == {"sm_mhz": 2010.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    hot = bench.ClockSampler.summarize(["0, 1500, 2070, 1400, 0x48, Active, Not Active, Active, Not Active"])
+    assert hot["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"] and hot["samples"] == 1
+    assert bench.ClockSampler.summarize([]) == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
