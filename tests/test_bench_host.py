@@ -58,3 +58,18 @@ def test_clock_record_summary():
     hot = bench.ClockSampler.summarize(["0, 1500, 2070, 1400, 0x48, Active, Not Active, Active, Not Active"])
     assert hot["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"] and hot["samples"] == 1
     assert bench.ClockSampler.summarize([]) == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+
+def test_kernel_work_matches_the_documented_bench_figures():
+    """The roofline's per-launch work at the bench workload (train_d2048_i5632_m29_o1,
+    476079 ELL entries, 164 backup rows): the gate GEMM's 2 T d I = 3.78e11 FLOP and the
+    backward token pass's ~214 MB of algorithmic bytes (dy, dx, the ELL, the records,
+    three weight matrices), as DESIGN states them."""
+    from synthetic import WORKLOADS
+    spec = WORKLOADS["train_d2048_i5632_m29_o1"]
+    stats = {"nnz_ell": 476079, "n_backup": 164}
+    bound, flop = bench.kernel_work("gate_pack", spec, stats)
+    assert bound == "tensor" and abs(flop - 3.78e11) / 3.78e11 < 0.005
+    bound, b = bench.kernel_work("sparse_bwd_token", spec, stats)
+    assert bound == "hbm" and abs(b - 214e6) / 214e6 < 0.01
+    assert bench.kernel_work("no_such_kernel", spec, stats) is None
