@@ -308,8 +308,10 @@ cudaError_t gemm_rows_times_nmajor_splitk(const uint16_t* const* A, const uint16
   // load that B tile once for both
   bool paired = segments % 2 == 0;
   for (int i = 0; paired && i < segments; i += 2) paired = B[i] == B[i + 1];
-  if (paired) return run_gemm<256, false, true, false, 3, EpiRedF32, 2>(maps, sh, ep, cap, s, "backup_rows_gemm");
-  return run_gemm<256, false, true, false, 4, EpiRedF32>(maps, sh, ep, cap, s, "backup_rows_gemm");
+  // (the trace label names the segment count, which sets the product's FLOPs)
+  const char* label = segments == 4 ? "backup_rows_gemm4" : "backup_rows_gemm";
+  if (paired) return run_gemm<256, false, true, false, 3, EpiRedF32, 2>(maps, sh, ep, cap, s, label);
+  return run_gemm<256, false, true, false, 4, EpiRedF32>(maps, sh, ep, cap, s, label);
 }
 
 // ------------------------------------------------------------------ dense backup, backward

@@ -199,7 +199,9 @@ def kernel_work(label: str, spec, stats: dict) -> tuple[str, float] | None:
     if label == "backup_grad":
         return "tensor", 2.0 * nb * d * I
     if label == "backup_rows_gemm":
-        return "tensor", 2.0 * 2 * nb * I * d      # two K segments (hi, lo); the dx GEMM has four
+        return "tensor", 2.0 * 2 * nb * I * d      # two K segments: y's (hi, lo), or a non-gated dx
+    if label == "backup_rows_gemm4":
+        return "tensor", 2.0 * 4 * nb * I * d      # the gated dx: dG and dU, each (hi, lo)
     if label == "backup_weight_grad":
         return "tensor", 2.0 * 2 * nb * I * d
     return None
